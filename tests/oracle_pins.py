@@ -1,0 +1,283 @@
+"""Checks that pin the float64 oracle to things other than itself.
+
+Each ``pin_*`` function raises AssertionError when the oracle disagrees with an
+independent statement of the same fact: a library routine (torch SDPA, torch's
+float32 -> bf16 cast), the complex-number form of the rotation with the page's
+1-based frequency formula, brute-force pure-Python loops, the causal full-sequence
+attention that the cached decode must reproduce row by row, or numbers the pages
+print. ``test_oracle_pins.py`` runs them on the oracle; ``test_oracle_mutations.py``
+plants plausible mistakes in the oracle and checks that some pin fails.
+"""
+
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ---------------------------------------------------------------------------- bf16
+def pin_bf16_exact_values():
+    cases = [
+        (1.0, 0x3F80), (-2.0, 0xC000), (0.0, 0x0000), (-0.0, 0x8000),
+        (1.0 + 2.0 ** -8, 0x3F80),                 # tie -> even (down)
+        (1.0 + 3 * 2.0 ** -8, 0x3F82),             # tie -> even (up)
+        (1.0 + 2.0 ** -8 + 2.0 ** -40, 0x3F81),    # just above the tie: up (no double rounding via fp32)
+        (1.0 + 2.0 ** -8 - 2.0 ** -40, 0x3F80),
+        (3.0e38, 0x7F62), (3.4e38, 0x7F80), (-math.inf, 0xFF80), (math.inf, 0x7F80),
+        (2.0 ** -130, 0x0008),                     # bf16 subnormal
+    ]
+    got = oracle.f64_to_bf16_bits(np.array([c[0] for c in cases]))
+    want = np.array([c[1] for c in cases], dtype=np.uint16)
+    assert np.array_equal(got, want), (got, want)
+    assert oracle.f64_to_bf16_bits(np.array([math.nan]))[0] & 0x7FFF > 0x7F80
+
+
+def pin_bf16_matches_torch_cast():
+    rng = np.random.default_rng(11)
+    x32 = np.concatenate([rng.standard_normal(20000).astype(np.float32) * s for s in (1e-3, 1.0, 7.0, 1e20)])
+    ref = torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.f64_to_bf16_bits(x32.astype(np.float64))
+    assert np.array_equal(got, ref)
+    back = oracle.bf16_bits_to_f64(ref)
+    assert np.array_equal(back, torch.from_numpy(ref.view(np.int16)).view(torch.bfloat16).double().numpy())
+
+
+# ---------------------------------------------------------------------------- RoPE
+def _page_theta(d, base=10000.0):
+    # theta_i = base^(-2(i-1)/d), i = 1..d/2, written with the page's 1-based index
+    return np.array([base ** (-2.0 * (i - 1) / d) for i in range(1, d // 2 + 1)])
+
+
+def pin_rope_complex_rotation():
+    rng = np.random.default_rng(1)
+    for d in (8, 64, 128):
+        for style in (0, 1):
+            x = rng.standard_normal((6, d))
+            pos = np.array([0, 1, 2, 127, 4095, 131071])
+            got = oracle.apply_rope(x, pos, 10000.0, style)
+            if style == 0:
+                z = x[:, : d // 2] + 1j * x[:, d // 2:]
+            else:
+                z = x[:, 0::2] + 1j * x[:, 1::2]
+            w = z * np.exp(1j * pos[:, None] * _page_theta(d)[None, :])
+            want = np.empty_like(x)
+            if style == 0:
+                want[:, : d // 2], want[:, d // 2:] = w.real, w.imag
+            else:
+                want[:, 0::2], want[:, 1::2] = w.real, w.imag
+            assert np.allclose(got, want, rtol=0, atol=1e-9), (d, style, np.abs(got - want).max())
+
+
+def pin_rope_relative_position():
+    rng = np.random.default_rng(2)
+    for style in (0, 1):
+        for _ in range(20):
+            q, k = rng.standard_normal(128), rng.standard_normal(128)
+            m, n = (int(v) for v in rng.integers(0, 131072, size=2))
+            lhs = oracle.apply_rope(q, m, style=style) @ oracle.apply_rope(k, n, style=style)
+            rhs = q @ oracle.apply_rope(k, n - m, style=style)
+            assert abs(lhs - rhs) < 1e-8 * (1 + abs(lhs)), (m, n, lhs, rhs)
+
+
+def pin_rope_rotation_properties():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((4, 64))
+    assert np.array_equal(oracle.apply_rope(x, 0), x)                 # position 0 is the identity
+    y = oracle.apply_rope(x, np.array([5, 77, 1000, 131071]))
+    assert np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-13)
+    # pair 1 turns by exactly the position (theta_1 = 1): e_0 -> cos m e_0 + sin m e_{d/2}
+    e0 = np.zeros(64); e0[0] = 1.0
+    r = oracle.apply_rope(e0, 3)
+    assert abs(r[0] - math.cos(3)) < 1e-15 and abs(r[32] - math.sin(3)) < 1e-15
+    assert np.count_nonzero(np.abs(r) > 1e-15) == 2
+    # the slowest pair turns by base^(-(d-2)/d) per position; frequencies fall geometrically
+    th = oracle.inv_freq(64)
+    assert abs(th[-1] - 10000.0 ** (-62 / 64)) < 1e-18
+    assert np.allclose(th[1:] / th[:-1], 10000.0 ** (-2 / 64), rtol=1e-13)
+
+
+# ---------------------------------------------------------------------------- GQA / attention
+def _loop_attention(qh, k, v, scale):
+    """Pure-Python single-query softmax attention (brute force)."""
+    s = [scale * sum(qh[i] * k[t][i] for i in range(len(qh))) for t in range(len(k))]
+    mx = max(s)
+    e = [math.exp(x - mx) for x in s]
+    z = sum(e)
+    return [sum(e[t] * v[t][j] for t in range(len(k))) / z for j in range(len(v[0]))]
+
+
+def pin_gqa_brute_force(hq=4, hkv_list=(4, 2, 1), d=8, L=9):
+    rng = np.random.default_rng(4)
+    for hkv in hkv_list:
+        q = rng.standard_normal((hq, d))
+        k = rng.standard_normal((hkv, L, d))
+        v = rng.standard_normal((hkv, L, d))
+        got = oracle.gqa_decode_attention(q, k, v)
+        for h in range(hq):
+            g = h // (hq // hkv)               # MHA: g = h; MQA: g = 0
+            want = _loop_attention(list(q[h]), k[g].tolist(), v[g].tolist(), 1 / math.sqrt(d))
+            assert np.allclose(got[h], want, rtol=0, atol=1e-12), (hkv, h)
+
+
+def pin_gqa_head_mapping():
+    # V of KV head g is the constant g + 1, so out[h] names the KV head query head h used.
+    rng = np.random.default_rng(5)
+    hq, hkv, d, L = 8, 2, 16, 5
+    q = rng.standard_normal((hq, d))
+    k = rng.standard_normal((hkv, L, d))
+    v = np.stack([np.full((L, d), g + 1.0) for g in range(hkv)])
+    out = oracle.gqa_decode_attention(q, k, v)
+    used = np.rint(out[:, 0]).astype(int) - 1
+    assert used.tolist() == [0, 0, 0, 0, 1, 1, 1, 1], used     # repeat_interleave, not tile
+
+
+def pin_attention_matches_torch_sdpa():
+    rng = np.random.default_rng(6)
+    for hq, hkv, d, L in ((32, 8, 128, 300), (4, 2, 64, 128), (8, 8, 64, 17), (8, 1, 64, 33)):
+        q = rng.standard_normal((hq, d))
+        k = rng.standard_normal((hkv, L, d))
+        v = rng.standard_normal((hkv, L, d))
+        got = oracle.gqa_decode_attention(q, k, v)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q)[None, :, None, :], torch.from_numpy(k)[None], torch.from_numpy(v)[None],
+            enable_gqa=True)[0, :, 0, :].numpy()
+        assert np.allclose(got, ref, rtol=0, atol=1e-12), (hq, hkv, np.abs(got - ref).max())
+
+
+def pin_causal_attention_matches_torch_sdpa():
+    rng = np.random.default_rng(7)
+    t, hq, hkv, d = 23, 4, 2, 16
+    q = rng.standard_normal((t, hq, d))
+    k = rng.standard_normal((t, hkv, d))
+    v = rng.standard_normal((t, hkv, d))
+    out, w = oracle.causal_attention(q, k, v, return_weights=True)
+    tq = lambda a: torch.from_numpy(np.ascontiguousarray(np.transpose(a, (1, 0, 2))))[None]  # noqa: E731
+    ref = torch.nn.functional.scaled_dot_product_attention(tq(q), tq(k), tq(v), is_causal=True,
+                                                           enable_gqa=True)[0].numpy()
+    assert np.allclose(out, np.transpose(ref, (1, 0, 2)), rtol=0, atol=1e-12)
+    # weights: rows sum to 1 and are strictly lower-triangular (nothing above the diagonal)
+    assert np.allclose(w.sum(-1), 1.0, atol=1e-13)
+    assert np.all(np.triu(w, k=1) == 0.0)
+
+
+def pin_softmax_large_scores():
+    # one key aligned with q at a huge score: the max-subtracted softmax stays finite and one-hot
+    d, L = 64, 50
+    rng = np.random.default_rng(8)
+    q = rng.standard_normal((1, d)) * 40
+    k = rng.standard_normal((1, L, d)) * 0.01
+    k[0, 17] = q[0] * 3.0
+    v = rng.standard_normal((1, L, d))
+    out = oracle.gqa_decode_attention(q, k, v)
+    assert np.all(np.isfinite(out)) and np.allclose(out[0], v[0, 17], atol=1e-12)
+
+
+# ---------------------------------------------------------------------------- cache + decode step
+def _stream_decode_vs_causal(layout, dtype="f64", style=0):
+    """Feed T tokens one decode step at a time and compare each step with causal attention."""
+    rng = np.random.default_rng(9)
+    T, hq, hkv, d, bs = 37, 4, 2, 16, 8
+    qs = rng.standard_normal((T, hq, d))
+    ks = rng.standard_normal((T, hkv, d))
+    vs = rng.standard_normal((T, hkv, d))
+    pos = np.arange(T)
+    ref = oracle.causal_attention(oracle.apply_rope(qs, pos[:, None], style=style),
+                                  oracle.apply_rope(ks, pos[:, None], style=style), vs)
+    if layout == "contiguous":
+        kc = np.full((1, hkv, T + 3, d), np.nan)
+        table = None
+    else:
+        nblk = 3 * math.ceil(T / bs)
+        kc = np.full((nblk, bs, hkv, d), np.nan)
+        table = rng.permutation(nblk)[: math.ceil(T / bs)][None, :].astype(np.int32)
+    vc = kc.copy()
+    for t in range(T):
+        q_rot = oracle.decode.rope_append(qs[t][None], ks[t][None], vs[t][None], np.array([t]), kc, vc,
+                                          dtype, table, bs, rope_style=style)
+        out = oracle.decode.decode_attention(q_rot, kc, vc, np.array([t + 1]), dtype, table, bs)
+        assert np.allclose(out[0], ref[t], rtol=0, atol=1e-12), (layout, t, np.abs(out[0] - ref[t]).max())
+
+
+def pin_decode_equals_causal_rows():
+    for layout in ("contiguous", "paged"):
+        for style in (0, 1):
+            _stream_decode_vs_causal(layout, style=style)
+
+
+def pin_paged_gather_order():
+    bs, hkv, d, nblk = 4, 2, 3, 10
+    pool = np.zeros((nblk, bs, hkv, d))
+    for p in range(nblk):
+        for s in range(bs):
+            pool[p, s] = p * 1000 + s
+    table = np.array([7, 2, 9, 0], dtype=np.int32)
+    got = oracle.logical_kv_paged(pool, table, bs, 14)                  # [hkv, 14, d]
+    want = np.array([table[t // bs] * 1000 + t % bs for t in range(14)], dtype=np.float64)
+    assert got.shape == (hkv, 14, d)
+    assert np.array_equal(got[1, :, 2], want)
+
+
+def pin_paged_equals_contiguous():
+    rng = np.random.default_rng(10)
+    B, hq, hkv, d, bs = 3, 8, 2, 32, 16
+    lens = np.array([1, 40, 64])
+    max_len = 64
+    q = rng.standard_normal((B, hq, d))
+    cont_k = rng.standard_normal((B, hkv, max_len, d))
+    cont_v = rng.standard_normal((B, hkv, max_len, d))
+    nper = max_len // bs
+    perm = rng.permutation(B * nper + 5)
+    table = perm[: B * nper].reshape(B, nper).astype(np.int32)
+    pool_k = np.full((B * nper + 5, bs, hkv, d), np.nan)
+    pool_v = pool_k.copy()
+    for b in range(B):
+        for t in range(lens[b]):
+            pool_k[table[b, t // bs], t % bs] = cont_k[b, :, t]
+            pool_v[table[b, t // bs], t % bs] = cont_v[b, :, t]
+    a = oracle.decode.decode_attention(q, cont_k, cont_v, lens, "f64")
+    p = oracle.decode.decode_attention(q, pool_k, pool_v, lens, "f64", table, bs)
+    assert np.array_equal(a, p)
+
+
+def pin_kv_bytes_pages_numbers():
+    with open(os.path.join(GOLDEN, "kv_cache_bytes.txt"), encoding="utf-8") as f:
+        rows = [ln.split("|")[0].split() for ln in f if ln.strip() and not ln.startswith("#")]
+    assert rows
+    for L, H, D, S, B, db, val, unit in rows:
+        got = oracle.kv_cache_bytes(int(L), int(H), int(D), int(S), int(B), int(db))
+        assert unit == "GiB" and got == float(val) * 2 ** 30, (got, val)
+    with open(os.path.join(GOLDEN, "kv_heads_ratio.txt"), encoding="utf-8") as f:
+        rows = [ln.split("|")[0].split() for ln in f if ln.strip() and not ln.startswith("#")]
+    mha = oracle.kv_cache_bytes(32, 32, 128, 4096, 1, 2)
+    for hkv, pct in rows:
+        ratio = oracle.kv_cache_bytes(32, int(hkv), 128, 4096, 1, 2) / mha
+        assert round(100 * ratio) == int(pct), (hkv, ratio)
+
+
+ALL_PINS = [
+    pin_bf16_exact_values, pin_bf16_matches_torch_cast,
+    pin_rope_complex_rotation, pin_rope_relative_position, pin_rope_rotation_properties,
+    pin_gqa_brute_force, pin_gqa_head_mapping, pin_attention_matches_torch_sdpa,
+    pin_causal_attention_matches_torch_sdpa, pin_softmax_large_scores,
+    pin_decode_equals_causal_rows, pin_paged_gather_order, pin_paged_equals_contiguous,
+    pin_kv_bytes_pages_numbers,
+]
+
+
+def failing_pins():
+    """Names of the pins that fail on the oracle as currently loaded."""
+    bad = []
+    for pin in ALL_PINS:
+        try:
+            with np.errstate(all="ignore"):
+                pin()
+        except (AssertionError, ValueError, IndexError, FloatingPointError):
+            bad.append(pin.__name__)
+    return bad

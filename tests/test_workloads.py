@@ -1,0 +1,60 @@
+"""The seeded input generator: determinism, block tables, shared prefixes, NaN poisoning (CPU)."""
+
+import math
+
+import numpy as np
+import pytest
+
+from workloads import CONFIGS, make_inputs, reduced
+
+
+def _finite(x, dtype):
+    if dtype == "bf16":
+        return (x & 0x7F80) != 0x7F80
+    return np.isfinite(x)
+
+
+@pytest.mark.parametrize("name", list(CONFIGS))
+def test_full_size_configs_are_consistent(name):
+    cfg = CONFIGS[name]
+    assert cfg.n_q_heads % cfg.n_kv_heads == 0
+    longest = cfg.seq_len if cfg.seq_len is not None else cfg.len_range[1]
+    assert longest <= cfg.capacity
+    if cfg.layout == "paged":
+        n_shared = cfg.shared_prefix_tokens // cfg.block_size
+        need = n_shared + cfg.batch * (math.ceil(longest / cfg.block_size) - n_shared)
+        assert need <= cfg.num_blocks
+
+
+@pytest.mark.parametrize("name", list(CONFIGS))
+def test_reduced_inputs_structure(name):
+    cfg = reduced(CONFIGS[name], batch=min(CONFIGS[name].batch, 5))
+    a = make_inputs(cfg)
+    b = make_inputs(cfg)
+    for f in ("q", "k_new", "v_new", "k_cache", "v_cache", "lengths"):
+        assert getattr(a, f).tobytes() == getattr(b, f).tobytes()
+    assert np.array_equal(a.positions, a.lengths - 1)
+    L = a.lengths
+    if cfg.layout == "contiguous":
+        for bb in range(cfg.batch):
+            assert _finite(a.k_cache[bb, :, : L[bb] - 1], cfg.dtype).all()
+            assert not _finite(a.k_cache[bb, :, L[bb] - 1:], cfg.dtype).any()
+        return
+    bs, t = cfg.block_size, a.block_table
+    n_shared = cfg.shared_prefix_tokens // bs
+    owned = []
+    for bb in range(cfg.batch):
+        nb = math.ceil(int(L[bb]) / bs)
+        assert np.all((t[bb, :nb] >= 0) & (t[bb, :nb] < cfg.num_blocks))
+        assert np.all(t[bb, nb:] == -1)
+        assert np.array_equal(t[bb, :n_shared], t[0, :n_shared])
+        owned.extend(t[bb, n_shared:nb].tolist())
+        for tok in range(int(L[bb]) - 1):                   # every cached token is finite
+            assert _finite(a.k_cache[t[bb, tok // bs], tok % bs], cfg.dtype).all()
+        last = t[bb, (L[bb] - 1) // bs]
+        assert not _finite(a.v_cache[last, (L[bb] - 1) % bs:], cfg.dtype).any()
+    owned.extend(t[0, :n_shared].tolist())
+    assert len(owned) == len(set(owned))                     # private blocks are never shared
+    unused = np.setdiff1d(np.arange(cfg.num_blocks), owned)
+    if unused.size:
+        assert not _finite(a.k_cache[unused], cfg.dtype).any()

@@ -1,0 +1,145 @@
+"""Seeded synthetic decode-step inputs.
+
+Recipe (one numpy ``Generator(PCG64(seed))`` per workload, draws in this order):
+
+1. attended lengths L_b: the fixed ``seq_len``, else ``integers(lo, hi, endpoint=True, size=B)``;
+2. paged only: ``permutation(num_blocks)`` is the free list; shared-prefix blocks are
+   popped from its end first, then sequences b = 0..B-1 pop ``ceil(L_b / bs)`` ids each
+   (prefix blocks excluded) in logical order; unused table entries are -1;
+3. q [B, Hq, D], then k_new [B, Hkv, D], then v_new [B, Hkv, D];
+4. the whole K cache, then the whole V cache (contiguous [B, Hkv, max_len, D] or
+   pool [num_blocks, bs, Hkv, D]), drawn in chunks of 2**24 values.
+
+Values are ``standard_normal(dtype=float32)`` rounded to the storage type (bf16 by
+round-to-nearest-even on the float32 bits; fp32 unchanged). The cache is read as
+already-rotated K (a rotation keeps iid N(0,1) vectors iid N(0,1)).
+
+Poisoning: every cache slot the step must not read before the append is NaN: in
+the contiguous cache the slots t >= L_b - 1 of sequence b; in the pools every block
+no table references, and in each sequence's last block the slots at positions
+>= L_b - 1. Position L_b - 1 is where the new token goes, so a missing append or an
+out-of-range read shows up as NaN in the output.
+
+bf16 arrays are carried as ``uint16`` bit patterns, fp32 as ``float32``.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+
+from .configs import WorkloadConfig
+
+_CHUNK = 1 << 24
+BF16_NAN = np.uint16(0x7FC0)
+
+
+def bf16_bits_from_f32(x: np.ndarray) -> np.ndarray:
+    """Round finite float32 values to bf16 (nearest, ties to even); returns uint16 bits."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = (u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def _normal_storage(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16 if dtype == "bf16" else np.float32)
+    for s in range(0, n, _CHUNK):
+        e = min(n, s + _CHUNK)
+        x = rng.standard_normal(e - s, dtype=np.float32)
+        out[s:e] = bf16_bits_from_f32(x) if dtype == "bf16" else x
+    return out.reshape(shape)
+
+
+@dataclasses.dataclass
+class DecodeInputs:
+    cfg: WorkloadConfig
+    lengths: np.ndarray            # int32 [B], attended lengths incl. the new token
+    positions: np.ndarray          # int32 [B], = lengths - 1 (position and slot of the new token)
+    q: np.ndarray                  # [B, Hq, D]
+    k_new: np.ndarray              # [B, Hkv, D]
+    v_new: np.ndarray              # [B, Hkv, D]
+    k_cache: np.ndarray            # contiguous [B, Hkv, max_len, D] or pool [num_blocks, bs, Hkv, D]
+    v_cache: np.ndarray
+    block_table: Optional[np.ndarray] = None   # int32 [B, max_blocks_per_seq], paged only
+
+    @property
+    def nan_value(self):
+        return BF16_NAN if self.cfg.dtype == "bf16" else np.float32(np.nan)
+
+
+def draw_lengths(cfg: WorkloadConfig, rng: np.random.Generator) -> np.ndarray:
+    if cfg.seq_len is not None:
+        lengths = np.full(cfg.batch, cfg.seq_len, dtype=np.int64)
+    else:
+        lo, hi = cfg.len_range
+        lengths = rng.integers(lo, hi, endpoint=True, size=cfg.batch)
+    if np.any(lengths > cfg.capacity) or np.any(lengths < 1):
+        raise ValueError(f"{cfg.name}: lengths outside [1, {cfg.capacity}]")
+    return lengths.astype(np.int32)
+
+
+def draw_block_table(cfg: WorkloadConfig, lengths: np.ndarray, rng: np.random.Generator) -> np.ndarray:
+    bs = cfg.block_size
+    free = list(rng.permutation(cfg.num_blocks))
+    n_shared = cfg.shared_prefix_tokens // bs
+    if cfg.shared_prefix_tokens % bs:
+        raise ValueError("shared prefix must be a whole number of blocks")
+    if n_shared and int(lengths.min()) - 1 < cfg.shared_prefix_tokens:
+        raise ValueError("the new token's slot must lie past the shared prefix")
+    shared = [free.pop() for _ in range(n_shared)]
+    table = np.full((cfg.batch, cfg.max_blocks_per_seq), -1, dtype=np.int32)
+    for b in range(cfg.batch):
+        nb = math.ceil(int(lengths[b]) / bs)
+        table[b, :n_shared] = shared
+        for j in range(n_shared, nb):
+            if not free:
+                raise ValueError(f"{cfg.name}: pool of {cfg.num_blocks} blocks exhausted")
+            table[b, j] = free.pop()
+    return table
+
+
+def make_inputs(cfg: WorkloadConfig, seed: Optional[int] = None, poison: bool = True) -> DecodeInputs:
+    rng = np.random.Generator(np.random.PCG64(cfg.seed if seed is None else seed))
+    B, Hq, Hkv, D = cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    lengths = draw_lengths(cfg, rng)
+    table = draw_block_table(cfg, lengths, rng) if cfg.layout == "paged" else None
+    q = _normal_storage(rng, (B, Hq, D), cfg.dtype)
+    k_new = _normal_storage(rng, (B, Hkv, D), cfg.dtype)
+    v_new = _normal_storage(rng, (B, Hkv, D), cfg.dtype)
+    if cfg.layout == "contiguous":
+        shape = (B, Hkv, cfg.max_len, D)
+    else:
+        shape = (cfg.num_blocks, cfg.block_size, Hkv, D)
+    k_cache = _normal_storage(rng, shape, cfg.dtype)
+    v_cache = _normal_storage(rng, shape, cfg.dtype)
+    inp = DecodeInputs(cfg=cfg, lengths=lengths, positions=(lengths - 1).astype(np.int32),
+                       q=q, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache,
+                       block_table=table)
+    if poison:
+        poison_unread(inp)
+    return inp
+
+
+def poison_unread(inp: DecodeInputs) -> None:
+    """Write NaN into every cache slot the step must not read before its append."""
+    cfg, nan = inp.cfg, inp.nan_value
+    if cfg.layout == "contiguous":
+        for b, L in enumerate(inp.lengths):
+            inp.k_cache[b, :, L - 1:, :] = nan
+            inp.v_cache[b, :, L - 1:, :] = nan
+        return
+    bs = cfg.block_size
+    used = np.zeros(cfg.num_blocks, dtype=bool)
+    for b, L in enumerate(inp.lengths):
+        nb = math.ceil(int(L) / bs)
+        used[inp.block_table[b, :nb]] = True
+        last = inp.block_table[b, (L - 1) // bs]
+        off = (L - 1) % bs
+        inp.k_cache[last, off:] = nan
+        inp.v_cache[last, off:] = nan
+    inp.k_cache[~used] = nan
+    inp.v_cache[~used] = nan
