@@ -1,0 +1,446 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark: RoPE + KV append + split-K GQA decode attention on one GB300.
+
+One step = one pass of the whole path over one batch: rra_rope_append, then the decode
+kernel (and the split merge when there is more than one split). Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU with its
+own seeded batch (no collective on the data path); the time is the max over ranks and
+the value counts the KV bytes of all ranks.
+"""
+
+from __future__ import annotations
+
+import sys
+
+if "--impl" in sys.argv and "reference" in sys.argv or "--cpu-worker" in sys.argv:
+    import os as _os
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        _os.environ[_v] = "1"           # the oracle runs on exactly one host core
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import CONFIGS, make_inputs, make_structure  # noqa: E402
+
+METRIC = "decode-attn KV GB/s & % of GB300 HBM peak; decode steps/s per layer"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "batched_paged"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+KERNEL_SOURCES = ["rope_gqa_paged_gb300/csrc/decode_kernels.cuh", "rope_gqa_paged_gb300/csrc/rra_device.cuh",
+                  "rope_gqa_paged_gb300/csrc/decode_paged.cu", "rope_gqa_paged_gb300/csrc/decode_contig.cu"]
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(CONFIGS), default=DEFAULT_WORKLOAD)
+    p.add_argument("--num-splits", type=int, default=-1, help="-1: the workload's own setting (0 = library choice)")
+    p.add_argument("--batch", type=int, default=0,
+                   help="override the batch (a smaller case for profiling; the paged pool shrinks to fit)")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="bounded CPU oracle sample (seconds)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------- helpers
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def aggregate(ms_per_step: float, kv_bytes: int, world: int, device=None):
+    """Max of the step time and sum of the KV bytes over ranks (a no-op for one rank)."""
+    if world <= 1:
+        return ms_per_step, kv_bytes
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms_per_step], dtype=torch.float64, device=device)
+    b = torch.tensor([float(kv_bytes)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(b.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """dram bytes per launch of the decode kernel from the committed ncu summary, if it is current."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}.md")
+    try:
+        text = open(path, encoding="utf-8").read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        for key in ("traffic_bytes_per_launch", "kernel_source_sha256"):
+            if line.strip().startswith(key + ":"):
+                vals[key] = line.split(":", 1)[1].strip().split()[0]
+    if vals.get("kernel_source_sha256") != kernel_source_hash() or "traffic_bytes_per_launch" not in vals:
+        return None
+    return int(vals["traffic_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid):
+        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+        self.proc = None
+        self.gpu = gpu_uuid
+
+    def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu:
+            cmd += ["-i", self.gpu]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            rows = [ln.split(",") for ln in open(self.path) if ln.strip()]
+        except OSError:
+            rows = []
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 8:
+                continue
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- our arm
+def workload_config(args):
+    cfg = CONFIGS[args.workload]
+    if args.batch and args.batch != cfg.batch:
+        import dataclasses
+        import math
+        kw = {"batch": args.batch, "name": cfg.name}
+        if cfg.layout == "paged":
+            longest = cfg.seq_len if cfg.seq_len is not None else cfg.len_range[1]
+            need = args.batch * math.ceil(longest / cfg.block_size) + 8
+            kw["num_blocks"] = min(cfg.num_blocks, need) if args.batch < cfg.batch else max(cfg.num_blocks, need)
+        cfg = dataclasses.replace(cfg, **kw)
+    return cfg
+
+
+def device_workload(cfg, seed, device):
+    """Seeded inputs at full size: lengths and block tables from the numpy recipe, cache
+    values N(0,1) drawn on the device (torch Philox, seeded), stored in the workload dtype."""
+    import torch
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    lengths, table = make_structure(cfg, seed)
+    g = torch.Generator(device=device)
+    g.manual_seed(1000003 * seed + 17)
+    B, Hq, Hkv, D = cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+    shape = (B, Hkv, cfg.max_len, D) if cfg.layout == "contiguous" else (cfg.num_blocks, cfg.block_size, Hkv, D)
+    w = {
+        "k_cache": torch.randn(shape, generator=g, device=device, dtype=dt),
+        "v_cache": torch.randn(shape, generator=g, device=device, dtype=dt),
+        "q": torch.randn(B, Hq, D, generator=g, device=device, dtype=dt),
+        "k_new": torch.randn(B, Hkv, D, generator=g, device=device, dtype=dt),
+        "v_new": torch.randn(B, Hkv, D, generator=g, device=device, dtype=dt),
+        "positions": torch.from_numpy(lengths - 1).to(device),
+        "seq_lens": torch.from_numpy(lengths).to(device),
+        "block_table": torch.from_numpy(table).to(device) if table is not None else None,
+    }
+    return w, lengths
+
+
+def run_ours(args):
+    import torch
+
+    from rope_gqa_paged_gb300 import DecodeStep, _build
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    _build.build()                                    # no-op when the library is current
+
+    cfg = workload_config(args)
+    splits_arg = cfg.num_splits if args.num_splits < 0 else args.num_splits
+    w, lengths = device_workload(cfg, cfg.seed + rank, device)
+    kv_bytes = cfg.kv_bytes(lengths)
+    step = DecodeStep(cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, w["k_cache"], w["v_cache"],
+                      w["block_table"], num_splits=splits_arg, rope_base=cfg.rope_base)
+    launches_per_step = 2 + (1 if step.splits > 1 else 0)
+    flush = None
+    if 2 * kv_bytes < 3 * L2_BYTES:                     # inputs not much larger than L2: flush between steps
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def one_step():
+        step.rope_append(w["q"], w["k_new"], w["v_new"], w["positions"])
+        return step
+
+    for _ in range(max(args.warmup, 3)):
+        step(w["q"], w["k_new"], w["v_new"], w["positions"], w["seq_lens"])
+    torch.cuda.synchronize(device)
+    step.reset_errors()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    sampler.start()
+    for i in range(K):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step.rope_append(w["q"], w["k_new"], w["v_new"], w["positions"])
+        ev[i][1].record(stream)
+        step.attend(w["seq_lens"])
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    clocks = sampler.stop()
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
+    rope_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    ms_local = sum(step_ms) / K
+    err_bits = step.error_bits()
+
+    # end to end through the public API: pinned host inputs in, host output back, every step
+    e2e = None
+    if not args.no_e2e:
+        host = {k: w[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "positions", "seq_lens")}
+        dev_in = {k: torch.empty_like(w[k]) for k in host}
+        out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+        e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        barrier(world)
+        torch.cuda.synchronize(device)
+        for i in range(K):
+            if flush is not None:
+                flush.fill_(i & 0xFF)
+            e_ev[i][0].record(stream)
+            for k in host:
+                dev_in[k].copy_(host[k], non_blocking=True)
+            out = step(dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["positions"], dev_in["seq_lens"])
+            out_host.copy_(out, non_blocking=True)
+            e_ev[i][1].record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        e2e_ms = sum(e_ev[i][0].elapsed_time(e_ev[i][1]) for i in range(K)) / K
+        e2e_ms, e2e_bytes = aggregate(e2e_ms, kv_bytes, world, device)
+        e2e = {"value": round(e2e_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
+               "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world}
+
+    ms, total_bytes = aggregate(ms_local, kv_bytes, world, device)
+    dec_avg = sum(dec_ms) / K
+    peak, peak_src = hbm_peak()
+    achieved = kv_bytes / (dec_avg * 1e-3) / 1e9
+    value = total_bytes / (ms * 1e-3) / 1e9
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded N(0,1); lengths/tables from the recipe)",
+        "config": {
+            "workload": cfg.name, "description": cfg.description, "batch_per_gpu": cfg.batch,
+            "n_q_heads": cfg.n_q_heads, "n_kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim,
+            "layout": cfg.layout, "block_size": cfg.block_size or None,
+            "seq_lens": (f"U[{cfg.len_range[0]},{cfg.len_range[1]}] mean {float(np.mean(lengths)):.1f}"
+                         if cfg.len_range else cfg.seq_len),
+            "num_splits": step.splits, "kv_bytes_per_step_per_gpu": kv_bytes,
+            "l2": ("flushed between steps (2x L2 write, outside the timed events)" if flush is not None
+                   else f"inputs larger than L2 ({kv_bytes / 2**20:.0f} MiB KV per step vs 129 MiB L2)"),
+            "parallelism": f"replicas x{world}",
+        },
+        "decode_steps_per_s_per_layer": round(1e3 / ms, 2),
+        "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_hbm": round(100 * value / world / peak, 2),
+        "kernel_ms": {"rope_append": round(sum(rope_ms) / K, 5), "decode_attn": round(dec_avg, 5)},
+        "roofline": {"kernel": "decode_split_kernel + split merge (one rra_decode_attn_* call)", "bound": "hbm",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": recorded_traffic(cfg.name)},
+        "gpu_launches": K * launches_per_step,
+        "device_error_bits": err_bits,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": None,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg.name, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- the oracle on host cores
+def oracle_sample_config(cfg, batch):
+    """The first ``batch`` sequences of a workload, with a pool just big enough for them."""
+    import dataclasses
+    import math
+    kw = {"batch": batch, "name": cfg.name + f"_sample{batch}"}
+    if cfg.layout == "paged":
+        longest = cfg.seq_len if cfg.seq_len is not None else cfg.len_range[1]
+        kw["num_blocks"] = batch * math.ceil(longest / cfg.block_size) + 8
+    return dataclasses.replace(cfg, **kw)
+
+
+def oracle_step_seconds(inp):
+    """Time the oracle's whole decode step (RoPE, append, attention) on one sample."""
+    from oracle import decode as odecode
+    cfg = inp.cfg
+    bs = cfg.block_size if inp.block_table is not None else 0
+    t0 = time.perf_counter()
+    odecode.decode_step(inp.q, inp.k_new, inp.v_new, inp.positions, inp.k_cache, inp.v_cache, cfg.dtype,
+                        inp.block_table, bs, rope_base=cfg.rope_base)
+    return time.perf_counter() - t0
+
+
+def cpu_worker(workload: str, seconds: float):
+    cfg = CONFIGS[workload]
+    sample_batch = 1 if cfg.batch == 1 or cfg.layout == "contiguous" else 2
+    inp = make_inputs(oracle_sample_config(cfg, sample_batch), seed=cfg.seed)
+    nbytes = cfg.kv_bytes(inp.lengths)
+    elapsed, done = 0.0, 0
+    while elapsed < seconds or done == 0:
+        elapsed += oracle_step_seconds(inp)
+        done += 1
+    return {"value": round(done * nbytes / elapsed / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"float64 numpy oracle (RoPE + append + attention) on the first {sample_batch} "
+                       f"sequence(s) of {workload} (lengths {inp.lengths.tolist()}), repeated {done}x "
+                       f"in {elapsed:.1f} s; BLAS limited to 1 thread")}
+
+
+def cpu_baseline(workload: str, seconds: float):
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[v] = "1"
+    for v in ("RANK", "LOCAL_RANK", "WORLD_SIZE"):
+        env.pop(v, None)
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", "--workload", workload,
+           "--cpu-seconds", str(seconds)]
+    try:
+        r = subprocess.run(cmd, env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True,
+                           timeout=max(120.0, 6 * seconds))
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # the baseline is reported, never required
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    cfg = CONFIGS[args.workload]
+    sample_batch = 1 if cfg.batch == 1 or cfg.layout == "contiguous" else 2
+    inp = make_inputs(oracle_sample_config(cfg, sample_batch), seed=cfg.seed)
+    nbytes = cfg.kv_bytes(inp.lengths)
+    for _ in range(args.warmup):
+        oracle_step_seconds(inp)
+    secs = [oracle_step_seconds(inp) for _ in range(args.steps)]
+    ms = 1e3 * sum(secs) / len(secs)
+    value = nbytes / (ms * 1e-3) / 1e9
+    sample = (f"float64 numpy oracle on the first {sample_batch} sequence(s) of {cfg.name} per step "
+              f"(lengths {inp.lengths.tolist()}); BLAS limited to 1 thread")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "description": cfg.description, "sample_batch": sample_batch},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.cpu_worker:
+        print(json.dumps(cpu_worker(args.workload, args.cpu_seconds)), flush=True)
+        return 0
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,170 @@
+/*
+ * rra.h — C ABI of the single-token RoPE + GQA decode-attention step (GB300, sm_103a).
+ *
+ * The step, per layer and per sequence b of a batch:
+ *   1. rotate the new token's q [Hq, D] and k [Hkv, D] at its absolute position pos_b
+ *      (RoPE, theta_i = base^(-2i/D), i = 0..D/2-1);
+ *   2. write the rotated k and the unrotated v into cache slot pos_b;
+ *   3. for every query head h: out[b,h] = softmax(q_rot[b,h] . K^T * scale) . V over
+ *      the first L_b cached tokens of KV head h / n_rep (n_rep = Hq / Hkv).
+ *
+ * Sources (pages, by title and section):
+ *   [KVC-GQA-RoPE] "Transformer推理核心：KV Cache、GQA与RoPE原理与工程实践":
+ *       §2.1 attention formula and decode shapes, §2.2 GQA / repeat_interleave,
+ *       §3 RoPE, §4.1 cache layout and paging, §5.1 the per-layer decode order.
+ *   [SelfAttn-Step] "4. 自注意力机制推理：单步计算、KV Cache的引入与原理":
+ *       §4.3 KV cache, §4.5 preallocated cache written by index at slot `step`.
+ *   [Opt-2026] "Transformer架构优化实战2026：注意力机制、KV Cache与推理加速完整指南":
+ *       §三 default scale 1/sqrt(d_k), §四 KVCache.update / PagedKVCache /
+ *       cache-size formula, §六 GQA (n_q_heads must be a multiple of n_kv_heads).
+ *
+ * Conventions shared by every entry point:
+ *   - Tensor pointers are DEVICE pointers owned by the caller; the library never
+ *     allocates, frees or keeps them. Every tensor pointer must be 16-byte aligned.
+ *   - Tensors are dense, row-major, with the element type `dt` (bf16 or fp32);
+ *     positions, seq_lens and block tables are int32.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *     asynchronous on it; a return of RRA_OK means the work was enqueued.
+ *   - Errors the host can see return a negative rra_status before anything is
+ *     enqueued. Errors only the device can see (a position or length beyond the
+ *     cache, a block id outside the pool, a pipeline wait that ran out) set bits of
+ *     *err_flag (a device int32 the caller zeroes and reads back; may be NULL) and
+ *     the affected work is skipped or clamped; no kernel traps.
+ *   - Shapes: B = batch, Hq / Hkv = query / KV heads (Hq % Hkv == 0), D = head_dim
+ *     (64 or 128). B == 0 is a no-op.
+ */
+#ifndef RRA_H
+#define RRA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define RRA_API __attribute__((visibility("default")))
+#else
+#define RRA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { RRA_F32 = 0, RRA_BF16 = 1 } rra_dtype;
+
+typedef enum {
+  RRA_OK = 0,
+  RRA_EINVAL = -1,        /* null pointer, bad shape, Hq % Hkv != 0, misaligned pointer */
+  RRA_EUNSUPPORTED = -2,  /* D not in {64,128}, unknown dtype, block_size not a power of two */
+  RRA_ERANGE = -3,        /* a size beyond what the kernels index (e.g. B > 65535) */
+  RRA_EWORKSPACE = -4,    /* workspace missing or smaller than rra_decode_workspace_bytes() */
+  RRA_ECUDA = -5          /* a CUDA runtime/driver call failed (see rra_last_cuda_error) */
+} rra_status;
+
+/* Bits the kernels OR into *err_flag. */
+enum {
+  RRA_ERR_POSITION = 1,   /* positions[b] < 0 or >= cache capacity: that sequence was not written */
+  RRA_ERR_BLOCK_ID = 2,   /* a block-table entry outside [0, num_blocks): block 0 was used instead */
+  RRA_ERR_SEQ_LEN = 4,    /* seq_lens[b] < 0 or > capacity: clamped into [0, capacity] */
+  RRA_ERR_TIMEOUT = 8     /* an in-kernel pipeline wait gave up (~1 s): results are invalid */
+};
+
+/* Steps 1-2: RoPE on q and k_new at positions[b], then append rotated k and raw v.
+ *
+ * [KVC-GQA-RoPE] §3 (frequencies base^(-2(i-1)/d), i = 1..d/2; the cache keeps
+ * rotated K so only the new token is rotated), §5.1 b.ii-iii; [SelfAttn-Step] §4.5
+ * (write slot `step`); [Opt-2026] §四 (KVCache.update; PagedKVCache block table).
+ *
+ *   q        [B, Hq, D]   input;  q_out [B, Hq, D] output (may alias q)
+ *   k_new    [B, Hkv, D]  input, rotated before it is stored
+ *   v_new    [B, Hkv, D]  input, stored unrotated
+ *   positions[B] int32    absolute position of the new token = its cache slot
+ *   Contiguous cache (block_table == NULL): k_cache, v_cache [B, Hkv, max_len, D];
+ *     slot pos of (b, g) is row ((b*Hkv + g)*max_len + pos).
+ *   Paged cache (block_table != NULL): k_cache, v_cache are pools
+ *     [num_blocks, block_size, Hkv, D]; block_table [B, max_blocks_per_seq] int32 lists
+ *     each sequence's physical blocks in logical order; token pos of sequence b lives
+ *     in block block_table[b][pos / block_size] at slot pos % block_size. The caller
+ *     must have allocated that block. block_size must be a power of two.
+ *   rope_base  RoPE base (10000 for the pages' models; > 1)
+ *   rope_style 0 = half-split pairs (i, i + D/2) ("rotate_half"), 1 = interleaved (2i, 2i+1)
+ * The angle pos * theta_i, its sine and cosine and the rotation are computed in float64
+ * and rounded once to dt (nearest even). Hq + Hkv must not exceed 524280.
+ */
+RRA_API int rra_rope_append(const void* q, const void* k_new, const void* v_new,
+                    const int32_t* positions, void* q_out,
+                    void* k_cache, void* v_cache,
+                    const int32_t* block_table, int max_blocks_per_seq,
+                    int block_size, int num_blocks, int max_len,
+                    int B, int Hq, int Hkv, int D, double rope_base, int rope_style,
+                    rra_dtype dt, int32_t* err_flag, void* stream);
+
+/* Step 3 on a contiguous cache [B, Hkv, max_len, D]:
+ *   out[b,h,:] = softmax(q_rot[b,h,:] . K[b, h/n_rep, 0:L_b, :]^T * scale) . V[b, h/n_rep, 0:L_b, :]
+ * [KVC-GQA-RoPE] §2.1, §2.2 (repeat_interleave: query head h reads KV head h / n_rep);
+ * [SelfAttn-Step] §4.1, §4.5 (K_eff = K_cache[:, :, :step+1]); [Opt-2026] §三 (scale).
+ *
+ *   q_rot     [B, Hq, D]   rotated queries (rra_rope_append's q_out)
+ *   seq_lens  [B] int32    L_b, attended tokens INCLUDING the new one (pos_b + 1);
+ *                          L_b == 0 gives a zero output row
+ *   out       [B, Hq, D]   written in dt (nearest even)
+ *   scale     <= 0 selects 1/sqrt(D)
+ *   num_splits  split-K chunks per sequence (flash-decoding); 0 = chosen by the library
+ *               from the SM count, B, Hkv and the cache capacity. The effective count is
+ *               rra_decode_num_splits(); with more than one split the partial results
+ *               go to `workspace` and a second kernel merges them.
+ *   workspace, ws_bytes  device scratch of at least rra_decode_workspace_bytes() bytes
+ *               (may be NULL when that is 0); contents need no initialisation.
+ * Softmax runs online in float32 per split (running max, running sum, rescaled
+ * accumulator) and the splits merge by log-sum-exp; the result equals the plain
+ * two-pass softmax up to float32 rounding.
+ */
+RRA_API int rra_decode_attn_contig(const void* q_rot, const void* k_cache, const void* v_cache,
+                           const int32_t* seq_lens, void* out,
+                           int B, int Hq, int Hkv, int D, int max_len, float scale,
+                           int num_splits, void* workspace, size_t ws_bytes,
+                           rra_dtype dt, int32_t* err_flag, void* stream);
+
+/* Step 3 on a paged cache: pools [num_blocks, block_size, Hkv, D], block_table
+ * [B, max_blocks_per_seq] int32 ([Opt-2026] §四 PagedKVCache.get_kv_for_attention:
+ * the logical K/V is the table-ordered concatenation of the blocks, cut to L_b).
+ * Only entries 0 .. ceil(L_b / block_size) - 1 of row b are read. Blocks may be
+ * shared between sequences (prefix sharing); they are only read. Other arguments
+ * as in rra_decode_attn_contig.
+ */
+RRA_API int rra_decode_attn_paged(const void* q_rot, const void* k_pool, const void* v_pool,
+                          const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* seq_lens, int block_size, int num_blocks,
+                          void* out, int B, int Hq, int Hkv, int D, float scale,
+                          int num_splits, void* workspace, size_t ws_bytes,
+                          rra_dtype dt, int32_t* err_flag, void* stream);
+
+/* Bytes of a K+V cache: 2 * n_layers * n_kv_heads * head_dim * seq_len * batch * dtype_bytes
+ * ([Opt-2026] §四 memory formula; [KVC-GQA-RoPE] §5.3). Host only; returns 0 when an
+ * argument is negative or the product overflows 64 bits. */
+RRA_API uint64_t rra_kv_bytes(int n_layers, int n_kv_heads, int head_dim, int64_t seq_len,
+                      int batch, int dtype_bytes);
+
+/* --- Helpers (host only; no counterpart on the pages) --- */
+
+/* Effective split count the decode entry points use for these arguments
+ * (max_tokens = max_len for contiguous, max_blocks_per_seq * block_size for paged;
+ * block_size = 0 for contiguous). Negative rra_status on bad arguments. Queries the
+ * current device's SM count when num_splits == 0. */
+RRA_API int rra_decode_num_splits(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
+                          int num_splits, rra_dtype dt);
+
+/* Workspace bytes for B sequences, Hq heads, head_dim D and an EFFECTIVE split count
+ * (from rra_decode_num_splits); 0 when splits <= 1. */
+RRA_API size_t rra_decode_workspace_bytes(int B, int Hq, int D, int splits);
+
+/* Static text for an rra_status value. */
+RRA_API const char* rra_status_str(int status);
+
+/* Text of the last CUDA error an entry point saw on this thread ("" if none). */
+RRA_API const char* rra_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RRA_H */

@@ -1,0 +1,425 @@
+// Split-K GQA decode attention for bf16 caches on the tensor cores (mma.sync m16n8k16).
+//
+// Same math and split/merge structure as decode_kernels.cuh ("Transformer推理核心：KV Cache、
+// GQA与RoPE原理与工程实践" §2.1, §2.2, §4.2; "Transformer架构优化实战2026：注意力机制、KV
+// Cache与推理加速完整指南" §三, §四), with the two contractions of a stage on the tensor cores:
+//
+//   S^T [16 tokens x 8 heads]  = K [16 tokens x D] . Q^T [D x 8 heads]       (D/16 mma)
+//   O^T [D x 8 heads]         += V^T [D x 16 tokens] . P [16 tokens x 8 heads] (D/16 mma)
+//
+// Tokens sit on M and the CTA's query heads (up to 8 of one KV head's group, zero-padded)
+// on N, so a warp keeps only O^T (D/16 fragments of 4 floats) and the scores of 16 tokens
+// in registers. The softmax works on the score fragment directly (each lane owns two heads
+// and two tokens of every 16); the probabilities go back to the tensor cores as the B
+// operand after one movmatrix transpose per 8x8 half, never touching shared memory.
+//
+// Data path: the producer warp streams K and V tiles with 4-D (paged pool) or 3-D
+// (contiguous cache) TMA tensor copies using the 128-byte swizzle, in 64-dim halves, into a
+// 3-stage ring; each consumer warp reads its 16-token slices with ldmatrix (K as the A
+// operand, V through ldmatrix.trans as V^T), conflict-free thanks to the swizzle.
+#pragma once
+
+#include "rra_device.cuh"
+#include "rra_internal.h"
+
+namespace rra {
+
+template <int D>
+struct MmaCfg {
+  static constexpr int kRowBytes = D * 2;                 // bf16
+  static constexpr int kHalves = D / 64;                  // 128-byte swizzle spans per row
+  static constexpr int kTile = 16384 / kRowBytes;         // tokens per stage (K 16 KB + V 16 KB)
+  static constexpr int kStages = 3;
+  static constexpr int kConsumerWarps = 4;
+  static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+  static constexpr int kWarpTokens = kTile / kConsumerWarps;
+  static constexpr int kSteps = kWarpTokens / 16;         // 16-token mma steps per warp per stage
+  static constexpr int kHalfBytes = kTile * 128;          // one 64-dim half of K or V of a stage
+  static constexpr int kStageBytes = 2 * kHalves * kHalfBytes;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kSmemBytes = 1024 + kRingBytes + 2 * kStages * 8 + kMaxTableEntries * 4;
+  static constexpr int kMaxHeads = 8;
+  static constexpr int kKSteps = D / 16;
+};
+
+// Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled buffer.
+__device__ __forceinline__ uint32_t swz(int r, int c) { return (r << 7) + (((c ^ r) & 7) << 4); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void tma_g2s_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                           uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <int D>
+struct MmaWarpState {
+  float o[D / 16][4];   // O^T fragments: dims 16*i + lane/4 (+8), heads 2*(lane%4) + {0,1}
+  float m[2], l[2];     // running max (log2 units) and this lane's partial sum, per owned head
+};
+
+// One 16-token slice of a stage for one warp. CHECK: tokens at or past `valid` are masked
+// (their V rows are zeroed first, so NaN or stale data never reaches the tensor cores).
+template <int D, bool CHECK>
+__device__ __forceinline__ void mma_step(MmaWarpState<D>& st, const uint32_t (&qb)[D / 16][2], uint32_t k_base,
+                                         uint32_t v_base, uint8_t* v_gen, int t0, int valid, int lane,
+                                         float scale_log2) {
+  using C = MmaCfg<D>;
+  if (CHECK) {  // zero V rows t0+i >= valid of this slice (each row: kHalves x 128 bytes)
+    const int first = max(valid - t0, 0);
+    if (first < 16) {
+      for (int idx = lane; idx < (16 - first) * C::kHalves * 8; idx += 32) {
+        const int r = t0 + first + idx / (C::kHalves * 8);
+        const int h = (idx / 8) % C::kHalves, c = idx % 8;
+        *reinterpret_cast<uint4*>(v_gen + h * C::kHalfBytes + swz(r, c)) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();  // these generic writes precede the next TMA write of the stage
+      __syncwarp();
+    }
+  }
+  // scores
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    const int mat = lane >> 3;
+    const int r = t0 + (lane & 7) + ((mat & 1) << 3);
+#pragma unroll
+    for (int kk = 0; kk < C::kKSteps; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(k_base + (kk >> 2) * C::kHalfBytes + swz(r, ((kk & 3) << 1) + (mat >> 1)), a);
+      mma_bf16(s, a, qb[kk][0], qb[kk][1]);
+    }
+  }
+  // online softmax on the fragment: s[j] token t0 + lane/4, s[2 + j] token t0 + lane/4 + 8; head 2*(lane%4) + j
+  const int ta = t0 + (lane >> 2), tb = ta + 8;
+  float x[2][2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    x[j][0] = (!CHECK || ta < valid) ? s[j] * scale_log2 : -INFINITY;
+    x[j][1] = (!CHECK || tb < valid) ? s[2 + j] * scale_log2 : -INFINITY;
+  }
+  float mnew[2];
+  bool grow = false;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float mx = fmaxf(x[j][0], x[j][1]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    mnew[j] = fmaxf(st.m[j], mx);
+    grow |= mnew[j] > st.m[j];
+  }
+  if (__any_sync(0xffffffffu, grow)) {
+    float alpha[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      alpha[j] = mnew[j] > st.m[j] ? exp2f(st.m[j] - mnew[j]) : 1.f;
+      st.l[j] *= alpha[j];
+      st.m[j] = mnew[j];
+    }
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      st.o[i][0] *= alpha[0];
+      st.o[i][1] *= alpha[1];
+      st.o[i][2] *= alpha[0];
+      st.o[i][3] *= alpha[1];
+    }
+  }
+  float p[2][2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float mref = st.m[j] == -INFINITY ? 0.f : st.m[j];
+    p[j][0] = exp2f(x[j][0] - mref);
+    p[j][1] = exp2f(x[j][1] - mref);
+    st.l[j] += p[j][0] + p[j][1];
+  }
+  // P as the B operand (k = token, n = head): transpose the two 8x8 token halves.
+  const uint32_t b0 = movmatrix_trans(pack_bf16x2(p[0][0], p[1][0]));
+  const uint32_t b1 = movmatrix_trans(pack_bf16x2(p[0][1], p[1][1]));
+  {
+    const int mat = lane >> 3;
+    const int r = t0 + (lane & 7) + ((mat >> 1) << 3);
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      uint32_t a[4];
+      ldsm_x4_trans(v_base + (i >> 2) * C::kHalfBytes + swz(r, ((i & 3) << 1) + (mat & 1)), a);
+      mma_bf16(st.o[i], a, b0, b1);
+    }
+  }
+}
+
+template <int D, bool PAGED>
+__global__ void __launch_bounds__(MmaCfg<D>::kThreads, 2)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+                      const DecodeArgs a) {
+  using C = MmaCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int n_rep = a.Hq / a.Hkv;
+  const int hpc = a.hpc;
+  const int slices = n_rep / hpc;
+  const int split = blockIdx.x / slices;
+  const int g = blockIdx.y;
+  const int h0 = g * n_rep + (blockIdx.x - split * slices) * hpc;
+  const int b = blockIdx.z;
+
+  int L = a.seq_lens[b];
+  if (L < 0 || L > a.capacity) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) flag_error(a.err, RRA_ERR_SEQ_LEN);
+    L = min(max(L, 0), a.capacity);
+  }
+  const int start = split * a.chunk;
+  if (start >= L) {
+    if (L == 0 && a.num_splits == 1) {
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(b) * a.Hq + h0) * D;
+      for (int i = threadIdx.x; i < hpc * D; i += blockDim.x) out[i] = __float2bfloat16_rn(0.f);
+    }
+    return;
+  }
+  const int end = min(L, start + a.chunk);
+  const int n_tiles = (end - start + C::kTile - 1) / C::kTile;
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRingBytes);
+  uint64_t* empty = full + C::kStages;
+  int32_t* tbl = reinterpret_cast<int32_t*>(empty + C::kStages);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::kConsumerWarps);
+    }
+    fence_barrier_init();
+  }
+  int first_blk = 0;
+  if constexpr (PAGED) {
+    first_blk = start >> a.log2_bs;
+    const int n_blk = ((end - 1) >> a.log2_bs) - first_blk + 1;
+    const int32_t* row = a.block_table + static_cast<size_t>(b) * a.max_blocks_per_seq + first_blk;
+    for (int i = threadIdx.x; i < n_blk; i += blockDim.x) {
+      int id = row[i];
+      if (id < 0 || id >= a.num_blocks) {
+        flag_error(a.err, RRA_ERR_BLOCK_ID);
+        id = 0;
+      }
+      tbl[i] = id;
+    }
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------------ producer
+  if (warp == C::kConsumerWarps) {
+    if (lane == 0) {
+      prefetch_tensormap(&k_map);
+      prefetch_tensormap(&v_map);
+      int issued = 0;
+      for (int it = 0; it < n_tiles; ++it) {
+        const int s = it % C::kStages;
+        if (it >= C::kStages && !mbar_wait(&empty[s], ((it / C::kStages) - 1) & 1)) {
+          flag_error(a.err, RRA_ERR_TIMEOUT);
+          break;
+        }
+        const int t0 = start + it * C::kTile;
+        uint8_t* kst = smem + s * C::kStageBytes;
+        uint8_t* vst = kst + C::kHalves * C::kHalfBytes;
+        if constexpr (PAGED) {
+          const int bs = 1 << a.log2_bs;
+          if (bs <= C::kTile) {  // whole blocks, one box of bs rows per block and half
+            const int rows = min(C::kTile, end - t0);
+            const int nblk = (rows + bs - 1) >> a.log2_bs;
+            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * C::kHalves * nblk * bs * 128));
+            const int j0 = (t0 >> a.log2_bs) - first_blk;
+            for (int jb = 0; jb < nblk; ++jb) {
+              const int phys = tbl[j0 + jb];
+#pragma unroll
+              for (int h = 0; h < C::kHalves; ++h) {
+                tma_g2s_4d(kst + h * C::kHalfBytes + jb * bs * 128, &k_map, 64 * h, g, 0, phys, &full[s]);
+                tma_g2s_4d(vst + h * C::kHalfBytes + jb * bs * 128, &v_map, 64 * h, g, 0, phys, &full[s]);
+              }
+            }
+          } else {  // a kTile-row window of one block
+            const int phys = tbl[(t0 >> a.log2_bs) - first_blk];
+            const int off = t0 & (bs - 1);
+            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * C::kHalves * C::kTile * 128));
+#pragma unroll
+            for (int h = 0; h < C::kHalves; ++h) {
+              tma_g2s_4d(kst + h * C::kHalfBytes, &k_map, 64 * h, g, off, phys, &full[s]);
+              tma_g2s_4d(vst + h * C::kHalfBytes, &v_map, 64 * h, g, off, phys, &full[s]);
+            }
+          }
+        } else {  // contiguous: box of kTile rows of sequence b, head g (rows past max_len read as 0)
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * C::kHalves * C::kTile * 128));
+          const int bg = b * a.Hkv + g;
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h) {
+            tma_g2s_3d(kst + h * C::kHalfBytes, &k_map, 64 * h, t0, bg, &full[s]);
+            tma_g2s_3d(vst + h * C::kHalfBytes, &v_map, 64 * h, t0, bg, &full[s]);
+          }
+        }
+        issued = it + 1;
+      }
+      for (int it = issued > C::kStages ? issued - C::kStages : 0; it < issued; ++it)
+        mbar_wait(&full[it % C::kStages], (it / C::kStages) & 1);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  // Q^T as the B operand: lane holds q[head lane/4][dims 16kk + 2(lane%4) + {0,1}] and (+8).
+  uint32_t qb[C::kKSteps][2];
+  {
+    const int hd = lane >> 2;
+    const uint32_t* q = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                          (static_cast<size_t>(b) * a.Hq + h0 + hd) * D);
+#pragma unroll
+    for (int kk = 0; kk < C::kKSteps; ++kk) {
+      qb[kk][0] = hd < hpc ? q[kk * 8 + (lane & 3)] : 0u;
+      qb[kk][1] = hd < hpc ? q[kk * 8 + 4 + (lane & 3)] : 0u;
+    }
+  }
+  MmaWarpState<D> st;
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
+  st.m[0] = st.m[1] = -INFINITY;
+  st.l[0] = st.l[1] = 0.f;
+
+  for (int it = 0; it < n_tiles; ++it) {
+    const int s = it % C::kStages;
+    if (!mbar_wait(&full[s], (it / C::kStages) & 1)) {
+      flag_error(a.err, RRA_ERR_TIMEOUT);
+      break;
+    }
+    uint8_t* kst = smem + s * C::kStageBytes;
+    uint8_t* vst = kst + C::kHalves * C::kHalfBytes;
+    const uint32_t k_base = smem_addr(kst), v_base = smem_addr(vst);
+    const int valid = min(C::kTile, end - (start + it * C::kTile));
+#pragma unroll
+    for (int step = 0; step < C::kSteps; ++step) {
+      const int t0 = warp * C::kWarpTokens + step * 16;
+      if (valid == C::kTile)
+        mma_step<D, false>(st, qb, k_base, v_base, vst, t0, valid, lane, a.scale_log2);
+      else if (t0 < valid)
+        mma_step<D, true>(st, qb, k_base, v_base, vst, t0, valid, lane, a.scale_log2);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+
+  // ------------------------------------------------------------------ merge the 4 warps
+  constexpr int kConsumers = C::kConsumerWarps * 32;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 4);
+    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 8);
+    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 16);
+  }
+  named_barrier_sync(1, kConsumers);
+  float* red_o = reinterpret_cast<float*>(smem);                 // [warps][8 heads][D]
+  float* red_m = red_o + C::kConsumerWarps * C::kMaxHeads * D;   // [warps][8 heads]
+  float* red_l = red_m + C::kConsumerWarps * C::kMaxHeads;
+  {
+    const int hd0 = 2 * (lane & 3), dl = lane >> 2;
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        red_o[(warp * C::kMaxHeads + hd0 + j) * D + 16 * i + dl] = st.o[i][j];
+        red_o[(warp * C::kMaxHeads + hd0 + j) * D + 16 * i + 8 + dl] = st.o[i][2 + j];
+      }
+    }
+    if (dl == 0) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        red_m[warp * C::kMaxHeads + hd0 + j] = st.m[j];
+        red_l[warp * C::kMaxHeads + hd0 + j] = st.l[j];
+      }
+    }
+  }
+  named_barrier_sync(1, kConsumers);
+  for (int idx = threadIdx.x; idx < hpc * D; idx += kConsumers) {
+    const int h = idx / D, d = idx - h * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < C::kConsumerWarps; ++w) M = fmaxf(M, red_m[w * C::kMaxHeads + h]);
+    float lsum = 0.f, osum = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < C::kConsumerWarps; ++w) {
+        const float wt = exp2f(red_m[w * C::kMaxHeads + h] - M);
+        lsum = fmaf(wt, red_l[w * C::kMaxHeads + h], lsum);
+        osum = fmaf(wt, red_o[(w * C::kMaxHeads + h) * D + d], osum);
+      }
+    }
+    const size_t bh = static_cast<size_t>(b) * a.Hq + h0 + h;
+    if (a.num_splits == 1) {
+      static_cast<__nv_bfloat16*>(a.out)[bh * D + d] = __float2bfloat16_rn(lsum > 0.f ? osum / lsum : 0.f);
+    } else {
+      const size_t ps = bh * a.num_splits + split;
+      a.ws_o[ps * D + d] = osum;
+      if (d == 0) {
+        a.ws_ml[2 * ps] = M;
+        a.ws_ml[2 * ps + 1] = lsum;
+      }
+    }
+  }
+}
+
+template <int D, bool PAGED>
+cudaError_t launch_decode_mma_t(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm, int hpc,
+                                cudaStream_t st) {
+  using C = MmaCfg<D>;
+  static int done[64] = {0};
+  auto kern = decode_mma_kernel<D, PAGED>;
+  cudaError_t e = ensure_smem(kern, C::kSmemBytes, done);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(a.num_splits * ((a.Hq / a.Hkv) / hpc), a.Hkv, a.B);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(km, vm, a);
+  return cudaGetLastError();
+}
+
+template <bool PAGED>
+cudaError_t launch_decode_mma(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm, int hpc,
+                              cudaStream_t st) {
+  if (a.D == 128) return launch_decode_mma_t<128, PAGED>(a, km, vm, hpc, st);
+  return launch_decode_mma_t<64, PAGED>(a, km, vm, hpc, st);
+}
+
+}  // namespace rra

@@ -1,0 +1,364 @@
+// The extern "C" entry points declared in include/rra.h: argument checks, split
+// planning, tensor-map encoding for the paged pools, and kernel dispatch.
+// Nothing here allocates device memory; every buffer belongs to the caller.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "rra_internal.h"
+
+namespace {
+
+thread_local char g_cuda_error[256] = "";
+
+int cuda_fail(cudaError_t e, const char* where) {
+  std::snprintf(g_cuda_error, sizeof(g_cuda_error), "%s: %s (%s)", where, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return RRA_ECUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+int ilog2(int x) {
+  int r = 0;
+  while ((1 << r) < x) ++r;
+  return r;
+}
+int elem_bytes(rra_dtype dt) { return dt == RRA_BF16 ? 2 : 4; }
+
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// How the decode work is cut: kernel, query heads per CTA, token chunk per split, split count.
+struct Plan {
+  bool mma = false;  // bf16 tensor-core kernel
+  int hpc = 1;
+  int tile = 0;
+  int chunk = 0;
+  int splits = 1;
+};
+
+// The tensor-core kernel takes bf16 with TMA destinations on 1024-byte swizzle atoms:
+// contiguous caches at least one tile long, paged blocks of at least 8 tokens.
+bool use_mma_kernel(rra_dtype dt, int D, int64_t max_tokens, int block_size) {
+  if (dt != RRA_BF16) return false;
+  if (block_size > 0) return block_size >= 8;
+  return max_tokens >= rra::decode_mma_tile_tokens(D);
+}
+
+int heads_per_cta(int n_rep, bool mma) {
+  if (mma) {
+    if (n_rep <= 8) return n_rep;
+    for (int h = 8; h > 1; --h)
+      if (n_rep % h == 0) return h;
+    return 1;
+  }
+  return n_rep % 4 == 0 ? 4 : (n_rep % 2 == 0 ? 2 : 1);
+}
+
+int check_shapes(int B, int Hq, int Hkv, int D, rra_dtype dt) {
+  if (dt != RRA_F32 && dt != RRA_BF16) return RRA_EUNSUPPORTED;
+  if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return RRA_EINVAL;
+  if (D != 64 && D != 128) return RRA_EUNSUPPORTED;
+  if (B > 65535) return RRA_ERANGE;
+  return RRA_OK;
+}
+
+// max_tokens: per-sequence capacity; block_size: 0 for a contiguous cache.
+int make_plan(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size, int requested, rra_dtype dt,
+              Plan* p) {
+  int st = check_shapes(B, Hq, Hkv, D, dt);
+  if (st != RRA_OK) return st;
+  if (requested < 0 || max_tokens < 0) return RRA_EINVAL;
+  if (max_tokens > (int64_t(1) << 30)) return RRA_ERANGE;
+  const int n_rep = Hq / Hkv;
+  p->mma = use_mma_kernel(dt, D, max_tokens, block_size);
+  p->hpc = heads_per_cta(n_rep, p->mma);
+  if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
+  p->tile = p->mma ? rra::decode_mma_tile_tokens(D) : rra::decode_tile_tokens(D, elem_bytes(dt));
+  const int64_t tiles = std::max<int64_t>(1, (max_tokens + p->tile - 1) / p->tile);
+  // A paged split copies its block ids to shared memory: at most kMaxTableEntries of them.
+  int64_t max_chunk_tiles = tiles;
+  if (block_size > 0)
+    max_chunk_tiles = std::max<int64_t>(1, (int64_t(rra::kMaxTableEntries - 1) * block_size) / p->tile);
+  int64_t chunk_tiles;
+  if (requested > 0) {
+    chunk_tiles = (tiles + requested - 1) / requested;
+  } else {
+    // Aim at ~4 CTAs per SM over the whole grid, each streaming 128..1024 tokens.
+    const int64_t units = int64_t(B) * Hkv * (n_rep / p->hpc);
+    const int64_t target = 4 * std::max(1, sm_count());
+    chunk_tiles = (tiles * units + target - 1) / target;
+    const int64_t lo = std::max(1, 128 / p->tile), hi = std::max(1, 1024 / p->tile);
+    chunk_tiles = std::min(std::max(chunk_tiles, lo), hi);
+  }
+  chunk_tiles = std::min(std::max<int64_t>(chunk_tiles, 1), max_chunk_tiles);
+  const int64_t splits = (tiles + chunk_tiles - 1) / chunk_tiles;
+  if (splits * (n_rep / p->hpc) > 65535 * 1024) return RRA_ERANGE;
+  p->chunk = static_cast<int>(chunk_tiles * p->tile);
+  p->splits = static_cast<int>(splits);
+  return RRA_OK;
+}
+
+size_t workspace_bytes(int B, int Hq, int D, int splits) {
+  if (splits <= 1 || B <= 0) return 0;
+  const size_t rows = size_t(B) * Hq * splits;
+  const size_t o_bytes = (rows * D * sizeof(float) + 255) & ~size_t(255);
+  return o_bytes + rows * 2 * sizeof(float);
+}
+
+// Tiled tensor map over `base` (rank 3 or 4, dims innermost first, strides in bytes of dims 1..).
+int encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+               const cuuint32_t* box, rra_dtype dt, bool swizzle128) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) {
+    std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled unavailable");
+    return RRA_ECUDA;
+  }
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r =
+      enc(map, dt == RRA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank,
+          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));
+    return RRA_ECUDA;
+  }
+  return RRA_OK;
+}
+
+// Pool [num_blocks, block_size, Hkv, D] as 4-D {D, Hkv, block_size, num_blocks}; the box is
+// one head's rows of one block (64-dim halves with the 128-byte swizzle for the mma kernel).
+int encode_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int Hkv, int D, int box_rows,
+                    rra_dtype dt, bool mma) {
+  const cuuint64_t es = elem_bytes(dt);
+  const cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(Hkv), cuuint64_t(block_size), cuuint64_t(num_blocks)};
+  const cuuint64_t strides[3] = {D * es, cuuint64_t(Hkv) * D * es, cuuint64_t(block_size) * Hkv * D * es};
+  const cuuint32_t box[4] = {cuuint32_t(mma ? 64 : D), 1u, cuuint32_t(box_rows), 1u};
+  return encode_map(map, pool, 4, dims, strides, box, dt, mma);
+}
+
+// Contiguous cache [B, Hkv, max_len, D] as 3-D {D, max_len, B*Hkv}, boxes of 64 dims x tile rows.
+int encode_contig_map(CUtensorMap* map, const void* cache, int B, int Hkv, int max_len, int D, int tile,
+                      rra_dtype dt) {
+  const cuuint64_t es = elem_bytes(dt);
+  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(max_len), cuuint64_t(B) * Hkv};
+  const cuuint64_t strides[2] = {D * es, cuuint64_t(max_len) * D * es};
+  const cuuint32_t box[3] = {64u, cuuint32_t(tile), 1u};
+  return encode_map(map, cache, 3, dims, strides, box, dt, true);
+}
+
+int check_workspace(const Plan& p, int B, int Hq, int D, const void* ws, size_t ws_bytes) {
+  const size_t need = workspace_bytes(B, Hq, D, p.splits);
+  if (need == 0) return RRA_OK;
+  if (ws == nullptr || ws_bytes < need || !aligned16(ws)) return RRA_EWORKSPACE;
+  return RRA_OK;
+}
+
+rra::DecodeArgs decode_args(const Plan& p, const void* q, const void* k, const void* v, const int32_t* seq_lens,
+                            void* out, int B, int Hq, int Hkv, int D, float scale, void* ws, int32_t* err) {
+  rra::DecodeArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.seq_lens = seq_lens;
+  a.out = out;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.hpc = p.hpc;
+  a.num_splits = p.splits;
+  a.chunk = p.chunk;
+  const float s = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
+  a.scale_log2 = s * 1.4426950408889634f;
+  a.err = err;
+  if (p.splits > 1) {
+    const size_t rows = size_t(B) * Hq * p.splits;
+    a.ws_o = static_cast<float*>(ws);
+    a.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ((rows * D * sizeof(float) + 255) & ~size_t(255)));
+  }
+  return a;
+}
+
+int finish_decode(const rra::DecodeArgs& a, rra_dtype dt, cudaError_t e, cudaStream_t st) {
+  if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+  if (a.num_splits > 1) {
+    e = rra::launch_decode_reduce(a, dt, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode reduce launch");
+  }
+  return RRA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rra_status_str(int status) {
+  switch (status) {
+    case RRA_OK: return "ok";
+    case RRA_EINVAL: return "invalid argument";
+    case RRA_EUNSUPPORTED: return "unsupported configuration";
+    case RRA_ERANGE: return "size out of range";
+    case RRA_EWORKSPACE: return "workspace missing or too small";
+    case RRA_ECUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+const char* rra_last_cuda_error(void) { return g_cuda_error; }
+
+uint64_t rra_kv_bytes(int n_layers, int n_kv_heads, int head_dim, int64_t seq_len, int batch, int dtype_bytes) {
+  if (n_layers < 0 || n_kv_heads < 0 || head_dim < 0 || seq_len < 0 || batch < 0 || dtype_bytes < 0) return 0;
+  const uint64_t f[6] = {2u, uint64_t(n_layers), uint64_t(n_kv_heads), uint64_t(head_dim), uint64_t(batch),
+                         uint64_t(dtype_bytes)};
+  uint64_t r = uint64_t(seq_len);
+  for (uint64_t x : f) {
+    if (x != 0 && r > UINT64_MAX / x) return 0;
+    r *= x;
+  }
+  return r;
+}
+
+int rra_decode_num_splits(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size, int num_splits,
+                          rra_dtype dt) {
+  if (block_size < 0 || (block_size > 0 && !pow2(block_size))) return block_size < 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
+  Plan p;
+  const int st = make_plan(B, Hq, Hkv, D, max_tokens, block_size, num_splits, dt, &p);
+  return st != RRA_OK ? st : p.splits;
+}
+
+size_t rra_decode_workspace_bytes(int B, int Hq, int D, int splits) { return workspace_bytes(B, Hq, D, splits); }
+
+int rra_rope_append(const void* q, const void* k_new, const void* v_new, const int32_t* positions, void* q_out,
+                    void* k_cache, void* v_cache, const int32_t* block_table, int max_blocks_per_seq, int block_size,
+                    int num_blocks, int max_len, int B, int Hq, int Hkv, int D, double rope_base, int rope_style,
+                    rra_dtype dt, int32_t* err_flag, void* stream) {
+  int st = check_shapes(B, Hq, Hkv, D, dt);
+  if (st != RRA_OK) return st;
+  if (!(rope_base > 1.0) || !std::isfinite(rope_base) || (rope_style != 0 && rope_style != 1)) return RRA_EINVAL;
+  if (int64_t(Hq) + Hkv > 8 * 65535) return RRA_ERANGE;
+  if (B == 0) return RRA_OK;
+  if (!q || !k_new || !v_new || !positions || !q_out || !k_cache || !v_cache) return RRA_EINVAL;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(q_out) || !aligned16(k_cache) ||
+      !aligned16(v_cache))
+    return RRA_EINVAL;
+  rra::RopeArgs a{};
+  if (block_table != nullptr) {
+    if (!pow2(block_size)) return block_size <= 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
+    if (max_blocks_per_seq < 1 || num_blocks < 1) return RRA_EINVAL;
+    if (int64_t(max_blocks_per_seq) * block_size > (int64_t(1) << 30)) return RRA_ERANGE;
+    a.log2_bs = ilog2(block_size);
+  } else if (max_len < 1) {
+    return RRA_EINVAL;
+  }
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.positions = positions;
+  a.q_out = q_out;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_table = block_table;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.max_len = max_len;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  constexpr double kPi = 3.14159265358979323846;
+  for (int i = 0; i < D / 2; ++i) a.inv_freq[i] = std::pow(rope_base, -2.0 * i / D) / kPi;
+  a.rope_style = rope_style;
+  a.err = err_flag;
+  const cudaError_t e = rra::launch_rope_append(a, dt, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RRA_OK : cuda_fail(e, "rope_append launch");
+}
+
+int rra_decode_attn_contig(const void* q_rot, const void* k_cache, const void* v_cache, const int32_t* seq_lens,
+                           void* out, int B, int Hq, int Hkv, int D, int max_len, float scale, int num_splits,
+                           void* workspace, size_t ws_bytes, rra_dtype dt, int32_t* err_flag, void* stream) {
+  if (max_len < 1) return RRA_EINVAL;
+  Plan p;
+  int st = make_plan(B, Hq, Hkv, D, max_len, 0, num_splits, dt, &p);
+  if (st != RRA_OK) return st;
+  if (B == 0) return RRA_OK;
+  if (!q_rot || !k_cache || !v_cache || !seq_lens || !out) return RRA_EINVAL;
+  if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return RRA_EINVAL;
+  if (!std::isfinite(scale)) return RRA_EINVAL;
+  st = check_workspace(p, B, Hq, D, workspace, ws_bytes);
+  if (st != RRA_OK) return st;
+  CUtensorMap km{}, vm{};
+  if (p.mma) {
+    st = encode_contig_map(&km, k_cache, B, Hkv, max_len, D, p.tile, dt);
+    if (st != RRA_OK) return st;
+    st = encode_contig_map(&vm, v_cache, B, Hkv, max_len, D, p.tile, dt);
+    if (st != RRA_OK) return st;
+  }
+  rra::DecodeArgs a = decode_args(p, q_rot, k_cache, v_cache, seq_lens, out, B, Hq, Hkv, D, scale, workspace, err_flag);
+  a.max_len = max_len;
+  a.capacity = max_len;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish_decode(a, dt, rra::launch_decode_contig(a, km, vm, dt, p.mma, s), s);
+}
+
+int rra_decode_attn_paged(const void* q_rot, const void* k_pool, const void* v_pool, const int32_t* block_table,
+                          int max_blocks_per_seq, const int32_t* seq_lens, int block_size, int num_blocks, void* out,
+                          int B, int Hq, int Hkv, int D, float scale, int num_splits, void* workspace,
+                          size_t ws_bytes, rra_dtype dt, int32_t* err_flag, void* stream) {
+  if (!pow2(block_size)) return block_size <= 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
+  if (max_blocks_per_seq < 1 || num_blocks < 1) return RRA_EINVAL;
+  const int64_t capacity = int64_t(max_blocks_per_seq) * block_size;
+  Plan p;
+  int st = make_plan(B, Hq, Hkv, D, capacity, block_size, num_splits, dt, &p);
+  if (st != RRA_OK) return st;
+  if (B == 0) return RRA_OK;
+  if (!q_rot || !k_pool || !v_pool || !block_table || !seq_lens || !out) return RRA_EINVAL;
+  if (!aligned16(q_rot) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out)) return RRA_EINVAL;
+  if (!std::isfinite(scale)) return RRA_EINVAL;
+  st = check_workspace(p, B, Hq, D, workspace, ws_bytes);
+  if (st != RRA_OK) return st;
+  const int box_rows = block_size < p.tile ? block_size : p.tile;
+  CUtensorMap km, vm;
+  st = encode_pool_map(&km, k_pool, num_blocks, block_size, Hkv, D, box_rows, dt, p.mma);
+  if (st != RRA_OK) return st;
+  st = encode_pool_map(&vm, v_pool, num_blocks, block_size, Hkv, D, box_rows, dt, p.mma);
+  if (st != RRA_OK) return st;
+  rra::DecodeArgs a = decode_args(p, q_rot, k_pool, v_pool, seq_lens, out, B, Hq, Hkv, D, scale, workspace, err_flag);
+  a.block_table = block_table;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.log2_bs = ilog2(block_size);
+  a.num_blocks = num_blocks;
+  a.max_len = 0;
+  a.capacity = static_cast<int>(capacity);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return finish_decode(a, dt, rra::launch_decode_paged(a, km, vm, dt, p.mma, s), s);
+}
+
+}  // extern "C"

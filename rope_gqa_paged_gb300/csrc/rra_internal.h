@@ -1,0 +1,72 @@
+// Launch interface between the C ABI (rra_abi.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/rra.h"
+
+namespace rra {
+
+constexpr int kMaxHeadDim = 512;
+
+struct RopeArgs {
+  const void* q;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* positions;
+  void* q_out;
+  void* k_cache;
+  void* v_cache;
+  const int32_t* block_table;  // nullptr: contiguous cache
+  int max_blocks_per_seq;
+  int log2_bs;
+  int num_blocks;
+  int max_len;
+  int B, Hq, Hkv, D;
+  int rope_style;
+  int32_t* err;
+  double inv_freq[kMaxHeadDim / 2];  // theta_i / pi, theta_i = base^(-2i/D), formed on the host in float64
+};
+
+struct DecodeArgs {
+  const void* q;                // q_rot [B, Hq, D]
+  const void* k;                // contiguous caches [B, Hkv, max_len, D] (paged: pools, read via tensor maps)
+  const void* v;
+  const int32_t* seq_lens;      // [B]
+  const int32_t* block_table;   // [B, max_blocks_per_seq] (paged only)
+  int max_blocks_per_seq;
+  int log2_bs;
+  int num_blocks;
+  void* out;                    // [B, Hq, D]
+  float* ws_o;                  // [B, Hq, splits, D] unnormalised partial outputs
+  float* ws_ml;                 // [B, Hq, splits, 2] (running max in log2 units, running sum)
+  int B, Hq, Hkv, D;
+  int max_len;                  // contiguous row stride in tokens
+  int capacity;                 // tokens a sequence can hold
+  int hpc;                      // query heads per CTA (divides Hq / Hkv)
+  int num_splits;               // effective split count
+  int chunk;                    // tokens per split (a multiple of the tile)
+  float scale_log2;             // softmax scale * log2(e)
+  int32_t* err;
+};
+
+// Tokens per pipeline stage for a head_dim and element size: K + V tiles of 16 KB.
+inline int decode_tile_tokens(int D, int elem_bytes) { return 8192 / (D * elem_bytes); }
+// Most block-table entries one split may need (bounds the per-CTA table copy).
+constexpr int kMaxTableEntries = 2048;
+
+cudaError_t launch_rope_append(const RopeArgs& a, rra_dtype dt, cudaStream_t stream);
+// Tokens per stage of the tensor-core (bf16) decode kernel: K + V tiles of 32 KB.
+inline int decode_mma_tile_tokens(int D) { return 16384 / (D * 2); }
+
+// use_mma: the bf16 tensor-core kernel (tensor maps with the 128-byte swizzle); otherwise the
+// CUDA-core kernel (contiguous: 1-D bulk copies, maps unused; paged: unswizzled maps).
+cudaError_t launch_decode_contig(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                 rra_dtype dt, bool use_mma, cudaStream_t stream);
+cudaError_t launch_decode_paged(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                rra_dtype dt, bool use_mma, cudaStream_t stream);
+cudaError_t launch_decode_reduce(const DecodeArgs& a, rra_dtype dt, cudaStream_t stream);
+
+}  // namespace rra

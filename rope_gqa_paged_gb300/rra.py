@@ -1,0 +1,162 @@
+"""ctypes binding of librra_gb300.so: the C entry points under the same names.
+
+Argument marshalling only: shapes are read from the torch tensors, pointers and the
+current CUDA stream are passed through, and a non-zero status raises RraError. Every
+step of the decode path runs in the library's CUDA kernels; there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+RRA_F32, RRA_BF16 = 0, 1
+RRA_ERR_POSITION, RRA_ERR_BLOCK_ID, RRA_ERR_SEQ_LEN, RRA_ERR_TIMEOUT = 1, 2, 4, 8
+
+_lib: Optional[ctypes.CDLL] = None
+
+_c_int, _c_i64, _c_u64, _c_size, _c_f32, _c_f64, _vp = (ctypes.c_int, ctypes.c_int64, ctypes.c_uint64,
+                                                         ctypes.c_size_t, ctypes.c_float, ctypes.c_double,
+                                                         ctypes.c_void_p)
+_SIGNATURES = {
+    "rra_rope_append": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                 _c_int, _c_int, _c_int, _c_int, _c_f64, _c_int, _c_int, _vp, _vp]),
+    "rra_decode_attn_contig": (_c_int, [_vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int, _c_f32,
+                                        _c_int, _vp, _c_size, _c_int, _vp, _vp]),
+    "rra_decode_attn_paged": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _vp, _c_int, _c_int,
+                                       _c_int, _c_int, _c_f32, _c_int, _vp, _c_size, _c_int, _vp, _vp]),
+    "rra_kv_bytes": (_c_u64, [_c_int, _c_int, _c_int, _c_i64, _c_int, _c_int]),
+    "rra_decode_num_splits": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int]),
+    "rra_decode_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "rra_status_str": (ctypes.c_char_p, [_c_int]),
+    "rra_last_cuda_error": (ctypes.c_char_p, []),
+}
+
+
+class RraError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        detail = lib().rra_status_str(status).decode()
+        if status == -5:
+            detail += ": " + lib().rra_last_cuda_error().decode()
+        super().__init__(f"{fn} returned {status} ({detail})")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load the library (it must have been built; see __graft_entry__.build())."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB_PATH):
+            raise RuntimeError(f"{_build.LIB_PATH} is missing: build the CUDA library first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        handle = ctypes.CDLL(_build.LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = handle
+    return _lib
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return RRA_BF16
+    if t.dtype == torch.float32:
+        return RRA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the decode kernels must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(name: str, status: int) -> None:
+    if status != 0:
+        raise RraError(name, status)
+
+
+# --------------------------------------------------------------------------- host-only helpers
+def rra_kv_bytes(n_layers: int, n_kv_heads: int, head_dim: int, seq_len: int, batch: int, dtype_bytes: int) -> int:
+    return int(lib().rra_kv_bytes(n_layers, n_kv_heads, head_dim, seq_len, batch, dtype_bytes))
+
+
+def rra_decode_num_splits(B: int, Hq: int, Hkv: int, D: int, max_tokens: int, block_size: int,
+                          num_splits: int, dtype: int) -> int:
+    r = lib().rra_decode_num_splits(B, Hq, Hkv, D, max_tokens, block_size, num_splits, dtype)
+    _check("rra_decode_num_splits", min(r, 0))
+    return r
+
+
+def rra_decode_workspace_bytes(B: int, Hq: int, D: int, splits: int) -> int:
+    return int(lib().rra_decode_workspace_bytes(B, Hq, D, splits))
+
+
+def rra_status_str(status: int) -> str:
+    return lib().rra_status_str(status).decode()
+
+
+# --------------------------------------------------------------------------- device entry points
+def rra_rope_append(q, k_new, v_new, positions, q_out, k_cache, v_cache, block_table=None,
+                    rope_base: float = 10000.0, rope_style: int = 0, err_flag=None, stream=None) -> None:
+    """RoPE on q / k_new at ``positions`` and append of rotated k and raw v into the cache.
+
+    Contiguous cache: k_cache/v_cache [B, Hkv, max_len, D]. Paged: pools
+    [num_blocks, block_size, Hkv, D] plus ``block_table`` [B, max_blocks_per_seq] int32.
+    """
+    B, Hq, D = q.shape
+    Hkv = k_new.shape[1]
+    if block_table is not None:
+        num_blocks, block_size = k_cache.shape[0], k_cache.shape[1]
+        mbps, max_len = block_table.shape[1], 0
+    else:
+        num_blocks = block_size = mbps = 0
+        max_len = k_cache.shape[2]
+    st = lib().rra_rope_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q_out), _ptr(k_cache),
+                               _ptr(v_cache), _ptr(block_table), mbps, block_size, num_blocks, max_len, B, Hq, Hkv,
+                               D, float(rope_base), int(rope_style), _dtype_code(q), _ptr(err_flag), _stream(stream))
+    _check("rra_rope_append", st)
+
+
+def rra_decode_attn_contig(q_rot, k_cache, v_cache, seq_lens, out, scale: float = 0.0, num_splits: int = 0,
+                           workspace=None, err_flag=None, stream=None) -> None:
+    """out = GQA softmax attention of q_rot over the first seq_lens[b] slots of a contiguous cache."""
+    B, Hq, D = q_rot.shape
+    Hkv, max_len = k_cache.shape[1], k_cache.shape[2]
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().rra_decode_attn_contig(_ptr(q_rot), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out), B, Hq,
+                                      Hkv, D, max_len, float(scale), int(num_splits), _ptr(workspace), ws_bytes,
+                                      _dtype_code(q_rot), _ptr(err_flag), _stream(stream))
+    _check("rra_decode_attn_contig", st)
+
+
+def rra_decode_attn_paged(q_rot, k_pool, v_pool, block_table, seq_lens, out, scale: float = 0.0,
+                          num_splits: int = 0, workspace=None, err_flag=None, stream=None) -> None:
+    """out = GQA softmax attention of q_rot over each sequence's blocks of a paged pool."""
+    B, Hq, D = q_rot.shape
+    num_blocks, block_size, Hkv = k_pool.shape[0], k_pool.shape[1], k_pool.shape[2]
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().rra_decode_attn_paged(_ptr(q_rot), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
+                                     block_table.shape[1], _ptr(seq_lens), block_size, num_blocks, _ptr(out), B, Hq,
+                                     Hkv, D, float(scale), int(num_splits), _ptr(workspace), ws_bytes,
+                                     _dtype_code(q_rot), _ptr(err_flag), _stream(stream))
+    _check("rra_decode_attn_paged", st)

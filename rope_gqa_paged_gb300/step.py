@@ -1,0 +1,63 @@
+"""DecodeStep: one layer's decode step (RoPE + append + GQA attention) on caller-owned caches.
+
+It owns the per-step buffers (rotated q, output, split-K workspace, device error word),
+allocated once through torch, and issues the library's kernels on the current stream:
+``rra_rope_append`` then ``rra_decode_attn_contig`` / ``rra_decode_attn_paged``.
+"""
+
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import rra
+
+
+class DecodeStep:
+    def __init__(self, batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int, k_cache: torch.Tensor,
+                 v_cache: torch.Tensor, block_table: Optional[torch.Tensor] = None, num_splits: int = 0,
+                 rope_base: float = 10000.0, rope_style: int = 0, scale: float = 0.0):
+        self.B, self.Hq, self.Hkv, self.D = batch, n_q_heads, n_kv_heads, head_dim
+        self.k_cache, self.v_cache, self.block_table = k_cache, v_cache, block_table
+        self.rope_base, self.rope_style, self.scale = rope_base, rope_style, scale
+        self.dtype, dev = k_cache.dtype, k_cache.device
+        code = rra.RRA_BF16 if self.dtype == torch.bfloat16 else rra.RRA_F32
+        if block_table is not None:
+            bs = k_cache.shape[1]
+            max_tokens = block_table.shape[1] * bs
+        else:
+            bs, max_tokens = 0, k_cache.shape[2]
+        self.splits = rra.rra_decode_num_splits(batch, n_q_heads, n_kv_heads, head_dim, max_tokens, bs,
+                                                num_splits, code)
+        self.num_splits = self.splits
+        ws = rra.rra_decode_workspace_bytes(batch, n_q_heads, head_dim, self.splits)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev) if ws else None
+        self.q_rot = torch.empty(batch, n_q_heads, head_dim, dtype=self.dtype, device=dev)
+        self.out = torch.empty(batch, n_q_heads, head_dim, dtype=self.dtype, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def rope_append(self, q, k_new, v_new, positions, stream=None) -> None:
+        rra.rra_rope_append(q, k_new, v_new, positions, self.q_rot, self.k_cache, self.v_cache, self.block_table,
+                            self.rope_base, self.rope_style, self.err, stream)
+
+    def attend(self, seq_lens, stream=None) -> torch.Tensor:
+        if self.block_table is None:
+            rra.rra_decode_attn_contig(self.q_rot, self.k_cache, self.v_cache, seq_lens, self.out, self.scale,
+                                       self.num_splits, self.workspace, self.err, stream)
+        else:
+            rra.rra_decode_attn_paged(self.q_rot, self.k_cache, self.v_cache, self.block_table, seq_lens, self.out,
+                                      self.scale, self.num_splits, self.workspace, self.err, stream)
+        return self.out
+
+    def __call__(self, q, k_new, v_new, positions, seq_lens, stream=None) -> torch.Tensor:
+        """Rotate, append, attend. ``seq_lens`` = positions + 1 for a plain decode step."""
+        self.rope_append(q, k_new, v_new, positions, stream)
+        return self.attend(seq_lens, stream)
+
+    def error_bits(self) -> int:
+        """Device error word (RRA_ERR_* bits) accumulated since the last reset; synchronises."""
+        return int(self.err.item())
+
+    def reset_errors(self) -> None:
+        self.err.zero_()

@@ -1,0 +1,130 @@
+"""Run one decode step through the C ABI and, separately, through the float64 oracle.
+
+The two sides share only the seeded inputs from ``workloads``: the GPU side gets
+torch device copies of the storage arrays; the oracle gets the same arrays on the host.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+import oracle
+from oracle import decode as odecode
+from workloads import DecodeInputs
+
+# Tolerances on the attention output (max abs error against the float64 oracle,
+# computed on the same stored inputs): 1e-4 for fp32 storage, 1e-2 for bf16 storage.
+OUT_ATOL = {"f32": 1e-4, "bf16": 1e-2}
+
+
+def to_torch(arr: np.ndarray, dtype: str, device) -> torch.Tensor:
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16)
+    elif dtype == "f32":
+        t = torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32))
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(arr))
+    return t.to(device)
+
+
+def to_numpy(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+@dataclasses.dataclass
+class GpuResult:
+    q_rot: np.ndarray
+    out: np.ndarray
+    k_cache: Optional[np.ndarray]
+    v_cache: Optional[np.ndarray]
+    err: int
+    splits: int
+
+
+def run_gpu(inp: DecodeInputs, num_splits: int = 0, rope_style: int = 0, device="cuda:0",
+            fetch_cache: bool = True, seq_lens: Optional[np.ndarray] = None) -> GpuResult:
+    from rope_gqa_paged_gb300 import DecodeStep
+
+    cfg = inp.cfg
+    dt = cfg.dtype
+    kc, vc = to_torch(inp.k_cache, dt, device), to_torch(inp.v_cache, dt, device)
+    table = to_torch(inp.block_table, "i32", device) if inp.block_table is not None else None
+    step = DecodeStep(cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, kc, vc, table,
+                      num_splits=num_splits or cfg.num_splits, rope_base=cfg.rope_base, rope_style=rope_style)
+    lens = inp.lengths if seq_lens is None else seq_lens
+    out = step(to_torch(inp.q, dt, device), to_torch(inp.k_new, dt, device), to_torch(inp.v_new, dt, device),
+               to_torch(inp.positions, "i32", device), to_torch(np.asarray(lens, dtype=np.int32), "i32", device))
+    torch.cuda.synchronize(device)
+    res = GpuResult(q_rot=to_numpy(step.q_rot), out=to_numpy(out),
+                    k_cache=to_numpy(kc) if fetch_cache else None, v_cache=to_numpy(vc) if fetch_cache else None,
+                    err=step.error_bits(), splits=step.splits)
+    del kc, vc, step
+    return res
+
+
+def run_oracle(inp: DecodeInputs, rope_style: int = 0, seq_lens=None):
+    """Whole-batch oracle on copies of the caches: (q_rot, k_cache, v_cache, out float64)."""
+    cfg = inp.cfg
+    bs = cfg.block_size if inp.block_table is not None else 0
+    return odecode.decode_step(inp.q, inp.k_new, inp.v_new, inp.positions, inp.k_cache, inp.v_cache, cfg.dtype,
+                               inp.block_table, bs, seq_lens=seq_lens, rope_base=cfg.rope_base,
+                               rope_style=rope_style)
+
+
+def oracle_for_sequences(inp: DecodeInputs, batches: Sequence[int], rope_style: int = 0):
+    """Oracle outputs for a few sequences of a (possibly huge) batch, one sequence at a time.
+
+    For each sequence b the logical K/V (L_b - 1 cached tokens) is gathered from the
+    input cache, the oracle appends the new token into a private one-sequence cache and
+    attends. Returns (q_rot rows, out rows float64), each [len(batches), Hq, D].
+    """
+    cfg = inp.cfg
+    bs = cfg.block_size if inp.block_table is not None else 0
+    q_rows, outs = [], []
+    for b in batches:
+        L = int(inp.lengths[b])
+        k = odecode.logical_kv(inp.k_cache, b, L, inp.block_table, bs)
+        v = odecode.logical_kv(inp.v_cache, b, L, inp.block_table, bs)
+        kc, vc = np.array(k)[None].copy(), np.array(v)[None].copy()       # [1, Hkv, L, D]
+        q_rot = odecode.rope_append(inp.q[b:b + 1], inp.k_new[b:b + 1], inp.v_new[b:b + 1],
+                                    inp.positions[b:b + 1], kc, vc, cfg.dtype, rope_base=cfg.rope_base,
+                                    rope_style=rope_style)
+        outs.append(odecode.decode_attention(q_rot, kc, vc, np.array([L]), cfg.dtype)[0])
+        q_rows.append(q_rot[0])
+    return np.stack(q_rows), np.stack(outs)
+
+
+def bf16_ulp_distance(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Distance in bf16 ulps between two arrays of bf16 bit patterns (sign-magnitude aware)."""
+    def ordered(x):
+        x = x.astype(np.int32)
+        return np.where(x & 0x8000, 0x8000 - x, x)  # negative values map below zero, -0 == +0
+    return np.abs(ordered(a) - ordered(b))
+
+
+def stored_to_f64(arr: np.ndarray, dtype: str) -> np.ndarray:
+    return oracle.storage_to_f64(arr, dtype)
+
+
+def assert_close_stored(got: np.ndarray, want: np.ndarray, dtype: str, what: str):
+    """Stored values (q_rot, appended k) agree within 1 bf16 ulp, or 4 fp32 ulps."""
+    if dtype == "bf16":
+        d = bf16_ulp_distance(got, want)
+        assert d.max() <= 1, f"{what}: {int(d.max())} bf16 ulps apart at {np.unravel_index(d.argmax(), d.shape)}"
+    else:
+        g, w = got.astype(np.float64), want.astype(np.float64)
+        tol = 4 * np.spacing(np.abs(w).astype(np.float32)).astype(np.float64)
+        assert np.all(np.abs(g - w) <= tol), f"{what}: max diff {np.abs(g - w).max()}"
+
+
+def out_error(got_stored: np.ndarray, want_f64: np.ndarray, dtype: str) -> float:
+    g = stored_to_f64(got_stored, dtype)
+    assert np.all(np.isfinite(g)), "non-finite attention output"
+    return float(np.abs(g - want_f64).max())

@@ -1,0 +1,104 @@
+"""The C-ABI library on the host: it builds, loads, exports every declared symbol, and its
+host-only functions and argument checks behave as documented (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from rope_gqa_paged_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+RRA_OK, RRA_EINVAL, RRA_EUNSUPPORTED, RRA_ERANGE, RRA_EWORKSPACE, RRA_ECUDA = 0, -1, -2, -3, -4, -5
+
+
+@pytest.fixture(scope="module")
+def rra():
+    _build.build()
+    from rope_gqa_paged_gb300 import rra as binding
+    return binding
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "rra.h"), encoding="utf-8").read()
+    return sorted(set(re.findall(r"RRA_API\s+[\w\s\*]+?\b(rra_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = _declared_symbols()
+    for name in ("rra_rope_append", "rra_decode_attn_contig", "rra_decode_attn_paged", "rra_kv_bytes"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(rra):
+    lib = ctypes.CDLL(_build.LIB_PATH)
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+    exported = set(re.findall(r" T (rra_\w+)", os.popen(f"nm -D --defined-only {_build.LIB_PATH}").read()))
+    assert exported == set(_declared_symbols())
+
+
+def test_kv_bytes_matches_oracle_and_pages(rra):
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        args = [int(x) for x in rng.integers(0, 300, size=6)]
+        args[3] = int(rng.integers(0, 1 << 20))
+        assert rra.rra_kv_bytes(*args) == oracle.kv_cache_bytes(*args)
+    assert rra.rra_kv_bytes(32, 32, 128, 1024, 1, 2) == 536870912            # 0.5 GB
+    assert rra.rra_kv_bytes(32, 32, 128, 131072, 1, 2) == 64 * 2 ** 30       # 64 GB
+    assert rra.rra_kv_bytes(-1, 8, 128, 10, 1, 2) == 0
+    assert rra.rra_kv_bytes(1 << 30, 1 << 30, 1 << 30, 1 << 30, 1, 2) == 0  # overflow
+
+
+def test_workspace_bytes(rra):
+    assert rra.rra_decode_workspace_bytes(64, 32, 128, 1) == 0
+    b = rra.rra_decode_workspace_bytes(1, 32, 128, 128)
+    assert b >= 32 * 128 * (128 + 2) * 4
+    assert rra.rra_decode_workspace_bytes(2, 32, 128, 128) > b
+
+
+def test_num_splits_planning(rra):
+    S = rra.rra_decode_num_splits
+    assert S(1, 32, 8, 128, 131072, 32, 128, rra.RRA_BF16) == 128              # explicit split count honoured
+    assert S(1, 4, 2, 64, 128, 0, 0, rra.RRA_F32) == 1                         # tiny case: one split
+    assert S(4, 32, 8, 128, 8192, 0, 1, rra.RRA_BF16) == 1
+    # a paged split holds at most 2047 block ids: block size 1 forces more splits than asked
+    assert S(1, 8, 8, 128, 65536, 1, 1, rra.RRA_BF16) > 1
+    for bad, status in (((1, 6, 4, 128, 64, 0, 0, 1), RRA_EINVAL), ((1, 8, 8, 96, 64, 0, 0, 1), RRA_EUNSUPPORTED),
+                        ((1, 8, 8, 128, 64, 12, 0, 1), RRA_EUNSUPPORTED), ((1, 8, 8, 128, 64, 0, 0, 7), RRA_EUNSUPPORTED),
+                        ((70000, 8, 8, 128, 64, 0, 0, 1), RRA_ERANGE), ((1, 8, 8, 128, 64, 0, -1, 1), RRA_EINVAL)):
+        assert rra.lib().rra_decode_num_splits(*bad) == status, bad
+
+
+def test_status_strings(rra):
+    for s in (RRA_OK, RRA_EINVAL, RRA_EUNSUPPORTED, RRA_ERANGE, RRA_EWORKSPACE, RRA_ECUDA):
+        assert rra.rra_status_str(s) not in ("", "unknown status")
+    assert rra.rra_status_str(42) == "unknown status"
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-only argument checks; never given fake pointers on a GPU")
+def test_argument_checks_reject_before_any_launch(rra):
+    lib = rra.lib()
+    P = 4096                                                                   # never dereferenced: checks fail first
+    # decode contig: Hq % Hkv != 0, unsupported D, null pointer, misaligned pointer, missing workspace
+    c = lib.rra_decode_attn_contig
+    assert c(P, P, P, P, P, 1, 6, 4, 128, 64, 0.0, 0, None, 0, 1, None, None) == RRA_EINVAL
+    assert c(P, P, P, P, P, 1, 8, 8, 96, 64, 0.0, 0, None, 0, 1, None, None) == RRA_EUNSUPPORTED
+    assert c(P, None, P, P, P, 1, 8, 8, 128, 64, 0.0, 0, None, 0, 1, None, None) == RRA_EINVAL
+    assert c(P + 8, P, P, P, P, 1, 8, 8, 128, 64, 0.0, 0, None, 0, 1, None, None) == RRA_EINVAL
+    assert c(P, P, P, P, P, 1, 8, 8, 128, 4096, 0.0, 8, None, 0, 1, None, None) == RRA_EWORKSPACE
+    assert c(P, P, P, P, P, 0, 8, 8, 128, 64, 0.0, 0, None, 0, 1, None, None) == RRA_OK   # empty batch: no-op
+    # decode paged: block size not a power of two, missing table
+    p = lib.rra_decode_attn_paged
+    assert p(P, P, P, P, 4, P, 12, 10, P, 1, 8, 8, 128, 0.0, 0, None, 0, 1, None, None) == RRA_EUNSUPPORTED
+    assert p(P, P, P, None, 4, P, 16, 10, P, 1, 8, 8, 128, 0.0, 0, None, 0, 1, None, None) == RRA_EINVAL
+    # rope append: bad style, bad base, Hq % Hkv
+    r = lib.rra_rope_append
+    assert r(P, P, P, P, P, P, P, None, 0, 0, 0, 64, 1, 8, 8, 128, 10000.0, 2, 1, None, None) == RRA_EINVAL
+    assert r(P, P, P, P, P, P, P, None, 0, 0, 0, 64, 1, 8, 8, 128, 0.5, 0, 1, None, None) == RRA_EINVAL
+    assert r(P, P, P, P, P, P, P, None, 0, 0, 0, 64, 1, 6, 4, 128, 10000.0, 0, 1, None, None) == RRA_EINVAL
+    assert r(P, P, P, P, P, P, P, None, 0, 0, 0, 64, 0, 8, 8, 128, 10000.0, 0, 1, None, None) == RRA_OK

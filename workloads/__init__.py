@@ -9,4 +9,4 @@ tests and the CUDA path can take their inputs from it without sharing code.
 """
 
 from .configs import CONFIGS, WorkloadConfig, get_config, reduced  # noqa: F401
-from .gen import DecodeInputs, make_inputs, bf16_bits_from_f32  # noqa: F401
+from .gen import DecodeInputs, make_inputs, make_structure, bf16_bits_from_f32  # noqa: F401

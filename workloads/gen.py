@@ -124,6 +124,18 @@ def make_inputs(cfg: WorkloadConfig, seed: Optional[int] = None, poison: bool = 
     return inp
 
 
+def make_structure(cfg: WorkloadConfig, seed: Optional[int] = None):
+    """Only the first two draws of the recipe: (lengths, block_table or None).
+
+    Same values as ``make_inputs`` gives for the same seed; used where the large cache
+    arrays are filled elsewhere (the benchmark fills them on the device).
+    """
+    rng = np.random.Generator(np.random.PCG64(cfg.seed if seed is None else seed))
+    lengths = draw_lengths(cfg, rng)
+    table = draw_block_table(cfg, lengths, rng) if cfg.layout == "paged" else None
+    return lengths, table
+
+
 def poison_unread(inp: DecodeInputs) -> None:
     """Write NaN into every cache slot the step must not read before its append."""
     cfg, nan = inp.cfg, inp.nan_value
