@@ -163,6 +163,34 @@ RRA_API const char* rra_status_str(int status);
 /* Text of the last CUDA error an entry point saw on this thread ("" if none). */
 RRA_API const char* rra_last_cuda_error(void);
 
+/* --- Decode without a caller workspace (the pages have no counterpart: this exists for
+ *     callers that must not allocate device memory when they run a step) ---
+ *
+ * rra_decode_attn_paged_noalloc is rra_decode_attn_paged with the split-K scratch taken
+ * from a fixed array inside the library instead of a caller workspace. It is meant for
+ * callers that cannot call cudaMalloc when they decode: code with no allocator of its own
+ * because a host framework owns all device memory, and loops that forbid allocation after
+ * start-up because allocating can block, fail or fragment memory mid-run. It allocates
+ * nothing and calls no allocating routine.
+ *   - The array holds rra_noalloc_scratch_bytes() (16 MiB) on every GPU that loads the
+ *     library, kept until the process exits. A step whose effective split count needs more
+ *     (rra_decode_workspace_bytes) returns RRA_EWORKSPACE before anything is launched;
+ *     ask for fewer splits then.
+ *   - All calls on a device share the array: calls whose kernels overlap on the GPU race
+ *     and give wrong results. Keep them on one stream or serialise them.
+ *   - Nothing needs clearing between calls; each call writes all the scratch it reads.
+ *   - The first call on each device (with that device current) looks up the array's
+ *     device address; make that first call before any stream capture starts.
+ * Arguments as in rra_decode_attn_paged, without workspace and ws_bytes. */
+RRA_API int rra_decode_attn_paged_noalloc(const void* q_rot, const void* k_pool, const void* v_pool,
+                                          const int32_t* block_table, int max_blocks_per_seq,
+                                          const int32_t* seq_lens, int block_size, int num_blocks,
+                                          void* out, int B, int Hq, int Hkv, int D, float scale,
+                                          int num_splits, rra_dtype dt, int32_t* err_flag, void* stream);
+
+/* Bytes of the fixed scratch array rra_decode_attn_paged_noalloc uses (16 MiB). */
+RRA_API size_t rra_noalloc_scratch_bytes(void);
+
 #ifdef __cplusplus
 }
 #endif

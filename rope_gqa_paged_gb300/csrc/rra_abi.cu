@@ -218,6 +218,10 @@ int finish_decode(const rra::DecodeArgs& a, rra_dtype dt, cudaError_t e, cudaStr
 
 }  // namespace
 
+namespace rra {
+void record_cuda_error(cudaError_t e, const char* where) { cuda_fail(e, where); }
+}  // namespace rra
+
 extern "C" {
 
 const char* rra_status_str(int status) {

@@ -57,6 +57,9 @@ inline int decode_tile_tokens(int D, int elem_bytes) { return 8192 / (D * elem_b
 // Most block-table entries one split may need (bounds the per-CTA table copy).
 constexpr int kMaxTableEntries = 2048;
 
+// Stores the text rra_last_cuda_error() returns on this thread.
+void record_cuda_error(cudaError_t e, const char* where);
+
 cudaError_t launch_rope_append(const RopeArgs& a, rra_dtype dt, cudaStream_t stream);
 // Tokens per stage of the tensor-core (bf16) decode kernel: K + V tiles of 32 KB.
 inline int decode_mma_tile_tokens(int D) { return 16384 / (D * 2); }
