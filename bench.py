@@ -59,6 +59,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="bounded CPU oracle sample (seconds)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-graph", action="store_true", help="time eager launches instead of a captured step")
     p.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     return p.parse_args(argv)
 
@@ -246,26 +247,22 @@ def run_ours(args):
         flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
-    def one_step():
-        step.rope_append(w["q"], w["k_new"], w["v_new"], w["positions"])
-        return step
-
     for _ in range(max(args.warmup, 3)):
         step(w["q"], w["k_new"], w["v_new"], w["positions"], w["seq_lens"])
     torch.cuda.synchronize(device)
     step.reset_errors()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
     except Exception:
         pass
-    sampler = ClockSampler(uuid)
+
+    # (1) per-kernel times: eager launches with events between the two library calls
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     barrier(world)
     torch.cuda.synchronize(device)
-    sampler.start()
     for i in range(K):
         if flush is not None:
             flush.fill_(i & 0xFF)
@@ -275,19 +272,43 @@ def run_ours(args):
         step.attend(w["seq_lens"])
         ev[i][2].record(stream)
     torch.cuda.synchronize(device)
-    barrier(world)
-    clocks = sampler.stop()
-    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(K)]
     rope_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    ms_local = sum(step_ms) / K
+    eager_ms = sum(ev[i][0].elapsed_time(ev[i][2]) for i in range(K)) / K
+
+    # (2) the step: one captured graph of both calls, replayed K times (eager if capture fails)
+    graph_note = "eager launches"
+    if not args.no_graph:
+        try:
+            step.capture(w["q"], w["k_new"], w["v_new"], w["positions"], w["seq_lens"])
+            graph_note = "CUDA graph of the step, replayed"
+        except Exception as e:  # capture is an optimisation; report how the step was timed
+            step.graph = None
+            graph_note = f"eager launches (graph capture failed: {type(e).__name__})"
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    sampler = ClockSampler(uuid)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    sampler.start()
+    for i in range(K):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        sev[i][0].record(stream)
+        if step.graph is not None:
+            step.replay()
+        else:
+            step(w["q"], w["k_new"], w["v_new"], w["positions"], w["seq_lens"])
+        sev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    clocks = sampler.stop()
+    ms_local = sum(sev[i][0].elapsed_time(sev[i][1]) for i in range(K)) / K
     err_bits = step.error_bits()
 
-    # end to end through the public API: pinned host inputs in, host output back, every step
+    # (3) end to end through the public API: pinned host inputs in, host output back, every step
     e2e = None
     if not args.no_e2e:
         host = {k: w[k].cpu().pin_memory() for k in ("q", "k_new", "v_new", "positions", "seq_lens")}
-        dev_in = {k: torch.empty_like(w[k]) for k in host}
         out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = out_host.numel() * out_host.element_size()
@@ -298,9 +319,10 @@ def run_ours(args):
             if flush is not None:
                 flush.fill_(i & 0xFF)
             e_ev[i][0].record(stream)
-            for k in host:
-                dev_in[k].copy_(host[k], non_blocking=True)
-            out = step(dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["positions"], dev_in["seq_lens"])
+            for k in host:                               # the captured step reads these buffers
+                w[k].copy_(host[k], non_blocking=True)
+            out = step.replay() if step.graph is not None else step(
+                w["q"], w["k_new"], w["v_new"], w["positions"], w["seq_lens"])
             out_host.copy_(out, non_blocking=True)
             e_ev[i][1].record(stream)
         torch.cuda.synchronize(device)
@@ -335,7 +357,9 @@ def run_ours(args):
         "decode_steps_per_s_per_layer": round(1e3 / ms, 2),
         "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / peak, 2),
-        "kernel_ms": {"rope_append": round(sum(rope_ms) / K, 5), "decode_attn": round(dec_avg, 5)},
+        "kernel_ms": {"rope_append": round(sum(rope_ms) / K, 5), "decode_attn": round(dec_avg, 5),
+                      "eager_step": round(eager_ms, 5)},
+        "step_timing": graph_note,
         "roofline": {"kernel": "decode_split_kernel + split merge (one rra_decode_attn_* call)", "bound": "hbm",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",

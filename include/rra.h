@@ -65,7 +65,8 @@ enum {
   RRA_ERR_POSITION = 1,   /* positions[b] < 0 or >= cache capacity: that sequence was not written */
   RRA_ERR_BLOCK_ID = 2,   /* a block-table entry outside [0, num_blocks): block 0 was used instead */
   RRA_ERR_SEQ_LEN = 4,    /* seq_lens[b] < 0 or > capacity: clamped into [0, capacity] */
-  RRA_ERR_TIMEOUT = 8     /* an in-kernel pipeline wait gave up (~1 s): results are invalid */
+  RRA_ERR_TIMEOUT = 8,    /* an in-kernel pipeline wait gave up (~1 s): results are invalid */
+  RRA_ERR_WORKSPACE = 16  /* the workspace's split counters were not zero: results are invalid */
 };
 
 /* Steps 1-2: RoPE on q and k_new at positions[b], then append rotated k and raw v.
@@ -113,9 +114,12 @@ RRA_API int rra_rope_append(const void* q, const void* k_new, const void* v_new,
  *               rra_decode_num_splits(); with more than one split the partial results
  *               go to `workspace` and a second kernel merges them.
  *   workspace, ws_bytes  device scratch of at least rra_decode_workspace_bytes() bytes
- *               (may be NULL when that is 0); contents need no initialisation.
+ *               (may be NULL when that is 0). It must be zero-filled before its first use;
+ *               every call leaves it ready for the next one (its split counters back at
+ *               zero). Calls sharing a workspace must not overlap on the GPU.
  * Softmax runs online in float32 per split (running max, running sum, rescaled
- * accumulator) and the splits merge by log-sum-exp; the result equals the plain
+ * accumulator); each split publishes its partial and the last split of a sequence to
+ * finish merges them by log-sum-exp in the same kernel. The result equals the plain
  * two-pass softmax up to float32 rounding.
  */
 RRA_API int rra_decode_attn_contig(const void* q_rot, const void* k_cache, const void* v_cache,
@@ -163,6 +167,11 @@ RRA_API const char* rra_status_str(int status);
 /* Text of the last CUDA error an entry point saw on this thread ("" if none). */
 RRA_API const char* rra_last_cuda_error(void);
 
+/* The library links its own copy of the CUDA runtime, whose current device is separate
+ * from the caller's: every entry point launches on the device selected here for the
+ * calling thread (device 0 until set), and `stream` must belong to that device. */
+RRA_API int rra_use_device(int device);
+
 /* --- Decode without a caller workspace (the pages have no counterpart: this exists for
  *     callers that must not allocate device memory when they run a step) ---
  *
@@ -178,7 +187,8 @@ RRA_API const char* rra_last_cuda_error(void);
  *     ask for fewer splits then.
  *   - All calls on a device share the array: calls whose kernels overlap on the GPU race
  *     and give wrong results. Keep them on one stream or serialise them.
- *   - Nothing needs clearing between calls; each call writes all the scratch it reads.
+ *   - Its split counters must start at zero: the array starts zeroed when the library is
+ *     loaded and every call leaves the counters at zero again.
  *   - The first call on each device (with that device current) looks up the array's
  *     device address; make that first call before any stream capture starts.
  * Arguments as in rra_decode_attn_paged, without workspace and ws_bytes. */

@@ -19,8 +19,9 @@
 //     q (pre-scaled by scale*log2 e), its slice of the output accumulator, and the running
 //     max / sum of its own token subsequence (online softmax in base 2, float32).
 //     Every K row is read from shared memory once and used by all HPC heads.
-//   * end: the 16 token groups merge through shared memory; one split writes the final
-//     row, several splits write (unnormalised o, max, sum) for decode_reduce_kernel.
+//   * end: the 16 token groups merge through shared memory; a sequence with one split
+//     writes its final row, otherwise each split publishes (unnormalised o, max, sum) and
+//     the last split to finish merges them (finish_split).
 // Every wait has a time limit; a wait that runs out sets RRA_ERR_TIMEOUT and the CTA
 // finishes without blocking.
 #pragma once
@@ -140,6 +141,131 @@ __device__ __forceinline__ void consume_stage(ConsumerState<T, D, HPC>& st, cons
   }
 }
 
+// ---- split-K completion ----------------------------------------------------------
+// A partial (for one query head) is an unnormalised output o[D] with its running max m
+// (log2 units) and running sum l. Merging partials i: M = max m_i, w_i = 2^(m_i - M),
+// o = sum w_i o_i, l = sum w_i l_i; the final row is o / l.
+
+// Counts this CTA's arrival at `cnt` (all `nthreads` consumer threads call it after their
+// last write). True in the CTA whose arrival brings the count to `target`; that CTA also puts
+// the counter back to zero, ready for the next call. No CTA ever waits for another.
+__device__ __forceinline__ bool arrive_last(int* cnt, int target, int* s_flag, int32_t* err, int tid,
+                                            int nthreads) {
+  __threadfence();  // this thread's writes are visible device-wide before the arrival
+  named_barrier_sync(1, nthreads);
+  if (tid == 0) {
+    const int arrived = atomicAdd(cnt, 1) + 1;
+    int last = 0;
+    if (arrived == target) {
+      last = 1;
+      atomicExch(cnt, 0);
+    } else if (arrived > target) {  // the workspace did not start zeroed: results are invalid
+      flag_error(err, RRA_ERR_WORKSPACE);
+      atomicExch(cnt, 0);
+    }
+    *s_flag = last;
+  }
+  named_barrier_sync(1, nthreads);
+  const bool last = *s_flag != 0;
+  if (last) __threadfence();  // see the partials of every CTA that arrived before
+  return last;
+}
+
+// Merges partials first .. first+count-1 of heads h0 .. h0+hpc-1 (rows row0 + h of a
+// [rows][stride] partial array) into the final output rows (dst_o == nullptr) or into one
+// partial at index dst_idx of a [rows][dst_stride] partial array.
+template <typename T, int D>
+__device__ void merge_partials(const DecodeArgs& a, const float* src_o, const float* src_ml, int stride, int first,
+                               int count, int hpc, size_t row0, float* dst_o, float* dst_ml, int dst_stride,
+                               int dst_idx, float* scratch, int tid, int nthreads) {
+  float* sm_w = scratch;                  // [hpc][count]: m_i, then the weights
+  float* sm_l = scratch + hpc * count;    // [hpc][count]
+  float* sm_ml = sm_l + hpc * count;      // [hpc][2]: merged (M, l)
+  for (int i = tid; i < hpc * count; i += nthreads) {
+    const int h = i / count, k = i - h * count;
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(src_ml) + (row0 + h) * stride + first + k);
+    sm_w[i] = ml.x;
+    sm_l[i] = ml.y;
+  }
+  named_barrier_sync(1, nthreads);
+  const bool final_row = dst_o == nullptr;
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int h = warp; h < hpc; h += nthreads >> 5) {
+    float M = -INFINITY;
+    for (int k = lane; k < count; k += 32) M = fmaxf(M, sm_w[h * count + k]);
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+    float ls = 0.f;
+    if (M != -INFINITY)
+      for (int k = lane; k < count; k += 32) ls = fmaf(exp2f(sm_w[h * count + k] - M), sm_l[h * count + k], ls);
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, x);
+    const float scale = final_row ? (ls > 0.f ? 1.f / ls : 0.f) : 1.f;
+    __syncwarp();
+    for (int k = lane; k < count; k += 32)
+      sm_w[h * count + k] = M != -INFINITY ? exp2f(sm_w[h * count + k] - M) * scale : 0.f;
+    if (lane == 0) {
+      sm_ml[2 * h] = M;
+      sm_ml[2 * h + 1] = ls;
+    }
+  }
+  named_barrier_sync(1, nthreads);
+  constexpr int kQ = D / 4;
+  for (int i = tid; i < hpc * kQ; i += nthreads) {
+    const int h = i / kQ, d = (i - h * kQ) * 4;
+    const float4* o = reinterpret_cast<const float4*>(src_o + ((row0 + h) * stride + first) * D + d);
+    const float* wts = sm_w + h * count;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int k = 0; k < count; ++k) {
+      const float wv = wts[k];
+      const float4 v = __ldcg(o + static_cast<size_t>(k) * kQ);
+      acc.x = fmaf(wv, v.x, acc.x);
+      acc.y = fmaf(wv, v.y, acc.y);
+      acc.z = fmaf(wv, v.z, acc.z);
+      acc.w = fmaf(wv, v.w, acc.w);
+    }
+    if (final_row) {
+      T* out = static_cast<T*>(a.out) + (row0 + h) * D + d;
+      Elem<T>::store(out, acc.x);
+      Elem<T>::store(out + 1, acc.y);
+      Elem<T>::store(out + 2, acc.z);
+      Elem<T>::store(out + 3, acc.w);
+    } else {
+      const size_t pd = (row0 + h) * dst_stride + dst_idx;
+      *reinterpret_cast<float4*>(dst_o + pd * D + d) = acc;
+      if (d == 0) *reinterpret_cast<float2*>(dst_ml + 2 * pd) = make_float2(sm_ml[2 * h], sm_ml[2 * h + 1]);
+    }
+  }
+}
+
+// Run by all consumer threads of a CTA after each has written its share of this split's
+// partial (index `split` of the [rows][num_splits] partial arrays). With n <= kMergeFanIn
+// splits, the last split to arrive merges them all into the output. With more, splits form
+// groups of kMergeFanIn: the last arrival of each group merges the group into a level-2
+// partial, and the last group to finish merges the level-2 partials into the output, so no
+// single CTA has to read every split at the end of the kernel.
+template <typename T, int D>
+__device__ __forceinline__ void finish_split(const DecodeArgs& a, int b, int h0, int hpc, int split, int n,
+                                             float* scratch, int* s_flag, int tid, int nthreads) {
+  const size_t row0 = static_cast<size_t>(b) * a.Hq + h0;
+  const int S = a.num_splits, G = a.num_groups;
+  if (n <= kMergeFanIn) {
+    if (arrive_last(a.counters + row0, n, s_flag, a.err, tid, nthreads))
+      merge_partials<T, D>(a, a.ws_o, a.ws_ml, S, 0, n, hpc, row0, nullptr, nullptr, 0, 0, scratch, tid, nthreads);
+    return;
+  }
+  const int grp = split / kMergeFanIn, first = grp * kMergeFanIn;
+  const int gsize = min(kMergeFanIn, n - first);
+  if (!arrive_last(a.group_counters + row0 * G + grp, gsize, s_flag, a.err, tid, nthreads)) return;
+  merge_partials<T, D>(a, a.ws_o, a.ws_ml, S, first, gsize, hpc, row0, a.ws2_o, a.ws2_ml, G, grp, scratch, tid,
+                       nthreads);
+  const int groups = (n + kMergeFanIn - 1) / kMergeFanIn;
+  if (arrive_last(a.counters + row0, groups, s_flag, a.err, tid, nthreads))
+    merge_partials<T, D>(a, a.ws2_o, a.ws2_ml, G, 0, groups, hpc, row0, nullptr, nullptr, 0, 0, scratch, tid,
+                         nthreads);
+}
+
 template <typename T, int D, int HPC, bool PAGED>
 __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 2)
     decode_split_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
@@ -160,8 +286,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 2)
     L = min(max(L, 0), a.capacity);
   }
   const int start = split * a.chunk;
+  const int n_work = (L + a.chunk - 1) / a.chunk;  // splits of this sequence that hold tokens
   if (start >= L) {
-    if (L == 0 && a.num_splits == 1) {  // nothing to attend to: a zero row
+    if (L == 0 && split == 0) {  // nothing to attend to: a zero row
       T* out = static_cast<T*>(a.out) + (static_cast<size_t>(b) * a.Hq + h0) * D;
       for (int i = threadIdx.x; i < HPC * D; i += blockDim.x) Elem<T>::store(out + i, 0.f);
     }
@@ -328,7 +455,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 2)
       }
     }
     const size_t bh = static_cast<size_t>(b) * a.Hq + h0 + h;
-    if (a.num_splits == 1) {
+    if (n_work == 1) {
       Elem<T>::store(static_cast<T*>(a.out) + bh * D + d, lsum > 0.f ? osum / lsum : 0.f);
     } else {
       const size_t ps = bh * a.num_splits + split;
@@ -339,60 +466,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 2)
       }
     }
   }
-}
-
-// Merge the splits of one (sequence, query head): M = max_s m_s, w_s = 2^(m_s - M),
-// out = sum_s w_s o_s / sum_s w_s l_s. One warp per (sequence, head), each lane owning
-// D/32 consecutive dims; only the splits that held tokens are read.
-constexpr int kReduceWarps = 4;
-
-template <typename T, int D>
-__global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const DecodeArgs a) {
-  constexpr int kDL = D / 32;  // dims per lane
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kReduceWarps + (threadIdx.x >> 5);  // b * Hq + hq
-  if (row >= a.B * a.Hq) return;
-  const int b = row / a.Hq;
-  const int L = min(max(a.seq_lens[b], 0), a.capacity);
-  const int n = (L + a.chunk - 1) / a.chunk;
-  const float* ml = a.ws_ml + static_cast<size_t>(row) * a.num_splits * 2;
-  const float* o = a.ws_o + static_cast<size_t>(row) * a.num_splits * D + lane * kDL;
-
-  float M = -INFINITY;
-  for (int s = lane; s < n; s += 32) M = fmaxf(M, ml[2 * s]);
-#pragma unroll
-  for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
-
-  float lsum = 0.f, acc[kDL];
-#pragma unroll
-  for (int e = 0; e < kDL; ++e) acc[e] = 0.f;
-  for (int s0 = 0; s0 < n; s0 += 32) {
-    const int s = s0 + lane;
-    const float w = s < n ? exp2f(ml[2 * s] - M) : 0.f;
-    lsum = fmaf(w, s < n ? ml[2 * s + 1] : 0.f, lsum);
-    const int cnt = min(32, n - s0);
-    for (int k = 0; k < cnt; ++k) {
-      const float wk = __shfl_sync(0xffffffffu, w, k);
-      const float* os = o + static_cast<size_t>(s0 + k) * D;
-      if constexpr (kDL == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(os);
-        acc[0] = fmaf(wk, v.x, acc[0]);
-        acc[1] = fmaf(wk, v.y, acc[1]);
-        acc[2] = fmaf(wk, v.z, acc[2]);
-        acc[3] = fmaf(wk, v.w, acc[3]);
-      } else {
-        const float2 v = *reinterpret_cast<const float2*>(os);
-        acc[0] = fmaf(wk, v.x, acc[0]);
-        acc[1] = fmaf(wk, v.y, acc[1]);
-      }
-    }
+  if (n_work > 1) {
+    __shared__ int s_last;
+    finish_split<T, D>(a, b, h0, HPC, split, n_work, reinterpret_cast<float*>(smem), &s_last, threadIdx.x,
+                       kConsumers);
   }
-#pragma unroll
-  for (int x = 16; x > 0; x >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, x);
-  const float inv = (n > 0 && lsum > 0.f) ? 1.f / lsum : 0.f;
-  T* out = static_cast<T*>(a.out) + static_cast<size_t>(row) * D + lane * kDL;
-#pragma unroll
-  for (int e = 0; e < kDL; ++e) Elem<T>::store(out + e, acc[e] * inv);
 }
 
 template <typename T, int D, int HPC, bool PAGED>

@@ -15,21 +15,32 @@
 //
 // Data path: the producer warp streams K and V tiles with 4-D (paged pool) or 3-D
 // (contiguous cache) TMA tensor copies using the 128-byte swizzle, in 64-dim halves, into a
-// 3-stage ring; each consumer warp reads its 16-token slices with ldmatrix (K as the A
+// 2-stage ring (three CTAs per SM); each consumer warp reads its 16-token slices with ldmatrix (K as the A
 // operand, V through ldmatrix.trans as V^T), conflict-free thanks to the swizzle.
 #pragma once
 
+#include "decode_kernels.cuh"
 #include "rra_device.cuh"
 #include "rra_internal.h"
 
 namespace rra {
+
+// Two 32 KB stages per CTA and three CTAs per SM (registers <= 136, ~68 KB shared memory
+// each): measured faster on GB300 than three stages at two CTAs per SM, because more CTAs
+// per SM overlap one CTA's start-up and epilogue with the others' streaming.
+#ifndef RRA_MMA_STAGES
+#define RRA_MMA_STAGES 2
+#endif
+#ifndef RRA_MMA_CTAS_PER_SM
+#define RRA_MMA_CTAS_PER_SM 3
+#endif
 
 template <int D>
 struct MmaCfg {
   static constexpr int kRowBytes = D * 2;                 // bf16
   static constexpr int kHalves = D / 64;                  // 128-byte swizzle spans per row
   static constexpr int kTile = 16384 / kRowBytes;         // tokens per stage (K 16 KB + V 16 KB)
-  static constexpr int kStages = 3;
+  static constexpr int kStages = RRA_MMA_STAGES;
   static constexpr int kConsumerWarps = 4;
   static constexpr int kThreads = (kConsumerWarps + 1) * 32;
   static constexpr int kWarpTokens = kTile / kConsumerWarps;
@@ -37,7 +48,7 @@ struct MmaCfg {
   static constexpr int kHalfBytes = kTile * 128;          // one 64-dim half of K or V of a stage
   static constexpr int kStageBytes = 2 * kHalves * kHalfBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kSmemBytes = 1024 + kRingBytes + 2 * kStages * 8 + kMaxTableEntries * 4;
+  static constexpr int kSmemBytes = 1024 + kRingBytes + 2 * kStages * 8 + kMmaTableEntries * 4;
   static constexpr int kMaxHeads = 8;
   static constexpr int kKSteps = D / 16;
 };
@@ -185,7 +196,7 @@ __device__ __forceinline__ void mma_step(MmaWarpState<D>& st, const uint32_t (&q
 }
 
 template <int D, bool PAGED>
-__global__ void __launch_bounds__(MmaCfg<D>::kThreads, 2)
+__global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     decode_mma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                       const DecodeArgs a) {
   using C = MmaCfg<D>;
@@ -206,8 +217,9 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 2)
     L = min(max(L, 0), a.capacity);
   }
   const int start = split * a.chunk;
+  const int n_work = (L + a.chunk - 1) / a.chunk;  // splits of this sequence that hold tokens
   if (start >= L) {
-    if (L == 0 && a.num_splits == 1) {
+    if (L == 0 && split == 0) {
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(b) * a.Hq + h0) * D;
       for (int i = threadIdx.x; i < hpc * D; i += blockDim.x) out[i] = __float2bfloat16_rn(0.f);
     }
@@ -389,7 +401,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 2)
       }
     }
     const size_t bh = static_cast<size_t>(b) * a.Hq + h0 + h;
-    if (a.num_splits == 1) {
+    if (n_work == 1) {
       static_cast<__nv_bfloat16*>(a.out)[bh * D + d] = __float2bfloat16_rn(lsum > 0.f ? osum / lsum : 0.f);
     } else {
       const size_t ps = bh * a.num_splits + split;
@@ -399,6 +411,11 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 2)
         a.ws_ml[2 * ps + 1] = lsum;
       }
     }
+  }
+  if (n_work > 1) {
+    __shared__ int s_last;
+    finish_split<__nv_bfloat16, D>(a, b, h0, hpc, split, n_work, reinterpret_cast<float*>(smem), &s_last,
+                                   threadIdx.x, kConsumers);
   }
 }
 

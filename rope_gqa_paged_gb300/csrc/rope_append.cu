@@ -37,11 +37,36 @@ __device__ __forceinline__ float rotate_diff(float a, float b, float ch, float c
 
 template <typename T>
 __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArgs a) {
-  __shared__ float cs[4][kPairsPerCta];  // cos hi, cos lo, sin hi, sin lo
+  constexpr int kRows = kRopeThreads / kPairsPerCta;  // head rows handled side by side
+  constexpr int kUnroll = 8;                          // head rows per thread loaded before any math
+  __shared__ float cs[4][kPairsPerCta];               // cos hi, cos lo, sin hi, sin lo
+  __shared__ size_t row_info[2];                      // cache row of KV head 0, stride between heads
+  __shared__ int append_ok;
   const int b = blockIdx.x;
   const int D = a.D, half = a.D / 2;
   const int i0 = blockIdx.y * kPairsPerCta;
   const int np = min(kPairsPerCta, half - i0);
+  const int heads = a.Hq + a.Hkv;
+  const bool inter = a.rope_style == 1;
+  const int j = threadIdx.x % kPairsPerCta;
+  const int ia = inter ? 2 * (i0 + j) : i0 + j;
+  const int ib = inter ? 2 * (i0 + j) + 1 : i0 + j + half;
+
+  auto src_row = [&](int hh) -> const T* {
+    return hh < a.Hq ? static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + hh) * D
+                     : static_cast<const T*>(a.k_new) + (static_cast<size_t>(b) * a.Hkv + hh - a.Hq) * D;
+  };
+  // The first kUnroll rows of q / k_new are loaded before the position is even known.
+  float xa[kUnroll], xb[kUnroll];
+#pragma unroll
+  for (int r = 0; r < kUnroll; ++r) {
+    const int hh = threadIdx.x / kPairsPerCta + kRows * r;
+    if (hh < heads && j < np) {
+      xa[r] = Elem<T>::load(src_row(hh) + ia);
+      xb[r] = Elem<T>::load(src_row(hh) + ib);
+    }
+  }
+
   const int pos = a.positions[b];
   const bool paged = a.block_table != nullptr;
   const long long cap = paged ? (static_cast<long long>(a.max_blocks_per_seq) << a.log2_bs) : a.max_len;
@@ -50,56 +75,59 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
     return;
   }
   if (threadIdx.x < np) {
-    double s, c;  // angle / pi = pos * (theta_i / pi): sincospi reduces its argument exactly
-    sincospi(static_cast<double>(pos) * a.inv_freq[i0 + threadIdx.x], &s, &c);
-    const float ch = static_cast<float>(c), sh = static_cast<float>(s);
+    double sn, cn;  // angle / pi = pos * (theta_i / pi): sincospi reduces its argument exactly
+    sincospi(static_cast<double>(pos) * a.inv_freq[i0 + threadIdx.x], &sn, &cn);
+    const float ch = static_cast<float>(cn), sh = static_cast<float>(sn);
     cs[0][threadIdx.x] = ch;
-    cs[1][threadIdx.x] = static_cast<float>(c - static_cast<double>(ch));
+    cs[1][threadIdx.x] = static_cast<float>(cn - static_cast<double>(ch));
     cs[2][threadIdx.x] = sh;
-    cs[3][threadIdx.x] = static_cast<float>(s - static_cast<double>(sh));
+    cs[3][threadIdx.x] = static_cast<float>(sn - static_cast<double>(sh));
   }
-
-  // Cache row of (sequence b, KV head 0) at the new token's slot; head g adds g * head_stride.
-  size_t row0 = 0, head_stride = 0;
-  bool append = true;
-  if (paged) {
-    const int phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (pos >> a.log2_bs)];
-    if (phys < 0 || phys >= a.num_blocks) {
-      if (threadIdx.x == 0 && blockIdx.y == 0) flag_error(a.err, RRA_ERR_BLOCK_ID);
-      append = false;
+  if (threadIdx.x == 32) {  // another warp resolves where the new token's K and V go
+    int ok = 1;
+    size_t row0 = 0, stride = 0;
+    if (paged) {
+      const int phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (pos >> a.log2_bs)];
+      if (phys < 0 || phys >= a.num_blocks) {
+        if (blockIdx.y == 0) flag_error(a.err, RRA_ERR_BLOCK_ID);
+        ok = 0;
+      } else {
+        row0 = ((static_cast<size_t>(phys) << a.log2_bs) + (pos & ((1 << a.log2_bs) - 1))) * a.Hkv;
+        stride = 1;
+      }
     } else {
-      row0 = ((static_cast<size_t>(phys) << a.log2_bs) + (pos & ((1 << a.log2_bs) - 1))) * a.Hkv;
-      head_stride = 1;
+      row0 = static_cast<size_t>(b) * a.Hkv * a.max_len + pos;
+      stride = a.max_len;
     }
-  } else {
-    row0 = static_cast<size_t>(b) * a.Hkv * a.max_len + pos;
-    head_stride = a.max_len;
+    row_info[0] = row0;
+    row_info[1] = stride;
+    append_ok = ok;
   }
   __syncthreads();
+  const size_t row0 = row_info[0], head_stride = row_info[1];
+  const bool append = append_ok != 0;
 
-  const bool inter = a.rope_style == 1;
-  const int heads = append ? a.Hq + a.Hkv : a.Hq;
-  constexpr int kRows = kRopeThreads / kPairsPerCta;
-  const int j = threadIdx.x % kPairsPerCta;
   if (j < np) {
-    const int i = i0 + j;
-    const int ia = inter ? 2 * i : i;
-    const int ib = inter ? 2 * i + 1 : i + half;
     const float ch = cs[0][j], cl = cs[1][j], sh = cs[2][j], sl = cs[3][j];
-    for (int hh = threadIdx.x / kPairsPerCta; hh < heads; hh += kRows) {
-      const T* src;
-      T* dst;
-      if (hh < a.Hq) {
-        src = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + hh) * D;
-        dst = static_cast<T*>(a.q_out) + (static_cast<size_t>(b) * a.Hq + hh) * D;
-      } else {
-        const int g = hh - a.Hq;
-        src = static_cast<const T*>(a.k_new) + (static_cast<size_t>(b) * a.Hkv + g) * D;
-        dst = static_cast<T*>(a.k_cache) + (row0 + g * head_stride) * D;
+    for (int base = 0; base < heads; base += kRows * kUnroll) {
+#pragma unroll
+      for (int r = 0; r < kUnroll; ++r) {
+        const int hh = base + threadIdx.x / kPairsPerCta + kRows * r;
+        if (hh >= heads) break;
+        if (base > 0) {  // rows past the first kUnroll per thread (more than 64 heads)
+          xa[r] = Elem<T>::load(src_row(hh) + ia);
+          xb[r] = Elem<T>::load(src_row(hh) + ib);
+        }
+        T* dst;
+        if (hh < a.Hq) {
+          dst = static_cast<T*>(a.q_out) + (static_cast<size_t>(b) * a.Hq + hh) * D;
+        } else {
+          if (!append) continue;
+          dst = static_cast<T*>(a.k_cache) + (row0 + (hh - a.Hq) * head_stride) * D;
+        }
+        Elem<T>::store(dst + ia, rotate_diff(xa[r], xb[r], ch, cl, sh, sl));   // a cos - b sin
+        Elem<T>::store(dst + ib, rotate_diff(xb[r], -xa[r], ch, cl, sh, sl));  // b cos + a sin
       }
-      const float xa = Elem<T>::load(src + ia), xb = Elem<T>::load(src + ib);
-      Elem<T>::store(dst + ia, rotate_diff(xa, xb, ch, cl, sh, sl));   // a cos - b sin
-      Elem<T>::store(dst + ib, rotate_diff(xb, -xa, ch, cl, sh, sl));  // b cos + a sin
     }
   }
   if (!append) return;

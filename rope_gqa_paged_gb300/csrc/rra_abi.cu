@@ -104,32 +104,58 @@ int make_plan(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
   const int64_t tiles = std::max<int64_t>(1, (max_tokens + p->tile - 1) / p->tile);
   // A paged split copies its block ids to shared memory: at most kMaxTableEntries of them.
   int64_t max_chunk_tiles = tiles;
-  if (block_size > 0)
-    max_chunk_tiles = std::max<int64_t>(1, (int64_t(rra::kMaxTableEntries - 1) * block_size) / p->tile);
+  if (block_size > 0) {
+    const int entries = p->mma ? rra::kMmaTableEntries : rra::kMaxTableEntries;
+    max_chunk_tiles = std::max<int64_t>(1, (int64_t(entries - 1) * block_size) / p->tile);
+  }
   int64_t chunk_tiles;
   if (requested > 0) {
     chunk_tiles = (tiles + requested - 1) / requested;
   } else {
-    // Aim at ~4 CTAs per SM over the whole grid, each streaming 128..1024 tokens.
+    // About two waves of resident CTAs (3 per SM for the mma kernel, 2 otherwise), each
+    // streaming 128..2048 tokens: fewer, longer CTAs pay their start-up and epilogue less
+    // often, while two waves keep the tail of ragged batches short.
     const int64_t units = int64_t(B) * Hkv * (n_rep / p->hpc);
-    const int64_t target = 4 * std::max(1, sm_count());
+    const int64_t target = 2 * (p->mma ? 3 : 2) * std::max(1, sm_count());
     chunk_tiles = (tiles * units + target - 1) / target;
-    const int64_t lo = std::max(1, 128 / p->tile), hi = std::max(1, 1024 / p->tile);
+    const int64_t lo = std::max(1, 128 / p->tile), hi = std::max(1, 2048 / p->tile);
     chunk_tiles = std::min(std::max(chunk_tiles, lo), hi);
   }
   chunk_tiles = std::min(std::max<int64_t>(chunk_tiles, 1), max_chunk_tiles);
+  chunk_tiles = std::max<int64_t>(chunk_tiles, (tiles + rra::kMaxSplits - 1) / rra::kMaxSplits);
+  if (chunk_tiles > max_chunk_tiles) return RRA_ERANGE;
   const int64_t splits = (tiles + chunk_tiles - 1) / chunk_tiles;
-  if (splits * (n_rep / p->hpc) > 65535 * 1024) return RRA_ERANGE;
+  if (splits * (n_rep / p->hpc) > int64_t(INT32_MAX) / 2) return RRA_ERANGE;
   p->chunk = static_cast<int>(chunk_tiles * p->tile);
   p->splits = static_cast<int>(splits);
   return RRA_OK;
 }
 
+// Workspace layout, each part 256-byte aligned (R = B*Hq, G = ceil(splits / kMergeFanIn)):
+// partials o [R, splits, D] and (max, sum) [R, splits, 2] floats, level-2 partials o [R, G, D]
+// and (max, sum) [R, G, 2] floats, counters [R] and group counters [R, G] int32.
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t o, ml, o2, ml2, cnt, gcnt, total;
+};
+
+WsLayout ws_layout(int B, int Hq, int D, int splits) {
+  const size_t R = size_t(B) * Hq, G = (size_t(splits) + rra::kMergeFanIn - 1) / rra::kMergeFanIn;
+  WsLayout l{};
+  l.o = 0;
+  l.ml = l.o + align256(R * splits * D * sizeof(float));
+  l.o2 = l.ml + align256(R * splits * 2 * sizeof(float));
+  l.ml2 = l.o2 + align256(R * G * D * sizeof(float));
+  l.cnt = l.ml2 + align256(R * G * 2 * sizeof(float));
+  l.gcnt = l.cnt + align256(R * sizeof(int));
+  l.total = l.gcnt + R * G * sizeof(int);
+  return l;
+}
+
 size_t workspace_bytes(int B, int Hq, int D, int splits) {
   if (splits <= 1 || B <= 0) return 0;
-  const size_t rows = size_t(B) * Hq * splits;
-  const size_t o_bytes = (rows * D * sizeof(float) + 255) & ~size_t(255);
-  return o_bytes + rows * 2 * sizeof(float);
+  return ws_layout(B, Hq, D, splits).total;
 }
 
 // Tiled tensor map over `base` (rank 3 or 4, dims innermost first, strides in bytes of dims 1..).
@@ -199,22 +225,21 @@ rra::DecodeArgs decode_args(const Plan& p, const void* q, const void* k, const v
   const float s = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
   a.scale_log2 = s * 1.4426950408889634f;
   a.err = err;
+  a.num_groups = (p.splits + rra::kMergeFanIn - 1) / rra::kMergeFanIn;
   if (p.splits > 1) {
-    const size_t rows = size_t(B) * Hq * p.splits;
-    a.ws_o = static_cast<float*>(ws);
-    a.ws_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + ((rows * D * sizeof(float) + 255) & ~size_t(255)));
+    const WsLayout l = ws_layout(B, Hq, D, p.splits);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    a.ws_o = reinterpret_cast<float*>(base + l.o);
+    a.ws_ml = reinterpret_cast<float*>(base + l.ml);
+    a.ws2_o = reinterpret_cast<float*>(base + l.o2);
+    a.ws2_ml = reinterpret_cast<float*>(base + l.ml2);
+    a.counters = reinterpret_cast<int*>(base + l.cnt);
+    a.group_counters = reinterpret_cast<int*>(base + l.gcnt);
   }
   return a;
 }
 
-int finish_decode(const rra::DecodeArgs& a, rra_dtype dt, cudaError_t e, cudaStream_t st) {
-  if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
-  if (a.num_splits > 1) {
-    e = rra::launch_decode_reduce(a, dt, st);
-    if (e != cudaSuccess) return cuda_fail(e, "decode reduce launch");
-  }
-  return RRA_OK;
-}
+int finish_decode(cudaError_t e) { return e == cudaSuccess ? RRA_OK : cuda_fail(e, "decode kernel launch"); }
 
 }  // namespace
 
@@ -237,6 +262,11 @@ const char* rra_status_str(int status) {
 }
 
 const char* rra_last_cuda_error(void) { return g_cuda_error; }
+
+int rra_use_device(int device) {
+  const cudaError_t e = cudaSetDevice(device);
+  return e == cudaSuccess ? RRA_OK : cuda_fail(e, "cudaSetDevice");
+}
 
 uint64_t rra_kv_bytes(int n_layers, int n_kv_heads, int head_dim, int64_t seq_len, int batch, int dtype_bytes) {
   if (n_layers < 0 || n_kv_heads < 0 || head_dim < 0 || seq_len < 0 || batch < 0 || dtype_bytes < 0) return 0;
@@ -329,7 +359,7 @@ int rra_decode_attn_contig(const void* q_rot, const void* k_cache, const void* v
   a.max_len = max_len;
   a.capacity = max_len;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return finish_decode(a, dt, rra::launch_decode_contig(a, km, vm, dt, p.mma, s), s);
+  return finish_decode(rra::launch_decode_contig(a, km, vm, dt, p.mma, s));
 }
 
 int rra_decode_attn_paged(const void* q_rot, const void* k_pool, const void* v_pool, const int32_t* block_table,
@@ -362,7 +392,7 @@ int rra_decode_attn_paged(const void* q_rot, const void* k_pool, const void* v_p
   a.max_len = 0;
   a.capacity = static_cast<int>(capacity);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return finish_decode(a, dt, rra::launch_decode_paged(a, km, vm, dt, p.mma, s), s);
+  return finish_decode(rra::launch_decode_paged(a, km, vm, dt, p.mma, s));
 }
 
 }  // extern "C"

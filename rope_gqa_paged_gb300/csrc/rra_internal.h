@@ -42,6 +42,11 @@ struct DecodeArgs {
   void* out;                    // [B, Hq, D]
   float* ws_o;                  // [B, Hq, splits, D] unnormalised partial outputs
   float* ws_ml;                 // [B, Hq, splits, 2] (running max in log2 units, running sum)
+  float* ws2_o;                 // [B, Hq, num_groups, D] level-2 partials (groups of kMergeFanIn splits)
+  float* ws2_ml;                // [B, Hq, num_groups, 2]
+  int* counters;                // [B, Hq] arrivals per (sequence, first head of a CTA's head slice)
+  int* group_counters;          // [B, Hq, num_groups] arrivals per group of splits
+  int num_groups;               // ceil(num_splits / kMergeFanIn)
   int B, Hq, Hkv, D;
   int max_len;                  // contiguous row stride in tokens
   int capacity;                 // tokens a sequence can hold
@@ -56,6 +61,11 @@ struct DecodeArgs {
 inline int decode_tile_tokens(int D, int elem_bytes) { return 8192 / (D * elem_bytes); }
 // Most block-table entries one split may need (bounds the per-CTA table copy).
 constexpr int kMaxTableEntries = 2048;
+// Most splits per sequence (the CTA that merges them stages 2 x 8 heads x splits floats in
+// shared memory).
+constexpr int kMaxSplits = 1024;
+// Splits merged by one CTA; more splits are merged in two levels.
+constexpr int kMergeFanIn = 16;
 
 // Stores the text rra_last_cuda_error() returns on this thread.
 void record_cuda_error(cudaError_t e, const char* where);
@@ -63,6 +73,8 @@ void record_cuda_error(cudaError_t e, const char* where);
 cudaError_t launch_rope_append(const RopeArgs& a, rra_dtype dt, cudaStream_t stream);
 // Tokens per stage of the tensor-core (bf16) decode kernel: K + V tiles of 32 KB.
 inline int decode_mma_tile_tokens(int D) { return 16384 / (D * 2); }
+// Most block-table entries one work item of the tensor-core kernel may span.
+constexpr int kMmaTableEntries = 256;
 
 // use_mma: the bf16 tensor-core kernel (tensor maps with the 128-byte swizzle); otherwise the
 // CUDA-core kernel (contiguous: 1-D bulk copies, maps unused; paged: unswizzled maps).
@@ -70,6 +82,5 @@ cudaError_t launch_decode_contig(const DecodeArgs& a, const CUtensorMap& k_map, 
                                  rra_dtype dt, bool use_mma, cudaStream_t stream);
 cudaError_t launch_decode_paged(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
                                 rra_dtype dt, bool use_mma, cudaStream_t stream);
-cudaError_t launch_decode_reduce(const DecodeArgs& a, rra_dtype dt, cudaStream_t stream);
 
 }  // namespace rra

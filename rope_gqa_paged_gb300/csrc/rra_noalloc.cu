@@ -14,7 +14,8 @@
 //   * Shared by every call on a device: two calls whose kernels overlap on the GPU (two
 //     streams, or two host threads) race on it and return wrong results. Issue them in
 //     one stream, or serialise them.
-//   * Nothing in it needs clearing: each call writes every partial its merge reads.
+//   * Its split counters must start at zero: a static device array starts zeroed when the
+//     library is loaded, and every call leaves the counters at zero again.
 //   * Its device address is looked up once per device, on the first call made while
 //     that device is current (cudaGetSymbolAddress); make that first call before any
 //     stream capture begins.

@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 from typing import Optional
 
 import torch
@@ -16,7 +17,7 @@ import torch
 from . import _build
 
 RRA_F32, RRA_BF16 = 0, 1
-RRA_ERR_POSITION, RRA_ERR_BLOCK_ID, RRA_ERR_SEQ_LEN, RRA_ERR_TIMEOUT = 1, 2, 4, 8
+RRA_ERR_POSITION, RRA_ERR_BLOCK_ID, RRA_ERR_SEQ_LEN, RRA_ERR_TIMEOUT, RRA_ERR_WORKSPACE = 1, 2, 4, 8, 16
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -35,6 +36,7 @@ _SIGNATURES = {
     "rra_decode_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "rra_status_str": (ctypes.c_char_p, [_c_int]),
     "rra_last_cuda_error": (ctypes.c_char_p, []),
+    "rra_use_device": (_c_int, [_c_int]),
 }
 
 
@@ -84,9 +86,18 @@ def _ptr(t: Optional[torch.Tensor]):
     return t.data_ptr()
 
 
-def _stream(stream) -> Optional[int]:
+_device_of_thread = threading.local()
+
+
+def _stream(stream, t: torch.Tensor) -> Optional[int]:
+    """The stream handle for a call on tensor ``t``'s device (selecting that device in the
+    library when the call runs on the default stream, which carries no device)."""
+    dev = t.device.index if t.device.index is not None else torch.cuda.current_device()
+    if getattr(_device_of_thread, "dev", None) != dev:
+        _check("rra_use_device", lib().rra_use_device(dev))
+        _device_of_thread.dev = dev
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        return torch.cuda.current_stream(t.device).cuda_stream
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
@@ -133,7 +144,7 @@ def rra_rope_append(q, k_new, v_new, positions, q_out, k_cache, v_cache, block_t
         max_len = k_cache.shape[2]
     st = lib().rra_rope_append(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q_out), _ptr(k_cache),
                                _ptr(v_cache), _ptr(block_table), mbps, block_size, num_blocks, max_len, B, Hq, Hkv,
-                               D, float(rope_base), int(rope_style), _dtype_code(q), _ptr(err_flag), _stream(stream))
+                               D, float(rope_base), int(rope_style), _dtype_code(q), _ptr(err_flag), _stream(stream, q))
     _check("rra_rope_append", st)
 
 
@@ -145,7 +156,7 @@ def rra_decode_attn_contig(q_rot, k_cache, v_cache, seq_lens, out, scale: float 
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = lib().rra_decode_attn_contig(_ptr(q_rot), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(out), B, Hq,
                                       Hkv, D, max_len, float(scale), int(num_splits), _ptr(workspace), ws_bytes,
-                                      _dtype_code(q_rot), _ptr(err_flag), _stream(stream))
+                                      _dtype_code(q_rot), _ptr(err_flag), _stream(stream, q_rot))
     _check("rra_decode_attn_contig", st)
 
 
@@ -158,5 +169,5 @@ def rra_decode_attn_paged(q_rot, k_pool, v_pool, block_table, seq_lens, out, sca
     st = lib().rra_decode_attn_paged(_ptr(q_rot), _ptr(k_pool), _ptr(v_pool), _ptr(block_table),
                                      block_table.shape[1], _ptr(seq_lens), block_size, num_blocks, _ptr(out), B, Hq,
                                      Hkv, D, float(scale), int(num_splits), _ptr(workspace), ws_bytes,
-                                     _dtype_code(q_rot), _ptr(err_flag), _stream(stream))
+                                     _dtype_code(q_rot), _ptr(err_flag), _stream(stream, q_rot))
     _check("rra_decode_attn_paged", st)

@@ -32,10 +32,11 @@ class DecodeStep:
                                                 num_splits, code)
         self.num_splits = self.splits
         ws = rra.rra_decode_workspace_bytes(batch, n_q_heads, head_dim, self.splits)
-        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev) if ws else None
+        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=dev) if ws else None  # zeroed once
         self.q_rot = torch.empty(batch, n_q_heads, head_dim, dtype=self.dtype, device=dev)
         self.out = torch.empty(batch, n_q_heads, head_dim, dtype=self.dtype, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.graph = None
 
     def rope_append(self, q, k_new, v_new, positions, stream=None) -> None:
         rra.rra_rope_append(q, k_new, v_new, positions, self.q_rot, self.k_cache, self.v_cache, self.block_table,
@@ -54,6 +55,29 @@ class DecodeStep:
         """Rotate, append, attend. ``seq_lens`` = positions + 1 for a plain decode step."""
         self.rope_append(q, k_new, v_new, positions, stream)
         return self.attend(seq_lens, stream)
+
+    def capture(self, q, k_new, v_new, positions, seq_lens) -> None:
+        """Record one whole step (both library calls) into a CUDA graph.
+
+        The graph is bound to these input tensors and to this object's output, workspace
+        and error buffers: refill the inputs in place, then ``replay()``. Replaying saves
+        the host-side launch cost of every kernel of the step.
+        """
+        import torch
+        side = torch.cuda.Stream(device=q.device)
+        side.wait_stream(torch.cuda.current_stream(q.device))
+        with torch.cuda.stream(side):
+            self(q, k_new, v_new, positions, seq_lens)
+        torch.cuda.current_stream(q.device).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self(q, k_new, v_new, positions, seq_lens)
+        self.graph = graph
+
+    def replay(self) -> torch.Tensor:
+        """Run the captured step on the current stream; returns the output buffer."""
+        self.graph.replay()
+        return self.out
 
     def error_bits(self) -> int:
         """Device error word (RRA_ERR_* bits) accumulated since the last reset; synchronises."""

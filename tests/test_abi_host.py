@@ -56,6 +56,7 @@ def test_kv_bytes_matches_oracle_and_pages(rra):
 
 def test_workspace_bytes(rra):
     assert rra.rra_decode_workspace_bytes(64, 32, 128, 1) == 0
+    assert rra.rra_decode_workspace_bytes(0, 32, 128, 8) == 0
     b = rra.rra_decode_workspace_bytes(1, 32, 128, 128)
     assert b >= 32 * 128 * (128 + 2) * 4
     assert rra.rra_decode_workspace_bytes(2, 32, 128, 128) > b

@@ -200,3 +200,20 @@ def test_full_size_sampled(name):
     q_ref, out_ref = H.oracle_for_sequences(inp, sample)
     _check_step(inp, gpu, q_ref, out_ref, batches=sample)
     _check_cache(inp, gpu)                                # untouched slots bit-exact, V appended exactly
+
+
+# ------------------------------------------------------------------ many splits: two-level merge
+@pytest.mark.parametrize("name,factor", [("llama3_8b_layer", 2), ("long_context", 32)])
+@pytest.mark.parametrize("splits", [16, 17, 40, 64])
+def test_many_splits_merge(name, factor, splits):
+    """More than 16 splits are merged in two levels (groups of 16, then the groups).
+
+    The effective split count is the request rounded to whole tiles (here 13..64 splits,
+    most of them above 16, with a partial last group)."""
+    cfg = reduced(CONFIGS[name], factor, 2)
+    inp = make_inputs(cfg, seed=21)
+    gpu = H.run_gpu(inp, num_splits=splits)
+    assert gpu.splits > 1
+    q_ref, _, _, out_ref = H.run_oracle(inp)
+    assert gpu.err == 0
+    _check_step(inp, gpu, q_ref, out_ref)

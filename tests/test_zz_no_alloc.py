@@ -57,7 +57,7 @@ def test_noalloc_matches_workspace_entry_point_twice(name, factor, batch, splits
     eff = rra.rra_decode_num_splits(cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.capacity,
                                     cfg.block_size, splits, rra.RRA_BF16)
     ws_bytes = rra.rra_decode_workspace_bytes(cfg.batch, cfg.n_q_heads, cfg.head_dim, eff)
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     ref = torch.empty_like(q)
     rra.rra_decode_attn_paged(q, kp, vp_, table, lens, ref, num_splits=splits, workspace=ws, err_flag=err)
     torch.cuda.synchronize()
