@@ -42,8 +42,9 @@ DEFAULT_WORKLOAD = "batched_paged"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
-KERNEL_SOURCES = ["rope_gqa_paged_gb300/csrc/decode_kernels.cuh", "rope_gqa_paged_gb300/csrc/rra_device.cuh",
-                  "rope_gqa_paged_gb300/csrc/decode_paged.cu", "rope_gqa_paged_gb300/csrc/decode_contig.cu"]
+KERNEL_SOURCES = ["rope_gqa_paged_gb300/csrc/decode_mma.cuh", "rope_gqa_paged_gb300/csrc/decode_kernels.cuh",
+                  "rope_gqa_paged_gb300/csrc/rra_device.cuh", "rope_gqa_paged_gb300/csrc/decode_paged.cu",
+                  "rope_gqa_paged_gb300/csrc/decode_contig.cu"]
 
 
 def parse_args(argv=None):
