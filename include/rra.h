@@ -142,6 +142,33 @@ RRA_API int rra_decode_attn_paged(const void* q_rot, const void* k_pool, const v
                           int num_splits, void* workspace, size_t ws_bytes,
                           rra_dtype dt, int32_t* err_flag, void* stream);
 
+/* The whole step in one call: RoPE on q and k_new at positions[b], append of rotated k and
+ * raw v at that slot, and the attention of every query head over the L_b = positions[b] + 1
+ * tokens now in the cache ([KVC-GQA-RoPE] §5.1 b.ii-vi; [SelfAttn-Step] §4.5). For bf16
+ * caches (paged blocks of at least 8 tokens, or contiguous caches of at least 64 tokens for
+ * D = 128) it is a single kernel: the CTA whose chunk holds the new token writes it into
+ * the cache before reading that tile, and every CTA rotates its own query heads; otherwise
+ * it runs rra_rope_append and then the decode kernel.
+ *   q        [B, Hq, D] unrotated queries; q_out [B, Hq, D] receives q_rot and must not
+ *            overlap q.
+ *   positions[B]: slot of the new token; positions outside the cache set RRA_ERR_POSITION and
+ *            leave that sequence's outputs unwritten.
+ * Other arguments as in rra_rope_append and rra_decode_attn_contig / rra_decode_attn_paged
+ * (same workspace and split rules). */
+RRA_API int rra_decode_step_contig(const void* q, const void* k_new, const void* v_new,
+                                   const int32_t* positions, void* q_out, void* k_cache, void* v_cache,
+                                   int max_len, void* out, int B, int Hq, int Hkv, int D,
+                                   double rope_base, int rope_style, float scale, int num_splits,
+                                   void* workspace, size_t ws_bytes, rra_dtype dt, int32_t* err_flag,
+                                   void* stream);
+RRA_API int rra_decode_step_paged(const void* q, const void* k_new, const void* v_new,
+                                  const int32_t* positions, void* q_out, void* k_pool, void* v_pool,
+                                  const int32_t* block_table, int max_blocks_per_seq, int block_size,
+                                  int num_blocks, void* out, int B, int Hq, int Hkv, int D,
+                                  double rope_base, int rope_style, float scale, int num_splits,
+                                  void* workspace, size_t ws_bytes, rra_dtype dt, int32_t* err_flag,
+                                  void* stream);
+
 /* Bytes of a K+V cache: 2 * n_layers * n_kv_heads * head_dim * seq_len * batch * dtype_bytes
  * ([Opt-2026] §四 memory formula; [KVC-GQA-RoPE] §5.3). Host only; returns 0 when an
  * argument is negative or the product overflows 64 bits. */

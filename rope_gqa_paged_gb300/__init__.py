@@ -8,7 +8,8 @@ and uses torch only for device memory and streams.
 from .rra import (RRA_BF16, RRA_ERR_BLOCK_ID, RRA_ERR_POSITION, RRA_ERR_SEQ_LEN, RRA_ERR_TIMEOUT,  # noqa: F401
                   RRA_ERR_WORKSPACE,
                   RRA_F32, RraError, lib, lib_path, rra_decode_attn_contig, rra_decode_attn_paged,
-                  rra_decode_num_splits, rra_decode_workspace_bytes, rra_kv_bytes, rra_rope_append,
+                  rra_decode_num_splits, rra_decode_step_contig, rra_decode_step_paged, rra_decode_workspace_bytes,
+                  rra_kv_bytes, rra_rope_append,
                   rra_status_str)
 from .step import DecodeStep  # noqa: F401
 from ._build import build  # noqa: F401

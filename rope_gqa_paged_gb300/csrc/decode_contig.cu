@@ -10,4 +10,9 @@ cudaError_t launch_decode_contig(const DecodeArgs& a, const CUtensorMap& k_map, 
   return launch_decode_any<false>(a, k_map, v_map, dt, a.hpc, stream);
 }
 
+cudaError_t launch_decode_step_contig(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
+                   cudaStream_t stream) {
+  return launch_decode_mma<false, true>(a, k_map, v_map, a.hpc, stream);
+}
+
 }  // namespace rra

@@ -280,9 +280,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D>::kThreads, 2)
   const int h0 = g * n_rep + (blockIdx.y - g * slices) * HPC;
   const int b = blockIdx.z;
 
-  int L = a.seq_lens[b];
+  int L = a.positions != nullptr ? a.positions[b] + 1 : a.seq_lens[b];
   if (L < 0 || L > a.capacity) {
-    if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) flag_error(a.err, RRA_ERR_SEQ_LEN);
+    if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0)
+      flag_error(a.err, a.positions != nullptr ? RRA_ERR_POSITION : RRA_ERR_SEQ_LEN);
     L = min(max(L, 0), a.capacity);
   }
   const int start = split * a.chunk;

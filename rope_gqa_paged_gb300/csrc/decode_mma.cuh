@@ -48,7 +48,12 @@ struct MmaCfg {
   static constexpr int kHalfBytes = kTile * 128;          // one 64-dim half of K or V of a stage
   static constexpr int kStageBytes = 2 * kHalves * kHalfBytes;
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kSmemBytes = 1024 + kRingBytes + 2 * kStages * 8 + kMmaTableEntries * 4;
+  // after the ring: full[kStages], empty[kStages], appended (8 bytes each), the block-id
+  // table, and cos/sin hi/lo [4][D/2] floats for the fused step
+  static constexpr int kOffBar = kRingBytes;
+  static constexpr int kOffTable = kOffBar + (2 * kStages + 1) * 8;
+  static constexpr int kOffCs = kOffTable + kMmaTableEntries * 4;
+  static constexpr int kSmemBytes = 1024 + kOffCs + 4 * (D / 2) * 4;
   static constexpr int kMaxHeads = 8;
   static constexpr int kKSteps = D / 16;
 };
@@ -195,7 +200,47 @@ __device__ __forceinline__ void mma_step(MmaWarpState<D>& st, const uint32_t (&q
   }
 }
 
-template <int D, bool PAGED>
+// Fused step only: rotates the consumer lane's q fragment (raw bf16 pairs, same layout as
+// the B operand) in place, with cos/sin hi/lo per frequency in `cs`.
+template <int D>
+__device__ __forceinline__ void rotate_q_fragment(uint32_t (&qb)[D / 16][2], const float* cs, int lane, int style) {
+  constexpr int KK = D / 16, HALF = D / 2;
+  const int c2 = 2 * (lane & 3);
+  auto unpack = [](uint32_t w, float& lo, float& hi) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+  };
+  if (style == 1) {  // interleaved pairs (2i, 2i+1): the two halves of each 32-bit word
+#pragma unroll
+    for (int kk = 0; kk < KK; ++kk)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int i = (16 * kk + 8 * r + c2) >> 1;
+        float x0, x1;
+        unpack(qb[kk][r], x0, x1);
+        const float ch = cs[i], cl = cs[HALF + i], sh = cs[2 * HALF + i], sl = cs[3 * HALF + i];
+        qb[kk][r] = pack_bf16x2(rotate_diff(x0, x1, ch, cl, sh, sl), rotate_diff(x1, -x0, ch, cl, sh, sl));
+      }
+    return;
+  }
+  // half-split pairs (i, i + D/2): k-step kk and kk + KK/2 hold the two members
+#pragma unroll
+  for (int kk = 0; kk < KK / 2; ++kk)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float a0, a1, b0, b1;
+      unpack(qb[kk][r], a0, a1);
+      unpack(qb[kk + KK / 2][r], b0, b1);
+      const int i0 = 16 * kk + 8 * r + c2, i1 = i0 + 1;
+      const float ch0 = cs[i0], cl0 = cs[HALF + i0], sh0 = cs[2 * HALF + i0], sl0 = cs[3 * HALF + i0];
+      const float ch1 = cs[i1], cl1 = cs[HALF + i1], sh1 = cs[2 * HALF + i1], sl1 = cs[3 * HALF + i1];
+      qb[kk][r] = pack_bf16x2(rotate_diff(a0, b0, ch0, cl0, sh0, sl0), rotate_diff(a1, b1, ch1, cl1, sh1, sl1));
+      qb[kk + KK / 2][r] =
+          pack_bf16x2(rotate_diff(b0, -a0, ch0, cl0, sh0, sl0), rotate_diff(b1, -a1, ch1, cl1, sh1, sl1));
+    }
+}
+
+template <int D, bool PAGED, bool FUSED>
 __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     decode_mma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                       const DecodeArgs a) {
@@ -211,10 +256,20 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   const int h0 = g * n_rep + (blockIdx.x - split * slices) * hpc;
   const int b = blockIdx.z;
 
-  int L = a.seq_lens[b];
-  if (L < 0 || L > a.capacity) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) flag_error(a.err, RRA_ERR_SEQ_LEN);
-    L = min(max(L, 0), a.capacity);
+  int L;
+  if constexpr (FUSED) {
+    const int pos = a.positions[b];
+    if (pos < 0 || pos >= a.capacity) {  // nothing is written for this sequence
+      if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) flag_error(a.err, RRA_ERR_POSITION);
+      return;
+    }
+    L = pos + 1;
+  } else {
+    L = a.seq_lens[b];
+    if (L < 0 || L > a.capacity) {
+      if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) flag_error(a.err, RRA_ERR_SEQ_LEN);
+      L = min(max(L, 0), a.capacity);
+    }
   }
   const int start = split * a.chunk;
   const int n_work = (L + a.chunk - 1) / a.chunk;  // splits of this sequence that hold tokens
@@ -227,10 +282,14 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   }
   const int end = min(L, start + a.chunk);
   const int n_tiles = (end - start + C::kTile - 1) / C::kTile;
+  // Fused step: this CTA's chunk holds the new token, so it writes it into the cache first.
+  const bool appender = FUSED && end == L;
 
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRingBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* empty = full + C::kStages;
-  int32_t* tbl = reinterpret_cast<int32_t*>(empty + C::kStages);
+  uint64_t* appended = empty + C::kStages;
+  int32_t* tbl = reinterpret_cast<int32_t*>(smem + C::kOffTable);
+  float* cs = reinterpret_cast<float*>(smem + C::kOffCs);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -239,6 +298,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], C::kConsumerWarps);
     }
+    mbar_init(appended, 1);
     fence_barrier_init();
   }
   int first_blk = 0;
@@ -270,6 +330,10 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
           break;
         }
         const int t0 = start + it * C::kTile;
+        if (appender && it == n_tiles - 1 && !mbar_wait(appended, 0)) {  // the new token is in this tile
+          flag_error(a.err, RRA_ERR_TIMEOUT);
+          break;
+        }
         uint8_t* kst = smem + s * C::kStageBytes;
         uint8_t* vst = kst + C::kHalves * C::kHalfBytes;
         if constexpr (PAGED) {
@@ -315,16 +379,74 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   }
 
   // ------------------------------------------------------------------ consumers
+  constexpr int kConsumerThreads = C::kConsumerWarps * 32;
   // Q^T as the B operand: lane holds q[head lane/4][dims 16kk + 2(lane%4) + {0,1}] and (+8).
   uint32_t qb[C::kKSteps][2];
+  const int hd = lane >> 2;
   {
-    const int hd = lane >> 2;
     const uint32_t* q = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.q) +
                                                           (static_cast<size_t>(b) * a.Hq + h0 + hd) * D);
 #pragma unroll
     for (int kk = 0; kk < C::kKSteps; ++kk) {
       qb[kk][0] = hd < hpc ? q[kk * 8 + (lane & 3)] : 0u;
       qb[kk][1] = hd < hpc ? q[kk * 8 + 4 + (lane & 3)] : 0u;
+    }
+  }
+  if constexpr (FUSED) {
+    // RoPE ("Transformer推理核心：KV Cache、GQA与RoPE原理与工程实践" §3): sine and cosine of
+    // pos * theta_i in float64 (sincospi of pos * theta_i / pi: exact argument reduction),
+    // split into float32 hi + lo for the error-free rotation.
+    const int pos = L - 1;
+    if (threadIdx.x < D / 2) {
+      double sn, cn;
+      sincospi(static_cast<double>(pos) * a.theta_pi[threadIdx.x], &sn, &cn);
+      const float ch = static_cast<float>(cn), sh = static_cast<float>(sn);
+      cs[threadIdx.x] = ch;
+      cs[D / 2 + threadIdx.x] = static_cast<float>(cn - static_cast<double>(ch));
+      cs[D + threadIdx.x] = sh;
+      cs[3 * (D / 2) + threadIdx.x] = static_cast<float>(sn - static_cast<double>(sh));
+    }
+    named_barrier_sync(1, kConsumerThreads);
+    rotate_q_fragment<D>(qb, cs, lane, a.rope_style);
+    if (warp == 0 && split == 0 && hd < hpc) {  // publish q_rot (rounded to bf16, as used here)
+      uint32_t* qo = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.q_out) +
+                                                 (static_cast<size_t>(b) * a.Hq + h0 + hd) * D);
+#pragma unroll
+      for (int kk = 0; kk < C::kKSteps; ++kk) {
+        qo[kk * 8 + (lane & 3)] = qb[kk][0];
+        qo[kk * 8 + 4 + (lane & 3)] = qb[kk][1];
+      }
+    }
+    if (appender && warp == 1) {
+      // Rotated k_new and raw v_new into slot pos of KV head g. Every head-slice CTA of this
+      // chunk writes the same bytes, so their writes cannot tear one another's reads.
+      size_t row = 0;
+      bool ok = true;
+      if constexpr (PAGED) {
+        const int phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (pos >> a.log2_bs)];
+        ok = phys >= 0 && phys < a.num_blocks;  // a bad id was flagged when the table was read
+        row = ((static_cast<size_t>(phys) << a.log2_bs) + (pos & ((1 << a.log2_bs) - 1))) * a.Hkv + g;
+      } else {
+        row = (static_cast<size_t>(b) * a.Hkv + g) * a.max_len + pos;
+      }
+      if (ok) {
+        const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(a.k_new) + (static_cast<size_t>(b) * a.Hkv + g) * D;
+        const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(a.v_new) + (static_cast<size_t>(b) * a.Hkv + g) * D;
+        __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(const_cast<void*>(a.k)) + row * D;
+        __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(const_cast<void*>(a.v)) + row * D;
+        const bool inter = a.rope_style == 1;
+        for (int i = lane; i < D / 2; i += 32) {
+          const int ia = inter ? 2 * i : i, ib = inter ? 2 * i + 1 : i + D / 2;
+          const float xa = __bfloat162float(kn[ia]), xb = __bfloat162float(kn[ib]);
+          const float ch = cs[i], cl = cs[D / 2 + i], sh = cs[D + i], sl = cs[3 * (D / 2) + i];
+          kc[ia] = __float2bfloat16_rn(rotate_diff(xa, xb, ch, cl, sh, sl));
+          kc[ib] = __float2bfloat16_rn(rotate_diff(xb, -xa, ch, cl, sh, sl));
+        }
+        for (int i = lane; i < D; i += 32) vc[i] = vn[i];
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // visible to the TMA that reads the slot
+      __syncwarp();
+      if (lane == 0) mbar_arrive(appended);
     }
   }
   MmaWarpState<D> st;
@@ -419,12 +541,12 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   }
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool FUSED>
 cudaError_t launch_decode_mma_t(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm, int hpc,
                                 cudaStream_t st) {
   using C = MmaCfg<D>;
   static int done[64] = {0};
-  auto kern = decode_mma_kernel<D, PAGED>;
+  auto kern = decode_mma_kernel<D, PAGED, FUSED>;
   cudaError_t e = ensure_smem(kern, C::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   const dim3 grid(a.num_splits * ((a.Hq / a.Hkv) / hpc), a.Hkv, a.B);
@@ -432,11 +554,11 @@ cudaError_t launch_decode_mma_t(const DecodeArgs& a, const CUtensorMap& km, cons
   return cudaGetLastError();
 }
 
-template <bool PAGED>
+template <bool PAGED, bool FUSED = false>
 cudaError_t launch_decode_mma(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm, int hpc,
                               cudaStream_t st) {
-  if (a.D == 128) return launch_decode_mma_t<128, PAGED>(a, km, vm, hpc, st);
-  return launch_decode_mma_t<64, PAGED>(a, km, vm, hpc, st);
+  if (a.D == 128) return launch_decode_mma_t<128, PAGED, FUSED>(a, km, vm, hpc, st);
+  return launch_decode_mma_t<64, PAGED, FUSED>(a, km, vm, hpc, st);
 }
 
 }  // namespace rra

@@ -10,4 +10,9 @@ cudaError_t launch_decode_paged(const DecodeArgs& a, const CUtensorMap& k_map, c
   return launch_decode_any<true>(a, k_map, v_map, dt, a.hpc, stream);
 }
 
+cudaError_t launch_decode_step_paged(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
+                   cudaStream_t stream) {
+  return launch_decode_mma<true, true>(a, k_map, v_map, a.hpc, stream);
+}
+
 }  // namespace rra

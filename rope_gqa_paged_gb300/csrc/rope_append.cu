@@ -24,17 +24,6 @@ namespace {
 constexpr int kPairsPerCta = 16;
 constexpr int kRopeThreads = 128;
 
-// a*(ch + cl) - b*(sh + sl) to ~1 float32 ulp of the result (no contraction: the
-// explicit _rn intrinsics keep each product's rounding error where the formula needs it).
-__device__ __forceinline__ float rotate_diff(float a, float b, float ch, float cl, float sh, float sl) {
-  const float p = __fmul_rn(a, ch);
-  const float ep = __fmaf_rn(a, ch, -p);
-  const float q = __fmul_rn(b, sh);
-  const float eq = __fmaf_rn(b, sh, -q);
-  const float small = __fadd_rn(__fsub_rn(ep, eq), __fsub_rn(__fmul_rn(a, cl), __fmul_rn(b, sl)));
-  return __fadd_rn(__fsub_rn(p, q), small);
-}
-
 template <typename T>
 __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArgs a) {
   constexpr int kRows = kRopeThreads / kPairsPerCta;  // head rows handled side by side

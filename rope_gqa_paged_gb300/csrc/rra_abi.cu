@@ -241,6 +241,31 @@ rra::DecodeArgs decode_args(const Plan& p, const void* q, const void* k, const v
 
 int finish_decode(cudaError_t e) { return e == cudaSuccess ? RRA_OK : cuda_fail(e, "decode kernel launch"); }
 
+// theta_i / pi for i < D/2, theta_i = base^(-2i/D), in float64.
+void fill_theta_pi(double* t, int D, double base) {
+  constexpr double kPi = 3.14159265358979323846;
+  for (int i = 0; i < D / 2; ++i) t[i] = std::pow(base, -2.0 * i / D) / kPi;
+}
+
+bool overlap(const void* a, const void* b, size_t bytes) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bytes && y < x + bytes;
+}
+
+// Checks shared by the two fused-step entry points (everything but the cache layout).
+int check_step_args(const void* q, const void* k_new, const void* v_new, const int32_t* positions, const void* q_out,
+                    const void* k_cache, const void* v_cache, const void* out, int B, int Hq, int D, double rope_base,
+                    int rope_style, float scale, rra_dtype dt) {
+  if (!(rope_base > 1.0) || !std::isfinite(rope_base) || (rope_style != 0 && rope_style != 1)) return RRA_EINVAL;
+  if (!std::isfinite(scale)) return RRA_EINVAL;
+  if (B == 0) return RRA_OK;
+  if (!q || !k_new || !v_new || !positions || !q_out || !k_cache || !v_cache || !out) return RRA_EINVAL;
+  for (const void* p : {q, k_new, v_new, q_out, k_cache, v_cache, out})
+    if (!aligned16(p)) return RRA_EINVAL;
+  if (overlap(q, q_out, size_t(B) * Hq * D * elem_bytes(dt))) return RRA_EINVAL;  // q is read after q_out is written
+  return RRA_OK;
+}
+
 }  // namespace
 
 namespace rra {
@@ -327,8 +352,7 @@ int rra_rope_append(const void* q, const void* k_new, const void* v_new, const i
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.D = D;
-  constexpr double kPi = 3.14159265358979323846;
-  for (int i = 0; i < D / 2; ++i) a.inv_freq[i] = std::pow(rope_base, -2.0 * i / D) / kPi;
+  fill_theta_pi(a.inv_freq, D, rope_base);
   a.rope_style = rope_style;
   a.err = err_flag;
   const cudaError_t e = rra::launch_rope_append(a, dt, static_cast<cudaStream_t>(stream));
@@ -393,6 +417,92 @@ int rra_decode_attn_paged(const void* q_rot, const void* k_pool, const void* v_p
   a.capacity = static_cast<int>(capacity);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   return finish_decode(rra::launch_decode_paged(a, km, vm, dt, p.mma, s));
+}
+
+int rra_decode_step_contig(const void* q, const void* k_new, const void* v_new, const int32_t* positions, void* q_out,
+                           void* k_cache, void* v_cache, int max_len, void* out, int B, int Hq, int Hkv, int D,
+                           double rope_base, int rope_style, float scale, int num_splits, void* workspace,
+                           size_t ws_bytes, rra_dtype dt, int32_t* err_flag, void* stream) {
+  if (max_len < 1) return RRA_EINVAL;
+  Plan p;
+  int st = make_plan(B, Hq, Hkv, D, max_len, 0, num_splits, dt, &p);
+  if (st != RRA_OK) return st;
+  st = check_step_args(q, k_new, v_new, positions, q_out, k_cache, v_cache, out, B, Hq, D, rope_base, rope_style,
+                       scale, dt);
+  if (st != RRA_OK || B == 0) return st;
+  st = check_workspace(p, B, Hq, D, workspace, ws_bytes);
+  if (st != RRA_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap km{}, vm{};
+  if (p.mma) {
+    st = encode_contig_map(&km, k_cache, B, Hkv, max_len, D, p.tile, dt);
+    if (st != RRA_OK) return st;
+    st = encode_contig_map(&vm, v_cache, B, Hkv, max_len, D, p.tile, dt);
+    if (st != RRA_OK) return st;
+  } else {  // two kernels: RoPE + append, then the decode with L_b = positions[b] + 1
+    st = rra_rope_append(q, k_new, v_new, positions, q_out, k_cache, v_cache, nullptr, 0, 0, 0, max_len, B, Hq, Hkv,
+                         D, rope_base, rope_style, dt, err_flag, stream);
+    if (st != RRA_OK) return st;
+  }
+  rra::DecodeArgs a =
+      decode_args(p, p.mma ? q : q_out, k_cache, v_cache, nullptr, out, B, Hq, Hkv, D, scale, workspace, err_flag);
+  a.max_len = max_len;
+  a.capacity = max_len;
+  a.positions = positions;
+  if (!p.mma) return finish_decode(rra::launch_decode_contig(a, km, vm, dt, false, s));
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.q_out = q_out;
+  a.rope_style = rope_style;
+  fill_theta_pi(a.theta_pi, D, rope_base);
+  return finish_decode(rra::launch_decode_step_contig(a, km, vm, s));
+}
+
+int rra_decode_step_paged(const void* q, const void* k_new, const void* v_new, const int32_t* positions, void* q_out,
+                          void* k_pool, void* v_pool, const int32_t* block_table, int max_blocks_per_seq,
+                          int block_size, int num_blocks, void* out, int B, int Hq, int Hkv, int D, double rope_base,
+                          int rope_style, float scale, int num_splits, void* workspace, size_t ws_bytes, rra_dtype dt,
+                          int32_t* err_flag, void* stream) {
+  if (!pow2(block_size)) return block_size <= 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
+  if (max_blocks_per_seq < 1 || num_blocks < 1) return RRA_EINVAL;
+  const int64_t capacity = int64_t(max_blocks_per_seq) * block_size;
+  Plan p;
+  int st = make_plan(B, Hq, Hkv, D, capacity, block_size, num_splits, dt, &p);
+  if (st != RRA_OK) return st;
+  st = check_step_args(q, k_new, v_new, positions, q_out, k_pool, v_pool, out, B, Hq, D, rope_base, rope_style, scale,
+                       dt);
+  if (st != RRA_OK || B == 0) return st;
+  if (!block_table) return RRA_EINVAL;
+  st = check_workspace(p, B, Hq, D, workspace, ws_bytes);
+  if (st != RRA_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int box_rows = block_size < p.tile ? block_size : p.tile;
+  CUtensorMap km, vm;
+  st = encode_pool_map(&km, k_pool, num_blocks, block_size, Hkv, D, box_rows, dt, p.mma);
+  if (st != RRA_OK) return st;
+  st = encode_pool_map(&vm, v_pool, num_blocks, block_size, Hkv, D, box_rows, dt, p.mma);
+  if (st != RRA_OK) return st;
+  if (!p.mma) {  // two kernels: RoPE + append, then the decode with L_b = positions[b] + 1
+    st = rra_rope_append(q, k_new, v_new, positions, q_out, k_pool, v_pool, block_table, max_blocks_per_seq,
+                         block_size, num_blocks, 0, B, Hq, Hkv, D, rope_base, rope_style, dt, err_flag, stream);
+    if (st != RRA_OK) return st;
+  }
+  rra::DecodeArgs a =
+      decode_args(p, p.mma ? q : q_out, k_pool, v_pool, nullptr, out, B, Hq, Hkv, D, scale, workspace, err_flag);
+  a.block_table = block_table;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.log2_bs = ilog2(block_size);
+  a.num_blocks = num_blocks;
+  a.max_len = 0;
+  a.capacity = static_cast<int>(capacity);
+  a.positions = positions;
+  if (!p.mma) return finish_decode(rra::launch_decode_paged(a, km, vm, dt, false, s));
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.q_out = q_out;
+  a.rope_style = rope_style;
+  fill_theta_pi(a.theta_pi, D, rope_base);
+  return finish_decode(rra::launch_decode_step_paged(a, km, vm, s));
 }
 
 }  // extern "C"

@@ -101,6 +101,20 @@ inline cudaError_t ensure_smem(Kernel k, int bytes, int* done_per_device) {
   return e;
 }
 
+// a*(ch + cl) - b*(sh + sl) to ~1 float32 ulp of the result, where (ch, cl) and (sh, sl)
+// are a cosine and a sine split into float32 hi + lo parts. The products a*ch and b*sh
+// are kept exactly as p + e with e = fma(x, y, -p) (Dekker's product using the FMA), so
+// the difference keeps full relative accuracy when the two products cancel. The explicit
+// _rn intrinsics stop the compiler from contracting the products into other operations.
+__device__ __forceinline__ float rotate_diff(float a, float b, float ch, float cl, float sh, float sl) {
+  const float p = __fmul_rn(a, ch);
+  const float ep = __fmaf_rn(a, ch, -p);
+  const float q = __fmul_rn(b, sh);
+  const float eq = __fmaf_rn(b, sh, -q);
+  const float small = __fadd_rn(__fsub_rn(ep, eq), __fsub_rn(__fmul_rn(a, cl), __fmul_rn(b, sl)));
+  return __fadd_rn(__fsub_rn(p, q), small);
+}
+
 // ---- element types --------------------------------------------------------
 template <typename T>
 struct Elem;

@@ -10,6 +10,7 @@
 namespace rra {
 
 constexpr int kMaxHeadDim = 512;
+constexpr int kMaxDecodeHeadDim = 128;
 
 struct RopeArgs {
   const void* q;
@@ -55,6 +56,15 @@ struct DecodeArgs {
   int chunk;                    // tokens per split (a multiple of the tile)
   float scale_log2;             // softmax scale * log2(e)
   int32_t* err;
+  // Fused step (RoPE + append inside the decode kernel). When `positions` is set, L_b =
+  // positions[b] + 1 and seq_lens is unused; the fused kernel also reads unrotated q,
+  // rotates it, writes q_out, and appends rotated k_new / raw v_new at the position.
+  const int32_t* positions;
+  const void* k_new;            // [B, Hkv, D]
+  const void* v_new;            // [B, Hkv, D]
+  void* q_out;                  // [B, Hq, D], must not overlap q
+  int rope_style;
+  double theta_pi[kMaxDecodeHeadDim / 2];  // theta_i / pi, theta_i = base^(-2i/D)
 };
 
 // Tokens per pipeline stage for a head_dim and element size: K + V tiles of 16 KB.
@@ -82,5 +92,10 @@ cudaError_t launch_decode_contig(const DecodeArgs& a, const CUtensorMap& k_map, 
                                  rra_dtype dt, bool use_mma, cudaStream_t stream);
 cudaError_t launch_decode_paged(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
                                 rra_dtype dt, bool use_mma, cudaStream_t stream);
+// The whole step in the tensor-core kernel (a.positions, a.k_new, a.v_new, a.q_out set).
+cudaError_t launch_decode_step_contig(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                      cudaStream_t stream);
+cudaError_t launch_decode_step_paged(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
+                                     cudaStream_t stream);
 
 }  // namespace rra

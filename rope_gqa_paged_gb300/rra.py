@@ -37,6 +37,11 @@ _SIGNATURES = {
     "rra_status_str": (ctypes.c_char_p, [_c_int]),
     "rra_last_cuda_error": (ctypes.c_char_p, []),
     "rra_use_device": (_c_int, [_c_int]),
+    "rra_decode_step_contig": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int,
+                                        _c_int, _c_f64, _c_int, _c_f32, _c_int, _vp, _c_size, _c_int, _vp, _vp]),
+    "rra_decode_step_paged": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _c_int,
+                                       _c_int, _c_int, _c_int, _c_f64, _c_int, _c_f32, _c_int, _vp, _c_size, _c_int,
+                                       _vp, _vp]),
 }
 
 
@@ -171,3 +176,32 @@ def rra_decode_attn_paged(q_rot, k_pool, v_pool, block_table, seq_lens, out, sca
                                      Hkv, D, float(scale), int(num_splits), _ptr(workspace), ws_bytes,
                                      _dtype_code(q_rot), _ptr(err_flag), _stream(stream, q_rot))
     _check("rra_decode_attn_paged", st)
+
+
+def rra_decode_step_contig(q, k_new, v_new, positions, q_out, k_cache, v_cache, out, rope_base: float = 10000.0,
+                           rope_style: int = 0, scale: float = 0.0, num_splits: int = 0, workspace=None,
+                           err_flag=None, stream=None) -> None:
+    """The whole decode step on a contiguous cache: RoPE, append at positions, attention over positions+1."""
+    B, Hq, D = q.shape
+    Hkv, max_len = k_cache.shape[1], k_cache.shape[2]
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().rra_decode_step_contig(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q_out), _ptr(k_cache),
+                                      _ptr(v_cache), max_len, _ptr(out), B, Hq, Hkv, D, float(rope_base),
+                                      int(rope_style), float(scale), int(num_splits), _ptr(workspace), ws_bytes,
+                                      _dtype_code(q), _ptr(err_flag), _stream(stream, q))
+    _check("rra_decode_step_contig", st)
+
+
+def rra_decode_step_paged(q, k_new, v_new, positions, q_out, k_pool, v_pool, block_table, out,
+                          rope_base: float = 10000.0, rope_style: int = 0, scale: float = 0.0, num_splits: int = 0,
+                          workspace=None, err_flag=None, stream=None) -> None:
+    """The whole decode step on a paged pool: RoPE, append at positions, attention over positions+1."""
+    B, Hq, D = q.shape
+    num_blocks, block_size, Hkv = k_pool.shape[0], k_pool.shape[1], k_pool.shape[2]
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().rra_decode_step_paged(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q_out), _ptr(k_pool),
+                                     _ptr(v_pool), _ptr(block_table), block_table.shape[1], block_size, num_blocks,
+                                     _ptr(out), B, Hq, Hkv, D, float(rope_base), int(rope_style), float(scale),
+                                     int(num_splits), _ptr(workspace), ws_bytes, _dtype_code(q), _ptr(err_flag),
+                                     _stream(stream, q))
+    _check("rra_decode_step_paged", st)

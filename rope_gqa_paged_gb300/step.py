@@ -51,12 +51,27 @@ class DecodeStep:
                                       self.scale, self.num_splits, self.workspace, self.err, stream)
         return self.out
 
-    def __call__(self, q, k_new, v_new, positions, seq_lens, stream=None) -> torch.Tensor:
-        """Rotate, append, attend. ``seq_lens`` = positions + 1 for a plain decode step."""
+    def fused(self, q, k_new, v_new, positions, stream=None) -> torch.Tensor:
+        """The whole step in one library call (one kernel for bf16 caches); attends positions + 1."""
+        if self.block_table is None:
+            rra.rra_decode_step_contig(q, k_new, v_new, positions, self.q_rot, self.k_cache, self.v_cache, self.out,
+                                       self.rope_base, self.rope_style, self.scale, self.num_splits, self.workspace,
+                                       self.err, stream)
+        else:
+            rra.rra_decode_step_paged(q, k_new, v_new, positions, self.q_rot, self.k_cache, self.v_cache,
+                                      self.block_table, self.out, self.rope_base, self.rope_style, self.scale,
+                                      self.num_splits, self.workspace, self.err, stream)
+        return self.out
+
+    def __call__(self, q, k_new, v_new, positions, seq_lens=None, stream=None) -> torch.Tensor:
+        """Rotate, append, attend. Without ``seq_lens`` this is the fused step (attending
+        positions + 1 tokens); with it, the two calls rra_rope_append + rra_decode_attn_*."""
+        if seq_lens is None:
+            return self.fused(q, k_new, v_new, positions, stream)
         self.rope_append(q, k_new, v_new, positions, stream)
         return self.attend(seq_lens, stream)
 
-    def capture(self, q, k_new, v_new, positions, seq_lens) -> None:
+    def capture(self, q, k_new, v_new, positions, seq_lens=None) -> None:
         """Record one whole step (both library calls) into a CUDA graph.
 
         The graph is bound to these input tensors and to this object's output, workspace

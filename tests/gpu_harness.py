@@ -49,7 +49,9 @@ class GpuResult:
 
 
 def run_gpu(inp: DecodeInputs, num_splits: int = 0, rope_style: int = 0, device="cuda:0",
-            fetch_cache: bool = True, seq_lens: Optional[np.ndarray] = None) -> GpuResult:
+            fetch_cache: bool = True, seq_lens: Optional[np.ndarray] = None, fused: bool = False) -> GpuResult:
+    """One decode step through the C ABI: the fused call (``fused``) or rra_rope_append +
+    rra_decode_attn_* (attending ``seq_lens``, default positions + 1)."""
     from rope_gqa_paged_gb300 import DecodeStep
 
     cfg = inp.cfg
@@ -59,8 +61,12 @@ def run_gpu(inp: DecodeInputs, num_splits: int = 0, rope_style: int = 0, device=
     step = DecodeStep(cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, kc, vc, table,
                       num_splits=num_splits or cfg.num_splits, rope_base=cfg.rope_base, rope_style=rope_style)
     lens = inp.lengths if seq_lens is None else seq_lens
-    out = step(to_torch(inp.q, dt, device), to_torch(inp.k_new, dt, device), to_torch(inp.v_new, dt, device),
-               to_torch(inp.positions, "i32", device), to_torch(np.asarray(lens, dtype=np.int32), "i32", device))
+    args = (to_torch(inp.q, dt, device), to_torch(inp.k_new, dt, device), to_torch(inp.v_new, dt, device),
+            to_torch(inp.positions, "i32", device))
+    if fused:
+        out = step(*args)
+    else:
+        out = step(*args, to_torch(np.asarray(lens, dtype=np.int32), "i32", device))
     torch.cuda.synchronize(device)
     res = GpuResult(q_rot=to_numpy(step.q_rot), out=to_numpy(out),
                     k_cache=to_numpy(kc) if fetch_cache else None, v_cache=to_numpy(vc) if fetch_cache else None,

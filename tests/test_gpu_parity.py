@@ -65,10 +65,11 @@ REDUCED = [("tiny_fp32", 1, None), ("llama3_8b_layer", 16, None), ("batched_page
 
 @pytest.mark.parametrize("name,factor,batch", REDUCED, ids=[r[0] for r in REDUCED])
 @pytest.mark.parametrize("splits", [0, 1, 3])
-def test_reduced_workload(name, factor, batch, splits):
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused_step"])
+def test_reduced_workload(name, factor, batch, splits, fused):
     cfg = CONFIGS[name] if factor == 1 else reduced(CONFIGS[name], factor, batch)
     inp = make_inputs(cfg)
-    gpu = H.run_gpu(inp, num_splits=splits)
+    gpu = H.run_gpu(inp, num_splits=splits, fused=fused)
     q_ref, k_ref, _, out_ref = H.run_oracle(inp)
     assert gpu.err == 0
     _check_step(inp, gpu, q_ref, out_ref)
@@ -76,10 +77,11 @@ def test_reduced_workload(name, factor, batch, splits):
 
 
 @pytest.mark.parametrize("layout", ["contiguous", "paged"])
-def test_interleaved_rope_pairs(layout):
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused_step"])
+def test_interleaved_rope_pairs(layout, fused):
     base = CONFIGS["llama3_8b_layer"] if layout == "contiguous" else CONFIGS["batched_paged"]
     inp = make_inputs(reduced(base, 16, 4), seed=3)
-    gpu = H.run_gpu(inp, rope_style=1)
+    gpu = H.run_gpu(inp, rope_style=1, fused=fused)
     q_ref, k_ref, _, out_ref = H.run_oracle(inp, rope_style=1)
     _check_step(inp, gpu, q_ref, out_ref)
     _check_cache(inp, gpu, _oracle_k_rows(inp, k_ref))
@@ -120,8 +122,8 @@ def test_edge_lengths(layout, bs):
             inp.block_table[b, :nb] = perm[k:k + nb]
             k += nb
     gen.poison_unread(inp)
-    for splits in (0, 1, 2, 5):
-        gpu = H.run_gpu(inp, num_splits=splits)
+    for splits, fused in ((0, False), (1, False), (2, False), (5, False), (0, True), (1, True), (5, True)):
+        gpu = H.run_gpu(inp, num_splits=splits, fused=fused)
         q_ref, k_ref, _, out_ref = H.run_oracle(inp)
         assert gpu.err == 0
         _check_step(inp, gpu, q_ref, out_ref)
@@ -191,7 +193,7 @@ FULL = ["llama3_8b_layer", "batched_paged", "long_context", "prefix_sweep_kv32",
 def test_full_size_sampled(name):
     cfg = CONFIGS[name]
     inp = make_inputs(cfg)
-    gpu = H.run_gpu(inp)                                  # the launch configuration the bench uses
+    gpu = H.run_gpu(inp, fused=True)                      # the launch configuration the bench uses
     assert gpu.err == 0
     rng = np.random.default_rng(1)
     sample = sorted(set([0, cfg.batch - 1] + rng.choice(cfg.batch, size=min(cfg.batch, 3), replace=False).tolist()))
@@ -212,8 +214,23 @@ def test_many_splits_merge(name, factor, splits):
     most of them above 16, with a partial last group)."""
     cfg = reduced(CONFIGS[name], factor, 2)
     inp = make_inputs(cfg, seed=21)
-    gpu = H.run_gpu(inp, num_splits=splits)
+    gpu = H.run_gpu(inp, num_splits=splits, fused=True)
     assert gpu.splits > 1
     q_ref, _, _, out_ref = H.run_oracle(inp)
     assert gpu.err == 0
     _check_step(inp, gpu, q_ref, out_ref)
+
+
+def test_fused_step_position_errors_are_flagged():
+    """A position outside the cache: flagged, that sequence untouched, the others correct."""
+    cfg = reduced(CONFIGS["batched_paged"], 16, 4)
+    inp = make_inputs(cfg, seed=14)
+    from rope_gqa_paged_gb300 import RRA_ERR_POSITION
+    good = H.run_gpu(inp, fused=True)
+    bad = inp.positions.copy()
+    inp.positions[2] = cfg.capacity + 7
+    gpu = H.run_gpu(inp, fused=True)
+    assert gpu.err & RRA_ERR_POSITION
+    keep = [0, 1, 3]
+    assert gpu.out[keep].tobytes() == good.out[keep].tobytes()
+    inp.positions[:] = bad
