@@ -112,14 +112,23 @@ int make_plan(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
   if (requested > 0) {
     chunk_tiles = (tiles + requested - 1) / requested;
   } else {
-    // About two waves of resident CTAs (3 per SM for the mma kernel, 2 otherwise), each
-    // streaming 128..2048 tokens: fewer, longer CTAs pay their start-up and epilogue less
-    // often, while two waves keep the tail of ragged batches short.
-    const int64_t units = int64_t(B) * Hkv * (n_rep / p->hpc);
-    const int64_t target = 2 * (p->mma ? 3 : 2) * std::max(1, sm_count());
-    chunk_tiles = (tiles * units + target - 1) / target;
-    const int64_t lo = std::max(1, 128 / p->tile), hi = std::max(1, 2048 / p->tile);
-    chunk_tiles = std::min(std::max(chunk_tiles, lo), hi);
+    // CTAs that fit on the GPU at once: 3 per SM for the mma kernel, 2 otherwise.
+    const int64_t resident = (p->mma ? 3 : 2) * int64_t(std::max(1, sm_count()));
+    const int64_t units = std::max<int64_t>(1, int64_t(B) * Hkv * (n_rep / p->hpc));  // CTAs per split
+    if (2 * units <= resident) {
+      // Few sequences x heads: as many splits as fit in ONE wave (a second wave that is barely
+      // started costs a whole CTA time), each at least 256 tokens long.
+      const int64_t splits_one_wave = std::max<int64_t>(1, resident / units);
+      chunk_tiles = (tiles + splits_one_wave - 1) / splits_one_wave;
+      chunk_tiles = std::max<int64_t>(chunk_tiles, std::max(1, 256 / p->tile));
+    } else {
+      // Many sequences x heads: about two waves, each CTA streaming 128..2048 tokens; fewer,
+      // longer CTAs pay start-up and epilogue less often, two waves keep ragged tails short.
+      const int64_t target = 2 * resident;
+      chunk_tiles = (tiles * units + target - 1) / target;
+      const int64_t lo = std::max(1, 128 / p->tile), hi = std::max(1, 2048 / p->tile);
+      chunk_tiles = std::min(std::max(chunk_tiles, lo), hi);
+    }
   }
   chunk_tiles = std::min(std::max<int64_t>(chunk_tiles, 1), max_chunk_tiles);
   chunk_tiles = std::max<int64_t>(chunk_tiles, (tiles + rra::kMaxSplits - 1) / rra::kMaxSplits);
