@@ -239,7 +239,10 @@ def run_ours(args):
     cfg = workload_config(args)
     splits_arg = cfg.num_splits if args.num_splits < 0 else args.num_splits
     w, lengths = device_workload(cfg, cfg.seed + rank, device)
-    kv_bytes = cfg.kv_bytes(lengths)
+    # The numerator is the unique KV bytes DRAM must deliver: a shared prefix is counted once.
+    # Without prefix sharing this equals the logical bytes the attention consumes.
+    kv_bytes = cfg.unique_kv_bytes(lengths)
+    logical_bytes = cfg.kv_bytes(lengths)
     step = DecodeStep(cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, w["k_cache"], w["v_cache"],
                       w["block_table"], num_splits=splits_arg, rope_base=cfg.rope_base)
     # the fused step is one kernel for bf16 with the tensor-core path, else rope + decode
@@ -365,6 +368,8 @@ def run_ours(args):
             "seq_lens": (f"U[{cfg.len_range[0]},{cfg.len_range[1]}] mean {float(np.mean(lengths)):.1f}"
                          if cfg.len_range else cfg.seq_len),
             "num_splits": step.splits, "kv_bytes_per_step_per_gpu": kv_bytes,
+            "logical_kv_bytes_per_step_per_gpu": logical_bytes,
+            "logical_kv_gbs": round(logical_bytes * world / (ms * 1e-3) / 1e9, 2),
             "l2": ("flushed between steps (2x L2 write, outside the timed events)" if flush is not None
                    else f"inputs larger than L2 ({kv_bytes / 2**20:.0f} MiB KV per step vs 129 MiB L2)"),
             "parallelism": f"replicas x{world}",
@@ -421,7 +426,7 @@ def cpu_worker(workload: str, seconds: float):
     cfg = CONFIGS[workload]
     sample_batch = 1 if cfg.batch == 1 or cfg.layout == "contiguous" else 2
     inp = make_inputs(oracle_sample_config(cfg, sample_batch), seed=cfg.seed)
-    nbytes = cfg.kv_bytes(inp.lengths)
+    nbytes = cfg.unique_kv_bytes(inp.lengths)
     elapsed, done = 0.0, 0
     while elapsed < seconds or done == 0:
         elapsed += oracle_step_seconds(inp)
@@ -455,7 +460,7 @@ def run_reference(args):
     cfg = CONFIGS[args.workload]
     sample_batch = 1 if cfg.batch == 1 or cfg.layout == "contiguous" else 2
     inp = make_inputs(oracle_sample_config(cfg, sample_batch), seed=cfg.seed)
-    nbytes = cfg.kv_bytes(inp.lengths)
+    nbytes = cfg.unique_kv_bytes(inp.lengths)
     for _ in range(args.warmup):
         oracle_step_seconds(inp)
     secs = [oracle_step_seconds(inp) for _ in range(args.steps)]

@@ -22,6 +22,9 @@ Pages cited (by title and section):
   (§二 standard attention, §三 FlashAttention's default 1/sqrt(d_k) scale, §四
   KVCache.update / PagedKVCache / the cache-size formula, §六 GQA and n_rep).
 
+``oracle.quant`` adds the INT8 KV cache with per-head scales and a bf16 window of
+recent tokens ([KVC-GQA-RoPE] §4.3), with its readings stated in its header.
+
 Parity status: every function here is pinned by tests that do not retype it
 (library routines, complex-number rotation, brute force, closed forms and the
 pages' worked numbers); none is "parity unpinned".
@@ -34,3 +37,4 @@ from .kvcache import (append_contiguous, append_paged, logical_kv_contiguous,  #
 from .attention import (repeat_kv, softmax, attention, gqa_decode_attention,  # noqa: F401
                         causal_attention)
 from .decode import decode_step  # noqa: F401
+from . import quant  # noqa: F401

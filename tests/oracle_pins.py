@@ -261,6 +261,156 @@ def pin_kv_bytes_pages_numbers():
         assert round(100 * ratio) == int(pct), (hkv, ratio)
 
 
+# ---------------------------------------------------------------------------- INT8 cache + bf16 window
+def _f32(bits):
+    return float(np.array([bits], dtype=np.uint32).view(np.float32)[0])
+
+
+def pin_int8_quantize_exact_values():
+    # scale 0.5: every quotient is exact, so the code is fixed by the rounding rule alone
+    cases = [(0.0, 0), (1.25, 2), (1.75, 4), (-1.25, -2), (-1.75, -4), (3.0, 6), (63.25, 126),
+             (63.5, 127), (63.75, 127), (1000.0, 127), (-1000.0, -127), (-63.75, -127),
+             (math.inf, 127), (-math.inf, -127)]
+    got = oracle.quant.quantize_int8(np.array([c[0] for c in cases]), 0.5)
+    assert got.tolist() == [c[1] for c in cases], got
+    # the quotient is taken in float32: both are exact ties in float32 (10.5, -47.5, which go
+    # to the even code) but lie just off the tie in float64 (10.50000015, -47.4999997)
+    odd = [(0.76171875, _f32(0x3D949249), 10), (-2.046875, _f32(0x3D308159), -48)]
+    for x, sc, want in odd:
+        assert oracle.quant.quantize_int8(np.array([x]), sc)[0] == want, (x, sc)
+        assert float(torch.round(torch.tensor(x, dtype=torch.float32) / torch.tensor(sc, dtype=torch.float32))) == want
+
+
+def pin_int8_round_trip_bound():
+    rng = np.random.default_rng(12)
+    for sc in (0.5, 1.0 / 32, 0.0371, 3.0e-3):
+        s32 = float(np.float32(sc))
+        # multiples of a power-of-two scale come back exactly
+        if sc in (0.5, 1.0 / 32):
+            n = np.arange(-127, 128)
+            assert np.array_equal(oracle.quant.quantize_int8(n * s32, s32), n)
+        x = oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits(rng.uniform(-127.4, 127.4, 50000) * s32))
+        c = oracle.quant.quantize_int8(x, s32)
+        inside = np.abs(x) <= 127.0 * s32                  # bf16 rounding may push a few past the range
+        err = np.abs(oracle.quant.dequantize_int8(c, s32) - x)[inside]
+        assert inside.mean() > 0.99 and err.max() <= s32 * (0.5 + 2.0 ** -16), (sc, err.max() / s32)
+        assert np.all(np.abs(c[~inside]) == 127)
+        assert np.array_equal(oracle.quant.quantize_int8(-x, s32), -c)      # symmetric, no zero point
+        order = np.argsort(x, kind="stable")
+        assert np.all(np.diff(c[order].astype(int)) >= 0)                  # monotone
+        assert c.min() >= -127 and c.max() <= 127
+
+
+def _ring_from_tokens(tokens, window):
+    """[Hkv, L, D] tokens -> ring [Hkv, W, D] holding token t in slot t mod W (last W tokens)."""
+    hkv, L, d = tokens.shape
+    ring = np.full((hkv, window, d), np.uint16(0x7FC0), dtype=np.uint16)
+    for t in range(max(0, L - window), L):
+        ring[:, t % window] = tokens[:, t]
+    return ring
+
+
+def pin_q8_full_window_is_the_bf16_step():
+    # a window at least as long as the sequence: nothing is read from the INT8 cache
+    rng = np.random.default_rng(13)
+    B, hq, hkv, d, max_len, W = 3, 8, 2, 16, 40, 48
+    lens = np.array([1, 17, 40])
+    q = oracle.f64_to_bf16_bits(rng.standard_normal((B, hq, d)))
+    kc = oracle.f64_to_bf16_bits(rng.standard_normal((B, hkv, max_len, d)))
+    vc = oracle.f64_to_bf16_bits(rng.standard_normal((B, hkv, max_len, d)))
+    kw = np.stack([_ring_from_tokens(kc[b, :, : lens[b]], W) for b in range(B)])
+    vw = np.stack([_ring_from_tokens(vc[b, :, : lens[b]], W) for b in range(B)])
+    codes = np.full((B, hkv, max_len, d), -128, dtype=np.int8)             # never read
+    ones = np.ones(hkv, dtype=np.float32)
+    got = oracle.quant.decode_attention_q8(q, codes, codes, ones, ones, kw, vw, lens, W)
+    want = oracle.decode.decode_attention(q, kc, vc, lens, "bf16")
+    assert np.allclose(got, want, rtol=0, atol=1e-13)
+
+
+def pin_q8_without_window_reads_code_times_scale():
+    # no window: every token is code * s_h, gathered through a paged table; the reference
+    # cache is built element by element in Python and attended by the plain decode
+    rng = np.random.default_rng(14)
+    B, hq, hkv, d, bs = 2, 6, 3, 8, 4
+    lens = np.array([9, 13])
+    nper = 4
+    table = rng.permutation(B * nper + 3)[: B * nper].reshape(B, nper).astype(np.int32)
+    kcodes = rng.integers(-127, 128, size=(B * nper + 3, bs, hkv, d)).astype(np.int8)
+    vcodes = rng.integers(-127, 128, size=kcodes.shape).astype(np.int8)
+    ks = np.array([0.01, 0.02, 0.03], dtype=np.float32)
+    vs = np.array([0.5, 0.25, 0.125], dtype=np.float32)
+    q = oracle.f64_to_bf16_bits(rng.standard_normal((B, hq, d)))
+    ref_k = np.zeros((B, hkv, nper * bs, d))
+    ref_v = np.zeros_like(ref_k)
+    for b in range(B):
+        for t in range(lens[b]):
+            blk, off = table[b, t // bs], t % bs
+            for g in range(hkv):
+                for i in range(d):
+                    ref_k[b, g, t, i] = int(kcodes[blk, off, g, i]) * float(ks[g])
+                    ref_v[b, g, t, i] = int(vcodes[blk, off, g, i]) * float(vs[g])
+    got = oracle.quant.decode_attention_q8(q, kcodes, vcodes, ks, vs, None, None, lens, 0, table, bs)
+    want = oracle.decode.decode_attention(oracle.bf16_bits_to_f64(q), ref_k, ref_v, lens, "f64")
+    assert np.allclose(got, want, rtol=0, atol=1e-13)
+
+
+def _q8_stream(window, layout, style):
+    """Feed T tokens one step at a time through the quantised step; after each step compare with
+    brute-force attention over the mixed-precision definition, then check the stored codes and ring."""
+    rng = np.random.default_rng(15 + window)
+    T, hq, hkv, d, bs = 13, 4, 2, 8, 4
+    qs = oracle.f64_to_bf16_bits(rng.standard_normal((T, hq, d)))
+    ks = oracle.f64_to_bf16_bits(rng.standard_normal((T, hkv, d)) * 2)
+    vs = oracle.f64_to_bf16_bits(rng.standard_normal((T, hkv, d)) * 2)
+    k_scale = np.array([0.02, 0.05], dtype=np.float32)
+    v_scale = np.array([0.04, 0.03], dtype=np.float32)
+    if layout == "contiguous":
+        kc = np.full((1, hkv, T + 2, d), -128, dtype=np.int8)
+        table = None
+    else:
+        kc = np.full((2 * math.ceil(T / bs), bs, hkv, d), -128, dtype=np.int8)
+        table = rng.permutation(kc.shape[0])[: math.ceil(T / bs)][None, :].astype(np.int32)
+    vc = kc.copy()
+    kw = np.full((1, hkv, max(window, 1), d), np.uint16(0x7FC0), dtype=np.uint16)
+    vw = kw.copy()
+    # the exact (bf16) rotated k of every token at its own position, and raw v
+    k_exact = np.stack([oracle.f64_to_bf16_bits(oracle.apply_rope(oracle.bf16_bits_to_f64(ks[t]), np.array([[t]]),
+                                                                  style=style)) for t in range(T)])
+    for p in range(T):
+        q_rot = oracle.quant.rope_append_q8(qs[p][None], ks[p][None], vs[p][None], np.array([p]), kc, vc,
+                                            k_scale, v_scale, kw, vw, window, table, bs, rope_style=style)
+        out = oracle.quant.decode_attention_q8(q_rot, kc, vc, k_scale, v_scale, kw, vw, np.array([p + 1]), window,
+                                               table, bs)
+        L = p + 1
+        qr = oracle.bf16_bits_to_f64(q_rot[0])
+        for h in range(hq):
+            g = h // (hq // hkv)
+            keys, vals = [], []
+            for t in range(L):
+                kx = oracle.bf16_bits_to_f64(k_exact[t, g])
+                vx = oracle.bf16_bits_to_f64(vs[t, g])
+                if window == 0 or t < L - window:            # old token: its INT8 value
+                    kx = oracle.quant.quantize_int8(kx, k_scale[g]).astype(np.float64) * float(k_scale[g])
+                    vx = oracle.quant.quantize_int8(vx, v_scale[g]).astype(np.float64) * float(v_scale[g])
+                keys.append(list(kx))
+                vals.append(list(vx))
+            want = _loop_attention(list(qr[h]), keys, vals, 1 / math.sqrt(d))
+            assert np.allclose(out[0, h], want, rtol=0, atol=1e-12), (window, layout, p, h)
+    for t in range(T):                                         # every token's code sits in its slot
+        blk = (0, slice(None), t) if table is None else (table[0, t // bs], t % bs)
+        for g in range(hkv):
+            kcode = kc[blk][g] if table is not None else kc[0, g, t]
+            assert np.array_equal(kcode, oracle.quant.quantize_int8(oracle.bf16_bits_to_f64(k_exact[t, g]), k_scale[g]))
+    for t in range(max(0, T - window), T):                     # the last W tokens sit in ring slot t mod W
+        assert np.array_equal(kw[0, :, t % window], k_exact[t]) and np.array_equal(vw[0, :, t % window], vs[t])
+
+
+def pin_q8_stream_matches_mixed_precision():
+    for window in (0, 1, 3, 5):
+        for layout in ("contiguous", "paged"):
+            _q8_stream(window, layout, style=window % 2)
+
+
 ALL_PINS = [
     pin_bf16_exact_values, pin_bf16_matches_torch_cast,
     pin_rope_complex_rotation, pin_rope_relative_position, pin_rope_rotation_properties,
@@ -268,6 +418,8 @@ ALL_PINS = [
     pin_causal_attention_matches_torch_sdpa, pin_softmax_large_scores,
     pin_decode_equals_causal_rows, pin_paged_gather_order, pin_paged_equals_contiguous,
     pin_kv_bytes_pages_numbers,
+    pin_int8_quantize_exact_values, pin_int8_round_trip_bound, pin_q8_full_window_is_the_bf16_step,
+    pin_q8_without_window_reads_code_times_scale, pin_q8_stream_matches_mixed_precision,
 ]
 
 

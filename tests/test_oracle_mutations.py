@@ -81,7 +81,45 @@ def _logical_kv_contiguous_short(cache, b, length):
     return cache[b, :, : max(length - 1, 1), :]
 
 
+def _q8_half_away_from_zero(x, scale):
+    r = np.asarray(x, dtype=np.float32) / np.asarray(scale, dtype=np.float32)
+    return np.clip(np.sign(r) * np.floor(np.abs(r) + 0.5), -127, 127).astype(np.int8)
+
+
+def _q8_range_to_minus_128(x, scale):
+    r = np.asarray(x, dtype=np.float32) / np.asarray(scale, dtype=np.float32)
+    return np.clip(np.rint(r), -128, 127).astype(np.int8)
+
+
+def _q8_quotient_in_float64(x, scale):
+    r = np.asarray(x, dtype=np.float64) / np.asarray(scale, dtype=np.float32).astype(np.float64)
+    return np.clip(np.rint(r), -127, 127).astype(np.int8)
+
+
+def _q8_ring_slot_shifted(codes, scale, win, b, length, window, block_table=None, block_size=0):
+    n_old = max(0, length - window) if window > 0 else length
+    out = _ORIG_Q["logical_kv_q8"](codes, scale, win, b, n_old, 0, block_table, block_size)
+    if n_old == length:
+        return out
+    recent = np.stack([oracle.bf16_bits_to_f64(win[b, :, (t + 1) % window, :]) for t in range(n_old, length)], axis=1)
+    return np.concatenate([out, recent], axis=1)
+
+
+def _q8_window_one_short(codes, scale, win, b, length, window, block_table=None, block_size=0):
+    w = max(window - 1, 0) if window > 1 else window
+    return _ORIG_Q["logical_kv_q8"](codes, scale, win, b, length, w, block_table, block_size)
+
+
+def _q8_dequantize_without_scale(codes, scale):
+    return np.asarray(codes, dtype=np.float64)
+
+
+def _q8_v_with_k_scale(q, k_new, v_new, positions, k_codes, v_codes, k_scale, v_scale, *args, **kw):
+    return _ORIG_Q["rope_append_q8"](q, k_new, v_new, positions, k_codes, v_codes, k_scale, k_scale, *args, **kw)
+
+
 _ORIG = {n: getattr(oracle, n) for n in ("apply_rope", "attention", "append_contiguous")}
+_ORIG_Q = {n: getattr(oracle.quant, n) for n in ("logical_kv_q8", "rope_append_q8")}
 
 MUTATIONS = {
     "rope rotates the wrong way": ("apply_rope", _rope_sign_flip),
@@ -95,6 +133,13 @@ MUTATIONS = {
     "kv bytes without the K+V factor 2": ("kv_cache_bytes", _kv_bytes_no_factor_two),
     "bf16 rounded through fp32": ("f64_to_bf16_bits", _bf16_double_rounding),
     "attention drops the newest token": ("logical_kv_contiguous", _logical_kv_contiguous_short),
+    "int8 rounds half away from zero": ("quantize_int8", _q8_half_away_from_zero),
+    "int8 codes reach -128": ("quantize_int8", _q8_range_to_minus_128),
+    "int8 quotient taken in float64": ("quantize_int8", _q8_quotient_in_float64),
+    "window ring read one slot off": ("logical_kv_q8", _q8_ring_slot_shifted),
+    "window one token short": ("logical_kv_q8", _q8_window_one_short),
+    "dequantisation drops the scale": ("dequantize_int8", _q8_dequantize_without_scale),
+    "v quantised with the k scales": ("rope_append_q8", _q8_v_with_k_scale),
 }
 
 

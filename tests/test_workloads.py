@@ -9,6 +9,8 @@ from workloads import CONFIGS, make_inputs, reduced
 
 
 def _finite(x, dtype):
+    if x.dtype == np.int8:                                   # INT8 codes: -128 is the poison
+        return x != -128
     if dtype == "bf16":
         return (x & 0x7F80) != 0x7F80
     return np.isfinite(x)
@@ -35,10 +37,19 @@ def test_reduced_inputs_structure(name):
         assert getattr(a, f).tobytes() == getattr(b, f).tobytes()
     assert np.array_equal(a.positions, a.lengths - 1)
     L = a.lengths
+    # slots read from the main cache: [0, first); the new token's slot and the window are poisoned
+    first = [max(0, int(x) - max(cfg.window, 1)) if cfg.int8 else int(x) - 1 for x in L]
+    if cfg.int8 and cfg.window:
+        W = cfg.window
+        for bb in range(cfg.batch):
+            live = [t % W for t in range(max(0, int(L[bb]) - W), int(L[bb]) - 1)]   # older window tokens
+            assert _finite(a.k_win[bb][:, live], "bf16").all()
+            dead = sorted(set(range(W)) - set(live))
+            assert (int(L[bb]) - 1) % W in dead and not _finite(a.v_win[bb][:, dead], "bf16").any()
     if cfg.layout == "contiguous":
         for bb in range(cfg.batch):
-            assert _finite(a.k_cache[bb, :, : L[bb] - 1], cfg.dtype).all()
-            assert not _finite(a.k_cache[bb, :, L[bb] - 1:], cfg.dtype).any()
+            assert _finite(a.k_cache[bb, :, : first[bb]], cfg.dtype).all()
+            assert not _finite(a.k_cache[bb, :, first[bb]:], cfg.dtype).any()
         return
     bs, t = cfg.block_size, a.block_table
     n_shared = cfg.shared_prefix_tokens // bs
@@ -49,10 +60,10 @@ def test_reduced_inputs_structure(name):
         assert np.all(t[bb, nb:] == -1)
         assert np.array_equal(t[bb, :n_shared], t[0, :n_shared])
         owned.extend(t[bb, n_shared:nb].tolist())
-        for tok in range(int(L[bb]) - 1):                   # every cached token is finite
+        for tok in range(first[bb]):                        # every token read from the cache is finite
             assert _finite(a.k_cache[t[bb, tok // bs], tok % bs], cfg.dtype).all()
-        last = t[bb, (L[bb] - 1) // bs]
-        assert not _finite(a.v_cache[last, (L[bb] - 1) % bs:], cfg.dtype).any()
+        for tok in range(max(first[bb], n_shared * bs), int(L[bb])):   # the rest of the sequence is poisoned
+            assert not _finite(a.v_cache[t[bb, tok // bs], tok % bs], cfg.dtype).any()
     owned.extend(t[0, :n_shared].tolist())
     assert len(owned) == len(set(owned))                     # private blocks are never shared
     unused = np.setdiff1d(np.arange(cfg.num_blocks), owned)

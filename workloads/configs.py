@@ -29,6 +29,8 @@ class WorkloadConfig:
     max_blocks_per_seq: int = 0     # paged: columns of the block table
     shared_prefix_tokens: int = 0   # paged: leading tokens of every sequence mapped to the same blocks
     num_splits: int = 0             # split-K chunks per sequence; 0 lets the library choose
+    kv_dtype: str = ""              # "" = the caches hold ``dtype``; "int8" = INT8 codes + per-head scales
+    window: int = 0                 # int8 only: recent tokens also kept in a bf16 ring of this many slots
     rope_base: float = 10000.0
     seed: int = 0
     description: str = ""
@@ -48,13 +50,28 @@ class WorkloadConfig:
             return self.max_len
         return self.max_blocks_per_seq * self.block_size
 
+    @property
+    def int8(self) -> bool:
+        return self.kv_dtype == "int8"
+
     def kv_bytes(self, lengths) -> int:
-        """Algorithmic K+V bytes one decode step streams: 2 * sum_b L_b * Hkv * D * elem."""
-        return 2 * int(sum(int(x) for x in lengths)) * self.n_kv_heads * self.head_dim * self.elem_bytes
+        """Algorithmic K+V bytes one decode step streams: 2 * sum_b L_b * Hkv * D * elem.
+
+        INT8 caches: the tokens older than the window cost 1 byte per element, the (at most
+        ``window``) most recent ones 2 bytes (bf16 ring); the per-head scales are not counted.
+        """
+        row = 2 * self.n_kv_heads * self.head_dim
+        if self.int8:
+            total = 0
+            for x in lengths:
+                recent = min(int(x), self.window)
+                total += (int(x) - recent) * row + recent * row * 2
+            return total
+        return int(sum(int(x) for x in lengths)) * row * self.elem_bytes
 
     def unique_kv_bytes(self, lengths) -> int:
         """K+V bytes with the shared prefix counted once (equals kv_bytes without sharing)."""
-        if not self.shared_prefix_tokens:
+        if not self.shared_prefix_tokens or self.int8:
             return self.kv_bytes(lengths)
         p = self.shared_prefix_tokens
         toks = p + sum(int(x) - p for x in lengths)
@@ -93,6 +110,17 @@ for _hkv in (32, 8, 1):
         description=f"MHA/GQA/MQA sweep, n_kv {_hkv}: batch 16, 32 q heads, D 128, context 8192, "
                     "first 2048 tokens on 128 shared blocks, block 16")
 
+# The INT8 cache ([KVC-GQA-RoPE] §4.3): the batch-64 paged and 128K workloads with INT8 codes,
+# per-head scales and the 128 most recent tokens kept in bf16.
+CONFIGS["batched_paged_int8"] = dataclasses.replace(
+    CONFIGS["batched_paged"], name="batched_paged_int8", kv_dtype="int8", window=128,
+    description="batched paged decode, INT8 KV cache (per-head scales) + 128-token bf16 window: batch 64, "
+                "32q/8kv, D 128, L_b ~ U[512,8192], block 16, pool 40000")
+CONFIGS["long_context_int8"] = dataclasses.replace(
+    CONFIGS["long_context"], name="long_context_int8", kv_dtype="int8", window=128, num_splits=0,
+    description="long-context decode, INT8 KV cache (per-head scales) + 128-token bf16 window: batch 1, "
+                "32q/8kv, D 128, context 131072, block 32")
+
 
 def get_config(name: str) -> WorkloadConfig:
     return CONFIGS[name]
@@ -129,4 +157,6 @@ def reduced(cfg: WorkloadConfig, factor: int = 16, batch: Optional[int] = None) 
         kw["num_blocks"] = max(need + 7, shrink(cfg.num_blocks, need + 7))
     if cfg.num_splits:
         kw["num_splits"] = max(2, cfg.num_splits // factor)
+    if cfg.window:
+        kw["window"] = max(16, (cfg.window // factor) // 8 * 8)
     return WorkloadConfig(**kw)

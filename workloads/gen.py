@@ -21,6 +21,16 @@ no table references, and in each sequence's last block the slots at positions
 out-of-range read shows up as NaN in the output.
 
 bf16 arrays are carried as ``uint16`` bit patterns, fp32 as ``float32``.
+
+INT8 caches (``kv_dtype == "int8"``): steps 1-3 are unchanged; step 4 draws the K then the V
+cache as integer codes ``clip(rint(32 * standard_normal(float32)), -127, 127)`` (N(0,1)
+values at a resolution of 1/32), then, with a window of W slots, the K then the V ring
+[B, Hkv, W, D] as bf16 N(0,1). The per-head scales are fixed, not drawn:
+k_scale[h] = (1 + (h % 4) / 8) / 32 and v_scale[h] = (1 + ((h + 2) % 4) / 8) / 32 (float32).
+Poisoning: -128 (a code quantisation never produces) in every cache slot the step must not
+read -- slots t >= max(0, L_b - max(W, 1)), i.e. the new token's slot and every slot the
+window covers -- and in every unreferenced block; NaN in the ring slot the new token will
+overwrite ((L_b - 1) mod W) and, while L_b - 1 < W, in the ring slots not yet filled.
 """
 
 from __future__ import annotations
@@ -65,9 +75,15 @@ class DecodeInputs:
     k_cache: np.ndarray            # contiguous [B, Hkv, max_len, D] or pool [num_blocks, bs, Hkv, D]
     v_cache: np.ndarray
     block_table: Optional[np.ndarray] = None   # int32 [B, max_blocks_per_seq], paged only
+    k_scale: Optional[np.ndarray] = None       # int8 only: float32 [Hkv]
+    v_scale: Optional[np.ndarray] = None
+    k_win: Optional[np.ndarray] = None         # int8 with a window: bf16 ring [B, Hkv, W, D]
+    v_win: Optional[np.ndarray] = None
 
     @property
     def nan_value(self):
+        if self.cfg.int8:
+            return np.int8(-128)
         return BF16_NAN if self.cfg.dtype == "bf16" else np.float32(np.nan)
 
 
@@ -114,14 +130,35 @@ def make_inputs(cfg: WorkloadConfig, seed: Optional[int] = None, poison: bool = 
         shape = (B, Hkv, cfg.max_len, D)
     else:
         shape = (cfg.num_blocks, cfg.block_size, Hkv, D)
-    k_cache = _normal_storage(rng, shape, cfg.dtype)
-    v_cache = _normal_storage(rng, shape, cfg.dtype)
+    extra = {}
+    if cfg.int8:
+        k_cache = _int8_codes(rng, shape)
+        v_cache = _int8_codes(rng, shape)
+        h = np.arange(Hkv)
+        extra["k_scale"] = ((1.0 + (h % 4) / 8.0) / 32.0).astype(np.float32)
+        extra["v_scale"] = ((1.0 + ((h + 2) % 4) / 8.0) / 32.0).astype(np.float32)
+        if cfg.window:
+            extra["k_win"] = _normal_storage(rng, (B, Hkv, cfg.window, D), "bf16")
+            extra["v_win"] = _normal_storage(rng, (B, Hkv, cfg.window, D), "bf16")
+    else:
+        k_cache = _normal_storage(rng, shape, cfg.dtype)
+        v_cache = _normal_storage(rng, shape, cfg.dtype)
     inp = DecodeInputs(cfg=cfg, lengths=lengths, positions=(lengths - 1).astype(np.int32),
                        q=q, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache,
-                       block_table=table)
+                       block_table=table, **extra)
     if poison:
         poison_unread(inp)
     return inp
+
+
+def _int8_codes(rng: np.random.Generator, shape) -> np.ndarray:
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.int8)
+    for s in range(0, n, _CHUNK):
+        e = min(n, s + _CHUNK)
+        x = rng.standard_normal(e - s, dtype=np.float32)
+        out[s:e] = np.clip(np.rint(x * 32.0), -127, 127)
+    return out.reshape(shape)
 
 
 def make_structure(cfg: WorkloadConfig, seed: Optional[int] = None):
@@ -137,21 +174,32 @@ def make_structure(cfg: WorkloadConfig, seed: Optional[int] = None):
 
 
 def poison_unread(inp: DecodeInputs) -> None:
-    """Write NaN into every cache slot the step must not read before its append."""
+    """Write NaN (INT8: -128) into every cache slot the step must not read before its append."""
     cfg, nan = inp.cfg, inp.nan_value
+    # first slot not read from the main cache: the new token's, or the window's first
+    first = [max(0, int(L) - max(cfg.window, 1)) if cfg.int8 else int(L) - 1 for L in inp.lengths]
+    if cfg.int8 and cfg.window:
+        W = cfg.window
+        for b, L in enumerate(inp.lengths):
+            for ring in (inp.k_win, inp.v_win):
+                ring[b, :, (int(L) - 1) % W, :] = BF16_NAN
+                if int(L) - 1 < W:
+                    ring[b, :, int(L) - 1:, :] = BF16_NAN
     if cfg.layout == "contiguous":
         for b, L in enumerate(inp.lengths):
-            inp.k_cache[b, :, L - 1:, :] = nan
-            inp.v_cache[b, :, L - 1:, :] = nan
+            inp.k_cache[b, :, first[b]:, :] = nan
+            inp.v_cache[b, :, first[b]:, :] = nan
         return
     bs = cfg.block_size
     used = np.zeros(cfg.num_blocks, dtype=bool)
     for b, L in enumerate(inp.lengths):
         nb = math.ceil(int(L) / bs)
         used[inp.block_table[b, :nb]] = True
-        last = inp.block_table[b, (L - 1) // bs]
-        off = (L - 1) % bs
-        inp.k_cache[last, off:] = nan
-        inp.v_cache[last, off:] = nan
+        n_shared = cfg.shared_prefix_tokens // bs
+        for t0 in range(first[b] - first[b] % bs, int(L), bs):   # blocks from the first unread slot on
+            blk, off = inp.block_table[b, t0 // bs], max(first[b] - t0, 0)
+            if t0 // bs >= n_shared:
+                inp.k_cache[blk, off:] = nan
+                inp.v_cache[blk, off:] = nan
     inp.k_cache[~used] = nan
     inp.v_cache[~used] = nan
