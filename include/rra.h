@@ -169,6 +169,65 @@ RRA_API int rra_decode_step_paged(const void* q, const void* k_new, const void* 
                                   void* workspace, size_t ws_bytes, rra_dtype dt, int32_t* err_flag,
                                   void* stream);
 
+/* --- INT8 KV cache with per-head scales and a bf16 window of recent tokens ---
+ *
+ * [KVC-GQA-RoPE] §4.3: K and V cached as INT8 instead of BF16 (half the bytes), with
+ * quantisation parameters calibrated per attention head, and the most recent tokens kept at
+ * high precision. The page gives no formula; these calls implement:
+ *   - codes: int8 c = clamp(round_half_even(x / s_g), -127, 127) for a value x of KV head g,
+ *     the quotient an IEEE float32 division; the value is c * s_g. x is the rotated k rounded
+ *     to bf16, or v. -128 is never written. k_scale, v_scale: float32 [Hkv] on the device,
+ *     positive and finite (calibrated by the caller; not checked).
+ *   - code caches: contiguous (block_table == NULL) k_codes, v_codes int8 [B, Hkv, max_len, D]
+ *     (max_len at least 16384 / D tokens), or paged pools int8 [num_blocks, block_size, Hkv, D]
+ *     (block_size a power of two >= 8) addressed through block_table as in the bf16 calls.
+ *   - window W (0, or a multiple of 8 up to 65536): k_win, v_win bf16 [B, Hkv, W, D] rings;
+ *     token t of sequence b lives in slot t % W. Every appended token is quantised into its
+ *     cache slot AND, with W > 0, written in bf16 to its ring slot. Attention over L_b tokens
+ *     reads tokens [0, L_b - W) from the codes and the last min(L_b, W) tokens from the ring.
+ *     With W == 0 the rings are not used (may be NULL).
+ *   - q, k_new, v_new, q_out, out are bf16; everything else as in the bf16 calls.
+ */
+
+/* rra_rope_append on an INT8 cache: RoPE on q and k_new at positions[b], then the quantised
+ * rotated k and v into cache slot positions[b] and their bf16 values into ring slot
+ * positions[b] % W. */
+RRA_API int rra_rope_append_q8(const void* q, const void* k_new, const void* v_new, const int32_t* positions,
+                               void* q_out, void* k_codes, void* v_codes, const float* k_scale,
+                               const float* v_scale, void* k_win, void* v_win, int window,
+                               const int32_t* block_table, int max_blocks_per_seq, int block_size,
+                               int num_blocks, int max_len, int B, int Hq, int Hkv, int D, double rope_base,
+                               int rope_style, int32_t* err_flag, void* stream);
+
+/* Attention of q_rot over the L_b = seq_lens[b] tokens of the mixed-precision cache (codes
+ * times scales, then the window's bf16 tokens), split-K as rra_decode_attn_paged. The INT8
+ * tokens are cut into splits (num_splits, 0 = chosen by the library) and the ring is one more
+ * partial; the workspace must hold rra_decode_workspace_bytes(B, Hq, D,
+ * rra_decode_q8_num_splits(...)) bytes, with the same zero-fill rule. */
+RRA_API int rra_decode_attn_q8(const void* q_rot, const void* k_codes, const void* v_codes, const float* k_scale,
+                               const float* v_scale, const void* k_win, const void* v_win, int window,
+                               const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                               int block_size, int num_blocks, int max_len, void* out, int B, int Hq, int Hkv,
+                               int D, float scale, int num_splits, void* workspace, size_t ws_bytes,
+                               int32_t* err_flag, void* stream);
+
+/* The whole step on an INT8 cache in one kernel: RoPE on q and k_new at positions[b], the
+ * quantised append (and ring write) of the new token, and the attention over L_b =
+ * positions[b] + 1 tokens. q_out receives q_rot and must not overlap q. */
+RRA_API int rra_decode_step_q8(const void* q, const void* k_new, const void* v_new, const int32_t* positions,
+                               void* q_out, void* k_codes, void* v_codes, const float* k_scale,
+                               const float* v_scale, void* k_win, void* v_win, int window,
+                               const int32_t* block_table, int max_blocks_per_seq, int block_size,
+                               int num_blocks, int max_len, void* out, int B, int Hq, int Hkv, int D,
+                               double rope_base, int rope_style, float scale, int num_splits, void* workspace,
+                               size_t ws_bytes, int32_t* err_flag, void* stream);
+
+/* Partial slots the INT8 decode uses (INT8 splits, plus one for the ring when window > 0):
+ * the `splits` argument of rra_decode_workspace_bytes. max_tokens and block_size as in
+ * rra_decode_num_splits. Negative rra_status on bad arguments. */
+RRA_API int rra_decode_q8_num_splits(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
+                                     int num_splits, int window);
+
 /* Bytes of a K+V cache: 2 * n_layers * n_kv_heads * head_dim * seq_len * batch * dtype_bytes
  * ([Opt-2026] §四 memory formula; [KVC-GQA-RoPE] §5.3). Host only; returns 0 when an
  * argument is negative or the product overflows 64 bits. */

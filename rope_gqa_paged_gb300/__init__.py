@@ -10,6 +10,7 @@ from .rra import (RRA_BF16, RRA_ERR_BLOCK_ID, RRA_ERR_POSITION, RRA_ERR_SEQ_LEN,
                   RRA_F32, RraError, lib, lib_path, rra_decode_attn_contig, rra_decode_attn_paged,
                   rra_decode_num_splits, rra_decode_step_contig, rra_decode_step_paged, rra_decode_workspace_bytes,
                   rra_kv_bytes, rra_rope_append,
-                  rra_status_str)
-from .step import DecodeStep  # noqa: F401
+                  rra_status_str, rra_rope_append_q8, rra_decode_attn_q8, rra_decode_step_q8,
+                  rra_decode_q8_num_splits)
+from .step import DecodeStep, DecodeStepQ8  # noqa: F401
 from ._build import build  # noqa: F401

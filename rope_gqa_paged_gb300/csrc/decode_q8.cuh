@@ -1,0 +1,610 @@
+// Split-K GQA decode attention over an INT8 KV cache with per-KV-head scales and a bf16 window
+// of recent tokens, on the tensor cores.
+//
+// "Transformer推理核心：KV Cache、GQA与RoPE原理与工程实践" §4.3: K and V cached as INT8 with
+// quantisation parameters calibrated per attention head, the most recent tokens kept at high
+// precision. Here a KV head g holds codes c with value c * s_g (K and V each with their own
+// scale), and the W most recent tokens of every sequence also sit in a bf16 ring of W slots
+// (token t in slot t mod W). Attention over L tokens reads tokens [0, L - W) as codes and the
+// last min(L, W) tokens from the ring; the softmax and the split/merge are those of
+// decode_mma.cuh.
+//
+// Work units: the INT8 tokens are cut into splits of `chunk` tokens as in the bf16 kernel; with
+// a window, one more unit per (sequence, KV head, head slice) streams the ring (the last grid
+// column). Each unit publishes one partial and the last to finish merges them.
+//
+// INT8 tiles (K and V, 16 KB each per stage, D-byte rows with the TMA swizzle) go through the
+// tensor cores as f16: ldmatrix loads 4 codes per lane, a byte permute places each code under
+// the f16 exponent of 1024 (0x64xx = 1024 + byte) after flipping its sign bit, and one f16x2
+// subtraction of 1152 leaves the code exactly. The dimension order inside each 16-dim slice is
+// permuted so the loaded bytes are already in mma fragment order:
+//   scores  S^T[16 tok x 8 heads] = C_K[16 tok x D] . Q'^T   with lane (g, t) holding dims
+//           4t..4t+3 of a slice as k = {2t, 2t+1, 2t+8, 2t+9} (q loaded in the same order);
+//   output  O^T[D x 8 heads] += C_V^T . P   with ldmatrix.trans giving lane (g, t) dims
+//           2g, 2g+1 of tokens 2t, 2t+1 (and +8), so fragment row g is dim 2g and row g+8 is
+//           dim 2g+1 of each 16-dim slice.
+// q is taken to f16 after a per-head power-of-two scaling (largest |q| in [2^14, 2^15)), exact
+// for bf16 values; the scores are multiplied by s_K * scale * log2(e) * 2^-e_h in float32 and
+// the output by s_V, so the only roundings are those of the f16 probabilities and the float32
+// accumulation.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "decode_mma.cuh"
+
+namespace rra {
+
+template <int D>
+struct Q8Cfg {
+  static constexpr int kTile = 16384 / D;          // INT8 tokens per stage (K 16 KB + V 16 KB)
+  static constexpr int kTileBytes = kTile * D;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static_assert(kStageBytes == MmaCfg<D>::kStageBytes, "window tiles reuse the INT8 stages");
+  static constexpr int kStages = MmaCfg<D>::kStages;
+  static constexpr int kConsumerWarps = 4;
+  static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+  static constexpr int kWarpTokens = kTile / kConsumerWarps;
+  static constexpr int kSteps = kWarpTokens / 16;
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  // after the ring: full[kStages], empty[kStages], appended; the block-id table; cos/sin
+  // hi/lo [4][D/2] floats; the rotated q rows [8][D] bf16 (fused step)
+  static constexpr int kOffBar = kRingBytes;
+  static constexpr int kOffTable = kOffBar + (2 * kStages + 1) * 8;
+  static constexpr int kOffCs = kOffTable + kMmaTableEntries * 4;
+  static constexpr int kOffQ = kOffCs + 4 * (D / 2) * 4;
+  static constexpr int kSmemBytes = 1024 + kOffQ + MmaCfg<D>::kMaxHeads * D * 2;
+};
+
+// Byte offset of 16-byte chunk c of row r in a tile of D-byte rows written by TMA with the
+// 128-byte (D = 128) or 64-byte (D = 64) swizzle.
+template <int D>
+__device__ __forceinline__ uint32_t swz8(int r, int c) {
+  if constexpr (D == 128) return swz(r, c);
+  return (r << 6) + ((((r >> 1) ^ c) & 3) << 4);
+}
+
+__device__ __forceinline__ uint32_t f16x2_minus_1152(uint32_t x) {
+  uint32_t y;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(y) : "r"(x), "r"(0x64806480u));
+  return y;
+}
+
+// Four INT8 codes (bytes 0..3 of w) as exact f16 pairs (bytes 0,1) and (bytes 2,3).
+__device__ __forceinline__ void s8x4_to_f16_01_23(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;  // code + 128 as an unsigned byte
+  lo = f16x2_minus_1152(__byte_perm(u, 0x64646464u, 0x5140));
+  hi = f16x2_minus_1152(__byte_perm(u, 0x64646464u, 0x7362));
+}
+
+// The same codes as f16 pairs (bytes 0,2) and (bytes 1,3).
+__device__ __forceinline__ void s8x4_to_f16_02_13(uint32_t w, uint32_t& ev, uint32_t& od) {
+  const uint32_t u = w ^ 0x80808080u;
+  ev = f16x2_minus_1152(__byte_perm(u, 0x64646464u, 0x5240));
+  od = f16x2_minus_1152(__byte_perm(u, 0x64646464u, 0x5341));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// One 16-token slice of an INT8 stage for one warp; `mult[j]` turns the raw score of owned
+// head 2*(lane%4)+j into log2 units. CHECK: tokens at or past `valid` get probability 0 (the
+// codes are finite whatever the bytes, so nothing needs clearing).
+template <int D, bool CHECK>
+__device__ __forceinline__ void q8_step(MmaWarpState<D>& st, const uint32_t (&qh)[D / 16][2], const float (&mult)[2],
+                                        uint32_t k_base, uint32_t v_base, int t0, int valid, int lane) {
+  const int mat = lane >> 3;
+  const int r = t0 + (lane & 7) + ((mat & 1) << 3);  // matrices: tokens 0-7 / 8-15 of chunk 2cc, then 2cc+1
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t w[4], a[4];
+    ldsm_x4(k_base + swz8<D>(r, 2 * cc + (mat >> 1)), w);
+    s8x4_to_f16_01_23(w[0], a[0], a[2]);
+    s8x4_to_f16_01_23(w[1], a[1], a[3]);
+    mma_f16(s, a, qh[2 * cc][0], qh[2 * cc][1]);
+    s8x4_to_f16_01_23(w[2], a[0], a[2]);
+    s8x4_to_f16_01_23(w[3], a[1], a[3]);
+    mma_f16(s, a, qh[2 * cc + 1][0], qh[2 * cc + 1][1]);
+  }
+  const int ta = t0 + (lane >> 2), tb = ta + 8;
+  float x[2][2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    x[j][0] = (!CHECK || ta < valid) ? s[j] * mult[j] : -INFINITY;
+    x[j][1] = (!CHECK || tb < valid) ? s[2 + j] * mult[j] : -INFINITY;
+  }
+  float mnew[2];
+  bool grow = false;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float mx = fmaxf(x[j][0], x[j][1]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    mnew[j] = fmaxf(st.m[j], mx);
+    grow |= mnew[j] > st.m[j];
+  }
+  if (__any_sync(0xffffffffu, grow)) {
+    float alpha[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      alpha[j] = mnew[j] > st.m[j] ? exp2f(st.m[j] - mnew[j]) : 1.f;
+      st.l[j] *= alpha[j];
+      st.m[j] = mnew[j];
+    }
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      st.o[i][0] *= alpha[0];
+      st.o[i][1] *= alpha[1];
+      st.o[i][2] *= alpha[0];
+      st.o[i][3] *= alpha[1];
+    }
+  }
+  float p[2][2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float mref = st.m[j] == -INFINITY ? 0.f : st.m[j];
+    p[j][0] = exp2f(x[j][0] - mref);
+    p[j][1] = exp2f(x[j][1] - mref);
+    st.l[j] += p[j][0] + p[j][1];
+  }
+  const uint32_t b0 = movmatrix_trans(pack_f16x2(p[0][0], p[1][0]));
+  const uint32_t b1 = movmatrix_trans(pack_f16x2(p[0][1], p[1][1]));
+#pragma unroll
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t w[4], a[4];
+    ldsm_x4_trans(v_base + swz8<D>(r, 2 * cc + (mat >> 1)), w);
+    s8x4_to_f16_02_13(w[0], a[0], a[1]);
+    s8x4_to_f16_02_13(w[1], a[2], a[3]);
+    mma_f16(st.o[2 * cc], a, b0, b1);
+    s8x4_to_f16_02_13(w[2], a[0], a[1]);
+    s8x4_to_f16_02_13(w[3], a[2], a[3]);
+    mma_f16(st.o[2 * cc + 1], a, b0, b1);
+  }
+}
+
+template <int D, bool PAGED, bool FUSED>
+__global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
+    decode_q8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+                     const __grid_constant__ CUtensorMap kw_map, const __grid_constant__ CUtensorMap vw_map,
+                     const DecodeArgs a) {
+  using C = Q8Cfg<D>;
+  using M = MmaCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int n_rep = a.Hq / a.Hkv;
+  const int hpc = a.hpc;
+  const int slices = n_rep / hpc;
+  const int split = blockIdx.x / slices;
+  const int g = blockIdx.y;
+  const int h0 = g * n_rep + (blockIdx.x - split * slices) * hpc;
+  const int b = blockIdx.z;
+  const bool has_win = a.window > 0;
+  const bool win_unit = has_win && split == a.num_splits - 1;
+
+  int L;
+  if constexpr (FUSED) {
+    const int pos = a.positions[b];
+    if (pos < 0 || pos >= a.capacity) {  // nothing is written for this sequence
+      if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) flag_error(a.err, RRA_ERR_POSITION);
+      return;
+    }
+    L = pos + 1;
+  } else {
+    L = a.seq_lens[b];
+    if (L < 0 || L > a.capacity) {
+      if (threadIdx.x == 0 && blockIdx.x == 0 && g == 0) flag_error(a.err, RRA_ERR_SEQ_LEN);
+      L = min(max(L, 0), a.capacity);
+    }
+  }
+  const int Lw = has_win ? min(L, a.window) : 0;  // tokens read from the ring
+  const int Lq = L - Lw;                          // tokens read as INT8 codes
+  const int nq = (Lq + a.chunk - 1) / a.chunk;
+  const int n_work = nq + (Lw > 0 ? 1 : 0);
+  int start, end, part;
+  if (win_unit) {
+    if (Lw == 0) return;
+    start = 0;
+    end = Lw;
+    part = nq;
+  } else {
+    start = split * a.chunk;
+    if (start >= Lq) {
+      if (L == 0 && split == 0) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(b) * a.Hq + h0) * D;
+        for (int i = threadIdx.x; i < hpc * D; i += blockDim.x) out[i] = __float2bfloat16_rn(0.f);
+      }
+      return;
+    }
+    end = min(Lq, start + a.chunk);
+    part = split;
+  }
+  const int rows = win_unit ? min(M::kTile, a.window) : C::kTile;  // tokens per stage of this unit
+  const int n_tiles = (end - start + rows - 1) / rows;
+  // Fused step: the unit that reads the new token writes it first (the window unit, else the
+  // INT8 unit whose chunk ends at L); the unit whose warp 0 publishes q_rot always has tokens.
+  const bool appender = FUSED && (has_win ? win_unit : end == L);
+  const bool publisher = FUSED && (has_win ? win_unit : split == 0);
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* appended = empty + C::kStages;
+  int32_t* tbl = reinterpret_cast<int32_t*>(smem + C::kOffTable);
+  float* cs = reinterpret_cast<float*>(smem + C::kOffCs);
+  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(smem + C::kOffQ);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::kConsumerWarps);
+    }
+    mbar_init(appended, 1);
+    fence_barrier_init();
+  }
+  int first_blk = 0;
+  if (PAGED && !win_unit) {
+    first_blk = start >> a.log2_bs;
+    const int n_blk = ((end - 1) >> a.log2_bs) - first_blk + 1;
+    const int32_t* row = a.block_table + static_cast<size_t>(b) * a.max_blocks_per_seq + first_blk;
+    for (int i = threadIdx.x; i < n_blk; i += blockDim.x) {
+      int id = row[i];
+      if (id < 0 || id >= a.num_blocks) {
+        flag_error(a.err, RRA_ERR_BLOCK_ID);
+        id = 0;
+      }
+      tbl[i] = id;
+    }
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------------ producer
+  if (warp == C::kConsumerWarps) {
+    if (lane == 0) {
+      if (win_unit) {
+        prefetch_tensormap(&kw_map);
+        prefetch_tensormap(&vw_map);
+      } else {
+        prefetch_tensormap(&k_map);
+        prefetch_tensormap(&v_map);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_tiles; ++it) {
+        const int s = it % C::kStages;
+        if (it >= C::kStages && !mbar_wait(&empty[s], ((it / C::kStages) - 1) & 1)) {
+          flag_error(a.err, RRA_ERR_TIMEOUT);
+          break;
+        }
+        // the new token: in the ring (any tile of it) or in the last INT8 tile of the appender
+        if (appender && (win_unit ? it == 0 : it == n_tiles - 1) && !mbar_wait(appended, 0)) {
+          flag_error(a.err, RRA_ERR_TIMEOUT);
+          break;
+        }
+        const int t0 = start + it * rows;
+        uint8_t* kst = smem + s * C::kStageBytes;
+        if (win_unit) {  // bf16 ring rows [t0, t0 + rows) of (b, g) in 64-dim halves
+          uint8_t* vst = kst + M::kHalves * M::kHalfBytes;
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * M::kHalves * rows * 128));
+          const int bg = b * a.Hkv + g;
+#pragma unroll
+          for (int h = 0; h < M::kHalves; ++h) {
+            tma_g2s_3d(kst + h * M::kHalfBytes, &kw_map, 64 * h, t0, bg, &full[s]);
+            tma_g2s_3d(vst + h * M::kHalfBytes, &vw_map, 64 * h, t0, bg, &full[s]);
+          }
+        } else {
+          uint8_t* vst = kst + C::kTileBytes;
+          if constexpr (PAGED) {
+            const int bs = 1 << a.log2_bs;
+            if (bs <= C::kTile) {  // whole blocks, one box of bs rows per block
+              const int n = min(C::kTile, end - t0);
+              const int nblk = (n + bs - 1) >> a.log2_bs;
+              mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * nblk * bs * D));
+              const int j0 = (t0 >> a.log2_bs) - first_blk;
+              for (int jb = 0; jb < nblk; ++jb) {
+                const int phys = tbl[j0 + jb];
+                tma_g2s_4d(kst + jb * bs * D, &k_map, 0, g, 0, phys, &full[s]);
+                tma_g2s_4d(vst + jb * bs * D, &v_map, 0, g, 0, phys, &full[s]);
+              }
+            } else {  // a kTile-row window of one block
+              const int phys = tbl[(t0 >> a.log2_bs) - first_blk];
+              const int off = t0 & (bs - 1);
+              mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * C::kTileBytes));
+              tma_g2s_4d(kst, &k_map, 0, g, off, phys, &full[s]);
+              tma_g2s_4d(vst, &v_map, 0, g, off, phys, &full[s]);
+            }
+          } else {  // contiguous: rows [t0, t0 + kTile) of (b, g); rows past max_len read as 0
+            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * C::kTileBytes));
+            const int bg = b * a.Hkv + g;
+            tma_g2s_3d(kst, &k_map, 0, t0, bg, &full[s]);
+            tma_g2s_3d(vst, &v_map, 0, t0, bg, &full[s]);
+          }
+        }
+        issued = it + 1;
+      }
+      for (int it = issued > C::kStages ? issued - C::kStages : 0; it < issued; ++it)
+        mbar_wait(&full[it % C::kStages], (it / C::kStages) & 1);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  constexpr int kConsumers = C::kConsumerWarps * 32;
+  const int hd = lane >> 2;
+  // q as the bf16 B operand (window unit, and the fused step's rotation): lane holds
+  // q[head lane/4][dims 16kk + 2(lane%4) + {0,1}] and (+8)
+  uint32_t qb[M::kKSteps][2];
+  const __nv_bfloat16* q_in = static_cast<const __nv_bfloat16*>(a.q) + (static_cast<size_t>(b) * a.Hq + h0) * D;
+  if (FUSED || win_unit) {
+    const uint32_t* q = reinterpret_cast<const uint32_t*>(q_in + hd * D);
+#pragma unroll
+    for (int kk = 0; kk < M::kKSteps; ++kk) {
+      qb[kk][0] = hd < hpc ? q[kk * 8 + (lane & 3)] : 0u;
+      qb[kk][1] = hd < hpc ? q[kk * 8 + 4 + (lane & 3)] : 0u;
+    }
+  }
+  const __nv_bfloat16* q_rows = q_in;  // where the INT8 unit reads rotated q rows from
+  if constexpr (FUSED) {
+    // RoPE ("Transformer推理核心：KV Cache、GQA与RoPE原理与工程实践" §3) as in decode_mma_kernel
+    const int pos = L - 1;
+    if (threadIdx.x < D / 2) {
+      double sn, cn;
+      sincospi(static_cast<double>(pos) * a.theta_pi[threadIdx.x], &sn, &cn);
+      const float ch = static_cast<float>(cn), sh = static_cast<float>(sn);
+      cs[threadIdx.x] = ch;
+      cs[D / 2 + threadIdx.x] = static_cast<float>(cn - static_cast<double>(ch));
+      cs[D + threadIdx.x] = sh;
+      cs[3 * (D / 2) + threadIdx.x] = static_cast<float>(sn - static_cast<double>(sh));
+    }
+    named_barrier_sync(1, kConsumers);
+    rotate_q_fragment<D>(qb, cs, lane, a.rope_style);
+    if (warp == 0 && hd < hpc) {  // rotated q rows (bf16) for this CTA, and q_rot for the caller
+      uint32_t* qo = reinterpret_cast<uint32_t*>(qs + hd * D);
+      uint32_t* qg = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.q_out) +
+                                                 (static_cast<size_t>(b) * a.Hq + h0 + hd) * D);
+#pragma unroll
+      for (int kk = 0; kk < M::kKSteps; ++kk) {
+        qo[kk * 8 + (lane & 3)] = qb[kk][0];
+        qo[kk * 8 + 4 + (lane & 3)] = qb[kk][1];
+        if (publisher) {
+          qg[kk * 8 + (lane & 3)] = qb[kk][0];
+          qg[kk * 8 + 4 + (lane & 3)] = qb[kk][1];
+        }
+      }
+    }
+    if (appender && warp == 1) {
+      // Quantised k (rotated, rounded to bf16) and v into cache slot pos of KV head g, and with
+      // a window their bf16 values into ring slot pos % window. Every head-slice CTA of this
+      // unit writes the same bytes.
+      size_t row = 0;
+      bool ok = true;
+      if constexpr (PAGED) {
+        const int phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (pos >> a.log2_bs)];
+        ok = phys >= 0 && phys < a.num_blocks;
+        row = ((static_cast<size_t>(phys) << a.log2_bs) + (pos & ((1 << a.log2_bs) - 1))) * a.Hkv + g;
+      } else {
+        row = (static_cast<size_t>(b) * a.Hkv + g) * a.max_len + pos;
+      }
+      const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(a.k_new) + (static_cast<size_t>(b) * a.Hkv + g) * D;
+      const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(a.v_new) + (static_cast<size_t>(b) * a.Hkv + g) * D;
+      int8_t* kc = static_cast<int8_t*>(const_cast<void*>(a.k)) + row * D;
+      int8_t* vc = static_cast<int8_t*>(const_cast<void*>(a.v)) + row * D;
+      const size_t wrow = ((static_cast<size_t>(b) * a.Hkv + g) * (has_win ? a.window : 1) + (has_win ? pos % a.window : 0)) * D;
+      __nv_bfloat16* kw = static_cast<__nv_bfloat16*>(a.k_win) + wrow;
+      __nv_bfloat16* vw = static_cast<__nv_bfloat16*>(a.v_win) + wrow;
+      const float ks = a.k_scale[g], vs = a.v_scale[g];
+      const bool inter = a.rope_style == 1;
+      for (int i = lane; i < D / 2; i += 32) {
+        const int ia = inter ? 2 * i : i, ib = inter ? 2 * i + 1 : i + D / 2;
+        const float xa = __bfloat162float(kn[ia]), xb = __bfloat162float(kn[ib]);
+        const float ch = cs[i], cl = cs[D / 2 + i], sh = cs[D + i], sl = cs[3 * (D / 2) + i];
+        const __nv_bfloat16 ra = __float2bfloat16_rn(rotate_diff(xa, xb, ch, cl, sh, sl));
+        const __nv_bfloat16 rb = __float2bfloat16_rn(rotate_diff(xb, -xa, ch, cl, sh, sl));
+        if (ok) {
+          kc[ia] = quantize_code(__bfloat162float(ra), ks);
+          kc[ib] = quantize_code(__bfloat162float(rb), ks);
+        }
+        if (has_win) {
+          kw[ia] = ra;
+          kw[ib] = rb;
+        }
+      }
+      for (int i = lane; i < D; i += 32) {
+        const __nv_bfloat16 x = vn[i];
+        if (ok) vc[i] = quantize_code(__bfloat162float(x), vs);
+        if (has_win) vw[i] = x;
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // visible to the TMA that reads the slot
+      __syncwarp();
+      if (lane == 0) mbar_arrive(appended);
+    }
+    q_rows = qs;
+    named_barrier_sync(1, kConsumers);  // the rotated rows in shared memory are complete
+  }
+
+  MmaWarpState<D> st;
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
+  st.m[0] = st.m[1] = -INFINITY;
+  st.l[0] = st.l[1] = 0.f;
+
+  if (win_unit) {
+    for (int it = 0; it < n_tiles; ++it) {
+      const int s = it % C::kStages;
+      if (!mbar_wait(&full[s], (it / C::kStages) & 1)) {
+        flag_error(a.err, RRA_ERR_TIMEOUT);
+        break;
+      }
+      uint8_t* kst = smem + s * C::kStageBytes;
+      uint8_t* vst = kst + M::kHalves * M::kHalfBytes;
+      const uint32_t k_base = smem_addr(kst), v_base = smem_addr(vst);
+      const int valid = min(rows, end - (start + it * rows));
+#pragma unroll
+      for (int step = 0; step < M::kSteps; ++step) {
+        const int t0 = warp * M::kWarpTokens + step * 16;
+        if (valid == M::kTile)
+          mma_step<D, false>(st, qb, k_base, v_base, vst, t0, valid, lane, a.scale_log2);
+        else if (t0 < valid)
+          mma_step<D, true>(st, qb, k_base, v_base, vst, t0, valid, lane, a.scale_log2);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  } else {
+    // q in the INT8 fragment order: lane holds dims 16c + 4(lane%4) + {0..3} of head lane/4,
+    // scaled by 2^e so that the head's largest |q| lies in [2^14, 2^15), then rounded to f16.
+    uint32_t qh[D / 16][2];
+    float down;
+    {
+      float xq[D / 16][4];
+      float amax = 0.f;
+      const __nv_bfloat16* qr = q_rows + hd * D + 4 * (lane & 3);
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        uint2 w = make_uint2(0u, 0u);
+        if (hd < hpc) w = *reinterpret_cast<const uint2*>(qr + 16 * c);
+        xq[c][0] = __uint_as_float(w.x << 16);
+        xq[c][1] = __uint_as_float(w.x & 0xffff0000u);
+        xq[c][2] = __uint_as_float(w.y << 16);
+        xq[c][3] = __uint_as_float(w.y & 0xffff0000u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(xq[c][e]));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      int e = 0;
+      if (amax > 0.f && amax <= 3.4e38f) e = min(max(14 - (static_cast<int>((__float_as_uint(amax) >> 23) & 0xff) - 127), -126), 126);
+      const float up = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+      down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        qh[c][0] = pack_f16x2(xq[c][0] * up, xq[c][1] * up);
+        qh[c][1] = pack_f16x2(xq[c][2] * up, xq[c][3] * up);
+      }
+    }
+    float mult[2];
+    {
+      const float base = a.k_scale[g] * a.scale_log2;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) mult[j] = base * __shfl_sync(0xffffffffu, down, 4 * (2 * (lane & 3) + j));
+    }
+    for (int it = 0; it < n_tiles; ++it) {
+      const int s = it % C::kStages;
+      if (!mbar_wait(&full[s], (it / C::kStages) & 1)) {
+        flag_error(a.err, RRA_ERR_TIMEOUT);
+        break;
+      }
+      uint8_t* kst = smem + s * C::kStageBytes;
+      const uint32_t k_base = smem_addr(kst), v_base = k_base + C::kTileBytes;
+      const int valid = min(C::kTile, end - (start + it * C::kTile));
+#pragma unroll
+      for (int step = 0; step < C::kSteps; ++step) {
+        const int t0 = warp * C::kWarpTokens + step * 16;
+        if (valid == C::kTile)
+          q8_step<D, false>(st, qh, mult, k_base, v_base, t0, valid, lane);
+        else if (t0 < valid)
+          q8_step<D, true>(st, qh, mult, k_base, v_base, t0, valid, lane);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+
+  // ------------------------------------------------------------------ merge the 4 warps
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 4);
+    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 8);
+    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 16);
+  }
+  named_barrier_sync(1, kConsumers);
+  float* red_o = reinterpret_cast<float*>(smem);                 // [warps][8 heads][D]
+  float* red_m = red_o + C::kConsumerWarps * M::kMaxHeads * D;   // [warps][8 heads]
+  float* red_l = red_m + C::kConsumerWarps * M::kMaxHeads;
+  {
+    const int hd0 = 2 * (lane & 3), dl = lane >> 2;
+    if (win_unit) {
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          red_o[(warp * M::kMaxHeads + hd0 + j) * D + 16 * i + dl] = st.o[i][j];
+          red_o[(warp * M::kMaxHeads + hd0 + j) * D + 16 * i + 8 + dl] = st.o[i][2 + j];
+        }
+    } else {  // fragment rows dl and dl + 8 are dims 2dl and 2dl + 1; V codes times the V scale
+      const float vs = a.v_scale[g];
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          *reinterpret_cast<float2*>(&red_o[(warp * M::kMaxHeads + hd0 + j) * D + 16 * i + 2 * dl]) =
+              make_float2(st.o[i][j] * vs, st.o[i][2 + j] * vs);
+    }
+    if (dl == 0) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        red_m[warp * M::kMaxHeads + hd0 + j] = st.m[j];
+        red_l[warp * M::kMaxHeads + hd0 + j] = st.l[j];
+      }
+    }
+  }
+  named_barrier_sync(1, kConsumers);
+  for (int idx = threadIdx.x; idx < hpc * D; idx += kConsumers) {
+    const int h = idx / D, d = idx - h * D;
+    float Mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < C::kConsumerWarps; ++w) Mx = fmaxf(Mx, red_m[w * M::kMaxHeads + h]);
+    float lsum = 0.f, osum = 0.f;
+    if (Mx != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < C::kConsumerWarps; ++w) {
+        const float wt = exp2f(red_m[w * M::kMaxHeads + h] - Mx);
+        lsum = fmaf(wt, red_l[w * M::kMaxHeads + h], lsum);
+        osum = fmaf(wt, red_o[(w * M::kMaxHeads + h) * D + d], osum);
+      }
+    }
+    const size_t bh = static_cast<size_t>(b) * a.Hq + h0 + h;
+    if (n_work == 1) {
+      static_cast<__nv_bfloat16*>(a.out)[bh * D + d] = __float2bfloat16_rn(lsum > 0.f ? osum / lsum : 0.f);
+    } else {
+      const size_t ps = bh * a.num_splits + part;
+      a.ws_o[ps * D + d] = osum;
+      if (d == 0) {
+        a.ws_ml[2 * ps] = Mx;
+        a.ws_ml[2 * ps + 1] = lsum;
+      }
+    }
+  }
+  if (n_work > 1) {
+    __shared__ int s_last;
+    finish_split<__nv_bfloat16, D>(a, b, h0, hpc, part, n_work, reinterpret_cast<float*>(smem), &s_last,
+                                   threadIdx.x, kConsumers);
+  }
+}
+
+template <int D, bool PAGED, bool FUSED>
+cudaError_t launch_decode_q8_t(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
+                               const CUtensorMap& kwm, const CUtensorMap& vwm, cudaStream_t st) {
+  using C = Q8Cfg<D>;
+  static int done[64] = {0};
+  auto kern = decode_q8_kernel<D, PAGED, FUSED>;
+  cudaError_t e = ensure_smem(kern, C::kSmemBytes, done);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(a.num_splits * ((a.Hq / a.Hkv) / a.hpc), a.Hkv, a.B);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(km, vm, kwm, vwm, a);
+  return cudaGetLastError();
+}
+
+}  // namespace rra

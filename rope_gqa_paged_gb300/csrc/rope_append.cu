@@ -15,6 +15,11 @@
 // float32 products (x*y = p + e exactly, with e = fma(x, y, -p): Dekker's product, using
 // the FMA) so that it keeps full relative accuracy when the two products cancel; the
 // result is then rounded once to the storage type.
+//
+// INT8 caches (§4.3 of the first page: INT8 K/V with per-head calibrated scales, recent
+// tokens kept at high precision): the rotated k is rounded to bf16 first, then quantised
+// with its KV head's scale into the cache slot; with a window the bf16 values also go to
+// slot pos % window of the sequence's ring.
 #include "rra_device.cuh"
 #include "rra_internal.h"
 
@@ -24,7 +29,7 @@ namespace {
 constexpr int kPairsPerCta = 16;
 constexpr int kRopeThreads = 128;
 
-template <typename T>
+template <typename T, bool Q8>
 __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArgs a) {
   constexpr int kRows = kRopeThreads / kPairsPerCta;  // head rows handled side by side
   constexpr int kUnroll = 8;                          // head rows per thread loaded before any math
@@ -107,15 +112,32 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
           xa[r] = Elem<T>::load(src_row(hh) + ia);
           xb[r] = Elem<T>::load(src_row(hh) + ib);
         }
-        T* dst;
+        const float ra = rotate_diff(xa[r], xb[r], ch, cl, sh, sl);   // a cos - b sin
+        const float rb = rotate_diff(xb[r], -xa[r], ch, cl, sh, sl);  // b cos + a sin
         if (hh < a.Hq) {
-          dst = static_cast<T*>(a.q_out) + (static_cast<size_t>(b) * a.Hq + hh) * D;
-        } else {
-          if (!append) continue;
-          dst = static_cast<T*>(a.k_cache) + (row0 + (hh - a.Hq) * head_stride) * D;
+          T* dst = static_cast<T*>(a.q_out) + (static_cast<size_t>(b) * a.Hq + hh) * D;
+          Elem<T>::store(dst + ia, ra);
+          Elem<T>::store(dst + ib, rb);
+        } else if (append) {
+          const int g = hh - a.Hq;
+          if constexpr (Q8) {
+            const __nv_bfloat16 ka = __float2bfloat16_rn(ra), kb = __float2bfloat16_rn(rb);
+            const float s = a.k_scale[g];
+            int8_t* dst = static_cast<int8_t*>(a.k_cache) + (row0 + g * head_stride) * D;
+            dst[ia] = quantize_code(__bfloat162float(ka), s);
+            dst[ib] = quantize_code(__bfloat162float(kb), s);
+            if (a.window > 0) {
+              __nv_bfloat16* w = static_cast<__nv_bfloat16*>(a.k_win) +
+                                 ((static_cast<size_t>(b) * a.Hkv + g) * a.window + pos % a.window) * D;
+              w[ia] = ka;
+              w[ib] = kb;
+            }
+          } else {
+            T* dst = static_cast<T*>(a.k_cache) + (row0 + g * head_stride) * D;
+            Elem<T>::store(dst + ia, ra);
+            Elem<T>::store(dst + ib, rb);
+          }
         }
-        Elem<T>::store(dst + ia, rotate_diff(xa[r], xb[r], ch, cl, sh, sl));   // a cos - b sin
-        Elem<T>::store(dst + ib, rotate_diff(xb[r], -xa[r], ch, cl, sh, sl));  // b cos + a sin
       }
     }
   }
@@ -124,10 +146,16 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
   const int dims = (D + gridDim.y - 1) / gridDim.y;
   const int d0 = blockIdx.y * dims, d1 = min(D, d0 + dims);
   const T* vn = static_cast<const T*>(a.v_new) + static_cast<size_t>(b) * a.Hkv * D;
-  T* vc = static_cast<T*>(a.v_cache);
   for (int idx = threadIdx.x; idx < a.Hkv * (d1 - d0); idx += blockDim.x) {
     const int g = idx / (d1 - d0), d = d0 + idx % (d1 - d0);
-    vc[(row0 + g * head_stride) * D + d] = vn[g * D + d];
+    if constexpr (Q8) {
+      const T x = vn[g * D + d];
+      static_cast<int8_t*>(a.v_cache)[(row0 + g * head_stride) * D + d] = quantize_code(Elem<T>::load(&x), a.v_scale[g]);
+      if (a.window > 0)
+        static_cast<T*>(a.v_win)[((static_cast<size_t>(b) * a.Hkv + g) * a.window + pos % a.window) * D + d] = x;
+    } else {
+      static_cast<T*>(a.v_cache)[(row0 + g * head_stride) * D + d] = vn[g * D + d];
+    }
   }
 }
 
@@ -136,9 +164,15 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
 cudaError_t launch_rope_append(const RopeArgs& a, rra_dtype dt, cudaStream_t stream) {
   const dim3 grid(a.B, (a.D / 2 + kPairsPerCta - 1) / kPairsPerCta);
   if (dt == RRA_BF16)
-    rope_append_kernel<__nv_bfloat16><<<grid, kRopeThreads, 0, stream>>>(a);
+    rope_append_kernel<__nv_bfloat16, false><<<grid, kRopeThreads, 0, stream>>>(a);
   else
-    rope_append_kernel<float><<<grid, kRopeThreads, 0, stream>>>(a);
+    rope_append_kernel<float, false><<<grid, kRopeThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_append_q8(const RopeArgs& a, cudaStream_t stream) {
+  const dim3 grid(a.B, (a.D / 2 + kPairsPerCta - 1) / kPairsPerCta);
+  rope_append_kernel<__nv_bfloat16, true><<<grid, kRopeThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -89,18 +89,9 @@ int check_shapes(int B, int Hq, int Hkv, int D, rra_dtype dt) {
   return RRA_OK;
 }
 
-// max_tokens: per-sequence capacity; block_size: 0 for a contiguous cache.
-int make_plan(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size, int requested, rra_dtype dt,
-              Plan* p) {
-  int st = check_shapes(B, Hq, Hkv, D, dt);
-  if (st != RRA_OK) return st;
-  if (requested < 0 || max_tokens < 0) return RRA_EINVAL;
-  if (max_tokens > (int64_t(1) << 30)) return RRA_ERANGE;
-  const int n_rep = Hq / Hkv;
-  p->mma = use_mma_kernel(dt, D, max_tokens, block_size);
-  p->hpc = heads_per_cta(n_rep, p->mma);
-  if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
-  p->tile = p->mma ? rra::decode_mma_tile_tokens(D) : rra::decode_tile_tokens(D, elem_bytes(dt));
+// Chunk and split count for a per-sequence capacity of max_tokens, once p->mma, p->hpc and
+// p->tile are set.
+int plan_splits(int B, int Hkv, int n_rep, int64_t max_tokens, int block_size, int requested, Plan* p) {
   const int64_t tiles = std::max<int64_t>(1, (max_tokens + p->tile - 1) / p->tile);
   // A paged split copies its block ids to shared memory: at most kMaxTableEntries of them.
   int64_t max_chunk_tiles = tiles;
@@ -140,6 +131,43 @@ int make_plan(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
   return RRA_OK;
 }
 
+// max_tokens: per-sequence capacity; block_size: 0 for a contiguous cache.
+int make_plan(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size, int requested, rra_dtype dt,
+              Plan* p) {
+  int st = check_shapes(B, Hq, Hkv, D, dt);
+  if (st != RRA_OK) return st;
+  if (requested < 0 || max_tokens < 0) return RRA_EINVAL;
+  if (max_tokens > (int64_t(1) << 30)) return RRA_ERANGE;
+  const int n_rep = Hq / Hkv;
+  p->mma = use_mma_kernel(dt, D, max_tokens, block_size);
+  p->hpc = heads_per_cta(n_rep, p->mma);
+  if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
+  p->tile = p->mma ? rra::decode_mma_tile_tokens(D) : rra::decode_tile_tokens(D, elem_bytes(dt));
+  return plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
+}
+
+// INT8 caches: the INT8 tokens split like the bf16 tensor-core kernel's (tiles of 16384 / D
+// tokens), plus one partial slot for the window's ring when window > 0. Paged blocks must hold
+// at least 8 tokens and a contiguous cache at least one tile; the window is a multiple of 8.
+int make_plan_q8(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size, int requested, int window,
+                 Plan* p) {
+  int st = check_shapes(B, Hq, Hkv, D, RRA_BF16);
+  if (st != RRA_OK) return st;
+  if (requested < 0 || max_tokens < 0 || window < 0) return RRA_EINVAL;
+  if (max_tokens > (int64_t(1) << 30)) return RRA_ERANGE;
+  if (window % 8 != 0 || window > 65536) return RRA_EUNSUPPORTED;
+  const int n_rep = Hq / Hkv;
+  p->mma = true;
+  p->hpc = heads_per_cta(n_rep, true);
+  if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
+  p->tile = rra::decode_q8_tile_tokens(D);
+  if (block_size > 0 ? block_size < 8 : max_tokens < p->tile) return RRA_EUNSUPPORTED;
+  st = plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
+  if (st != RRA_OK) return st;
+  if (window > 0) ++p->splits;
+  return RRA_OK;
+}
+
 // Workspace layout, each part 256-byte aligned (R = B*Hq, G = ceil(splits / kMergeFanIn)):
 // partials o [R, splits, D] and (max, sum) [R, splits, 2] floats, level-2 partials o [R, G, D]
 // and (max, sum) [R, G, 2] floats, counters [R] and group counters [R, G] int32.
@@ -168,24 +196,49 @@ size_t workspace_bytes(int B, int Hq, int D, int splits) {
 }
 
 // Tiled tensor map over `base` (rank 3 or 4, dims innermost first, strides in bytes of dims 1..).
-int encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-               const cuuint32_t* box, rra_dtype dt, bool swizzle128) {
+int encode_map_typed(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                     const cuuint32_t* box, CUtensorMapDataType type, CUtensorMapSwizzle swizzle) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) {
     std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled unavailable");
     return RRA_ECUDA;
   }
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  const CUresult r =
-      enc(map, dt == RRA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank,
-          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = enc(map, type, rank, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     std::snprintf(g_cuda_error, sizeof(g_cuda_error), "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));
     return RRA_ECUDA;
   }
   return RRA_OK;
+}
+
+int encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+               const cuuint32_t* box, rra_dtype dt, bool swizzle128) {
+  return encode_map_typed(map, base, rank, dims, strides, box,
+                          dt == RRA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// INT8 code caches: rows of D bytes with the 128-byte (D = 128) or 64-byte (D = 64) swizzle.
+// Paged pools [num_blocks, block_size, Hkv, D] as {D, Hkv, block_size, num_blocks} with boxes of
+// one head's `box_rows` rows; contiguous caches [B, Hkv, max_len, D] as {D, max_len, B*Hkv}.
+int encode_q8_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int Hkv, int D,
+                       int box_rows) {
+  const cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(Hkv), cuuint64_t(block_size), cuuint64_t(num_blocks)};
+  const cuuint64_t strides[3] = {cuuint64_t(D), cuuint64_t(Hkv) * D, cuuint64_t(block_size) * Hkv * D};
+  const cuuint32_t box[4] = {cuuint32_t(D), 1u, cuuint32_t(box_rows), 1u};
+  return encode_map_typed(map, pool, 4, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                          D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+int encode_q8_contig_map(CUtensorMap* map, const void* cache, int B, int Hkv, int max_len, int D, int tile) {
+  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(max_len), cuuint64_t(B) * Hkv};
+  const cuuint64_t strides[2] = {cuuint64_t(D), cuuint64_t(max_len) * D};
+  const cuuint32_t box[3] = {cuuint32_t(D), cuuint32_t(tile), 1u};
+  return encode_map_typed(map, cache, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                          D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // Pool [num_blocks, block_size, Hkv, D] as 4-D {D, Hkv, block_size, num_blocks}; the box is
@@ -273,6 +326,72 @@ int check_step_args(const void* q, const void* k_new, const void* v_new, const i
     if (!aligned16(p)) return RRA_EINVAL;
   if (overlap(q, q_out, size_t(B) * Hq * D * elem_bytes(dt))) return RRA_EINVAL;  // q is read after q_out is written
   return RRA_OK;
+}
+
+// Checks and tensor maps shared by the INT8 entry points. Contiguous (block_table == NULL):
+// codes [B, Hkv, max_len, D]; paged: pools [num_blocks, block_size, Hkv, D].
+struct Q8Layout {
+  int64_t capacity = 0;
+  int log2_bs = 0;
+};
+
+int q8_layout(const int32_t* block_table, int max_blocks_per_seq, int block_size, int num_blocks, int max_len,
+              Q8Layout* l) {
+  if (block_table != nullptr) {
+    if (!pow2(block_size)) return block_size <= 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
+    if (max_blocks_per_seq < 1 || num_blocks < 1) return RRA_EINVAL;
+    l->capacity = int64_t(max_blocks_per_seq) * block_size;
+    l->log2_bs = ilog2(block_size);
+  } else {
+    if (max_len < 1) return RRA_EINVAL;
+    l->capacity = max_len;
+  }
+  return RRA_OK;
+}
+
+int check_q8_buffers(const void* k_codes, const void* v_codes, const float* k_scale, const float* v_scale,
+                     const void* k_win, const void* v_win, int window) {
+  if (!k_codes || !v_codes || !k_scale || !v_scale) return RRA_EINVAL;
+  if (!aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scale) || !aligned16(v_scale)) return RRA_EINVAL;
+  if (window > 0 && (!k_win || !v_win || !aligned16(k_win) || !aligned16(v_win))) return RRA_EINVAL;
+  return RRA_OK;
+}
+
+int q8_maps(const Plan& p, const void* k_codes, const void* v_codes, const void* k_win, const void* v_win, int window,
+            const int32_t* block_table, int block_size, int num_blocks, int max_len, int B, int Hkv, int D,
+            CUtensorMap* km, CUtensorMap* vm, CUtensorMap* kwm, CUtensorMap* vwm) {
+  int st;
+  if (block_table != nullptr) {
+    const int box_rows = block_size < p.tile ? block_size : p.tile;
+    st = encode_q8_pool_map(km, k_codes, num_blocks, block_size, Hkv, D, box_rows);
+    if (st == RRA_OK) st = encode_q8_pool_map(vm, v_codes, num_blocks, block_size, Hkv, D, box_rows);
+  } else {
+    st = encode_q8_contig_map(km, k_codes, B, Hkv, max_len, D, p.tile);
+    if (st == RRA_OK) st = encode_q8_contig_map(vm, v_codes, B, Hkv, max_len, D, p.tile);
+  }
+  if (st != RRA_OK || window == 0) return st;
+  const int rows = std::min(window, rra::decode_mma_tile_tokens(D));  // ring rows per stage
+  st = encode_contig_map(kwm, k_win, B, Hkv, window, D, rows, RRA_BF16);
+  if (st == RRA_OK) st = encode_contig_map(vwm, v_win, B, Hkv, window, D, rows, RRA_BF16);
+  return st;
+}
+
+void set_q8_args(rra::DecodeArgs* a, const Q8Layout& l, const void* k_codes, const void* v_codes, const float* k_scale,
+                 const float* v_scale, void* k_win, void* v_win, int window, const int32_t* block_table,
+                 int max_blocks_per_seq, int num_blocks, int max_len) {
+  a->k = k_codes;
+  a->v = v_codes;
+  a->k_scale = k_scale;
+  a->v_scale = v_scale;
+  a->k_win = k_win;
+  a->v_win = v_win;
+  a->window = window;
+  a->block_table = block_table;
+  a->max_blocks_per_seq = max_blocks_per_seq;
+  a->log2_bs = l.log2_bs;
+  a->num_blocks = num_blocks;
+  a->max_len = block_table != nullptr ? 0 : max_len;
+  a->capacity = static_cast<int>(l.capacity);
 }
 
 }  // namespace
@@ -512,6 +631,127 @@ int rra_decode_step_paged(const void* q, const void* k_new, const void* v_new, c
   a.rope_style = rope_style;
   fill_theta_pi(a.theta_pi, D, rope_base);
   return finish_decode(rra::launch_decode_step_paged(a, km, vm, s));
+}
+
+int rra_decode_q8_num_splits(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size, int num_splits,
+                             int window) {
+  if (block_size < 0 || (block_size > 0 && !pow2(block_size))) return block_size < 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
+  Plan p;
+  const int st = make_plan_q8(B, Hq, Hkv, D, max_tokens, block_size, num_splits, window, &p);
+  return st != RRA_OK ? st : p.splits;
+}
+
+int rra_rope_append_q8(const void* q, const void* k_new, const void* v_new, const int32_t* positions, void* q_out,
+                       void* k_codes, void* v_codes, const float* k_scale, const float* v_scale, void* k_win,
+                       void* v_win, int window, const int32_t* block_table, int max_blocks_per_seq, int block_size,
+                       int num_blocks, int max_len, int B, int Hq, int Hkv, int D, double rope_base, int rope_style,
+                       int32_t* err_flag, void* stream) {
+  int st = check_shapes(B, Hq, Hkv, D, RRA_BF16);
+  if (st != RRA_OK) return st;
+  if (!(rope_base > 1.0) || !std::isfinite(rope_base) || (rope_style != 0 && rope_style != 1)) return RRA_EINVAL;
+  if (window < 0) return RRA_EINVAL;
+  if (int64_t(Hq) + Hkv > 8 * 65535) return RRA_ERANGE;
+  Q8Layout l;
+  st = q8_layout(block_table, max_blocks_per_seq, block_size, num_blocks, max_len, &l);
+  if (st != RRA_OK) return st;
+  if (l.capacity > (int64_t(1) << 30)) return RRA_ERANGE;
+  if (B == 0) return RRA_OK;
+  if (!q || !k_new || !v_new || !positions || !q_out) return RRA_EINVAL;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(q_out)) return RRA_EINVAL;
+  st = check_q8_buffers(k_codes, v_codes, k_scale, v_scale, k_win, v_win, window);
+  if (st != RRA_OK) return st;
+  rra::RopeArgs a{};
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.positions = positions;
+  a.q_out = q_out;
+  a.k_cache = k_codes;
+  a.v_cache = v_codes;
+  a.block_table = block_table;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.log2_bs = l.log2_bs;
+  a.num_blocks = num_blocks;
+  a.max_len = max_len;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.rope_style = rope_style;
+  a.err = err_flag;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.k_win = k_win;
+  a.v_win = v_win;
+  a.window = window;
+  fill_theta_pi(a.inv_freq, D, rope_base);
+  const cudaError_t e = rra::launch_rope_append_q8(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RRA_OK : cuda_fail(e, "rope_append_q8 launch");
+}
+
+int rra_decode_attn_q8(const void* q_rot, const void* k_codes, const void* v_codes, const float* k_scale,
+                       const float* v_scale, const void* k_win, const void* v_win, int window,
+                       const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens, int block_size,
+                       int num_blocks, int max_len, void* out, int B, int Hq, int Hkv, int D, float scale,
+                       int num_splits, void* workspace, size_t ws_bytes, int32_t* err_flag, void* stream) {
+  Q8Layout l;
+  int st = q8_layout(block_table, max_blocks_per_seq, block_size, num_blocks, max_len, &l);
+  if (st != RRA_OK) return st;
+  Plan p;
+  st = make_plan_q8(B, Hq, Hkv, D, l.capacity, block_table ? block_size : 0, num_splits, window, &p);
+  if (st != RRA_OK) return st;
+  if (!std::isfinite(scale)) return RRA_EINVAL;
+  if (B == 0) return RRA_OK;
+  if (!q_rot || !seq_lens || !out || !aligned16(q_rot) || !aligned16(out)) return RRA_EINVAL;
+  st = check_q8_buffers(k_codes, v_codes, k_scale, v_scale, k_win, v_win, window);
+  if (st != RRA_OK) return st;
+  st = check_workspace(p, B, Hq, D, workspace, ws_bytes);
+  if (st != RRA_OK) return st;
+  CUtensorMap km{}, vm{}, kwm{}, vwm{};
+  st = q8_maps(p, k_codes, v_codes, k_win, v_win, window, block_table, block_size, num_blocks, max_len, B, Hkv, D,
+               &km, &vm, &kwm, &vwm);
+  if (st != RRA_OK) return st;
+  rra::DecodeArgs a = decode_args(p, q_rot, k_codes, v_codes, seq_lens, out, B, Hq, Hkv, D, scale, workspace, err_flag);
+  set_q8_args(&a, l, k_codes, v_codes, k_scale, v_scale, const_cast<void*>(k_win), const_cast<void*>(v_win), window,
+              block_table, max_blocks_per_seq, num_blocks, max_len);
+  return finish_decode(rra::launch_decode_q8(a, km, vm, kwm, vwm, block_table != nullptr, false,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int rra_decode_step_q8(const void* q, const void* k_new, const void* v_new, const int32_t* positions, void* q_out,
+                       void* k_codes, void* v_codes, const float* k_scale, const float* v_scale, void* k_win,
+                       void* v_win, int window, const int32_t* block_table, int max_blocks_per_seq, int block_size,
+                       int num_blocks, int max_len, void* out, int B, int Hq, int Hkv, int D, double rope_base,
+                       int rope_style, float scale, int num_splits, void* workspace, size_t ws_bytes,
+                       int32_t* err_flag, void* stream) {
+  Q8Layout l;
+  int st = q8_layout(block_table, max_blocks_per_seq, block_size, num_blocks, max_len, &l);
+  if (st != RRA_OK) return st;
+  Plan p;
+  st = make_plan_q8(B, Hq, Hkv, D, l.capacity, block_table ? block_size : 0, num_splits, window, &p);
+  if (st != RRA_OK) return st;
+  st = check_step_args(q, k_new, v_new, positions, q_out, k_codes, v_codes, out, B, Hq, D, rope_base, rope_style,
+                       scale, RRA_BF16);
+  if (st != RRA_OK || B == 0) return st;
+  st = check_q8_buffers(k_codes, v_codes, k_scale, v_scale, k_win, v_win, window);
+  if (st != RRA_OK) return st;
+  st = check_workspace(p, B, Hq, D, workspace, ws_bytes);
+  if (st != RRA_OK) return st;
+  CUtensorMap km{}, vm{}, kwm{}, vwm{};
+  st = q8_maps(p, k_codes, v_codes, k_win, v_win, window, block_table, block_size, num_blocks, max_len, B, Hkv, D,
+               &km, &vm, &kwm, &vwm);
+  if (st != RRA_OK) return st;
+  rra::DecodeArgs a = decode_args(p, q, k_codes, v_codes, nullptr, out, B, Hq, Hkv, D, scale, workspace, err_flag);
+  set_q8_args(&a, l, k_codes, v_codes, k_scale, v_scale, k_win, v_win, window, block_table, max_blocks_per_seq,
+              num_blocks, max_len);
+  a.positions = positions;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.q_out = q_out;
+  a.rope_style = rope_style;
+  fill_theta_pi(a.theta_pi, D, rope_base);
+  return finish_decode(rra::launch_decode_q8(a, km, vm, kwm, vwm, block_table != nullptr, true,
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

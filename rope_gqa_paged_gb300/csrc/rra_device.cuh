@@ -152,4 +152,12 @@ struct Elem<float> {
   __device__ __forceinline__ static void store_f64(float* p, double v) { *p = static_cast<float>(v); }
 };
 
+// Symmetric INT8 code of x at scale s ("Transformer推理核心：KV Cache、GQA与RoPE原理与工程实践"
+// §4.3, per-head calibrated INT8): clamp(round_half_even(x / s), -127, 127), the quotient an
+// IEEE float32 division (nearest even). A NaN input gives -127.
+__device__ __forceinline__ int8_t quantize_code(float x, float s) {
+  const float r = fminf(fmaxf(__fdiv_rn(x, s), -127.f), 127.f);
+  return static_cast<int8_t>(__float2int_rn(r));
+}
+
 }  // namespace rra

@@ -28,6 +28,13 @@ struct RopeArgs {
   int B, Hq, Hkv, D;
   int rope_style;
   int32_t* err;
+  // INT8 caches only: k_cache / v_cache hold int8 codes, quantised with these per-KV-head
+  // scales; with window > 0 the bf16 values also go to ring slot pos % window.
+  const float* k_scale;
+  const float* v_scale;
+  void* k_win;                  // bf16 [B, Hkv, window, D]
+  void* v_win;
+  int window;
   double inv_freq[kMaxHeadDim / 2];  // theta_i / pi, theta_i = base^(-2i/D), formed on the host in float64
 };
 
@@ -64,6 +71,14 @@ struct DecodeArgs {
   const void* v_new;            // [B, Hkv, D]
   void* q_out;                  // [B, Hq, D], must not overlap q
   int rope_style;
+  // INT8 caches (decode_q8.cuh): k / v hold codes with these per-KV-head scales; with
+  // window > 0 the `window` most recent tokens are read from the bf16 rings instead, and the
+  // last of the num_splits partial slots belongs to the ring.
+  const float* k_scale;
+  const float* v_scale;
+  void* k_win;                  // bf16 [B, Hkv, window, D]
+  void* v_win;
+  int window;
   double theta_pi[kMaxDecodeHeadDim / 2];  // theta_i / pi, theta_i = base^(-2i/D)
 };
 
@@ -81,6 +96,8 @@ constexpr int kMergeFanIn = 16;
 void record_cuda_error(cudaError_t e, const char* where);
 
 cudaError_t launch_rope_append(const RopeArgs& a, rra_dtype dt, cudaStream_t stream);
+// RoPE + append into an INT8 cache (bf16 q / k_new / v_new; a.k_scale etc. set).
+cudaError_t launch_rope_append_q8(const RopeArgs& a, cudaStream_t stream);
 // Tokens per stage of the tensor-core (bf16) decode kernel: K + V tiles of 32 KB.
 inline int decode_mma_tile_tokens(int D) { return 16384 / (D * 2); }
 // Most block-table entries one work item of the tensor-core kernel may span.
@@ -97,5 +114,12 @@ cudaError_t launch_decode_step_contig(const DecodeArgs& a, const CUtensorMap& k_
                                       cudaStream_t stream);
 cudaError_t launch_decode_step_paged(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
                                      cudaStream_t stream);
+// Tokens per stage of the INT8 decode kernel (K + V codes, 32 KB).
+inline int decode_q8_tile_tokens(int D) { return 16384 / D; }
+// INT8 caches: attention only (a.seq_lens) or the fused step (a.positions, a.k_new, ...).
+// k_map / v_map cover the code caches, kw_map / vw_map the bf16 rings (unused without a window).
+cudaError_t launch_decode_q8(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
+                             const CUtensorMap& kw_map, const CUtensorMap& vw_map, bool paged, bool fused,
+                             cudaStream_t stream);
 
 }  // namespace rra

@@ -100,3 +100,55 @@ class DecodeStep:
 
     def reset_errors(self) -> None:
         self.err.zero_()
+
+
+class DecodeStepQ8(DecodeStep):
+    """The decode step on an INT8 KV cache with per-head scales and a bf16 window of recent tokens.
+
+    k_codes / v_codes: int8 [B, Hkv, max_len, D] or pools [num_blocks, block_size, Hkv, D] (with
+    ``block_table``); k_scale / v_scale: float32 [Hkv]; k_win / v_win: bf16 rings [B, Hkv, W, D]
+    or None (no window). q, k_new, v_new and the output are bf16.
+    """
+
+    def __init__(self, batch: int, n_q_heads: int, n_kv_heads: int, head_dim: int, k_codes: torch.Tensor,
+                 v_codes: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                 k_win: Optional[torch.Tensor] = None, v_win: Optional[torch.Tensor] = None,
+                 block_table: Optional[torch.Tensor] = None, num_splits: int = 0, rope_base: float = 10000.0,
+                 rope_style: int = 0, scale: float = 0.0):
+        self.B, self.Hq, self.Hkv, self.D = batch, n_q_heads, n_kv_heads, head_dim
+        self.k_cache, self.v_cache, self.block_table = k_codes, v_codes, block_table
+        self.k_scale, self.v_scale, self.k_win, self.v_win = k_scale, v_scale, k_win, v_win
+        self.window = k_win.shape[2] if k_win is not None else 0
+        self.rope_base, self.rope_style, self.scale = rope_base, rope_style, scale
+        self.dtype, dev = torch.bfloat16, k_codes.device
+        if block_table is not None:
+            bs = k_codes.shape[1]
+            max_tokens = block_table.shape[1] * bs
+        else:
+            bs, max_tokens = 0, k_codes.shape[2]
+        self.splits = rra.rra_decode_q8_num_splits(batch, n_q_heads, n_kv_heads, head_dim, max_tokens, bs,
+                                                   num_splits, self.window)
+        self.num_splits = num_splits
+        ws = rra.rra_decode_workspace_bytes(batch, n_q_heads, head_dim, self.splits)
+        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=dev) if ws else None  # zeroed once
+        self.q_rot = torch.empty(batch, n_q_heads, head_dim, dtype=self.dtype, device=dev)
+        self.out = torch.empty(batch, n_q_heads, head_dim, dtype=self.dtype, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.graph = None
+
+    def rope_append(self, q, k_new, v_new, positions, stream=None) -> None:
+        rra.rra_rope_append_q8(q, k_new, v_new, positions, self.q_rot, self.k_cache, self.v_cache, self.k_scale,
+                               self.v_scale, self.k_win, self.v_win, self.block_table, self.rope_base,
+                               self.rope_style, self.err, stream)
+
+    def attend(self, seq_lens, stream=None) -> torch.Tensor:
+        rra.rra_decode_attn_q8(self.q_rot, self.k_cache, self.v_cache, self.k_scale, self.v_scale, seq_lens,
+                               self.out, self.k_win, self.v_win, self.block_table, self.scale, self.num_splits,
+                               self.workspace, self.err, stream)
+        return self.out
+
+    def fused(self, q, k_new, v_new, positions, stream=None) -> torch.Tensor:
+        rra.rra_decode_step_q8(q, k_new, v_new, positions, self.q_rot, self.k_cache, self.v_cache, self.k_scale,
+                               self.v_scale, self.out, self.k_win, self.v_win, self.block_table, self.rope_base,
+                               self.rope_style, self.scale, self.num_splits, self.workspace, self.err, stream)
+        return self.out

@@ -134,3 +134,55 @@ def out_error(got_stored: np.ndarray, want_f64: np.ndarray, dtype: str) -> float
     g = stored_to_f64(got_stored, dtype)
     assert np.all(np.isfinite(g)), "non-finite attention output"
     return float(np.abs(g - want_f64).max())
+
+
+# ---------------------------------------------------------------------------- INT8 cache
+@dataclasses.dataclass
+class GpuQ8Result:
+    q_rot: np.ndarray
+    out: np.ndarray
+    k_codes: np.ndarray
+    v_codes: np.ndarray
+    k_win: Optional[np.ndarray]
+    v_win: Optional[np.ndarray]
+    err: int
+    splits: int
+
+
+def run_gpu_q8(inp: DecodeInputs, num_splits: int = 0, rope_style: int = 0, device="cuda:0",
+               seq_lens: Optional[np.ndarray] = None, fused: bool = False) -> GpuQ8Result:
+    """One INT8-cache step through the C ABI: the fused call or rra_rope_append_q8 + rra_decode_attn_q8."""
+    from rope_gqa_paged_gb300 import DecodeStepQ8
+
+    cfg = inp.cfg
+    kc = torch.from_numpy(np.ascontiguousarray(inp.k_cache)).to(device)
+    vc = torch.from_numpy(np.ascontiguousarray(inp.v_cache)).to(device)
+    kw = to_torch(inp.k_win, "bf16", device) if inp.k_win is not None else None
+    vw = to_torch(inp.v_win, "bf16", device) if inp.v_win is not None else None
+    table = to_torch(inp.block_table, "i32", device) if inp.block_table is not None else None
+    step = DecodeStepQ8(cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, kc, vc,
+                        torch.from_numpy(inp.k_scale).to(device), torch.from_numpy(inp.v_scale).to(device), kw, vw,
+                        table, num_splits=num_splits or cfg.num_splits, rope_base=cfg.rope_base,
+                        rope_style=rope_style)
+    args = (to_torch(inp.q, "bf16", device), to_torch(inp.k_new, "bf16", device), to_torch(inp.v_new, "bf16", device),
+            to_torch(inp.positions, "i32", device))
+    if fused:
+        out = step(*args)
+    else:
+        lens = inp.lengths if seq_lens is None else seq_lens
+        out = step(*args, to_torch(np.asarray(lens, dtype=np.int32), "i32", device))
+    torch.cuda.synchronize(device)
+    res = GpuQ8Result(q_rot=to_numpy(step.q_rot), out=to_numpy(out), k_codes=kc.cpu().numpy(),
+                      v_codes=vc.cpu().numpy(), k_win=to_numpy(kw) if kw is not None else None,
+                      v_win=to_numpy(vw) if vw is not None else None, err=step.error_bits(), splits=step.splits)
+    del kc, vc, kw, vw, step
+    return res
+
+
+def run_oracle_q8(inp: DecodeInputs, rope_style: int = 0, seq_lens=None):
+    """(q_rot, k_codes, v_codes, k_win, v_win, out float64) of the oracle on copies of the caches."""
+    cfg = inp.cfg
+    bs = cfg.block_size if inp.block_table is not None else 0
+    return oracle.quant.decode_step_q8(inp.q, inp.k_new, inp.v_new, inp.positions, inp.k_cache, inp.v_cache,
+                                       inp.k_scale, inp.v_scale, inp.k_win, inp.v_win, cfg.window, inp.block_table,
+                                       bs, seq_lens=seq_lens, rope_base=cfg.rope_base, rope_style=rope_style)

@@ -103,3 +103,52 @@ def test_argument_checks_reject_before_any_launch(rra):
     assert r(P, P, P, P, P, P, P, None, 0, 0, 0, 64, 1, 8, 8, 128, 0.5, 0, 1, None, None) == RRA_EINVAL
     assert r(P, P, P, P, P, P, P, None, 0, 0, 0, 64, 1, 6, 4, 128, 10000.0, 0, 1, None, None) == RRA_EINVAL
     assert r(P, P, P, P, P, P, P, None, 0, 0, 0, 64, 0, 8, 8, 128, 10000.0, 0, 1, None, None) == RRA_OK
+
+
+def test_q8_planning(rra):
+    S = rra.rra_decode_q8_num_splits
+    assert S(1, 32, 8, 128, 131072, 32, 64, 128) == 65                          # 64 INT8 splits + the ring
+    assert S(1, 32, 8, 128, 131072, 32, 64, 0) == 64                            # no window, no ring slot
+    # one split asked for, but a split spans at most 255 block ids of 16 tokens: 3 INT8 splits + the ring
+    assert S(4, 32, 8, 128, 8192, 16, 1, 16) == S(4, 32, 8, 128, 8192, 16, 1, 0) + 1 == 4
+    lib = rra.lib()
+    for bad, status in (((1, 8, 8, 128, 1024, 16, 0, 12), RRA_EUNSUPPORTED),   # window not a multiple of 8
+                        ((1, 8, 8, 128, 1024, 16, 0, -8), RRA_EINVAL),
+                        ((1, 8, 8, 128, 1024, 4, 0, 16), RRA_EUNSUPPORTED),    # blocks under 8 tokens
+                        ((1, 8, 8, 128, 64, 0, 0, 16), RRA_EUNSUPPORTED),      # contiguous cache under one tile
+                        ((1, 8, 8, 96, 1024, 16, 0, 16), RRA_EUNSUPPORTED),
+                        ((1, 6, 4, 128, 1024, 16, 0, 16), RRA_EINVAL)):
+        assert lib.rra_decode_q8_num_splits(*bad) == status, bad
+    # the workspace for INT8 splits + ring slot
+    assert rra.rra_decode_workspace_bytes(1, 32, 128, S(1, 32, 8, 128, 131072, 32, 64, 128)) > \
+        rra.rra_decode_workspace_bytes(1, 32, 128, 64)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-only argument checks; never given fake pointers on a GPU")
+def test_q8_argument_checks_reject_before_any_launch(rra):
+    lib = rra.lib()
+    P = 4096
+    a = lib.rra_decode_attn_q8
+    # (q_rot, kc, vc, ks, vs, kw, vw, W, table, mbps, lens, bs, nblk, max_len, out, B, Hq, Hkv, D, scale, splits,
+    #  ws, ws_bytes, err, stream)
+    ok = [P, P, P, P, P, P, P, 16, P, 64, P, 16, 100, 0, P, 1, 8, 8, 128, 0.0, 1, None, 0, None, None]
+    def call(**kw):
+        args = list(ok)
+        names = ["q", "kc", "vc", "ks", "vs", "kw", "vw", "W", "table", "mbps", "lens", "bs", "nblk", "max_len",
+                 "out", "B", "Hq", "Hkv", "D", "scale", "splits", "ws", "ws_bytes", "err", "stream"]
+        for k, v in kw.items():
+            args[names.index(k)] = v
+        return a(*args)
+    assert call(B=0) == RRA_OK
+    assert call(ks=None) == RRA_EINVAL                                          # scales are required
+    assert call(kw=None) == RRA_EINVAL                                          # a window needs its rings
+    assert call(W=12) == RRA_EUNSUPPORTED
+    assert call(bs=4, nblk=100) == RRA_EUNSUPPORTED
+    assert call(kc=P + 8) == RRA_EINVAL
+    assert call(splits=8) == RRA_EWORKSPACE                                     # several splits need scratch
+    assert call(table=None, max_len=64) == RRA_EUNSUPPORTED                    # contiguous shorter than a tile
+    r = lib.rra_rope_append_q8
+    assert r(P, P, P, P, P, P, P, None, P, P, P, 16, None, 0, 0, 0, 256, 1, 8, 8, 128, 10000.0, 0, None,
+             None) == RRA_EINVAL                                                # missing K scale
+    assert r(P, P, P, P, P, P, P, P, P, None, P, 16, None, 0, 0, 0, 256, 1, 8, 8, 128, 10000.0, 0, None,
+             None) == RRA_EINVAL                                                # missing k ring
