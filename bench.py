@@ -207,9 +207,16 @@ def device_workload(cfg, seed, device):
     g.manual_seed(1000003 * seed + 17)
     B, Hq, Hkv, D = cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     shape = (B, Hkv, cfg.max_len, D) if cfg.layout == "contiguous" else (cfg.num_blocks, cfg.block_size, Hkv, D)
+    if cfg.int8:  # INT8 codes: N(0,1) at a resolution of 1/32, clipped; fixed per-head scales; bf16 rings
+        codes = lambda: torch.randn(shape, generator=g, device=device).mul_(32).round_().clamp_(-127, 127).to(  # noqa: E731
+            torch.int8)
+        kc, vc = codes(), codes()
+    else:
+        kc = torch.randn(shape, generator=g, device=device, dtype=dt)
+        vc = torch.randn(shape, generator=g, device=device, dtype=dt)
     w = {
-        "k_cache": torch.randn(shape, generator=g, device=device, dtype=dt),
-        "v_cache": torch.randn(shape, generator=g, device=device, dtype=dt),
+        "k_cache": kc,
+        "v_cache": vc,
         "q": torch.randn(B, Hq, D, generator=g, device=device, dtype=dt),
         "k_new": torch.randn(B, Hkv, D, generator=g, device=device, dtype=dt),
         "v_new": torch.randn(B, Hkv, D, generator=g, device=device, dtype=dt),
@@ -217,13 +224,21 @@ def device_workload(cfg, seed, device):
         "seq_lens": torch.from_numpy(lengths).to(device),
         "block_table": torch.from_numpy(table).to(device) if table is not None else None,
     }
+    if cfg.int8:
+        h = np.arange(Hkv)
+        w["k_scale"] = torch.from_numpy(((1.0 + (h % 4) / 8.0) / 32.0).astype(np.float32)).to(device)
+        w["v_scale"] = torch.from_numpy(((1.0 + ((h + 2) % 4) / 8.0) / 32.0).astype(np.float32)).to(device)
+        w["k_win"] = w["v_win"] = None
+        if cfg.window:
+            w["k_win"] = torch.randn(B, Hkv, cfg.window, D, generator=g, device=device, dtype=torch.bfloat16)
+            w["v_win"] = torch.randn(B, Hkv, cfg.window, D, generator=g, device=device, dtype=torch.bfloat16)
     return w, lengths
 
 
 def run_ours(args):
     import torch
 
-    from rope_gqa_paged_gb300 import DecodeStep, _build
+    from rope_gqa_paged_gb300 import DecodeStep, DecodeStepQ8, _build
 
     rank, local_rank, world = dist_env()
     if world > 1:
@@ -243,11 +258,17 @@ def run_ours(args):
     # Without prefix sharing this equals the logical bytes the attention consumes.
     kv_bytes = cfg.unique_kv_bytes(lengths)
     logical_bytes = cfg.kv_bytes(lengths)
-    step = DecodeStep(cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, w["k_cache"], w["v_cache"],
-                      w["block_table"], num_splits=splits_arg, rope_base=cfg.rope_base)
-    # the fused step is one kernel for bf16 with the tensor-core path, else rope + decode
-    mma_path = cfg.dtype == "bf16" and ((cfg.layout == "paged" and cfg.block_size >= 8) or
-                                        (cfg.layout == "contiguous" and cfg.max_len >= 16384 // (2 * cfg.head_dim)))
+    if cfg.int8:
+        step = DecodeStepQ8(cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, w["k_cache"], w["v_cache"],
+                            w["k_scale"], w["v_scale"], w["k_win"], w["v_win"], w["block_table"],
+                            num_splits=splits_arg, rope_base=cfg.rope_base)
+    else:
+        step = DecodeStep(cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, w["k_cache"], w["v_cache"],
+                          w["block_table"], num_splits=splits_arg, rope_base=cfg.rope_base)
+    # the fused step is one kernel for INT8 caches and for bf16 with the tensor-core path, else rope + decode
+    mma_path = cfg.int8 or (cfg.dtype == "bf16" and (
+        (cfg.layout == "paged" and cfg.block_size >= 8) or
+        (cfg.layout == "contiguous" and cfg.max_len >= 16384 // (2 * cfg.head_dim))))
     launches_per_step = 1 if mma_path else 2
     flush = None
     if 2 * kv_bytes < 3 * L2_BYTES:                     # inputs not much larger than L2: flush between steps
@@ -360,7 +381,7 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded N(0,1); lengths/tables from the recipe)",
+        "vs_baseline": None, "dtype": "int8 K/V codes + bf16 window, f16 mma, f32 softmax" if cfg.int8 else cfg.dtype, "data": "synthetic (seeded N(0,1); lengths/tables from the recipe)",
         "config": {
             "workload": cfg.name, "description": cfg.description, "batch_per_gpu": cfg.batch,
             "n_q_heads": cfg.n_q_heads, "n_kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim,
@@ -381,7 +402,9 @@ def run_ours(args):
                                                                        "decode_attn": round(dec_avg, 5),
                                                                        "both": round(eager_ms, 5)}},
         "step_timing": graph_note,
-        "roofline": {"kernel": ("decode_mma_kernel, fused step (RoPE + append + split-K attention + merge)"
+        "roofline": {"kernel": ("decode_q8_kernel, fused step (RoPE + quantised append + split-K attention over "
+                                "INT8 codes and the bf16 window + merge)" if cfg.int8 else
+                                "decode_mma_kernel, fused step (RoPE + append + split-K attention + merge)"
                                 if mma_path else "rope_append + decode_split_kernel (fused-step call)"),
                      "bound": "hbm",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
@@ -417,8 +440,14 @@ def oracle_step_seconds(inp):
     cfg = inp.cfg
     bs = cfg.block_size if inp.block_table is not None else 0
     t0 = time.perf_counter()
-    odecode.decode_step(inp.q, inp.k_new, inp.v_new, inp.positions, inp.k_cache, inp.v_cache, cfg.dtype,
-                        inp.block_table, bs, rope_base=cfg.rope_base)
+    if cfg.int8:
+        from oracle import quant
+        quant.decode_step_q8(inp.q, inp.k_new, inp.v_new, inp.positions, inp.k_cache, inp.v_cache, inp.k_scale,
+                             inp.v_scale, inp.k_win, inp.v_win, cfg.window, inp.block_table, bs,
+                             rope_base=cfg.rope_base)
+    else:
+        odecode.decode_step(inp.q, inp.k_new, inp.v_new, inp.positions, inp.k_cache, inp.v_cache, cfg.dtype,
+                            inp.block_table, bs, rope_base=cfg.rope_base)
     return time.perf_counter() - t0
 
 

@@ -13,13 +13,14 @@
 // a window, one more unit per (sequence, KV head, head slice) streams the ring (the last grid
 // column). Each unit publishes one partial and the last to finish merges them.
 //
-// INT8 tiles (K and V, 16 KB each per stage, D-byte rows with the TMA swizzle) go through the
-// tensor cores as f16: ldmatrix loads 4 codes per lane, a byte permute places each code under
-// the f16 exponent of 1024 (0x64xx = 1024 + byte) after flipping its sign bit, and one f16x2
-// subtraction of 1152 leaves the code exactly. The dimension order inside each 16-dim slice is
-// permuted so the loaded bytes are already in mma fragment order:
+// INT8 tiles (K and V codes, D-byte rows with the TMA swizzle) go through the tensor cores as
+// f16: ldmatrix loads 4 codes per lane; one lop3 keeps bytes 0 and 2 (or, after a shift, 1 and
+// 3), flips their sign bits and puts the f16 exponent of 1024 above them (0x64xx = 1024 + byte),
+// and one f16x2 subtraction of 1152 leaves each code exactly. The dimension order inside each
+// 16-dim slice is permuted so those byte pairs are already in mma fragment order:
 //   scores  S^T[16 tok x 8 heads] = C_K[16 tok x D] . Q'^T   with lane (g, t) holding dims
-//           4t..4t+3 of a slice as k = {2t, 2t+1, 2t+8, 2t+9} (q loaded in the same order);
+//           4t..4t+3 of a slice, dims (4t, 4t+2) as k = (2t, 2t+1) and (4t+1, 4t+3) as
+//           k = (2t+8, 2t+9) (q packed in the same order);
 //   output  O^T[D x 8 heads] += C_V^T . P   with ldmatrix.trans giving lane (g, t) dims
 //           2g, 2g+1 of tokens 2t, 2t+1 (and +8), so fragment row g is dim 2g and row g+8 is
 //           dim 2g+1 of each 16-dim slice.
@@ -27,6 +28,11 @@
 // for bf16 values; the scores are multiplied by s_K * scale * log2(e) * 2^-e_h in float32 and
 // the output by s_V, so the only roundings are those of the f16 probabilities and the float32
 // accumulation.
+//
+// Pipeline: RRA_Q8_STAGES stages of RRA_Q8_STAGE_BYTES (four of 16 KB by default: 64 INT8
+// tokens at D = 128, one 16-token mma step per consumer warp), so about three quarters of the
+// ring is in flight while the consumers work on one stage. The ring unit reuses the same
+// memory as two 32 KB bf16 stages.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -37,16 +43,18 @@ namespace rra {
 
 template <int D>
 struct Q8Cfg {
-  static constexpr int kTile = 16384 / D;          // INT8 tokens per stage (K 16 KB + V 16 KB)
-  static constexpr int kTileBytes = kTile * D;
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static_assert(kStageBytes == MmaCfg<D>::kStageBytes, "window tiles reuse the INT8 stages");
-  static constexpr int kStages = MmaCfg<D>::kStages;
+  static constexpr int kStageBytes = RRA_Q8_STAGE_BYTES;
+  static constexpr int kTileBytes = kStageBytes / 2;     // K or V codes of one stage
+  static constexpr int kTile = kTileBytes / D;           // INT8 tokens per stage
+  static constexpr int kStages = RRA_Q8_STAGES;
   static constexpr int kConsumerWarps = 4;
   static constexpr int kThreads = (kConsumerWarps + 1) * 32;
   static constexpr int kWarpTokens = kTile / kConsumerWarps;
   static constexpr int kSteps = kWarpTokens / 16;
+  static_assert(kSteps >= 1 && kWarpTokens % 16 == 0, "each consumer warp takes whole 16-token steps");
   static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kWinStages = 2;                   // the ring unit: bf16 stages of MmaCfg<D>
+  static_assert(kRingBytes >= kWinStages * MmaCfg<D>::kStageBytes, "the ring unit needs two bf16 stages");
   // after the ring: full[kStages], empty[kStages], appended; the block-id table; cos/sin
   // hi/lo [4][D/2] floats; the rotated q rows [8][D] bf16 (fused step)
   static constexpr int kOffBar = kRingBytes;
@@ -70,18 +78,18 @@ __device__ __forceinline__ uint32_t f16x2_minus_1152(uint32_t x) {
   return y;
 }
 
-// Four INT8 codes (bytes 0..3 of w) as exact f16 pairs (bytes 0,1) and (bytes 2,3).
-__device__ __forceinline__ void s8x4_to_f16_01_23(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t u = w ^ 0x80808080u;  // code + 128 as an unsigned byte
-  lo = f16x2_minus_1152(__byte_perm(u, 0x64646464u, 0x5140));
-  hi = f16x2_minus_1152(__byte_perm(u, 0x64646464u, 0x7362));
+// Bytes 0 and 2 of w with their sign bits flipped, each under the f16 exponent byte 0x64:
+// per bit, b ? (a ^ c) : c with b = 0x00ff00ff and c = 0x64806480 (lop3 table 0x6a).
+__device__ __forceinline__ uint32_t bytes02_to_f16_biased(uint32_t w) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(d) : "r"(w), "r"(0x00ff00ffu), "r"(0x64806480u));
+  return d;
 }
 
-// The same codes as f16 pairs (bytes 0,2) and (bytes 1,3).
-__device__ __forceinline__ void s8x4_to_f16_02_13(uint32_t w, uint32_t& ev, uint32_t& od) {
-  const uint32_t u = w ^ 0x80808080u;
-  ev = f16x2_minus_1152(__byte_perm(u, 0x64646464u, 0x5240));
-  od = f16x2_minus_1152(__byte_perm(u, 0x64646464u, 0x5341));
+// Four INT8 codes (bytes 0..3 of w) as exact f16 pairs (bytes 0, 2) and (bytes 1, 3).
+__device__ __forceinline__ void s8x4_to_f16_even_odd(uint32_t w, uint32_t& ev, uint32_t& od) {
+  ev = f16x2_minus_1152(bytes02_to_f16_biased(w));
+  od = f16x2_minus_1152(bytes02_to_f16_biased(__umulhi(w, 0x01000000u)));  // w >> 8 on the multiply pipe
 }
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -110,11 +118,11 @@ __device__ __forceinline__ void q8_step(MmaWarpState<D>& st, const uint32_t (&qh
   for (int cc = 0; cc < D / 32; ++cc) {
     uint32_t w[4], a[4];
     ldsm_x4(k_base + swz8<D>(r, 2 * cc + (mat >> 1)), w);
-    s8x4_to_f16_01_23(w[0], a[0], a[2]);
-    s8x4_to_f16_01_23(w[1], a[1], a[3]);
+    s8x4_to_f16_even_odd(w[0], a[0], a[2]);
+    s8x4_to_f16_even_odd(w[1], a[1], a[3]);
     mma_f16(s, a, qh[2 * cc][0], qh[2 * cc][1]);
-    s8x4_to_f16_01_23(w[2], a[0], a[2]);
-    s8x4_to_f16_01_23(w[3], a[1], a[3]);
+    s8x4_to_f16_even_odd(w[2], a[0], a[2]);
+    s8x4_to_f16_even_odd(w[3], a[1], a[3]);
     mma_f16(s, a, qh[2 * cc + 1][0], qh[2 * cc + 1][1]);
   }
   const int ta = t0 + (lane >> 2), tb = ta + 8;
@@ -165,11 +173,11 @@ __device__ __forceinline__ void q8_step(MmaWarpState<D>& st, const uint32_t (&qh
   for (int cc = 0; cc < D / 32; ++cc) {
     uint32_t w[4], a[4];
     ldsm_x4_trans(v_base + swz8<D>(r, 2 * cc + (mat >> 1)), w);
-    s8x4_to_f16_02_13(w[0], a[0], a[1]);
-    s8x4_to_f16_02_13(w[1], a[2], a[3]);
+    s8x4_to_f16_even_odd(w[0], a[0], a[1]);
+    s8x4_to_f16_even_odd(w[1], a[2], a[3]);
     mma_f16(st.o[2 * cc], a, b0, b1);
-    s8x4_to_f16_02_13(w[2], a[0], a[1]);
-    s8x4_to_f16_02_13(w[3], a[2], a[3]);
+    s8x4_to_f16_even_odd(w[2], a[0], a[1]);
+    s8x4_to_f16_even_odd(w[3], a[2], a[3]);
     mma_f16(st.o[2 * cc + 1], a, b0, b1);
   }
 }
@@ -281,10 +289,13 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
         prefetch_tensormap(&k_map);
         prefetch_tensormap(&v_map);
       }
+      // the ring unit runs two 32 KB bf16 stages over the same memory and barriers
+      const int nst = win_unit ? C::kWinStages : C::kStages;
+      const int stage_bytes = win_unit ? M::kStageBytes : C::kStageBytes;
       int issued = 0;
       for (int it = 0; it < n_tiles; ++it) {
-        const int s = it % C::kStages;
-        if (it >= C::kStages && !mbar_wait(&empty[s], ((it / C::kStages) - 1) & 1)) {
+        const int s = it % nst;
+        if (it >= nst && !mbar_wait(&empty[s], ((it / nst) - 1) & 1)) {
           flag_error(a.err, RRA_ERR_TIMEOUT);
           break;
         }
@@ -294,7 +305,7 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
           break;
         }
         const int t0 = start + it * rows;
-        uint8_t* kst = smem + s * C::kStageBytes;
+        uint8_t* kst = smem + s * stage_bytes;
         if (win_unit) {  // bf16 ring rows [t0, t0 + rows) of (b, g) in 64-dim halves
           uint8_t* vst = kst + M::kHalves * M::kHalfBytes;
           mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * M::kHalves * rows * 128));
@@ -334,8 +345,7 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
         }
         issued = it + 1;
       }
-      for (int it = issued > C::kStages ? issued - C::kStages : 0; it < issued; ++it)
-        mbar_wait(&full[it % C::kStages], (it / C::kStages) & 1);
+      for (int it = issued > nst ? issued - nst : 0; it < issued; ++it) mbar_wait(&full[it % nst], (it / nst) & 1);
     }
     return;
   }
@@ -442,12 +452,12 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
 
   if (win_unit) {
     for (int it = 0; it < n_tiles; ++it) {
-      const int s = it % C::kStages;
-      if (!mbar_wait(&full[s], (it / C::kStages) & 1)) {
+      const int s = it % C::kWinStages;
+      if (!mbar_wait(&full[s], (it / C::kWinStages) & 1)) {
         flag_error(a.err, RRA_ERR_TIMEOUT);
         break;
       }
-      uint8_t* kst = smem + s * C::kStageBytes;
+      uint8_t* kst = smem + s * M::kStageBytes;
       uint8_t* vst = kst + M::kHalves * M::kHalfBytes;
       const uint32_t k_base = smem_addr(kst), v_base = smem_addr(vst);
       const int valid = min(rows, end - (start + it * rows));
@@ -490,8 +500,8 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
       down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
 #pragma unroll
       for (int c = 0; c < D / 16; ++c) {
-        qh[c][0] = pack_f16x2(xq[c][0] * up, xq[c][1] * up);
-        qh[c][1] = pack_f16x2(xq[c][2] * up, xq[c][3] * up);
+        qh[c][0] = pack_f16x2(xq[c][0] * up, xq[c][2] * up);   // dims 4t, 4t+2 as k = 2t, 2t+1
+        qh[c][1] = pack_f16x2(xq[c][1] * up, xq[c][3] * up);   // dims 4t+1, 4t+3 as k = 2t+8, 2t+9
       }
     }
     float mult[2];

@@ -91,7 +91,9 @@ int check_shapes(int B, int Hq, int Hkv, int D, rra_dtype dt) {
 
 // Chunk and split count for a per-sequence capacity of max_tokens, once p->mma, p->hpc and
 // p->tile are set.
-int plan_splits(int B, int Hkv, int n_rep, int64_t max_tokens, int block_size, int requested, Plan* p) {
+// extra_units: CTAs per (sequence, head slice) beyond the splits (the INT8 kernel's ring unit).
+int plan_splits(int B, int Hkv, int n_rep, int64_t max_tokens, int block_size, int requested, Plan* p,
+                int extra_units = 0) {
   const int64_t tiles = std::max<int64_t>(1, (max_tokens + p->tile - 1) / p->tile);
   // A paged split copies its block ids to shared memory: at most kMaxTableEntries of them.
   int64_t max_chunk_tiles = tiles;
@@ -109,7 +111,7 @@ int plan_splits(int B, int Hkv, int n_rep, int64_t max_tokens, int block_size, i
     if (2 * units <= resident) {
       // Few sequences x heads: as many splits as fit in ONE wave (a second wave that is barely
       // started costs a whole CTA time), each at least 256 tokens long.
-      const int64_t splits_one_wave = std::max<int64_t>(1, resident / units);
+      const int64_t splits_one_wave = std::max<int64_t>(1, resident / units - extra_units);
       chunk_tiles = (tiles + splits_one_wave - 1) / splits_one_wave;
       chunk_tiles = std::max<int64_t>(chunk_tiles, std::max(1, 256 / p->tile));
     } else {
@@ -162,7 +164,7 @@ int make_plan_q8(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_si
   if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
   p->tile = rra::decode_q8_tile_tokens(D);
   if (block_size > 0 ? block_size < 8 : max_tokens < p->tile) return RRA_EUNSUPPORTED;
-  st = plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
+  st = plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p, window > 0 ? 1 : 0);
   if (st != RRA_OK) return st;
   if (window > 0) ++p->splits;
   return RRA_OK;

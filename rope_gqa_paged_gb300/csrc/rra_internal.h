@@ -114,8 +114,15 @@ cudaError_t launch_decode_step_contig(const DecodeArgs& a, const CUtensorMap& k_
                                       cudaStream_t stream);
 cudaError_t launch_decode_step_paged(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
                                      cudaStream_t stream);
-// Tokens per stage of the INT8 decode kernel (K + V codes, 32 KB).
-inline int decode_q8_tile_tokens(int D) { return 16384 / D; }
+// Pipeline of the INT8 decode kernel: RRA_Q8_STAGES stages of RRA_Q8_STAGE_BYTES (K + V codes).
+#ifndef RRA_Q8_STAGES
+#define RRA_Q8_STAGES 4
+#endif
+#ifndef RRA_Q8_STAGE_BYTES
+#define RRA_Q8_STAGE_BYTES 16384
+#endif
+// Tokens per stage of the INT8 decode kernel.
+inline int decode_q8_tile_tokens(int D) { return RRA_Q8_STAGE_BYTES / 2 / D; }
 // INT8 caches: attention only (a.seq_lens) or the fused step (a.positions, a.k_new, ...).
 // k_map / v_map cover the code caches, kw_map / vw_map the bf16 rings (unused without a window).
 cudaError_t launch_decode_q8(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,

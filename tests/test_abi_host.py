@@ -115,7 +115,7 @@ def test_q8_planning(rra):
     for bad, status in (((1, 8, 8, 128, 1024, 16, 0, 12), RRA_EUNSUPPORTED),   # window not a multiple of 8
                         ((1, 8, 8, 128, 1024, 16, 0, -8), RRA_EINVAL),
                         ((1, 8, 8, 128, 1024, 4, 0, 16), RRA_EUNSUPPORTED),    # blocks under 8 tokens
-                        ((1, 8, 8, 128, 64, 0, 0, 16), RRA_EUNSUPPORTED),      # contiguous cache under one tile
+                        ((1, 8, 8, 128, 32, 0, 0, 16), RRA_EUNSUPPORTED),      # contiguous cache under one tile
                         ((1, 8, 8, 96, 1024, 16, 0, 16), RRA_EUNSUPPORTED),
                         ((1, 6, 4, 128, 1024, 16, 0, 16), RRA_EINVAL)):
         assert lib.rra_decode_q8_num_splits(*bad) == status, bad
@@ -146,7 +146,7 @@ def test_q8_argument_checks_reject_before_any_launch(rra):
     assert call(bs=4, nblk=100) == RRA_EUNSUPPORTED
     assert call(kc=P + 8) == RRA_EINVAL
     assert call(splits=8) == RRA_EWORKSPACE                                     # several splits need scratch
-    assert call(table=None, max_len=64) == RRA_EUNSUPPORTED                    # contiguous shorter than a tile
+    assert call(table=None, max_len=32) == RRA_EUNSUPPORTED                    # contiguous shorter than a tile
     r = lib.rra_rope_append_q8
     assert r(P, P, P, P, P, P, P, None, P, P, P, 16, None, 0, 0, 0, 256, 1, 8, 8, 128, 10000.0, 0, None,
              None) == RRA_EINVAL                                                # missing K scale
