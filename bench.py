@@ -45,6 +45,9 @@ L2_BYTES = 129 * 2 ** 20
 KERNEL_SOURCES = ["rope_gqa_paged_gb300/csrc/decode_mma.cuh", "rope_gqa_paged_gb300/csrc/decode_kernels.cuh",
                   "rope_gqa_paged_gb300/csrc/rra_device.cuh", "rope_gqa_paged_gb300/csrc/decode_paged.cu",
                   "rope_gqa_paged_gb300/csrc/decode_contig.cu"]
+KERNEL_SOURCES_INT8 = KERNEL_SOURCES + ["rope_gqa_paged_gb300/csrc/decode_q8.cuh",
+                                        "rope_gqa_paged_gb300/csrc/decode_q8.cu",
+                                        "rope_gqa_paged_gb300/csrc/rra_internal.h"]
 
 
 def parse_args(argv=None):
@@ -98,9 +101,9 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(int8: bool = False) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in (KERNEL_SOURCES_INT8 if int8 else KERNEL_SOURCES):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -118,7 +121,8 @@ def recorded_traffic(workload: str):
         for key in ("traffic_bytes_per_launch", "kernel_source_sha256"):
             if line.strip().startswith(key + ":"):
                 vals[key] = line.split(":", 1)[1].strip().split()[0]
-    if vals.get("kernel_source_sha256") != kernel_source_hash() or "traffic_bytes_per_launch" not in vals:
+    int8 = CONFIGS[workload].int8 if workload in CONFIGS else False
+    if vals.get("kernel_source_sha256") != kernel_source_hash(int8) or "traffic_bytes_per_launch" not in vals:
         return None
     return int(vals["traffic_bytes_per_launch"])
 

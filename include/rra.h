@@ -201,9 +201,9 @@ RRA_API int rra_rope_append_q8(const void* q, const void* k_new, const void* v_n
 
 /* Attention of q_rot over the L_b = seq_lens[b] tokens of the mixed-precision cache (codes
  * times scales, then the window's bf16 tokens), split-K as rra_decode_attn_paged. The INT8
- * tokens are cut into splits (num_splits, 0 = chosen by the library) and the ring is one more
- * partial; the workspace must hold rra_decode_workspace_bytes(B, Hq, D,
- * rra_decode_q8_num_splits(...)) bytes, with the same zero-fill rule. */
+ * tokens are cut into splits (num_splits, 0 = chosen by the library); the split holding the
+ * last INT8 tokens also reads the ring. The workspace must hold rra_decode_workspace_bytes(B,
+ * Hq, D, rra_decode_q8_num_splits(...)) bytes, with the same zero-fill rule. */
 RRA_API int rra_decode_attn_q8(const void* q_rot, const void* k_codes, const void* v_codes, const float* k_scale,
                                const float* v_scale, const void* k_win, const void* v_win, int window,
                                const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
@@ -222,8 +222,8 @@ RRA_API int rra_decode_step_q8(const void* q, const void* k_new, const void* v_n
                                double rope_base, int rope_style, float scale, int num_splits, void* workspace,
                                size_t ws_bytes, int32_t* err_flag, void* stream);
 
-/* Partial slots the INT8 decode uses (INT8 splits, plus one for the ring when window > 0):
- * the `splits` argument of rra_decode_workspace_bytes. max_tokens and block_size as in
+/* Effective INT8 split count of rra_decode_attn_q8 / rra_decode_step_q8: the `splits`
+ * argument of rra_decode_workspace_bytes. max_tokens and block_size as in
  * rra_decode_num_splits. Negative rra_status on bad arguments. */
 RRA_API int rra_decode_q8_num_splits(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
                                      int num_splits, int window);

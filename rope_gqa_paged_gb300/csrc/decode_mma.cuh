@@ -113,7 +113,8 @@ struct MmaWarpState {
 
 // One 16-token slice of a stage for one warp. CHECK: tokens at or past `valid` are masked
 // (their V rows are zeroed first, so NaN or stale data never reaches the tensor cores).
-template <int D, bool CHECK>
+// HALF: bytes of one 64-dim half of K or V in the stage (rows of the tile x 128).
+template <int D, bool CHECK, int HALF = MmaCfg<D>::kHalfBytes>
 __device__ __forceinline__ void mma_step(MmaWarpState<D>& st, const uint32_t (&qb)[D / 16][2], uint32_t k_base,
                                          uint32_t v_base, uint8_t* v_gen, int t0, int valid, int lane,
                                          float scale_log2) {
@@ -124,7 +125,7 @@ __device__ __forceinline__ void mma_step(MmaWarpState<D>& st, const uint32_t (&q
       for (int idx = lane; idx < (16 - first) * C::kHalves * 8; idx += 32) {
         const int r = t0 + first + idx / (C::kHalves * 8);
         const int h = (idx / 8) % C::kHalves, c = idx % 8;
-        *reinterpret_cast<uint4*>(v_gen + h * C::kHalfBytes + swz(r, c)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(v_gen + h * HALF + swz(r, c)) = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async_smem();  // these generic writes precede the next TMA write of the stage
       __syncwarp();
@@ -138,7 +139,7 @@ __device__ __forceinline__ void mma_step(MmaWarpState<D>& st, const uint32_t (&q
 #pragma unroll
     for (int kk = 0; kk < C::kKSteps; ++kk) {
       uint32_t a[4];
-      ldsm_x4(k_base + (kk >> 2) * C::kHalfBytes + swz(r, ((kk & 3) << 1) + (mat >> 1)), a);
+      ldsm_x4(k_base + (kk >> 2) * HALF + swz(r, ((kk & 3) << 1) + (mat >> 1)), a);
       mma_bf16(s, a, qb[kk][0], qb[kk][1]);
     }
   }
@@ -194,7 +195,7 @@ __device__ __forceinline__ void mma_step(MmaWarpState<D>& st, const uint32_t (&q
 #pragma unroll
     for (int i = 0; i < D / 16; ++i) {
       uint32_t a[4];
-      ldsm_x4_trans(v_base + (i >> 2) * C::kHalfBytes + swz(r, ((i & 3) << 1) + (mat & 1)), a);
+      ldsm_x4_trans(v_base + (i >> 2) * HALF + swz(r, ((i & 3) << 1) + (mat & 1)), a);
       mma_bf16(st.o[i], a, b0, b1);
     }
   }

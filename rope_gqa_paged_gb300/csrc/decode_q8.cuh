@@ -9,9 +9,11 @@
 // last min(L, W) tokens from the ring; the softmax and the split/merge are those of
 // decode_mma.cuh.
 //
-// Work units: the INT8 tokens are cut into splits of `chunk` tokens as in the bf16 kernel; with
-// a window, one more unit per (sequence, KV head, head slice) streams the ring (the last grid
-// column). Each unit publishes one partial and the last to finish merges them.
+// Work units: the INT8 tokens are cut into splits of `chunk` tokens as in the bf16 kernel. The
+// CTA of the last split that holds INT8 tokens (split 0 when there are none) then streams the
+// ring through the same stages as bf16 tiles of 32 tokens (D = 128), after turning its INT8
+// accumulator into the bf16 fragment layout (warp shuffles, times s_V), so every CTA publishes
+// one partial and the last to finish merges them.
 //
 // INT8 tiles (K and V codes, D-byte rows with the TMA swizzle) go through the tensor cores as
 // f16: ldmatrix loads 4 codes per lane; one lop3 keeps bytes 0 and 2 (or, after a shift, 1 and
@@ -30,9 +32,8 @@
 // accumulation.
 //
 // Pipeline: RRA_Q8_STAGES stages of RRA_Q8_STAGE_BYTES (four of 16 KB by default: 64 INT8
-// tokens at D = 128, one 16-token mma step per consumer warp), so about three quarters of the
-// ring is in flight while the consumers work on one stage. The ring unit reuses the same
-// memory as two 32 KB bf16 stages.
+// tokens at D = 128, one 16-token mma step per consumer warp; or 32 bf16 ring tokens, taken by
+// two of the four warps).
 #pragma once
 
 #include <cuda_fp16.h>
@@ -53,8 +54,9 @@ struct Q8Cfg {
   static constexpr int kSteps = kWarpTokens / 16;
   static_assert(kSteps >= 1 && kWarpTokens % 16 == 0, "each consumer warp takes whole 16-token steps");
   static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kWinStages = 2;                   // the ring unit: bf16 stages of MmaCfg<D>
-  static_assert(kRingBytes >= kWinStages * MmaCfg<D>::kStageBytes, "the ring unit needs two bf16 stages");
+  static constexpr int kWinTile = kStageBytes / (4 * D);  // bf16 ring tokens per stage (K + V)
+  static constexpr int kWinHalf = kWinTile * 128;         // one 64-dim half of a ring tile
+  static_assert(kWinTile % 16 == 0 && kWinTile / 16 <= kConsumerWarps, "ring tiles: whole steps, one per warp");
   // after the ring: full[kStages], empty[kStages], appended; the block-id table; cos/sin
   // hi/lo [4][D/2] floats; the rotated q rows [8][D] bf16 (fused step)
   static constexpr int kOffBar = kRingBytes;
@@ -182,6 +184,25 @@ __device__ __forceinline__ void q8_step(MmaWarpState<D>& st, const uint32_t (&qh
   }
 }
 
+// Moves an INT8-phase accumulator (fragment rows g / g+8 = dims 2g / 2g+1 of each 16-dim slice,
+// in code units) into the bf16 layout (rows g / g+8 = dims g / g+8), times the V scale.
+template <int D>
+__device__ __forceinline__ void q8_acc_to_bf16_layout(MmaWarpState<D>& st, float vs, int lane) {
+  const int dl = lane >> 2, t = lane & 3;
+  const int src0 = ((dl >> 1) << 2) | t, src1 = (((dl >> 1) + 4) << 2) | t;  // owners of dims dl, dl + 8
+  const bool odd = dl & 1;
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float e0 = __shfl_sync(0xffffffffu, st.o[i][j], src0), o0 = __shfl_sync(0xffffffffu, st.o[i][2 + j], src0);
+      const float e1 = __shfl_sync(0xffffffffu, st.o[i][j], src1), o1 = __shfl_sync(0xffffffffu, st.o[i][2 + j], src1);
+      st.o[i][j] = (odd ? o0 : e0) * vs;
+      st.o[i][2 + j] = (odd ? o1 : e1) * vs;
+    }
+  }
+}
+
 template <int D, bool PAGED, bool FUSED>
 __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     decode_q8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
@@ -200,7 +221,6 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   const int h0 = g * n_rep + (blockIdx.x - split * slices) * hpc;
   const int b = blockIdx.z;
   const bool has_win = a.window > 0;
-  const bool win_unit = has_win && split == a.num_splits - 1;
 
   int L;
   if constexpr (FUSED) {
@@ -220,31 +240,25 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   const int Lw = has_win ? min(L, a.window) : 0;  // tokens read from the ring
   const int Lq = L - Lw;                          // tokens read as INT8 codes
   const int nq = (Lq + a.chunk - 1) / a.chunk;
-  const int n_work = nq + (Lw > 0 ? 1 : 0);
-  int start, end, part;
-  if (win_unit) {
-    if (Lw == 0) return;
-    start = 0;
-    end = Lw;
-    part = nq;
-  } else {
-    start = split * a.chunk;
-    if (start >= Lq) {
-      if (L == 0 && split == 0) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(b) * a.Hq + h0) * D;
-        for (int i = threadIdx.x; i < hpc * D; i += blockDim.x) out[i] = __float2bfloat16_rn(0.f);
-      }
-      return;
+  const int n_work = max(nq, Lw > 0 ? 1 : 0);     // one partial per CTA with tokens
+  const bool ring_owner = Lw > 0 && split == max(nq - 1, 0);
+  const int start = split * a.chunk;
+  if (start >= Lq && !ring_owner) {
+    if (L == 0 && split == 0) {
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(b) * a.Hq + h0) * D;
+      for (int i = threadIdx.x; i < hpc * D; i += blockDim.x) out[i] = __float2bfloat16_rn(0.f);
     }
-    end = min(Lq, start + a.chunk);
-    part = split;
+    return;
   }
-  const int rows = win_unit ? min(M::kTile, a.window) : C::kTile;  // tokens per stage of this unit
-  const int n_tiles = (end - start + rows - 1) / rows;
-  // Fused step: the unit that reads the new token writes it first (the window unit, else the
-  // INT8 unit whose chunk ends at L); the unit whose warp 0 publishes q_rot always has tokens.
-  const bool appender = FUSED && (has_win ? win_unit : end == L);
-  const bool publisher = FUSED && (has_win ? win_unit : split == 0);
+  const int end = min(Lq, start + a.chunk);
+  const int n_q8 = start < Lq ? (end - start + C::kTile - 1) / C::kTile : 0;
+  const int wrows = min(C::kWinTile, max(a.window, 1));   // ring rows per tile
+  const int n_win = ring_owner ? (Lw + wrows - 1) / wrows : 0;
+  const int n_tiles = n_q8 + n_win;
+  // Fused step: the CTA that reads the new token writes it first (the ring owner, else the CTA
+  // whose INT8 chunk ends at L); the CTA whose warp 0 publishes q_rot always has tokens.
+  const bool appender = FUSED && (has_win ? ring_owner : end == L);
+  const bool publisher = FUSED && (has_win ? ring_owner : split == 0);
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* empty = full + C::kStages;
@@ -264,7 +278,7 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     fence_barrier_init();
   }
   int first_blk = 0;
-  if (PAGED && !win_unit) {
+  if (PAGED && n_q8 > 0) {
     first_blk = start >> a.log2_bs;
     const int n_blk = ((end - 1) >> a.log2_bs) - first_blk + 1;
     const int32_t* row = a.block_table + static_cast<size_t>(b) * a.max_blocks_per_seq + first_blk;
@@ -282,40 +296,39 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   // ------------------------------------------------------------------ producer
   if (warp == C::kConsumerWarps) {
     if (lane == 0) {
-      if (win_unit) {
-        prefetch_tensormap(&kw_map);
-        prefetch_tensormap(&vw_map);
-      } else {
+      if (n_q8 > 0) {
         prefetch_tensormap(&k_map);
         prefetch_tensormap(&v_map);
       }
-      // the ring unit runs two 32 KB bf16 stages over the same memory and barriers
-      const int nst = win_unit ? C::kWinStages : C::kStages;
-      const int stage_bytes = win_unit ? M::kStageBytes : C::kStageBytes;
+      if (n_win > 0) {
+        prefetch_tensormap(&kw_map);
+        prefetch_tensormap(&vw_map);
+      }
       int issued = 0;
       for (int it = 0; it < n_tiles; ++it) {
-        const int s = it % nst;
-        if (it >= nst && !mbar_wait(&empty[s], ((it / nst) - 1) & 1)) {
+        const int s = it % C::kStages;
+        if (it >= C::kStages && !mbar_wait(&empty[s], ((it / C::kStages) - 1) & 1)) {
           flag_error(a.err, RRA_ERR_TIMEOUT);
           break;
         }
-        // the new token: in the ring (any tile of it) or in the last INT8 tile of the appender
-        if (appender && (win_unit ? it == 0 : it == n_tiles - 1) && !mbar_wait(appended, 0)) {
+        // the new token: in the ring (before its first tile) or in the appender's last INT8 tile
+        if (appender && it == (has_win ? n_q8 : n_q8 - 1) && !mbar_wait(appended, 0)) {
           flag_error(a.err, RRA_ERR_TIMEOUT);
           break;
         }
-        const int t0 = start + it * rows;
-        uint8_t* kst = smem + s * stage_bytes;
-        if (win_unit) {  // bf16 ring rows [t0, t0 + rows) of (b, g) in 64-dim halves
-          uint8_t* vst = kst + M::kHalves * M::kHalfBytes;
-          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * M::kHalves * rows * 128));
+        uint8_t* kst = smem + s * C::kStageBytes;
+        if (it >= n_q8) {  // bf16 ring rows [t0, t0 + wrows) of (b, g) in 64-dim halves
+          const int t0 = (it - n_q8) * wrows;
+          uint8_t* vst = kst + M::kHalves * C::kWinHalf;
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * M::kHalves * wrows * 128));
           const int bg = b * a.Hkv + g;
 #pragma unroll
           for (int h = 0; h < M::kHalves; ++h) {
-            tma_g2s_3d(kst + h * M::kHalfBytes, &kw_map, 64 * h, t0, bg, &full[s]);
-            tma_g2s_3d(vst + h * M::kHalfBytes, &vw_map, 64 * h, t0, bg, &full[s]);
+            tma_g2s_3d(kst + h * C::kWinHalf, &kw_map, 64 * h, t0, bg, &full[s]);
+            tma_g2s_3d(vst + h * C::kWinHalf, &vw_map, 64 * h, t0, bg, &full[s]);
           }
         } else {
+          const int t0 = start + it * C::kTile;
           uint8_t* vst = kst + C::kTileBytes;
           if constexpr (PAGED) {
             const int bs = 1 << a.log2_bs;
@@ -345,7 +358,8 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
         }
         issued = it + 1;
       }
-      for (int it = issued > nst ? issued - nst : 0; it < issued; ++it) mbar_wait(&full[it % nst], (it / nst) & 1);
+      for (int it = issued > C::kStages ? issued - C::kStages : 0; it < issued; ++it)
+        mbar_wait(&full[it % C::kStages], (it / C::kStages) & 1);
     }
     return;
   }
@@ -353,20 +367,20 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   // ------------------------------------------------------------------ consumers
   constexpr int kConsumers = C::kConsumerWarps * 32;
   const int hd = lane >> 2;
-  // q as the bf16 B operand (window unit, and the fused step's rotation): lane holds
-  // q[head lane/4][dims 16kk + 2(lane%4) + {0,1}] and (+8)
-  uint32_t qb[M::kKSteps][2];
   const __nv_bfloat16* q_in = static_cast<const __nv_bfloat16*>(a.q) + (static_cast<size_t>(b) * a.Hq + h0) * D;
-  if (FUSED || win_unit) {
-    const uint32_t* q = reinterpret_cast<const uint32_t*>(q_in + hd * D);
+  const __nv_bfloat16* q_rows = q_in;  // rotated q rows: q_rot in memory, or the fused step's own
+  // q as the bf16 B operand (lane holds q[head lane/4][dims 16kk + 2(lane%4) + {0,1}] and (+8))
+  auto load_qb = [&](const __nv_bfloat16* rows, uint32_t (&qb)[M::kKSteps][2]) {
+    const uint32_t* q = reinterpret_cast<const uint32_t*>(rows + hd * D);
 #pragma unroll
     for (int kk = 0; kk < M::kKSteps; ++kk) {
       qb[kk][0] = hd < hpc ? q[kk * 8 + (lane & 3)] : 0u;
       qb[kk][1] = hd < hpc ? q[kk * 8 + 4 + (lane & 3)] : 0u;
     }
-  }
-  const __nv_bfloat16* q_rows = q_in;  // where the INT8 unit reads rotated q rows from
+  };
   if constexpr (FUSED) {
+    uint32_t qb[M::kKSteps][2];
+    load_qb(q_in, qb);
     // RoPE ("Transformer推理核心：KV Cache、GQA与RoPE原理与工程实践" §3) as in decode_mma_kernel
     const int pos = L - 1;
     if (threadIdx.x < D / 2) {
@@ -411,7 +425,7 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
       const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(a.v_new) + (static_cast<size_t>(b) * a.Hkv + g) * D;
       int8_t* kc = static_cast<int8_t*>(const_cast<void*>(a.k)) + row * D;
       int8_t* vc = static_cast<int8_t*>(const_cast<void*>(a.v)) + row * D;
-      const size_t wrow = ((static_cast<size_t>(b) * a.Hkv + g) * (has_win ? a.window : 1) + (has_win ? pos % a.window : 0)) * D;
+      const size_t wrow = has_win ? ((static_cast<size_t>(b) * a.Hkv + g) * a.window + pos % a.window) * D : 0;
       __nv_bfloat16* kw = static_cast<__nv_bfloat16*>(a.k_win) + wrow;
       __nv_bfloat16* vw = static_cast<__nv_bfloat16*>(a.v_win) + wrow;
       const float ks = a.k_scale[g], vs = a.v_scale[g];
@@ -450,29 +464,7 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   st.m[0] = st.m[1] = -INFINITY;
   st.l[0] = st.l[1] = 0.f;
 
-  if (win_unit) {
-    for (int it = 0; it < n_tiles; ++it) {
-      const int s = it % C::kWinStages;
-      if (!mbar_wait(&full[s], (it / C::kWinStages) & 1)) {
-        flag_error(a.err, RRA_ERR_TIMEOUT);
-        break;
-      }
-      uint8_t* kst = smem + s * M::kStageBytes;
-      uint8_t* vst = kst + M::kHalves * M::kHalfBytes;
-      const uint32_t k_base = smem_addr(kst), v_base = smem_addr(vst);
-      const int valid = min(rows, end - (start + it * rows));
-#pragma unroll
-      for (int step = 0; step < M::kSteps; ++step) {
-        const int t0 = warp * M::kWarpTokens + step * 16;
-        if (valid == M::kTile)
-          mma_step<D, false>(st, qb, k_base, v_base, vst, t0, valid, lane, a.scale_log2);
-        else if (t0 < valid)
-          mma_step<D, true>(st, qb, k_base, v_base, vst, t0, valid, lane, a.scale_log2);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-    }
-  } else {
+  if (n_q8 > 0) {
     // q in the INT8 fragment order: lane holds dims 16c + 4(lane%4) + {0..3} of head lane/4,
     // scaled by 2^e so that the head's largest |q| lies in [2^14, 2^15), then rounded to f16.
     uint32_t qh[D / 16][2];
@@ -510,14 +502,13 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
 #pragma unroll
       for (int j = 0; j < 2; ++j) mult[j] = base * __shfl_sync(0xffffffffu, down, 4 * (2 * (lane & 3) + j));
     }
-    for (int it = 0; it < n_tiles; ++it) {
+    for (int it = 0; it < n_q8; ++it) {
       const int s = it % C::kStages;
       if (!mbar_wait(&full[s], (it / C::kStages) & 1)) {
         flag_error(a.err, RRA_ERR_TIMEOUT);
         break;
       }
-      uint8_t* kst = smem + s * C::kStageBytes;
-      const uint32_t k_base = smem_addr(kst), v_base = k_base + C::kTileBytes;
+      const uint32_t k_base = smem_addr(smem + s * C::kStageBytes), v_base = k_base + C::kTileBytes;
       const int valid = min(C::kTile, end - (start + it * C::kTile));
 #pragma unroll
       for (int step = 0; step < C::kSteps; ++step) {
@@ -526,6 +517,31 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
           q8_step<D, false>(st, qh, mult, k_base, v_base, t0, valid, lane);
         else if (t0 < valid)
           q8_step<D, true>(st, qh, mult, k_base, v_base, t0, valid, lane);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    q8_acc_to_bf16_layout<D>(st, a.v_scale[g], lane);
+  }
+  if (n_win > 0) {
+    uint32_t qb[M::kKSteps][2];
+    load_qb(q_rows, qb);
+    for (int it = n_q8; it < n_tiles; ++it) {
+      const int s = it % C::kStages;
+      if (!mbar_wait(&full[s], (it / C::kStages) & 1)) {
+        flag_error(a.err, RRA_ERR_TIMEOUT);
+        break;
+      }
+      uint8_t* kst = smem + s * C::kStageBytes;
+      uint8_t* vst = kst + M::kHalves * C::kWinHalf;
+      const uint32_t k_base = smem_addr(kst), v_base = smem_addr(vst);
+      const int valid = min(wrows, Lw - (it - n_q8) * wrows);
+      const int t0 = warp * 16;  // one 16-token step per warp; ring tiles hold up to kWinTile tokens
+      if (t0 < C::kWinTile) {
+        if (valid == C::kWinTile)
+          mma_step<D, false, C::kWinHalf>(st, qb, k_base, v_base, vst, t0, valid, lane, a.scale_log2);
+        else if (t0 < valid)
+          mma_step<D, true, C::kWinHalf>(st, qb, k_base, v_base, vst, t0, valid, lane, a.scale_log2);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -545,23 +561,13 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   float* red_l = red_m + C::kConsumerWarps * M::kMaxHeads;
   {
     const int hd0 = 2 * (lane & 3), dl = lane >> 2;
-    if (win_unit) {
 #pragma unroll
-      for (int i = 0; i < D / 16; ++i)
+    for (int i = 0; i < D / 16; ++i)
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          red_o[(warp * M::kMaxHeads + hd0 + j) * D + 16 * i + dl] = st.o[i][j];
-          red_o[(warp * M::kMaxHeads + hd0 + j) * D + 16 * i + 8 + dl] = st.o[i][2 + j];
-        }
-    } else {  // fragment rows dl and dl + 8 are dims 2dl and 2dl + 1; V codes times the V scale
-      const float vs = a.v_scale[g];
-#pragma unroll
-      for (int i = 0; i < D / 16; ++i)
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-          *reinterpret_cast<float2*>(&red_o[(warp * M::kMaxHeads + hd0 + j) * D + 16 * i + 2 * dl]) =
-              make_float2(st.o[i][j] * vs, st.o[i][2 + j] * vs);
-    }
+      for (int j = 0; j < 2; ++j) {
+        red_o[(warp * M::kMaxHeads + hd0 + j) * D + 16 * i + dl] = st.o[i][j];
+        red_o[(warp * M::kMaxHeads + hd0 + j) * D + 16 * i + 8 + dl] = st.o[i][2 + j];
+      }
     if (dl == 0) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -589,7 +595,7 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     if (n_work == 1) {
       static_cast<__nv_bfloat16*>(a.out)[bh * D + d] = __float2bfloat16_rn(lsum > 0.f ? osum / lsum : 0.f);
     } else {
-      const size_t ps = bh * a.num_splits + part;
+      const size_t ps = bh * a.num_splits + split;
       a.ws_o[ps * D + d] = osum;
       if (d == 0) {
         a.ws_ml[2 * ps] = Mx;
@@ -599,7 +605,7 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   }
   if (n_work > 1) {
     __shared__ int s_last;
-    finish_split<__nv_bfloat16, D>(a, b, h0, hpc, part, n_work, reinterpret_cast<float*>(smem), &s_last,
+    finish_split<__nv_bfloat16, D>(a, b, h0, hpc, split, n_work, reinterpret_cast<float*>(smem), &s_last,
                                    threadIdx.x, kConsumers);
   }
 }

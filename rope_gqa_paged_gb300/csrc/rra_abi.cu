@@ -148,9 +148,10 @@ int make_plan(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
   return plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
 }
 
-// INT8 caches: the INT8 tokens split like the bf16 tensor-core kernel's (tiles of 16384 / D
-// tokens), plus one partial slot for the window's ring when window > 0. Paged blocks must hold
-// at least 8 tokens and a contiguous cache at least one tile; the window is a multiple of 8.
+// INT8 caches: the INT8 tokens split like the bf16 tensor-core kernel's (tiles of
+// decode_q8_tile_tokens(D) tokens); the window's ring is streamed by the CTA of the last split,
+// so it adds no split. Paged blocks must hold at least 8 tokens and a contiguous cache at least
+// one tile; the window is a multiple of 8.
 int make_plan_q8(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size, int requested, int window,
                  Plan* p) {
   int st = check_shapes(B, Hq, Hkv, D, RRA_BF16);
@@ -164,10 +165,7 @@ int make_plan_q8(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_si
   if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
   p->tile = rra::decode_q8_tile_tokens(D);
   if (block_size > 0 ? block_size < 8 : max_tokens < p->tile) return RRA_EUNSUPPORTED;
-  st = plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p, window > 0 ? 1 : 0);
-  if (st != RRA_OK) return st;
-  if (window > 0) ++p->splits;
-  return RRA_OK;
+  return plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
 }
 
 // Workspace layout, each part 256-byte aligned (R = B*Hq, G = ceil(splits / kMergeFanIn)):
@@ -372,7 +370,7 @@ int q8_maps(const Plan& p, const void* k_codes, const void* v_codes, const void*
     if (st == RRA_OK) st = encode_q8_contig_map(vm, v_codes, B, Hkv, max_len, D, p.tile);
   }
   if (st != RRA_OK || window == 0) return st;
-  const int rows = std::min(window, rra::decode_mma_tile_tokens(D));  // ring rows per stage
+  const int rows = std::min(window, RRA_Q8_STAGE_BYTES / (4 * D));  // ring rows per stage (K + V bf16)
   st = encode_contig_map(kwm, k_win, B, Hkv, window, D, rows, RRA_BF16);
   if (st == RRA_OK) st = encode_contig_map(vwm, v_win, B, Hkv, window, D, rows, RRA_BF16);
   return st;

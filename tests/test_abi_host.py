@@ -107,10 +107,10 @@ def test_argument_checks_reject_before_any_launch(rra):
 
 def test_q8_planning(rra):
     S = rra.rra_decode_q8_num_splits
-    assert S(1, 32, 8, 128, 131072, 32, 64, 128) == 65                          # 64 INT8 splits + the ring
-    assert S(1, 32, 8, 128, 131072, 32, 64, 0) == 64                            # no window, no ring slot
-    # one split asked for, but a split spans at most 255 block ids of 16 tokens: 3 INT8 splits + the ring
-    assert S(4, 32, 8, 128, 8192, 16, 1, 16) == S(4, 32, 8, 128, 8192, 16, 1, 0) + 1 == 4
+    assert S(1, 32, 8, 128, 131072, 32, 64, 128) == 64                          # the ring adds no split
+    assert S(1, 32, 8, 128, 131072, 32, 64, 0) == 64
+    # one split asked for, but a split spans at most 255 block ids of 16 tokens
+    assert S(4, 32, 8, 128, 8192, 16, 1, 16) == 3
     lib = rra.lib()
     for bad, status in (((1, 8, 8, 128, 1024, 16, 0, 12), RRA_EUNSUPPORTED),   # window not a multiple of 8
                         ((1, 8, 8, 128, 1024, 16, 0, -8), RRA_EINVAL),
@@ -119,9 +119,6 @@ def test_q8_planning(rra):
                         ((1, 8, 8, 96, 1024, 16, 0, 16), RRA_EUNSUPPORTED),
                         ((1, 6, 4, 128, 1024, 16, 0, 16), RRA_EINVAL)):
         assert lib.rra_decode_q8_num_splits(*bad) == status, bad
-    # the workspace for INT8 splits + ring slot
-    assert rra.rra_decode_workspace_bytes(1, 32, 128, S(1, 32, 8, 128, 131072, 32, 64, 128)) > \
-        rra.rra_decode_workspace_bytes(1, 32, 128, 64)
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="host-only argument checks; never given fake pointers on a GPU")
