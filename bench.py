@@ -320,33 +320,73 @@ def run_ours(args):
     torch.cuda.synchronize(device)
     fused_ms = sum(fev[i][0].elapsed_time(fev[i][1]) for i in range(K)) / K
 
-    # (2) the step: one captured graph of both calls, replayed K times (eager if capture fails)
+    # (2) the step, K times back to back. Inputs larger than L2: all K steps captured in one CUDA
+    # graph (a decode loop's shape: each decode kernel overlaps its launch and first loads with
+    # the end of the kernel before it), timed by events around that one replay. Inputs that fit
+    # in L2: a one-step graph replayed K times, L2 flushed between steps outside the events.
     graph_note = "eager launches"
+    multi = None
     if not args.no_graph:
         try:
-            step.capture(w["q"], w["k_new"], w["v_new"], w["positions"])
-            graph_note = "CUDA graph of the fused step, replayed"
+            single = step.capture(w["q"], w["k_new"], w["v_new"], w["positions"])
+            if flush is None:
+                multi = step.capture(w["q"], w["k_new"], w["v_new"], w["positions"], repeat=K)
+            step.graph = single
+            graph_note = (f"one CUDA graph of {K} fused steps, replayed once" if multi is not None
+                          else "CUDA graph of the fused step, replayed per step (L2 flushed between steps)")
         except Exception as e:  # capture is an optimisation; report how the step was timed
-            step.graph = None
+            step.graph, multi = None, None
             graph_note = f"eager launches (graph capture failed: {type(e).__name__})"
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    sampler = ClockSampler(uuid)
-    barrier(world)
-    torch.cuda.synchronize(device)
-    sampler.start()
-    for i in range(K):
-        if flush is not None:
-            flush.fill_(i & 0xFF)
-        sev[i][0].record(stream)
+
+    def one_step():
         if step.graph is not None:
             step.replay()
         else:
             step(w["q"], w["k_new"], w["v_new"], w["positions"])
+
+    # per-step replays (the reported time when L2 is flushed; otherwise the single-step figure)
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize(device)
+    for i in range(K):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        sev[i][0].record(stream)
+        one_step()
         sev[i][1].record(stream)
     torch.cuda.synchronize(device)
-    barrier(world)
+    single_ms = sum(sev[i][0].elapsed_time(sev[i][1]) for i in range(K)) / K
+
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    t_warm = time.perf_counter()
+    while time.perf_counter() - t_warm < 0.6:     # load the GPU so the clock samples see it busy
+        (multi.replay() if multi is not None else one_step())
+        torch.cuda.synchronize(device)
+    if multi is not None:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(device)
+        ev0.record(stream)
+        multi.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        ms_local = ev0.elapsed_time(ev1) / K
+    else:
+        barrier(world)
+        torch.cuda.synchronize(device)
+        for i in range(K):
+            if flush is not None:
+                flush.fill_(i & 0xFF)
+            sev[i][0].record(stream)
+            one_step()
+            sev[i][1].record(stream)
+        torch.cuda.synchronize(device)
+        barrier(world)
+        ms_local = sum(sev[i][0].elapsed_time(sev[i][1]) for i in range(K)) / K
     clocks = sampler.stop()
-    ms_local = sum(sev[i][0].elapsed_time(sev[i][1]) for i in range(K)) / K
+    step.graph = single if step.graph is not None else None
     err_bits = step.error_bits()
 
     # (3) end to end through the public API: pinned host inputs in, host output back, every step
@@ -406,6 +446,7 @@ def run_ours(args):
                                                                        "decode_attn": round(dec_avg, 5),
                                                                        "both": round(eager_ms, 5)}},
         "step_timing": graph_note,
+        "single_step_graph_ms": round(single_ms, 5),
         "roofline": {"kernel": ("decode_q8_kernel, fused step (RoPE + quantised append + split-K attention over "
                                 "INT8 codes and the bf16 window + merge)" if cfg.int8 else
                                 "decode_mma_kernel, fused step (RoPE + append + split-K attention + merge)"

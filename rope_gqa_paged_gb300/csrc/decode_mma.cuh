@@ -257,6 +257,41 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   const int h0 = g * n_rep + (blockIdx.x - split * slices) * hpc;
   const int b = blockIdx.z;
 
+  // Programmatic dependent launch: the next kernel may be scheduled now. Until the previous
+  // kernel has finished, only warm L2 with this CTA's first tiles, from lengths and block ids
+  // read ahead (they may still change: they only choose what to prefetch, clamped in range).
+  pdl_launch_dependents();
+  if (threadIdx.x == C::kConsumerWarps * 32) {
+    const int Ls = min(max(FUSED ? a.positions[b] + 1 : a.seq_lens[b], 0), a.capacity);
+    const int s0 = split * a.chunk;
+    const int e0 = min(Ls, s0 + a.chunk);
+    const int nt = s0 < Ls ? min((e0 - s0 + C::kTile - 1) / C::kTile, C::kStages) : 0;
+    for (int it = 0; it < nt; ++it) {
+      const int t0 = s0 + it * C::kTile;
+      if constexpr (PAGED) {
+        const int bs = 1 << a.log2_bs;
+        const bool whole = bs <= C::kTile;
+        const int nblk = whole ? (min(C::kTile, e0 - t0) + bs - 1) >> a.log2_bs : 1;
+        for (int jb = 0; jb < nblk; ++jb) {
+          int phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (t0 >> a.log2_bs) + jb];
+          phys = min(max(phys, 0), a.num_blocks - 1);
+#pragma unroll
+          for (int h = 0; h < C::kHalves; ++h) {
+            tma_prefetch_l2_4d(&k_map, 64 * h, g, whole ? 0 : (t0 & (bs - 1)), phys);
+            tma_prefetch_l2_4d(&v_map, 64 * h, g, whole ? 0 : (t0 & (bs - 1)), phys);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < C::kHalves; ++h) {
+          tma_prefetch_l2_3d(&k_map, 64 * h, t0, b * a.Hkv + g);
+          tma_prefetch_l2_3d(&v_map, 64 * h, t0, b * a.Hkv + g);
+        }
+      }
+    }
+  }
+  pdl_wait();
+
   int L;
   if constexpr (FUSED) {
     const int pos = a.positions[b];
@@ -551,8 +586,7 @@ cudaError_t launch_decode_mma_t(const DecodeArgs& a, const CUtensorMap& km, cons
   cudaError_t e = ensure_smem(kern, C::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   const dim3 grid(a.num_splits * ((a.Hq / a.Hkv) / hpc), a.Hkv, a.B);
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(km, vm, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(C::kThreads), C::kSmemBytes, st, km, vm, a);
 }
 
 template <bool PAGED, bool FUSED = false>

@@ -71,14 +71,15 @@ class DecodeStep:
         self.rope_append(q, k_new, v_new, positions, stream)
         return self.attend(seq_lens, stream)
 
-    def capture(self, q, k_new, v_new, positions, seq_lens=None) -> None:
-        """Record one whole step (both library calls) into a CUDA graph.
+    def capture(self, q, k_new, v_new, positions, seq_lens=None, repeat: int = 1, between=None):
+        """Record the step (``repeat`` times back to back, calling ``between()`` before each
+        repetition after the first) into a CUDA graph; returns it and keeps it for ``replay()``.
 
         The graph is bound to these input tensors and to this object's output, workspace
         and error buffers: refill the inputs in place, then ``replay()``. Replaying saves
-        the host-side launch cost of every kernel of the step.
+        the host-side launch cost of every kernel of the step, and inside one graph each
+        decode kernel overlaps its launch with the end of the kernel before it.
         """
-        import torch
         side = torch.cuda.Stream(device=q.device)
         side.wait_stream(torch.cuda.current_stream(q.device))
         with torch.cuda.stream(side):
@@ -86,8 +87,12 @@ class DecodeStep:
         torch.cuda.current_stream(q.device).wait_stream(side)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            self(q, k_new, v_new, positions, seq_lens)
+            for i in range(repeat):
+                if i and between is not None:
+                    between()
+                self(q, k_new, v_new, positions, seq_lens)
         self.graph = graph
+        return graph
 
     def replay(self) -> torch.Tensor:
         """Run the captured step on the current stream; returns the output buffer."""
