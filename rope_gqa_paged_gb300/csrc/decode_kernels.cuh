@@ -146,15 +146,23 @@ __device__ __forceinline__ void consume_stage(ConsumerState<T, D, HPC>& st, cons
 // (log2 units) and running sum l. Merging partials i: M = max m_i, w_i = 2^(m_i - M),
 // o = sum w_i o_i, l = sum w_i l_i; the final row is o / l.
 
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Counts this CTA's arrival at `cnt` (all `nthreads` consumer threads call it after their
 // last write). True in the CTA whose arrival brings the count to `target`; that CTA also puts
 // the counter back to zero, ready for the next call. No CTA ever waits for another.
+// Ordering: the barrier orders every thread's partial writes before thread 0's arrival, whose
+// release makes them visible device-wide; its acquire (in the last CTA) and the second barrier
+// order the other CTAs' partials before this CTA's merge reads (which bypass L1).
 __device__ __forceinline__ bool arrive_last(int* cnt, int target, int* s_flag, int32_t* err, int tid,
                                             int nthreads) {
-  __threadfence();  // this thread's writes are visible device-wide before the arrival
   named_barrier_sync(1, nthreads);
   if (tid == 0) {
-    const int arrived = atomicAdd(cnt, 1) + 1;
+    const int arrived = atomic_add_acq_rel_gpu(cnt, 1) + 1;
     int last = 0;
     if (arrived == target) {
       last = 1;
@@ -166,9 +174,7 @@ __device__ __forceinline__ bool arrive_last(int* cnt, int target, int* s_flag, i
     *s_flag = last;
   }
   named_barrier_sync(1, nthreads);
-  const bool last = *s_flag != 0;
-  if (last) __threadfence();  // see the partials of every CTA that arrived before
-  return last;
+  return *s_flag != 0;
 }
 
 // Merges partials first .. first+count-1 of heads h0 .. h0+hpc-1 (rows row0 + h of a
