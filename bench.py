@@ -211,6 +211,7 @@ def device_workload(cfg, seed, device):
     g.manual_seed(1000003 * seed + 17)
     B, Hq, Hkv, D = cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     shape = (B, Hkv, cfg.max_len, D) if cfg.layout == "contiguous" else (cfg.num_blocks, cfg.block_size, Hkv, D)
+    lead = (B,) if cfg.gamma == 1 else (B, cfg.gamma)
     if cfg.int8:  # INT8 codes: N(0,1) at a resolution of 1/32, clipped; fixed per-head scales; bf16 rings
         codes = lambda: torch.randn(shape, generator=g, device=device).mul_(32).round_().clamp_(-127, 127).to(  # noqa: E731
             torch.int8)
@@ -221,10 +222,10 @@ def device_workload(cfg, seed, device):
     w = {
         "k_cache": kc,
         "v_cache": vc,
-        "q": torch.randn(B, Hq, D, generator=g, device=device, dtype=dt),
-        "k_new": torch.randn(B, Hkv, D, generator=g, device=device, dtype=dt),
-        "v_new": torch.randn(B, Hkv, D, generator=g, device=device, dtype=dt),
-        "positions": torch.from_numpy(lengths - 1).to(device),
+        "q": torch.randn(*lead, Hq, D, generator=g, device=device, dtype=dt),
+        "k_new": torch.randn(*lead, Hkv, D, generator=g, device=device, dtype=dt),
+        "v_new": torch.randn(*lead, Hkv, D, generator=g, device=device, dtype=dt),
+        "positions": torch.from_numpy(lengths - cfg.gamma).to(device),
         "seq_lens": torch.from_numpy(lengths).to(device),
         "block_table": torch.from_numpy(table).to(device) if table is not None else None,
     }

@@ -23,7 +23,9 @@ Pages cited (by title and section):
   KVCache.update / PagedKVCache / the cache-size formula, §六 GQA and n_rep).
 
 ``oracle.quant`` adds the INT8 KV cache with per-head scales and a bf16 window of
-recent tokens ([KVC-GQA-RoPE] §4.3), with its readings stated in its header.
+recent tokens ([KVC-GQA-RoPE] §4.3), and ``oracle.verify`` the multi-query decode of a
+speculative-verify step (gamma new tokens, causal inside the chunk; [Opt-2026] §五), each
+with its readings stated in its header.
 
 Parity status: every function here is pinned by tests that do not retype it
 (library routines, complex-number rotation, brute force, closed forms and the
@@ -38,3 +40,4 @@ from .attention import (repeat_kv, softmax, attention, gqa_decode_attention,  # 
                         causal_attention)
 from .decode import decode_step  # noqa: F401
 from . import quant  # noqa: F401
+from . import verify  # noqa: F401

@@ -411,6 +411,60 @@ def pin_q8_stream_matches_mixed_precision():
             _q8_stream(window, layout, style=window % 2)
 
 
+# ---------------------------------------------------------------------------- speculative verify
+def _verify_case(layout, gamma=4, seed=21):
+    rng = np.random.default_rng(seed)
+    B, hq, hkv, d, bs = 2, 8, 2, 16, 4
+    p0 = np.array([5, 11])                                    # first new token of each sequence
+    cap = 20
+    q = oracle.f64_to_bf16_bits(rng.standard_normal((B, gamma, hq, d)))
+    kn = oracle.f64_to_bf16_bits(rng.standard_normal((B, gamma, hkv, d)))
+    vn = oracle.f64_to_bf16_bits(rng.standard_normal((B, gamma, hkv, d)))
+    if layout == "contiguous":
+        kc = oracle.f64_to_bf16_bits(rng.standard_normal((B, hkv, cap, d)))
+        table = None
+    else:
+        kc = oracle.f64_to_bf16_bits(rng.standard_normal((3 * cap // bs, bs, hkv, d)))
+        table = rng.permutation(kc.shape[0])[: 2 * (cap // bs)].reshape(2, cap // bs).astype(np.int32)
+    vc = oracle.f64_to_bf16_bits(rng.standard_normal(kc.shape))
+    return q, kn, vn, p0, kc, vc, table, bs
+
+
+def pin_verify_equals_sequential_decode():
+    # verifying gamma tokens at once must give what decoding them one at a time gives
+    for layout in ("contiguous", "paged"):
+        for style in (0, 1):
+            q, kn, vn, p0, kc, vc, table, bs = _verify_case(layout)
+            got_q, got_k, got_v, got = oracle.verify.verify_step(q, kn, vn, p0, kc, vc, "bf16", table, bs,
+                                                                 rope_style=style)
+            k2, v2 = kc.copy(), vc.copy()
+            for j in range(q.shape[1]):
+                q_rot, k2, v2, out = oracle.decode.decode_step(q[:, j], kn[:, j], vn[:, j], p0 + j, k2, v2, "bf16",
+                                                               table, bs, rope_style=style)
+                assert np.array_equal(got_q[:, j], q_rot)
+                assert np.allclose(got[:, j], out, rtol=0, atol=1e-13), (layout, j)
+            assert got_k.tobytes() == k2.tobytes() and got_v.tobytes() == v2.tobytes()
+
+
+def pin_verify_equals_causal_rows():
+    # the last gamma rows of causal attention over the whole sequence (per-position RoPE)
+    rng = np.random.default_rng(22)
+    T, gamma, hq, hkv, d = 19, 4, 4, 2, 16
+    qs = rng.standard_normal((T, hq, d))
+    ks = rng.standard_normal((T, hkv, d))
+    vs = rng.standard_normal((T, hkv, d))
+    pos = np.arange(T)
+    ref = oracle.causal_attention(oracle.apply_rope(qs, pos[:, None]), oracle.apply_rope(ks, pos[:, None]), vs)
+    p0 = T - gamma
+    kc = np.full((1, hkv, T + 2, d), np.nan)
+    vc = kc.copy()
+    kc[0, :, :p0] = np.transpose(oracle.apply_rope(ks[:p0], pos[:p0, None]), (1, 0, 2))   # cached: rotated
+    vc[0, :, :p0] = np.transpose(vs[:p0], (1, 0, 2))
+    _, _, _, out = oracle.verify.verify_step(qs[p0:][None], ks[p0:][None], vs[p0:][None], np.array([p0]), kc, vc,
+                                             "f64")
+    assert np.allclose(out[0], ref[p0:], rtol=0, atol=1e-12), np.abs(out[0] - ref[p0:]).max()
+
+
 ALL_PINS = [
     pin_bf16_exact_values, pin_bf16_matches_torch_cast,
     pin_rope_complex_rotation, pin_rope_relative_position, pin_rope_rotation_properties,
@@ -420,6 +474,7 @@ ALL_PINS = [
     pin_kv_bytes_pages_numbers,
     pin_int8_quantize_exact_values, pin_int8_round_trip_bound, pin_q8_full_window_is_the_bf16_step,
     pin_q8_without_window_reads_code_times_scale, pin_q8_stream_matches_mixed_precision,
+    pin_verify_equals_sequential_decode, pin_verify_equals_causal_rows,
 ]
 
 

@@ -118,6 +118,36 @@ def _q8_v_with_k_scale(q, k_new, v_new, positions, k_codes, v_codes, k_scale, v_
     return _ORIG_Q["rope_append_q8"](q, k_new, v_new, positions, k_codes, v_codes, k_scale, k_scale, *args, **kw)
 
 
+def _verify_without_chunk_mask(q_rot, k_cache, v_cache, positions, dtype, block_table=None, block_size=0,
+                               scale=None, batches=None):
+    gamma = q_rot.shape[1]
+    outs = []
+    for b in range(len(positions)):
+        L = int(positions[b]) + gamma
+        k = oracle.storage_to_f64(oracle.decode.logical_kv(k_cache, b, L, block_table, block_size), dtype)
+        v = oracle.storage_to_f64(oracle.decode.logical_kv(v_cache, b, L, block_table, block_size), dtype)
+        outs.append(np.stack([oracle.gqa_decode_attention(oracle.storage_to_f64(q_rot[b, j], dtype), k, v, scale)
+                              for j in range(gamma)]))
+    return np.stack(outs)
+
+
+def _verify_rope_at_first_position(q, k_new, v_new, positions, k_cache, v_cache, dtype, block_table=None,
+                                   block_size=0, rope_base=10000.0, rope_style=0):
+    gamma = q.shape[1]
+    pos = np.repeat(np.asarray(positions)[:, None], gamma, axis=1)
+    q_rot = oracle.f64_to_storage(oracle.apply_rope(oracle.storage_to_f64(q, dtype), pos[:, :, None], rope_base,
+                                                    rope_style), dtype)
+    k_rot = oracle.f64_to_storage(oracle.apply_rope(oracle.storage_to_f64(k_new, dtype), pos[:, :, None],
+                                                    rope_base, rope_style), dtype)
+    for j in range(gamma):
+        slot = np.asarray(positions) + j
+        if block_table is None:
+            oracle.append_contiguous(k_cache, v_cache, k_rot[:, j], v_new[:, j], slot)
+        else:
+            oracle.append_paged(k_cache, v_cache, block_table, block_size, k_rot[:, j], v_new[:, j], slot)
+    return q_rot
+
+
 _ORIG = {n: getattr(oracle, n) for n in ("apply_rope", "attention", "append_contiguous")}
 _ORIG_Q = {n: getattr(oracle.quant, n) for n in ("logical_kv_q8", "rope_append_q8")}
 
@@ -140,6 +170,8 @@ MUTATIONS = {
     "window one token short": ("logical_kv_q8", _q8_window_one_short),
     "dequantisation drops the scale": ("dequantize_int8", _q8_dequantize_without_scale),
     "v quantised with the k scales": ("rope_append_q8", _q8_v_with_k_scale),
+    "verify without the causal mask inside the chunk": ("verify_attention", _verify_without_chunk_mask),
+    "verify rotates every new token at the first position": ("rope_append_verify", _verify_rope_at_first_position),
 }
 
 

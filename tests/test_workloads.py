@@ -35,10 +35,11 @@ def test_reduced_inputs_structure(name):
     b = make_inputs(cfg)
     for f in ("q", "k_new", "v_new", "k_cache", "v_cache", "lengths"):
         assert getattr(a, f).tobytes() == getattr(b, f).tobytes()
-    assert np.array_equal(a.positions, a.lengths - 1)
+    assert np.array_equal(a.positions, a.lengths - cfg.gamma)
+    assert a.q.shape[:-2] == ((cfg.batch,) if cfg.gamma == 1 else (cfg.batch, cfg.gamma))
     L = a.lengths
-    # slots read from the main cache: [0, first); the new token's slot and the window are poisoned
-    first = [max(0, int(x) - max(cfg.window, 1)) if cfg.int8 else int(x) - 1 for x in L]
+    # slots read from the main cache: [0, first); the new tokens' slots and the window are poisoned
+    first = [max(0, int(x) - max(cfg.window, 1)) if cfg.int8 else int(x) - cfg.gamma for x in L]
     if cfg.int8 and cfg.window:
         W = cfg.window
         for bb in range(cfg.batch):

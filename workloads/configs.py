@@ -31,6 +31,7 @@ class WorkloadConfig:
     num_splits: int = 0             # split-K chunks per sequence; 0 lets the library choose
     kv_dtype: str = ""              # "" = the caches hold ``dtype``; "int8" = INT8 codes + per-head scales
     window: int = 0                 # int8 only: recent tokens also kept in a bf16 ring of this many slots
+    gamma: int = 1                  # new tokens per sequence (> 1: a speculative-verify step)
     rope_base: float = 10000.0
     seed: int = 0
     description: str = ""
@@ -120,6 +121,16 @@ CONFIGS["long_context_int8"] = dataclasses.replace(
     CONFIGS["long_context"], name="long_context_int8", kv_dtype="int8", window=128, num_splits=0,
     description="long-context decode, INT8 KV cache (per-head scales) + 128-token bf16 window: batch 1, "
                 "32q/8kv, D 128, context 131072, block 32")
+
+# The speculative-verify step ([Opt-2026] §五, gamma = 4): the batch-64 paged and 128K workloads
+# with 4 new tokens per sequence, causal inside the chunk; L_b counts all 4.
+CONFIGS["batched_paged_verify4"] = dataclasses.replace(
+    CONFIGS["batched_paged"], name="batched_paged_verify4", gamma=4,
+    description="speculative verify, 4 new tokens per sequence: batch 64, 32q/8kv, D 128, L_b ~ U[512,8192], "
+                "block 16, pool 40000")
+CONFIGS["long_context_verify4"] = dataclasses.replace(
+    CONFIGS["long_context"], name="long_context_verify4", gamma=4, num_splits=0,
+    description="speculative verify, 4 new tokens: batch 1, 32q/8kv, D 128, context 131072, block 32")
 
 
 def get_config(name: str) -> WorkloadConfig:

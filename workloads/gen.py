@@ -22,6 +22,10 @@ out-of-range read shows up as NaN in the output.
 
 bf16 arrays are carried as ``uint16`` bit patterns, fp32 as ``float32``.
 
+Speculative verify (``gamma > 1``): q, k_new, v_new are drawn as [B, gamma, H, D]; the gamma new
+tokens of sequence b sit at positions L_b - gamma .. L_b - 1 (``positions`` holds the first),
+and every slot from L_b - gamma on is poisoned.
+
 INT8 caches (``kv_dtype == "int8"``): steps 1-3 are unchanged; step 4 draws the K then the V
 cache as integer codes ``clip(rint(32 * standard_normal(float32)), -127, 127)`` (N(0,1)
 values at a resolution of 1/32), then, with a window of W slots, the K then the V ring
@@ -68,10 +72,10 @@ def _normal_storage(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
 class DecodeInputs:
     cfg: WorkloadConfig
     lengths: np.ndarray            # int32 [B], attended lengths incl. the new token
-    positions: np.ndarray          # int32 [B], = lengths - 1 (position and slot of the new token)
-    q: np.ndarray                  # [B, Hq, D]
-    k_new: np.ndarray              # [B, Hkv, D]
-    v_new: np.ndarray              # [B, Hkv, D]
+    positions: np.ndarray          # int32 [B], = lengths - gamma (position and slot of the (first) new token)
+    q: np.ndarray                  # [B, Hq, D]  ([B, gamma, Hq, D] when gamma > 1)
+    k_new: np.ndarray              # [B, Hkv, D] ([B, gamma, Hkv, D] when gamma > 1)
+    v_new: np.ndarray              # [B, Hkv, D] ([B, gamma, Hkv, D] when gamma > 1)
     k_cache: np.ndarray            # contiguous [B, Hkv, max_len, D] or pool [num_blocks, bs, Hkv, D]
     v_cache: np.ndarray
     block_table: Optional[np.ndarray] = None   # int32 [B, max_blocks_per_seq], paged only
@@ -93,8 +97,8 @@ def draw_lengths(cfg: WorkloadConfig, rng: np.random.Generator) -> np.ndarray:
     else:
         lo, hi = cfg.len_range
         lengths = rng.integers(lo, hi, endpoint=True, size=cfg.batch)
-    if np.any(lengths > cfg.capacity) or np.any(lengths < 1):
-        raise ValueError(f"{cfg.name}: lengths outside [1, {cfg.capacity}]")
+    if np.any(lengths > cfg.capacity) or np.any(lengths < cfg.gamma):
+        raise ValueError(f"{cfg.name}: lengths outside [{cfg.gamma}, {cfg.capacity}]")
     return lengths.astype(np.int32)
 
 
@@ -123,9 +127,10 @@ def make_inputs(cfg: WorkloadConfig, seed: Optional[int] = None, poison: bool = 
     B, Hq, Hkv, D = cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     lengths = draw_lengths(cfg, rng)
     table = draw_block_table(cfg, lengths, rng) if cfg.layout == "paged" else None
-    q = _normal_storage(rng, (B, Hq, D), cfg.dtype)
-    k_new = _normal_storage(rng, (B, Hkv, D), cfg.dtype)
-    v_new = _normal_storage(rng, (B, Hkv, D), cfg.dtype)
+    lead = (B,) if cfg.gamma == 1 else (B, cfg.gamma)
+    q = _normal_storage(rng, lead + (Hq, D), cfg.dtype)
+    k_new = _normal_storage(rng, lead + (Hkv, D), cfg.dtype)
+    v_new = _normal_storage(rng, lead + (Hkv, D), cfg.dtype)
     if cfg.layout == "contiguous":
         shape = (B, Hkv, cfg.max_len, D)
     else:
@@ -143,7 +148,7 @@ def make_inputs(cfg: WorkloadConfig, seed: Optional[int] = None, poison: bool = 
     else:
         k_cache = _normal_storage(rng, shape, cfg.dtype)
         v_cache = _normal_storage(rng, shape, cfg.dtype)
-    inp = DecodeInputs(cfg=cfg, lengths=lengths, positions=(lengths - 1).astype(np.int32),
+    inp = DecodeInputs(cfg=cfg, lengths=lengths, positions=(lengths - cfg.gamma).astype(np.int32),
                        q=q, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache,
                        block_table=table, **extra)
     if poison:
@@ -177,7 +182,7 @@ def poison_unread(inp: DecodeInputs) -> None:
     """Write NaN (INT8: -128) into every cache slot the step must not read before its append."""
     cfg, nan = inp.cfg, inp.nan_value
     # first slot not read from the main cache: the new token's, or the window's first
-    first = [max(0, int(L) - max(cfg.window, 1)) if cfg.int8 else int(L) - 1 for L in inp.lengths]
+    first = [max(0, int(L) - max(cfg.window, 1)) if cfg.int8 else int(L) - cfg.gamma for L in inp.lengths]
     if cfg.int8 and cfg.window:
         W = cfg.window
         for b, L in enumerate(inp.lengths):
