@@ -228,6 +228,53 @@ RRA_API int rra_decode_step_q8(const void* q, const void* k_new, const void* v_n
 RRA_API int rra_decode_q8_num_splits(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
                                      int num_splits, int window);
 
+/* --- Multi-query decode: the speculative-verify step ---
+ *
+ * [Opt-2026] §五: the target model checks gamma draft tokens (gamma = 4 on the page) in one pass.
+ * Sequence b gets gamma new tokens at positions p_b .. p_b + gamma - 1 (positions[b] = p_b);
+ * each is rotated at its own position and appended at that slot, and query token j attends
+ * tokens [0, p_b + j] -- the cached ones and the new ones up to itself -- exactly what
+ * decoding the tokens one at a time gives. q, k_new, v_new, q_out and out are laid out
+ * [B, gamma, H, D]; caches, block tables and the other arguments as in the decode calls
+ * (contiguous when block_table is NULL; paged blocks of at least 8 tokens, contiguous caches of
+ * at least 16384 / (2 D) tokens; bf16 only for the attention). gamma is 1..16.
+ */
+
+/* rra_rope_append for gamma new tokens per sequence (token j at positions[b] + j). With
+ * gamma == 1 it is rra_rope_append; bf16 or fp32. */
+RRA_API int rra_rope_append_verify(const void* q, const void* k_new, const void* v_new, const int32_t* positions,
+                                   void* q_out, void* k_cache, void* v_cache, const int32_t* block_table,
+                                   int max_blocks_per_seq, int block_size, int num_blocks, int max_len, int B,
+                                   int gamma, int Hq, int Hkv, int D, double rope_base, int rope_style, rra_dtype dt,
+                                   int32_t* err_flag, void* stream);
+
+/* out[b, j, h] = softmax(q_rot[b, j, h] . K[b, h / n_rep, 0 : p_b + j + 1]^T * scale) . V[...] for
+ * bf16 caches that already hold the new tokens. One CTA serves up to 16 query rows (heads x new
+ * tokens) of a KV head, so each K/V byte read serves all of them; split-K with the same merge
+ * as the decode calls. The workspace must hold rra_verify_workspace_bytes(B, gamma, Hq, Hkv, D,
+ * rra_verify_num_splits(...)) bytes, zero-filled before its first use (left zeroed by every
+ * call). Positions with p_b + gamma beyond the cache set RRA_ERR_POSITION and skip b. */
+RRA_API int rra_verify_attn(const void* q_rot, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                            int max_blocks_per_seq, const int32_t* positions, int block_size, int num_blocks,
+                            int max_len, void* out, int B, int gamma, int Hq, int Hkv, int D, float scale,
+                            int num_splits, void* workspace, size_t ws_bytes, int32_t* err_flag, void* stream);
+
+/* The whole verify step: rra_rope_append_verify then rra_verify_attn on q_out (two kernels; the
+ * second starts its launch while the first finishes). bf16. q_out must not overlap q. */
+RRA_API int rra_verify_step(const void* q, const void* k_new, const void* v_new, const int32_t* positions,
+                            void* q_out, void* k_cache, void* v_cache, const int32_t* block_table,
+                            int max_blocks_per_seq, int block_size, int num_blocks, int max_len, void* out, int B,
+                            int gamma, int Hq, int Hkv, int D, double rope_base, int rope_style, float scale,
+                            int num_splits, void* workspace, size_t ws_bytes, int32_t* err_flag, void* stream);
+
+/* Effective split count of rra_verify_attn (max_tokens and block_size as in
+ * rra_decode_num_splits); negative rra_status on bad arguments. */
+RRA_API int rra_verify_num_splits(int B, int gamma, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
+                                  int num_splits);
+
+/* Workspace bytes of rra_verify_attn for an effective split count; 0 when splits <= 1. */
+RRA_API size_t rra_verify_workspace_bytes(int B, int gamma, int Hq, int Hkv, int D, int splits);
+
 /* Bytes of a K+V cache: 2 * n_layers * n_kv_heads * head_dim * seq_len * batch * dtype_bytes
  * ([Opt-2026] §四 memory formula; [KVC-GQA-RoPE] §5.3). Host only; returns 0 when an
  * argument is negative or the product overflows 64 bits. */

@@ -177,13 +177,18 @@ __device__ __forceinline__ bool arrive_last(int* cnt, int target, int* s_flag, i
   return *s_flag != 0;
 }
 
-// Merges partials first .. first+count-1 of heads h0 .. h0+hpc-1 (rows row0 + h of a
-// [rows][stride] partial array) into the final output rows (dst_o == nullptr) or into one
+// Partial row r is output row r (decode: rows b * Hq + h).
+struct SameRow {
+  __device__ size_t operator()(size_t r) const { return r; }
+};
+
+// Merges partials first .. first+count-1 of rows row0 .. row0+hpc-1 of a [rows][stride]
+// partial array into the final output rows out_row(row0 + h) (dst_o == nullptr) or into one
 // partial at index dst_idx of a [rows][dst_stride] partial array.
-template <typename T, int D>
+template <typename T, int D, typename OutRow = SameRow>
 __device__ void merge_partials(const DecodeArgs& a, const float* src_o, const float* src_ml, int stride, int first,
                                int count, int hpc, size_t row0, float* dst_o, float* dst_ml, int dst_stride,
-                               int dst_idx, float* scratch, int tid, int nthreads) {
+                               int dst_idx, float* scratch, int tid, int nthreads, OutRow out_row = OutRow()) {
   float* sm_w = scratch;                  // [hpc][count]: m_i, then the weights
   float* sm_l = scratch + hpc * count;    // [hpc][count]
   float* sm_ml = sm_l + hpc * count;      // [hpc][2]: merged (M, l)
@@ -232,7 +237,7 @@ __device__ void merge_partials(const DecodeArgs& a, const float* src_o, const fl
       acc.w = fmaf(wv, v.w, acc.w);
     }
     if (final_row) {
-      T* out = static_cast<T*>(a.out) + (row0 + h) * D + d;
+      T* out = static_cast<T*>(a.out) + out_row(row0 + h) * D + d;
       Elem<T>::store(out, acc.x);
       Elem<T>::store(out + 1, acc.y);
       Elem<T>::store(out + 2, acc.z);
@@ -251,14 +256,15 @@ __device__ void merge_partials(const DecodeArgs& a, const float* src_o, const fl
 // groups of kMergeFanIn: the last arrival of each group merges the group into a level-2
 // partial, and the last group to finish merges the level-2 partials into the output, so no
 // single CTA has to read every split at the end of the kernel.
-template <typename T, int D>
-__device__ __forceinline__ void finish_split(const DecodeArgs& a, int b, int h0, int hpc, int split, int n,
-                                             float* scratch, int* s_flag, int tid, int nthreads) {
-  const size_t row0 = static_cast<size_t>(b) * a.Hq + h0;
+template <typename T, int D, typename OutRow = SameRow>
+__device__ __forceinline__ void finish_split_rows(const DecodeArgs& a, size_t row0, int hpc, int split, int n,
+                                                  float* scratch, int* s_flag, int tid, int nthreads,
+                                                  OutRow out_row = OutRow()) {
   const int S = a.num_splits, G = a.num_groups;
   if (n <= kMergeFanIn) {
     if (arrive_last(a.counters + row0, n, s_flag, a.err, tid, nthreads))
-      merge_partials<T, D>(a, a.ws_o, a.ws_ml, S, 0, n, hpc, row0, nullptr, nullptr, 0, 0, scratch, tid, nthreads);
+      merge_partials<T, D>(a, a.ws_o, a.ws_ml, S, 0, n, hpc, row0, nullptr, nullptr, 0, 0, scratch, tid, nthreads,
+                           out_row);
     return;
   }
   const int grp = split / kMergeFanIn, first = grp * kMergeFanIn;
@@ -269,7 +275,13 @@ __device__ __forceinline__ void finish_split(const DecodeArgs& a, int b, int h0,
   const int groups = (n + kMergeFanIn - 1) / kMergeFanIn;
   if (arrive_last(a.counters + row0, groups, s_flag, a.err, tid, nthreads))
     merge_partials<T, D>(a, a.ws2_o, a.ws2_ml, G, 0, groups, hpc, row0, nullptr, nullptr, 0, 0, scratch, tid,
-                         nthreads);
+                         nthreads, out_row);
+}
+
+template <typename T, int D>
+__device__ __forceinline__ void finish_split(const DecodeArgs& a, int b, int h0, int hpc, int split, int n,
+                                             float* scratch, int* s_flag, int tid, int nthreads) {
+  finish_split_rows<T, D>(a, static_cast<size_t>(b) * a.Hq + h0, hpc, split, n, scratch, s_flag, tid, nthreads);
 }
 
 template <typename T, int D, int HPC, bool PAGED>

@@ -36,7 +36,11 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
   __shared__ float cs[4][kPairsPerCta];               // cos hi, cos lo, sin hi, sin lo
   __shared__ size_t row_info[2];                      // cache row of KV head 0, stride between heads
   __shared__ int append_ok;
-  const int b = blockIdx.x;
+  // One CTA row per new token: token j of sequence b (gamma new tokens per sequence, j = 0 for a
+  // decode step) sits at position positions[b] + j; its q / k_new / v_new / q_out row is v.
+  const int gam = max(a.gamma, 1);
+  const int v = blockIdx.x;
+  const int b = v / gam, j_new = v - b * gam;
   const int D = a.D, half = a.D / 2;
   const int i0 = blockIdx.y * kPairsPerCta;
   const int np = min(kPairsPerCta, half - i0);
@@ -47,8 +51,8 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
   const int ib = inter ? 2 * (i0 + j) + 1 : i0 + j + half;
 
   auto src_row = [&](int hh) -> const T* {
-    return hh < a.Hq ? static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.Hq + hh) * D
-                     : static_cast<const T*>(a.k_new) + (static_cast<size_t>(b) * a.Hkv + hh - a.Hq) * D;
+    return hh < a.Hq ? static_cast<const T*>(a.q) + (static_cast<size_t>(v) * a.Hq + hh) * D
+                     : static_cast<const T*>(a.k_new) + (static_cast<size_t>(v) * a.Hkv + hh - a.Hq) * D;
   };
   // The first kUnroll rows of q / k_new are loaded before the position is even known.
   float xa[kUnroll], xb[kUnroll];
@@ -61,7 +65,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
     }
   }
 
-  const int pos = a.positions[b];
+  const int pos = a.positions[b] + j_new;
   const bool paged = a.block_table != nullptr;
   const long long cap = paged ? (static_cast<long long>(a.max_blocks_per_seq) << a.log2_bs) : a.max_len;
   if (pos < 0 || pos >= cap) {
@@ -115,7 +119,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
         const float ra = rotate_diff(xa[r], xb[r], ch, cl, sh, sl);   // a cos - b sin
         const float rb = rotate_diff(xb[r], -xa[r], ch, cl, sh, sl);  // b cos + a sin
         if (hh < a.Hq) {
-          T* dst = static_cast<T*>(a.q_out) + (static_cast<size_t>(b) * a.Hq + hh) * D;
+          T* dst = static_cast<T*>(a.q_out) + (static_cast<size_t>(v) * a.Hq + hh) * D;
           Elem<T>::store(dst + ia, ra);
           Elem<T>::store(dst + ib, rb);
         } else if (append) {
@@ -145,7 +149,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
   // V is stored unrotated: this CTA copies its share of the dims of every KV head.
   const int dims = (D + gridDim.y - 1) / gridDim.y;
   const int d0 = blockIdx.y * dims, d1 = min(D, d0 + dims);
-  const T* vn = static_cast<const T*>(a.v_new) + static_cast<size_t>(b) * a.Hkv * D;
+  const T* vn = static_cast<const T*>(a.v_new) + static_cast<size_t>(v) * a.Hkv * D;
   for (int idx = threadIdx.x; idx < a.Hkv * (d1 - d0); idx += blockDim.x) {
     const int g = idx / (d1 - d0), d = d0 + idx % (d1 - d0);
     if constexpr (Q8) {
@@ -162,7 +166,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
 }  // namespace
 
 cudaError_t launch_rope_append(const RopeArgs& a, rra_dtype dt, cudaStream_t stream) {
-  const dim3 grid(a.B, (a.D / 2 + kPairsPerCta - 1) / kPairsPerCta);
+  const dim3 grid(a.B * (a.gamma > 1 ? a.gamma : 1), (a.D / 2 + kPairsPerCta - 1) / kPairsPerCta);
   if (dt == RRA_BF16)
     rope_append_kernel<__nv_bfloat16, false><<<grid, kRopeThreads, 0, stream>>>(a);
   else

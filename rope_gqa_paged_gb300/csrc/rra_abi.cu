@@ -56,6 +56,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // How the decode work is cut: kernel, query heads per CTA, token chunk per split, split count.
 struct Plan {
+  int ctas_per_sm = 0;  // resident CTAs per SM of the kernel (0: 3 for the tensor-core kernels, else 2)
   bool mma = false;  // bf16 tensor-core kernel
   int hpc = 1;
   int tile = 0;
@@ -106,7 +107,7 @@ int plan_splits(int B, int Hkv, int n_rep, int64_t max_tokens, int block_size, i
     chunk_tiles = (tiles + requested - 1) / requested;
   } else {
     // CTAs that fit on the GPU at once: 3 per SM for the mma kernel, 2 otherwise.
-    const int64_t resident = (p->mma ? 3 : 2) * int64_t(std::max(1, sm_count()));
+    const int64_t resident = (p->ctas_per_sm ? p->ctas_per_sm : (p->mma ? 3 : 2)) * int64_t(std::max(1, sm_count()));
     const int64_t units = std::max<int64_t>(1, int64_t(B) * Hkv * (n_rep / p->hpc));  // CTAs per split
     if (2 * units <= resident) {
       // Few sequences x heads: as many splits as fit in ONE wave (a second wave that is barely
@@ -166,6 +167,36 @@ int make_plan_q8(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_si
   p->tile = rra::decode_q8_tile_tokens(D);
   if (block_size > 0 ? block_size < 8 : max_tokens < p->tile) return RRA_EUNSUPPORTED;
   return plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
+}
+
+// Speculative verify: one CTA serves hpc heads x gamma new tokens (at most 16 query rows) of one
+// KV head; hpc is the largest divisor of n_rep with hpc * gamma <= 16. Two CTAs per SM.
+int verify_hpc(int n_rep, int gamma) {
+  for (int h = std::min(n_rep, 16 / gamma); h > 1; --h)
+    if (n_rep % h == 0) return h;
+  return 1;
+}
+
+int make_plan_verify(int B, int gamma, int Hq, int Hkv, int D, int64_t max_tokens, int block_size, int requested,
+                     Plan* p) {
+  int st = check_shapes(B, Hq, Hkv, D, RRA_BF16);
+  if (st != RRA_OK) return st;
+  if (requested < 0 || max_tokens < 0 || gamma < 1) return RRA_EINVAL;
+  if (gamma > 16) return RRA_EUNSUPPORTED;
+  if (max_tokens > (int64_t(1) << 30) || int64_t(B) * gamma > (int64_t(1) << 24)) return RRA_ERANGE;
+  const int n_rep = Hq / Hkv;
+  p->mma = true;
+  p->ctas_per_sm = 2;
+  p->hpc = verify_hpc(n_rep, gamma);
+  if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
+  p->tile = rra::decode_mma_tile_tokens(D);
+  if (block_size > 0 ? block_size < 8 : max_tokens < p->tile) return RRA_EUNSUPPORTED;
+  return plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
+}
+
+// Partial rows of the verify kernel: 16 per (sequence, KV head, head slice).
+int64_t verify_rows(int B, int gamma, int Hq, int Hkv) {
+  return int64_t(B) * Hkv * ((Hq / Hkv) / verify_hpc(Hq / Hkv, gamma)) * 16;
 }
 
 // Workspace layout, each part 256-byte aligned (R = B*Hq, G = ceil(splits / kMergeFanIn)):
@@ -447,8 +478,19 @@ int rra_rope_append(const void* q, const void* k_new, const void* v_new, const i
                     void* k_cache, void* v_cache, const int32_t* block_table, int max_blocks_per_seq, int block_size,
                     int num_blocks, int max_len, int B, int Hq, int Hkv, int D, double rope_base, int rope_style,
                     rra_dtype dt, int32_t* err_flag, void* stream) {
+  return rra_rope_append_verify(q, k_new, v_new, positions, q_out, k_cache, v_cache, block_table, max_blocks_per_seq,
+                                block_size, num_blocks, max_len, B, 1, Hq, Hkv, D, rope_base, rope_style, dt, err_flag,
+                                stream);
+}
+
+int rra_rope_append_verify(const void* q, const void* k_new, const void* v_new, const int32_t* positions, void* q_out,
+                           void* k_cache, void* v_cache, const int32_t* block_table, int max_blocks_per_seq,
+                           int block_size, int num_blocks, int max_len, int B, int gamma, int Hq, int Hkv, int D,
+                           double rope_base, int rope_style, rra_dtype dt, int32_t* err_flag, void* stream) {
   int st = check_shapes(B, Hq, Hkv, D, dt);
   if (st != RRA_OK) return st;
+  if (gamma < 1) return RRA_EINVAL;
+  if (int64_t(B) * gamma > 2147483647LL) return RRA_ERANGE;
   if (!(rope_base > 1.0) || !std::isfinite(rope_base) || (rope_style != 0 && rope_style != 1)) return RRA_EINVAL;
   if (int64_t(Hq) + Hkv > 8 * 65535) return RRA_ERANGE;
   if (B == 0) return RRA_OK;
@@ -480,6 +522,7 @@ int rra_rope_append(const void* q, const void* k_new, const void* v_new, const i
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.D = D;
+  a.gamma = gamma;
   fill_theta_pi(a.inv_freq, D, rope_base);
   a.rope_style = rope_style;
   a.err = err_flag;
@@ -752,6 +795,97 @@ int rra_decode_step_q8(const void* q, const void* k_new, const void* v_new, cons
   fill_theta_pi(a.theta_pi, D, rope_base);
   return finish_decode(rra::launch_decode_q8(a, km, vm, kwm, vwm, block_table != nullptr, true,
                                              static_cast<cudaStream_t>(stream)));
+}
+
+int rra_verify_num_splits(int B, int gamma, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
+                          int num_splits) {
+  if (block_size < 0 || (block_size > 0 && !pow2(block_size))) return block_size < 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
+  Plan p;
+  const int st = make_plan_verify(B, gamma, Hq, Hkv, D, max_tokens, block_size, num_splits, &p);
+  return st != RRA_OK ? st : p.splits;
+}
+
+size_t rra_verify_workspace_bytes(int B, int gamma, int Hq, int Hkv, int D, int splits) {
+  if (B <= 0 || gamma < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || gamma > 16) return 0;
+  const int64_t rows = verify_rows(B, gamma, Hq, Hkv);
+  if (rows > INT32_MAX) return 0;
+  return workspace_bytes(1, static_cast<int>(rows), D, splits);
+}
+
+int rra_verify_attn(const void* q_rot, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                    int max_blocks_per_seq, const int32_t* positions, int block_size, int num_blocks, int max_len,
+                    void* out, int B, int gamma, int Hq, int Hkv, int D, float scale, int num_splits, void* workspace,
+                    size_t ws_bytes, int32_t* err_flag, void* stream) {
+  int64_t capacity;
+  if (block_table != nullptr) {
+    if (!pow2(block_size)) return block_size <= 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
+    if (max_blocks_per_seq < 1 || num_blocks < 1) return RRA_EINVAL;
+    capacity = int64_t(max_blocks_per_seq) * block_size;
+  } else {
+    if (max_len < 1) return RRA_EINVAL;
+    capacity = max_len;
+  }
+  Plan p;
+  int st = make_plan_verify(B, gamma, Hq, Hkv, D, capacity, block_table ? block_size : 0, num_splits, &p);
+  if (st != RRA_OK) return st;
+  if (!std::isfinite(scale)) return RRA_EINVAL;
+  if (B == 0) return RRA_OK;
+  if (!q_rot || !k_cache || !v_cache || !positions || !out) return RRA_EINVAL;
+  if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return RRA_EINVAL;
+  const int64_t rows = verify_rows(B, gamma, Hq, Hkv);
+  if (rows > INT32_MAX) return RRA_ERANGE;
+  st = check_workspace(p, 1, static_cast<int>(rows), D, workspace, ws_bytes);
+  if (st != RRA_OK) return st;
+  CUtensorMap km{}, vm{};
+  if (block_table != nullptr) {
+    const int box_rows = block_size < p.tile ? block_size : p.tile;
+    st = encode_pool_map(&km, k_cache, num_blocks, block_size, Hkv, D, box_rows, RRA_BF16, true);
+    if (st == RRA_OK) st = encode_pool_map(&vm, v_cache, num_blocks, block_size, Hkv, D, box_rows, RRA_BF16, true);
+  } else {
+    st = encode_contig_map(&km, k_cache, B, Hkv, max_len, D, p.tile, RRA_BF16);
+    if (st == RRA_OK) st = encode_contig_map(&vm, v_cache, B, Hkv, max_len, D, p.tile, RRA_BF16);
+  }
+  if (st != RRA_OK) return st;
+  // the workspace holds `rows` partial rows: laid out as for one sequence of `rows` heads
+  rra::DecodeArgs a = decode_args(p, q_rot, k_cache, v_cache, nullptr, out, 1, static_cast<int>(rows), 1, D, scale,
+                                  workspace, err_flag);
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.gamma = gamma;
+  a.positions = positions;
+  a.block_table = block_table;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.log2_bs = block_table ? ilog2(block_size) : 0;
+  a.num_blocks = num_blocks;
+  a.max_len = block_table ? 0 : max_len;
+  a.capacity = static_cast<int>(capacity);
+  return finish_decode(rra::launch_decode_verify(a, km, vm, block_table != nullptr, static_cast<cudaStream_t>(stream)));
+}
+
+int rra_verify_step(const void* q, const void* k_new, const void* v_new, const int32_t* positions, void* q_out,
+                    void* k_cache, void* v_cache, const int32_t* block_table, int max_blocks_per_seq, int block_size,
+                    int num_blocks, int max_len, void* out, int B, int gamma, int Hq, int Hkv, int D, double rope_base,
+                    int rope_style, float scale, int num_splits, void* workspace, size_t ws_bytes, int32_t* err_flag,
+                    void* stream) {
+  // argument checks of the attention first, so that nothing is enqueued when it would refuse
+  int64_t capacity = block_table ? int64_t(max_blocks_per_seq) * block_size : max_len;
+  Plan p;
+  if (block_table != nullptr && !pow2(block_size)) return block_size <= 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
+  int st = make_plan_verify(B, gamma, Hq, Hkv, D, capacity, block_table ? block_size : 0, num_splits, &p);
+  if (st != RRA_OK) return st;
+  st = check_step_args(q, k_new, v_new, positions, q_out, k_cache, v_cache, out, B * gamma, Hq, D, rope_base,
+                       rope_style, scale, RRA_BF16);
+  if (st != RRA_OK || B == 0) return st;
+  const int64_t rows = verify_rows(B, gamma, Hq, Hkv);
+  st = check_workspace(p, 1, static_cast<int>(rows), D, workspace, ws_bytes);
+  if (st != RRA_OK) return st;
+  st = rra_rope_append_verify(q, k_new, v_new, positions, q_out, k_cache, v_cache, block_table, max_blocks_per_seq,
+                              block_size, num_blocks, max_len, B, gamma, Hq, Hkv, D, rope_base, rope_style, RRA_BF16,
+                              err_flag, stream);
+  if (st != RRA_OK) return st;
+  return rra_verify_attn(q_out, k_cache, v_cache, block_table, max_blocks_per_seq, positions, block_size, num_blocks,
+                         max_len, out, B, gamma, Hq, Hkv, D, scale, num_splits, workspace, ws_bytes, err_flag, stream);
 }
 
 }  // extern "C"

@@ -28,6 +28,7 @@ struct RopeArgs {
   int B, Hq, Hkv, D;
   int rope_style;
   int32_t* err;
+  int gamma;                    // new tokens per sequence (0 or 1: one); q/k_new/v_new/q_out [B*gamma, H, D]
   // INT8 caches only: k_cache / v_cache hold int8 codes, quantised with these per-KV-head
   // scales; with window > 0 the bf16 values also go to ring slot pos % window.
   const float* k_scale;
@@ -79,6 +80,9 @@ struct DecodeArgs {
   void* k_win;                  // bf16 [B, Hkv, window, D]
   void* v_win;
   int window;
+  // Speculative verify (verify.cuh): gamma new tokens per sequence at positions[b] ..
+  // positions[b] + gamma - 1; q and out are [B, gamma, Hq, D].
+  int gamma;
   double theta_pi[kMaxDecodeHeadDim / 2];  // theta_i / pi, theta_i = base^(-2i/D)
 };
 
@@ -121,6 +125,9 @@ cudaError_t launch_decode_step_paged(const DecodeArgs& a, const CUtensorMap& k_m
 #ifndef RRA_Q8_STAGE_BYTES
 #define RRA_Q8_STAGE_BYTES 16384
 #endif
+// Speculative verify: attention of gamma new tokens per sequence (a.gamma, a.positions set).
+cudaError_t launch_decode_verify(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map, bool paged,
+                                 cudaStream_t stream);
 // Tokens per stage of the INT8 decode kernel.
 inline int decode_q8_tile_tokens(int D) { return RRA_Q8_STAGE_BYTES / 2 / D; }
 // INT8 caches: attention only (a.seq_lens) or the fused step (a.positions, a.k_new, ...).

@@ -52,6 +52,15 @@ _SIGNATURES = {
                                     _c_int, _c_int, _c_int, _vp, _c_int, _c_int, _c_int, _c_int, _c_f64, _c_int,
                                     _c_f32, _c_int, _vp, _c_size, _vp, _vp]),
     "rra_decode_q8_num_splits": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int]),
+    "rra_rope_append_verify": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                        _c_int, _c_int, _c_int, _c_int, _c_int, _c_f64, _c_int, _c_int, _vp, _vp]),
+    "rra_verify_attn": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _vp, _c_int, _c_int,
+                                 _c_int, _c_int, _c_int, _c_f32, _c_int, _vp, _c_size, _vp, _vp]),
+    "rra_verify_step": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp,
+                                 _c_int, _c_int, _c_int, _c_int, _c_int, _c_f64, _c_int, _c_f32, _c_int, _vp, _c_size,
+                                 _vp, _vp]),
+    "rra_verify_num_splits": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_int]),
+    "rra_verify_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
 }
 
 
@@ -278,3 +287,60 @@ def rra_decode_step_q8(q, k_new, v_new, positions, q_out, k_codes, v_codes, k_sc
                                   float(rope_base), int(rope_style), float(scale), int(num_splits), _ptr(workspace),
                                   ws_bytes, _ptr(err_flag), _stream(stream, q))
     _check("rra_decode_step_q8", st)
+
+
+# --------------------------------------------------------------------------- speculative verify
+def _cache_layout(k_cache, block_table):
+    """(block_table columns, block_size, num_blocks, max_len, Hkv) of a bf16 / fp32 cache."""
+    if block_table is not None:
+        return block_table.shape[1], k_cache.shape[1], k_cache.shape[0], 0, k_cache.shape[2]
+    return 0, 0, 0, k_cache.shape[2], k_cache.shape[1]
+
+
+def rra_verify_num_splits(B: int, gamma: int, Hq: int, Hkv: int, D: int, max_tokens: int, block_size: int,
+                          num_splits: int) -> int:
+    r = lib().rra_verify_num_splits(B, gamma, Hq, Hkv, D, max_tokens, block_size, num_splits)
+    _check("rra_verify_num_splits", min(r, 0))
+    return r
+
+
+def rra_verify_workspace_bytes(B: int, gamma: int, Hq: int, Hkv: int, D: int, splits: int) -> int:
+    return int(lib().rra_verify_workspace_bytes(B, gamma, Hq, Hkv, D, splits))
+
+
+def rra_rope_append_verify(q, k_new, v_new, positions, q_out, k_cache, v_cache, block_table=None,
+                           rope_base: float = 10000.0, rope_style: int = 0, err_flag=None, stream=None) -> None:
+    """RoPE on q / k_new [B, gamma, H, D] (token j at positions[b] + j) and append of the gamma tokens."""
+    B, gamma, Hq, D = q.shape
+    mbps, bs, nblk, max_len, Hkv = _cache_layout(k_cache, block_table)
+    st = lib().rra_rope_append_verify(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q_out), _ptr(k_cache),
+                                      _ptr(v_cache), _ptr(block_table), mbps, bs, nblk, max_len, B, gamma, Hq, Hkv, D,
+                                      float(rope_base), int(rope_style), _dtype_code(q), _ptr(err_flag),
+                                      _stream(stream, q))
+    _check("rra_rope_append_verify", st)
+
+
+def rra_verify_attn(q_rot, k_cache, v_cache, positions, out, block_table=None, scale: float = 0.0, num_splits: int = 0,
+                    workspace=None, err_flag=None, stream=None) -> None:
+    """out[b, j] = attention of q_rot[b, j] over tokens [0, positions[b] + j] (bf16 caches)."""
+    B, gamma, Hq, D = q_rot.shape
+    mbps, bs, nblk, max_len, Hkv = _cache_layout(k_cache, block_table)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().rra_verify_attn(_ptr(q_rot), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), mbps, _ptr(positions), bs,
+                               nblk, max_len, _ptr(out), B, gamma, Hq, Hkv, D, float(scale), int(num_splits),
+                               _ptr(workspace), ws_bytes, _ptr(err_flag), _stream(stream, q_rot))
+    _check("rra_verify_attn", st)
+
+
+def rra_verify_step(q, k_new, v_new, positions, q_out, k_cache, v_cache, out, block_table=None,
+                    rope_base: float = 10000.0, rope_style: int = 0, scale: float = 0.0, num_splits: int = 0,
+                    workspace=None, err_flag=None, stream=None) -> None:
+    """The whole speculative-verify step: RoPE + append of the gamma tokens, then their causal attention."""
+    B, gamma, Hq, D = q.shape
+    mbps, bs, nblk, max_len, Hkv = _cache_layout(k_cache, block_table)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().rra_verify_step(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q_out), _ptr(k_cache),
+                               _ptr(v_cache), _ptr(block_table), mbps, bs, nblk, max_len, _ptr(out), B, gamma, Hq, Hkv,
+                               D, float(rope_base), int(rope_style), float(scale), int(num_splits), _ptr(workspace),
+                               ws_bytes, _ptr(err_flag), _stream(stream, q))
+    _check("rra_verify_step", st)

@@ -157,3 +157,57 @@ class DecodeStepQ8(DecodeStep):
                                self.v_scale, self.out, self.k_win, self.v_win, self.block_table, self.rope_base,
                                self.rope_style, self.scale, self.num_splits, self.workspace, self.err, stream)
         return self.out
+
+
+class VerifyStep(DecodeStep):
+    """The speculative-verify step: gamma new tokens per sequence, causal inside the chunk.
+
+    q / k_new / v_new are [B, gamma, H, D]; ``positions[b]`` is the first new token's position,
+    and the output is [B, gamma, Hq, D]. Caches as for DecodeStep (bf16).
+    """
+
+    def __init__(self, batch: int, gamma: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                 k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: Optional[torch.Tensor] = None,
+                 num_splits: int = 0, rope_base: float = 10000.0, rope_style: int = 0, scale: float = 0.0):
+        self.B, self.gamma, self.Hq, self.Hkv, self.D = batch, gamma, n_q_heads, n_kv_heads, head_dim
+        self.k_cache, self.v_cache, self.block_table = k_cache, v_cache, block_table
+        self.rope_base, self.rope_style, self.scale = rope_base, rope_style, scale
+        self.dtype, dev = k_cache.dtype, k_cache.device
+        if block_table is not None:
+            bs = k_cache.shape[1]
+            max_tokens = block_table.shape[1] * bs
+        else:
+            bs, max_tokens = 0, k_cache.shape[2]
+        self.splits = rra.rra_verify_num_splits(batch, gamma, n_q_heads, n_kv_heads, head_dim, max_tokens, bs,
+                                                num_splits)
+        self.num_splits = num_splits
+        ws = rra.rra_verify_workspace_bytes(batch, gamma, n_q_heads, n_kv_heads, head_dim, self.splits)
+        self.workspace = torch.zeros(ws, dtype=torch.uint8, device=dev) if ws else None  # zeroed once
+        self.q_rot = torch.empty(batch, gamma, n_q_heads, head_dim, dtype=self.dtype, device=dev)
+        self.out = torch.empty(batch, gamma, n_q_heads, head_dim, dtype=self.dtype, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.graph = None
+
+    def rope_append(self, q, k_new, v_new, positions, stream=None) -> None:
+        rra.rra_rope_append_verify(q, k_new, v_new, positions, self.q_rot, self.k_cache, self.v_cache,
+                                   self.block_table, self.rope_base, self.rope_style, self.err, stream)
+
+    def attend(self, positions, stream=None) -> torch.Tensor:
+        """Attention of the already-appended gamma tokens (``positions``: the first one's)."""
+        rra.rra_verify_attn(self.q_rot, self.k_cache, self.v_cache, positions, self.out, self.block_table, self.scale,
+                            self.num_splits, self.workspace, self.err, stream)
+        return self.out
+
+    def fused(self, q, k_new, v_new, positions, stream=None) -> torch.Tensor:
+        rra.rra_verify_step(q, k_new, v_new, positions, self.q_rot, self.k_cache, self.v_cache, self.out,
+                            self.block_table, self.rope_base, self.rope_style, self.scale, self.num_splits,
+                            self.workspace, self.err, stream)
+        return self.out
+
+    def __call__(self, q, k_new, v_new, positions, seq_lens=None, stream=None) -> torch.Tensor:
+        """The step in one library call (seq_lens None), or the two calls (seq_lens ignored: the
+        attended lengths follow from the positions)."""
+        if seq_lens is None:
+            return self.fused(q, k_new, v_new, positions, stream)
+        self.rope_append(q, k_new, v_new, positions, stream)
+        return self.attend(positions, stream)

@@ -186,3 +186,32 @@ def run_oracle_q8(inp: DecodeInputs, rope_style: int = 0, seq_lens=None):
     return oracle.quant.decode_step_q8(inp.q, inp.k_new, inp.v_new, inp.positions, inp.k_cache, inp.v_cache,
                                        inp.k_scale, inp.v_scale, inp.k_win, inp.v_win, cfg.window, inp.block_table,
                                        bs, seq_lens=seq_lens, rope_base=cfg.rope_base, rope_style=rope_style)
+
+
+# ---------------------------------------------------------------------------- speculative verify
+def run_gpu_verify(inp: DecodeInputs, num_splits: int = 0, rope_style: int = 0, device="cuda:0",
+                   fused: bool = True) -> GpuResult:
+    """One verify step (gamma new tokens per sequence) through the C ABI."""
+    from rope_gqa_paged_gb300 import VerifyStep
+
+    cfg = inp.cfg
+    dt = cfg.dtype
+    kc, vc = to_torch(inp.k_cache, dt, device), to_torch(inp.v_cache, dt, device)
+    table = to_torch(inp.block_table, "i32", device) if inp.block_table is not None else None
+    step = VerifyStep(cfg.batch, cfg.gamma, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, kc, vc, table,
+                      num_splits=num_splits or cfg.num_splits, rope_base=cfg.rope_base, rope_style=rope_style)
+    args = (to_torch(inp.q, dt, device), to_torch(inp.k_new, dt, device), to_torch(inp.v_new, dt, device),
+            to_torch(inp.positions, "i32", device))
+    out = step(*args) if fused else step(*args, seq_lens=True)
+    torch.cuda.synchronize(device)
+    res = GpuResult(q_rot=to_numpy(step.q_rot), out=to_numpy(out), k_cache=to_numpy(kc), v_cache=to_numpy(vc),
+                    err=step.error_bits(), splits=step.splits)
+    del kc, vc, step
+    return res
+
+
+def run_oracle_verify(inp: DecodeInputs, rope_style: int = 0):
+    cfg = inp.cfg
+    bs = cfg.block_size if inp.block_table is not None else 0
+    return oracle.verify.verify_step(inp.q, inp.k_new, inp.v_new, inp.positions, inp.k_cache, inp.v_cache, cfg.dtype,
+                                     inp.block_table, bs, rope_base=cfg.rope_base, rope_style=rope_style)

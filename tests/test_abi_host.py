@@ -149,3 +149,19 @@ def test_q8_argument_checks_reject_before_any_launch(rra):
              None) == RRA_EINVAL                                                # missing K scale
     assert r(P, P, P, P, P, P, P, P, P, None, P, 16, None, 0, 0, 0, 256, 1, 8, 8, 128, 10000.0, 0, None,
              None) == RRA_EINVAL                                                # missing k ring
+
+
+def test_verify_planning(rra):
+    S = rra.rra_verify_num_splits
+    assert S(64, 4, 32, 8, 128, 8192, 16, 4) == 4
+    assert S(1, 4, 32, 8, 128, 131072, 32, 64) == 64
+    lib = rra.lib()
+    for bad, status in (((1, 0, 32, 8, 128, 1024, 16, 0), RRA_EINVAL),        # gamma 0
+                        ((1, 17, 32, 8, 128, 1024, 16, 0), RRA_EUNSUPPORTED),  # gamma above 16
+                        ((1, 4, 32, 8, 128, 1024, 4, 0), RRA_EUNSUPPORTED),   # blocks under 8 tokens
+                        ((1, 4, 32, 8, 128, 32, 0, 0), RRA_EUNSUPPORTED),     # contiguous cache under one tile
+                        ((1, 4, 6, 4, 128, 1024, 16, 0), RRA_EINVAL)):
+        assert lib.rra_verify_num_splits(*bad) == status, bad
+    # 16 partial rows per (sequence, KV head, head slice): MQA with gamma 4 takes 8 slices of 4 heads
+    assert rra.rra_verify_workspace_bytes(2, 4, 32, 1, 128, 4) == rra.rra_verify_workspace_bytes(1, 4, 32, 8, 128, 4) * 2
+    assert rra.rra_verify_workspace_bytes(2, 4, 32, 8, 128, 1) == 0
