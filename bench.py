@@ -243,7 +243,7 @@ def device_workload(cfg, seed, device):
 def run_ours(args):
     import torch
 
-    from rope_gqa_paged_gb300 import DecodeStep, DecodeStepQ8, _build
+    from rope_gqa_paged_gb300 import DecodeStep, DecodeStepQ8, VerifyStep, _build
 
     rank, local_rank, world = dist_env()
     if world > 1:
@@ -263,7 +263,10 @@ def run_ours(args):
     # Without prefix sharing this equals the logical bytes the attention consumes.
     kv_bytes = cfg.unique_kv_bytes(lengths)
     logical_bytes = cfg.kv_bytes(lengths)
-    if cfg.int8:
+    if cfg.gamma > 1:
+        step = VerifyStep(cfg.batch, cfg.gamma, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, w["k_cache"],
+                          w["v_cache"], w["block_table"], num_splits=splits_arg, rope_base=cfg.rope_base)
+    elif cfg.int8:
         step = DecodeStepQ8(cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, w["k_cache"], w["v_cache"],
                             w["k_scale"], w["v_scale"], w["k_win"], w["v_win"], w["block_table"],
                             num_splits=splits_arg, rope_base=cfg.rope_base)
@@ -274,7 +277,8 @@ def run_ours(args):
     mma_path = cfg.int8 or (cfg.dtype == "bf16" and (
         (cfg.layout == "paged" and cfg.block_size >= 8) or
         (cfg.layout == "contiguous" and cfg.max_len >= 16384 // (2 * cfg.head_dim))))
-    launches_per_step = 1 if mma_path else 2
+    launches_per_step = 1 if mma_path and cfg.gamma == 1 else 2
+    attend_arg = w["positions"] if cfg.gamma > 1 else w["seq_lens"]   # verify: lengths follow the positions
     flush = None
     if 2 * kv_bytes < 3 * L2_BYTES:                     # inputs not much larger than L2: flush between steps
         flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=device)
@@ -303,7 +307,7 @@ def run_ours(args):
         ev[i][0].record(stream)
         step.rope_append(w["q"], w["k_new"], w["v_new"], w["positions"])
         ev[i][1].record(stream)
-        step.attend(w["seq_lens"])
+        step.attend(attend_arg)
         ev[i][2].record(stream)
     torch.cuda.synchronize(device)
     rope_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
@@ -448,7 +452,9 @@ def run_ours(args):
                                                                        "both": round(eager_ms, 5)}},
         "step_timing": graph_note,
         "single_step_graph_ms": round(single_ms, 5),
-        "roofline": {"kernel": ("decode_q8_kernel, fused step (RoPE + quantised append + split-K attention over "
+        "roofline": {"kernel": ("rope_append (gamma tokens) + decode_verify_kernel (causal split-K attention of "
+                                f"{cfg.gamma} new tokens per sequence + merge)" if cfg.gamma > 1 else
+                                "decode_q8_kernel, fused step (RoPE + quantised append + split-K attention over "
                                 "INT8 codes and the bf16 window + merge)" if cfg.int8 else
                                 "decode_mma_kernel, fused step (RoPE + append + split-K attention + merge)"
                                 if mma_path else "rope_append + decode_split_kernel (fused-step call)"),
@@ -486,7 +492,11 @@ def oracle_step_seconds(inp):
     cfg = inp.cfg
     bs = cfg.block_size if inp.block_table is not None else 0
     t0 = time.perf_counter()
-    if cfg.int8:
+    if cfg.gamma > 1:
+        from oracle import verify
+        verify.verify_step(inp.q, inp.k_new, inp.v_new, inp.positions, inp.k_cache, inp.v_cache, cfg.dtype,
+                           inp.block_table, bs, rope_base=cfg.rope_base)
+    elif cfg.int8:
         from oracle import quant
         quant.decode_step_q8(inp.q, inp.k_new, inp.v_new, inp.positions, inp.k_cache, inp.v_cache, inp.k_scale,
                              inp.v_scale, inp.k_win, inp.v_win, cfg.window, inp.block_table, bs,

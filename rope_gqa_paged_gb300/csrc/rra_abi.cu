@@ -170,7 +170,7 @@ int make_plan_q8(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_si
 }
 
 // Speculative verify: one CTA serves hpc heads x gamma new tokens (at most 16 query rows) of one
-// KV head; hpc is the largest divisor of n_rep with hpc * gamma <= 16. Two CTAs per SM.
+// KV head; hpc is the largest divisor of n_rep with hpc * gamma <= 16. Three CTAs per SM.
 int verify_hpc(int n_rep, int gamma) {
   for (int h = std::min(n_rep, 16 / gamma); h > 1; --h)
     if (n_rep % h == 0) return h;
@@ -186,7 +186,6 @@ int make_plan_verify(int B, int gamma, int Hq, int Hkv, int D, int64_t max_token
   if (max_tokens > (int64_t(1) << 30) || int64_t(B) * gamma > (int64_t(1) << 24)) return RRA_ERANGE;
   const int n_rep = Hq / Hkv;
   p->mma = true;
-  p->ctas_per_sm = 2;
   p->hpc = verify_hpc(n_rep, gamma);
   if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
   p->tile = rra::decode_mma_tile_tokens(D);

@@ -14,7 +14,7 @@
 // and the score accumulator of two 8-token halves is already the A fragment of P. The causal
 // limit of each row masks the new tokens it may not see. The pipeline (TMA into a ring of 32 KB
 // stages of 64-dim halves, 128-byte swizzle), the 4-warp token split, the merge of the warps
-// and of the splits are those of decode_mma.cuh / decode_kernels.cuh.
+// and of the splits are those of decode_mma.cuh / decode_kernels.cuh; three CTAs per SM.
 #pragma once
 
 #include "decode_mma.cuh"
@@ -154,7 +154,7 @@ struct VerifyRows {
 };
 
 template <int D, bool PAGED>
-__global__ void __launch_bounds__(MmaCfg<D>::kThreads, 2)
+__global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     decode_verify_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                          const DecodeArgs a) {
   using C = MmaCfg<D>;
