@@ -37,6 +37,7 @@ if ROOT not in sys.path:
 from workloads import CONFIGS, make_inputs, make_structure  # noqa: E402
 
 METRIC = "decode-attn KV GB/s & % of GB300 HBM peak; decode steps/s per layer"
+PREFILL_METRIC = "prefill causal attention TFLOP/s & % of GB300 bf16 tensor peak"
 UNIT = "GB/s"
 DEFAULT_WORKLOAD = "batched_paged"
 NOMINAL_HBM_GBS = 8000.0
@@ -90,6 +91,22 @@ def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def tensor_peak():
+    """Sustained bf16 dense TFLOP/s (the prefill kernel runs for tens to hundreds of ms)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"]), "measured (MEASURED_PEAKS.json bf16_tflops_sustained)"
+    except (OSError, KeyError, ValueError):
+        return 1700.0, "fallback (1.7 PFLOP/s sustained)"
+
+
+def prefill_flops(cfg, lengths) -> int:
+    """Causal attention FLOPs of a prefill step: 4 D Hq per (prompt token, attended key)."""
+    T = cfg.gamma
+    keys = sum(T * (int(L) - T) + T * (T + 1) // 2 for L in lengths)
+    return 4 * cfg.head_dim * cfg.n_q_heads * keys
 
 
 def hbm_peak():
@@ -243,7 +260,7 @@ def device_workload(cfg, seed, device):
 def run_ours(args):
     import torch
 
-    from rope_gqa_paged_gb300 import DecodeStep, DecodeStepQ8, VerifyStep, _build
+    from rope_gqa_paged_gb300 import DecodeStep, DecodeStepQ8, PrefillStep, VerifyStep, _build
 
     rank, local_rank, world = dist_env()
     if world > 1:
@@ -263,7 +280,15 @@ def run_ours(args):
     # Without prefix sharing this equals the logical bytes the attention consumes.
     kv_bytes = cfg.unique_kv_bytes(lengths)
     logical_bytes = cfg.kv_bytes(lengths)
-    if cfg.gamma > 1:
+    prefill = cfg.gamma > 16
+    if prefill:   # the work is causal attention FLOPs, reported in TFLOP/s
+        work, div, unit, metric = prefill_flops(cfg, lengths), 1e12, "TFLOP/s", PREFILL_METRIC
+    else:         # the work is KV bytes, reported in GB/s
+        work, div, unit, metric = kv_bytes, 1e9, UNIT, METRIC
+    if prefill:
+        step = PrefillStep(cfg.batch, cfg.gamma, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, w["k_cache"],
+                           w["v_cache"], w["block_table"], rope_base=cfg.rope_base)
+    elif cfg.gamma > 1:
         step = VerifyStep(cfg.batch, cfg.gamma, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, w["k_cache"],
                           w["v_cache"], w["block_table"], num_splits=splits_arg, rope_base=cfg.rope_base)
     elif cfg.int8:
@@ -416,19 +441,24 @@ def run_ours(args):
         torch.cuda.synchronize(device)
         barrier(world)
         e2e_ms = sum(e_ev[i][0].elapsed_time(e_ev[i][1]) for i in range(K)) / K
-        e2e_ms, e2e_bytes = aggregate(e2e_ms, kv_bytes, world, device)
-        e2e = {"value": round(e2e_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
+        e2e_ms, e2e_work = aggregate(e2e_ms, work, world, device)
+        e2e = {"value": round(e2e_work / (e2e_ms * 1e-3) / div, 2), "unit": unit, "ms_per_step": round(e2e_ms, 4),
                "h2d_bytes_per_step": h2d * world, "d2h_bytes_per_step": d2h * world}
 
-    ms, total_bytes = aggregate(ms_local, kv_bytes, world, device)
+    ms, total_work = aggregate(ms_local, work, world, device)
     dec_avg = sum(dec_ms) / K
-    peak, peak_src = hbm_peak()
-    achieved = kv_bytes / (fused_ms * 1e-3) / 1e9
-    value = total_bytes / (ms * 1e-3) / 1e9
+    if prefill:   # the dominant kernel is the attention itself (the append is ~1 % of the step)
+        peak, peak_src = tensor_peak()
+        achieved = work / (dec_avg * 1e-3) / div
+    else:
+        peak, peak_src = hbm_peak()
+        peak_src = f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+        achieved = work / (fused_ms * 1e-3) / div
+    value = total_work / (ms * 1e-3) / div
     if rank != 0:
         return 0
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": K,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8 K/V codes + bf16 window, f16 mma, f32 softmax" if cfg.int8 else cfg.dtype, "data": "synthetic (seeded N(0,1); lengths/tables from the recipe)",
         "config": {
@@ -438,6 +468,8 @@ def run_ours(args):
             "seq_lens": (f"U[{cfg.len_range[0]},{cfg.len_range[1]}] mean {float(np.mean(lengths)):.1f}"
                          if cfg.len_range else cfg.seq_len),
             "num_splits": step.splits, "kv_bytes_per_step_per_gpu": kv_bytes,
+            "new_tokens_per_sequence": cfg.gamma,
+            "work_per_step_per_gpu": work, "work_unit": "FLOP" if prefill else "byte",
             "logical_kv_bytes_per_step_per_gpu": logical_bytes,
             "logical_kv_gbs": round(logical_bytes * world / (ms * 1e-3) / 1e9, 2),
             "l2": ("flushed between steps (2x L2 write, outside the timed events)" if flush is not None
@@ -445,22 +477,24 @@ def run_ours(args):
             "parallelism": f"replicas x{world}",
         },
         "decode_steps_per_s_per_layer": round(1e3 / ms, 2),
-        "pct_of_nominal_8TBs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
-        "pct_of_measured_hbm": round(100 * value / world / peak, 2),
+        "pct_of_nominal_8TBs": None if prefill else round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_hbm": None if prefill else round(100 * value / world / peak, 2),
+        "pct_of_measured_tensor": round(100 * value / world / peak, 2) if prefill else None,
         "kernel_ms": {"fused_step": round(fused_ms, 5), "two_calls": {"rope_append": round(sum(rope_ms) / K, 5),
                                                                        "decode_attn": round(dec_avg, 5),
                                                                        "both": round(eager_ms, 5)}},
         "step_timing": graph_note,
         "single_step_graph_ms": round(single_ms, 5),
-        "roofline": {"kernel": ("rope_append (gamma tokens) + decode_verify_kernel (causal split-K attention of "
+        "roofline": {"kernel": ("prefill_kernel (causal attention of the prompt, 64 query rows per CTA)" if prefill else
+                                "rope_append (gamma tokens) + decode_verify_kernel (causal split-K attention of "
                                 f"{cfg.gamma} new tokens per sequence + merge)" if cfg.gamma > 1 else
                                 "decode_q8_kernel, fused step (RoPE + quantised append + split-K attention over "
                                 "INT8 codes and the bf16 window + merge)" if cfg.int8 else
                                 "decode_mma_kernel, fused step (RoPE + append + split-K attention + merge)"
                                 if mma_path else "rope_append + decode_split_kernel (fused-step call)"),
-                     "bound": "hbm",
-                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "bound": "tensor" if prefill else "hbm",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
                      "traffic": recorded_traffic(cfg.name)},
         "gpu_launches": K * launches_per_step,
         "device_error_bits": err_bits,
@@ -480,10 +514,21 @@ def oracle_sample_config(cfg, batch):
     import dataclasses
     import math
     kw = {"batch": batch, "name": cfg.name + f"_sample{batch}"}
+    if cfg.gamma > 16:          # prefill: a 512-token prompt of the same shape
+        kw.update(seq_len=512, gamma=512)
     if cfg.layout == "paged":
         longest = cfg.seq_len if cfg.seq_len is not None else cfg.len_range[1]
         kw["num_blocks"] = batch * math.ceil(longest / cfg.block_size) + 8
     return dataclasses.replace(cfg, **kw)
+
+
+def sample_work(inp):
+    """(work, divisor, unit, metric) of one oracle step on a sample: KV bytes in GB/s, or for a
+    prefill the causal attention FLOPs in TFLOP/s."""
+    cfg = inp.cfg
+    if cfg.gamma > 16:
+        return prefill_flops(cfg, inp.lengths), 1e12, "TFLOP/s", PREFILL_METRIC
+    return cfg.unique_kv_bytes(inp.lengths), 1e9, UNIT, METRIC
 
 
 def oracle_step_seconds(inp):
@@ -511,12 +556,12 @@ def cpu_worker(workload: str, seconds: float):
     cfg = CONFIGS[workload]
     sample_batch = 1 if cfg.batch == 1 or cfg.layout == "contiguous" else 2
     inp = make_inputs(oracle_sample_config(cfg, sample_batch), seed=cfg.seed)
-    nbytes = cfg.unique_kv_bytes(inp.lengths)
+    work, div, unit, _ = sample_work(inp)
     elapsed, done = 0.0, 0
     while elapsed < seconds or done == 0:
         elapsed += oracle_step_seconds(inp)
         done += 1
-    return {"value": round(done * nbytes / elapsed / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": round(done * work / elapsed / div, 6), "unit": unit, "cores": 1, "kind": "oracle",
             "sample": (f"float64 numpy oracle (RoPE + append + attention) on the first {sample_batch} "
                        f"sequence(s) of {workload} (lengths {inp.lengths.tolist()}), repeated {done}x "
                        f"in {elapsed:.1f} s; BLAS limited to 1 thread")}
@@ -545,21 +590,21 @@ def run_reference(args):
     cfg = CONFIGS[args.workload]
     sample_batch = 1 if cfg.batch == 1 or cfg.layout == "contiguous" else 2
     inp = make_inputs(oracle_sample_config(cfg, sample_batch), seed=cfg.seed)
-    nbytes = cfg.unique_kv_bytes(inp.lengths)
+    work, div, unit, metric = sample_work(inp)
     for _ in range(args.warmup):
         oracle_step_seconds(inp)
     secs = [oracle_step_seconds(inp) for _ in range(args.steps)]
     ms = 1e3 * sum(secs) / len(secs)
-    value = nbytes / (ms * 1e-3) / 1e9
+    value = work / (ms * 1e-3) / div
     sample = (f"float64 numpy oracle on the first {sample_batch} sequence(s) of {cfg.name} per step "
               f"(lengths {inp.lengths.tolist()}); BLAS limited to 1 thread")
     print(json.dumps({
-        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": metric, "value": round(value, 6), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg.name, "description": cfg.description, "sample_batch": sample_batch},
-        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
-        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
     return 0
 

@@ -275,6 +275,31 @@ RRA_API int rra_verify_num_splits(int B, int gamma, int Hq, int Hkv, int D, int6
 /* Workspace bytes of rra_verify_attn for an effective split count; 0 when splits <= 1. */
 RRA_API size_t rra_verify_workspace_bytes(int B, int gamma, int Hq, int Hkv, int D, int splits);
 
+/* --- Prefill: causal attention of a whole prompt (or a chunk of one after a cached prefix) ---
+ *
+ * [Opt-2026] §三 (FlashAttention: softmax(Q K^T / sqrt(d)) V by blocks with a running max and
+ * sum, never materialising the T x T scores). The T prompt tokens of sequence b sit at
+ * positions p_b .. p_b + T - 1 (positions[b] = p_b; p_b = 0 for a fresh prompt), and token t
+ * attends tokens [0, p_b + t]: the definition of the verify calls with gamma = T.
+ * rra_rope_append_verify(..., gamma = T, ...) rotates and appends them; then: */
+
+/* out[b, t, h] = softmax(q_rot[b, t, h] . K[b, h / n_rep, 0 : p_b + t + 1]^T * scale) . V[...],
+ * bf16, q_rot and out [B, T, Hq, D], caches as in the decode calls (paged blocks of at least 8
+ * tokens, contiguous caches of at least 16384 / (2 D) tokens). 64 query rows per CTA, no
+ * workspace. A prompt that runs past the cache sets RRA_ERR_POSITION and skips b. */
+RRA_API int rra_prefill_attn(const void* q_rot, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                             int max_blocks_per_seq, const int32_t* positions, int block_size, int num_blocks,
+                             int max_len, void* out, int B, int T, int Hq, int Hkv, int D, float scale,
+                             int32_t* err_flag, void* stream);
+
+/* rra_rope_append_verify with gamma = T, then rra_prefill_attn on q_out. bf16. q_out must not
+ * overlap q. */
+RRA_API int rra_prefill_step(const void* q, const void* k_new, const void* v_new, const int32_t* positions,
+                             void* q_out, void* k_cache, void* v_cache, const int32_t* block_table,
+                             int max_blocks_per_seq, int block_size, int num_blocks, int max_len, void* out, int B,
+                             int T, int Hq, int Hkv, int D, double rope_base, int rope_style, float scale,
+                             int32_t* err_flag, void* stream);
+
 /* Bytes of a K+V cache: 2 * n_layers * n_kv_heads * head_dim * seq_len * batch * dtype_bytes
  * ([Opt-2026] §四 memory formula; [KVC-GQA-RoPE] §5.3). Host only; returns 0 when an
  * argument is negative or the product overflows 64 bits. */

@@ -12,6 +12,6 @@ from .rra import (RRA_BF16, RRA_ERR_BLOCK_ID, RRA_ERR_POSITION, RRA_ERR_SEQ_LEN,
                   rra_kv_bytes, rra_rope_append,
                   rra_status_str, rra_rope_append_q8, rra_decode_attn_q8, rra_decode_step_q8,
                   rra_decode_q8_num_splits, rra_rope_append_verify, rra_verify_attn, rra_verify_step,
-                  rra_verify_num_splits, rra_verify_workspace_bytes)
-from .step import DecodeStep, DecodeStepQ8, VerifyStep  # noqa: F401
+                  rra_verify_num_splits, rra_verify_workspace_bytes, rra_prefill_attn, rra_prefill_step)
+from .step import DecodeStep, DecodeStepQ8, PrefillStep, VerifyStep  # noqa: F401
 from ._build import build  # noqa: F401

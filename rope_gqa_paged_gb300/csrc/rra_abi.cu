@@ -193,6 +193,13 @@ int make_plan_verify(int B, int gamma, int Hq, int Hkv, int D, int64_t max_token
   return plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
 }
 
+// Prefill: 64 query rows per CTA, hpc heads x 64 / hpc prompt tokens; hpc divides n_rep and 64.
+int prefill_hpc(int n_rep) {
+  for (int h = std::min(n_rep, 64); h > 1; --h)
+    if (n_rep % h == 0 && 64 % h == 0) return h;
+  return 1;
+}
+
 // Partial rows of the verify kernel: 16 per (sequence, KV head, head slice).
 int64_t verify_rows(int B, int gamma, int Hq, int Hkv) {
   return int64_t(B) * Hkv * ((Hq / Hkv) / verify_hpc(Hq / Hkv, gamma)) * 16;
@@ -885,6 +892,85 @@ int rra_verify_step(const void* q, const void* k_new, const void* v_new, const i
   if (st != RRA_OK) return st;
   return rra_verify_attn(q_out, k_cache, v_cache, block_table, max_blocks_per_seq, positions, block_size, num_blocks,
                          max_len, out, B, gamma, Hq, Hkv, D, scale, num_splits, workspace, ws_bytes, err_flag, stream);
+}
+
+int rra_prefill_attn(const void* q_rot, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                     int max_blocks_per_seq, const int32_t* positions, int block_size, int num_blocks, int max_len,
+                     void* out, int B, int T, int Hq, int Hkv, int D, float scale, int32_t* err_flag, void* stream) {
+  int st = check_shapes(B, Hq, Hkv, D, RRA_BF16);
+  if (st != RRA_OK) return st;
+  if (T < 1 || !std::isfinite(scale)) return RRA_EINVAL;
+  int64_t capacity;
+  if (block_table != nullptr) {
+    if (!pow2(block_size)) return block_size <= 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
+    if (block_size < 8) return RRA_EUNSUPPORTED;
+    if (max_blocks_per_seq < 1 || num_blocks < 1) return RRA_EINVAL;
+    capacity = int64_t(max_blocks_per_seq) * block_size;
+  } else {
+    if (max_len < 1) return RRA_EINVAL;
+    if (max_len < rra::decode_mma_tile_tokens(D)) return RRA_EUNSUPPORTED;
+    capacity = max_len;
+  }
+  if (capacity > (int64_t(1) << 30)) return RRA_ERANGE;
+  const int n_rep = Hq / Hkv;
+  const int hpc = prefill_hpc(n_rep);
+  if (int64_t(Hkv) * (n_rep / hpc) > 65535) return RRA_ERANGE;
+  if (B == 0) return RRA_OK;
+  if (!q_rot || !k_cache || !v_cache || !positions || !out) return RRA_EINVAL;
+  if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return RRA_EINVAL;
+  const int tile = rra::decode_mma_tile_tokens(D);
+  CUtensorMap km{}, vm{};
+  if (block_table != nullptr) {
+    const int box_rows = block_size < tile ? block_size : tile;
+    st = encode_pool_map(&km, k_cache, num_blocks, block_size, Hkv, D, box_rows, RRA_BF16, true);
+    if (st == RRA_OK) st = encode_pool_map(&vm, v_cache, num_blocks, block_size, Hkv, D, box_rows, RRA_BF16, true);
+  } else {
+    st = encode_contig_map(&km, k_cache, B, Hkv, max_len, D, tile, RRA_BF16);
+    if (st == RRA_OK) st = encode_contig_map(&vm, v_cache, B, Hkv, max_len, D, tile, RRA_BF16);
+  }
+  if (st != RRA_OK) return st;
+  rra::DecodeArgs a{};
+  a.q = q_rot;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.out = out;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.hpc = hpc;
+  a.gamma = T;
+  a.positions = positions;
+  a.block_table = block_table;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.log2_bs = block_table ? ilog2(block_size) : 0;
+  a.num_blocks = num_blocks;
+  a.max_len = block_table ? 0 : max_len;
+  a.capacity = static_cast<int>(capacity);
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
+  a.scale_log2 = sc * 1.4426950408889634f;
+  a.err = err_flag;
+  return finish_decode(rra::launch_prefill(a, km, vm, block_table != nullptr, static_cast<cudaStream_t>(stream)));
+}
+
+int rra_prefill_step(const void* q, const void* k_new, const void* v_new, const int32_t* positions, void* q_out,
+                     void* k_cache, void* v_cache, const int32_t* block_table, int max_blocks_per_seq, int block_size,
+                     int num_blocks, int max_len, void* out, int B, int T, int Hq, int Hkv, int D, double rope_base,
+                     int rope_style, float scale, int32_t* err_flag, void* stream) {
+  int st = check_shapes(B, Hq, Hkv, D, RRA_BF16);
+  if (st != RRA_OK) return st;
+  if (T < 1) return RRA_EINVAL;
+  if (block_table != nullptr ? (!pow2(block_size) || block_size < 8) : max_len < rra::decode_mma_tile_tokens(D))
+    return block_table != nullptr && block_size <= 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
+  st = check_step_args(q, k_new, v_new, positions, q_out, k_cache, v_cache, out, B * T, Hq, D, rope_base, rope_style,
+                       scale, RRA_BF16);
+  if (st != RRA_OK || B == 0) return st;
+  st = rra_rope_append_verify(q, k_new, v_new, positions, q_out, k_cache, v_cache, block_table, max_blocks_per_seq,
+                              block_size, num_blocks, max_len, B, T, Hq, Hkv, D, rope_base, rope_style, RRA_BF16,
+                              err_flag, stream);
+  if (st != RRA_OK) return st;
+  return rra_prefill_attn(q_out, k_cache, v_cache, block_table, max_blocks_per_seq, positions, block_size, num_blocks,
+                          max_len, out, B, T, Hq, Hkv, D, scale, err_flag, stream);
 }
 
 }  // extern "C"

@@ -128,6 +128,10 @@ cudaError_t launch_decode_step_paged(const DecodeArgs& a, const CUtensorMap& k_m
 // Speculative verify: attention of gamma new tokens per sequence (a.gamma, a.positions set).
 cudaError_t launch_decode_verify(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map, bool paged,
                                  cudaStream_t stream);
+// Prefill: causal attention of the T = a.gamma prompt tokens of each sequence (a.positions: the
+// first one's position); 64 query rows (a.hpc heads x 64 / a.hpc tokens) per CTA.
+cudaError_t launch_prefill(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map, bool paged,
+                           cudaStream_t stream);
 // Tokens per stage of the INT8 decode kernel.
 inline int decode_q8_tile_tokens(int D) { return RRA_Q8_STAGE_BYTES / 2 / D; }
 // INT8 caches: attention only (a.seq_lens) or the fused step (a.positions, a.k_new, ...).

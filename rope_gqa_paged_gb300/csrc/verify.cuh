@@ -39,8 +39,9 @@ __device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uin
 // One 16-token slice of a stage for one warp. t0: the slice's first row in the stage; tok0: its
 // token index; lim0 / lim1: the last token rows lane/4 and lane/4 + 8 may attend (-1: padding).
 // CHECK: rows at or past `valid` of the stage are not tokens of this chunk; their V rows are
-// zeroed first so that no stale value reaches the tensor cores.
-template <int D, bool CHECK>
+// zeroed first so that no stale value reaches the tensor cores. SPLIT_P: P enters P.V as a
+// bf16 part plus the bf16 rounding of its remainder (for rows that attend few tokens).
+template <int D, bool CHECK, bool SPLIT_P = true>
 __device__ __forceinline__ void verify_step(VerifyState<D>& st, const uint32_t (&qa)[D / 16][4], uint32_t k_base,
                                             uint32_t v_base, uint8_t* v_gen, int t0, int tok0, int valid, int lim0,
                                             int lim1, int lane, float scale_log2) {
@@ -131,8 +132,10 @@ __device__ __forceinline__ void verify_step(VerifyState<D>& st, const uint32_t (
       ldsm_x4_trans(v_base + (j >> 2) * C::kHalfBytes + swz(r, ((j & 3) << 1) + (mat >> 1)), b);
       mma_bf16(st.o[2 * j], pa, b[0], b[1]);
       mma_bf16(st.o[2 * j + 1], pa, b[2], b[3]);
-      mma_bf16(st.o[2 * j], pl, b[0], b[1]);
-      mma_bf16(st.o[2 * j + 1], pl, b[2], b[3]);
+      if (SPLIT_P) {
+        mma_bf16(st.o[2 * j], pl, b[0], b[1]);
+        mma_bf16(st.o[2 * j + 1], pl, b[2], b[3]);
+      }
     }
   }
 }

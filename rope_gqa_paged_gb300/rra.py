@@ -61,6 +61,10 @@ _SIGNATURES = {
                                  _vp, _vp]),
     "rra_verify_num_splits": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_int]),
     "rra_verify_workspace_bytes": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "rra_prefill_attn": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _vp, _c_int, _c_int,
+                                  _c_int, _c_int, _c_int, _c_f32, _vp, _vp]),
+    "rra_prefill_step": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _vp,
+                                  _c_int, _c_int, _c_int, _c_int, _c_int, _c_f64, _c_int, _c_f32, _vp, _vp]),
 }
 
 
@@ -344,3 +348,27 @@ def rra_verify_step(q, k_new, v_new, positions, q_out, k_cache, v_cache, out, bl
                                D, float(rope_base), int(rope_style), float(scale), int(num_splits), _ptr(workspace),
                                ws_bytes, _ptr(err_flag), _stream(stream, q))
     _check("rra_verify_step", st)
+
+
+# --------------------------------------------------------------------------- prefill
+def rra_prefill_attn(q_rot, k_cache, v_cache, positions, out, block_table=None, scale: float = 0.0, err_flag=None,
+                     stream=None) -> None:
+    """out[b, t] = causal attention of prompt token t (q_rot [B, T, Hq, D]) over tokens [0, positions[b] + t]."""
+    B, T, Hq, D = q_rot.shape
+    mbps, bs, nblk, max_len, Hkv = _cache_layout(k_cache, block_table)
+    st = lib().rra_prefill_attn(_ptr(q_rot), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), mbps, _ptr(positions), bs,
+                                nblk, max_len, _ptr(out), B, T, Hq, Hkv, D, float(scale), _ptr(err_flag),
+                                _stream(stream, q_rot))
+    _check("rra_prefill_attn", st)
+
+
+def rra_prefill_step(q, k_new, v_new, positions, q_out, k_cache, v_cache, out, block_table=None,
+                     rope_base: float = 10000.0, rope_style: int = 0, scale: float = 0.0, err_flag=None,
+                     stream=None) -> None:
+    """RoPE + append of the T prompt tokens, then their causal attention."""
+    B, T, Hq, D = q.shape
+    mbps, bs, nblk, max_len, Hkv = _cache_layout(k_cache, block_table)
+    st = lib().rra_prefill_step(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q_out), _ptr(k_cache),
+                                _ptr(v_cache), _ptr(block_table), mbps, bs, nblk, max_len, _ptr(out), B, T, Hq, Hkv, D,
+                                float(rope_base), int(rope_style), float(scale), _ptr(err_flag), _stream(stream, q))
+    _check("rra_prefill_step", st)

@@ -211,3 +211,32 @@ class VerifyStep(DecodeStep):
             return self.fused(q, k_new, v_new, positions, stream)
         self.rope_append(q, k_new, v_new, positions, stream)
         return self.attend(positions, stream)
+
+
+class PrefillStep(VerifyStep):
+    """Prefill of T prompt tokens per sequence (positions[b]: the first one's position, 0 for a
+    fresh prompt): RoPE + append, then causal attention. No split-K workspace."""
+
+    def __init__(self, batch: int, prompt_len: int, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                 k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: Optional[torch.Tensor] = None,
+                 rope_base: float = 10000.0, rope_style: int = 0, scale: float = 0.0):
+        self.B, self.gamma, self.Hq, self.Hkv, self.D = batch, prompt_len, n_q_heads, n_kv_heads, head_dim
+        self.k_cache, self.v_cache, self.block_table = k_cache, v_cache, block_table
+        self.rope_base, self.rope_style, self.scale = rope_base, rope_style, scale
+        self.dtype, dev = k_cache.dtype, k_cache.device
+        self.splits = self.num_splits = 1
+        self.workspace = None
+        self.q_rot = torch.empty(batch, prompt_len, n_q_heads, head_dim, dtype=self.dtype, device=dev)
+        self.out = torch.empty(batch, prompt_len, n_q_heads, head_dim, dtype=self.dtype, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.graph = None
+
+    def attend(self, positions, stream=None) -> torch.Tensor:
+        rra.rra_prefill_attn(self.q_rot, self.k_cache, self.v_cache, positions, self.out, self.block_table, self.scale,
+                             self.err, stream)
+        return self.out
+
+    def fused(self, q, k_new, v_new, positions, stream=None) -> torch.Tensor:
+        rra.rra_prefill_step(q, k_new, v_new, positions, self.q_rot, self.k_cache, self.v_cache, self.out,
+                             self.block_table, self.rope_base, self.rope_style, self.scale, self.err, stream)
+        return self.out

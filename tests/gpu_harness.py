@@ -16,8 +16,9 @@ import oracle
 from oracle import decode as odecode
 from workloads import DecodeInputs
 
-# Tolerances on the attention output (max abs error against the float64 oracle,
-# computed on the same stored inputs): 1e-4 for fp32 storage, 1e-2 for bf16 storage.
+# Tolerances on the attention output (max abs error against the float64 oracle, computed on
+# the same stored inputs, beyond half an ulp of the output's storage type -- see out_error):
+# 1e-4 for fp32 storage, 1e-2 for bf16 storage.
 OUT_ATOL = {"f32": 1e-4, "bf16": 1e-2}
 
 
@@ -130,10 +131,25 @@ def assert_close_stored(got: np.ndarray, want: np.ndarray, dtype: str, what: str
         assert np.all(np.abs(g - w) <= tol), f"{what}: max diff {np.abs(g - w).max()}"
 
 
+def half_ulp(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Half a unit in the last place of the storage type at |x| (the rounding every stored
+    output carries): bf16 keeps 8 significant bits, fp32 24."""
+    bits = 8 if dtype == "bf16" else 24
+    ax = np.abs(np.asarray(x, dtype=np.float64))
+    _, e = np.frexp(ax)
+    e = np.where(ax > 0, np.maximum(e, -125), -125)   # below the normal range the grid stops shrinking
+    return np.ldexp(0.5, e - bits)
+
+
 def out_error(got_stored: np.ndarray, want_f64: np.ndarray, dtype: str) -> float:
+    """Attention-output error beyond the output's own storage rounding: max over elements of
+    |stored - float64 result| - half an ulp of the storage type at the result. The tolerance
+    (1e-2 bf16, 1e-4 fp32) bounds the computation; a value stored in bf16 cannot be closer than
+    half an ulp to an arbitrary real (0.0156 for outputs of magnitude 4..8)."""
     g = stored_to_f64(got_stored, dtype)
     assert np.all(np.isfinite(g)), "non-finite attention output"
-    return float(np.abs(g - want_f64).max())
+    want = np.asarray(want_f64, dtype=np.float64)
+    return float((np.abs(g - want) - half_ulp(np.maximum(np.abs(want), np.abs(g)), dtype)).max())
 
 
 # ---------------------------------------------------------------------------- INT8 cache
@@ -215,3 +231,22 @@ def run_oracle_verify(inp: DecodeInputs, rope_style: int = 0):
     bs = cfg.block_size if inp.block_table is not None else 0
     return oracle.verify.verify_step(inp.q, inp.k_new, inp.v_new, inp.positions, inp.k_cache, inp.v_cache, cfg.dtype,
                                      inp.block_table, bs, rope_base=cfg.rope_base, rope_style=rope_style)
+
+
+def run_gpu_prefill(inp: DecodeInputs, rope_style: int = 0, device="cuda:0", fused: bool = True) -> GpuResult:
+    """One prefill step (T = gamma prompt tokens per sequence) through the C ABI."""
+    from rope_gqa_paged_gb300 import PrefillStep
+
+    cfg = inp.cfg
+    kc, vc = to_torch(inp.k_cache, "bf16", device), to_torch(inp.v_cache, "bf16", device)
+    table = to_torch(inp.block_table, "i32", device) if inp.block_table is not None else None
+    step = PrefillStep(cfg.batch, inp.q.shape[1], cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, kc, vc, table,
+                       rope_base=cfg.rope_base, rope_style=rope_style)
+    args = (to_torch(inp.q, "bf16", device), to_torch(inp.k_new, "bf16", device), to_torch(inp.v_new, "bf16", device),
+            to_torch(inp.positions, "i32", device))
+    out = step(*args) if fused else step(*args, seq_lens=True)
+    torch.cuda.synchronize(device)
+    res = GpuResult(q_rot=to_numpy(step.q_rot), out=to_numpy(out), k_cache=to_numpy(kc), v_cache=to_numpy(vc),
+                    err=step.error_bits(), splits=1)
+    del kc, vc, step
+    return res

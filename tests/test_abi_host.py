@@ -165,3 +165,20 @@ def test_verify_planning(rra):
     # 16 partial rows per (sequence, KV head, head slice): MQA with gamma 4 takes 8 slices of 4 heads
     assert rra.rra_verify_workspace_bytes(2, 4, 32, 1, 128, 4) == rra.rra_verify_workspace_bytes(1, 4, 32, 8, 128, 4) * 2
     assert rra.rra_verify_workspace_bytes(2, 4, 32, 8, 128, 1) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-only argument checks; never given fake pointers on a GPU")
+def test_prefill_and_verify_argument_checks(rra):
+    lib = rra.lib()
+    P = 4096
+    a = lib.rra_prefill_attn
+    # (q, kc, vc, table, mbps, pos, bs, nblk, max_len, out, B, T, Hq, Hkv, D, scale, err, stream)
+    assert a(P, P, P, P, 64, P, 16, 100, 0, P, 0, 8, 32, 8, 128, 0.0, None, None) == RRA_OK        # empty batch
+    assert a(P, P, P, P, 64, P, 16, 100, 0, P, 1, 0, 32, 8, 128, 0.0, None, None) == RRA_EINVAL    # no prompt
+    assert a(P, P, P, P, 64, P, 4, 100, 0, P, 1, 8, 32, 8, 128, 0.0, None, None) == RRA_EUNSUPPORTED  # block < 8
+    assert a(P, P, P, None, 0, P, 0, 0, 32, P, 1, 8, 32, 8, 128, 0.0, None, None) == RRA_EUNSUPPORTED  # short cache
+    assert a(P + 8, P, P, P, 64, P, 16, 100, 0, P, 1, 8, 32, 8, 128, 0.0, None, None) == RRA_EINVAL  # misaligned
+    v = lib.rra_verify_attn
+    # (q, kc, vc, table, mbps, pos, bs, nblk, max_len, out, B, gamma, Hq, Hkv, D, scale, splits, ws, ws_bytes, err, st)
+    assert v(P, P, P, P, 64, P, 16, 100, 0, P, 1, 4, 32, 8, 128, 0.0, 8, None, 0, None, None) == RRA_EWORKSPACE
+    assert v(P, P, P, P, 64, P, 16, 100, 0, P, 1, 20, 32, 8, 128, 0.0, 0, None, 0, None, None) == RRA_EUNSUPPORTED

@@ -132,6 +132,17 @@ CONFIGS["long_context_verify4"] = dataclasses.replace(
     CONFIGS["long_context"], name="long_context_verify4", gamma=4, num_splits=0,
     description="speculative verify, 4 new tokens: batch 1, 32q/8kv, D 128, context 131072, block 32")
 
+# Prefill ([Opt-2026] §三, FlashAttention and its 128K figure): the whole prompt as new tokens at
+# positions 0 .. T-1, causal attention; gamma = T.
+CONFIGS["prefill_8k"] = _paged(
+    "prefill_8k", batch=1, n_q_heads=32, n_kv_heads=8, head_dim=128, dtype="bf16", seq_len=8192, gamma=8192,
+    block_size=32, num_blocks=256, max_blocks_per_seq=256,
+    description="prefill of an 8K prompt: batch 1, 32q/8kv, D 128, causal, paged block 32")
+CONFIGS["prefill_128k"] = _paged(
+    "prefill_128k", batch=1, n_q_heads=32, n_kv_heads=8, head_dim=128, dtype="bf16", seq_len=131072, gamma=131072,
+    block_size=32, num_blocks=4096, max_blocks_per_seq=4096,
+    description="prefill of a 128K prompt: batch 1, 32q/8kv, D 128, causal, paged block 32")
+
 
 def get_config(name: str) -> WorkloadConfig:
     return CONFIGS[name]
@@ -170,4 +181,6 @@ def reduced(cfg: WorkloadConfig, factor: int = 16, batch: Optional[int] = None) 
         kw["num_splits"] = max(2, cfg.num_splits // factor)
     if cfg.window:
         kw["window"] = max(16, (cfg.window // factor) // 8 * 8)
+    if cfg.gamma > 16:                     # a prefill: the prompt is the whole sequence
+        kw["gamma"] = kw["seq_len"]
     return WorkloadConfig(**kw)
