@@ -465,6 +465,70 @@ def pin_verify_equals_causal_rows():
     assert np.allclose(out[0], ref[p0:], rtol=0, atol=1e-12), np.abs(out[0] - ref[p0:]).max()
 
 
+def pin_int4_codes_and_packing():
+    # exact codes at scale 0.5 (ties to even, clamp at +-7), and the nibble layout of the pages'
+    # "two codes per byte" reading: even dim low nibble, odd dim high nibble, two's complement
+    cases = [(0.0, 0), (1.25, 2), (1.75, 4), (-1.25, -2), (3.25, 6), (3.75, 7), (100.0, 7), (-100.0, -7)]
+    got = oracle.quant.quantize_int4(np.array([c[0] for c in cases]), 0.5)
+    assert got.tolist() == [c[1] for c in cases], got
+    codes = np.array([[1, -1, 7, -7, 0, -8, 3, 2]], dtype=np.int8)
+    packed = oracle.quant.pack_int4(codes)
+    assert packed.tolist() == [[0xF1, 0x97, 0x80, 0x23]], [hex(x) for x in packed[0]]
+    assert np.array_equal(oracle.quant.unpack_int4(packed), codes)
+    rng = np.random.default_rng(23)
+    c = rng.integers(-8, 8, size=(5, 64)).astype(np.int8)
+    assert np.array_equal(oracle.quant.unpack_int4(oracle.quant.pack_int4(c)), c)
+
+
+def pin_int4_stream_matches_mixed_precision():
+    # the token-by-token stream with 4-bit codes: stored bytes unpack to quantize_int4 of the exact values
+    for window in (0, 3):
+        for layout in ("contiguous", "paged"):
+            rng = np.random.default_rng(40 + window)
+            T, hq, hkv, d, bs = 9, 4, 2, 8, 4
+            qs = oracle.f64_to_bf16_bits(rng.standard_normal((T, hq, d)))
+            ks = oracle.f64_to_bf16_bits(rng.standard_normal((T, hkv, d)))
+            vs = oracle.f64_to_bf16_bits(rng.standard_normal((T, hkv, d)))
+            k_scale = np.array([0.5, 0.75], dtype=np.float32)
+            v_scale = np.array([0.6, 0.4], dtype=np.float32)
+            if layout == "contiguous":
+                kc = np.full((1, hkv, T + 2, d // 2), 0x88, dtype=np.uint8)
+                table = None
+            else:
+                kc = np.full((2 * math.ceil(T / bs), bs, hkv, d // 2), 0x88, dtype=np.uint8)
+                table = rng.permutation(kc.shape[0])[: math.ceil(T / bs)][None, :].astype(np.int32)
+            vc = kc.copy()
+            kw = np.full((1, hkv, max(window, 1), d), np.uint16(0x7FC0), dtype=np.uint16)
+            vw = kw.copy()
+            k_exact = [oracle.f64_to_bf16_bits(oracle.apply_rope(oracle.bf16_bits_to_f64(ks[t]), np.array([[t]])))
+                       for t in range(T)]
+            for p in range(T):
+                q_rot = oracle.quant.rope_append_q8(qs[p][None], ks[p][None], vs[p][None], np.array([p]), kc, vc,
+                                                    k_scale, v_scale, kw, vw, window, table, bs, bits=4)
+                out = oracle.quant.decode_attention_q8(q_rot, kc, vc, k_scale, v_scale, kw, vw, np.array([p + 1]),
+                                                       window, table, bs, bits=4)
+                L = p + 1
+                qr = oracle.bf16_bits_to_f64(q_rot[0])
+                for h in range(hq):
+                    g = h // (hq // hkv)
+                    keys, vals = [], []
+                    for t in range(L):
+                        kx = oracle.bf16_bits_to_f64(k_exact[t][g])
+                        vx = oracle.bf16_bits_to_f64(vs[t, g])
+                        if window == 0 or t < L - window:
+                            kx = oracle.quant.quantize_int4(kx, k_scale[g]).astype(np.float64) * float(k_scale[g])
+                            vx = oracle.quant.quantize_int4(vx, v_scale[g]).astype(np.float64) * float(v_scale[g])
+                        keys.append(list(kx))
+                        vals.append(list(vx))
+                    want = _loop_attention(list(qr[h]), keys, vals, 1 / math.sqrt(d))
+                    assert np.allclose(out[0, h], want, rtol=0, atol=1e-12), (window, layout, p, h)
+            for t in range(T):
+                row = kc[0, :, t] if table is None else kc[table[0, t // bs], t % bs]
+                want = np.stack([oracle.quant.quantize_int4(oracle.bf16_bits_to_f64(k_exact[t][g]), k_scale[g])
+                                 for g in range(hkv)])
+                assert np.array_equal(oracle.quant.unpack_int4(row), want), (layout, t)
+
+
 ALL_PINS = [
     pin_bf16_exact_values, pin_bf16_matches_torch_cast,
     pin_rope_complex_rotation, pin_rope_relative_position, pin_rope_rotation_properties,
@@ -475,6 +539,7 @@ ALL_PINS = [
     pin_int8_quantize_exact_values, pin_int8_round_trip_bound, pin_q8_full_window_is_the_bf16_step,
     pin_q8_without_window_reads_code_times_scale, pin_q8_stream_matches_mixed_precision,
     pin_verify_equals_sequential_decode, pin_verify_equals_causal_rows,
+    pin_int4_codes_and_packing, pin_int4_stream_matches_mixed_precision,
 ]
 
 

@@ -81,33 +81,49 @@ def _logical_kv_contiguous_short(cache, b, length):
     return cache[b, :, : max(length - 1, 1), :]
 
 
-def _q8_half_away_from_zero(x, scale):
+def _q8_half_away_from_zero(x, scale, bits=8):
     r = np.asarray(x, dtype=np.float32) / np.asarray(scale, dtype=np.float32)
-    return np.clip(np.sign(r) * np.floor(np.abs(r) + 0.5), -127, 127).astype(np.int8)
+    m = (1 << (bits - 1)) - 1
+    return np.clip(np.sign(r) * np.floor(np.abs(r) + 0.5), -m, m).astype(np.int8)
 
 
-def _q8_range_to_minus_128(x, scale):
+def _q8_range_to_minus_128(x, scale, bits=8):
     r = np.asarray(x, dtype=np.float32) / np.asarray(scale, dtype=np.float32)
-    return np.clip(np.rint(r), -128, 127).astype(np.int8)
+    m = (1 << (bits - 1)) - 1
+    return np.clip(np.rint(r), -m - 1, m).astype(np.int8)
 
 
-def _q8_quotient_in_float64(x, scale):
+def _q8_quotient_in_float64(x, scale, bits=8):
     r = np.asarray(x, dtype=np.float64) / np.asarray(scale, dtype=np.float32).astype(np.float64)
-    return np.clip(np.rint(r), -127, 127).astype(np.int8)
+    m = (1 << (bits - 1)) - 1
+    return np.clip(np.rint(r), -m, m).astype(np.int8)
 
 
-def _q8_ring_slot_shifted(codes, scale, win, b, length, window, block_table=None, block_size=0):
+def _q8_ring_slot_shifted(codes, scale, win, b, length, window, block_table=None, block_size=0, bits=8):
     n_old = max(0, length - window) if window > 0 else length
-    out = _ORIG_Q["logical_kv_q8"](codes, scale, win, b, n_old, 0, block_table, block_size)
+    out = _ORIG_Q["logical_kv_q8"](codes, scale, win, b, n_old, 0, block_table, block_size, bits)
     if n_old == length:
         return out
     recent = np.stack([oracle.bf16_bits_to_f64(win[b, :, (t + 1) % window, :]) for t in range(n_old, length)], axis=1)
     return np.concatenate([out, recent], axis=1)
 
 
-def _q8_window_one_short(codes, scale, win, b, length, window, block_table=None, block_size=0):
+def _q8_window_one_short(codes, scale, win, b, length, window, block_table=None, block_size=0, bits=8):
     w = max(window - 1, 0) if window > 1 else window
-    return _ORIG_Q["logical_kv_q8"](codes, scale, win, b, length, w, block_table, block_size)
+    return _ORIG_Q["logical_kv_q8"](codes, scale, win, b, length, w, block_table, block_size, bits)
+
+
+def _q4_nibbles_swapped(codes):
+    c = np.asarray(codes, dtype=np.int8).astype(np.uint8) & np.uint8(0x0F)
+    return (c[..., 1::2] | (c[..., 0::2] << np.uint8(4))).astype(np.uint8)
+
+
+def _q4_unpack_unsigned(packed):
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.int8)
+    out[..., 0::2] = (p & np.uint8(0x0F)).astype(np.int8)
+    out[..., 1::2] = (p >> np.uint8(4)).astype(np.int8)
+    return out
 
 
 def _q8_dequantize_without_scale(codes, scale):
@@ -163,9 +179,11 @@ MUTATIONS = {
     "kv bytes without the K+V factor 2": ("kv_cache_bytes", _kv_bytes_no_factor_two),
     "bf16 rounded through fp32": ("f64_to_bf16_bits", _bf16_double_rounding),
     "attention drops the newest token": ("logical_kv_contiguous", _logical_kv_contiguous_short),
-    "int8 rounds half away from zero": ("quantize_int8", _q8_half_away_from_zero),
-    "int8 codes reach -128": ("quantize_int8", _q8_range_to_minus_128),
-    "int8 quotient taken in float64": ("quantize_int8", _q8_quotient_in_float64),
+    "int8 rounds half away from zero": ("quantize", _q8_half_away_from_zero),
+    "int8 codes reach -128": ("quantize", _q8_range_to_minus_128),
+    "int8 quotient taken in float64": ("quantize", _q8_quotient_in_float64),
+    "int4 nibbles packed in the wrong order": ("pack_int4", _q4_nibbles_swapped),
+    "int4 nibbles read as unsigned": ("unpack_int4", _q4_unpack_unsigned),
     "window ring read one slot off": ("logical_kv_q8", _q8_ring_slot_shifted),
     "window one token short": ("logical_kv_q8", _q8_window_one_short),
     "dequantisation drops the scale": ("dequantize_int8", _q8_dequantize_without_scale),

@@ -11,6 +11,8 @@ from workloads import CONFIGS, make_inputs, reduced
 def _finite(x, dtype):
     if x.dtype == np.int8:                                   # INT8 codes: -128 is the poison
         return x != -128
+    if x.dtype == np.uint8:                                  # packed INT4 codes: 0x88 (two -8 codes)
+        return x != 0x88
     if dtype == "bf16":
         return (x & 0x7F80) != 0x7F80
     return np.isfinite(x)

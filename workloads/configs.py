@@ -29,7 +29,7 @@ class WorkloadConfig:
     max_blocks_per_seq: int = 0     # paged: columns of the block table
     shared_prefix_tokens: int = 0   # paged: leading tokens of every sequence mapped to the same blocks
     num_splits: int = 0             # split-K chunks per sequence; 0 lets the library choose
-    kv_dtype: str = ""              # "" = the caches hold ``dtype``; "int8" = INT8 codes + per-head scales
+    kv_dtype: str = ""              # "" = the caches hold ``dtype``; "int8" / "int4" = codes + per-head scales
     window: int = 0                 # int8 only: recent tokens also kept in a bf16 ring of this many slots
     gamma: int = 1                  # new tokens per sequence (> 1: a speculative-verify step)
     rope_base: float = 10000.0
@@ -53,7 +53,12 @@ class WorkloadConfig:
 
     @property
     def int8(self) -> bool:
-        return self.kv_dtype == "int8"
+        """A quantised cache (INT8 or INT4 codes with per-head scales)."""
+        return self.kv_dtype in ("int8", "int4")
+
+    @property
+    def code_bits(self) -> int:
+        return 4 if self.kv_dtype == "int4" else 8
 
     def kv_bytes(self, lengths) -> int:
         """Algorithmic K+V bytes one decode step streams: 2 * sum_b L_b * Hkv * D * elem.
@@ -66,7 +71,7 @@ class WorkloadConfig:
             total = 0
             for x in lengths:
                 recent = min(int(x), self.window)
-                total += (int(x) - recent) * row + recent * row * 2
+                total += (int(x) - recent) * row * self.code_bits // 8 + recent * row * 2
             return total
         return int(sum(int(x) for x in lengths)) * row * self.elem_bytes
 
@@ -117,9 +122,17 @@ CONFIGS["batched_paged_int8"] = dataclasses.replace(
     CONFIGS["batched_paged"], name="batched_paged_int8", kv_dtype="int8", window=128,
     description="batched paged decode, INT8 KV cache (per-head scales) + 128-token bf16 window: batch 64, "
                 "32q/8kv, D 128, L_b ~ U[512,8192], block 16, pool 40000")
+CONFIGS["batched_paged_int4"] = dataclasses.replace(
+    CONFIGS["batched_paged_int8"], name="batched_paged_int4", kv_dtype="int4",
+    description="batched paged decode, INT4 KV cache (per-head scales) + 128-token bf16 window: batch 64, "
+                "32q/8kv, D 128, L_b ~ U[512,8192], block 16, pool 40000")
 CONFIGS["long_context_int8"] = dataclasses.replace(
     CONFIGS["long_context"], name="long_context_int8", kv_dtype="int8", window=128, num_splits=0,
     description="long-context decode, INT8 KV cache (per-head scales) + 128-token bf16 window: batch 1, "
+                "32q/8kv, D 128, context 131072, block 32")
+CONFIGS["long_context_int4"] = dataclasses.replace(
+    CONFIGS["long_context_int8"], name="long_context_int4", kv_dtype="int4",
+    description="long-context decode, INT4 KV cache (per-head scales) + 128-token bf16 window: batch 1, "
                 "32q/8kv, D 128, context 131072, block 32")
 
 # The speculative-verify step ([Opt-2026] §五, gamma = 4): the batch-64 paged and 128K workloads

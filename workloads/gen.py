@@ -26,6 +26,11 @@ Speculative verify (``gamma > 1``): q, k_new, v_new are drawn as [B, gamma, H, D
 tokens of sequence b sit at positions L_b - gamma .. L_b - 1 (``positions`` holds the first),
 and every slot from L_b - gamma on is poisoned.
 
+INT4 caches (``kv_dtype == "int4"``): as INT8 with codes ``clip(rint(1.75 * N(0,1)), -7, 7)``
+packed two per byte (even dimension in the low nibble), scales (1 + (h mod 4)/8)/1.75 and
+(1 + ((h+2) mod 4)/8)/1.75, and the poison byte 0x88 (two -8 codes, which quantisation never
+produces).
+
 INT8 caches (``kv_dtype == "int8"``): steps 1-3 are unchanged; step 4 draws the K then the V
 cache as integer codes ``clip(rint(32 * standard_normal(float32)), -127, 127)`` (N(0,1)
 values at a resolution of 1/32), then, with a window of W slots, the K then the V ring
@@ -86,6 +91,8 @@ class DecodeInputs:
 
     @property
     def nan_value(self):
+        if self.cfg.kv_dtype == "int4":
+            return np.uint8(0x88)
         if self.cfg.int8:
             return np.int8(-128)
         return BF16_NAN if self.cfg.dtype == "bf16" else np.float32(np.nan)
@@ -137,11 +144,12 @@ def make_inputs(cfg: WorkloadConfig, seed: Optional[int] = None, poison: bool = 
         shape = (cfg.num_blocks, cfg.block_size, Hkv, D)
     extra = {}
     if cfg.int8:
-        k_cache = _int8_codes(rng, shape)
-        v_cache = _int8_codes(rng, shape)
+        per_unit = 32.0 if cfg.code_bits == 8 else 1.75      # codes per unit of N(0,1)
+        k_cache = _codes(rng, shape, cfg.code_bits, per_unit)
+        v_cache = _codes(rng, shape, cfg.code_bits, per_unit)
         h = np.arange(Hkv)
-        extra["k_scale"] = ((1.0 + (h % 4) / 8.0) / 32.0).astype(np.float32)
-        extra["v_scale"] = ((1.0 + ((h + 2) % 4) / 8.0) / 32.0).astype(np.float32)
+        extra["k_scale"] = ((1.0 + (h % 4) / 8.0) / per_unit).astype(np.float32)
+        extra["v_scale"] = ((1.0 + ((h + 2) % 4) / 8.0) / per_unit).astype(np.float32)
         if cfg.window:
             extra["k_win"] = _normal_storage(rng, (B, Hkv, cfg.window, D), "bf16")
             extra["v_win"] = _normal_storage(rng, (B, Hkv, cfg.window, D), "bf16")
@@ -156,14 +164,21 @@ def make_inputs(cfg: WorkloadConfig, seed: Optional[int] = None, poison: bool = 
     return inp
 
 
-def _int8_codes(rng: np.random.Generator, shape) -> np.ndarray:
+def _codes(rng: np.random.Generator, shape, bits: int, per_unit: float) -> np.ndarray:
+    """Integer codes clip(rint(per_unit * N(0,1)), -(2^(bits-1) - 1), ...): int8, or for 4 bits
+    packed two per byte (even index in the low nibble) along the last axis."""
+    m = (1 << (bits - 1)) - 1
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.int8)
     for s in range(0, n, _CHUNK):
         e = min(n, s + _CHUNK)
         x = rng.standard_normal(e - s, dtype=np.float32)
-        out[s:e] = np.clip(np.rint(x * 32.0), -127, 127)
-    return out.reshape(shape)
+        out[s:e] = np.clip(np.rint(x * per_unit), -m, m)
+    out = out.reshape(shape)
+    if bits == 8:
+        return out
+    u = out.astype(np.uint8) & np.uint8(0x0F)
+    return (u[..., 0::2] | (u[..., 1::2] << np.uint8(4))).astype(np.uint8)
 
 
 def make_structure(cfg: WorkloadConfig, seed: Optional[int] = None):
