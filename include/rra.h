@@ -228,6 +228,34 @@ RRA_API int rra_decode_step_q8(const void* q, const void* k_new, const void* v_n
 RRA_API int rra_decode_q8_num_splits(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
                                      int num_splits, int window);
 
+/* INT4 codes ([KVC-GQA-RoPE] §4.3: INT8 or INT4): the same four calls with 4-bit codes
+ * clamp(round_half_even(x / s_g), -7, 7) (float32 quotient; -8 never written), two per byte:
+ * dims 2j and 2j+1 in byte j, the even one in the low nibble, as 4-bit two's complement. The
+ * code caches hold D / 2 bytes per token and head ([B, Hkv, max_len, D/2] or pools
+ * [num_blocks, block_size, Hkv, D/2]); head_dim 128 only; rra_rope_append_q4 takes at most 32
+ * KV heads. Contiguous caches need at least 128 tokens. Everything else as for INT8. */
+RRA_API int rra_rope_append_q4(const void* q, const void* k_new, const void* v_new, const int32_t* positions,
+                               void* q_out, void* k_codes, void* v_codes, const float* k_scale,
+                               const float* v_scale, void* k_win, void* v_win, int window,
+                               const int32_t* block_table, int max_blocks_per_seq, int block_size,
+                               int num_blocks, int max_len, int B, int Hq, int Hkv, int D, double rope_base,
+                               int rope_style, int32_t* err_flag, void* stream);
+RRA_API int rra_decode_attn_q4(const void* q_rot, const void* k_codes, const void* v_codes, const float* k_scale,
+                               const float* v_scale, const void* k_win, const void* v_win, int window,
+                               const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens,
+                               int block_size, int num_blocks, int max_len, void* out, int B, int Hq, int Hkv,
+                               int D, float scale, int num_splits, void* workspace, size_t ws_bytes,
+                               int32_t* err_flag, void* stream);
+RRA_API int rra_decode_step_q4(const void* q, const void* k_new, const void* v_new, const int32_t* positions,
+                               void* q_out, void* k_codes, void* v_codes, const float* k_scale,
+                               const float* v_scale, void* k_win, void* v_win, int window,
+                               const int32_t* block_table, int max_blocks_per_seq, int block_size,
+                               int num_blocks, int max_len, void* out, int B, int Hq, int Hkv, int D,
+                               double rope_base, int rope_style, float scale, int num_splits, void* workspace,
+                               size_t ws_bytes, int32_t* err_flag, void* stream);
+RRA_API int rra_decode_q4_num_splits(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
+                                     int num_splits, int window);
+
 /* --- Multi-query decode: the speculative-verify step ---
  *
  * [Opt-2026] §五: the target model checks gamma draft tokens (gamma = 4 on the page) in one pass.

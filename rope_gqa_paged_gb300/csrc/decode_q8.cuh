@@ -42,11 +42,12 @@
 
 namespace rra {
 
-template <int D>
+template <int D, int BITS = 8>
 struct Q8Cfg {
+  static constexpr int kRowBytes = D * BITS / 8;         // codes of one token and head
   static constexpr int kStageBytes = RRA_Q8_STAGE_BYTES;
   static constexpr int kTileBytes = kStageBytes / 2;     // K or V codes of one stage
-  static constexpr int kTile = kTileBytes / D;           // INT8 tokens per stage
+  static constexpr int kTile = kTileBytes / kRowBytes;   // tokens per stage
   static constexpr int kStages = RRA_Q8_STAGES;
   static constexpr int kConsumerWarps = 4;
   static constexpr int kThreads = (kConsumerWarps + 1) * 32;
@@ -63,15 +64,33 @@ struct Q8Cfg {
   static constexpr int kOffTable = kOffBar + (2 * kStages + 1) * 8;
   static constexpr int kOffCs = kOffTable + kMmaTableEntries * 4;
   static constexpr int kOffQ = kOffCs + 4 * (D / 2) * 4;
-  static constexpr int kSmemBytes = 1024 + kOffQ + MmaCfg<D>::kMaxHeads * D * 2;
+  static constexpr int kOffK = kOffQ + MmaCfg<D>::kMaxHeads * D * 2;  // the appended k (bf16), INT4 packing
+  static constexpr int kSmemBytes = 1024 + kOffK + D * 2;
 };
 
-// Byte offset of 16-byte chunk c of row r in a tile of D-byte rows written by TMA with the
-// 128-byte (D = 128) or 64-byte (D = 64) swizzle.
-template <int D>
+// Byte offset of 16-byte chunk c of row r in a tile of RB-byte rows written by TMA with the
+// 128-byte (RB = 128) or 64-byte (RB = 64) swizzle.
+template <int RB>
 __device__ __forceinline__ uint32_t swz8(int r, int c) {
-  if constexpr (D == 128) return swz(r, c);
+  if constexpr (RB == 128) return swz(r, c);
   return (r << 6) + ((((r >> 1) ^ c) & 3) << 4);
+}
+
+// INT4: nibbles 0 and 4 of w as an exact f16 pair: sign bit flipped, under the exponent of 1024
+// (lop3 table 0x6a, per bit b ? a^c : c), minus 1032.
+__device__ __forceinline__ uint32_t nib04_to_f16(uint32_t w) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(d) : "r"(w), "r"(0x000f000fu), "r"(0x64086408u));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(d), "r"(0x64086408u));
+  return d;
+}
+
+// INT4: nibbles 1 and 5 of w: 1024 + 16 (n ^ 8) under the same exponent, times 1/16 minus 72.
+__device__ __forceinline__ uint32_t nib15_to_f16(uint32_t w) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(d) : "r"(w), "r"(0x00f000f0u), "r"(0x64806480u));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(d), "r"(0x2c002c00u), "r"(0xd480d480u));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t f16x2_minus_1152(uint32_t x) {
@@ -110,22 +129,48 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 // One 16-token slice of an INT8 stage for one warp; `mult[j]` turns the raw score of owned
 // head 2*(lane%4)+j into log2 units. CHECK: tokens at or past `valid` get probability 0 (the
 // codes are finite whatever the bytes, so nothing needs clearing).
-template <int D, bool CHECK>
+template <int D, bool CHECK, int BITS = 8>
 __device__ __forceinline__ void q8_step(MmaWarpState<D>& st, const uint32_t (&qh)[D / 16][2], const float (&mult)[2],
                                         uint32_t k_base, uint32_t v_base, int t0, int valid, int lane) {
+  constexpr int RB = D * BITS / 8;
   const int mat = lane >> 3;
   const int r = t0 + (lane & 7) + ((mat & 1) << 3);  // matrices: tokens 0-7 / 8-15 of chunk 2cc, then 2cc+1
   float s[4] = {0.f, 0.f, 0.f, 0.f};
+  if constexpr (BITS == 4) {
+    // a 16-byte chunk c holds 32 dims: lane gets dims 32c + 8t .. +7 of rows g / g+8, nibble i = dim 8t + i;
+    // slice 2c takes dims (8t, 8t+4) as k = (2t, 2t+1) and (8t+1, 8t+5) as (2t+8, 2t+9), slice 2c+1 the rest
+#pragma unroll
+    for (int cc = 0; cc < RB / 32; ++cc) {
+      uint32_t w[4], a[4];
+      ldsm_x4(k_base + swz8<RB>(r, 2 * cc + (mat >> 1)), w);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t wa = w[2 * h], wb = w[2 * h + 1], wa8 = wa >> 8, wb8 = wb >> 8;
+        const int c = 2 * cc + h;
+        a[0] = nib04_to_f16(wa);
+        a[1] = nib04_to_f16(wb);
+        a[2] = nib15_to_f16(wa);
+        a[3] = nib15_to_f16(wb);
+        mma_f16(s, a, qh[2 * c][0], qh[2 * c][1]);
+        a[0] = nib04_to_f16(wa8);
+        a[1] = nib04_to_f16(wb8);
+        a[2] = nib15_to_f16(wa8);
+        a[3] = nib15_to_f16(wb8);
+        mma_f16(s, a, qh[2 * c + 1][0], qh[2 * c + 1][1]);
+      }
+    }
+  } else {
 #pragma unroll
   for (int cc = 0; cc < D / 32; ++cc) {
     uint32_t w[4], a[4];
-    ldsm_x4(k_base + swz8<D>(r, 2 * cc + (mat >> 1)), w);
+    ldsm_x4(k_base + swz8<RB>(r, 2 * cc + (mat >> 1)), w);
     s8x4_to_f16_even_odd(w[0], a[0], a[2]);
     s8x4_to_f16_even_odd(w[1], a[1], a[3]);
     mma_f16(s, a, qh[2 * cc][0], qh[2 * cc][1]);
     s8x4_to_f16_even_odd(w[2], a[0], a[2]);
     s8x4_to_f16_even_odd(w[3], a[1], a[3]);
     mma_f16(s, a, qh[2 * cc + 1][0], qh[2 * cc + 1][1]);
+  }
   }
   const int ta = t0 + (lane >> 2), tb = ta + 8;
   float x[2][2];
@@ -171,10 +216,35 @@ __device__ __forceinline__ void q8_step(MmaWarpState<D>& st, const uint32_t (&qh
   }
   const uint32_t b0 = movmatrix_trans(pack_f16x2(p[0][0], p[1][0]));
   const uint32_t b1 = movmatrix_trans(pack_f16x2(p[0][1], p[1][1]));
+  if constexpr (BITS == 4) {
+    // ldmatrix.trans gives lane (g, t) the 16-bit column g (dims 32c + 4g .. +3) of tokens 2t, 2t+1
+    // (and +8): fragment rows g / g+8 of sub-tile s are dims 32c + 4g + 2s / + 2s + 1
+#pragma unroll
+    for (int cc = 0; cc < RB / 32; ++cc) {
+      uint32_t w[4], a[4];
+      ldsm_x4_trans(v_base + swz8<RB>(r, 2 * cc + (mat >> 1)), w);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t ra = w[2 * h], rb = w[2 * h + 1], ra8 = ra >> 8, rb8 = rb >> 8;
+        const int c = 2 * cc + h;
+        a[0] = nib04_to_f16(ra);
+        a[1] = nib15_to_f16(ra);
+        a[2] = nib04_to_f16(rb);
+        a[3] = nib15_to_f16(rb);
+        mma_f16(st.o[2 * c], a, b0, b1);
+        a[0] = nib04_to_f16(ra8);
+        a[1] = nib15_to_f16(ra8);
+        a[2] = nib04_to_f16(rb8);
+        a[3] = nib15_to_f16(rb8);
+        mma_f16(st.o[2 * c + 1], a, b0, b1);
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int cc = 0; cc < D / 32; ++cc) {
     uint32_t w[4], a[4];
-    ldsm_x4_trans(v_base + swz8<D>(r, 2 * cc + (mat >> 1)), w);
+    ldsm_x4_trans(v_base + swz8<RB>(r, 2 * cc + (mat >> 1)), w);
     s8x4_to_f16_even_odd(w[0], a[0], a[1]);
     s8x4_to_f16_even_odd(w[1], a[2], a[3]);
     mma_f16(st.o[2 * cc], a, b0, b1);
@@ -203,12 +273,42 @@ __device__ __forceinline__ void q8_acc_to_bf16_layout(MmaWarpState<D>& st, float
   }
 }
 
-template <int D, bool PAGED, bool FUSED>
-__global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
+// The INT4 version: fragment rows g / g+8 of sub-tile s of chunk c are dims 32c + 4g + 2s / + 1.
+template <int D>
+__device__ __forceinline__ void q4_acc_to_bf16_layout(MmaWarpState<D>& st, float vs, int lane) {
+  const int dl = lane >> 2, t = lane & 3;
+  const int s_sel = (dl >> 1) & 1, e_sel = dl & 1;  // sub-tile and row half of dims dl, dl + 8 in a chunk
+  float res[D / 16][4];
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) {
+    const int c = i >> 1;
+#pragma unroll
+    for (int f = 0; f < 2; ++f) {
+      const int rem = 16 * (i & 1) + dl + 8 * f;   // dim within chunk c
+      const int src = ((rem >> 2) << 2) | t;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float v00 = __shfl_sync(0xffffffffu, st.o[2 * c][j], src);
+        const float v01 = __shfl_sync(0xffffffffu, st.o[2 * c][2 + j], src);
+        const float v10 = __shfl_sync(0xffffffffu, st.o[2 * c + 1][j], src);
+        const float v11 = __shfl_sync(0xffffffffu, st.o[2 * c + 1][2 + j], src);
+        const float v = s_sel ? (e_sel ? v11 : v10) : (e_sel ? v01 : v00);
+        res[i][2 * f + j] = v * vs;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) st.o[i][k] = res[i][k];
+}
+
+template <int D, int BITS, bool PAGED, bool FUSED>
+__global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_MMA_CTAS_PER_SM)
     decode_q8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                      const __grid_constant__ CUtensorMap kw_map, const __grid_constant__ CUtensorMap vw_map,
                      const DecodeArgs a) {
-  using C = Q8Cfg<D>;
+  using C = Q8Cfg<D, BITS>;
   using M = MmaCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -364,12 +464,12 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
             if (bs <= C::kTile) {  // whole blocks, one box of bs rows per block
               const int n = min(C::kTile, end - t0);
               const int nblk = (n + bs - 1) >> a.log2_bs;
-              mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * nblk * bs * D));
+              mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * nblk * bs * C::kRowBytes));
               const int j0 = (t0 >> a.log2_bs) - first_blk;
               for (int jb = 0; jb < nblk; ++jb) {
                 const int phys = tbl[j0 + jb];
-                tma_g2s_4d(kst + jb * bs * D, &k_map, 0, g, 0, phys, &full[s]);
-                tma_g2s_4d(vst + jb * bs * D, &v_map, 0, g, 0, phys, &full[s]);
+                tma_g2s_4d(kst + jb * bs * C::kRowBytes, &k_map, 0, g, 0, phys, &full[s]);
+                tma_g2s_4d(vst + jb * bs * C::kRowBytes, &v_map, 0, g, 0, phys, &full[s]);
               }
             } else {  // a kTile-row window of one block
               const int phys = tbl[(t0 >> a.log2_bs) - first_blk];
@@ -459,24 +559,41 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
       __nv_bfloat16* vw = static_cast<__nv_bfloat16*>(a.v_win) + wrow;
       const float ks = a.k_scale[g], vs = a.v_scale[g];
       const bool inter = a.rope_style == 1;
+      __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(smem + C::kOffK);  // rotated k (INT4 packing)
       for (int i = lane; i < D / 2; i += 32) {
         const int ia = inter ? 2 * i : i, ib = inter ? 2 * i + 1 : i + D / 2;
         const float xa = __bfloat162float(kn[ia]), xb = __bfloat162float(kn[ib]);
         const float ch = cs[i], cl = cs[D / 2 + i], sh = cs[D + i], sl = cs[3 * (D / 2) + i];
         const __nv_bfloat16 ra = __float2bfloat16_rn(rotate_diff(xa, xb, ch, cl, sh, sl));
         const __nv_bfloat16 rb = __float2bfloat16_rn(rotate_diff(xb, -xa, ch, cl, sh, sl));
-        if (ok) {
-          kc[ia] = quantize_code(__bfloat162float(ra), ks);
-          kc[ib] = quantize_code(__bfloat162float(rb), ks);
+        if constexpr (BITS == 8) {
+          if (ok) {
+            kc[ia] = quantize_code(__bfloat162float(ra), ks);
+            kc[ib] = quantize_code(__bfloat162float(rb), ks);
+          }
+        } else {
+          kr[ia] = ra;
+          kr[ib] = rb;
         }
         if (has_win) {
           kw[ia] = ra;
           kw[ib] = rb;
         }
       }
+      if constexpr (BITS == 4) {  // codes of dims 2j, 2j+1 in byte j: the even one in the low nibble
+        __syncwarp();
+        uint8_t* kc4 = reinterpret_cast<uint8_t*>(const_cast<void*>(a.k)) + row * (D / 2);
+        uint8_t* vc4 = reinterpret_cast<uint8_t*>(const_cast<void*>(a.v)) + row * (D / 2);
+        for (int j = lane; j < D / 2 && ok; j += 32) {
+          kc4[j] = pack_nibbles(quantize_code4(__bfloat162float(kr[2 * j]), ks),
+                                quantize_code4(__bfloat162float(kr[2 * j + 1]), ks));
+          vc4[j] = pack_nibbles(quantize_code4(__bfloat162float(vn[2 * j]), vs),
+                                quantize_code4(__bfloat162float(vn[2 * j + 1]), vs));
+        }
+      }
       for (int i = lane; i < D; i += 32) {
         const __nv_bfloat16 x = vn[i];
-        if (ok) vc[i] = quantize_code(__bfloat162float(x), vs);
+        if (BITS == 8 && ok) vc[i] = quantize_code(__bfloat162float(x), vs);
         if (has_win) vw[i] = x;
       }
       asm volatile("fence.proxy.async.global;" ::: "memory");  // visible to the TMA that reads the slot
@@ -501,11 +618,13 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     {
       float xq[D / 16][4];
       float amax = 0.f;
-      const __nv_bfloat16* qr = q_rows + hd * D + 4 * (lane & 3);
+      // INT8: row c = dims 16c + 4t .. +3; INT4: rows 2c', 2c'+1 = dims 32c' + 8t .. +3, + 4 .. +7
+      const __nv_bfloat16* qr = q_rows + hd * D + (BITS == 8 ? 4 : 8) * (lane & 3);
 #pragma unroll
       for (int c = 0; c < D / 16; ++c) {
         uint2 w = make_uint2(0u, 0u);
-        if (hd < hpc) w = *reinterpret_cast<const uint2*>(qr + 16 * c);
+        const int off = BITS == 8 ? 16 * c : 32 * (c >> 1) + 4 * (c & 1);
+        if (hd < hpc) w = *reinterpret_cast<const uint2*>(qr + off);
         xq[c][0] = __uint_as_float(w.x << 16);
         xq[c][1] = __uint_as_float(w.x & 0xffff0000u);
         xq[c][2] = __uint_as_float(w.y << 16);
@@ -521,8 +640,17 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
       down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
 #pragma unroll
       for (int c = 0; c < D / 16; ++c) {
-        qh[c][0] = pack_f16x2(xq[c][0] * up, xq[c][2] * up);   // dims 4t, 4t+2 as k = 2t, 2t+1
-        qh[c][1] = pack_f16x2(xq[c][1] * up, xq[c][3] * up);   // dims 4t+1, 4t+3 as k = 2t+8, 2t+9
+        if constexpr (BITS == 8) {
+          qh[c][0] = pack_f16x2(xq[c][0] * up, xq[c][2] * up);   // dims 4t, 4t+2 as k = 2t, 2t+1
+          qh[c][1] = pack_f16x2(xq[c][1] * up, xq[c][3] * up);   // dims 4t+1, 4t+3 as k = 2t+8, 2t+9
+        } else {  // slice c of chunk c/2: dims 8t + 2(c&1) + {0, 4} and + {1, 5} (xq rows hold 4 dims)
+          const int base = (c >> 1) * 2;   // xq row pair holding dims 32(c/2) + 8t .. +7
+          const int o = 2 * (c & 1);
+          const float* lo4 = xq[base];      // dims 8t .. 8t+3
+          const float* hi4 = xq[base + 1];  // dims 8t+4 .. 8t+7
+          qh[c][0] = pack_f16x2(lo4[o] * up, hi4[o] * up);
+          qh[c][1] = pack_f16x2(lo4[o + 1] * up, hi4[o + 1] * up);
+        }
       }
     }
     float mult[2];
@@ -543,14 +671,17 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
       for (int step = 0; step < C::kSteps; ++step) {
         const int t0 = warp * C::kWarpTokens + step * 16;
         if (valid == C::kTile)
-          q8_step<D, false>(st, qh, mult, k_base, v_base, t0, valid, lane);
+          q8_step<D, false, BITS>(st, qh, mult, k_base, v_base, t0, valid, lane);
         else if (t0 < valid)
-          q8_step<D, true>(st, qh, mult, k_base, v_base, t0, valid, lane);
+          q8_step<D, true, BITS>(st, qh, mult, k_base, v_base, t0, valid, lane);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    q8_acc_to_bf16_layout<D>(st, a.v_scale[g], lane);
+    if constexpr (BITS == 4)
+      q4_acc_to_bf16_layout<D>(st, a.v_scale[g], lane);
+    else
+      q8_acc_to_bf16_layout<D>(st, a.v_scale[g], lane);
   }
   if (n_win > 0) {
     uint32_t qb[M::kKSteps][2];
@@ -639,12 +770,12 @@ __global__ void __launch_bounds__(Q8Cfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   }
 }
 
-template <int D, bool PAGED, bool FUSED>
+template <int D, int BITS, bool PAGED, bool FUSED>
 cudaError_t launch_decode_q8_t(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
                                const CUtensorMap& kwm, const CUtensorMap& vwm, cudaStream_t st) {
-  using C = Q8Cfg<D>;
+  using C = Q8Cfg<D, BITS>;
   static int done[64] = {0};
-  auto kern = decode_q8_kernel<D, PAGED, FUSED>;
+  auto kern = decode_q8_kernel<D, BITS, PAGED, FUSED>;
   cudaError_t e = ensure_smem(kern, C::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   const dim3 grid(a.num_splits * ((a.Hq / a.Hkv) / a.hpc), a.Hkv, a.B);

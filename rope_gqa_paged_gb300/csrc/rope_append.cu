@@ -163,7 +163,105 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
   }
 }
 
+// INT4 caches (bf16 q / k / v, head_dim 128): one CTA per sequence. The rotated k of every KV
+// head is rounded to bf16 into shared memory first, so that each thread can then pack the codes
+// of dims 2j and 2j+1 into byte j (the even one in the low nibble); v packs straight from v_new.
+constexpr int kMaxQ4Heads = 32;
+
+__global__ void __launch_bounds__(kRopeThreads) rope_append_q4_kernel(const RopeArgs a) {
+  constexpr int D = 128, HALF = D / 2;
+  __shared__ float cs[4][HALF];
+  __shared__ __nv_bfloat16 kr[kMaxQ4Heads][D];
+  __shared__ size_t row_info[2];
+  __shared__ int append_ok;
+  const int b = blockIdx.x;
+  const int pos = a.positions[b];
+  const bool paged = a.block_table != nullptr;
+  const long long cap = paged ? (static_cast<long long>(a.max_blocks_per_seq) << a.log2_bs) : a.max_len;
+  if (pos < 0 || pos >= cap) {
+    if (threadIdx.x == 0) flag_error(a.err, RRA_ERR_POSITION);
+    return;
+  }
+  if (threadIdx.x < HALF) {
+    double sn, cn;
+    sincospi(static_cast<double>(pos) * a.inv_freq[threadIdx.x], &sn, &cn);
+    const float ch = static_cast<float>(cn), sh = static_cast<float>(sn);
+    cs[0][threadIdx.x] = ch;
+    cs[1][threadIdx.x] = static_cast<float>(cn - static_cast<double>(ch));
+    cs[2][threadIdx.x] = sh;
+    cs[3][threadIdx.x] = static_cast<float>(sn - static_cast<double>(sh));
+  }
+  if (threadIdx.x == HALF) {
+    int ok = 1;
+    size_t row0 = 0, stride = 0;
+    if (paged) {
+      const int phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (pos >> a.log2_bs)];
+      if (phys < 0 || phys >= a.num_blocks) {
+        flag_error(a.err, RRA_ERR_BLOCK_ID);
+        ok = 0;
+      } else {
+        row0 = ((static_cast<size_t>(phys) << a.log2_bs) + (pos & ((1 << a.log2_bs) - 1))) * a.Hkv;
+        stride = 1;
+      }
+    } else {
+      row0 = static_cast<size_t>(b) * a.Hkv * a.max_len + pos;
+      stride = a.max_len;
+    }
+    row_info[0] = row0;
+    row_info[1] = stride;
+    append_ok = ok;
+  }
+  __syncthreads();
+  const bool inter = a.rope_style == 1;
+  const __nv_bfloat16* qin = static_cast<const __nv_bfloat16*>(a.q) + static_cast<size_t>(b) * a.Hq * D;
+  __nv_bfloat16* qout = static_cast<__nv_bfloat16*>(a.q_out) + static_cast<size_t>(b) * a.Hq * D;
+  const __nv_bfloat16* kin = static_cast<const __nv_bfloat16*>(a.k_new) + static_cast<size_t>(b) * a.Hkv * D;
+  const __nv_bfloat16* vin = static_cast<const __nv_bfloat16*>(a.v_new) + static_cast<size_t>(b) * a.Hkv * D;
+  for (int idx = threadIdx.x; idx < (a.Hq + a.Hkv) * HALF; idx += blockDim.x) {
+    const int hh = idx / HALF, i = idx - hh * HALF;
+    const int ia = inter ? 2 * i : i, ib = inter ? 2 * i + 1 : i + HALF;
+    const bool is_q = hh < a.Hq;
+    const __nv_bfloat16* src = is_q ? qin + static_cast<size_t>(hh) * D : kin + static_cast<size_t>(hh - a.Hq) * D;
+    const float xa = __bfloat162float(src[ia]), xb = __bfloat162float(src[ib]);
+    const __nv_bfloat16 ra = __float2bfloat16_rn(rotate_diff(xa, xb, cs[0][i], cs[1][i], cs[2][i], cs[3][i]));
+    const __nv_bfloat16 rb = __float2bfloat16_rn(rotate_diff(xb, -xa, cs[0][i], cs[1][i], cs[2][i], cs[3][i]));
+    if (is_q) {
+      qout[static_cast<size_t>(hh) * D + ia] = ra;
+      qout[static_cast<size_t>(hh) * D + ib] = rb;
+    } else {
+      kr[hh - a.Hq][ia] = ra;
+      kr[hh - a.Hq][ib] = rb;
+    }
+  }
+  __syncthreads();
+  if (!append_ok) return;
+  const size_t row0 = row_info[0], stride = row_info[1];
+  uint8_t* kc = static_cast<uint8_t*>(a.k_cache);
+  uint8_t* vc = static_cast<uint8_t*>(a.v_cache);
+  for (int idx = threadIdx.x; idx < a.Hkv * HALF; idx += blockDim.x) {
+    const int g = idx / HALF, j = idx - g * HALF;
+    const float ks = a.k_scale[g], vs = a.v_scale[g];
+    const size_t byte = (row0 + g * stride) * HALF + j;
+    const __nv_bfloat16 k0 = kr[g][2 * j], k1 = kr[g][2 * j + 1];
+    const __nv_bfloat16 v0 = vin[static_cast<size_t>(g) * D + 2 * j], v1 = vin[static_cast<size_t>(g) * D + 2 * j + 1];
+    kc[byte] = pack_nibbles(quantize_code4(__bfloat162float(k0), ks), quantize_code4(__bfloat162float(k1), ks));
+    vc[byte] = pack_nibbles(quantize_code4(__bfloat162float(v0), vs), quantize_code4(__bfloat162float(v1), vs));
+    if (a.window > 0) {
+      const size_t w = ((static_cast<size_t>(b) * a.Hkv + g) * a.window + pos % a.window) * D + 2 * j;
+      static_cast<__nv_bfloat16*>(a.k_win)[w] = k0;
+      static_cast<__nv_bfloat16*>(a.k_win)[w + 1] = k1;
+      static_cast<__nv_bfloat16*>(a.v_win)[w] = v0;
+      static_cast<__nv_bfloat16*>(a.v_win)[w + 1] = v1;
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_rope_append_q4(const RopeArgs& a, cudaStream_t stream) {
+  rope_append_q4_kernel<<<a.B, kRopeThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rope_append(const RopeArgs& a, rra_dtype dt, cudaStream_t stream) {
   const dim3 grid(a.B * (a.gamma > 1 ? a.gamma : 1), (a.D / 2 + kPairsPerCta - 1) / kPairsPerCta);

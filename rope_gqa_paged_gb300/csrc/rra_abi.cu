@@ -154,9 +154,10 @@ int make_plan(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
 // so it adds no split. Paged blocks must hold at least 8 tokens and a contiguous cache at least
 // one tile; the window is a multiple of 8.
 int make_plan_q8(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size, int requested, int window,
-                 Plan* p) {
+                 Plan* p, int bits = 8) {
   int st = check_shapes(B, Hq, Hkv, D, RRA_BF16);
   if (st != RRA_OK) return st;
+  if (bits == 4 && D != 128) return RRA_EUNSUPPORTED;  // INT4 tiles: 64-byte rows
   if (requested < 0 || max_tokens < 0 || window < 0) return RRA_EINVAL;
   if (max_tokens > (int64_t(1) << 30)) return RRA_ERANGE;
   if (window % 8 != 0 || window > 65536) return RRA_EUNSUPPORTED;
@@ -164,7 +165,7 @@ int make_plan_q8(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_si
   p->mma = true;
   p->hpc = heads_per_cta(n_rep, true);
   if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
-  p->tile = rra::decode_q8_tile_tokens(D);
+  p->tile = rra::decode_q8_tile_tokens(D, bits);
   if (block_size > 0 ? block_size < 8 : max_tokens < p->tile) return RRA_EUNSUPPORTED;
   return plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
 }
@@ -261,21 +262,22 @@ int encode_map(CUtensorMap* map, const void* base, int rank, const cuuint64_t* d
 // INT8 code caches: rows of D bytes with the 128-byte (D = 128) or 64-byte (D = 64) swizzle.
 // Paged pools [num_blocks, block_size, Hkv, D] as {D, Hkv, block_size, num_blocks} with boxes of
 // one head's `box_rows` rows; contiguous caches [B, Hkv, max_len, D] as {D, max_len, B*Hkv}.
-int encode_q8_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int Hkv, int D,
+// RB: bytes of codes per token and head (D for INT8, D / 2 for INT4): 128 or 64.
+int encode_q8_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int block_size, int Hkv, int RB,
                        int box_rows) {
-  const cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(Hkv), cuuint64_t(block_size), cuuint64_t(num_blocks)};
-  const cuuint64_t strides[3] = {cuuint64_t(D), cuuint64_t(Hkv) * D, cuuint64_t(block_size) * Hkv * D};
-  const cuuint32_t box[4] = {cuuint32_t(D), 1u, cuuint32_t(box_rows), 1u};
+  const cuuint64_t dims[4] = {cuuint64_t(RB), cuuint64_t(Hkv), cuuint64_t(block_size), cuuint64_t(num_blocks)};
+  const cuuint64_t strides[3] = {cuuint64_t(RB), cuuint64_t(Hkv) * RB, cuuint64_t(block_size) * Hkv * RB};
+  const cuuint32_t box[4] = {cuuint32_t(RB), 1u, cuuint32_t(box_rows), 1u};
   return encode_map_typed(map, pool, 4, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                          D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+                          RB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-int encode_q8_contig_map(CUtensorMap* map, const void* cache, int B, int Hkv, int max_len, int D, int tile) {
-  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(max_len), cuuint64_t(B) * Hkv};
-  const cuuint64_t strides[2] = {cuuint64_t(D), cuuint64_t(max_len) * D};
-  const cuuint32_t box[3] = {cuuint32_t(D), cuuint32_t(tile), 1u};
+int encode_q8_contig_map(CUtensorMap* map, const void* cache, int B, int Hkv, int max_len, int RB, int tile) {
+  const cuuint64_t dims[3] = {cuuint64_t(RB), cuuint64_t(max_len), cuuint64_t(B) * Hkv};
+  const cuuint64_t strides[2] = {cuuint64_t(RB), cuuint64_t(max_len) * RB};
+  const cuuint32_t box[3] = {cuuint32_t(RB), cuuint32_t(tile), 1u};
   return encode_map_typed(map, cache, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                          D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+                          RB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // Pool [num_blocks, block_size, Hkv, D] as 4-D {D, Hkv, block_size, num_blocks}; the box is
@@ -396,15 +398,16 @@ int check_q8_buffers(const void* k_codes, const void* v_codes, const float* k_sc
 
 int q8_maps(const Plan& p, const void* k_codes, const void* v_codes, const void* k_win, const void* v_win, int window,
             const int32_t* block_table, int block_size, int num_blocks, int max_len, int B, int Hkv, int D,
-            CUtensorMap* km, CUtensorMap* vm, CUtensorMap* kwm, CUtensorMap* vwm) {
+            CUtensorMap* km, CUtensorMap* vm, CUtensorMap* kwm, CUtensorMap* vwm, int bits = 8) {
   int st;
+  const int RB = D * bits / 8;
   if (block_table != nullptr) {
     const int box_rows = block_size < p.tile ? block_size : p.tile;
-    st = encode_q8_pool_map(km, k_codes, num_blocks, block_size, Hkv, D, box_rows);
-    if (st == RRA_OK) st = encode_q8_pool_map(vm, v_codes, num_blocks, block_size, Hkv, D, box_rows);
+    st = encode_q8_pool_map(km, k_codes, num_blocks, block_size, Hkv, RB, box_rows);
+    if (st == RRA_OK) st = encode_q8_pool_map(vm, v_codes, num_blocks, block_size, Hkv, RB, box_rows);
   } else {
-    st = encode_q8_contig_map(km, k_codes, B, Hkv, max_len, D, p.tile);
-    if (st == RRA_OK) st = encode_q8_contig_map(vm, v_codes, B, Hkv, max_len, D, p.tile);
+    st = encode_q8_contig_map(km, k_codes, B, Hkv, max_len, RB, p.tile);
+    if (st == RRA_OK) st = encode_q8_contig_map(vm, v_codes, B, Hkv, max_len, RB, p.tile);
   }
   if (st != RRA_OK || window == 0) return st;
   const int rows = std::min(window, RRA_Q8_STAGE_BYTES / (4 * D));  // ring rows per stage (K + V bf16)
@@ -436,6 +439,133 @@ void set_q8_args(rra::DecodeArgs* a, const Q8Layout& l, const void* k_codes, con
 namespace rra {
 void record_cuda_error(cudaError_t e, const char* where) { cuda_fail(e, where); }
 }  // namespace rra
+
+static int decode_qk_num_splits(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size, int num_splits,
+                                int window, int bits) {
+  if (block_size < 0 || (block_size > 0 && !pow2(block_size))) return block_size < 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
+  Plan p;
+  const int st = make_plan_q8(B, Hq, Hkv, D, max_tokens, block_size, num_splits, window, &p, bits);
+  return st != RRA_OK ? st : p.splits;
+}
+
+static int rope_append_qk(int bits, const void* q, const void* k_new, const void* v_new, const int32_t* positions, void* q_out,
+                       void* k_codes, void* v_codes, const float* k_scale, const float* v_scale, void* k_win,
+                       void* v_win, int window, const int32_t* block_table, int max_blocks_per_seq, int block_size,
+                       int num_blocks, int max_len, int B, int Hq, int Hkv, int D, double rope_base, int rope_style,
+                       int32_t* err_flag, void* stream) {
+  int st = check_shapes(B, Hq, Hkv, D, RRA_BF16);
+  if (st != RRA_OK) return st;
+  if (!(rope_base > 1.0) || !std::isfinite(rope_base) || (rope_style != 0 && rope_style != 1)) return RRA_EINVAL;
+  if (window < 0) return RRA_EINVAL;
+  if (bits == 4 && (D != 128 || Hkv > 32)) return RRA_EUNSUPPORTED;
+  if (window > 0 && (window % 8 != 0 || window > 65536)) return RRA_EUNSUPPORTED;
+  if (int64_t(Hq) + Hkv > 8 * 65535) return RRA_ERANGE;
+  Q8Layout l;
+  st = q8_layout(block_table, max_blocks_per_seq, block_size, num_blocks, max_len, &l);
+  if (st != RRA_OK) return st;
+  if (l.capacity > (int64_t(1) << 30)) return RRA_ERANGE;
+  if (B == 0) return RRA_OK;
+  if (!q || !k_new || !v_new || !positions || !q_out) return RRA_EINVAL;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(q_out)) return RRA_EINVAL;
+  st = check_q8_buffers(k_codes, v_codes, k_scale, v_scale, k_win, v_win, window);
+  if (st != RRA_OK) return st;
+  rra::RopeArgs a{};
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.positions = positions;
+  a.q_out = q_out;
+  a.k_cache = k_codes;
+  a.v_cache = v_codes;
+  a.block_table = block_table;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.log2_bs = l.log2_bs;
+  a.num_blocks = num_blocks;
+  a.max_len = max_len;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.D = D;
+  a.rope_style = rope_style;
+  a.err = err_flag;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  a.k_win = k_win;
+  a.v_win = v_win;
+  a.window = window;
+  fill_theta_pi(a.inv_freq, D, rope_base);
+  const cudaError_t e = bits == 4 ? rra::launch_rope_append_q4(a, static_cast<cudaStream_t>(stream))
+                                  : rra::launch_rope_append_q8(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RRA_OK : cuda_fail(e, "rope_append (quantised) launch");
+}
+
+static int decode_attn_qk(int bits, const void* q_rot, const void* k_codes, const void* v_codes, const float* k_scale,
+                       const float* v_scale, const void* k_win, const void* v_win, int window,
+                       const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens, int block_size,
+                       int num_blocks, int max_len, void* out, int B, int Hq, int Hkv, int D, float scale,
+                       int num_splits, void* workspace, size_t ws_bytes, int32_t* err_flag, void* stream) {
+  Q8Layout l;
+  int st = q8_layout(block_table, max_blocks_per_seq, block_size, num_blocks, max_len, &l);
+  if (st != RRA_OK) return st;
+  Plan p;
+  st = make_plan_q8(B, Hq, Hkv, D, l.capacity, block_table ? block_size : 0, num_splits, window, &p, bits);
+  if (st != RRA_OK) return st;
+  if (!std::isfinite(scale)) return RRA_EINVAL;
+  if (B == 0) return RRA_OK;
+  if (!q_rot || !seq_lens || !out || !aligned16(q_rot) || !aligned16(out)) return RRA_EINVAL;
+  st = check_q8_buffers(k_codes, v_codes, k_scale, v_scale, k_win, v_win, window);
+  if (st != RRA_OK) return st;
+  st = check_workspace(p, B, Hq, D, workspace, ws_bytes);
+  if (st != RRA_OK) return st;
+  CUtensorMap km{}, vm{}, kwm{}, vwm{};
+  st = q8_maps(p, k_codes, v_codes, k_win, v_win, window, block_table, block_size, num_blocks, max_len, B, Hkv, D,
+               &km, &vm, &kwm, &vwm, bits);
+  if (st != RRA_OK) return st;
+  rra::DecodeArgs a = decode_args(p, q_rot, k_codes, v_codes, seq_lens, out, B, Hq, Hkv, D, scale, workspace, err_flag);
+  set_q8_args(&a, l, k_codes, v_codes, k_scale, v_scale, const_cast<void*>(k_win), const_cast<void*>(v_win), window,
+              block_table, max_blocks_per_seq, num_blocks, max_len);
+  a.code_bits = bits;
+  return finish_decode(rra::launch_decode_q8(a, km, vm, kwm, vwm, block_table != nullptr, false,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+static int decode_step_qk(int bits, const void* q, const void* k_new, const void* v_new, const int32_t* positions, void* q_out,
+                       void* k_codes, void* v_codes, const float* k_scale, const float* v_scale, void* k_win,
+                       void* v_win, int window, const int32_t* block_table, int max_blocks_per_seq, int block_size,
+                       int num_blocks, int max_len, void* out, int B, int Hq, int Hkv, int D, double rope_base,
+                       int rope_style, float scale, int num_splits, void* workspace, size_t ws_bytes,
+                       int32_t* err_flag, void* stream) {
+  Q8Layout l;
+  int st = q8_layout(block_table, max_blocks_per_seq, block_size, num_blocks, max_len, &l);
+  if (st != RRA_OK) return st;
+  Plan p;
+  st = make_plan_q8(B, Hq, Hkv, D, l.capacity, block_table ? block_size : 0, num_splits, window, &p, bits);
+  if (st != RRA_OK) return st;
+  st = check_step_args(q, k_new, v_new, positions, q_out, k_codes, v_codes, out, B, Hq, D, rope_base, rope_style,
+                       scale, RRA_BF16);
+  if (st != RRA_OK || B == 0) return st;
+  st = check_q8_buffers(k_codes, v_codes, k_scale, v_scale, k_win, v_win, window);
+  if (st != RRA_OK) return st;
+  st = check_workspace(p, B, Hq, D, workspace, ws_bytes);
+  if (st != RRA_OK) return st;
+  CUtensorMap km{}, vm{}, kwm{}, vwm{};
+  st = q8_maps(p, k_codes, v_codes, k_win, v_win, window, block_table, block_size, num_blocks, max_len, B, Hkv, D,
+               &km, &vm, &kwm, &vwm, bits);
+  if (st != RRA_OK) return st;
+  rra::DecodeArgs a = decode_args(p, q, k_codes, v_codes, nullptr, out, B, Hq, Hkv, D, scale, workspace, err_flag);
+  set_q8_args(&a, l, k_codes, v_codes, k_scale, v_scale, k_win, v_win, window, block_table, max_blocks_per_seq,
+              num_blocks, max_len);
+  a.code_bits = bits;
+  a.positions = positions;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.q_out = q_out;
+  a.rope_style = rope_style;
+  fill_theta_pi(a.theta_pi, D, rope_base);
+  return finish_decode(rra::launch_decode_q8(a, km, vm, kwm, vwm, block_table != nullptr, true,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
 
 extern "C" {
 
@@ -684,124 +814,48 @@ int rra_decode_step_paged(const void* q, const void* k_new, const void* v_new, c
 
 int rra_decode_q8_num_splits(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size, int num_splits,
                              int window) {
-  if (block_size < 0 || (block_size > 0 && !pow2(block_size))) return block_size < 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
-  Plan p;
-  const int st = make_plan_q8(B, Hq, Hkv, D, max_tokens, block_size, num_splits, window, &p);
-  return st != RRA_OK ? st : p.splits;
+  return decode_qk_num_splits(B, Hq, Hkv, D, max_tokens, block_size, num_splits, window, 8);
 }
 
-int rra_rope_append_q8(const void* q, const void* k_new, const void* v_new, const int32_t* positions, void* q_out,
-                       void* k_codes, void* v_codes, const float* k_scale, const float* v_scale, void* k_win,
-                       void* v_win, int window, const int32_t* block_table, int max_blocks_per_seq, int block_size,
-                       int num_blocks, int max_len, int B, int Hq, int Hkv, int D, double rope_base, int rope_style,
-                       int32_t* err_flag, void* stream) {
-  int st = check_shapes(B, Hq, Hkv, D, RRA_BF16);
-  if (st != RRA_OK) return st;
-  if (!(rope_base > 1.0) || !std::isfinite(rope_base) || (rope_style != 0 && rope_style != 1)) return RRA_EINVAL;
-  if (window < 0) return RRA_EINVAL;
-  if (int64_t(Hq) + Hkv > 8 * 65535) return RRA_ERANGE;
-  Q8Layout l;
-  st = q8_layout(block_table, max_blocks_per_seq, block_size, num_blocks, max_len, &l);
-  if (st != RRA_OK) return st;
-  if (l.capacity > (int64_t(1) << 30)) return RRA_ERANGE;
-  if (B == 0) return RRA_OK;
-  if (!q || !k_new || !v_new || !positions || !q_out) return RRA_EINVAL;
-  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(q_out)) return RRA_EINVAL;
-  st = check_q8_buffers(k_codes, v_codes, k_scale, v_scale, k_win, v_win, window);
-  if (st != RRA_OK) return st;
-  rra::RopeArgs a{};
-  a.q = q;
-  a.k_new = k_new;
-  a.v_new = v_new;
-  a.positions = positions;
-  a.q_out = q_out;
-  a.k_cache = k_codes;
-  a.v_cache = v_codes;
-  a.block_table = block_table;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.log2_bs = l.log2_bs;
-  a.num_blocks = num_blocks;
-  a.max_len = max_len;
-  a.B = B;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.D = D;
-  a.rope_style = rope_style;
-  a.err = err_flag;
-  a.k_scale = k_scale;
-  a.v_scale = v_scale;
-  a.k_win = k_win;
-  a.v_win = v_win;
-  a.window = window;
-  fill_theta_pi(a.inv_freq, D, rope_base);
-  const cudaError_t e = rra::launch_rope_append_q8(a, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? RRA_OK : cuda_fail(e, "rope_append_q8 launch");
+int rra_decode_q4_num_splits(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size, int num_splits,
+                             int window) {
+  return decode_qk_num_splits(B, Hq, Hkv, D, max_tokens, block_size, num_splits, window, 4);
 }
 
-int rra_decode_attn_q8(const void* q_rot, const void* k_codes, const void* v_codes, const float* k_scale,
-                       const float* v_scale, const void* k_win, const void* v_win, int window,
-                       const int32_t* block_table, int max_blocks_per_seq, const int32_t* seq_lens, int block_size,
-                       int num_blocks, int max_len, void* out, int B, int Hq, int Hkv, int D, float scale,
-                       int num_splits, void* workspace, size_t ws_bytes, int32_t* err_flag, void* stream) {
-  Q8Layout l;
-  int st = q8_layout(block_table, max_blocks_per_seq, block_size, num_blocks, max_len, &l);
-  if (st != RRA_OK) return st;
-  Plan p;
-  st = make_plan_q8(B, Hq, Hkv, D, l.capacity, block_table ? block_size : 0, num_splits, window, &p);
-  if (st != RRA_OK) return st;
-  if (!std::isfinite(scale)) return RRA_EINVAL;
-  if (B == 0) return RRA_OK;
-  if (!q_rot || !seq_lens || !out || !aligned16(q_rot) || !aligned16(out)) return RRA_EINVAL;
-  st = check_q8_buffers(k_codes, v_codes, k_scale, v_scale, k_win, v_win, window);
-  if (st != RRA_OK) return st;
-  st = check_workspace(p, B, Hq, D, workspace, ws_bytes);
-  if (st != RRA_OK) return st;
-  CUtensorMap km{}, vm{}, kwm{}, vwm{};
-  st = q8_maps(p, k_codes, v_codes, k_win, v_win, window, block_table, block_size, num_blocks, max_len, B, Hkv, D,
-               &km, &vm, &kwm, &vwm);
-  if (st != RRA_OK) return st;
-  rra::DecodeArgs a = decode_args(p, q_rot, k_codes, v_codes, seq_lens, out, B, Hq, Hkv, D, scale, workspace, err_flag);
-  set_q8_args(&a, l, k_codes, v_codes, k_scale, v_scale, const_cast<void*>(k_win), const_cast<void*>(v_win), window,
-              block_table, max_blocks_per_seq, num_blocks, max_len);
-  return finish_decode(rra::launch_decode_q8(a, km, vm, kwm, vwm, block_table != nullptr, false,
-                                             static_cast<cudaStream_t>(stream)));
-}
+#define RRA_APPEND_ARGS                                                                                             \
+  const void *q, const void *k_new, const void *v_new, const int32_t *positions, void *q_out, void *k_codes,         \
+      void *v_codes, const float *k_scale, const float *v_scale, void *k_win, void *v_win, int window,               \
+      const int32_t *block_table, int max_blocks_per_seq, int block_size, int num_blocks, int max_len, int B, int Hq, \
+      int Hkv, int D, double rope_base, int rope_style, int32_t *err_flag, void *stream
+#define RRA_APPEND_PASS                                                                                               \
+  q, k_new, v_new, positions, q_out, k_codes, v_codes, k_scale, v_scale, k_win, v_win, window, block_table,            \
+      max_blocks_per_seq, block_size, num_blocks, max_len, B, Hq, Hkv, D, rope_base, rope_style, err_flag, stream
+int rra_rope_append_q8(RRA_APPEND_ARGS) { return rope_append_qk(8, RRA_APPEND_PASS); }
+int rra_rope_append_q4(RRA_APPEND_ARGS) { return rope_append_qk(4, RRA_APPEND_PASS); }
 
-int rra_decode_step_q8(const void* q, const void* k_new, const void* v_new, const int32_t* positions, void* q_out,
-                       void* k_codes, void* v_codes, const float* k_scale, const float* v_scale, void* k_win,
-                       void* v_win, int window, const int32_t* block_table, int max_blocks_per_seq, int block_size,
-                       int num_blocks, int max_len, void* out, int B, int Hq, int Hkv, int D, double rope_base,
-                       int rope_style, float scale, int num_splits, void* workspace, size_t ws_bytes,
-                       int32_t* err_flag, void* stream) {
-  Q8Layout l;
-  int st = q8_layout(block_table, max_blocks_per_seq, block_size, num_blocks, max_len, &l);
-  if (st != RRA_OK) return st;
-  Plan p;
-  st = make_plan_q8(B, Hq, Hkv, D, l.capacity, block_table ? block_size : 0, num_splits, window, &p);
-  if (st != RRA_OK) return st;
-  st = check_step_args(q, k_new, v_new, positions, q_out, k_codes, v_codes, out, B, Hq, D, rope_base, rope_style,
-                       scale, RRA_BF16);
-  if (st != RRA_OK || B == 0) return st;
-  st = check_q8_buffers(k_codes, v_codes, k_scale, v_scale, k_win, v_win, window);
-  if (st != RRA_OK) return st;
-  st = check_workspace(p, B, Hq, D, workspace, ws_bytes);
-  if (st != RRA_OK) return st;
-  CUtensorMap km{}, vm{}, kwm{}, vwm{};
-  st = q8_maps(p, k_codes, v_codes, k_win, v_win, window, block_table, block_size, num_blocks, max_len, B, Hkv, D,
-               &km, &vm, &kwm, &vwm);
-  if (st != RRA_OK) return st;
-  rra::DecodeArgs a = decode_args(p, q, k_codes, v_codes, nullptr, out, B, Hq, Hkv, D, scale, workspace, err_flag);
-  set_q8_args(&a, l, k_codes, v_codes, k_scale, v_scale, k_win, v_win, window, block_table, max_blocks_per_seq,
-              num_blocks, max_len);
-  a.positions = positions;
-  a.k_new = k_new;
-  a.v_new = v_new;
-  a.q_out = q_out;
-  a.rope_style = rope_style;
-  fill_theta_pi(a.theta_pi, D, rope_base);
-  return finish_decode(rra::launch_decode_q8(a, km, vm, kwm, vwm, block_table != nullptr, true,
-                                             static_cast<cudaStream_t>(stream)));
-}
+#define RRA_ATTN_ARGS                                                                                                 \
+  const void *q_rot, const void *k_codes, const void *v_codes, const float *k_scale, const float *v_scale,            \
+      const void *k_win, const void *v_win, int window, const int32_t *block_table, int max_blocks_per_seq,           \
+      const int32_t *seq_lens, int block_size, int num_blocks, int max_len, void *out, int B, int Hq, int Hkv, int D, \
+      float scale, int num_splits, void *workspace, size_t ws_bytes, int32_t *err_flag, void *stream
+#define RRA_ATTN_PASS                                                                                                 \
+  q_rot, k_codes, v_codes, k_scale, v_scale, k_win, v_win, window, block_table, max_blocks_per_seq, seq_lens,          \
+      block_size, num_blocks, max_len, out, B, Hq, Hkv, D, scale, num_splits, workspace, ws_bytes, err_flag, stream
+int rra_decode_attn_q8(RRA_ATTN_ARGS) { return decode_attn_qk(8, RRA_ATTN_PASS); }
+int rra_decode_attn_q4(RRA_ATTN_ARGS) { return decode_attn_qk(4, RRA_ATTN_PASS); }
+
+#define RRA_STEP_ARGS                                                                                                 \
+  const void *q, const void *k_new, const void *v_new, const int32_t *positions, void *q_out, void *k_codes,         \
+      void *v_codes, const float *k_scale, const float *v_scale, void *k_win, void *v_win, int window,               \
+      const int32_t *block_table, int max_blocks_per_seq, int block_size, int num_blocks, int max_len, void *out,     \
+      int B, int Hq, int Hkv, int D, double rope_base, int rope_style, float scale, int num_splits, void *workspace,  \
+      size_t ws_bytes, int32_t *err_flag, void *stream
+#define RRA_STEP_PASS                                                                                                 \
+  q, k_new, v_new, positions, q_out, k_codes, v_codes, k_scale, v_scale, k_win, v_win, window, block_table,            \
+      max_blocks_per_seq, block_size, num_blocks, max_len, out, B, Hq, Hkv, D, rope_base, rope_style, scale,          \
+      num_splits, workspace, ws_bytes, err_flag, stream
+int rra_decode_step_q8(RRA_STEP_ARGS) { return decode_step_qk(8, RRA_STEP_PASS); }
+int rra_decode_step_q4(RRA_STEP_ARGS) { return decode_step_qk(4, RRA_STEP_PASS); }
 
 int rra_verify_num_splits(int B, int gamma, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
                           int num_splits) {

@@ -204,4 +204,15 @@ __device__ __forceinline__ int8_t quantize_code(float x, float s) {
   return static_cast<int8_t>(__float2int_rn(r));
 }
 
+// 4-bit code of x at scale s: clamp(round_half_even(x / s), -7, 7) (float32 quotient).
+__device__ __forceinline__ int quantize_code4(float x, float s) {
+  const float r = fminf(fmaxf(__fdiv_rn(x, s), -7.f), 7.f);
+  return __float2int_rn(r);
+}
+
+// Two 4-bit two's complement codes in one byte: `lo` in bits 0-3, `hi` in bits 4-7.
+__device__ __forceinline__ uint8_t pack_nibbles(int lo, int hi) {
+  return static_cast<uint8_t>((lo & 0xf) | ((hi & 0xf) << 4));
+}
+
 }  // namespace rra

@@ -80,6 +80,7 @@ struct DecodeArgs {
   void* k_win;                  // bf16 [B, Hkv, window, D]
   void* v_win;
   int window;
+  int code_bits;                // 8 (INT8 codes) or 4 (INT4, two per byte)
   // Speculative verify (verify.cuh): gamma new tokens per sequence at positions[b] ..
   // positions[b] + gamma - 1; q and out are [B, gamma, Hq, D].
   int gamma;
@@ -102,6 +103,8 @@ void record_cuda_error(cudaError_t e, const char* where);
 cudaError_t launch_rope_append(const RopeArgs& a, rra_dtype dt, cudaStream_t stream);
 // RoPE + append into an INT8 cache (bf16 q / k_new / v_new; a.k_scale etc. set).
 cudaError_t launch_rope_append_q8(const RopeArgs& a, cudaStream_t stream);
+// The same into an INT4 cache (head_dim 128, at most 32 KV heads).
+cudaError_t launch_rope_append_q4(const RopeArgs& a, cudaStream_t stream);
 // Tokens per stage of the tensor-core (bf16) decode kernel: K + V tiles of 32 KB.
 inline int decode_mma_tile_tokens(int D) { return 16384 / (D * 2); }
 // Most block-table entries one work item of the tensor-core kernel may span.
@@ -132,8 +135,8 @@ cudaError_t launch_decode_verify(const DecodeArgs& a, const CUtensorMap& k_map, 
 // first one's position); 64 query rows (a.hpc heads x 64 / a.hpc tokens) per CTA.
 cudaError_t launch_prefill(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map, bool paged,
                            cudaStream_t stream);
-// Tokens per stage of the INT8 decode kernel.
-inline int decode_q8_tile_tokens(int D) { return RRA_Q8_STAGE_BYTES / 2 / D; }
+// Tokens per stage of the INT8 (bits 8) / INT4 (bits 4) decode kernel.
+inline int decode_q8_tile_tokens(int D, int bits = 8) { return RRA_Q8_STAGE_BYTES / 2 / (D * bits / 8); }
 // INT8 caches: attention only (a.seq_lens) or the fused step (a.positions, a.k_new, ...).
 // k_map / v_map cover the code caches, kw_map / vw_map the bf16 rings (unused without a window).
 cudaError_t launch_decode_q8(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,

@@ -52,6 +52,8 @@ _SIGNATURES = {
                                     _c_int, _c_int, _c_int, _vp, _c_int, _c_int, _c_int, _c_int, _c_f64, _c_int,
                                     _c_f32, _c_int, _vp, _c_size, _vp, _vp]),
     "rra_decode_q8_num_splits": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_i64, _c_int, _c_int, _c_int]),
+    "rra_rope_append_q4": None, "rra_decode_attn_q4": None, "rra_decode_step_q4": None,
+    "rra_decode_q4_num_splits": None,
     "rra_rope_append_verify": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                         _c_int, _c_int, _c_int, _c_int, _c_int, _c_f64, _c_int, _c_int, _vp, _vp]),
     "rra_verify_attn": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int, _vp, _c_int, _c_int,
@@ -89,6 +91,8 @@ def lib() -> ctypes.CDLL:
             raise RuntimeError(f"{_build.LIB_PATH} is missing: build the CUDA library first "
                                "(python -c 'import __graft_entry__ as g; g.build()')")
         handle = ctypes.CDLL(_build.LIB_PATH)
+        for name in [n for n, sig in _SIGNATURES.items() if sig is None]:   # INT4 twins of the INT8 calls
+            _SIGNATURES[name] = _SIGNATURES[name.replace("_q4", "_q8")]
         for name, (res, args) in _SIGNATURES.items():
             fn = getattr(handle, name)
             fn.restype, fn.argtypes = res, args
@@ -238,59 +242,72 @@ def _q8_layout(codes, block_table):
     return 0, 0, 0, codes.shape[2]
 
 
+def _qfn(name: str, bits: int):
+    """The INT8 (bits 8) or INT4 (bits 4) entry point of a quantised-cache call."""
+    if bits not in (8, 4):
+        raise ValueError("code width must be 8 or 4 bits")
+    full = name if bits == 8 else name.replace("_q8", "_q4")
+    return full, getattr(lib(), full)
+
+
 def rra_decode_q8_num_splits(B: int, Hq: int, Hkv: int, D: int, max_tokens: int, block_size: int, num_splits: int,
-                             window: int) -> int:
-    r = lib().rra_decode_q8_num_splits(B, Hq, Hkv, D, max_tokens, block_size, num_splits, window)
-    _check("rra_decode_q8_num_splits", min(r, 0))
+                             window: int, bits: int = 8) -> int:
+    name, fn = _qfn("rra_decode_q8_num_splits", bits)
+    r = fn(B, Hq, Hkv, D, max_tokens, block_size, num_splits, window)
+    _check(name, min(r, 0))
     return r
 
 
 def rra_rope_append_q8(q, k_new, v_new, positions, q_out, k_codes, v_codes, k_scale, v_scale, k_win=None, v_win=None,
                        block_table=None, rope_base: float = 10000.0, rope_style: int = 0, err_flag=None,
-                       stream=None) -> None:
-    """RoPE on bf16 q / k_new, then quantised append into the INT8 caches (and the bf16 rings)."""
+                       stream=None, bits: int = 8) -> None:
+    """RoPE on bf16 q / k_new, then quantised append into the INT8 (or INT4) caches and the bf16 rings."""
     B, Hq, D = q.shape
     Hkv = k_new.shape[1]
     window = k_win.shape[2] if k_win is not None else 0
     mbps, bs, nblk, max_len = _q8_layout(k_codes, block_table)
-    st = lib().rra_rope_append_q8(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q_out), _ptr(k_codes),
+    name, fn = _qfn("rra_rope_append_q8", bits)
+    st = fn(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q_out), _ptr(k_codes),
                                   _ptr(v_codes), _ptr(k_scale), _ptr(v_scale), _ptr(k_win), _ptr(v_win), window,
                                   _ptr(block_table), mbps, bs, nblk, max_len, B, Hq, Hkv, D, float(rope_base),
                                   int(rope_style), _ptr(err_flag), _stream(stream, q))
-    _check("rra_rope_append_q8", st)
+    _check(name, st)
 
 
 def rra_decode_attn_q8(q_rot, k_codes, v_codes, k_scale, v_scale, seq_lens, out, k_win=None, v_win=None,
                        block_table=None, scale: float = 0.0, num_splits: int = 0, workspace=None, err_flag=None,
-                       stream=None) -> None:
+                       stream=None, bits: int = 8) -> None:
     """Attention of q_rot over the INT8 cache (tokens older than the window) and the bf16 rings."""
     B, Hq, D = q_rot.shape
     Hkv = k_codes.shape[2] if block_table is not None else k_codes.shape[1]
     window = k_win.shape[2] if k_win is not None else 0
     mbps, bs, nblk, max_len = _q8_layout(k_codes, block_table)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = lib().rra_decode_attn_q8(_ptr(q_rot), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale),
+    name, fn = _qfn("rra_decode_attn_q8", bits)
+    st = fn(_ptr(q_rot), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale),
                                   _ptr(k_win), _ptr(v_win), window, _ptr(block_table), mbps, _ptr(seq_lens), bs, nblk,
                                   max_len, _ptr(out), B, Hq, Hkv, D, float(scale), int(num_splits), _ptr(workspace),
                                   ws_bytes, _ptr(err_flag), _stream(stream, q_rot))
-    _check("rra_decode_attn_q8", st)
+    _check(name, st)
 
 
 def rra_decode_step_q8(q, k_new, v_new, positions, q_out, k_codes, v_codes, k_scale, v_scale, out, k_win=None,
                        v_win=None, block_table=None, rope_base: float = 10000.0, rope_style: int = 0,
-                       scale: float = 0.0, num_splits: int = 0, workspace=None, err_flag=None, stream=None) -> None:
+                       scale: float = 0.0, num_splits: int = 0, workspace=None, err_flag=None, stream=None,
+                       bits: int = 8) -> None:
     """The whole step on an INT8 cache in one kernel: RoPE, quantised append, attention over positions + 1."""
     B, Hq, D = q.shape
     Hkv = k_new.shape[1]
     window = k_win.shape[2] if k_win is not None else 0
     mbps, bs, nblk, max_len = _q8_layout(k_codes, block_table)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    st = lib().rra_decode_step_q8(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q_out), _ptr(k_codes),
+    name, fn = _qfn("rra_decode_step_q8", bits)
+    st = fn(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q_out), _ptr(k_codes),
                                   _ptr(v_codes), _ptr(k_scale), _ptr(v_scale), _ptr(k_win), _ptr(v_win), window,
                                   _ptr(block_table), mbps, bs, nblk, max_len, _ptr(out), B, Hq, Hkv, D,
                                   float(rope_base), int(rope_style), float(scale), int(num_splits), _ptr(workspace),
                                   ws_bytes, _ptr(err_flag), _stream(stream, q))
-    _check("rra_decode_step_q8", st)
+    _check(name, st)
 
 
 # --------------------------------------------------------------------------- speculative verify

@@ -108,7 +108,8 @@ class DecodeStep:
 
 
 class DecodeStepQ8(DecodeStep):
-    """The decode step on an INT8 KV cache with per-head scales and a bf16 window of recent tokens.
+    """The decode step on an INT8 (bits 8) or INT4 (bits 4, two codes per byte) KV cache with
+    per-head scales and a bf16 window of recent tokens.
 
     k_codes / v_codes: int8 [B, Hkv, max_len, D] or pools [num_blocks, block_size, Hkv, D] (with
     ``block_table``); k_scale / v_scale: float32 [Hkv]; k_win / v_win: bf16 rings [B, Hkv, W, D]
@@ -119,8 +120,9 @@ class DecodeStepQ8(DecodeStep):
                  v_codes: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
                  k_win: Optional[torch.Tensor] = None, v_win: Optional[torch.Tensor] = None,
                  block_table: Optional[torch.Tensor] = None, num_splits: int = 0, rope_base: float = 10000.0,
-                 rope_style: int = 0, scale: float = 0.0):
+                 rope_style: int = 0, scale: float = 0.0, bits: int = 8):
         self.B, self.Hq, self.Hkv, self.D = batch, n_q_heads, n_kv_heads, head_dim
+        self.bits = bits
         self.k_cache, self.v_cache, self.block_table = k_codes, v_codes, block_table
         self.k_scale, self.v_scale, self.k_win, self.v_win = k_scale, v_scale, k_win, v_win
         self.window = k_win.shape[2] if k_win is not None else 0
@@ -132,7 +134,7 @@ class DecodeStepQ8(DecodeStep):
         else:
             bs, max_tokens = 0, k_codes.shape[2]
         self.splits = rra.rra_decode_q8_num_splits(batch, n_q_heads, n_kv_heads, head_dim, max_tokens, bs,
-                                                   num_splits, self.window)
+                                                   num_splits, self.window, bits)
         self.num_splits = num_splits
         ws = rra.rra_decode_workspace_bytes(batch, n_q_heads, head_dim, self.splits)
         self.workspace = torch.zeros(ws, dtype=torch.uint8, device=dev) if ws else None  # zeroed once
@@ -144,18 +146,19 @@ class DecodeStepQ8(DecodeStep):
     def rope_append(self, q, k_new, v_new, positions, stream=None) -> None:
         rra.rra_rope_append_q8(q, k_new, v_new, positions, self.q_rot, self.k_cache, self.v_cache, self.k_scale,
                                self.v_scale, self.k_win, self.v_win, self.block_table, self.rope_base,
-                               self.rope_style, self.err, stream)
+                               self.rope_style, self.err, stream, bits=self.bits)
 
     def attend(self, seq_lens, stream=None) -> torch.Tensor:
         rra.rra_decode_attn_q8(self.q_rot, self.k_cache, self.v_cache, self.k_scale, self.v_scale, seq_lens,
                                self.out, self.k_win, self.v_win, self.block_table, self.scale, self.num_splits,
-                               self.workspace, self.err, stream)
+                               self.workspace, self.err, stream, bits=self.bits)
         return self.out
 
     def fused(self, q, k_new, v_new, positions, stream=None) -> torch.Tensor:
         rra.rra_decode_step_q8(q, k_new, v_new, positions, self.q_rot, self.k_cache, self.v_cache, self.k_scale,
                                self.v_scale, self.out, self.k_win, self.v_win, self.block_table, self.rope_base,
-                               self.rope_style, self.scale, self.num_splits, self.workspace, self.err, stream)
+                               self.rope_style, self.scale, self.num_splits, self.workspace, self.err, stream,
+                               bits=self.bits)
         return self.out
 
 

@@ -179,7 +179,7 @@ def run_gpu_q8(inp: DecodeInputs, num_splits: int = 0, rope_style: int = 0, devi
     step = DecodeStepQ8(cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, kc, vc,
                         torch.from_numpy(inp.k_scale).to(device), torch.from_numpy(inp.v_scale).to(device), kw, vw,
                         table, num_splits=num_splits or cfg.num_splits, rope_base=cfg.rope_base,
-                        rope_style=rope_style)
+                        rope_style=rope_style, bits=cfg.code_bits)
     args = (to_torch(inp.q, "bf16", device), to_torch(inp.k_new, "bf16", device), to_torch(inp.v_new, "bf16", device),
             to_torch(inp.positions, "i32", device))
     if fused:
@@ -201,7 +201,8 @@ def run_oracle_q8(inp: DecodeInputs, rope_style: int = 0, seq_lens=None):
     bs = cfg.block_size if inp.block_table is not None else 0
     return oracle.quant.decode_step_q8(inp.q, inp.k_new, inp.v_new, inp.positions, inp.k_cache, inp.v_cache,
                                        inp.k_scale, inp.v_scale, inp.k_win, inp.v_win, cfg.window, inp.block_table,
-                                       bs, seq_lens=seq_lens, rope_base=cfg.rope_base, rope_style=rope_style)
+                                       bs, seq_lens=seq_lens, rope_base=cfg.rope_base, rope_style=rope_style,
+                                       bits=cfg.code_bits)
 
 
 # ---------------------------------------------------------------------------- speculative verify

@@ -1,4 +1,4 @@
-"""INT8 KV cache with per-head scales and a bf16 window: CUDA path against the float64 oracle.
+"""INT8 / INT4 KV cache with per-head scales and a bf16 window: CUDA path against the float64 oracle.
 
 Bars (same inputs on both sides): q_rot and the ring's k within 1 bf16 ulp; the ring's v and
 every V code bit-exact; a K code equal to the quantisation of the GPU's own bf16 k wherever
@@ -30,6 +30,7 @@ def _slot(inp, b, pos):
 def _check_q8(inp, gpu, ref, fused_or_append=True, out_batches=None):
     cfg = inp.cfg
     q_ref, kc_ref, vc_ref, kw_ref, vw_ref, out_ref = ref
+    bits = cfg.code_bits
     H.assert_close_stored(gpu.q_rot, q_ref, "bf16", "q_rot")
     bs = range(cfg.batch) if out_batches is None else out_batches
     err = H.out_error(gpu.out[list(bs)], out_ref[list(bs)], "bf16")
@@ -43,14 +44,16 @@ def _check_q8(inp, gpu, ref, fused_or_append=True, out_batches=None):
         idx = _slot(inp, b, pos)
         # V codes: the quantisation of an input value, bit-exact
         assert vc[idx].tobytes() == vc_ref[idx].tobytes(), f"V codes of sequence {b}"
-        kd = np.abs(kc[idx].astype(int) - kc_ref[idx].astype(int))
+        kd = np.abs(oracle.quant.load_codes(kc[idx], bits).astype(int) -
+                    oracle.quant.load_codes(kc_ref[idx], bits).astype(int))
         assert kd.max() <= 1, f"K codes of sequence {b} differ by {kd.max()}"
         if W:
             s = pos % W
             H.assert_close_stored(kw[b, :, s], kw_ref[b, :, s], "bf16", f"ring k of sequence {b}")
             assert vw[b, :, s].tobytes() == vw_ref[b, :, s].tobytes(), f"ring v of sequence {b}"
             # the code is the quantisation of the GPU's own bf16 k, decided in float32
-            mine = oracle.quant.quantize_int8(oracle.bf16_bits_to_f64(kw[b, :, s]), inp.k_scale[:, None])
+            mine = oracle.quant.store_codes(
+                oracle.quant.quantize(oracle.bf16_bits_to_f64(kw[b, :, s]), inp.k_scale[:, None], bits), bits)
             assert np.array_equal(kc[idx], mine), f"K codes of sequence {b} vs its ring value"
             kw[b, :, s], vw[b, :, s] = inp.k_win[b, :, s], inp.v_win[b, :, s]
         else:
@@ -63,7 +66,8 @@ def _check_q8(inp, gpu, ref, fused_or_append=True, out_batches=None):
     return err
 
 
-REDUCED = [("batched_paged_int8", 16, 8), ("long_context_int8", 64, 1)]
+REDUCED = [("batched_paged_int8", 16, 8), ("long_context_int8", 64, 1), ("batched_paged_int4", 16, 8),
+           ("long_context_int4", 64, 1)]
 
 
 @pytest.mark.parametrize("name,factor,batch", REDUCED, ids=[r[0] for r in REDUCED])
@@ -80,13 +84,13 @@ def test_q8_reduced_workload(name, factor, batch, window, splits, fused):
     _check_q8(inp, gpu, H.run_oracle_q8(inp))
 
 
-def _edge_cfg(layout, lengths, window, block_size=16, head_dim=128, hq=8, hkv=2, max_len=None):
+def _edge_cfg(layout, lengths, window, block_size=16, head_dim=128, hq=8, hkv=2, max_len=None, bits=8):
     lengths = list(lengths)
     longest = max(lengths)
-    kw = dict(name=f"q8_edge_{layout}", batch=len(lengths), n_q_heads=hq, n_kv_heads=hkv, head_dim=head_dim,
-              dtype="bf16", layout=layout, len_range=(min(lengths), longest), kv_dtype="int8", window=window)
+    kw = dict(name=f"q{bits}_edge_{layout}", batch=len(lengths), n_q_heads=hq, n_kv_heads=hkv, head_dim=head_dim,
+              dtype="bf16", layout=layout, len_range=(min(lengths), longest), kv_dtype=f"int{bits}", window=window)
     if layout == "contiguous":
-        kw["max_len"] = max_len or max(longest, 16384 // head_dim)
+        kw["max_len"] = max_len or max(longest, 8192 // (head_dim * bits // 8))
     else:
         kw.update(block_size=block_size, max_blocks_per_seq=-(-longest // block_size))
         kw["num_blocks"] = len(lengths) * kw["max_blocks_per_seq"] + 5
@@ -113,8 +117,9 @@ EDGE_LENGTHS = [1, 2, 15, 16, 17, 31, 32, 33, 127, 128, 129, 300]
                                                ("paged", 256)])
 @pytest.mark.parametrize("window", [0, 16, 32])
 @pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused_step"])
-def test_q8_edge_lengths(layout, block_size, window, fused):
-    cfg = _edge_cfg(layout, EDGE_LENGTHS, window, block_size=block_size or 16)
+@pytest.mark.parametrize("bits", [8, 4], ids=["int8", "int4"])
+def test_q8_edge_lengths(layout, block_size, window, fused, bits):
+    cfg = _edge_cfg(layout, EDGE_LENGTHS, window, block_size=block_size or 16, bits=bits)
     inp = _with_lengths(cfg, EDGE_LENGTHS)
     for splits in (0, 2):
         gpu = H.run_gpu_q8(inp, num_splits=splits, fused=fused)
@@ -123,11 +128,11 @@ def test_q8_edge_lengths(layout, block_size, window, fused):
 
 
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (32, 1), (12, 4), (64, 4)], ids=["mha", "mqa", "nrep3", "nrep16"])
-@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("head_dim,bits", [(64, 8), (128, 8), (128, 4)], ids=["d64_int8", "d128_int8", "d128_int4"])
 @pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused_step"])
-def test_q8_heads_and_head_dim(hq, hkv, head_dim, fused):
+def test_q8_heads_and_head_dim(hq, hkv, head_dim, bits, fused):
     lengths = [5, 200, 611]
-    cfg = _edge_cfg("paged", lengths, 16, block_size=16, head_dim=head_dim, hq=hq, hkv=hkv)
+    cfg = _edge_cfg("paged", lengths, 16, block_size=16, head_dim=head_dim, hq=hq, hkv=hkv, bits=bits)
     inp = _with_lengths(cfg, lengths, seed=7)
     gpu = H.run_gpu_q8(inp, num_splits=3, fused=fused, rope_style=1 if head_dim == 64 else 0)
     assert gpu.err == 0
@@ -136,19 +141,21 @@ def test_q8_heads_and_head_dim(hq, hkv, head_dim, fused):
 
 @pytest.mark.parametrize("splits", [17, 40])
 @pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused_step"])
-def test_q8_many_splits_merge(splits, fused):
+@pytest.mark.parametrize("bits", [8, 4], ids=["int8", "int4"])
+def test_q8_many_splits_merge(splits, fused, bits):
     lengths = [4100, 2500]
-    cfg = _edge_cfg("paged", lengths, 64, block_size=32)
+    cfg = _edge_cfg("paged", lengths, 64, block_size=32, bits=bits)
     inp = _with_lengths(cfg, lengths, seed=11)
     gpu = H.run_gpu_q8(inp, num_splits=splits, fused=fused)
     assert gpu.err == 0 and gpu.splits > 16
     _check_q8(inp, gpu, H.run_oracle_q8(inp))
 
 
-def test_q8_position_errors_are_flagged():
+@pytest.mark.parametrize("bits", [8, 4], ids=["int8", "int4"])
+def test_q8_position_errors_are_flagged(bits):
     from rope_gqa_paged_gb300 import RRA_ERR_POSITION
     lengths = [40, 60]
-    cfg = _edge_cfg("paged", lengths, 16)
+    cfg = _edge_cfg("paged", lengths, 16, bits=bits)
     inp = _with_lengths(cfg, lengths)
     inp.positions = np.array([39, cfg.capacity], dtype=np.int32)      # second one is past the cache
     gpu = H.run_gpu_q8(inp, fused=True)
