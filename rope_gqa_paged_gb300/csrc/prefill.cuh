@@ -13,6 +13,8 @@
 // warp step, so each K/V byte brought into shared memory serves 64 rows. The CTA streams keys
 // [0, its last row's position]: the slices past a warp's own last row are skipped, and the
 // query blocks are launched longest first. No split-K: each warp normalises and writes its rows.
+// Whole 32-token windows go through a two-slice step (more independent mma chains per warp);
+// two CTAs per SM leave the registers for it.
 #pragma once
 
 #include "verify.cuh"
@@ -21,8 +23,104 @@ namespace rra {
 
 constexpr int kPrefillRows = 64;
 
+// 32 tokens of a stage for one warp (rows t0 .. t0+31, all within the chunk), bf16 P: the
+// verify step on two 16-token slices at once -- four independent score chains instead of two,
+// one softmax reduction and at most one rescale per 32 tokens. lim0 / lim1 as in verify_step.
+template <int D>
+__device__ __forceinline__ void prefill_step32(VerifyState<D>& st, const uint32_t (&qa)[D / 16][4], uint32_t k_base,
+                                               uint32_t v_base, int t0, int tok0, int lim0, int lim1, int lane,
+                                               float scale_log2) {
+  using C = MmaCfg<D>;
+  const int mat = lane >> 3, t = lane & 3;
+  float s[4][4];
+#pragma unroll
+  for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+  {
+    const int r = t0 + (lane & 7) + ((mat >> 1) << 3);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      uint32_t b[4], c[4];
+      const uint32_t off = (kk >> 2) * C::kHalfBytes;
+      ldsm_x4(k_base + off + swz(r, ((kk & 3) << 1) + (mat & 1)), b);
+      ldsm_x4(k_base + off + swz(r + 16, ((kk & 3) << 1) + (mat & 1)), c);
+      mma_bf16(s[0], qa[kk], b[0], b[1]);
+      mma_bf16(s[1], qa[kk], b[2], b[3]);
+      mma_bf16(s[2], qa[kk], c[0], c[1]);
+      mma_bf16(s[3], qa[kk], c[2], c[3]);
+    }
+  }
+  float x[4][4];
+#pragma unroll
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int tok = tok0 + 8 * n + 2 * t + (c & 1);
+      x[n][c] = tok <= (c < 2 ? lim0 : lim1) ? s[n][c] * scale_log2 : -INFINITY;
+    }
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int n = 0; n < 4; ++n) {
+    mx[0] = fmaxf(mx[0], fmaxf(x[n][0], x[n][1]));
+    mx[1] = fmaxf(mx[1], fmaxf(x[n][2], x[n][3]));
+  }
+  bool grow = false;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+    mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+    mx[i] = fmaxf(st.m[i], mx[i]);
+    grow |= mx[i] > st.m[i];
+  }
+  if (__any_sync(0xffffffffu, grow)) {
+    float alpha[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      alpha[i] = mx[i] > st.m[i] ? exp2f(st.m[i] - mx[i]) : 1.f;
+      st.l[i] *= alpha[i];
+      st.m[i] = mx[i];
+    }
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) {
+      st.o[nt][0] *= alpha[0];
+      st.o[nt][1] *= alpha[0];
+      st.o[nt][2] *= alpha[1];
+      st.o[nt][3] *= alpha[1];
+    }
+  }
+  const float mref[2] = {st.m[0] == -INFINITY ? 0.f : st.m[0], st.m[1] == -INFINITY ? 0.f : st.m[1]};
+  uint32_t pa[2][4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float p[2][4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) p[n][c] = exp2f(x[2 * h + n][c] - mref[c >> 1]);
+    st.l[0] += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+    st.l[1] += (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
+    pa[h][0] = pack_bf16x2(p[0][0], p[0][1]);
+    pa[h][1] = pack_bf16x2(p[0][2], p[0][3]);
+    pa[h][2] = pack_bf16x2(p[1][0], p[1][1]);
+    pa[h][3] = pack_bf16x2(p[1][2], p[1][3]);
+  }
+  {
+    const int r = t0 + (lane & 7) + ((mat & 1) << 3);
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) {
+      uint32_t b[4], c[4];
+      const uint32_t off = (j >> 2) * C::kHalfBytes;
+      ldsm_x4_trans(v_base + off + swz(r, ((j & 3) << 1) + (mat >> 1)), b);
+      ldsm_x4_trans(v_base + off + swz(r + 16, ((j & 3) << 1) + (mat >> 1)), c);
+      mma_bf16(st.o[2 * j], pa[0], b[0], b[1]);
+      mma_bf16(st.o[2 * j + 1], pa[0], b[2], b[3]);
+      mma_bf16(st.o[2 * j], pa[1], c[0], c[1]);
+      mma_bf16(st.o[2 * j + 1], pa[1], c[2], c[3]);
+    }
+  }
+}
+
 template <int D, bool PAGED>
-__global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
+__global__ void __launch_bounds__(MmaCfg<D>::kThreads, 2)
     prefill_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                    const DecodeArgs a) {
   using C = MmaCfg<D>;
@@ -178,7 +276,12 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     const int tile0 = it * C::kTile;
     const int valid = min(C::kTile, end - tile0);
 #pragma unroll 1
-    for (int t0 = 0; t0 < valid && tile0 + t0 <= last; t0 += 16) {
+    for (int t0 = 0; t0 < valid && tile0 + t0 <= last;) {
+      if (!precise && t0 + 32 <= valid) {  // two whole slices at once
+        prefill_step32<D>(st, qa, k_base, v_base, t0, tile0 + t0, lim[0], lim[1], lane, a.scale_log2);
+        t0 += 32;
+        continue;
+      }
       const bool partial = t0 + 16 > valid;
       if (precise) {
         if (partial)
@@ -195,6 +298,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
           verify_step<D, false, false>(st, qa, k_base, v_base, vst, t0, tile0 + t0, valid, lim[0], lim[1], lane,
                                        a.scale_log2);
       }
+      t0 += 16;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
