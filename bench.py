@@ -229,9 +229,17 @@ def device_workload(cfg, seed, device):
     B, Hq, Hkv, D = cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     shape = (B, Hkv, cfg.max_len, D) if cfg.layout == "contiguous" else (cfg.num_blocks, cfg.block_size, Hkv, D)
     lead = (B,) if cfg.gamma == 1 else (B, cfg.gamma)
-    if cfg.int8:  # INT8 codes: N(0,1) at a resolution of 1/32, clipped; fixed per-head scales; bf16 rings
-        codes = lambda: torch.randn(shape, generator=g, device=device).mul_(32).round_().clamp_(-127, 127).to(  # noqa: E731
-            torch.int8)
+    per_unit = 32.0 if cfg.code_bits == 8 else 1.75   # codes per unit of N(0,1), as in the numpy recipe
+    if cfg.int8:  # codes: N(0,1) at a resolution of 1/per_unit, clipped; fixed per-head scales; bf16 rings
+        m = (1 << (cfg.code_bits - 1)) - 1
+
+        def codes():
+            c = torch.randn(shape, generator=g, device=device).mul_(per_unit).round_().clamp_(-m, m).to(torch.int8)
+            if cfg.code_bits == 8:
+                return c
+            n = c.to(torch.uint8) & 0x0F                   # INT4: two codes per byte, the even dim low
+            return (n[..., 0::2] | (n[..., 1::2] << 4)).contiguous()
+
         kc, vc = codes(), codes()
     else:
         kc = torch.randn(shape, generator=g, device=device, dtype=dt)
@@ -248,8 +256,8 @@ def device_workload(cfg, seed, device):
     }
     if cfg.int8:
         h = np.arange(Hkv)
-        w["k_scale"] = torch.from_numpy(((1.0 + (h % 4) / 8.0) / 32.0).astype(np.float32)).to(device)
-        w["v_scale"] = torch.from_numpy(((1.0 + ((h + 2) % 4) / 8.0) / 32.0).astype(np.float32)).to(device)
+        w["k_scale"] = torch.from_numpy(((1.0 + (h % 4) / 8.0) / per_unit).astype(np.float32)).to(device)
+        w["v_scale"] = torch.from_numpy(((1.0 + ((h + 2) % 4) / 8.0) / per_unit).astype(np.float32)).to(device)
         w["k_win"] = w["v_win"] = None
         if cfg.window:
             w["k_win"] = torch.randn(B, Hkv, cfg.window, D, generator=g, device=device, dtype=torch.bfloat16)
@@ -294,7 +302,7 @@ def run_ours(args):
     elif cfg.int8:
         step = DecodeStepQ8(cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, w["k_cache"], w["v_cache"],
                             w["k_scale"], w["v_scale"], w["k_win"], w["v_win"], w["block_table"],
-                            num_splits=splits_arg, rope_base=cfg.rope_base)
+                            num_splits=splits_arg, rope_base=cfg.rope_base, bits=cfg.code_bits)
     else:
         step = DecodeStep(cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, w["k_cache"], w["v_cache"],
                           w["block_table"], num_splits=splits_arg, rope_base=cfg.rope_base)
@@ -460,7 +468,7 @@ def run_ours(args):
     line = {
         "metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": K,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int8 K/V codes + bf16 window, f16 mma, f32 softmax" if cfg.int8 else cfg.dtype, "data": "synthetic (seeded N(0,1); lengths/tables from the recipe)",
+        "vs_baseline": None, "dtype": f"int{cfg.code_bits} K/V codes + bf16 window, f16 mma, f32 softmax" if cfg.int8 else cfg.dtype, "data": "synthetic (seeded N(0,1); lengths/tables from the recipe)",
         "config": {
             "workload": cfg.name, "description": cfg.description, "batch_per_gpu": cfg.batch,
             "n_q_heads": cfg.n_q_heads, "n_kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim,
@@ -489,7 +497,7 @@ def run_ours(args):
                                 "rope_append (gamma tokens) + decode_verify_kernel (causal split-K attention of "
                                 f"{cfg.gamma} new tokens per sequence + merge)" if cfg.gamma > 1 else
                                 "decode_q8_kernel, fused step (RoPE + quantised append + split-K attention over "
-                                "INT8 codes and the bf16 window + merge)" if cfg.int8 else
+                                f"INT{cfg.code_bits} codes and the bf16 window + merge)" if cfg.int8 else
                                 "decode_mma_kernel, fused step (RoPE + append + split-K attention + merge)"
                                 if mma_path else "rope_append + decode_split_kernel (fused-step call)"),
                      "bound": "tensor" if prefill else "hbm",
@@ -545,7 +553,7 @@ def oracle_step_seconds(inp):
         from oracle import quant
         quant.decode_step_q8(inp.q, inp.k_new, inp.v_new, inp.positions, inp.k_cache, inp.v_cache, inp.k_scale,
                              inp.v_scale, inp.k_win, inp.v_win, cfg.window, inp.block_table, bs,
-                             rope_base=cfg.rope_base)
+                             rope_base=cfg.rope_base, bits=cfg.code_bits)
     else:
         odecode.decode_step(inp.q, inp.k_new, inp.v_new, inp.positions, inp.k_cache, inp.v_cache, cfg.dtype,
                             inp.block_table, bs, rope_base=cfg.rope_base)

@@ -128,38 +128,15 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 
 // One 16-token slice of an INT8 stage for one warp; `mult[j]` turns the raw score of owned
 // head 2*(lane%4)+j into log2 units. CHECK: tokens at or past `valid` get probability 0 (the
-// codes are finite whatever the bytes, so nothing needs clearing).
-template <int D, bool CHECK, int BITS = 8>
+// codes are finite whatever the bytes, so nothing needs clearing). The score sum runs as two
+// independent mma chains (the two 16-dim slices of each 32-byte chunk) added at the end.
+template <int D, bool CHECK>
 __device__ __forceinline__ void q8_step(MmaWarpState<D>& st, const uint32_t (&qh)[D / 16][2], const float (&mult)[2],
                                         uint32_t k_base, uint32_t v_base, int t0, int valid, int lane) {
-  constexpr int RB = D * BITS / 8;
+  constexpr int RB = D;
   const int mat = lane >> 3;
   const int r = t0 + (lane & 7) + ((mat & 1) << 3);  // matrices: tokens 0-7 / 8-15 of chunk 2cc, then 2cc+1
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
-  if constexpr (BITS == 4) {
-    // a 16-byte chunk c holds 32 dims: lane gets dims 32c + 8t .. +7 of rows g / g+8, nibble i = dim 8t + i;
-    // slice 2c takes dims (8t, 8t+4) as k = (2t, 2t+1) and (8t+1, 8t+5) as (2t+8, 2t+9), slice 2c+1 the rest
-#pragma unroll
-    for (int cc = 0; cc < RB / 32; ++cc) {
-      uint32_t w[4], a[4];
-      ldsm_x4(k_base + swz8<RB>(r, 2 * cc + (mat >> 1)), w);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t wa = w[2 * h], wb = w[2 * h + 1], wa8 = wa >> 8, wb8 = wb >> 8;
-        const int c = 2 * cc + h;
-        a[0] = nib04_to_f16(wa);
-        a[1] = nib04_to_f16(wb);
-        a[2] = nib15_to_f16(wa);
-        a[3] = nib15_to_f16(wb);
-        mma_f16(s, a, qh[2 * c][0], qh[2 * c][1]);
-        a[0] = nib04_to_f16(wa8);
-        a[1] = nib04_to_f16(wb8);
-        a[2] = nib15_to_f16(wa8);
-        a[3] = nib15_to_f16(wb8);
-        mma_f16(s, a, qh[2 * c + 1][0], qh[2 * c + 1][1]);
-      }
-    }
-  } else {
+  float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int cc = 0; cc < D / 32; ++cc) {
     uint32_t w[4], a[4];
@@ -169,9 +146,10 @@ __device__ __forceinline__ void q8_step(MmaWarpState<D>& st, const uint32_t (&qh
     mma_f16(s, a, qh[2 * cc][0], qh[2 * cc][1]);
     s8x4_to_f16_even_odd(w[2], a[0], a[2]);
     s8x4_to_f16_even_odd(w[3], a[1], a[3]);
-    mma_f16(s, a, qh[2 * cc + 1][0], qh[2 * cc + 1][1]);
+    mma_f16(s2, a, qh[2 * cc + 1][0], qh[2 * cc + 1][1]);
   }
-  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) s[i] += s2[i];
   const int ta = t0 + (lane >> 2), tb = ta + 8;
   float x[2][2];
 #pragma unroll
@@ -216,31 +194,6 @@ __device__ __forceinline__ void q8_step(MmaWarpState<D>& st, const uint32_t (&qh
   }
   const uint32_t b0 = movmatrix_trans(pack_f16x2(p[0][0], p[1][0]));
   const uint32_t b1 = movmatrix_trans(pack_f16x2(p[0][1], p[1][1]));
-  if constexpr (BITS == 4) {
-    // ldmatrix.trans gives lane (g, t) the 16-bit column g (dims 32c + 4g .. +3) of tokens 2t, 2t+1
-    // (and +8): fragment rows g / g+8 of sub-tile s are dims 32c + 4g + 2s / + 2s + 1
-#pragma unroll
-    for (int cc = 0; cc < RB / 32; ++cc) {
-      uint32_t w[4], a[4];
-      ldsm_x4_trans(v_base + swz8<RB>(r, 2 * cc + (mat >> 1)), w);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t ra = w[2 * h], rb = w[2 * h + 1], ra8 = ra >> 8, rb8 = rb >> 8;
-        const int c = 2 * cc + h;
-        a[0] = nib04_to_f16(ra);
-        a[1] = nib15_to_f16(ra);
-        a[2] = nib04_to_f16(rb);
-        a[3] = nib15_to_f16(rb);
-        mma_f16(st.o[2 * c], a, b0, b1);
-        a[0] = nib04_to_f16(ra8);
-        a[1] = nib15_to_f16(ra8);
-        a[2] = nib04_to_f16(rb8);
-        a[3] = nib15_to_f16(rb8);
-        mma_f16(st.o[2 * c + 1], a, b0, b1);
-      }
-    }
-    return;
-  }
 #pragma unroll
   for (int cc = 0; cc < D / 32; ++cc) {
     uint32_t w[4], a[4];
@@ -251,6 +204,120 @@ __device__ __forceinline__ void q8_step(MmaWarpState<D>& st, const uint32_t (&qh
     s8x4_to_f16_even_odd(w[2], a[0], a[1]);
     s8x4_to_f16_even_odd(w[3], a[2], a[3]);
     mma_f16(st.o[2 * cc + 1], a, b0, b1);
+  }
+}
+
+// INT4 (64-byte rows, 64-byte swizzle), two 16-token slices at once (tokens t0 .. t0 + 31 of the
+// stage): the two score chains are independent and interleave, one softmax update covers 32
+// tokens (at most one rescale), and each output fragment takes both slices' P.
+// Fragment orders: a 16-byte chunk c holds 32 dims. For the scores ldmatrix gives lane (g, t)
+// dims 32c + 8t .. +7 of rows g / g+8 (nibble i = dim 8t + i); 16-dim slice 2c takes dims
+// (8t, 8t+4) as k = (2t, 2t+1) and (8t+1, 8t+5) as (2t+8, 2t+9), slice 2c+1 the same after a
+// shift by 8 bits (dims 8t+2, 8t+6 and 8t+3, 8t+7); q is packed to match. For the output
+// ldmatrix.trans gives lane (g, t) the 16-bit column g (dims 32c + 4g .. +3) of tokens 2t, 2t+1
+// (and +8): fragment rows g / g+8 of sub-tile s are dims 32c + 4g + 2s / + 2s + 1.
+template <int D, bool CHECK>
+__device__ __forceinline__ void q4_step32(MmaWarpState<D>& st, const uint32_t (&qh)[D / 16][2], const float (&mult)[2],
+                                          uint32_t k_base, uint32_t v_base, int t0, int valid, int lane) {
+  constexpr int RB = D / 2;
+  constexpr uint32_t kSlice = 16 * RB;  // 16 rows further down the tile (same swizzle phase)
+  const int mat = lane >> 3;
+  const int r = t0 + (lane & 7) + ((mat & 1) << 3);
+  float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+  for (int cc = 0; cc < RB / 32; ++cc) {
+    uint32_t w[2][4];
+    const uint32_t off = swz8<RB>(r, 2 * cc + (mat >> 1));
+    ldsm_x4(k_base + off, w[0]);
+    ldsm_x4(k_base + off + kSlice, w[1]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = 2 * cc + h;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t wa = w[u][2 * h], wb = w[u][2 * h + 1];
+        const uint32_t a[4] = {nib04_to_f16(wa), nib04_to_f16(wb), nib15_to_f16(wa), nib15_to_f16(wb)};
+        mma_f16(s[u], a, qh[2 * c][0], qh[2 * c][1]);
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t wa8 = w[u][2 * h] >> 8, wb8 = w[u][2 * h + 1] >> 8;
+        const uint32_t a[4] = {nib04_to_f16(wa8), nib04_to_f16(wb8), nib15_to_f16(wa8), nib15_to_f16(wb8)};
+        mma_f16(s[u], a, qh[2 * c + 1][0], qh[2 * c + 1][1]);
+      }
+    }
+  }
+  // x[j][k]: head 2(lane%4)+j at token t0 + lane/4 + 8k
+  const int ta = t0 + (lane >> 2);
+  float x[2][4];
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      x[j][k] = (!CHECK || ta + 8 * k < valid) ? s[k >> 1][2 * (k & 1) + j] * mult[j] : -INFINITY;
+  float mnew[2];
+  bool grow = false;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float mx = fmaxf(fmaxf(x[j][0], x[j][1]), fmaxf(x[j][2], x[j][3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    mnew[j] = fmaxf(st.m[j], mx);
+    grow |= mnew[j] > st.m[j];
+  }
+  if (__any_sync(0xffffffffu, grow)) {
+    float alpha[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      alpha[j] = mnew[j] > st.m[j] ? exp2f(st.m[j] - mnew[j]) : 1.f;
+      st.l[j] *= alpha[j];
+      st.m[j] = mnew[j];
+    }
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      st.o[i][0] *= alpha[0];
+      st.o[i][1] *= alpha[1];
+      st.o[i][2] *= alpha[0];
+      st.o[i][3] *= alpha[1];
+    }
+  }
+  float p[2][4];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float mref = st.m[j] == -INFINITY ? 0.f : st.m[j];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) p[j][k] = exp2f(x[j][k] - mref);
+    st.l[j] += (p[j][0] + p[j][1]) + (p[j][2] + p[j][3]);
+  }
+  uint32_t pb[2][2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    pb[u][0] = movmatrix_trans(pack_f16x2(p[0][2 * u], p[1][2 * u]));
+    pb[u][1] = movmatrix_trans(pack_f16x2(p[0][2 * u + 1], p[1][2 * u + 1]));
+  }
+#pragma unroll
+  for (int cc = 0; cc < RB / 32; ++cc) {
+    uint32_t w[2][4];
+    const uint32_t off = swz8<RB>(r, 2 * cc + (mat >> 1));
+    ldsm_x4_trans(v_base + off, w[0]);
+    ldsm_x4_trans(v_base + off + kSlice, w[1]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = 2 * cc + h;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t ra = w[u][2 * h], rb = w[u][2 * h + 1];
+        const uint32_t a[4] = {nib04_to_f16(ra), nib15_to_f16(ra), nib04_to_f16(rb), nib15_to_f16(rb)};
+        mma_f16(st.o[2 * c], a, pb[u][0], pb[u][1]);
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const uint32_t ra8 = w[u][2 * h] >> 8, rb8 = w[u][2 * h + 1] >> 8;
+        const uint32_t a[4] = {nib04_to_f16(ra8), nib15_to_f16(ra8), nib04_to_f16(rb8), nib15_to_f16(rb8)};
+        mma_f16(st.o[2 * c + 1], a, pb[u][0], pb[u][1]);
+      }
+    }
   }
 }
 
@@ -667,13 +734,20 @@ __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_MMA_CTAS_PER_SM)
       }
       const uint32_t k_base = smem_addr(smem + s * C::kStageBytes), v_base = k_base + C::kTileBytes;
       const int valid = min(C::kTile, end - (start + it * C::kTile));
+      if constexpr (BITS == 4 && C::kWarpTokens == 32) {
+        const int t0 = warp * 32;
+        if (valid == C::kTile)
+          q4_step32<D, false>(st, qh, mult, k_base, v_base, t0, valid, lane);
+        else if (t0 < valid)
+          q4_step32<D, true>(st, qh, mult, k_base, v_base, t0, valid, lane);
+      } else
 #pragma unroll
       for (int step = 0; step < C::kSteps; ++step) {
         const int t0 = warp * C::kWarpTokens + step * 16;
         if (valid == C::kTile)
-          q8_step<D, false, BITS>(st, qh, mult, k_base, v_base, t0, valid, lane);
+          q8_step<D, false>(st, qh, mult, k_base, v_base, t0, valid, lane);
         else if (t0 < valid)
-          q8_step<D, true, BITS>(st, qh, mult, k_base, v_base, t0, valid, lane);
+          q8_step<D, true>(st, qh, mult, k_base, v_base, t0, valid, lane);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);

@@ -235,8 +235,12 @@ def rra_decode_step_paged(q, k_new, v_new, positions, q_out, k_pool, v_pool, blo
 
 
 # --------------------------------------------------------------------------- INT8 KV cache
-def _q8_layout(codes, block_table):
-    """(block_table columns, block_size, num_blocks, max_len) of an INT8 code cache."""
+def _q8_layout(codes, block_table, D: int, bits: int):
+    """(block_table columns, block_size, num_blocks, max_len) of an INT8 / INT4 code cache, whose
+    rows must hold D * bits / 8 bytes (one code per byte, or two)."""
+    if codes.shape[-1] * codes.element_size() != D * bits // 8:
+        raise ValueError(f"a {bits}-bit code cache of head dim {D} has rows of {D * bits // 8} bytes, "
+                         f"got {codes.shape[-1] * codes.element_size()}")
     if block_table is not None:
         return block_table.shape[1], codes.shape[1], codes.shape[0], 0
     return 0, 0, 0, codes.shape[2]
@@ -265,7 +269,7 @@ def rra_rope_append_q8(q, k_new, v_new, positions, q_out, k_codes, v_codes, k_sc
     B, Hq, D = q.shape
     Hkv = k_new.shape[1]
     window = k_win.shape[2] if k_win is not None else 0
-    mbps, bs, nblk, max_len = _q8_layout(k_codes, block_table)
+    mbps, bs, nblk, max_len = _q8_layout(k_codes, block_table, D, bits)
     name, fn = _qfn("rra_rope_append_q8", bits)
     st = fn(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q_out), _ptr(k_codes),
                                   _ptr(v_codes), _ptr(k_scale), _ptr(v_scale), _ptr(k_win), _ptr(v_win), window,
@@ -281,7 +285,7 @@ def rra_decode_attn_q8(q_rot, k_codes, v_codes, k_scale, v_scale, seq_lens, out,
     B, Hq, D = q_rot.shape
     Hkv = k_codes.shape[2] if block_table is not None else k_codes.shape[1]
     window = k_win.shape[2] if k_win is not None else 0
-    mbps, bs, nblk, max_len = _q8_layout(k_codes, block_table)
+    mbps, bs, nblk, max_len = _q8_layout(k_codes, block_table, D, bits)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     name, fn = _qfn("rra_decode_attn_q8", bits)
     st = fn(_ptr(q_rot), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale),
@@ -299,7 +303,7 @@ def rra_decode_step_q8(q, k_new, v_new, positions, q_out, k_codes, v_codes, k_sc
     B, Hq, D = q.shape
     Hkv = k_new.shape[1]
     window = k_win.shape[2] if k_win is not None else 0
-    mbps, bs, nblk, max_len = _q8_layout(k_codes, block_table)
+    mbps, bs, nblk, max_len = _q8_layout(k_codes, block_table, D, bits)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     name, fn = _qfn("rra_decode_step_q8", bits)
     st = fn(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(positions), _ptr(q_out), _ptr(k_codes),

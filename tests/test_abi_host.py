@@ -182,3 +182,16 @@ def test_prefill_and_verify_argument_checks(rra):
     # (q, kc, vc, table, mbps, pos, bs, nblk, max_len, out, B, gamma, Hq, Hkv, D, scale, splits, ws, ws_bytes, err, st)
     assert v(P, P, P, P, 64, P, 16, 100, 0, P, 1, 4, 32, 8, 128, 0.0, 8, None, 0, None, None) == RRA_EWORKSPACE
     assert v(P, P, P, P, 64, P, 16, 100, 0, P, 1, 20, 32, 8, 128, 0.0, 0, None, 0, None, None) == RRA_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("bits,width,dtype,ok", [(8, 128, torch.int8, True), (4, 64, torch.uint8, True),
+                                                 (4, 128, torch.int8, False), (8, 64, torch.uint8, False)])
+def test_binding_checks_the_code_row_width(rra, bits, width, dtype, ok):
+    """A code cache whose rows do not hold D * bits / 8 bytes is refused by the binding."""
+    codes = torch.zeros(4, 16, 2, width, dtype=dtype)
+    table = torch.zeros(1, 4, dtype=torch.int32)
+    if ok:
+        assert rra._q8_layout(codes, table, 128, bits) == (4, 16, 4, 0)
+    else:
+        with pytest.raises(ValueError):
+            rra._q8_layout(codes, table, 128, bits)

@@ -72,3 +72,24 @@ def test_reduced_inputs_structure(name):
     unused = np.setdiff1d(np.arange(cfg.num_blocks), owned)
     if unused.size:
         assert not _finite(a.k_cache[unused], cfg.dtype).any()
+
+
+@pytest.mark.parametrize("name", ["batched_paged_int8", "batched_paged_int4", "long_context_int4"])
+def test_bench_device_workload_matches_the_code_width(name):
+    """The bench's device-drawn caches have the storage of the numpy recipe: one INT8 code per
+    byte, or two INT4 codes per byte with the even dimension in the low nibble, and the recipe's
+    scales."""
+    import torch
+
+    import bench
+    from oracle import quant
+    cfg = reduced(CONFIGS[name], 64, batch=2)
+    w, _ = bench.device_workload(cfg, 0, torch.device("cpu"))
+    kc = w["k_cache"]
+    assert kc.dtype == (torch.int8 if cfg.code_bits == 8 else torch.uint8)
+    assert kc.shape[-1] == cfg.head_dim * cfg.code_bits // 8
+    codes = quant.load_codes(kc.numpy(), cfg.code_bits)
+    m = (1 << (cfg.code_bits - 1)) - 1
+    assert codes.min() >= -m and codes.max() <= m and len(np.unique(codes)) > m
+    ref = make_inputs(cfg)
+    assert np.array_equal(w["k_scale"].numpy(), ref.k_scale) and np.array_equal(w["v_scale"].numpy(), ref.v_scale)
