@@ -22,7 +22,7 @@ The page gives no formula, so this module takes the plainest reading that fits i
   [0, L - W) from the INT8 cache and tokens [max(0, L - W), L) from the ring, so a token is
   read at high precision while it is among the W most recent and quantised afterwards.
 
-INT4 ("或INT4") takes the same reading with 4-bit codes: ``clamp(round_half_even(x / s_h), -7, 7)``
+INT4, which the passage names as the alternative to INT8, takes the same reading with 4-bit codes: ``clamp(round_half_even(x / s_h), -7, 7)``
 (-8 is never produced), two codes per byte, the even dimension in the low nibble and the odd one
 in the high nibble, each as a 4-bit two's complement; the caches hold D/2 bytes per token and
 head.
