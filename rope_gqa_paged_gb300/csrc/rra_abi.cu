@@ -1004,6 +1004,16 @@ int rra_prefill_attn(const void* q_rot, const void* k_cache, const void* v_cache
   const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
   a.scale_log2 = sc * 1.4426950408889634f;
   a.err = err_flag;
+  if (D == 128) {  // the tcgen05 kernel: q_rot [B*T, Hq, D] read as 128-token boxes of one head
+    CUtensorMap qm{};
+    const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(Hq), cuuint64_t(B) * T};
+    const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(Hq) * D * 2};
+    const cuuint32_t box[3] = {64u, 1u, 128u};
+    st = encode_map(&qm, q_rot, 3, dims, strides, box, RRA_BF16, true);
+    if (st != RRA_OK) return st;
+    return finish_decode(
+        rra::launch_prefill_tc(a, qm, km, vm, block_table != nullptr, static_cast<cudaStream_t>(stream)));
+  }
   return finish_decode(rra::launch_prefill(a, km, vm, block_table != nullptr, static_cast<cudaStream_t>(stream)));
 }
 

@@ -135,6 +135,10 @@ cudaError_t launch_decode_verify(const DecodeArgs& a, const CUtensorMap& k_map, 
 // first one's position); 64 query rows (a.hpc heads x 64 / a.hpc tokens) per CTA.
 cudaError_t launch_prefill(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map, bool paged,
                            cudaStream_t stream);
+// Prefill on the tcgen05 tensor cores (head_dim 128): 128 prompt tokens of one query head per
+// CTA; q_map covers q_rot as {D, Hq, B*T} with boxes of 64 dims x 1 head x 128 tokens.
+cudaError_t launch_prefill_tc(const DecodeArgs& a, const CUtensorMap& q_map, const CUtensorMap& k_map,
+                              const CUtensorMap& v_map, bool paged, cudaStream_t stream);
 // Tokens per stage of the INT8 (bits 8) / INT4 (bits 4) decode kernel.
 inline int decode_q8_tile_tokens(int D, int bits = 8) { return RRA_Q8_STAGE_BYTES / 2 / (D * bits / 8); }
 // INT8 caches: attention only (a.seq_lens) or the fused step (a.positions, a.k_new, ...).

@@ -1,0 +1,104 @@
+// Fifth-generation tensor core (tcgen05) primitives for sm_103a, as inline PTX: Tensor Memory
+// allocation, the single-thread MMA with operands in shared memory (by matrix descriptor) and
+// the accumulator in Tensor Memory, its completion through an mbarrier, and the warp loads and
+// stores between Tensor Memory and registers.
+//
+// Tensor Memory (TMEM) is 128 lanes x 512 columns of 32-bit cells per SM; an address is
+// (lane << 16) | column. With M = 128 and one CTA, row i of an MMA accumulator sits in lane i,
+// column j of the accumulator in column base + j, and warp w of the CTA reads and writes lanes
+// 32 (w % 4) .. + 31 only.
+#pragma once
+
+#include <cstdint>
+
+#include "rra_device.cuh"
+
+namespace rra {
+namespace tc {
+
+// ---- Tensor Memory allocation (one warp, all lanes) --------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// ---- ordering between tcgen05 operations and thread synchronisation ----------------------
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// generic-proxy writes to shared memory made visible to the tensor core's (async proxy) reads
+__device__ __forceinline__ void fence_smem_to_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// ---- descriptors ---------------------------------------------------------------------------
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand: start address, leading and
+// stride byte offsets (all >> 4), the fixed version bits 46..48 = 0b001, base offset 0 (every
+// operand tile starts on a 1024-byte boundary), swizzle mode 2 (128 bytes) in bits 61..63.
+// K-major operands (rows of 64 bf16 along K): 8-row groups 1024 bytes apart; an MMA's K = 16
+// elements are 32 bytes of one swizzled row, selected by advancing the start address.
+// MN-major operands (rows of 64 bf16 along M or N, one row per K index): 8-row groups along K
+// 1024 bytes apart, one 64-wide atom along M/N per MMA.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// Instruction descriptor of kind::f16: f32 accumulator (bits 4..5 = 1), bf16 A and B (bits 7..9
+// and 10..12 = 1), A K-major (bit 15 = 0), B K-major or MN-major (bit 16), N >> 3 in bits 17..22,
+// M >> 4 in bits 24..28, dense.
+constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---- MMA -------------------------------------------------------------------------------------
+// D[tmem] (+)= A[smem] . B[smem]; issued by one thread; `accumulate` 0 overwrites D.
+__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives once on `bar` when every tcgen05 operation this thread issued before has completed.
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// ---- Tensor Memory <-> registers (whole warp; lane i <-> TMEM lane base + i) ---------------
+#define RRA_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
+                  "=r"(r[i + 6]), "=r"(r[i + 7])
+#define RRA_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
+                  "r"(r[i + 6]), "r"(r[i + 7])
+
+// 32 consecutive columns of this lane's row.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : RRA_R8(0), RRA_R8(8), RRA_R8(16), RRA_R8(24)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      RRA_W8(0), RRA_W8(8), RRA_W8(16), RRA_W8(24)
+      : "memory");
+}
+#undef RRA_R8
+#undef RRA_W8
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+}  // namespace tc
+}  // namespace rra

@@ -55,8 +55,8 @@ def _cfg(layout, prefix, T, batch=2, block_size=16, head_dim=128, hq=32, hkv=8):
 
 
 @pytest.mark.parametrize("layout,block_size", [("contiguous", 0), ("paged", 8), ("paged", 16), ("paged", 256)])
-@pytest.mark.parametrize("prefix,T", [(0, 1), (0, 2), (0, 17), (0, 64), (0, 65), (0, 300), (37, 5), (100, 130),
-                                      (1000, 64)])
+@pytest.mark.parametrize("prefix,T", [(0, 1), (0, 2), (0, 17), (0, 64), (0, 65), (0, 257), (0, 300), (37, 5),
+                                      (100, 130), (200, 200), (1000, 64)])
 def test_prefill_lengths_and_prefix(layout, block_size, prefix, T):
     inp = _inputs(_cfg(layout, prefix, T, block_size=block_size or 16), seed=prefix + T)
     _check(inp, H.run_gpu_prefill(inp))
