@@ -15,8 +15,8 @@
 //   softmax           warpgroup k, one row per thread: the S row from TMEM (read twice: the
 //                     max, then the probabilities), causal mask on diagonal tiles, running max,
 //                     P in bf16 to shared memory in the K-major 128-byte-swizzled layout
-//   O_k += P_k V_j    16 MMAs (M 128, N 64, K 16; V as an MN-major operand) into TMEM columns
-//                     [256 + 128k, 384 + 128k)
+//   O_k += P_k V_j    8 MMAs (M 128, N 128, K 16; V as an MN-major operand: its two 64-dim
+//                     halves are the N atoms) into TMEM columns [256 + 128k, 384 + 128k)
 // One lane of the last warp issues every MMA in the order PV_0, S_0 (next tile), PV_1, S_1 (next
 // tile), so the tensor cores work on one query tile while the other tile's softmax runs; the warp
 // before it is the TMA producer. The running max only moves (and O and the sum are rescaled in
@@ -46,7 +46,7 @@ constexpr float kRescaleLog2 = 8.f;           // move the running max only when 
 constexpr int kPreciseKeys = 256;             // blocks whose first row sees fewer keys split P
 
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, 128, false);   // Q (K-major) . K^T (K-major)
-constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, 64, true);    // P (K-major) . V (MN-major)
+constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, 128, true);   // P (K-major) . V (MN-major)
 
 template <int NQ>
 struct Cfg {
@@ -92,6 +92,53 @@ __device__ __forceinline__ void ld_s64(uint32_t taddr, float (&s)[64]) {
     s[i] = __uint_as_float(v[0][i]);
     s[32 + i] = __uint_as_float(v[1][i]);
   }
+}
+
+// Pass 1: the max of this row's visible S columns (raw scores). MASK: only columns < nvis count.
+template <bool MASK>
+__device__ __forceinline__ float row_max(uint32_t s_col, int nvis) {
+  float mx[8];  // independent chains
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    float s[64];
+    ld_s64(s_col + 64 * c, s);
+#pragma unroll
+    for (int i = 0; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], (!MASK || 64 * c + i < nvis) ? s[i] : -INFINITY);
+  }
+  return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+}
+
+// Pass 2 / 3: 2^(S * scale_log2 - mref) of the row into its P row (K-major, swizzled), as bf16
+// (LO false; returns the row's sum) or as the bf16 rounding of what that leaves (LO true).
+template <bool MASK, bool LO>
+__device__ __forceinline__ float row_probs(uint32_t s_col, uint8_t* p_smem, int r, int nvis, float sl, float mref) {
+  float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    float s[64];
+    ld_s64(s_col + 64 * c, s);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 8 * q + 2 * e;
+        const float e0 = ex2((!MASK || 64 * c + i < nvis) ? fmaf(s[i], sl, -mref) : -INFINITY);
+        const float e1 = ex2((!MASK || 64 * c + i + 1 < nvis) ? fmaf(s[i + 1], sl, -mref) : -INFINITY);
+        const uint32_t hi = pack_bf16x2(e0, e1);
+        if constexpr (LO) {
+          w[e] = pack_bf16x2(e0 - __uint_as_float(hi << 16), e1 - __uint_as_float(hi & 0xffff0000u));
+        } else {
+          ls[e] += e0 + e1;
+          w[e] = hi;
+        }
+      }
+      *reinterpret_cast<uint4*>(p_smem + tile_chunk_offset(r, 8 * c + q)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
 
 template <int NQ, bool PAGED>
@@ -254,11 +301,8 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kKeys / 16; ++kk) {
               const uint64_t pd = tc::sw128_desc(pk + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 1024, 1024);
-#pragma unroll
-              for (int nh = 0; nh < 2; ++nh)
-                tc::mma_bf16_ss(tmem + kColO + 128 * k + 64 * nh, pd,
-                                tc::sw128_desc(v_base + nh * kHalfBytes + kk * 2048, 1024, 1024), kIdescPV,
-                                (j > 0 || u > 0 || kk > 0) ? 1u : 0u);
+              tc::mma_bf16_ss(tmem + kColO + 128 * k, pd, tc::sw128_desc(v_base + kk * 2048, kHalfBytes, 1024),
+                              kIdescPV, (j > 0 || u > 0 || kk > 0) ? 1u : 0u);
             }
             tc::commit(&o_done[k]);
           }
@@ -293,15 +337,7 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
       tc::fence_after_sync();
       const bool masked = (j + 1) * kKeys - 1 > lim_min;
       const int nvis = masked ? min(max(lim - j * kKeys + 1, 0), kKeys) : kKeys;
-      // pass 1: the row's max over its visible keys
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float s[64];
-        ld_s64(s_col + 64 * c, s);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) mx = fmaxf(mx, (!masked || 64 * c + i < nvis) ? s[i] : -INFINITY);
-      }
+      const float mx = masked ? row_max<true>(s_col, nvis) : row_max<false>(s_col, nvis);
       const float m_new = fmaxf(m_use, mx * sl);
       const bool rescale = m_new > m_use + kRescaleLog2;  // also the first finite max
       float alpha = 1.f;
@@ -350,29 +386,13 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
           }
         }
         // pass 2 (and 3): probabilities into the P tile -- the bf16 part, then its remainder
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float s[64];
-          ld_s64(s_col + 64 * c, s);
-          float ls = 0.f;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int i = 8 * q + 2 * e;
-              const float x0 = (!masked || 64 * c + i < nvis) ? fmaf(s[i], sl, -mref) : -INFINITY;
-              const float x1 = (!masked || 64 * c + i + 1 < nvis) ? fmaf(s[i + 1], sl, -mref) : -INFINITY;
-              const float e0 = ex2(x0), e1 = ex2(x1);
-              ls += e0 + e1;
-              const uint32_t hi = pack_bf16x2(e0, e1);
-              w[e] = u == 0 ? hi
-                            : pack_bf16x2(e0 - __uint_as_float(hi << 16), e1 - __uint_as_float(hi & 0xffff0000u));
-            }
-            *reinterpret_cast<uint4*>(p_smem + tile_chunk_offset(r, 8 * c + q)) = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-          if (u == 0) l += ls;
-        }
+        if (u == 0)
+          l += masked ? row_probs<true, false>(s_col, p_smem, r, nvis, sl, mref)
+                      : row_probs<false, false>(s_col, p_smem, r, nvis, sl, mref);
+        else if (masked)
+          row_probs<true, true>(s_col, p_smem, r, nvis, sl, mref);
+        else
+          row_probs<false, true>(s_col, p_smem, r, nvis, sl, mref);
         tc::fence_smem_to_async();
         tc::fence_before_sync();
         mbar_arrive(&p_full[k]);

@@ -41,7 +41,7 @@ __device__ __forceinline__ void fence_smem_to_async() { asm volatile("fence.prox
 // K-major operands (rows of 64 bf16 along K): 8-row groups 1024 bytes apart; an MMA's K = 16
 // elements are 32 bytes of one swizzled row, selected by advancing the start address.
 // MN-major operands (rows of 64 bf16 along M or N, one row per K index): 8-row groups along K
-// 1024 bytes apart, one 64-wide atom along M/N per MMA.
+// 1024 bytes apart (the stride byte offset), 64-wide atoms along M or N `lbo` bytes apart.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
