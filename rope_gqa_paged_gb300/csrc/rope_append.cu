@@ -28,6 +28,7 @@ namespace {
 
 constexpr int kPairsPerCta = 16;
 constexpr int kRopeThreads = 128;
+constexpr int kRowsKernelMin = 256;  // token rows from which one CTA per row beats splitting each row
 
 template <typename T, bool Q8>
 __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArgs a) {
@@ -163,6 +164,114 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
   }
 }
 
+// Many new tokens (prefill, speculative verify), bf16, every row 16-byte aligned: one CTA per
+// token row, 16-byte vectors. The rotation and rounding are those of rope_append_kernel (the
+// same sine/cosine split and error-free products), so both kernels write the same bits.
+__global__ void __launch_bounds__(kRopeThreads) rope_append_rows_kernel(const RopeArgs a) {
+  __shared__ float cs[4][kMaxHeadDim / 2];
+  __shared__ size_t row_info[2];
+  __shared__ int append_ok;
+  const int gam = max(a.gamma, 1);
+  const int v = blockIdx.x;
+  const int b = v / gam, j_new = v - b * gam;
+  const int D = a.D, half = a.D / 2;
+  const int pos = a.positions[b] + j_new;
+  const bool paged = a.block_table != nullptr;
+  const long long cap = paged ? (static_cast<long long>(a.max_blocks_per_seq) << a.log2_bs) : a.max_len;
+  if (pos < 0 || pos >= cap) {
+    if (threadIdx.x == 0) flag_error(a.err, RRA_ERR_POSITION);
+    return;
+  }
+  for (int i = threadIdx.x; i < half; i += blockDim.x) {
+    double sn, cn;  // angle / pi = pos * (theta_i / pi): sincospi reduces its argument exactly
+    sincospi(static_cast<double>(pos) * a.inv_freq[i], &sn, &cn);
+    const float ch = static_cast<float>(cn), sh = static_cast<float>(sn);
+    cs[0][i] = ch;
+    cs[1][i] = static_cast<float>(cn - static_cast<double>(ch));
+    cs[2][i] = sh;
+    cs[3][i] = static_cast<float>(sn - static_cast<double>(sh));
+  }
+  if (threadIdx.x == kRopeThreads - 1) {  // where the token's K and V go
+    int ok = 1;
+    size_t row0 = 0, stride = 0;
+    if (paged) {
+      const int phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (pos >> a.log2_bs)];
+      if (phys < 0 || phys >= a.num_blocks) {
+        flag_error(a.err, RRA_ERR_BLOCK_ID);
+        ok = 0;
+      } else {
+        row0 = ((static_cast<size_t>(phys) << a.log2_bs) + (pos & ((1 << a.log2_bs) - 1))) * a.Hkv;
+        stride = 1;
+      }
+    } else {
+      row0 = static_cast<size_t>(b) * a.Hkv * a.max_len + pos;
+      stride = a.max_len;
+    }
+    row_info[0] = row0;
+    row_info[1] = stride;
+    append_ok = ok;
+  }
+  __syncthreads();
+  const size_t row0 = row_info[0], head_stride = row_info[1];
+  const bool append = append_ok != 0;
+  const bool inter = a.rope_style == 1;
+  const int heads = a.Hq + a.Hkv;
+  // a task is 8 dims: half-split pairs (i, i + D/2) for i in [8t, 8t + 8) (two vectors), or the
+  // interleaved pairs (2i, 2i + 1) for i in [4t, 4t + 4) (one vector)
+  const int per_head = inter ? D / 8 : half / 8;
+  auto pack8 = [](const float (&x)[8]) {
+    uint4 r;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 p = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+      w[e] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    return r;
+  };
+  for (int task = threadIdx.x; task < heads * per_head; task += blockDim.x) {
+    const int hh = task / per_head, t = task - hh * per_head;
+    const bool is_q = hh < a.Hq;
+    if (!is_q && !append) continue;
+    const __nv_bfloat16* src =
+        is_q ? static_cast<const __nv_bfloat16*>(a.q) + (static_cast<size_t>(v) * a.Hq + hh) * D
+             : static_cast<const __nv_bfloat16*>(a.k_new) + (static_cast<size_t>(v) * a.Hkv + hh - a.Hq) * D;
+    __nv_bfloat16* dst = is_q ? static_cast<__nv_bfloat16*>(a.q_out) + (static_cast<size_t>(v) * a.Hq + hh) * D
+                              : static_cast<__nv_bfloat16*>(a.k_cache) + (row0 + (hh - a.Hq) * head_stride) * D;
+    if (!inter) {
+      float xa[8], xb[8], oa[8], ob[8];
+      Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(src + 8 * t), xa);
+      Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(src + half + 8 * t), xb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int i = 8 * t + e;
+        oa[e] = rotate_diff(xa[e], xb[e], cs[0][i], cs[1][i], cs[2][i], cs[3][i]);   // a cos - b sin
+        ob[e] = rotate_diff(xb[e], -xa[e], cs[0][i], cs[1][i], cs[2][i], cs[3][i]);  // b cos + a sin
+      }
+      *reinterpret_cast<uint4*>(dst + 8 * t) = pack8(oa);
+      *reinterpret_cast<uint4*>(dst + half + 8 * t) = pack8(ob);
+    } else {
+      float x[8], o[8];
+      Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(src + 8 * t), x);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 4 * t + e;
+        o[2 * e] = rotate_diff(x[2 * e], x[2 * e + 1], cs[0][i], cs[1][i], cs[2][i], cs[3][i]);
+        o[2 * e + 1] = rotate_diff(x[2 * e + 1], -x[2 * e], cs[0][i], cs[1][i], cs[2][i], cs[3][i]);
+      }
+      *reinterpret_cast<uint4*>(dst + 8 * t) = pack8(o);
+    }
+  }
+  if (!append) return;
+  // V is stored unrotated
+  const uint4* vn = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.v_new) +
+                                                   static_cast<size_t>(v) * a.Hkv * D);
+  for (int task = threadIdx.x; task < a.Hkv * (D / 8); task += blockDim.x) {
+    const int g = task / (D / 8), t = task - g * (D / 8);
+    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.v_cache) + (row0 + g * head_stride) * D)[t] = vn[task];
+  }
+}
+
 // INT4 caches (bf16 q / k / v, head_dim 128): one CTA per sequence. The rotated k of every KV
 // head is rounded to bf16 into shared memory first, so that each thread can then pack the codes
 // of dims 2j and 2j+1 into byte j (the even one in the low nibble); v packs straight from v_new.
@@ -264,7 +373,14 @@ cudaError_t launch_rope_append_q4(const RopeArgs& a, cudaStream_t stream) {
 }
 
 cudaError_t launch_rope_append(const RopeArgs& a, rra_dtype dt, cudaStream_t stream) {
-  const dim3 grid(a.B * (a.gamma > 1 ? a.gamma : 1), (a.D / 2 + kPairsPerCta - 1) / kPairsPerCta);
+  const int rows = a.B * (a.gamma > 1 ? a.gamma : 1);
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  if (dt == RRA_BF16 && rows >= kRowsKernelMin && a.D % 16 == 0 && al16(a.q) && al16(a.k_new) && al16(a.v_new) && al16(a.q_out) &&
+      al16(a.k_cache) && al16(a.v_cache)) {
+    rope_append_rows_kernel<<<rows, kRopeThreads, 0, stream>>>(a);
+    return cudaGetLastError();
+  }
+  const dim3 grid(rows, (a.D / 2 + kPairsPerCta - 1) / kPairsPerCta);
   if (dt == RRA_BF16)
     rope_append_kernel<__nv_bfloat16, false><<<grid, kRopeThreads, 0, stream>>>(a);
   else
