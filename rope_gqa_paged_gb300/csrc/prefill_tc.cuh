@@ -12,9 +12,9 @@
 // shared memory serves NQ x 128 rows. Key tiles of 128 tokens stream through a three-slot ring
 // (K_0, V_0, K_1, V_1, ... by TMA with the 128-byte swizzle). For query tile k and key tile j:
 //   S_k = Q_k K_j^T   8 MMAs (M 128, N 128, K 16) into TMEM columns [128k, 128k + 128)
-//   softmax           warpgroup k, one row per thread: the S row from TMEM (read twice: the
-//                     max, then the probabilities), causal mask on diagonal tiles, running max,
-//                     P in bf16 to shared memory in the K-major 128-byte-swizzled layout
+//   softmax           warpgroup k, one row per thread: the S row from TMEM into registers (one
+//                     wait), causal mask on diagonal tiles, running max, P in bf16 to shared
+//                     memory in the K-major 128-byte-swizzled layout
 //   O_k += P_k V_j    8 MMAs (M 128, N 128, K 16; V as an MN-major operand: its two 64-dim
 //                     halves are the N atoms) into TMEM columns [256 + 128k, 384 + 128k)
 // One lane of the last warp issues every MMA in the order PV_0, S_0 (next tile), PV_1, S_1 (next
@@ -81,62 +81,49 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x on the special-function 
   return y;
 }
 
-// 64 consecutive S columns of this thread's row (two 32-column loads, one wait).
-__device__ __forceinline__ void ld_s64(uint32_t taddr, float (&s)[64]) {
-  uint32_t v[2][32];
-  tc::tmem_ld32(taddr, v[0]);
-  tc::tmem_ld32(taddr + 32, v[1]);
+// The whole S row of this thread (128 columns: four 32-column loads, one wait).
+__device__ __forceinline__ void ld_row(uint32_t taddr, float (&s)[kKeys]) {
+  uint32_t v[kKeys / 32][32];
+#pragma unroll
+  for (int c = 0; c < kKeys / 32; ++c) tc::tmem_ld32(taddr + 32 * c, v[c]);
   tc::tmem_wait_ld();
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    s[i] = __uint_as_float(v[0][i]);
-    s[32 + i] = __uint_as_float(v[1][i]);
-  }
+  for (int c = 0; c < kKeys / 32; ++c)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(v[c][i]);
 }
 
-// Pass 1: the max of this row's visible S columns (raw scores). MASK: only columns < nvis count.
-template <bool MASK>
-__device__ __forceinline__ float row_max(uint32_t s_col, int nvis) {
+__device__ __forceinline__ float row_max(const float (&s)[kKeys]) {
   float mx[8];  // independent chains
 #pragma unroll
-  for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+  for (int i = 0; i < 8; ++i) mx[i] = s[i];
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    float s[64];
-    ld_s64(s_col + 64 * c, s);
-#pragma unroll
-    for (int i = 0; i < 64; ++i) mx[i & 7] = fmaxf(mx[i & 7], (!MASK || 64 * c + i < nvis) ? s[i] : -INFINITY);
-  }
+  for (int i = 8; i < kKeys; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
   return fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
 }
 
-// Pass 2 / 3: 2^(S * scale_log2 - mref) of the row into its P row (K-major, swizzled), as bf16
-// (LO false; returns the row's sum) or as the bf16 rounding of what that leaves (LO true).
-template <bool MASK, bool LO>
-__device__ __forceinline__ float row_probs(uint32_t s_col, uint8_t* p_smem, int r, int nvis, float sl, float mref) {
+// 2^(S * scale_log2 - mref) of the row into its P row (K-major, swizzled), as bf16 (LO false;
+// returns the row's sum) or as the bf16 rounding of what that leaves (LO true). Masked columns
+// hold -inf and give 0.
+template <bool LO>
+__device__ __forceinline__ float row_probs(const float (&s)[kKeys], uint8_t* p_smem, int r, float sl, float mref) {
   float ls[4] = {0.f, 0.f, 0.f, 0.f};  // independent chains
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    float s[64];
-    ld_s64(s_col + 64 * c, s);
+  for (int q = 0; q < kKeys / 8; ++q) {
+    uint32_t w[4];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = 8 * q + 2 * e;
-        const float e0 = ex2((!MASK || 64 * c + i < nvis) ? fmaf(s[i], sl, -mref) : -INFINITY);
-        const float e1 = ex2((!MASK || 64 * c + i + 1 < nvis) ? fmaf(s[i + 1], sl, -mref) : -INFINITY);
-        const uint32_t hi = pack_bf16x2(e0, e1);
-        if constexpr (LO) {
-          w[e] = pack_bf16x2(e0 - __uint_as_float(hi << 16), e1 - __uint_as_float(hi & 0xffff0000u));
-        } else {
-          ls[e] += e0 + e1;
-          w[e] = hi;
-        }
+    for (int e = 0; e < 4; ++e) {
+      const int i = 8 * q + 2 * e;
+      const float e0 = ex2(fmaf(s[i], sl, -mref)), e1 = ex2(fmaf(s[i + 1], sl, -mref));
+      const uint32_t hi = pack_bf16x2(e0, e1);
+      if constexpr (LO) {
+        w[e] = pack_bf16x2(e0 - __uint_as_float(hi << 16), e1 - __uint_as_float(hi & 0xffff0000u));
+      } else {
+        ls[e] += e0 + e1;
+        w[e] = hi;
       }
-      *reinterpret_cast<uint4*>(p_smem + tile_chunk_offset(r, 8 * c + q)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
+    *reinterpret_cast<uint4*>(p_smem + tile_chunk_offset(r, q)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
@@ -335,40 +322,39 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
         break;
       }
       tc::fence_after_sync();
-      const bool masked = (j + 1) * kKeys - 1 > lim_min;
-      const int nvis = masked ? min(max(lim - j * kKeys + 1, 0), kKeys) : kKeys;
-      const float mx = masked ? row_max<true>(s_col, nvis) : row_max<false>(s_col, nvis);
-      const float m_new = fmaxf(m_use, mx * sl);
-      const bool rescale = m_new > m_use + kRescaleLog2;  // also the first finite max
-      float alpha = 1.f;
-      if (rescale) {
-        alpha = ex2(m_use - m_new);
-        m_use = m_new;
-      }
-      const float mref = m_use == -INFINITY ? 0.f : m_use;
-      l *= alpha;
-      for (int u = 0; u < passes; ++u, ++pv) {
-        // the previous P.V pass of this tile has read the P buffer and O is stable
-        if (pv > 0) {
-          if (!warp_wait(&o_done[k], (pv - 1) & 1)) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-        }
-        if (u == 0 && j > 0 && __any_sync(0xffffffffu, rescale)) {  // warp-collective; alpha = 1 elsewhere
-#pragma unroll 1
-          for (int c = 0; c < kD / 32; ++c) {
-            uint32_t v[32];
-            tc::tmem_ld32(o_col + 32 * c, v);
-            tc::tmem_wait_ld();
+      const bool diag = (j + 1) * kKeys - 1 > lim_min;  // keys past some row's limit: mask them
+      const int nvis = lim - j * kKeys + 1;
+      auto load_s = [&](float (&sv)[kKeys]) {
+        ld_row(s_col, sv);
+        if (diag) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tc::tmem_st32(o_col + 32 * c, v);
-          }
-          tc::tmem_wait_st();
+          for (int i = 0; i < kKeys; ++i) sv[i] = i < nvis ? sv[i] : -INFINITY;
         }
-        if (k == 0 && u == 0 && j == n_tiles - 1 && last_valid < kKeys) {
+      };
+      // the previous P.V pass has read the P buffer and O is stable
+      auto wait_pv = [&]() -> bool {
+        if (pv == 0) return true;
+        if (!warp_wait(&o_done[k], (pv - 1) & 1)) return false;
+        tc::fence_after_sync();
+        return true;
+      };
+      float alpha = 1.f;
+      bool rescale = false;
+      {
+        float sv[kKeys];
+        load_s(sv);
+        const float m_new = fmaxf(m_use, row_max(sv) * sl);
+        rescale = m_new > m_use + kRescaleLog2;  // also the first finite max
+        if (rescale) {
+          alpha = ex2(m_use - m_new);
+          m_use = m_new;
+        }
+        const float mref = m_use == -INFINITY ? 0.f : m_use;
+        if (!wait_pv()) {
+          ok = false;
+          break;
+        }
+        if (k == 0 && j == n_tiles - 1 && last_valid < kKeys) {
           // keys past the end of the prompt: their V rows (stale or poisoned) become zeros so that
           // 0 * V stays 0 in the tensor core (query tile 0's P.V reads this V first)
           const int rv = 2 * j + 1;
@@ -385,17 +371,36 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
             }
           }
         }
-        // pass 2 (and 3): probabilities into the P tile -- the bf16 part, then its remainder
-        if (u == 0)
-          l += masked ? row_probs<true, false>(s_col, p_smem, r, nvis, sl, mref)
-                      : row_probs<false, false>(s_col, p_smem, r, nvis, sl, mref);
-        else if (masked)
-          row_probs<true, true>(s_col, p_smem, r, nvis, sl, mref);
-        else
-          row_probs<false, true>(s_col, p_smem, r, nvis, sl, mref);
+        l = l * alpha + row_probs<false>(sv, p_smem, r, sl, mref);  // the bf16 part of P
+      }
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {  // O rows whose max moved (warp-collective; alpha = 1 elsewhere)
+#pragma unroll 1
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t v[32];
+          tc::tmem_ld32(o_col + 32 * c, v);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tc::tmem_st32(o_col + 32 * c, v);
+        }
+        tc::tmem_wait_st();
+      }
+      tc::fence_smem_to_async();
+      tc::fence_before_sync();
+      mbar_arrive(&p_full[k]);
+      ++pv;
+      if (passes == 2) {  // short rows: the remainder of P in a second pass (S is still in TMEM)
+        if (!wait_pv()) {
+          ok = false;
+          break;
+        }
+        float sv[kKeys];
+        load_s(sv);
+        row_probs<true>(sv, p_smem, r, sl, m_use == -INFINITY ? 0.f : m_use);
         tc::fence_smem_to_async();
         tc::fence_before_sync();
         mbar_arrive(&p_full[k]);
+        ++pv;
       }
       if (!ok) break;
     }
