@@ -512,7 +512,9 @@ def run_ours(args):
                                                                        "both": round(eager_ms, 5)}},
         "step_timing": graph_note,
         "single_step_graph_ms": round(single_ms, 5),
-        "roofline": {"kernel": ("prefill_kernel (causal attention of the prompt, 64 query rows per CTA)" if prefill else
+        "roofline": {"kernel": (("prefill_tc_kernel (tcgen05: causal attention of the prompt, 128 tokens x 2 query heads per "
+                                 "CTA, S and O in Tensor Memory)" if cfg.head_dim == 128 else
+                                 "prefill_kernel (mma.sync: causal attention of the prompt, 64 query rows per CTA)") if prefill else
                                 "decode_verify_kernel (causal split-K attention of "
                                 f"{cfg.gamma} new tokens per sequence + merge; the append is a separate launch)"
                                 if cfg.gamma > 1 else
