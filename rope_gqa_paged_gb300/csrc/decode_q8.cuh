@@ -64,8 +64,7 @@ struct Q8Cfg {
   static constexpr int kOffTable = kOffBar + (2 * kStages + 1) * 8;
   static constexpr int kOffCs = kOffTable + kMmaTableEntries * 4;
   static constexpr int kOffQ = kOffCs + 4 * (D / 2) * 4;
-  static constexpr int kOffK = kOffQ + MmaCfg<D>::kMaxHeads * D * 2;  // the appended k (bf16), INT4 packing
-  static constexpr int kSmemBytes = 1024 + kOffK + D * 2;
+  static constexpr int kSmemBytes = 1024 + kOffQ + MmaCfg<D>::kMaxHeads * D * 2;
 };
 
 // Byte offset of 16-byte chunk c of row r in a tile of RB-byte rows written by TMA with the
@@ -370,6 +369,108 @@ __device__ __forceinline__ void q4_acc_to_bf16_layout(MmaWarpState<D>& st, float
     for (int k = 0; k < 4; ++k) st.o[i][k] = res[i][k];
 }
 
+// The fused step's append, by one warp: quantised k (rotated, rounded to bf16) and v into cache
+// slot pos of KV head g, and with a window their bf16 values into ring slot pos % window. Lane l
+// holds dims E l .. E l + E - 1 (E = D / 32) of k_new and v_new as bf16 pairs; a half-split
+// RoPE pair (i, i + D/2) sits in lanes l and l ^ 16. The rotation and the codes are those of the
+// append kernel. `phys`: the sequence's block id for pos (paged). Every head-slice CTA of this
+// unit writes the same bytes. Arrives on `appended` once the writes are visible to TMA reads.
+template <int D, int BITS, bool PAGED>
+__device__ __forceinline__ void append_token_q8(const DecodeArgs& a, const float* cs, const uint32_t (&kraw)[D / 64],
+                                                const uint32_t (&vraw)[D / 64], int phys, int b, int g, int pos,
+                                                bool has_win, int lane, uint64_t* appended) {
+  constexpr int E = D / 32;
+  size_t row = 0;
+  bool ok = true;
+  if constexpr (PAGED) {
+    ok = phys >= 0 && phys < a.num_blocks;  // a bad id was flagged when the table was read
+    row = ((static_cast<size_t>(phys) << a.log2_bs) + (pos & ((1 << a.log2_bs) - 1))) * a.Hkv + g;
+  } else {
+    row = (static_cast<size_t>(b) * a.Hkv + g) * a.max_len + pos;
+  }
+  float kx[E], vx[E];
+#pragma unroll
+  for (int w = 0; w < E / 2; ++w) {
+    kx[2 * w] = __uint_as_float(kraw[w] << 16);
+    kx[2 * w + 1] = __uint_as_float(kraw[w] & 0xffff0000u);
+    vx[2 * w] = __uint_as_float(vraw[w] << 16);
+    vx[2 * w + 1] = __uint_as_float(vraw[w] & 0xffff0000u);
+  }
+  __nv_bfloat16 kr[E];
+  if (a.rope_style == 1) {  // interleaved pairs (2i, 2i + 1), both in this lane
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const int i = (E * lane + e) / 2;
+      const float ch = cs[i], cl = cs[D / 2 + i], sh = cs[D + i], sl = cs[3 * (D / 2) + i];
+      kr[e] = __float2bfloat16_rn(rotate_diff(kx[e], kx[e + 1], ch, cl, sh, sl));
+      kr[e + 1] = __float2bfloat16_rn(rotate_diff(kx[e + 1], -kx[e], ch, cl, sh, sl));
+    }
+  } else {  // half-split pairs (i, i + D/2): the partner is 16 lanes away
+    const bool first = lane < 16;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float partner = __shfl_xor_sync(0xffffffffu, kx[e], 16);
+      const int i = E * (lane & 15) + e;
+      const float ch = cs[i], cl = cs[D / 2 + i], sh = cs[D + i], sl = cs[3 * (D / 2) + i];
+      kr[e] = __float2bfloat16_rn(first ? rotate_diff(kx[e], partner, ch, cl, sh, sl)     // a cos - b sin
+                                        : rotate_diff(kx[e], -partner, ch, cl, sh, sl));  // b cos + a sin
+    }
+  }
+  const float ks = a.k_scale[g], vs = a.v_scale[g];
+  if (ok) {
+    if constexpr (BITS == 8) {
+      uint32_t kc = 0, vc = 0;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        kc |= static_cast<uint32_t>(static_cast<uint8_t>(quantize_code(__bfloat162float(kr[e]), ks))) << (8 * e);
+        vc |= static_cast<uint32_t>(static_cast<uint8_t>(quantize_code(vx[e], vs))) << (8 * e);
+      }
+      int8_t* kd = static_cast<int8_t*>(const_cast<void*>(a.k)) + row * D + E * lane;
+      int8_t* vd = static_cast<int8_t*>(const_cast<void*>(a.v)) + row * D + E * lane;
+      if constexpr (E == 4) {
+        *reinterpret_cast<uint32_t*>(kd) = kc;
+        *reinterpret_cast<uint32_t*>(vd) = vc;
+      } else {
+        *reinterpret_cast<uint16_t*>(kd) = static_cast<uint16_t>(kc);
+        *reinterpret_cast<uint16_t*>(vd) = static_cast<uint16_t>(vc);
+      }
+    } else {  // codes of dims 2j, 2j+1 in byte j, the even one in the low nibble
+      uint32_t kc = 0, vc = 0;
+#pragma unroll
+      for (int j = 0; j < E / 2; ++j) {
+        kc |= static_cast<uint32_t>(pack_nibbles(quantize_code4(__bfloat162float(kr[2 * j]), ks),
+                                                 quantize_code4(__bfloat162float(kr[2 * j + 1]), ks)))
+              << (8 * j);
+        vc |= static_cast<uint32_t>(pack_nibbles(quantize_code4(vx[2 * j], vs), quantize_code4(vx[2 * j + 1], vs)))
+              << (8 * j);
+      }
+      uint8_t* kd = static_cast<uint8_t*>(const_cast<void*>(a.k)) + row * (D / 2) + (E / 2) * lane;
+      uint8_t* vd = static_cast<uint8_t*>(const_cast<void*>(a.v)) + row * (D / 2) + (E / 2) * lane;
+      static_assert(E == 4, "INT4 caches: head dim 128");
+      *reinterpret_cast<uint16_t*>(kd) = static_cast<uint16_t>(kc);
+      *reinterpret_cast<uint16_t*>(vd) = static_cast<uint16_t>(vc);
+    }
+  }
+  if (has_win) {
+    const size_t wrow = ((static_cast<size_t>(b) * a.Hkv + g) * a.window + pos % a.window) * D + E * lane;
+    uint32_t kw[E / 2];
+#pragma unroll
+    for (int w = 0; w < E / 2; ++w)
+      kw[w] = static_cast<uint32_t>(__bfloat16_as_ushort(kr[2 * w])) |
+              (static_cast<uint32_t>(__bfloat16_as_ushort(kr[2 * w + 1])) << 16);
+    uint32_t* kwd = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.k_win) + wrow);
+    uint32_t* vwd = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.v_win) + wrow);
+#pragma unroll
+    for (int w = 0; w < E / 2; ++w) {
+      kwd[w] = kw[w];
+      vwd[w] = vraw[w];
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");  // visible to the TMA that reads the slot
+  __syncwarp();
+  if (lane == 0) mbar_arrive(appended);
+}
+
 template <int D, int BITS, bool PAGED, bool FUSED>
 __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_MMA_CTAS_PER_SM)
     decode_q8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
@@ -579,6 +680,22 @@ __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_MMA_CTAS_PER_SM)
     load_qb(q_in, qb);
     // RoPE ("Transformer推理核心：KV Cache、GQA与RoPE原理与工程实践" §3) as in decode_mma_kernel
     const int pos = L - 1;
+    // the appender warp fetches the new token's k and v (D / 32 dims per lane) and its block id
+    // now, so that the loads overlap the sine / cosine below
+    const bool app_warp = appender && warp == 1;
+    uint32_t kraw[D / 64], vraw[D / 64];
+    int phys = 0;
+    if (app_warp) {
+      const size_t off = (static_cast<size_t>(b) * a.Hkv + g) * D + lane * (D / 32);
+      const uint32_t* kn = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.k_new) + off);
+      const uint32_t* vn = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.v_new) + off);
+#pragma unroll
+      for (int w = 0; w < D / 64; ++w) {
+        kraw[w] = kn[w];
+        vraw[w] = vn[w];
+      }
+      if constexpr (PAGED) phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (pos >> a.log2_bs)];
+    }
     if (threadIdx.x < D / 2) {
       double sn, cn;
       sincospi(static_cast<double>(pos) * a.theta_pi[threadIdx.x], &sn, &cn);
@@ -604,71 +721,11 @@ __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_MMA_CTAS_PER_SM)
         }
       }
     }
-    if (appender && warp == 1) {
-      // Quantised k (rotated, rounded to bf16) and v into cache slot pos of KV head g, and with
-      // a window their bf16 values into ring slot pos % window. Every head-slice CTA of this
-      // unit writes the same bytes.
-      size_t row = 0;
-      bool ok = true;
-      if constexpr (PAGED) {
-        const int phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (pos >> a.log2_bs)];
-        ok = phys >= 0 && phys < a.num_blocks;
-        row = ((static_cast<size_t>(phys) << a.log2_bs) + (pos & ((1 << a.log2_bs) - 1))) * a.Hkv + g;
-      } else {
-        row = (static_cast<size_t>(b) * a.Hkv + g) * a.max_len + pos;
-      }
-      const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(a.k_new) + (static_cast<size_t>(b) * a.Hkv + g) * D;
-      const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(a.v_new) + (static_cast<size_t>(b) * a.Hkv + g) * D;
-      int8_t* kc = static_cast<int8_t*>(const_cast<void*>(a.k)) + row * D;
-      int8_t* vc = static_cast<int8_t*>(const_cast<void*>(a.v)) + row * D;
-      const size_t wrow = has_win ? ((static_cast<size_t>(b) * a.Hkv + g) * a.window + pos % a.window) * D : 0;
-      __nv_bfloat16* kw = static_cast<__nv_bfloat16*>(a.k_win) + wrow;
-      __nv_bfloat16* vw = static_cast<__nv_bfloat16*>(a.v_win) + wrow;
-      const float ks = a.k_scale[g], vs = a.v_scale[g];
-      const bool inter = a.rope_style == 1;
-      __nv_bfloat16* kr = reinterpret_cast<__nv_bfloat16*>(smem + C::kOffK);  // rotated k (INT4 packing)
-      for (int i = lane; i < D / 2; i += 32) {
-        const int ia = inter ? 2 * i : i, ib = inter ? 2 * i + 1 : i + D / 2;
-        const float xa = __bfloat162float(kn[ia]), xb = __bfloat162float(kn[ib]);
-        const float ch = cs[i], cl = cs[D / 2 + i], sh = cs[D + i], sl = cs[3 * (D / 2) + i];
-        const __nv_bfloat16 ra = __float2bfloat16_rn(rotate_diff(xa, xb, ch, cl, sh, sl));
-        const __nv_bfloat16 rb = __float2bfloat16_rn(rotate_diff(xb, -xa, ch, cl, sh, sl));
-        if constexpr (BITS == 8) {
-          if (ok) {
-            kc[ia] = quantize_code(__bfloat162float(ra), ks);
-            kc[ib] = quantize_code(__bfloat162float(rb), ks);
-          }
-        } else {
-          kr[ia] = ra;
-          kr[ib] = rb;
-        }
-        if (has_win) {
-          kw[ia] = ra;
-          kw[ib] = rb;
-        }
-      }
-      if constexpr (BITS == 4) {  // codes of dims 2j, 2j+1 in byte j: the even one in the low nibble
-        __syncwarp();
-        uint8_t* kc4 = reinterpret_cast<uint8_t*>(const_cast<void*>(a.k)) + row * (D / 2);
-        uint8_t* vc4 = reinterpret_cast<uint8_t*>(const_cast<void*>(a.v)) + row * (D / 2);
-        for (int j = lane; j < D / 2 && ok; j += 32) {
-          kc4[j] = pack_nibbles(quantize_code4(__bfloat162float(kr[2 * j]), ks),
-                                quantize_code4(__bfloat162float(kr[2 * j + 1]), ks));
-          vc4[j] = pack_nibbles(quantize_code4(__bfloat162float(vn[2 * j]), vs),
-                                quantize_code4(__bfloat162float(vn[2 * j + 1]), vs));
-        }
-      }
-      for (int i = lane; i < D; i += 32) {
-        const __nv_bfloat16 x = vn[i];
-        if (BITS == 8 && ok) vc[i] = quantize_code(__bfloat162float(x), vs);
-        if (has_win) vw[i] = x;
-      }
-      asm volatile("fence.proxy.async.global;" ::: "memory");  // visible to the TMA that reads the slot
-      __syncwarp();
-      if (lane == 0) mbar_arrive(appended);
-    }
     q_rows = qs;
     named_barrier_sync(1, kConsumers);  // the rotated rows in shared memory are complete
+    // the appender warp writes the new token after the barrier: the other warps start streaming
+    if (app_warp)
+      append_token_q8<D, BITS, PAGED>(a, cs, kraw, vraw, phys, b, g, pos, has_win, lane, appended);
   }
 
   MmaWarpState<D> st;
