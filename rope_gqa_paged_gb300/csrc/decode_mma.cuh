@@ -241,6 +241,64 @@ __device__ __forceinline__ void rotate_q_fragment(uint32_t (&qb)[D / 16][2], con
     }
 }
 
+// The fused step's append, by one warp: rotated k_new and raw v_new into slot pos of KV head g.
+// Lane l holds dims E l .. E l + E - 1 (E = D / 32) of both as bf16 pairs; a half-split RoPE
+// pair (i, i + D/2) sits in lanes l and l ^ 16. The rotation is the append kernel's. Every
+// head-slice CTA of this chunk writes the same bytes, so their writes cannot tear one another's
+// reads. Arrives on `appended` once the writes are visible to TMA reads.
+template <int D, bool PAGED>
+__device__ __forceinline__ void append_token_bf16(const DecodeArgs& a, const float* cs, const uint32_t (&kraw)[D / 64],
+                                                  const uint32_t (&vraw)[D / 64], int phys, int b, int g, int pos,
+                                                  int lane, uint64_t* appended) {
+  constexpr int E = D / 32;
+  size_t row = 0;
+  bool ok = true;
+  if constexpr (PAGED) {
+    ok = phys >= 0 && phys < a.num_blocks;  // a bad id was flagged when the table was read
+    row = ((static_cast<size_t>(phys) << a.log2_bs) + (pos & ((1 << a.log2_bs) - 1))) * a.Hkv + g;
+  } else {
+    row = (static_cast<size_t>(b) * a.Hkv + g) * a.max_len + pos;
+  }
+  float kx[E];
+#pragma unroll
+  for (int w = 0; w < E / 2; ++w) {
+    kx[2 * w] = __uint_as_float(kraw[w] << 16);
+    kx[2 * w + 1] = __uint_as_float(kraw[w] & 0xffff0000u);
+  }
+  float kr[E];
+  if (a.rope_style == 1) {  // interleaved pairs (2i, 2i + 1), both in this lane
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+      const int i = (E * lane + e) / 2;
+      const float ch = cs[i], cl = cs[D / 2 + i], sh = cs[D + i], sl = cs[3 * (D / 2) + i];
+      kr[e] = rotate_diff(kx[e], kx[e + 1], ch, cl, sh, sl);
+      kr[e + 1] = rotate_diff(kx[e + 1], -kx[e], ch, cl, sh, sl);
+    }
+  } else {  // half-split pairs (i, i + D/2): the partner is 16 lanes away
+    const bool first = lane < 16;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float partner = __shfl_xor_sync(0xffffffffu, kx[e], 16);
+      const int i = E * (lane & 15) + e;
+      const float ch = cs[i], cl = cs[D / 2 + i], sh = cs[D + i], sl = cs[3 * (D / 2) + i];
+      kr[e] = first ? rotate_diff(kx[e], partner, ch, cl, sh, sl)     // a cos - b sin
+                    : rotate_diff(kx[e], -partner, ch, cl, sh, sl);   // b cos + a sin
+    }
+  }
+  if (ok) {
+    uint32_t* kd = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(const_cast<void*>(a.k)) + row * D + E * lane);
+    uint32_t* vd = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(const_cast<void*>(a.v)) + row * D + E * lane);
+#pragma unroll
+    for (int w = 0; w < E / 2; ++w) {
+      kd[w] = pack_bf16x2(kr[2 * w], kr[2 * w + 1]);
+      vd[w] = vraw[w];
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");  // visible to the TMA that reads the slot
+  __syncwarp();
+  if (lane == 0) mbar_arrive(appended);
+}
+
 template <int D, bool PAGED, bool FUSED>
 __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     decode_mma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
@@ -433,6 +491,22 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     // pos * theta_i in float64 (sincospi of pos * theta_i / pi: exact argument reduction),
     // split into float32 hi + lo for the error-free rotation.
     const int pos = L - 1;
+    // the appender warp fetches the new token's k and v (D / 32 dims per lane) and its block id
+    // now, so that the loads overlap the sine / cosine below
+    const bool app_warp = appender && warp == 1;
+    uint32_t kraw[D / 64], vraw[D / 64];
+    int phys = 0;
+    if (app_warp) {
+      const size_t off = (static_cast<size_t>(b) * a.Hkv + g) * D + lane * (D / 32);
+      const uint32_t* kn = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.k_new) + off);
+      const uint32_t* vn = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.v_new) + off);
+#pragma unroll
+      for (int w = 0; w < D / 64; ++w) {
+        kraw[w] = kn[w];
+        vraw[w] = vn[w];
+      }
+      if constexpr (PAGED) phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (pos >> a.log2_bs)];
+    }
     if (threadIdx.x < D / 2) {
       double sn, cn;
       sincospi(static_cast<double>(pos) * a.theta_pi[threadIdx.x], &sn, &cn);
@@ -453,37 +527,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
         qo[kk * 8 + 4 + (lane & 3)] = qb[kk][1];
       }
     }
-    if (appender && warp == 1) {
-      // Rotated k_new and raw v_new into slot pos of KV head g. Every head-slice CTA of this
-      // chunk writes the same bytes, so their writes cannot tear one another's reads.
-      size_t row = 0;
-      bool ok = true;
-      if constexpr (PAGED) {
-        const int phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (pos >> a.log2_bs)];
-        ok = phys >= 0 && phys < a.num_blocks;  // a bad id was flagged when the table was read
-        row = ((static_cast<size_t>(phys) << a.log2_bs) + (pos & ((1 << a.log2_bs) - 1))) * a.Hkv + g;
-      } else {
-        row = (static_cast<size_t>(b) * a.Hkv + g) * a.max_len + pos;
-      }
-      if (ok) {
-        const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(a.k_new) + (static_cast<size_t>(b) * a.Hkv + g) * D;
-        const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(a.v_new) + (static_cast<size_t>(b) * a.Hkv + g) * D;
-        __nv_bfloat16* kc = static_cast<__nv_bfloat16*>(const_cast<void*>(a.k)) + row * D;
-        __nv_bfloat16* vc = static_cast<__nv_bfloat16*>(const_cast<void*>(a.v)) + row * D;
-        const bool inter = a.rope_style == 1;
-        for (int i = lane; i < D / 2; i += 32) {
-          const int ia = inter ? 2 * i : i, ib = inter ? 2 * i + 1 : i + D / 2;
-          const float xa = __bfloat162float(kn[ia]), xb = __bfloat162float(kn[ib]);
-          const float ch = cs[i], cl = cs[D / 2 + i], sh = cs[D + i], sl = cs[3 * (D / 2) + i];
-          kc[ia] = __float2bfloat16_rn(rotate_diff(xa, xb, ch, cl, sh, sl));
-          kc[ib] = __float2bfloat16_rn(rotate_diff(xb, -xa, ch, cl, sh, sl));
-        }
-        for (int i = lane; i < D; i += 32) vc[i] = vn[i];
-      }
-      asm volatile("fence.proxy.async.global;" ::: "memory");  // visible to the TMA that reads the slot
-      __syncwarp();
-      if (lane == 0) mbar_arrive(appended);
-    }
+    if (app_warp) append_token_bf16<D, PAGED>(a, cs, kraw, vraw, phys, b, g, pos, lane, appended);
   }
   MmaWarpState<D> st;
 #pragma unroll
