@@ -234,3 +234,33 @@ def test_fused_step_position_errors_are_flagged():
     keep = [0, 1, 3]
     assert gpu.out[keep].tobytes() == good.out[keep].tobytes()
     inp.positions[:] = bad
+
+
+# ------------------------------------------------------------------ heads per KV group
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (32, 1), (12, 4), (32, 2), (64, 4), (64, 1)],
+                         ids=["mha", "mqa", "nrep3", "nrep16", "nrep16b", "nrep64"])
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused_step"])
+def test_heads_and_head_dim(hq, hkv, head_dim, fused):
+    """GQA groups of 1 to 64 query heads (up to 32 served by one CTA from one KV stream), both
+    head dims, paged blocks of 16, lengths across tiles; split counts 0 and 3."""
+    import dataclasses
+    lens = [5, 200, 611]
+    cfg = dataclasses.replace(CONFIGS["batched_paged"], name=f"heads_{hq}_{hkv}_{head_dim}", batch=len(lens),
+                              n_q_heads=hq, n_kv_heads=hkv, head_dim=head_dim, len_range=(min(lens), max(lens)),
+                              max_blocks_per_seq=-(-max(lens) // 16), num_blocks=len(lens) * (-(-max(lens) // 16)) + 5,
+                              num_splits=0)
+    from workloads import gen
+    inp = gen.make_inputs(dataclasses.replace(cfg, len_range=(max(lens), max(lens))), seed=9, poison=False)
+    inp.lengths[:] = lens
+    inp.positions[:] = np.array(lens) - 1
+    for b, L in enumerate(lens):
+        inp.block_table[b, -(-L // 16):] = -1
+    gen.poison_unread(inp)
+    style = 1 if head_dim == 64 else 0
+    for splits in (0, 3):
+        gpu = H.run_gpu(inp, num_splits=splits, fused=fused, rope_style=style)
+        q_ref, k_ref, _, out_ref = H.run_oracle(inp, rope_style=style)
+        assert gpu.err == 0
+        _check_step(inp, gpu, q_ref, out_ref)
+        _check_cache(inp, gpu, _oracle_k_rows(inp, k_ref))
