@@ -141,6 +141,23 @@ def half_ulp(x: np.ndarray, dtype: str) -> np.ndarray:
     return np.ldexp(0.5, e - bits)
 
 
+# Relative bar: long rows average many values, so their outputs are small (|out| ~ sqrt(1/L),
+# about 0.005 at 128K) and an absolute 1e-2 says little there. The error beyond the storage
+# rounding, over the RMS of the same output row of the float64 result, stays below 5 %: the bf16
+# (f16 for quantised caches) probabilities perturb each weight by about 2^-9 relative, well under
+# 1 % of the row's RMS, while a wrong token, head or block gives errors of order one.
+REL_RMS_BAR = 0.05
+
+
+def rel_rms_error(got_stored: np.ndarray, want_f64: np.ndarray, dtype: str) -> float:
+    """Max over output rows (last axis) of the error beyond half an ulp over the row's RMS."""
+    want = np.asarray(want_f64, dtype=np.float64)
+    got = stored_to_f64(got_stored, dtype)
+    excess = np.maximum(np.abs(got - want) - half_ulp(np.maximum(np.abs(want), np.abs(got)), dtype), 0.0).max(axis=-1)
+    rms = np.sqrt(np.mean(want * want, axis=-1))
+    return float((excess / np.maximum(rms, 1e-30)).max())
+
+
 def out_error(got_stored: np.ndarray, want_f64: np.ndarray, dtype: str) -> float:
     """Attention-output error beyond the output's own storage rounding: max over elements of
     |stored - float64 result| - half an ulp of the storage type at the result. The tolerance

@@ -22,6 +22,8 @@ def _check_step(inp, gpu, q_ref, out_ref, batches=None):
     H.assert_close_stored(gpu.q_rot[list(bs)], q_ref, cfg.dtype, "q_rot")
     err = H.out_error(gpu.out[list(bs)], out_ref, cfg.dtype)
     assert err <= H.OUT_ATOL[cfg.dtype], f"{cfg.name}: out max abs err {err:.3e}"
+    rel = H.rel_rms_error(gpu.out[list(bs)], out_ref, cfg.dtype)
+    assert rel <= H.REL_RMS_BAR, f"{cfg.name}: out error {rel:.3e} of the row RMS"
     return err
 
 

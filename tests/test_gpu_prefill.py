@@ -31,6 +31,8 @@ def _check(inp, gpu, rope_style=0):
     H.assert_close_stored(gpu.q_rot, q_ref, "bf16", "q_rot")
     err = H.out_error(gpu.out, out_ref, "bf16")
     assert err <= H.OUT_ATOL["bf16"], f"{cfg.name}: out max abs err {err:.3e}"
+    rel = H.rel_rms_error(gpu.out, out_ref, "bf16")
+    assert rel <= H.REL_RMS_BAR, f"{cfg.name}: out error {rel:.3e} of the row RMS"
     H.assert_close_stored(gpu.k_cache, k_ref, "bf16", "K cache")
     assert gpu.v_cache.tobytes() == v_ref.tobytes(), "V cache"
     return err
@@ -97,3 +99,5 @@ def test_prefill_128k_sampled_rows():
                                            np.transpose(vf[: t + 1], (1, 0, 2)))
         e = H.out_error(gpu.out[0, t], want, "bf16")
         assert e <= H.OUT_ATOL["bf16"], (t, e)
+        rel = H.rel_rms_error(gpu.out[0, t], want, "bf16")
+        assert rel <= H.REL_RMS_BAR, (t, rel)

@@ -35,6 +35,8 @@ def _check_q8(inp, gpu, ref, fused_or_append=True, out_batches=None):
     bs = range(cfg.batch) if out_batches is None else out_batches
     err = H.out_error(gpu.out[list(bs)], out_ref[list(bs)], "bf16")
     assert err <= H.OUT_ATOL["bf16"], f"{cfg.name}: out max abs err {err:.3e}"
+    rel = H.rel_rms_error(gpu.out[list(bs)], out_ref[list(bs)], "bf16")
+    assert rel <= H.REL_RMS_BAR, f"{cfg.name}: out error {rel:.3e} of the row RMS"
     kc, vc = gpu.k_codes.copy(), gpu.v_codes.copy()
     W = cfg.window
     kw = gpu.k_win.copy() if W else None

@@ -31,6 +31,8 @@ def _check(inp, gpu, ref):
     H.assert_close_stored(gpu.q_rot, q_ref, "bf16", "q_rot")
     err = H.out_error(gpu.out, out_ref, "bf16")
     assert err <= H.OUT_ATOL["bf16"], f"{cfg.name}: out max abs err {err:.3e}"
+    rel = H.rel_rms_error(gpu.out, out_ref, "bf16")
+    assert rel <= H.REL_RMS_BAR, f"{cfg.name}: out error {rel:.3e} of the row RMS"
     kc, vc = gpu.k_cache.copy(), gpu.v_cache.copy()
     for b in range(cfg.batch):
         for j in range(cfg.gamma):
