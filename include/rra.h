@@ -313,8 +313,11 @@ RRA_API size_t rra_verify_workspace_bytes(int B, int gamma, int Hq, int Hkv, int
 
 /* out[b, t, h] = softmax(q_rot[b, t, h] . K[b, h / n_rep, 0 : p_b + t + 1]^T * scale) . V[...],
  * bf16, q_rot and out [B, T, Hq, D], caches as in the decode calls (paged blocks of at least 8
- * tokens, contiguous caches of at least 16384 / (2 D) tokens). 64 query rows per CTA, no
- * workspace. A prompt that runs past the cache sets RRA_ERR_POSITION and skips b. */
+ * tokens, contiguous caches of at least 16384 / (2 D) tokens). No workspace. Head dim 128 runs
+ * on the tcgen05 tensor cores (128 prompt tokens of one or two query heads per CTA, one CTA per
+ * SM, scores and outputs in Tensor Memory; q_rot and out 16-byte aligned, as checked); head dim
+ * 64 on mma.sync (64 query rows per CTA). A prompt that runs past the cache sets
+ * RRA_ERR_POSITION and skips b; a pipeline wait that runs out sets RRA_ERR_TIMEOUT. */
 RRA_API int rra_prefill_attn(const void* q_rot, const void* k_cache, const void* v_cache, const int32_t* block_table,
                              int max_blocks_per_seq, const int32_t* positions, int block_size, int num_blocks,
                              int max_len, void* out, int B, int T, int Hq, int Hkv, int D, float scale,
