@@ -297,6 +297,9 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
       qa[kk][2 + i] = r < rows ? q[kk * 8 + 4 + t] : 0u;
     }
   }
+  // rows attend at least p0 + 1 keys: from 256 on, a bf16 P is exact enough (the split of P into
+  // a bf16 part and its remainder is for rows that see a few tokens, as in the prefill kernel)
+  const bool precise = p0 < 256;
   VerifyState<D> st;
 #pragma unroll
   for (int nt = 0; nt < D / 8; ++nt) st.o[nt][0] = st.o[nt][1] = st.o[nt][2] = st.o[nt][3] = 0.f;
@@ -319,10 +322,21 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
 #pragma unroll
     for (int step = 0; step < C::kSteps; ++step) {
       const int t0 = warp * C::kWarpTokens + step * 16;
-      if (!edge)
-        verify_step<D, false>(st, qa, k_base, v_base, vst, t0, tile0 + t0, valid, lim[0], lim[1], lane, a.scale_log2);
-      else if (t0 < valid)
-        verify_step<D, true>(st, qa, k_base, v_base, vst, t0, tile0 + t0, valid, lim[0], lim[1], lane, a.scale_log2);
+      if (!edge) {
+        if (precise)
+          verify_step<D, false, true>(st, qa, k_base, v_base, vst, t0, tile0 + t0, valid, lim[0], lim[1], lane,
+                                      a.scale_log2);
+        else
+          verify_step<D, false, false>(st, qa, k_base, v_base, vst, t0, tile0 + t0, valid, lim[0], lim[1], lane,
+                                       a.scale_log2);
+      } else if (t0 < valid) {
+        if (precise)
+          verify_step<D, true, true>(st, qa, k_base, v_base, vst, t0, tile0 + t0, valid, lim[0], lim[1], lane,
+                                     a.scale_log2);
+        else
+          verify_step<D, true, false>(st, qa, k_base, v_base, vst, t0, tile0 + t0, valid, lim[0], lim[1], lane,
+                                      a.scale_log2);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
