@@ -95,7 +95,7 @@ constexpr int kMaxTableEntries = 2048;
 // shared memory).
 constexpr int kMaxSplits = 1024;
 // Splits merged by one CTA; more splits are merged in two levels.
-constexpr int kMergeFanIn = 16;
+constexpr int kMergeFanIn = 32;
 
 // Stores the text rra_last_cuda_error() returns on this thread.
 void record_cuda_error(cudaError_t e, const char* where);

@@ -208,12 +208,12 @@ def test_full_size_sampled(name):
 
 # ------------------------------------------------------------------ many splits: two-level merge
 @pytest.mark.parametrize("name,factor", [("llama3_8b_layer", 2), ("long_context", 32)])
-@pytest.mark.parametrize("splits", [16, 17, 40, 64])
+@pytest.mark.parametrize("splits", [17, 33, 40, 64, 100])
 def test_many_splits_merge(name, factor, splits):
-    """More than 16 splits are merged in two levels (groups of 16, then the groups).
+    """More than 32 splits are merged in two levels (groups of 32, then the groups).
 
-    The effective split count is the request rounded to whole tiles (here 13..64 splits,
-    most of them above 16, with a partial last group)."""
+    The effective split count is the request rounded to whole tiles (one level up to 32 splits,
+    two above, with a partial last group)."""
     cfg = reduced(CONFIGS[name], factor, 2)
     inp = make_inputs(cfg, seed=21)
     gpu = H.run_gpu(inp, num_splits=splits, fused=True)
