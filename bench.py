@@ -46,14 +46,14 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
 KERNEL_SOURCES = ["rope_gqa_paged_gb300/csrc/decode_mma.cuh", "rope_gqa_paged_gb300/csrc/decode_kernels.cuh",
                   "rope_gqa_paged_gb300/csrc/rra_device.cuh", "rope_gqa_paged_gb300/csrc/decode_paged.cu",
-                  "rope_gqa_paged_gb300/csrc/decode_contig.cu"]
+                  "rope_gqa_paged_gb300/csrc/decode_contig.cu", "rope_gqa_paged_gb300/csrc/rra_internal.h"]
 KERNEL_SOURCES_INT8 = KERNEL_SOURCES + ["rope_gqa_paged_gb300/csrc/decode_q8.cuh",
-                                        "rope_gqa_paged_gb300/csrc/decode_q8.cu",
-                                        "rope_gqa_paged_gb300/csrc/rra_internal.h"]
+                                        "rope_gqa_paged_gb300/csrc/decode_q8.cu"]
 KERNEL_SOURCES_VERIFY = KERNEL_SOURCES + ["rope_gqa_paged_gb300/csrc/verify.cuh", "rope_gqa_paged_gb300/csrc/verify.cu",
-                                          "rope_gqa_paged_gb300/csrc/rope_append.cu",
-                                          "rope_gqa_paged_gb300/csrc/rra_internal.h"]
+                                          "rope_gqa_paged_gb300/csrc/rope_append.cu"]
 KERNEL_SOURCES_PREFILL = KERNEL_SOURCES_VERIFY + ["rope_gqa_paged_gb300/csrc/prefill.cuh",
+                                                  "rope_gqa_paged_gb300/csrc/prefill_tc.cuh",
+                                                  "rope_gqa_paged_gb300/csrc/tcgen05.cuh",
                                                   "rope_gqa_paged_gb300/csrc/prefill.cu"]
 
 
