@@ -272,15 +272,17 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_rows_kernel(const Ro
   }
 }
 
-// INT4 caches (bf16 q / k / v, head_dim 128): one CTA per sequence. The rotated k of every KV
-// head is rounded to bf16 into shared memory first, so that each thread can then pack the codes
-// of dims 2j and 2j+1 into byte j (the even one in the low nibble); v packs straight from v_new.
-constexpr int kMaxQ4Heads = 32;
+// INT4 caches (bf16 q / k / v, head_dim 128): one CTA per sequence, one warp per head row. Lane l
+// holds dims 4l .. 4l + 3 (one 8-byte vector, all of a warp's rows loaded before any arithmetic);
+// a half-split RoPE pair (i, i + 64) sits in lanes l and l ^ 16. The codes of dims 2j and 2j + 1
+// go to byte j (the even one in the low nibble): two bytes per lane. Rotation and rounding are
+// those of rope_append_kernel.
+constexpr int kQ4Warps = 8;
+constexpr int kQ4RowsPerWarp = 6;
 
-__global__ void __launch_bounds__(kRopeThreads) rope_append_q4_kernel(const RopeArgs a) {
+__global__ void __launch_bounds__(kQ4Warps * 32) rope_append_q4_kernel(const RopeArgs a) {
   constexpr int D = 128, HALF = D / 2;
   __shared__ float cs[4][HALF];
-  __shared__ __nv_bfloat16 kr[kMaxQ4Heads][D];
   __shared__ size_t row_info[2];
   __shared__ int append_ok;
   const int b = blockIdx.x;
@@ -292,7 +294,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_q4_kernel(const Rope
     return;
   }
   if (threadIdx.x < HALF) {
-    double sn, cn;
+    double sn, cn;  // angle / pi = pos * (theta_i / pi): sincospi reduces its argument exactly
     sincospi(static_cast<double>(pos) * a.inv_freq[threadIdx.x], &sn, &cn);
     const float ch = static_cast<float>(cn), sh = static_cast<float>(sn);
     cs[0][threadIdx.x] = ch;
@@ -300,7 +302,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_q4_kernel(const Rope
     cs[2][threadIdx.x] = sh;
     cs[3][threadIdx.x] = static_cast<float>(sn - static_cast<double>(sh));
   }
-  if (threadIdx.x == HALF) {
+  if (threadIdx.x == kQ4Warps * 32 - 1) {  // where the token's codes go
     int ok = 1;
     size_t row0 = 0, stride = 0;
     if (paged) {
@@ -320,47 +322,77 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_q4_kernel(const Rope
     row_info[1] = stride;
     append_ok = ok;
   }
-  __syncthreads();
-  const bool inter = a.rope_style == 1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int heads = a.Hq + a.Hkv;
+  const bool inter = a.rope_style == 1, first = lane < 16;
   const __nv_bfloat16* qin = static_cast<const __nv_bfloat16*>(a.q) + static_cast<size_t>(b) * a.Hq * D;
   __nv_bfloat16* qout = static_cast<__nv_bfloat16*>(a.q_out) + static_cast<size_t>(b) * a.Hq * D;
   const __nv_bfloat16* kin = static_cast<const __nv_bfloat16*>(a.k_new) + static_cast<size_t>(b) * a.Hkv * D;
   const __nv_bfloat16* vin = static_cast<const __nv_bfloat16*>(a.v_new) + static_cast<size_t>(b) * a.Hkv * D;
-  for (int idx = threadIdx.x; idx < (a.Hq + a.Hkv) * HALF; idx += blockDim.x) {
-    const int hh = idx / HALF, i = idx - hh * HALF;
-    const int ia = inter ? 2 * i : i, ib = inter ? 2 * i + 1 : i + HALF;
-    const bool is_q = hh < a.Hq;
-    const __nv_bfloat16* src = is_q ? qin + static_cast<size_t>(hh) * D : kin + static_cast<size_t>(hh - a.Hq) * D;
-    const float xa = __bfloat162float(src[ia]), xb = __bfloat162float(src[ib]);
-    const __nv_bfloat16 ra = __float2bfloat16_rn(rotate_diff(xa, xb, cs[0][i], cs[1][i], cs[2][i], cs[3][i]));
-    const __nv_bfloat16 rb = __float2bfloat16_rn(rotate_diff(xb, -xa, cs[0][i], cs[1][i], cs[2][i], cs[3][i]));
-    if (is_q) {
-      qout[static_cast<size_t>(hh) * D + ia] = ra;
-      qout[static_cast<size_t>(hh) * D + ib] = rb;
-    } else {
-      kr[hh - a.Hq][ia] = ra;
-      kr[hh - a.Hq][ib] = rb;
+  for (int base = 0; base < heads; base += kQ4Warps * kQ4RowsPerWarp) {
+    uint2 xr[kQ4RowsPerWarp], vr[kQ4RowsPerWarp];
+#pragma unroll
+    for (int r = 0; r < kQ4RowsPerWarp; ++r) {
+      const int hh = base + warp + kQ4Warps * r;
+      if (hh < heads) {
+        const bool is_q = hh < a.Hq;
+        xr[r] = *reinterpret_cast<const uint2*>((is_q ? qin + static_cast<size_t>(hh) * D
+                                                      : kin + static_cast<size_t>(hh - a.Hq) * D) + 4 * lane);
+        if (!is_q) vr[r] = *reinterpret_cast<const uint2*>(vin + static_cast<size_t>(hh - a.Hq) * D + 4 * lane);
+      }
     }
-  }
-  __syncthreads();
-  if (!append_ok) return;
-  const size_t row0 = row_info[0], stride = row_info[1];
-  uint8_t* kc = static_cast<uint8_t*>(a.k_cache);
-  uint8_t* vc = static_cast<uint8_t*>(a.v_cache);
-  for (int idx = threadIdx.x; idx < a.Hkv * HALF; idx += blockDim.x) {
-    const int g = idx / HALF, j = idx - g * HALF;
-    const float ks = a.k_scale[g], vs = a.v_scale[g];
-    const size_t byte = (row0 + g * stride) * HALF + j;
-    const __nv_bfloat16 k0 = kr[g][2 * j], k1 = kr[g][2 * j + 1];
-    const __nv_bfloat16 v0 = vin[static_cast<size_t>(g) * D + 2 * j], v1 = vin[static_cast<size_t>(g) * D + 2 * j + 1];
-    kc[byte] = pack_nibbles(quantize_code4(__bfloat162float(k0), ks), quantize_code4(__bfloat162float(k1), ks));
-    vc[byte] = pack_nibbles(quantize_code4(__bfloat162float(v0), vs), quantize_code4(__bfloat162float(v1), vs));
-    if (a.window > 0) {
-      const size_t w = ((static_cast<size_t>(b) * a.Hkv + g) * a.window + pos % a.window) * D + 2 * j;
-      static_cast<__nv_bfloat16*>(a.k_win)[w] = k0;
-      static_cast<__nv_bfloat16*>(a.k_win)[w + 1] = k1;
-      static_cast<__nv_bfloat16*>(a.v_win)[w] = v0;
-      static_cast<__nv_bfloat16*>(a.v_win)[w + 1] = v1;
+    __syncthreads();  // the sine / cosine table and the cache row are ready
+    const size_t row0 = row_info[0], stride = row_info[1];
+    const bool append = append_ok != 0;
+#pragma unroll
+    for (int r = 0; r < kQ4RowsPerWarp; ++r) {
+      const int hh = base + warp + kQ4Warps * r;  // the same for the whole warp
+      if (hh >= heads) continue;
+      const float x[4] = {__uint_as_float(xr[r].x << 16), __uint_as_float(xr[r].x & 0xffff0000u),
+                          __uint_as_float(xr[r].y << 16), __uint_as_float(xr[r].y & 0xffff0000u)};
+      __nv_bfloat16 o[4];
+      if (inter) {  // pairs (2i, 2i + 1) inside the lane
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          const int i = 2 * lane + e / 2;
+          o[e] = __float2bfloat16_rn(rotate_diff(x[e], x[e + 1], cs[0][i], cs[1][i], cs[2][i], cs[3][i]));
+          o[e + 1] = __float2bfloat16_rn(rotate_diff(x[e + 1], -x[e], cs[0][i], cs[1][i], cs[2][i], cs[3][i]));
+        }
+      } else {  // pairs (i, i + 64): the partner is 16 lanes away
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float partner = __shfl_xor_sync(0xffffffffu, x[e], 16);
+          const int i = 4 * (lane & 15) + e;
+          o[e] = __float2bfloat16_rn(first ? rotate_diff(x[e], partner, cs[0][i], cs[1][i], cs[2][i], cs[3][i])
+                                           : rotate_diff(x[e], -partner, cs[0][i], cs[1][i], cs[2][i], cs[3][i]));
+        }
+      }
+      const uint2 packed = make_uint2(
+          static_cast<uint32_t>(__bfloat16_as_ushort(o[0])) | (static_cast<uint32_t>(__bfloat16_as_ushort(o[1])) << 16),
+          static_cast<uint32_t>(__bfloat16_as_ushort(o[2])) | (static_cast<uint32_t>(__bfloat16_as_ushort(o[3])) << 16));
+      if (hh < a.Hq) {
+        *reinterpret_cast<uint2*>(qout + static_cast<size_t>(hh) * D + 4 * lane) = packed;
+        continue;
+      }
+      if (!append) continue;
+      const int g = hh - a.Hq;
+      const float ks = a.k_scale[g], vs = a.v_scale[g];
+      const float v[4] = {__uint_as_float(vr[r].x << 16), __uint_as_float(vr[r].x & 0xffff0000u),
+                          __uint_as_float(vr[r].y << 16), __uint_as_float(vr[r].y & 0xffff0000u)};
+      const size_t byte = (row0 + g * stride) * HALF + 2 * lane;
+      const uint16_t kc = static_cast<uint16_t>(
+          pack_nibbles(quantize_code4(__bfloat162float(o[0]), ks), quantize_code4(__bfloat162float(o[1]), ks)) |
+          (pack_nibbles(quantize_code4(__bfloat162float(o[2]), ks), quantize_code4(__bfloat162float(o[3]), ks)) << 8));
+      const uint16_t vc = static_cast<uint16_t>(
+          pack_nibbles(quantize_code4(v[0], vs), quantize_code4(v[1], vs)) |
+          (pack_nibbles(quantize_code4(v[2], vs), quantize_code4(v[3], vs)) << 8));
+      *reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(a.k_cache) + byte) = kc;
+      *reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(a.v_cache) + byte) = vc;
+      if (a.window > 0) {
+        const size_t w = ((static_cast<size_t>(b) * a.Hkv + g) * a.window + pos % a.window) * D + 4 * lane;
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.k_win) + w) = packed;
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.v_win) + w) = vr[r];
+      }
     }
   }
 }
@@ -368,7 +400,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_q4_kernel(const Rope
 }  // namespace
 
 cudaError_t launch_rope_append_q4(const RopeArgs& a, cudaStream_t stream) {
-  rope_append_q4_kernel<<<a.B, kRopeThreads, 0, stream>>>(a);
+  rope_append_q4_kernel<<<a.B, kQ4Warps * 32, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
