@@ -16,10 +16,10 @@
 // the FMA) so that it keeps full relative accuracy when the two products cancel; the
 // result is then rounded once to the storage type.
 //
-// INT8 caches (§4.3 of the first page: INT8 K/V with per-head calibrated scales, recent
-// tokens kept at high precision): the rotated k is rounded to bf16 first, then quantised
-// with its KV head's scale into the cache slot; with a window the bf16 values also go to
-// slot pos % window of the sequence's ring.
+// Quantised caches (§4.3 of the first page: INT8 or INT4 K/V with per-head calibrated scales,
+// recent tokens kept at high precision; rope_append_qx_kernel): the rotated k is rounded to
+// bf16 first, then quantised with its KV head's scale into the cache slot; with a window the
+// bf16 values also go to slot pos % window of the sequence's ring.
 #include "rra_device.cuh"
 #include "rra_internal.h"
 
@@ -30,7 +30,7 @@ constexpr int kPairsPerCta = 16;
 constexpr int kRopeThreads = 128;
 constexpr int kRowsKernelMin = 256;  // token rows from which one CTA per row beats splitting each row
 
-template <typename T, bool Q8>
+template <typename T>
 __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArgs a) {
   constexpr int kRows = kRopeThreads / kPairsPerCta;  // head rows handled side by side
   constexpr int kUnroll = 8;                          // head rows per thread loaded before any math
@@ -125,23 +125,9 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
           Elem<T>::store(dst + ib, rb);
         } else if (append) {
           const int g = hh - a.Hq;
-          if constexpr (Q8) {
-            const __nv_bfloat16 ka = __float2bfloat16_rn(ra), kb = __float2bfloat16_rn(rb);
-            const float s = a.k_scale[g];
-            int8_t* dst = static_cast<int8_t*>(a.k_cache) + (row0 + g * head_stride) * D;
-            dst[ia] = quantize_code(__bfloat162float(ka), s);
-            dst[ib] = quantize_code(__bfloat162float(kb), s);
-            if (a.window > 0) {
-              __nv_bfloat16* w = static_cast<__nv_bfloat16*>(a.k_win) +
-                                 ((static_cast<size_t>(b) * a.Hkv + g) * a.window + pos % a.window) * D;
-              w[ia] = ka;
-              w[ib] = kb;
-            }
-          } else {
-            T* dst = static_cast<T*>(a.k_cache) + (row0 + g * head_stride) * D;
-            Elem<T>::store(dst + ia, ra);
-            Elem<T>::store(dst + ib, rb);
-          }
+          T* dst = static_cast<T*>(a.k_cache) + (row0 + g * head_stride) * D;
+          Elem<T>::store(dst + ia, ra);
+          Elem<T>::store(dst + ib, rb);
         }
       }
     }
@@ -153,14 +139,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
   const T* vn = static_cast<const T*>(a.v_new) + static_cast<size_t>(v) * a.Hkv * D;
   for (int idx = threadIdx.x; idx < a.Hkv * (d1 - d0); idx += blockDim.x) {
     const int g = idx / (d1 - d0), d = d0 + idx % (d1 - d0);
-    if constexpr (Q8) {
-      const T x = vn[g * D + d];
-      static_cast<int8_t*>(a.v_cache)[(row0 + g * head_stride) * D + d] = quantize_code(Elem<T>::load(&x), a.v_scale[g]);
-      if (a.window > 0)
-        static_cast<T*>(a.v_win)[((static_cast<size_t>(b) * a.Hkv + g) * a.window + pos % a.window) * D + d] = x;
-    } else {
-      static_cast<T*>(a.v_cache)[(row0 + g * head_stride) * D + d] = vn[g * D + d];
-    }
+    static_cast<T*>(a.v_cache)[(row0 + g * head_stride) * D + d] = vn[g * D + d];
   }
 }
 
@@ -272,16 +251,48 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_rows_kernel(const Ro
   }
 }
 
-// INT4 caches (bf16 q / k / v, head_dim 128): one CTA per sequence, one warp per head row. Lane l
-// holds dims 4l .. 4l + 3 (one 8-byte vector, all of a warp's rows loaded before any arithmetic);
-// a half-split RoPE pair (i, i + 64) sits in lanes l and l ^ 16. The codes of dims 2j and 2j + 1
-// go to byte j (the even one in the low nibble): two bytes per lane. Rotation and rounding are
-// those of rope_append_kernel.
+// Quantised caches (bf16 q / k / v; INT8 codes, or INT4 two per byte at head dim 128): one CTA per
+// sequence, one warp per head row. Lane l holds dims E l .. E l + E - 1 (E = D / 32: one vector,
+// all of a warp's rows loaded before any arithmetic); a half-split RoPE pair (i, i + D/2) sits in
+// lanes l and l ^ 16. INT4: the codes of dims 2j and 2j + 1 go to byte j (the even one in the low
+// nibble). Rotation, rounding and codes are those of rope_append_kernel.
 constexpr int kQ4Warps = 8;
 constexpr int kQ4RowsPerWarp = 6;
 
-__global__ void __launch_bounds__(kQ4Warps * 32) rope_append_q4_kernel(const RopeArgs a) {
-  constexpr int D = 128, HALF = D / 2;
+template <int D>
+struct LaneVec;  // E = D / 32 bf16 per lane
+template <>
+struct LaneVec<128> {
+  using T = uint2;
+  __device__ __forceinline__ static void unpack(T w, float (&x)[4]) {
+    x[0] = __uint_as_float(w.x << 16);
+    x[1] = __uint_as_float(w.x & 0xffff0000u);
+    x[2] = __uint_as_float(w.y << 16);
+    x[3] = __uint_as_float(w.y & 0xffff0000u);
+  }
+  __device__ __forceinline__ static T pack(const __nv_bfloat16 (&o)[4]) {
+    return make_uint2(static_cast<uint32_t>(__bfloat16_as_ushort(o[0])) | (static_cast<uint32_t>(__bfloat16_as_ushort(o[1])) << 16),
+                      static_cast<uint32_t>(__bfloat16_as_ushort(o[2])) | (static_cast<uint32_t>(__bfloat16_as_ushort(o[3])) << 16));
+  }
+};
+template <>
+struct LaneVec<64> {
+  using T = uint32_t;
+  __device__ __forceinline__ static void unpack(T w, float (&x)[2]) {
+    x[0] = __uint_as_float(w << 16);
+    x[1] = __uint_as_float(w & 0xffff0000u);
+  }
+  __device__ __forceinline__ static T pack(const __nv_bfloat16 (&o)[2]) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(o[0])) | (static_cast<uint32_t>(__bfloat16_as_ushort(o[1])) << 16);
+  }
+};
+
+template <int D, int BITS>
+__global__ void __launch_bounds__(kQ4Warps * 32) rope_append_qx_kernel(const RopeArgs a) {
+  constexpr int HALF = D / 2, E = D / 32;
+  constexpr int RB = D * BITS / 8;  // code bytes per row
+  using V = LaneVec<D>;
+  using VT = typename V::T;
   __shared__ float cs[4][HALF];
   __shared__ size_t row_info[2];
   __shared__ int append_ok;
@@ -330,15 +341,15 @@ __global__ void __launch_bounds__(kQ4Warps * 32) rope_append_q4_kernel(const Rop
   const __nv_bfloat16* kin = static_cast<const __nv_bfloat16*>(a.k_new) + static_cast<size_t>(b) * a.Hkv * D;
   const __nv_bfloat16* vin = static_cast<const __nv_bfloat16*>(a.v_new) + static_cast<size_t>(b) * a.Hkv * D;
   for (int base = 0; base < heads; base += kQ4Warps * kQ4RowsPerWarp) {
-    uint2 xr[kQ4RowsPerWarp], vr[kQ4RowsPerWarp];
+    VT xr[kQ4RowsPerWarp], vr[kQ4RowsPerWarp];
 #pragma unroll
     for (int r = 0; r < kQ4RowsPerWarp; ++r) {
       const int hh = base + warp + kQ4Warps * r;
       if (hh < heads) {
         const bool is_q = hh < a.Hq;
-        xr[r] = *reinterpret_cast<const uint2*>((is_q ? qin + static_cast<size_t>(hh) * D
-                                                      : kin + static_cast<size_t>(hh - a.Hq) * D) + 4 * lane);
-        if (!is_q) vr[r] = *reinterpret_cast<const uint2*>(vin + static_cast<size_t>(hh - a.Hq) * D + 4 * lane);
+        xr[r] = *reinterpret_cast<const VT*>((is_q ? qin + static_cast<size_t>(hh) * D
+                                                   : kin + static_cast<size_t>(hh - a.Hq) * D) + E * lane);
+        if (!is_q) vr[r] = *reinterpret_cast<const VT*>(vin + static_cast<size_t>(hh - a.Hq) * D + E * lane);
       }
     }
     __syncthreads();  // the sine / cosine table and the cache row are ready
@@ -348,50 +359,65 @@ __global__ void __launch_bounds__(kQ4Warps * 32) rope_append_q4_kernel(const Rop
     for (int r = 0; r < kQ4RowsPerWarp; ++r) {
       const int hh = base + warp + kQ4Warps * r;  // the same for the whole warp
       if (hh >= heads) continue;
-      const float x[4] = {__uint_as_float(xr[r].x << 16), __uint_as_float(xr[r].x & 0xffff0000u),
-                          __uint_as_float(xr[r].y << 16), __uint_as_float(xr[r].y & 0xffff0000u)};
-      __nv_bfloat16 o[4];
+      float x[E];
+      V::unpack(xr[r], x);
+      __nv_bfloat16 o[E];
       if (inter) {  // pairs (2i, 2i + 1) inside the lane
 #pragma unroll
-        for (int e = 0; e < 4; e += 2) {
-          const int i = 2 * lane + e / 2;
+        for (int e = 0; e < E; e += 2) {
+          const int i = (E * lane + e) / 2;
           o[e] = __float2bfloat16_rn(rotate_diff(x[e], x[e + 1], cs[0][i], cs[1][i], cs[2][i], cs[3][i]));
           o[e + 1] = __float2bfloat16_rn(rotate_diff(x[e + 1], -x[e], cs[0][i], cs[1][i], cs[2][i], cs[3][i]));
         }
-      } else {  // pairs (i, i + 64): the partner is 16 lanes away
+      } else {  // pairs (i, i + D/2): the partner is 16 lanes away
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < E; ++e) {
           const float partner = __shfl_xor_sync(0xffffffffu, x[e], 16);
-          const int i = 4 * (lane & 15) + e;
+          const int i = E * (lane & 15) + e;
           o[e] = __float2bfloat16_rn(first ? rotate_diff(x[e], partner, cs[0][i], cs[1][i], cs[2][i], cs[3][i])
                                            : rotate_diff(x[e], -partner, cs[0][i], cs[1][i], cs[2][i], cs[3][i]));
         }
       }
-      const uint2 packed = make_uint2(
-          static_cast<uint32_t>(__bfloat16_as_ushort(o[0])) | (static_cast<uint32_t>(__bfloat16_as_ushort(o[1])) << 16),
-          static_cast<uint32_t>(__bfloat16_as_ushort(o[2])) | (static_cast<uint32_t>(__bfloat16_as_ushort(o[3])) << 16));
+      const VT packed = V::pack(o);
       if (hh < a.Hq) {
-        *reinterpret_cast<uint2*>(qout + static_cast<size_t>(hh) * D + 4 * lane) = packed;
+        *reinterpret_cast<VT*>(qout + static_cast<size_t>(hh) * D + E * lane) = packed;
         continue;
       }
       if (!append) continue;
       const int g = hh - a.Hq;
       const float ks = a.k_scale[g], vs = a.v_scale[g];
-      const float v[4] = {__uint_as_float(vr[r].x << 16), __uint_as_float(vr[r].x & 0xffff0000u),
-                          __uint_as_float(vr[r].y << 16), __uint_as_float(vr[r].y & 0xffff0000u)};
-      const size_t byte = (row0 + g * stride) * HALF + 2 * lane;
-      const uint16_t kc = static_cast<uint16_t>(
-          pack_nibbles(quantize_code4(__bfloat162float(o[0]), ks), quantize_code4(__bfloat162float(o[1]), ks)) |
-          (pack_nibbles(quantize_code4(__bfloat162float(o[2]), ks), quantize_code4(__bfloat162float(o[3]), ks)) << 8));
-      const uint16_t vc = static_cast<uint16_t>(
-          pack_nibbles(quantize_code4(v[0], vs), quantize_code4(v[1], vs)) |
-          (pack_nibbles(quantize_code4(v[2], vs), quantize_code4(v[3], vs)) << 8));
-      *reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(a.k_cache) + byte) = kc;
-      *reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(a.v_cache) + byte) = vc;
+      float v[E];
+      V::unpack(vr[r], v);
+      uint8_t* kd = static_cast<uint8_t*>(a.k_cache) + (row0 + g * stride) * RB + (E * BITS / 8) * lane;
+      uint8_t* vd = static_cast<uint8_t*>(a.v_cache) + (row0 + g * stride) * RB + (E * BITS / 8) * lane;
+      uint32_t kc = 0, vc = 0;
+      if constexpr (BITS == 8) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          kc |= static_cast<uint32_t>(static_cast<uint8_t>(quantize_code(__bfloat162float(o[e]), ks))) << (8 * e);
+          vc |= static_cast<uint32_t>(static_cast<uint8_t>(quantize_code(v[e], vs))) << (8 * e);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < E / 2; ++j) {
+          kc |= static_cast<uint32_t>(pack_nibbles(quantize_code4(__bfloat162float(o[2 * j]), ks),
+                                                   quantize_code4(__bfloat162float(o[2 * j + 1]), ks)))
+                << (8 * j);
+          vc |= static_cast<uint32_t>(pack_nibbles(quantize_code4(v[2 * j], vs), quantize_code4(v[2 * j + 1], vs)))
+                << (8 * j);
+        }
+      }
+      if constexpr (E * BITS / 8 == 4) {
+        *reinterpret_cast<uint32_t*>(kd) = kc;
+        *reinterpret_cast<uint32_t*>(vd) = vc;
+      } else {
+        *reinterpret_cast<uint16_t*>(kd) = static_cast<uint16_t>(kc);
+        *reinterpret_cast<uint16_t*>(vd) = static_cast<uint16_t>(vc);
+      }
       if (a.window > 0) {
-        const size_t w = ((static_cast<size_t>(b) * a.Hkv + g) * a.window + pos % a.window) * D + 4 * lane;
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.k_win) + w) = packed;
-        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.v_win) + w) = vr[r];
+        const size_t w = ((static_cast<size_t>(b) * a.Hkv + g) * a.window + pos % a.window) * D + E * lane;
+        *reinterpret_cast<VT*>(static_cast<__nv_bfloat16*>(a.k_win) + w) = packed;
+        *reinterpret_cast<VT*>(static_cast<__nv_bfloat16*>(a.v_win) + w) = vr[r];
       }
     }
   }
@@ -400,7 +426,7 @@ __global__ void __launch_bounds__(kQ4Warps * 32) rope_append_q4_kernel(const Rop
 }  // namespace
 
 cudaError_t launch_rope_append_q4(const RopeArgs& a, cudaStream_t stream) {
-  rope_append_q4_kernel<<<a.B, kQ4Warps * 32, 0, stream>>>(a);
+  rope_append_qx_kernel<128, 4><<<a.B, kQ4Warps * 32, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -414,15 +440,17 @@ cudaError_t launch_rope_append(const RopeArgs& a, rra_dtype dt, cudaStream_t str
   }
   const dim3 grid(rows, (a.D / 2 + kPairsPerCta - 1) / kPairsPerCta);
   if (dt == RRA_BF16)
-    rope_append_kernel<__nv_bfloat16, false><<<grid, kRopeThreads, 0, stream>>>(a);
+    rope_append_kernel<__nv_bfloat16><<<grid, kRopeThreads, 0, stream>>>(a);
   else
-    rope_append_kernel<float, false><<<grid, kRopeThreads, 0, stream>>>(a);
+    rope_append_kernel<float><<<grid, kRopeThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_rope_append_q8(const RopeArgs& a, cudaStream_t stream) {
-  const dim3 grid(a.B, (a.D / 2 + kPairsPerCta - 1) / kPairsPerCta);
-  rope_append_kernel<__nv_bfloat16, true><<<grid, kRopeThreads, 0, stream>>>(a);
+  if (a.D == 128)
+    rope_append_qx_kernel<128, 8><<<a.B, kQ4Warps * 32, 0, stream>>>(a);
+  else
+    rope_append_qx_kernel<64, 8><<<a.B, kQ4Warps * 32, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
