@@ -223,6 +223,43 @@ def test_many_splits_merge(name, factor, splits):
     _check_step(inp, gpu, q_ref, out_ref)
 
 
+# ------------------------------------------------------------------ many splits, ragged lengths
+@pytest.mark.parametrize("layout,block", [("contiguous", 0), ("paged", 16), ("paged", 256)],
+                         ids=["contiguous", "paged16", "paged256"])
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused_step"])
+def test_many_splits_ragged(layout, block, head_dim, fused):
+    """64 requested splits of a 4096-token capacity (one tile each: 32 splits at D 64) over
+    lengths 70, 1500 and 4000: a sequence whose second split is partial, CTAs past a sequence's
+    end that only return, and a sequence merged in two levels; paged blocks smaller and larger
+    than the tile."""
+    import dataclasses
+    from workloads import gen
+    lens, cap = [70, 1500, 4000], 4096
+    if layout == "contiguous":
+        cfg = dataclasses.replace(CONFIGS["llama3_8b_layer"], name=f"ragged_c_{head_dim}", batch=len(lens),
+                                  head_dim=head_dim, seq_len=max(lens), max_len=cap, num_splits=64)
+    else:
+        nb = cap // block
+        cfg = dataclasses.replace(CONFIGS["batched_paged"], name=f"ragged_p{block}_{head_dim}", batch=len(lens),
+                                  head_dim=head_dim, block_size=block, len_range=(max(lens), max(lens)),
+                                  max_blocks_per_seq=nb, num_blocks=len(lens) * nb + 5, num_splits=64)
+    inp = gen.make_inputs(cfg, seed=31, poison=False)
+    inp.lengths[:] = lens
+    inp.positions[:] = np.array(lens) - 1
+    if inp.block_table is not None:
+        for b, L in enumerate(lens):
+            inp.block_table[b, -(-L // block):] = -1
+    gen.poison_unread(inp)
+    style = 1 if head_dim == 64 else 0
+    gpu = H.run_gpu(inp, fused=fused, rope_style=style)
+    assert gpu.splits == cap // (16384 // (2 * head_dim))
+    q_ref, k_ref, _, out_ref = H.run_oracle(inp, rope_style=style)
+    assert gpu.err == 0
+    _check_step(inp, gpu, q_ref, out_ref)
+    _check_cache(inp, gpu, _oracle_k_rows(inp, k_ref))
+
+
 def test_fused_step_position_errors_are_flagged():
     """A position outside the cache: flagged, that sequence untouched, the others correct."""
     cfg = reduced(CONFIGS["batched_paged"], 16, 4)
