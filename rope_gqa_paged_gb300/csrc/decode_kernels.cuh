@@ -192,6 +192,19 @@ __device__ void merge_partials(const DecodeArgs& a, const float* src_o, const fl
   float* sm_w = scratch;                  // [hpc][count]: m_i, then the weights
   float* sm_l = scratch + hpc * count;    // [hpc][count]
   float* sm_ml = sm_l + hpc * count;      // [hpc][2]: merged (M, l)
+  constexpr int kQ = D / 4;
+  constexpr int kBatch = 16;              // o rows of partials one thread fetches at once
+  const int n_items = hpc * kQ;           // (head, 4 dims) output items
+  // The first batch of this thread's first item is fetched before the weights are known (it
+  // does not depend on them), so its L2 round trip overlaps the (m, l) one.
+  float4 pre[kBatch];
+  if (tid < n_items) {
+    const int h = tid / kQ, d = (tid - h * kQ) * 4;
+    const float4* o = reinterpret_cast<const float4*>(src_o + ((row0 + h) * stride + first) * D + d);
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+      pre[k] = k < count ? __ldcg(o + static_cast<size_t>(k) * kQ) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   for (int i = tid; i < hpc * count; i += nthreads) {
     const int h = i / count, k = i - h * count;
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(src_ml) + (row0 + h) * stride + first + k);
@@ -221,20 +234,32 @@ __device__ void merge_partials(const DecodeArgs& a, const float* src_o, const fl
     }
   }
   named_barrier_sync(1, nthreads);
-  constexpr int kQ = D / 4;
-  for (int i = tid; i < hpc * kQ; i += nthreads) {
+  for (int i = tid; i < n_items; i += nthreads) {
     const int h = i / kQ, d = (i - h * kQ) * 4;
     const float4* o = reinterpret_cast<const float4*>(src_o + ((row0 + h) * stride + first) * D + d);
     const float* wts = sm_w + h * count;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int k = 0; k < count; ++k) {
-      const float wv = wts[k];
-      const float4 v = __ldcg(o + static_cast<size_t>(k) * kQ);
+    auto add = [&](float wv, const float4& v) {
       acc.x = fmaf(wv, v.x, acc.x);
       acc.y = fmaf(wv, v.y, acc.y);
       acc.z = fmaf(wv, v.z, acc.z);
       acc.w = fmaf(wv, v.w, acc.w);
+    };
+    int k0 = 0;
+    if (i == tid) {  // the batch fetched ahead
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (k < count) add(wts[k], pre[k]);
+      k0 = kBatch;
+    }
+    for (; k0 < count; k0 += kBatch) {  // all loads of a batch are issued before its FMAs
+      float4 v[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        v[k] = k0 + k < count ? __ldcg(o + static_cast<size_t>(k0 + k) * kQ) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (k0 + k < count) add(wts[k0 + k], v[k]);
     }
     if (final_row) {
       T* out = static_cast<T*>(a.out) + out_row(row0 + h) * D + d;
