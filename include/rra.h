@@ -316,8 +316,9 @@ RRA_API size_t rra_verify_workspace_bytes(int B, int gamma, int Hq, int Hkv, int
  * tokens, contiguous caches of at least 16384 / (2 D) tokens). No workspace. Head dim 128 runs
  * on the tcgen05 tensor cores (128 prompt tokens of one or two query heads per CTA, one CTA per
  * SM, scores and outputs in Tensor Memory; q_rot and out 16-byte aligned, as checked); head dim
- * 64 on mma.sync (64 query rows per CTA). A prompt that runs past the cache sets
- * RRA_ERR_POSITION and skips b; a pipeline wait that runs out sets RRA_ERR_TIMEOUT. */
+ * 64 on mma.sync (64 query rows per CTA). RRA_ERANGE when (T / 64 + 1) * Hq exceeds 2^31 - 1
+ * (the CTA count of one sequence). A prompt that runs past the cache sets RRA_ERR_POSITION
+ * and skips b; a pipeline wait that runs out sets RRA_ERR_TIMEOUT. */
 RRA_API int rra_prefill_attn(const void* q_rot, const void* k_cache, const void* v_cache, const int32_t* block_table,
                              int max_blocks_per_seq, const int32_t* positions, int block_size, int num_blocks,
                              int max_len, void* out, int B, int T, int Hq, int Hkv, int D, float scale,

@@ -133,9 +133,16 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 2)
   const int qt = kPrefillRows / hpc;  // prompt tokens per CTA
   const int slices = n_rep / hpc;
   const int n_qb = (T + qt - 1) / qt;
-  const int qb = n_qb - 1 - static_cast<int>(blockIdx.x);  // longest blocks first
-  const int slice = blockIdx.y % slices;
-  const int g = blockIdx.y / slices;
+  // One CTA per (query block, KV head, head slice), in index order: band by band of KV heads
+  // whose K and V fit in L2 together, the longest causal blocks of a band first.
+  const int hs_band = (a.kv_band > 0 ? a.kv_band : a.Hkv) * slices;  // (KV head, slice) pairs per band
+  const int band_ctas = n_qb * hs_band;
+  const int band = static_cast<int>(blockIdx.x) / band_ctas;
+  const int j = static_cast<int>(blockIdx.x) - band * band_ctas;
+  const int qb = n_qb - 1 - j / hs_band;
+  const int hs = band * hs_band + j % hs_band;
+  const int slice = hs % slices;
+  const int g = hs / slices;
   const int h0 = g * n_rep + slice * hpc;
   const int b = blockIdx.z;
   const int q0 = qb * qt;
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, 2)
 
   const int p0 = a.positions[b];
   if (p0 < 0 || p0 + T > a.capacity) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) flag_error(a.err, RRA_ERR_POSITION);
+    if (threadIdx.x == 0 && blockIdx.x == 0) flag_error(a.err, RRA_ERR_POSITION);
     return;
   }
   const int q_end = min(T, q0 + qt);
@@ -331,7 +338,7 @@ cudaError_t launch_prefill_t(const DecodeArgs& a, const CUtensorMap& km, const C
   cudaError_t e = ensure_smem(kern, C::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   const int qt = kPrefillRows / a.hpc;
-  const dim3 grid((a.gamma + qt - 1) / qt, a.Hkv * ((a.Hq / a.Hkv) / a.hpc), a.B);
+  const dim3 grid(((a.gamma + qt - 1) / qt) * (a.Hkv * ((a.Hq / a.Hkv) / a.hpc)), 1, a.B);
   return launch_pdl(kern, grid, dim3(C::kThreads), C::kSmemBytes, st, km, vm, a);
 }
 

@@ -138,8 +138,15 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
 
   const int T = a.gamma;
   const int n_qb = (T + kRows - 1) / kRows;
-  const int qb = n_qb - 1 - static_cast<int>(blockIdx.x);  // longest blocks first
-  const int h0 = blockIdx.y * NQ;                          // query heads h0 .. h0 + NQ - 1, one KV group
+  // One CTA per (query block, head group). The GPU starts CTAs in index order: within a band of
+  // KV groups whose K and V fit in L2 together, the longest causal blocks of all its head groups
+  // come first (the short ones make the tail), then the next band.
+  const int hg_band = (a.kv_band > 0 ? a.kv_band : a.Hkv) * ((a.Hq / a.Hkv) / NQ);  // head groups per band
+  const int band_ctas = n_qb * hg_band;
+  const int band = static_cast<int>(blockIdx.x) / band_ctas;
+  const int j = static_cast<int>(blockIdx.x) - band * band_ctas;
+  const int qb = n_qb - 1 - j / hg_band;
+  const int h0 = (band * hg_band + j % hg_band) * NQ;  // query heads h0 .. h0 + NQ - 1, one KV group
   const int g = h0 / (a.Hq / a.Hkv);
   const int b = blockIdx.z;
   const int q0 = qb * kRows;
@@ -151,7 +158,7 @@ __global__ void __launch_bounds__(Cfg<NQ>::kThreads, 1)
 
   const int p0 = a.positions[b];
   if (p0 < 0 || p0 + T > a.capacity) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) flag_error(a.err, RRA_ERR_POSITION);
+    if (threadIdx.x == 0 && blockIdx.x == 0) flag_error(a.err, RRA_ERR_POSITION);
     return;
   }
   const int q_end = min(T, q0 + kRows);
@@ -444,7 +451,7 @@ cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& qm, const CUtensorM
   auto kern = prefill_tc_kernel<NQ, PAGED>;
   cudaError_t e = ensure_smem(kern, C::kSmemBytes, done);
   if (e != cudaSuccess) return e;
-  const dim3 grid((a.gamma + kRows - 1) / kRows, a.Hq / NQ, a.B);
+  const dim3 grid(((a.gamma + kRows - 1) / kRows) * (a.Hq / NQ), 1, a.B);
   return launch_pdl(kern, grid, dim3(C::kThreads), C::kSmemBytes, st, qm, km, vm, a);
 }
 

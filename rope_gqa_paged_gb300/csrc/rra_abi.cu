@@ -201,6 +201,27 @@ int prefill_hpc(int n_rep) {
   return 1;
 }
 
+// Limits of a prefill launch, checked before anything is enqueued: a capacity of at most 2^30
+// tokens, head groups within the grid's second dimension, and the CTAs of one sequence (query
+// blocks of at least 64 / hpc prompt tokens x head groups, or 128 tokens x pairs of heads) within
+// its first: at most (T / 64 + 1) * Hq.
+int check_prefill_limits(int T, int Hq, int Hkv, int64_t capacity) {
+  if (capacity > (int64_t(1) << 30)) return RRA_ERANGE;
+  const int n_rep = Hq / Hkv;
+  if (int64_t(Hkv) * (n_rep / prefill_hpc(n_rep)) > 65535) return RRA_ERANGE;
+  if ((int64_t(T) / 64 + 1) * Hq > int64_t(INT32_MAX)) return RRA_ERANGE;
+  return RRA_OK;
+}
+
+// KV groups per prefill scheduling band: as many as have their prompt's K and V (T x D x 2 x
+// 2 bytes each, bf16) within 64 MB, half of the L2, and divide Hkv; at least one.
+int prefill_kv_band(int T, int Hkv, int D) {
+  const int64_t per_group = int64_t(T) * D * 4;
+  int g = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(Hkv, (int64_t(64) << 20) / per_group)));
+  while (Hkv % g != 0) --g;
+  return g;
+}
+
 // Partial rows of the verify kernel: 16 per (sequence, KV head, head slice).
 int64_t verify_rows(int B, int gamma, int Hq, int Hkv) {
   return int64_t(B) * Hkv * ((Hq / Hkv) / verify_hpc(Hq / Hkv, gamma)) * 16;
@@ -965,10 +986,10 @@ int rra_prefill_attn(const void* q_rot, const void* k_cache, const void* v_cache
     if (max_len < rra::decode_mma_tile_tokens(D)) return RRA_EUNSUPPORTED;
     capacity = max_len;
   }
-  if (capacity > (int64_t(1) << 30)) return RRA_ERANGE;
+  st = check_prefill_limits(T, Hq, Hkv, capacity);
+  if (st != RRA_OK) return st;
   const int n_rep = Hq / Hkv;
   const int hpc = prefill_hpc(n_rep);
-  if (int64_t(Hkv) * (n_rep / hpc) > 65535) return RRA_ERANGE;
   if (B == 0) return RRA_OK;
   if (!q_rot || !k_cache || !v_cache || !positions || !out) return RRA_EINVAL;
   if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return RRA_EINVAL;
@@ -994,6 +1015,7 @@ int rra_prefill_attn(const void* q_rot, const void* k_cache, const void* v_cache
   a.D = D;
   a.hpc = hpc;
   a.gamma = T;
+  a.kv_band = prefill_kv_band(T, Hkv, D);
   a.positions = positions;
   a.block_table = block_table;
   a.max_blocks_per_seq = max_blocks_per_seq;
@@ -1026,6 +1048,10 @@ int rra_prefill_step(const void* q, const void* k_new, const void* v_new, const 
   if (T < 1) return RRA_EINVAL;
   if (block_table != nullptr ? (!pow2(block_size) || block_size < 8) : max_len < rra::decode_mma_tile_tokens(D))
     return block_table != nullptr && block_size <= 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
+  st = check_prefill_limits(T, Hq, Hkv,
+                            block_table != nullptr ? int64_t(max_blocks_per_seq) * block_size : int64_t(max_len));
+  if (st != RRA_OK) return st;
+  if (int64_t(B) * T > int64_t(INT32_MAX)) return RRA_ERANGE;  // rows of q / q_out / out
   st = check_step_args(q, k_new, v_new, positions, q_out, k_cache, v_cache, out, B * T, Hq, D, rope_base, rope_style,
                        scale, RRA_BF16);
   if (st != RRA_OK || B == 0) return st;

@@ -84,6 +84,9 @@ struct DecodeArgs {
   // Speculative verify (verify.cuh): gamma new tokens per sequence at positions[b] ..
   // positions[b] + gamma - 1; q and out are [B, gamma, Hq, D].
   int gamma;
+  // Prefill: CTAs run band by band, a band being kv_band KV groups (0: all of them) whose keys
+  // and values fit in L2 together, longest query blocks first within a band.
+  int kv_band;
   double theta_pi[kMaxDecodeHeadDim / 2];  // theta_i / pi, theta_i = base^(-2i/D)
 };
 

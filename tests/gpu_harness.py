@@ -252,7 +252,8 @@ def run_oracle_verify(inp: DecodeInputs, rope_style: int = 0):
 
 
 def run_gpu_prefill(inp: DecodeInputs, rope_style: int = 0, device="cuda:0", fused: bool = True) -> GpuResult:
-    """One prefill step (T = gamma prompt tokens per sequence) through the C ABI."""
+    """One prefill step (T = gamma prompt tokens per sequence) through the C ABI. The output is
+    filled with NaN first, so a row that no CTA writes cannot pass for a result."""
     from rope_gqa_paged_gb300 import PrefillStep
 
     cfg = inp.cfg
@@ -262,6 +263,7 @@ def run_gpu_prefill(inp: DecodeInputs, rope_style: int = 0, device="cuda:0", fus
                        rope_base=cfg.rope_base, rope_style=rope_style)
     args = (to_torch(inp.q, "bf16", device), to_torch(inp.k_new, "bf16", device), to_torch(inp.v_new, "bf16", device),
             to_torch(inp.positions, "i32", device))
+    step.out.fill_(float("nan"))
     out = step(*args) if fused else step(*args, seq_lens=True)
     torch.cuda.synchronize(device)
     res = GpuResult(q_rot=to_numpy(step.q_rot), out=to_numpy(out), k_cache=to_numpy(kc), v_cache=to_numpy(vc),

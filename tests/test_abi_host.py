@@ -178,6 +178,9 @@ def test_prefill_and_verify_argument_checks(rra):
     assert a(P, P, P, P, 64, P, 4, 100, 0, P, 1, 8, 32, 8, 128, 0.0, None, None) == RRA_EUNSUPPORTED  # block < 8
     assert a(P, P, P, None, 0, P, 0, 0, 32, P, 1, 8, 32, 8, 128, 0.0, None, None) == RRA_EUNSUPPORTED  # short cache
     assert a(P + 8, P, P, P, 64, P, 16, 100, 0, P, 1, 8, 32, 8, 128, 0.0, None, None) == RRA_EINVAL  # misaligned
+    big_t = (1 << 30) - 1                                                                           # CTAs
+    assert a(P, P, P, P, 1 << 20, P, 1024, 100, 0, P, 1, big_t, 256, 8, 128, 0.0, None, None) == RRA_ERANGE
+    assert a(P, P, P, P, 1 << 20, P, 1024, 100, 0, P, 0, big_t, 64, 8, 128, 0.0, None, None) == RRA_OK
     v = lib.rra_verify_attn
     # (q, kc, vc, table, mbps, pos, bs, nblk, max_len, out, B, gamma, Hq, Hkv, D, scale, splits, ws, ws_bytes, err, st)
     assert v(P, P, P, P, 64, P, 16, 100, 0, P, 1, 4, 32, 8, 128, 0.0, 8, None, 0, None, None) == RRA_EWORKSPACE
