@@ -185,7 +185,10 @@ struct SameRow {
 // Merges partials first .. first+count-1 of rows row0 .. row0+hpc-1 of a [rows][stride]
 // partial array into the final output rows out_row(row0 + h) (dst_o == nullptr) or into one
 // partial at index dst_idx of a [rows][dst_stride] partial array.
-template <typename T, int D, typename OutRow = SameRow>
+// EARLY: the partial outputs are fetched 16 at a time per thread, the first batch before the
+// weights are known (one output item per thread, as the decode kernels have); otherwise 8 at a
+// time after them (the verify kernel, with several items per thread, measured faster so).
+template <typename T, int D, typename OutRow = SameRow, bool EARLY = true>
 __device__ void merge_partials(const DecodeArgs& a, const float* src_o, const float* src_ml, int stride, int first,
                                int count, int hpc, size_t row0, float* dst_o, float* dst_ml, int dst_stride,
                                int dst_idx, float* scratch, int tid, int nthreads, OutRow out_row = OutRow()) {
@@ -198,7 +201,7 @@ __device__ void merge_partials(const DecodeArgs& a, const float* src_o, const fl
   // The first batch of this thread's first item is fetched before the weights are known (it
   // does not depend on them), so its L2 round trip overlaps the (m, l) one.
   float4 pre[kBatch];
-  if (tid < n_items) {
+  if (EARLY && tid < n_items) {
     const int h = tid / kQ, d = (tid - h * kQ) * 4;
     const float4* o = reinterpret_cast<const float4*>(src_o + ((row0 + h) * stride + first) * D + d);
 #pragma unroll
@@ -245,8 +248,12 @@ __device__ void merge_partials(const DecodeArgs& a, const float* src_o, const fl
       acc.z = fmaf(wv, v.z, acc.z);
       acc.w = fmaf(wv, v.w, acc.w);
     };
-    int k0 = 0;
-    if (i == tid) {  // the batch fetched ahead
+    if constexpr (!EARLY) {
+#pragma unroll 8
+      for (int k = 0; k < count; ++k) add(wts[k], __ldcg(o + static_cast<size_t>(k) * kQ));
+    }
+    int k0 = EARLY ? 0 : count;
+    if (EARLY && i == tid) {  // the batch fetched ahead
 #pragma unroll
       for (int k = 0; k < kBatch; ++k)
         if (k < count) add(wts[k], pre[k]);
@@ -281,26 +288,26 @@ __device__ void merge_partials(const DecodeArgs& a, const float* src_o, const fl
 // groups of kMergeFanIn: the last arrival of each group merges the group into a level-2
 // partial, and the last group to finish merges the level-2 partials into the output, so no
 // single CTA has to read every split at the end of the kernel.
-template <typename T, int D, typename OutRow = SameRow>
+template <typename T, int D, typename OutRow = SameRow, bool EARLY = true>
 __device__ __forceinline__ void finish_split_rows(const DecodeArgs& a, size_t row0, int hpc, int split, int n,
                                                   float* scratch, int* s_flag, int tid, int nthreads,
                                                   OutRow out_row = OutRow()) {
   const int S = a.num_splits, G = a.num_groups;
   if (n <= kMergeFanIn) {
     if (arrive_last(a.counters + row0, n, s_flag, a.err, tid, nthreads))
-      merge_partials<T, D>(a, a.ws_o, a.ws_ml, S, 0, n, hpc, row0, nullptr, nullptr, 0, 0, scratch, tid, nthreads,
-                           out_row);
+      merge_partials<T, D, OutRow, EARLY>(a, a.ws_o, a.ws_ml, S, 0, n, hpc, row0, nullptr, nullptr, 0, 0, scratch,
+                                          tid, nthreads, out_row);
     return;
   }
   const int grp = split / kMergeFanIn, first = grp * kMergeFanIn;
   const int gsize = min(kMergeFanIn, n - first);
   if (!arrive_last(a.group_counters + row0 * G + grp, gsize, s_flag, a.err, tid, nthreads)) return;
-  merge_partials<T, D>(a, a.ws_o, a.ws_ml, S, first, gsize, hpc, row0, a.ws2_o, a.ws2_ml, G, grp, scratch, tid,
-                       nthreads);
+  merge_partials<T, D, SameRow, EARLY>(a, a.ws_o, a.ws_ml, S, first, gsize, hpc, row0, a.ws2_o, a.ws2_ml, G, grp,
+                                       scratch, tid, nthreads);
   const int groups = (n + kMergeFanIn - 1) / kMergeFanIn;
   if (arrive_last(a.counters + row0, groups, s_flag, a.err, tid, nthreads))
-    merge_partials<T, D>(a, a.ws2_o, a.ws2_ml, G, 0, groups, hpc, row0, nullptr, nullptr, 0, 0, scratch, tid,
-                         nthreads, out_row);
+    merge_partials<T, D, OutRow, EARLY>(a, a.ws2_o, a.ws2_ml, G, 0, groups, hpc, row0, nullptr, nullptr, 0, 0,
+                                        scratch, tid, nthreads, out_row);
 }
 
 template <typename T, int D>

@@ -393,8 +393,9 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   }
   if (n_work > 1) {
     __shared__ int s_last;
-    finish_split_rows<__nv_bfloat16, D>(a, vbase, rows, split, n_work, reinterpret_cast<float*>(smem), &s_last,
-                                        threadIdx.x, kConsumers, out_row);
+    finish_split_rows<__nv_bfloat16, D, VerifyRows, false>(a, vbase, rows, split, n_work,
+                                                           reinterpret_cast<float*>(smem), &s_last, threadIdx.x,
+                                                           kConsumers, out_row);
   }
 }
 
