@@ -80,23 +80,19 @@ def test_prefill_position_errors_are_flagged():
     assert gpu.err & RRA_ERR_POSITION
 
 
-@pytest.mark.slow
-def test_prefill_128k_sampled_rows():
-    """The full 128K prompt; a few rows checked one by one against the oracle's definition, and
-    every row written (the output starts as NaN; this size runs its CTAs in bands of one KV head)."""
-    cfg = CONFIGS["prefill_128k"]
-    inp = make_inputs(cfg)
-    gpu = H.run_gpu_prefill(inp)
+def _check_sampled_rows(inp, gpu, rows):
+    """Every output value written (the harness starts from NaN), and the given prompt rows (one
+    sequence, prompt from position 0) checked one by one against the oracle's definition."""
     assert gpu.err == 0
     bits = np.asarray(gpu.out).view(np.uint16)
     nan = ((bits & 0x7F80) == 0x7F80) & ((bits & 0x007F) != 0)
     assert not nan.any(), f"{int(nan.sum())} output values never written"
-    T = cfg.gamma
+    T = inp.cfg.gamma
     pos = np.arange(T)
     k_rot = oracle.f64_to_bf16_bits(oracle.apply_rope(oracle.bf16_bits_to_f64(inp.k_new[0]), pos[:, None]))
     kf = oracle.bf16_bits_to_f64(k_rot)                           # [T, Hkv, D]
     vf = oracle.bf16_bits_to_f64(inp.v_new[0])
-    for t in (0, 1, 63, 4095, 70001, T - 1):
+    for t in rows:
         q_rot = oracle.f64_to_bf16_bits(oracle.apply_rope(oracle.bf16_bits_to_f64(inp.q[0, t]), np.array([t])))
         H.assert_close_stored(gpu.q_rot[0, t], q_rot, "bf16", f"q_rot {t}")
         want = oracle.gqa_decode_attention(oracle.bf16_bits_to_f64(q_rot), np.transpose(kf[: t + 1], (1, 0, 2)),
@@ -105,3 +101,21 @@ def test_prefill_128k_sampled_rows():
         assert e <= H.OUT_ATOL["bf16"], (t, e)
         rel = H.rel_rms_error(gpu.out[0, t], want, "bf16")
         assert rel <= H.REL_RMS_BAR, (t, rel)
+
+
+@pytest.mark.slow
+def test_prefill_128k_sampled_rows():
+    """The full 128K prompt (its CTAs run in bands of one KV head: 64 MB of K and V each)."""
+    cfg = CONFIGS["prefill_128k"]
+    inp = make_inputs(cfg)
+    _check_sampled_rows(inp, H.run_gpu_prefill(inp), (0, 1, 63, 4095, 70001, cfg.gamma - 1))
+
+
+@pytest.mark.parametrize("head_dim", [64, 128])
+def test_prefill_40k_bands_sampled_rows(head_dim):
+    """A 40000-token prompt: its CTAs run in bands of 4 (D 64) or 2 (D 128) of the 8 KV heads,
+    the bands whose K and V fit in 64 MB; rows of the first and last query blocks and between."""
+    T = 40000
+    inp = _inputs(_cfg("paged", 0, T, batch=1, block_size=32, head_dim=head_dim), seed=40)
+    rows = (0, 5, 127, 128, 20011, 39871, T - 1)
+    _check_sampled_rows(inp, H.run_gpu_prefill(inp), rows)
