@@ -27,6 +27,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import time
 
 import numpy as np
@@ -169,7 +170,7 @@ class ClockSampler:
               "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_uuid):
-        self.path = os.path.join(ROOT, "gpurun_out", f".clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"rra_clocks_{os.getpid()}.csv")
         self.proc = None
         self.gpu = gpu_uuid
 
