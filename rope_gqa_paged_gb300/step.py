@@ -71,7 +71,8 @@ class DecodeStep:
         self.rope_append(q, k_new, v_new, positions, stream)
         return self.attend(seq_lens, stream)
 
-    def capture(self, q, k_new, v_new, positions, seq_lens=None, repeat: int = 1, between=None):
+    def capture(self, q, k_new, v_new, positions, seq_lens=None, repeat: int = 1, between=None, before=None,
+                after=None):
         """Record the step (``repeat`` times back to back, calling ``between()`` before each
         repetition after the first) into a CUDA graph; returns it and keeps it for ``replay()``.
 
@@ -79,18 +80,27 @@ class DecodeStep:
         and error buffers: refill the inputs in place, then ``replay()``. Replaying saves
         the host-side launch cost of every kernel of the step, and inside one graph each
         decode kernel overlaps its launch with the end of the kernel before it.
+        ``before()`` / ``after()`` record work around every repetition into the same graph,
+        e.g. the copy of the step's inputs from pinned host memory and of its output back.
         """
+        def one():
+            if before is not None:
+                before()
+            self(q, k_new, v_new, positions, seq_lens)
+            if after is not None:
+                after()
+
         side = torch.cuda.Stream(device=q.device)
         side.wait_stream(torch.cuda.current_stream(q.device))
         with torch.cuda.stream(side):
-            self(q, k_new, v_new, positions, seq_lens)
+            one()
         torch.cuda.current_stream(q.device).wait_stream(side)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for i in range(repeat):
                 if i and between is not None:
                     between()
-                self(q, k_new, v_new, positions, seq_lens)
+                one()
         self.graph = graph
         return graph
 
