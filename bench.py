@@ -194,32 +194,38 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         try:
-            rows = [ln.split(",") for ln in open(self.path) if ln.strip()]
+            with open(self.path) as f:
+                lines = f.readlines()
         except OSError:
-            rows = []
-        for r in rows:
-            r = [x.strip() for x in r]
-            if len(r) < 8:
-                continue
-            try:
-                sm.append(float(r[0]))
-                mx.append(float(r[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, r[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
+            lines = []
         try:
             os.remove(self.path)
         except OSError:
             pass
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return summarize_clock_samples(lines)
+
+
+def summarize_clock_samples(lines):
+    """nvidia-smi rows in ClockSampler.FIELDS order -> {sm_mhz (median), sm_max_mhz, reasons
+    (throttle reasons seen active in any sample), samples}, or None without a usable row."""
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ln in lines:
+        r = [x.strip() for x in ln.split(",")]
+        if len(r) < 8:
+            continue
+        try:
+            sm.append(float(r[0]))
+            mx.append(float(r[1]))
+        except ValueError:
+            continue
+        for n, v in zip(names, r[4:8]):
+            if v.lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # ---------------------------------------------------------------------------- our arm
