@@ -372,13 +372,16 @@ RRA_API int rra_use_device(int device);
  * start-up because allocating can block, fail or fragment memory mid-run. It allocates
  * nothing and calls no allocating routine.
  *   - The array holds rra_noalloc_scratch_bytes() (16 MiB) on every GPU that loads the
- *     library, kept until the process exits. A step whose effective split count needs more
- *     (rra_decode_workspace_bytes) returns RRA_EWORKSPACE before anything is launched;
- *     ask for fewer splits then.
+ *     library, kept until the process exits: its first 1 MiB holds the split merge's
+ *     arrival counters (at the same place for every shape), the other 15 MiB the split
+ *     partials. A step whose effective split count needs more than that (for instance
+ *     rra_decode_workspace_bytes above 15 MiB) returns RRA_EWORKSPACE before anything is
+ *     enqueued; ask for fewer splits then.
+ *   - The counters must be zero when the kernel starts: every call clears the ones it
+ *     uses with a cudaMemsetAsync on `stream` before its launch (this allocates nothing),
+ *     so each call is independent of what earlier calls, of any shape, left in the array.
  *   - All calls on a device share the array: calls whose kernels overlap on the GPU race
  *     and give wrong results. Keep them on one stream or serialise them.
- *   - Its split counters must start at zero: the array starts zeroed when the library is
- *     loaded and every call leaves the counters at zero again.
  *   - The first call on each device (with that device current) looks up the array's
  *     device address; make that first call before any stream capture starts.
  * Arguments as in rra_decode_attn_paged, without workspace and ws_bytes. */

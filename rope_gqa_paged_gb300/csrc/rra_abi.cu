@@ -254,6 +254,18 @@ size_t workspace_bytes(int B, int Hq, int D, int splits) {
   return ws_layout(B, Hq, D, splits).total;
 }
 
+// The partial arrays alone (everything before the counters), and the counters alone in int32s.
+size_t partial_bytes(int B, int Hq, int D, int splits) {
+  if (splits <= 1 || B <= 0) return 0;
+  return ws_layout(B, Hq, D, splits).cnt;
+}
+
+size_t counter_ints(int B, int Hq, int splits) {
+  if (splits <= 1 || B <= 0) return 0;
+  const size_t R = size_t(B) * Hq, G = (size_t(splits) + rra::kMergeFanIn - 1) / rra::kMergeFanIn;
+  return R + R * G;
+}
+
 // Tiled tensor map over `base` (rank 3 or 4, dims innermost first, strides in bytes of dims 1..).
 int encode_map_typed(CUtensorMap* map, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
                      const cuuint32_t* box, CUtensorMapDataType type, CUtensorMapSwizzle swizzle) {
@@ -329,8 +341,11 @@ int check_workspace(const Plan& p, int B, int Hq, int D, const void* ws, size_t 
   return RRA_OK;
 }
 
+// counters: when set, the arrival counters live there ([B*Hq] counters, then [B*Hq, G] group
+// counters) instead of inside `ws`, which then holds only the partial arrays.
 rra::DecodeArgs decode_args(const Plan& p, const void* q, const void* k, const void* v, const int32_t* seq_lens,
-                            void* out, int B, int Hq, int Hkv, int D, float scale, void* ws, int32_t* err) {
+                            void* out, int B, int Hq, int Hkv, int D, float scale, void* ws, int32_t* err,
+                            int* counters = nullptr) {
   rra::DecodeArgs a{};
   a.q = q;
   a.k = k;
@@ -357,6 +372,10 @@ rra::DecodeArgs decode_args(const Plan& p, const void* q, const void* k, const v
     a.ws2_ml = reinterpret_cast<float*>(base + l.ml2);
     a.counters = reinterpret_cast<int*>(base + l.cnt);
     a.group_counters = reinterpret_cast<int*>(base + l.gcnt);
+    if (counters != nullptr) {
+      a.counters = counters;
+      a.group_counters = counters + size_t(B) * Hq;
+    }
   }
   return a;
 }
@@ -718,6 +737,22 @@ int rra_decode_attn_paged(const void* q_rot, const void* k_pool, const void* v_p
                           int max_blocks_per_seq, const int32_t* seq_lens, int block_size, int num_blocks, void* out,
                           int B, int Hq, int Hkv, int D, float scale, int num_splits, void* workspace,
                           size_t ws_bytes, rra_dtype dt, int32_t* err_flag, void* stream) {
+  return rra::decode_attn_paged_ext(q_rot, k_pool, v_pool, block_table, max_blocks_per_seq, seq_lens, block_size,
+                                    num_blocks, out, B, Hq, Hkv, D, scale, num_splits, workspace, ws_bytes, nullptr,
+                                    dt, err_flag, stream);
+}
+
+}  // extern "C"
+
+namespace rra {
+
+size_t decode_partial_bytes(int B, int Hq, int D, int splits) { return partial_bytes(B, Hq, D, splits); }
+size_t decode_counter_ints(int B, int Hq, int splits) { return counter_ints(B, Hq, splits); }
+
+int decode_attn_paged_ext(const void* q_rot, const void* k_pool, const void* v_pool, const int32_t* block_table,
+                          int max_blocks_per_seq, const int32_t* seq_lens, int block_size, int num_blocks, void* out,
+                          int B, int Hq, int Hkv, int D, float scale, int num_splits, void* workspace,
+                          size_t ws_bytes, int* counters, rra_dtype dt, int32_t* err_flag, void* stream) {
   if (!pow2(block_size)) return block_size <= 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
   if (max_blocks_per_seq < 1 || num_blocks < 1) return RRA_EINVAL;
   const int64_t capacity = int64_t(max_blocks_per_seq) * block_size;
@@ -728,7 +763,12 @@ int rra_decode_attn_paged(const void* q_rot, const void* k_pool, const void* v_p
   if (!q_rot || !k_pool || !v_pool || !block_table || !seq_lens || !out) return RRA_EINVAL;
   if (!aligned16(q_rot) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out)) return RRA_EINVAL;
   if (!std::isfinite(scale)) return RRA_EINVAL;
-  st = check_workspace(p, B, Hq, D, workspace, ws_bytes);
+  if (counters == nullptr) {
+    st = check_workspace(p, B, Hq, D, workspace, ws_bytes);
+  } else if (p.splits > 1 &&
+             (workspace == nullptr || !aligned16(workspace) || ws_bytes < partial_bytes(B, Hq, D, p.splits))) {
+    st = RRA_EWORKSPACE;
+  }
   if (st != RRA_OK) return st;
   const int box_rows = block_size < p.tile ? block_size : p.tile;
   CUtensorMap km, vm;
@@ -736,7 +776,8 @@ int rra_decode_attn_paged(const void* q_rot, const void* k_pool, const void* v_p
   if (st != RRA_OK) return st;
   st = encode_pool_map(&vm, v_pool, num_blocks, block_size, Hkv, D, box_rows, dt, p.mma);
   if (st != RRA_OK) return st;
-  rra::DecodeArgs a = decode_args(p, q_rot, k_pool, v_pool, seq_lens, out, B, Hq, Hkv, D, scale, workspace, err_flag);
+  rra::DecodeArgs a =
+      decode_args(p, q_rot, k_pool, v_pool, seq_lens, out, B, Hq, Hkv, D, scale, workspace, err_flag, counters);
   a.block_table = block_table;
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.log2_bs = ilog2(block_size);
@@ -746,6 +787,10 @@ int rra_decode_attn_paged(const void* q_rot, const void* k_pool, const void* v_p
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   return finish_decode(rra::launch_decode_paged(a, km, vm, dt, p.mma, s));
 }
+
+}  // namespace rra
+
+extern "C" {
 
 int rra_decode_step_contig(const void* q, const void* k_new, const void* v_new, const int32_t* positions, void* q_out,
                            void* k_cache, void* v_cache, int max_len, void* out, int B, int Hq, int Hkv, int D,

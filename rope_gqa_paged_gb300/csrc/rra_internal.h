@@ -100,6 +100,18 @@ constexpr int kMaxSplits = 1024;
 // Splits merged by one CTA; more splits are merged in two levels.
 constexpr int kMergeFanIn = 32;
 
+// rra_decode_attn_paged with the split arrival counters at `counters` (decode_counter_ints
+// int32s, all zero when the kernel starts) and only the partial arrays (decode_partial_bytes)
+// in `workspace`. counters == nullptr: exactly rra_decode_attn_paged.
+int decode_attn_paged_ext(const void* q_rot, const void* k_pool, const void* v_pool, const int32_t* block_table,
+                          int max_blocks_per_seq, const int32_t* seq_lens, int block_size, int num_blocks, void* out,
+                          int B, int Hq, int Hkv, int D, float scale, int num_splits, void* workspace,
+                          size_t ws_bytes, int* counters, rra_dtype dt, int32_t* err_flag, void* stream);
+// Bytes of the partial arrays, and int32 arrival counters, of a decode with an effective split
+// count (both 0 when splits <= 1).
+size_t decode_partial_bytes(int B, int Hq, int D, int splits);
+size_t decode_counter_ints(int B, int Hq, int splits);
+
 // Stores the text rra_last_cuda_error() returns on this thread.
 void record_cuda_error(cudaError_t e, const char* where);
 
