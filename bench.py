@@ -21,7 +21,6 @@ if "--impl" in sys.argv and "reference" in sys.argv or "--cpu-worker" in sys.arg
         _os.environ[_v] = "1"           # the oracle runs on exactly one host core
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -42,6 +41,10 @@ METRIC = "decode-attn KV GB/s & % of GB300 HBM peak; decode steps/s per layer"
 PREFILL_METRIC = "prefill causal attention TFLOP/s & % of GB300 bf16 tensor peak"
 UNIT = "GB/s"
 DEFAULT_WORKLOAD = "batched_paged"
+EXTRA_WORKLOAD = "long_context"
+# keys of a workload record that the extra record does not repeat (they describe the whole line)
+SHARED_KEYS = ("metric", "n_gpus", "steps", "warmup", "higher_is_better", "scaling", "vs_baseline", "data",
+               "cpu_baseline")
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 2 ** 20
@@ -64,7 +67,9 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=sorted(CONFIGS), default=DEFAULT_WORKLOAD)
+    p.add_argument("--workload", choices=sorted(CONFIGS), default=None,
+                   help=f"default: {DEFAULT_WORKLOAD}, with a {EXTRA_WORKLOAD} record in the same line")
+    p.add_argument("--no-extra", action="store_true", help=f"default workload only (no {EXTRA_WORKLOAD} record)")
     p.add_argument("--num-splits", type=int, default=-1, help="-1: the workload's own setting (0 = library choice)")
     p.add_argument("--batch", type=int, default=0,
                    help="override the batch (a smaller case for profiling; the paged pool shrinks to fit)")
@@ -142,25 +147,23 @@ def kernel_source_hash(cfg) -> str:
     return h.hexdigest()[:16]
 
 
+TRAFFIC_FILE = os.path.join("profiles", "traffic.json")
+
+
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the workload's dominant kernel from the committed ncu summary
-    (the profiles/*.md file whose ``workload:`` line names it), if its kernel sources are unchanged."""
+    """DRAM bytes per launch of the workload's dominant kernel from the committed ncu capture
+    (``profiles/traffic.json``, one record per workload), if its kernel sources are unchanged."""
     if workload not in CONFIGS:
         return None
-    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
-        vals = {}
-        with open(path, encoding="utf-8") as f:
-            for line in f:
-                for key in ("workload", "traffic_bytes_per_launch", "kernel_source_sha256"):
-                    if line.strip().startswith(key + ":"):
-                        vals[key] = line.split(":", 1)[1].strip().split()[0]
-        if vals.get("workload") != workload:
-            continue
-        if vals.get("kernel_source_sha256") != kernel_source_hash(CONFIGS[workload]) or \
-                "traffic_bytes_per_launch" not in vals:
-            return None
-        return int(vals["traffic_bytes_per_launch"])
-    return None
+    try:
+        with open(os.path.join(ROOT, TRAFFIC_FILE), encoding="utf-8") as f:
+            rec = json.load(f).get(workload)
+    except (OSError, ValueError):
+        return None
+    if not isinstance(rec, dict) or rec.get("kernel_source_sha256") != kernel_source_hash(CONFIGS[workload]):
+        return None
+    t = rec.get("traffic_bytes_per_launch")
+    return int(t) if isinstance(t, int) and t > 0 else None
 
 
 class ClockSampler:
@@ -230,7 +233,7 @@ def summarize_clock_samples(lines):
 
 # ---------------------------------------------------------------------------- our arm
 def workload_config(args):
-    cfg = CONFIGS[args.workload]
+    cfg = CONFIGS[args.workload or DEFAULT_WORKLOAD]
     if args.batch and args.batch != cfg.batch:
         import dataclasses
         import math
@@ -293,7 +296,7 @@ def device_workload(cfg, seed, device):
 def run_ours(args):
     import torch
 
-    from rope_gqa_paged_gb300 import DecodeStep, DecodeStepQ8, PrefillStep, VerifyStep, _build
+    from rope_gqa_paged_gb300 import _build
 
     rank, local_rank, world = dist_env()
     if world > 1:
@@ -307,7 +310,34 @@ def run_ours(args):
     _build.build()                                    # no-op when the library is current
 
     cfg = workload_config(args)
-    splits_arg = cfg.num_splits if args.num_splits < 0 else args.num_splits
+    line = measure(args, cfg, device, rank, world)
+    # The default run also measures the 128K long-context step (the second configuration the
+    # >= 70 %-of-HBM target names) in the same process, at its configured 128 splits.
+    extra = None
+    if args.workload is None and not args.no_extra:
+        import gc
+        gc.collect()
+        torch.cuda.empty_cache()
+        extra = measure(args, CONFIGS[EXTRA_WORKLOAD], device, rank, world, splits_override=-1)
+    if rank != 0:
+        return 0
+    if extra is not None:
+        line[EXTRA_WORKLOAD] = {k: v for k, v in extra.items() if k not in SHARED_KEYS}
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg.name, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def measure(args, cfg, device, rank, world, splits_override=None):
+    """Times one workload's step (per-kernel eager times, the captured step, clocks, e2e) and
+    returns its JSON record (without the CPU baseline)."""
+    import torch
+
+    from rope_gqa_paged_gb300 import DecodeStep, DecodeStepQ8, PrefillStep, VerifyStep
+
+    nsplit = args.num_splits if splits_override is None else splits_override
+    splits_arg = cfg.num_splits if nsplit < 0 else nsplit
     w, lengths = device_workload(cfg, cfg.seed + rank, device)
     # The numerator is the unique KV bytes DRAM must deliver: a shared prefix is counted once.
     # Without prefix sharing this equals the logical bytes the attention consumes.
@@ -513,8 +543,6 @@ def run_ours(args):
         # verify: the dominant kernel is the attention launch itself (the gamma-token append is its own kernel)
         achieved = work / ((dec_avg if cfg.gamma > 1 else fused_ms) * 1e-3) / div
     value = total_work / (ms * 1e-3) / div
-    if rank != 0:
-        return 0
     line = {
         "metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": K,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
@@ -563,10 +591,8 @@ def run_ours(args):
         "e2e": e2e,
         "cpu_baseline": None,
     }
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg.name, args.cpu_seconds)
-    print(json.dumps(line), flush=True)
-    return 0
+    del step, w
+    return line
 
 
 # ---------------------------------------------------------------------------- the oracle on host cores
@@ -613,19 +639,139 @@ def oracle_step_seconds(inp):
     return time.perf_counter() - t0
 
 
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def available_memory_bytes() -> int:
+    """Memory the oracle processes may use: MemAvailable, capped by a cgroup limit if one is set."""
+    avail = 8 << 30
+    try:
+        with open("/proc/meminfo") as f:
+            for ln in f:
+                if ln.startswith("MemAvailable:"):
+                    avail = int(ln.split()[1]) * 1024
+    except OSError:
+        pass
+    for path in ("/sys/fs/cgroup/memory.max", "/sys/fs/cgroup/memory/memory.limit_in_bytes"):
+        try:
+            with open(path) as f:
+                v = f.read().strip()
+            if v.isdigit():
+                avail = min(avail, int(v))
+        except OSError:
+            pass
+    return avail
+
+
+def oracle_sample_bytes(cfg) -> int:
+    """Rough peak memory of one oracle step on a batch-1 sample: the stored caches twice (input and
+    the step's copy) and the float64 logical K and V."""
+    s = oracle_sample_config(cfg, 1)
+    longest = s.seq_len if s.seq_len is not None else s.len_range[1]
+    per_tok = s.n_kv_heads * s.head_dim
+    cache = (s.num_blocks * s.block_size if s.layout == "paged" else s.max_len) * per_tok * 4
+    return 2 * cache + 2 * longest * per_tok * 8 + (256 << 20)
+
+
+def _oracle_proc(workload, index, conn):
+    """One host core's share: a batch-1 sample of the workload (seed + index), then commands:
+    ("step",) runs one oracle step; ("run", seconds) repeats steps for that long; None stops."""
+    cfg = CONFIGS[workload]
+    inp = make_inputs(oracle_sample_config(cfg, 1), seed=cfg.seed + index)
+    work = sample_work(inp)[0]
+    conn.send(("ready", int(inp.lengths[0])))
+    while True:
+        cmd = conn.recv()
+        if cmd is None:
+            break
+        if cmd[0] == "step":
+            conn.send((work, oracle_step_seconds(inp)))
+        else:
+            elapsed, done = 0.0, 0
+            while elapsed < cmd[1] or done == 0:
+                elapsed += oracle_step_seconds(inp)
+                done += 1
+            conn.send((done * work, elapsed))
+    conn.close()
+
+
+class OracleCores:
+    """The float64 oracle on every host core: one process per core (spawned, so safe to start after
+    CUDA), each with its own batch-1 sample of the workload, driven in lock step."""
+
+    def __init__(self, workload: str, cores: int):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.conns, self.procs = [], []
+        for i in range(cores):
+            parent, child = ctx.Pipe()
+            p = ctx.Process(target=_oracle_proc, args=(workload, i, child), daemon=True)
+            p.start()
+            self.conns.append(parent)
+            self.procs.append(p)
+        self.lengths = [c.recv()[1] for c in self.conns]
+
+    def step(self):
+        """One oracle step on every core's sample: (work summed over cores, wall seconds)."""
+        t0 = time.perf_counter()
+        for c in self.conns:
+            c.send(("step",))
+        work = sum(c.recv()[0] for c in self.conns)
+        return work, time.perf_counter() - t0
+
+    def run(self, seconds: float):
+        """Every core repeats steps for ``seconds``: (work summed over cores, longest elapsed)."""
+        for c in self.conns:
+            c.send(("run", seconds))
+        res = [c.recv() for c in self.conns]
+        return sum(r[0] for r in res), max(r[1] for r in res)
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send(None)
+            except OSError:
+                pass
+        for p in self.procs:
+            p.join(timeout=10)
+
+
+def oracle_core_count(cfg) -> int:
+    """Every host core, fewer if the batch-1 samples would not fit in half the available memory."""
+    return max(1, min(host_cores(), available_memory_bytes() // 2 // oracle_sample_bytes(cfg)))
+
+
 def cpu_worker(workload: str, seconds: float):
     cfg = CONFIGS[workload]
+    # all host cores: one process per core, each its own batch-1 sample (seeds seed .. seed + n - 1)
+    n = oracle_core_count(cfg)
+    pool = OracleCores(workload, n)
+    try:
+        work_all, wall = pool.run(seconds)
+        lengths = pool.lengths
+    finally:
+        pool.close()
+    _, div, unit, _ = sample_work(make_inputs(oracle_sample_config(cfg, 1), seed=cfg.seed))
+    # one host core: the first sequences of the workload
     sample_batch = 1 if cfg.batch == 1 or cfg.layout == "contiguous" else 2
     inp = make_inputs(oracle_sample_config(cfg, sample_batch), seed=cfg.seed)
-    work, div, unit, _ = sample_work(inp)
+    work = sample_work(inp)[0]
     elapsed, done = 0.0, 0
     while elapsed < seconds or done == 0:
         elapsed += oracle_step_seconds(inp)
         done += 1
-    return {"value": round(done * work / elapsed / div, 6), "unit": unit, "cores": 1, "kind": "oracle",
-            "sample": (f"float64 numpy oracle (RoPE + append + attention) on the first {sample_batch} "
-                       f"sequence(s) of {workload} (lengths {inp.lengths.tolist()}), repeated {done}x "
-                       f"in {elapsed:.1f} s; BLAS limited to 1 thread")}
+    return {"value": round(work_all / wall / div, 6), "unit": unit, "cores": n, "kind": "oracle",
+            "sample": (f"float64 numpy oracle (RoPE + append + attention), one process per host core ({n} of "
+                       f"{host_cores()}), each on its own batch-1 sample of {workload} (seeds {cfg.seed}.."
+                       f"{cfg.seed + n - 1}, lengths {lengths}) repeated for {seconds:.0f} s; BLAS limited to 1 "
+                       "thread per process"),
+            "one_core": {"value": round(done * work / elapsed / div, 6), "unit": unit, "cores": 1,
+                         "sample": (f"the first {sample_batch} sequence(s) of {workload} (lengths "
+                                    f"{inp.lengths.tolist()}), repeated {done}x in {elapsed:.1f} s on one core")}}
 
 
 def cpu_baseline(workload: str, seconds: float):
@@ -638,33 +784,40 @@ def cpu_baseline(workload: str, seconds: float):
            "--cpu-seconds", str(seconds)]
     try:
         r = subprocess.run(cmd, env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True,
-                           timeout=max(120.0, 6 * seconds))
+                           timeout=max(180.0, 10 * seconds))
         return json.loads(r.stdout.strip().splitlines()[-1])
     except Exception as e:  # the baseline is reported, never required
-        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {e}"}
+        return {"value": None, "unit": UNIT, "cores": 0, "kind": "oracle", "sample": f"failed: {e}"}
 
 
 def run_reference(args):
+    """The reference arm: the float64 oracle on every host core (one process per core, each its own
+    batch-1 sample of the workload); one step = one oracle step on every core's sample."""
     rank, _, world = dist_env()
     if rank != 0:
         return 0
-    cfg = CONFIGS[args.workload]
-    sample_batch = 1 if cfg.batch == 1 or cfg.layout == "contiguous" else 2
-    inp = make_inputs(oracle_sample_config(cfg, sample_batch), seed=cfg.seed)
-    work, div, unit, metric = sample_work(inp)
-    for _ in range(args.warmup):
-        oracle_step_seconds(inp)
-    secs = [oracle_step_seconds(inp) for _ in range(args.steps)]
-    ms = 1e3 * sum(secs) / len(secs)
+    cfg = CONFIGS[args.workload or DEFAULT_WORKLOAD]
+    n = oracle_core_count(cfg)
+    pool = OracleCores(cfg.name, n)
+    try:
+        for _ in range(args.warmup):
+            pool.step()
+        steps = [pool.step() for _ in range(args.steps)]
+    finally:
+        pool.close()
+    work = sum(w for w, _ in steps) / len(steps)
+    ms = 1e3 * sum(t for _, t in steps) / len(steps)
+    _, div, unit, metric = sample_work(make_inputs(oracle_sample_config(cfg, 1), seed=cfg.seed))
     value = work / (ms * 1e-3) / div
-    sample = (f"float64 numpy oracle on the first {sample_batch} sequence(s) of {cfg.name} per step "
-              f"(lengths {inp.lengths.tolist()}); BLAS limited to 1 thread")
+    sample = (f"float64 numpy oracle, one process per host core ({n} of {host_cores()}), each on its own batch-1 "
+              f"sample of {cfg.name} (seeds {cfg.seed}..{cfg.seed + n - 1}, lengths {pool.lengths}); one step = one "
+              "oracle step on every sample; BLAS limited to 1 thread per process")
     print(json.dumps({
         "impl": "reference", "metric": metric, "value": round(value, 6), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.name, "description": cfg.description, "sample_batch": sample_batch},
-        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
+        "config": {"workload": cfg.name, "description": cfg.description, "sample": f"{n} batch-1 samples"},
+        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": n, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
     return 0
@@ -673,7 +826,7 @@ def run_reference(args):
 def main(argv=None):
     args = parse_args(argv)
     if args.cpu_worker:
-        print(json.dumps(cpu_worker(args.workload, args.cpu_seconds)), flush=True)
+        print(json.dumps(cpu_worker(args.workload or DEFAULT_WORKLOAD, args.cpu_seconds)), flush=True)
         return 0
     if args.impl == "reference":
         return run_reference(args)

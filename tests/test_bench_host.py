@@ -28,39 +28,39 @@ def test_clock_samples_median_max_and_reasons():
     assert bench.summarize_clock_samples([]) is None
 
 
-def _profile(tmp_path, workload, sha, traffic):
+def _traffic(tmp_path, records):
     d = tmp_path / "profiles"
     d.mkdir(exist_ok=True)
-    (d / f"{workload}.md").write_text(f"# summary\n\nworkload: {workload}\n\ntraffic_bytes_per_launch: {traffic}\n"
-                                      f"kernel_source_sha256: {sha}\n")
+    (d / "traffic.json").write_text(json.dumps(records))
 
 
 def test_recorded_traffic_only_while_kernel_sources_hash_the_same(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "kernel_source_hash", lambda cfg: "abc123")
-    _profile(tmp_path, "batched_paged", "abc123", 1167529216)
-    _profile(tmp_path, "long_context", "stale0", 538345728)
+    _traffic(tmp_path, {"batched_paged": {"traffic_bytes_per_launch": 1167529216, "kernel_source_sha256": "abc123"},
+                        "long_context": {"traffic_bytes_per_launch": 538345728, "kernel_source_sha256": "stale0"}})
     assert bench.recorded_traffic("batched_paged") == 1167529216
     assert bench.recorded_traffic("long_context") is None      # the kernels changed since the capture
     assert bench.recorded_traffic("prefill_128k") is None      # no capture at all
     assert bench.recorded_traffic("no_such_workload") is None
 
 
-def test_committed_profiles_name_known_workloads():
-    """Every committed ncu summary with a launch list names a workload of the bench, once, and
-    carries the traffic and source-hash lines the bench reads."""
-    names = []
-    for fn in sorted(os.listdir(os.path.join(ROOT, "profiles"))):
-        text = open(os.path.join(ROOT, "profiles", fn), encoding="utf-8").read()
-        lines = {ln.split(":", 1)[0]: ln.split(":", 1)[1].strip() for ln in text.splitlines()
-                 if ln.startswith(("workload:", "traffic_bytes_per_launch:", "kernel_source_sha256:"))}
-        if not lines:          # a single-kernel summary without a launch list
-            continue
-        assert lines.get("workload") in bench.CONFIGS, fn
-        assert int(lines["traffic_bytes_per_launch"]) > 0, fn
-        assert len(lines["kernel_source_sha256"]) == 16, fn
-        names.append(lines["workload"])
-    assert len(names) == len(set(names)) >= 9
+def test_recorded_traffic_without_a_data_file(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.recorded_traffic("batched_paged") is None
+
+
+def test_committed_traffic_records_name_known_workloads_and_summaries():
+    """Every record of the committed traffic file names a bench workload, a positive byte count,
+    a 16-hex-digit source hash and an ncu summary under profiles/ that exists."""
+    with open(os.path.join(ROOT, "profiles", "traffic.json"), encoding="utf-8") as f:
+        recs = json.load(f)
+    assert len(recs) >= 9
+    for name, rec in recs.items():
+        assert name in bench.CONFIGS, name
+        assert isinstance(rec["traffic_bytes_per_launch"], int) and rec["traffic_bytes_per_launch"] > 0, name
+        assert len(rec["kernel_source_sha256"]) == 16, name
+        assert rec["summary"].startswith("profiles/") and os.path.exists(os.path.join(ROOT, rec["summary"])), name
 
 
 def test_reference_arm_prints_one_json_line():
@@ -75,3 +75,25 @@ def test_reference_arm_prints_one_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_default_run_adds_the_long_context_record():
+    """With no --workload the bench measures batched_paged and adds a long_context record (its own
+    timing, roofline, clocks and e2e); the keys that describe the whole line are not repeated."""
+    args = bench.parse_args([])
+    assert args.workload is None and not args.no_extra
+    assert bench.workload_config(args).name == bench.DEFAULT_WORKLOAD == "batched_paged"
+    assert bench.EXTRA_WORKLOAD == "long_context" and bench.CONFIGS["long_context"].num_splits == 128
+    for k in ("value", "ms_per_step", "roofline", "clocks", "e2e", "config", "gpu_launches"):
+        assert k not in bench.SHARED_KEYS
+    assert bench.parse_args(["--workload", "batched_paged"]).workload == "batched_paged"
+
+
+def test_cpu_worker_reports_all_cores_and_one_core():
+    r = subprocess.run([sys.executable, "bench.py", "--cpu-worker", "--cpu-seconds", "0.5"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    assert d["kind"] == "oracle" and d["value"] > 0 and d["unit"] == "GB/s"
+    assert 1 <= d["cores"] <= bench.host_cores()
+    assert d["one_core"]["cores"] == 1 and d["one_core"]["value"] > 0
