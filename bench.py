@@ -365,7 +365,8 @@ def measure(args, cfg, device, rank, world, splits_override=None):
     mma_path = cfg.int8 or (cfg.dtype == "bf16" and (
         (cfg.layout == "paged" and cfg.block_size >= 8) or
         (cfg.layout == "contiguous" and cfg.max_len >= 16384 // (2 * cfg.head_dim))))
-    launches_per_step = 1 if mma_path and cfg.gamma == 1 else 2
+    # one kernel: the fused decode step (tensor-core path) and the verify step up to 8 new tokens
+    launches_per_step = 1 if (mma_path and cfg.gamma == 1) or 1 < cfg.gamma <= 8 else 2
     attend_arg = w["positions"] if cfg.gamma > 1 else w["seq_lens"]   # verify: lengths follow the positions
     flush = None
     if 2 * kv_bytes < 3 * L2_BYTES:                     # inputs not much larger than L2: flush between steps
@@ -540,8 +541,8 @@ def measure(args, cfg, device, rank, world, splits_override=None):
     else:
         peak, peak_src = hbm_peak()
         peak_src = f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
-        # verify: the dominant kernel is the attention launch itself (the gamma-token append is its own kernel)
-        achieved = work / ((dec_avg if cfg.gamma > 1 else fused_ms) * 1e-3) / div
+        # the fused step's kernel (decode, or verify up to 8 new tokens); above that the verify attention launch
+        achieved = work / ((dec_avg if cfg.gamma > 8 else fused_ms) * 1e-3) / div
     value = total_work / (ms * 1e-3) / div
     line = {
         "metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": K,
@@ -574,8 +575,10 @@ def measure(args, cfg, device, rank, world, splits_override=None):
         "roofline": {"kernel": (("prefill_tc_kernel (tcgen05: causal attention of the prompt, 128 tokens x 2 query heads per "
                                  "CTA, S and O in Tensor Memory)" if cfg.head_dim == 128 else
                                  "prefill_kernel (mma.sync: causal attention of the prompt, 64 query rows per CTA)") if prefill else
-                                "decode_verify_kernel (causal split-K attention of "
-                                f"{cfg.gamma} new tokens per sequence + merge; the append is a separate launch)"
+                                ("decode_verify_kernel, fused step (RoPE + append of "
+                                 f"{cfg.gamma} new tokens per sequence + causal split-K attention + merge)"
+                                 if cfg.gamma <= 8 else "decode_verify_kernel (causal split-K attention of "
+                                 f"{cfg.gamma} new tokens per sequence + merge; the append is a separate launch)")
                                 if cfg.gamma > 1 else
                                 "decode_q8_kernel, fused step (RoPE + quantised append + split-K attention over "
                                 f"INT{cfg.code_bits} codes and the bf16 window + merge)" if cfg.int8 else

@@ -287,8 +287,14 @@ RRA_API int rra_verify_attn(const void* q_rot, const void* k_cache, const void* 
                             int max_len, void* out, int B, int gamma, int Hq, int Hkv, int D, float scale,
                             int num_splits, void* workspace, size_t ws_bytes, int32_t* err_flag, void* stream);
 
-/* The whole verify step: rra_rope_append_verify then rra_verify_attn on q_out (two kernels; the
- * second starts its launch while the first finishes). bf16. q_out must not overlap q. */
+/* The whole verify step: RoPE of the gamma new tokens' q and k at positions p_b .. p_b + gamma - 1,
+ * their append, and the attention of rra_verify_attn, with q_rot also written to q_out. Up to
+ * gamma 8 this is ONE kernel: each CTA rotates its query rows in registers (sines and cosines
+ * of the gamma positions in float64, once per CTA), and the CTAs whose chunk holds new tokens
+ * write them into the cache before their own TMA reads the tile that holds them. Above gamma 8
+ * it runs rra_rope_append_verify then rra_verify_attn on q_out (two kernels). Same results
+ * either way. bf16. q_out must not overlap q. ("Transformer架构优化实战2026：注意力机制、KV
+ * Cache与推理加速完整指南" §五; RoPE as in rra_rope_append.) */
 RRA_API int rra_verify_step(const void* q, const void* k_new, const void* v_new, const int32_t* positions,
                             void* q_out, void* k_cache, void* v_cache, const int32_t* block_table,
                             int max_blocks_per_seq, int block_size, int num_blocks, int max_len, void* out, int B,

@@ -388,6 +388,15 @@ void fill_theta_pi(double* t, int D, double base) {
   for (int i = 0; i < D / 2; ++i) t[i] = std::pow(base, -2.0 * i / D) / kPi;
 }
 
+// cos theta_i and sin theta_i in float64.
+void fill_cos_sin_theta(double* c, double* s, int D, double base) {
+  for (int i = 0; i < D / 2; ++i) {
+    const double th = std::pow(base, -2.0 * i / D);
+    c[i] = std::cos(th);
+    s[i] = std::sin(th);
+  }
+}
+
 bool overlap(const void* a, const void* b, size_t bytes) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + bytes && y < x + bytes;
@@ -606,6 +615,80 @@ static int decode_step_qk(int bits, const void* q, const void* k_new, const void
                                              static_cast<cudaStream_t>(stream)));
 }
 
+
+namespace {
+
+// The fused verify step's extra inputs (rra_verify_step with gamma <= 8).
+struct VerifyFusedArgs {
+  const void* k_new;
+  const void* v_new;
+  void* q_out;
+  int rope_style;
+  double rope_base;
+};
+
+// rra_verify_attn, or with `fused` the whole verify step in one launch.
+int verify_launch(const void* q_rot, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                  int max_blocks_per_seq, const int32_t* positions, int block_size, int num_blocks, int max_len,
+                  void* out, int B, int gamma, int Hq, int Hkv, int D, float scale, int num_splits, void* workspace,
+                  size_t ws_bytes, int32_t* err_flag, void* stream, const VerifyFusedArgs* fused) {
+  int64_t capacity;
+  if (block_table != nullptr) {
+    if (!pow2(block_size)) return block_size <= 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
+    if (max_blocks_per_seq < 1 || num_blocks < 1) return RRA_EINVAL;
+    capacity = int64_t(max_blocks_per_seq) * block_size;
+  } else {
+    if (max_len < 1) return RRA_EINVAL;
+    capacity = max_len;
+  }
+  Plan p;
+  int st = make_plan_verify(B, gamma, Hq, Hkv, D, capacity, block_table ? block_size : 0, num_splits, &p);
+  if (st != RRA_OK) return st;
+  if (!std::isfinite(scale)) return RRA_EINVAL;
+  if (B == 0) return RRA_OK;
+  if (!q_rot || !k_cache || !v_cache || !positions || !out) return RRA_EINVAL;
+  if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return RRA_EINVAL;
+  const int64_t rows = verify_rows(B, gamma, Hq, Hkv);
+  if (rows > INT32_MAX) return RRA_ERANGE;
+  st = check_workspace(p, 1, static_cast<int>(rows), D, workspace, ws_bytes);
+  if (st != RRA_OK) return st;
+  CUtensorMap km{}, vm{};
+  if (block_table != nullptr) {
+    const int box_rows = block_size < p.tile ? block_size : p.tile;
+    st = encode_pool_map(&km, k_cache, num_blocks, block_size, Hkv, D, box_rows, RRA_BF16, true);
+    if (st == RRA_OK) st = encode_pool_map(&vm, v_cache, num_blocks, block_size, Hkv, D, box_rows, RRA_BF16, true);
+  } else {
+    st = encode_contig_map(&km, k_cache, B, Hkv, max_len, D, p.tile, RRA_BF16);
+    if (st == RRA_OK) st = encode_contig_map(&vm, v_cache, B, Hkv, max_len, D, p.tile, RRA_BF16);
+  }
+  if (st != RRA_OK) return st;
+  // the workspace holds `rows` partial rows: laid out as for one sequence of `rows` heads
+  rra::DecodeArgs a = decode_args(p, q_rot, k_cache, v_cache, nullptr, out, 1, static_cast<int>(rows), 1, D, scale,
+                                  workspace, err_flag);
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.gamma = gamma;
+  a.positions = positions;
+  a.block_table = block_table;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.log2_bs = block_table ? ilog2(block_size) : 0;
+  a.num_blocks = num_blocks;
+  a.max_len = block_table ? 0 : max_len;
+  a.capacity = static_cast<int>(capacity);
+  if (fused != nullptr) {  // q_rot is the unrotated q: the kernel rotates it and appends the new tokens
+    a.k_new = fused->k_new;
+    a.v_new = fused->v_new;
+    a.q_out = fused->q_out;
+    a.rope_style = fused->rope_style;
+    fill_theta_pi(a.theta_pi, D, fused->rope_base);
+    fill_cos_sin_theta(a.cos_theta, a.sin_theta, D, fused->rope_base);
+  }
+  return finish_decode(
+      rra::launch_decode_verify(a, km, vm, block_table != nullptr, fused != nullptr, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -942,51 +1025,9 @@ int rra_verify_attn(const void* q_rot, const void* k_cache, const void* v_cache,
                     int max_blocks_per_seq, const int32_t* positions, int block_size, int num_blocks, int max_len,
                     void* out, int B, int gamma, int Hq, int Hkv, int D, float scale, int num_splits, void* workspace,
                     size_t ws_bytes, int32_t* err_flag, void* stream) {
-  int64_t capacity;
-  if (block_table != nullptr) {
-    if (!pow2(block_size)) return block_size <= 0 ? RRA_EINVAL : RRA_EUNSUPPORTED;
-    if (max_blocks_per_seq < 1 || num_blocks < 1) return RRA_EINVAL;
-    capacity = int64_t(max_blocks_per_seq) * block_size;
-  } else {
-    if (max_len < 1) return RRA_EINVAL;
-    capacity = max_len;
-  }
-  Plan p;
-  int st = make_plan_verify(B, gamma, Hq, Hkv, D, capacity, block_table ? block_size : 0, num_splits, &p);
-  if (st != RRA_OK) return st;
-  if (!std::isfinite(scale)) return RRA_EINVAL;
-  if (B == 0) return RRA_OK;
-  if (!q_rot || !k_cache || !v_cache || !positions || !out) return RRA_EINVAL;
-  if (!aligned16(q_rot) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return RRA_EINVAL;
-  const int64_t rows = verify_rows(B, gamma, Hq, Hkv);
-  if (rows > INT32_MAX) return RRA_ERANGE;
-  st = check_workspace(p, 1, static_cast<int>(rows), D, workspace, ws_bytes);
-  if (st != RRA_OK) return st;
-  CUtensorMap km{}, vm{};
-  if (block_table != nullptr) {
-    const int box_rows = block_size < p.tile ? block_size : p.tile;
-    st = encode_pool_map(&km, k_cache, num_blocks, block_size, Hkv, D, box_rows, RRA_BF16, true);
-    if (st == RRA_OK) st = encode_pool_map(&vm, v_cache, num_blocks, block_size, Hkv, D, box_rows, RRA_BF16, true);
-  } else {
-    st = encode_contig_map(&km, k_cache, B, Hkv, max_len, D, p.tile, RRA_BF16);
-    if (st == RRA_OK) st = encode_contig_map(&vm, v_cache, B, Hkv, max_len, D, p.tile, RRA_BF16);
-  }
-  if (st != RRA_OK) return st;
-  // the workspace holds `rows` partial rows: laid out as for one sequence of `rows` heads
-  rra::DecodeArgs a = decode_args(p, q_rot, k_cache, v_cache, nullptr, out, 1, static_cast<int>(rows), 1, D, scale,
-                                  workspace, err_flag);
-  a.B = B;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.gamma = gamma;
-  a.positions = positions;
-  a.block_table = block_table;
-  a.max_blocks_per_seq = max_blocks_per_seq;
-  a.log2_bs = block_table ? ilog2(block_size) : 0;
-  a.num_blocks = num_blocks;
-  a.max_len = block_table ? 0 : max_len;
-  a.capacity = static_cast<int>(capacity);
-  return finish_decode(rra::launch_decode_verify(a, km, vm, block_table != nullptr, static_cast<cudaStream_t>(stream)));
+  return verify_launch(q_rot, k_cache, v_cache, block_table, max_blocks_per_seq, positions, block_size, num_blocks,
+                       max_len, out, B, gamma, Hq, Hkv, D, scale, num_splits, workspace, ws_bytes, err_flag, stream,
+                       nullptr);
 }
 
 int rra_verify_step(const void* q, const void* k_new, const void* v_new, const int32_t* positions, void* q_out,
@@ -1006,6 +1047,12 @@ int rra_verify_step(const void* q, const void* k_new, const void* v_new, const i
   const int64_t rows = verify_rows(B, gamma, Hq, Hkv);
   st = check_workspace(p, 1, static_cast<int>(rows), D, workspace, ws_bytes);
   if (st != RRA_OK) return st;
+  if (gamma <= rra::kVerifyFusedMaxGammaHost) {  // one launch: RoPE, append and attention
+    const VerifyFusedArgs f{k_new, v_new, q_out, rope_style, rope_base};
+    return verify_launch(q, k_cache, v_cache, block_table, max_blocks_per_seq, positions, block_size, num_blocks,
+                         max_len, out, B, gamma, Hq, Hkv, D, scale, num_splits, workspace, ws_bytes, err_flag, stream,
+                         &f);
+  }
   st = rra_rope_append_verify(q, k_new, v_new, positions, q_out, k_cache, v_cache, block_table, max_blocks_per_seq,
                               block_size, num_blocks, max_len, B, gamma, Hq, Hkv, D, rope_base, rope_style, RRA_BF16,
                               err_flag, stream);

@@ -88,6 +88,10 @@ struct DecodeArgs {
   // and values fit in L2 together, longest query blocks first within a band.
   int kv_band;
   double theta_pi[kMaxDecodeHeadDim / 2];  // theta_i / pi, theta_i = base^(-2i/D)
+  // cos theta_i and sin theta_i (float64, host): the verify step reaches the angles of positions
+  // p + 1, p + 2, ... from that of p by complex multiplication
+  double cos_theta[kMaxDecodeHeadDim / 2];
+  double sin_theta[kMaxDecodeHeadDim / 2];
 };
 
 // Tokens per pipeline stage for a head_dim and element size: K + V tiles of 16 KB.
@@ -144,8 +148,12 @@ cudaError_t launch_decode_step_paged(const DecodeArgs& a, const CUtensorMap& k_m
 #define RRA_Q8_STAGE_BYTES 16384
 #endif
 // Speculative verify: attention of gamma new tokens per sequence (a.gamma, a.positions set).
+// fused: the whole step (a.q unrotated; a.k_new, a.v_new, a.q_out, a.rope_style, a.theta_pi set;
+// gamma <= 8).
 cudaError_t launch_decode_verify(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map, bool paged,
-                                 cudaStream_t stream);
+                                 bool fused, cudaStream_t stream);
+// Largest gamma of the one-launch verify step.
+constexpr int kVerifyFusedMaxGammaHost = 8;
 // Prefill: causal attention of the T = a.gamma prompt tokens of each sequence (a.positions: the
 // first one's position); 64 query rows (a.hpc heads x 64 / a.hpc tokens) per CTA.
 cudaError_t launch_prefill(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map, bool paged,

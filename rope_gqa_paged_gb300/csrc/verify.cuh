@@ -22,6 +22,65 @@
 namespace rra {
 
 constexpr int kVerifyRows = 16;
+// The fused verify step (RoPE of the gamma new tokens' q and k, their append and the attention in
+// one launch) keeps the sines and cosines of up to this many positions in shared memory; larger
+// gamma runs as two launches.
+constexpr int kVerifyFusedMaxGamma = 8;
+
+template <int D>
+constexpr int verify_smem_bytes(bool fused) {
+  return MmaCfg<D>::kSmemBytes + (fused ? (kVerifyFusedMaxGamma - 1) * 4 * (D / 2) * 4 : 0);
+}
+
+// Fused step only: rotates the two query rows of the lane's A fragment (rows lane/4 and lane/4 + 8,
+// row r = head hh * gamma + token j at position p0 + j) in place, with cos/sin hi/lo of token j at
+// cs + j * 2D. Padding rows (r >= rows) stay zero.
+template <int D>
+__device__ __forceinline__ void rotate_q_rows(uint32_t (&qa)[D / 16][4], const float* cs, int rows, int gamma, int lane,
+                                              int style) {
+  constexpr int KK = D / 16, HALF = D / 2;
+  const int c2 = 2 * (lane & 3);
+  auto unpack = [](uint32_t w, float& lo, float& hi) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+  };
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = (lane >> 2) + 8 * i;
+    if (r >= rows) continue;
+    const float* c = cs + (r % gamma) * 2 * D;
+    if (style == 1) {  // interleaved pairs (2f, 2f + 1): the two halves of each 32-bit word
+#pragma unroll
+      for (int kk = 0; kk < KK; ++kk)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t& w = qa[kk][hf ? 2 + i : i];
+          const int f = (16 * kk + 8 * hf + c2) >> 1;
+          float x0, x1;
+          unpack(w, x0, x1);
+          const float ch = c[f], cl = c[HALF + f], sh = c[2 * HALF + f], sl = c[3 * HALF + f];
+          w = pack_bf16x2(rotate_diff(x0, x1, ch, cl, sh, sl), rotate_diff(x1, -x0, ch, cl, sh, sl));
+        }
+      continue;
+    }
+    // half-split pairs (f, f + D/2): k-steps kk and kk + KK/2 hold the two members
+#pragma unroll
+    for (int kk = 0; kk < KK / 2; ++kk)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t& wa = qa[kk][hf ? 2 + i : i];
+        uint32_t& wb = qa[kk + KK / 2][hf ? 2 + i : i];
+        float a0, a1, b0, b1;
+        unpack(wa, a0, a1);
+        unpack(wb, b0, b1);
+        const int f0 = 16 * kk + 8 * hf + c2, f1 = f0 + 1;
+        const float ch0 = c[f0], cl0 = c[HALF + f0], sh0 = c[2 * HALF + f0], sl0 = c[3 * HALF + f0];
+        const float ch1 = c[f1], cl1 = c[HALF + f1], sh1 = c[2 * HALF + f1], sl1 = c[3 * HALF + f1];
+        wa = pack_bf16x2(rotate_diff(a0, b0, ch0, cl0, sh0, sl0), rotate_diff(a1, b1, ch1, cl1, sh1, sl1));
+        wb = pack_bf16x2(rotate_diff(b0, -a0, ch0, cl0, sh0, sl0), rotate_diff(b1, -a1, ch1, cl1, sh1, sl1));
+      }
+  }
+}
 
 template <int D>
 struct VerifyState {
@@ -156,7 +215,14 @@ struct VerifyRows {
   }
 };
 
-template <int D, bool PAGED>
+// FUSED: the whole verify step in this launch. a.q holds the unrotated q of the gamma new tokens
+// (gamma <= kVerifyFusedMaxGamma); the consumer warps take sin/cos of the gamma positions once per
+// CTA (float64 sincospi, as the decode step), rotate their query rows in registers, and split-0
+// CTAs publish q_rot. A CTA whose chunk holds new tokens rotates their k_new and writes them and
+// v_new into the cache, one warp per token, and its producer waits for those writes (an mbarrier
+// with one arrival per token) before the TMA of the first tile that holds a new token. Head-slice
+// CTAs of that chunk write identical bytes.
+template <int D, bool PAGED, bool FUSED = false>
 __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     decode_verify_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                          const DecodeArgs a) {
@@ -178,7 +244,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   const VerifyRows out_row{a.Hq, a.Hkv, n_rep, slices, hpc, gamma};
 
   pdl_launch_dependents();
-  pdl_wait();  // the append kernel before this one wrote the new tokens and q_rot
+  pdl_wait();  // the kernel before this one (the append, or the previous step) has finished
 
   const int p0 = a.positions[b];
   int L = p0 + gamma;
@@ -191,9 +257,14 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   if (start >= L) return;
   const int end = min(L, start + a.chunk);
   const int n_tiles = (end - start + C::kTile - 1) / C::kTile;
+  // fused step: new tokens app_lo .. app_hi - 1 lie in this chunk and are appended here
+  const int app_lo = FUSED ? max(p0, start) : 0, app_hi = FUSED ? min(L, end) : 0;
+  const bool appender = FUSED && app_lo < app_hi;
+  const int first_new_tile = appender ? (app_lo - start) / C::kTile : n_tiles;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* empty = full + C::kStages;
+  uint64_t* appended = empty + C::kStages;
   int32_t* tbl = reinterpret_cast<int32_t*>(smem + C::kOffTable);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -203,6 +274,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], C::kConsumerWarps);
     }
+    mbar_init(appended, appender ? app_hi - app_lo : 1);
     fence_barrier_init();
   }
   int first_blk = 0;
@@ -230,6 +302,10 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
       for (int it = 0; it < n_tiles; ++it) {
         const int s = it % C::kStages;
         if (it >= C::kStages && !mbar_wait(&empty[s], ((it / C::kStages) - 1) & 1)) {
+          flag_error(a.err, RRA_ERR_TIMEOUT);
+          break;
+        }
+        if (it == first_new_tile && !mbar_wait(appended, 0)) {  // the new tokens start in this tile
           flag_error(a.err, RRA_ERR_TIMEOUT);
           break;
         }
@@ -295,6 +371,65 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     for (int kk = 0; kk < D / 16; ++kk) {
       qa[kk][i] = r < rows ? q[kk * 8 + t] : 0u;
       qa[kk][2 + i] = r < rows ? q[kk * 8 + 4 + t] : 0u;
+    }
+  }
+  if constexpr (FUSED) {
+    // RoPE ("Transformer推理核心：KV Cache、GQA与RoPE原理与工程实践" §3) at positions p0 .. p0 + gamma - 1:
+    // sin / cos of p0 * theta_i in float64 (sincospi: exact argument reduction), then of
+    // (p0 + j) * theta_i by j float64 complex multiplications by e^(i theta_i) (relative error
+    // ~j * 2^-53, far below what the float32 hi + lo split keeps), split into float32 hi + lo
+    // for the error-free rotation; [gamma][4][D/2] floats. One float64 sincospi per frequency and
+    // CTA: the FP64 pipe is narrow, and every CTA of the sequence needs the same table.
+    float* cs = reinterpret_cast<float*>(smem + C::kOffCs);
+    for (int i = threadIdx.x; i < D / 2; i += kConsumers) {
+      double sn, cn;
+      sincospi(static_cast<double>(p0) * a.theta_pi[i], &sn, &cn);
+      const double c1 = a.cos_theta[i], s1 = a.sin_theta[i];
+      for (int j = 0; j < gamma; ++j) {
+        float* c = cs + j * 2 * D;
+        const float ch = static_cast<float>(cn), sh = static_cast<float>(sn);
+        c[i] = ch;
+        c[D / 2 + i] = static_cast<float>(cn - static_cast<double>(ch));
+        c[D + i] = sh;
+        c[3 * (D / 2) + i] = static_cast<float>(sn - static_cast<double>(sh));
+        const double cn2 = fma(cn, c1, -sn * s1), sn2 = fma(sn, c1, cn * s1);
+        cn = cn2;
+        sn = sn2;
+      }
+    }
+    named_barrier_sync(1, kConsumers);
+    rotate_q_rows<D>(qa, cs, rows, gamma, lane, a.rope_style);
+    if (warp == 0 && split == 0) {  // publish q_rot (rounded to bf16, as used here)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int r = rg + 8 * i;
+        if (r >= rows) continue;
+        const int hh = r / gamma, j = r - hh * gamma;
+        uint32_t* qo = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.q_out) +
+                                                   ((static_cast<size_t>(b) * gamma + j) * a.Hq + h0 + hh) * D);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          qo[kk * 8 + t] = qa[kk][i];
+          qo[kk * 8 + 4 + t] = qa[kk][2 + i];
+        }
+      }
+    }
+    if (appender) {  // one warp per new token of this chunk
+      for (int pos = app_lo + warp; pos < app_hi; pos += C::kConsumerWarps) {
+        const int j = pos - p0;
+        const size_t off = ((static_cast<size_t>(b) * gamma + j) * a.Hkv + g) * D + lane * (D / 32);
+        const uint32_t* kn = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.k_new) + off);
+        const uint32_t* vn = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.v_new) + off);
+        uint32_t kraw[D / 64], vraw[D / 64];
+#pragma unroll
+        for (int w = 0; w < D / 64; ++w) {
+          kraw[w] = kn[w];
+          vraw[w] = vn[w];
+        }
+        int phys = 0;
+        if constexpr (PAGED) phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (pos >> a.log2_bs)];
+        append_token_bf16<D, PAGED>(a, cs + j * 2 * D, kraw, vraw, phys, b, g, pos, lane, appended);
+      }
     }
   }
   // rows attend at least p0 + 1 keys: from 256 on, a bf16 P is exact enough (the split of P into
@@ -399,16 +534,17 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   }
 }
 
-template <int D, bool PAGED>
+template <int D, bool PAGED, bool FUSED>
 cudaError_t launch_decode_verify_t(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
                                    cudaStream_t st) {
   using C = MmaCfg<D>;
+  constexpr int kSmem = verify_smem_bytes<D>(FUSED);
   static int done[64] = {0};
-  auto kern = decode_verify_kernel<D, PAGED>;
-  cudaError_t e = ensure_smem(kern, C::kSmemBytes, done);
+  auto kern = decode_verify_kernel<D, PAGED, FUSED>;
+  cudaError_t e = ensure_smem(kern, kSmem, done);
   if (e != cudaSuccess) return e;
   const dim3 grid(a.num_splits * ((a.Hq / a.Hkv) / a.hpc), a.Hkv, a.B);
-  return launch_pdl(kern, grid, dim3(C::kThreads), C::kSmemBytes, st, km, vm, a);
+  return launch_pdl(kern, grid, dim3(C::kThreads), kSmem, st, km, vm, a);
 }
 
 }  // namespace rra

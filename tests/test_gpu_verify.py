@@ -82,22 +82,26 @@ def _inputs(cfg, lengths, seed=5):
 
 @pytest.mark.parametrize("layout,block_size", [("contiguous", 0), ("paged", 8), ("paged", 16), ("paged", 256)])
 @pytest.mark.parametrize("gamma", [1, 2, 4, 8, 16])
-def test_verify_edge_lengths(layout, block_size, gamma):
+@pytest.mark.parametrize("fused", [True, False], ids=["verify_step", "two_calls"])
+def test_verify_edge_lengths(layout, block_size, gamma, fused):
+    """The verify step is one launch up to gamma 8 (RoPE and append inside the attention kernel),
+    two launches above; the two calls (append, then attention) are checked alike. Lengths put the
+    new tokens at the start of the cache, across tile edges and, with 2 splits, across chunks."""
     lengths = [gamma, gamma + 1, 63 + gamma, 64, 65 + gamma, 300]
     lengths = [max(L, gamma) for L in lengths]
     cfg = _cfg(layout, lengths, gamma, block_size=block_size or 16)
     inp = _inputs(cfg, lengths)
     for splits in (0, 2):
-        _check(inp, H.run_gpu_verify(inp, num_splits=splits), H.run_oracle_verify(inp))
+        _check(inp, H.run_gpu_verify(inp, num_splits=splits, fused=fused), H.run_oracle_verify(inp))
 
 
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (32, 1), (12, 4), (64, 4)], ids=["mha", "mqa", "nrep3", "nrep16"])
 @pytest.mark.parametrize("head_dim", [64, 128])
-def test_verify_heads_and_head_dim(hq, hkv, head_dim):
+@pytest.mark.parametrize("style", [0, 1], ids=["half_split", "interleaved"])
+def test_verify_heads_and_head_dim(hq, hkv, head_dim, style):
     lengths = [9, 200, 611]
     cfg = _cfg("paged", lengths, 4, head_dim=head_dim, hq=hq, hkv=hkv)
     inp = _inputs(cfg, lengths, seed=9)
-    style = 1 if head_dim == 64 else 0
     _check(inp, H.run_gpu_verify(inp, num_splits=3, rope_style=style), H.run_oracle_verify(inp, rope_style=style))
 
 
