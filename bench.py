@@ -232,6 +232,21 @@ def summarize_clock_samples(lines):
 
 
 # ---------------------------------------------------------------------------- our arm
+def capture_repeat(fn, times: int, device):
+    """One CUDA graph of ``fn()`` recorded ``times`` times back to back."""
+    import torch
+    side = torch.cuda.Stream(device=device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream(device).wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(times):
+            fn()
+    return g
+
+
 def workload_config(args):
     cfg = CONFIGS[args.workload or DEFAULT_WORKLOAD]
     if args.batch and args.batch != cfg.batch:
@@ -417,19 +432,26 @@ def measure(args, cfg, device, rank, world, splits_override=None):
     # (2) the step, K times back to back. Inputs larger than L2: all K steps captured in one CUDA
     # graph (a decode loop's shape: each decode kernel overlaps its launch and first loads with
     # the end of the kernel before it), timed by events around that one replay. Inputs that fit
-    # in L2: a one-step graph replayed K times, L2 flushed between steps outside the events.
+    # in L2: one graph of K x (2xL2 flush, step) and one of the K flushes alone, each replayed once
+    # between events; the step time is the difference over K (events around every replay of a
+    # one-step graph add about 6 us that a trivial kernel measures too: reported beside it).
     graph_note = "eager launches"
-    multi = None
+    multi = fgraph = None
     if not args.no_graph:
         try:
             single = step.capture(w["q"], w["k_new"], w["v_new"], w["positions"])
             if flush is None:
                 multi = step.capture(w["q"], w["k_new"], w["v_new"], w["positions"], repeat=K)
+            else:
+                multi = step.capture(w["q"], w["k_new"], w["v_new"], w["positions"], repeat=K,
+                                     before=lambda: flush.fill_(1))
+                fgraph = capture_repeat(lambda: flush.fill_(1), K, device)
             step.graph = single
-            graph_note = (f"one CUDA graph of {K} fused steps, replayed once" if multi is not None
-                          else "CUDA graph of the fused step, replayed per step (L2 flushed between steps)")
+            graph_note = (f"one CUDA graph of {K} fused steps, replayed once" if flush is None else
+                          f"one CUDA graph of {K} x (2xL2 flush + fused step) minus one of the {K} flushes, "
+                          "each replayed once")
         except Exception as e:  # capture is an optimisation; report how the step was timed
-            step.graph, multi = None, None
+            step.graph, multi, fgraph = None, None, None
             graph_note = f"eager launches (graph capture failed: {type(e).__name__})"
 
     def one_step():
@@ -457,6 +479,7 @@ def measure(args, cfg, device, rank, world, splits_override=None):
     while time.perf_counter() - t_warm < 0.6:     # load the GPU so the clock samples see it busy
         (multi.replay() if multi is not None else one_step())
         torch.cuda.synchronize(device)
+    flush_ms = None
     if multi is not None:
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
@@ -465,8 +488,15 @@ def measure(args, cfg, device, rank, world, splits_override=None):
         multi.replay()
         ev1.record(stream)
         torch.cuda.synchronize(device)
-        barrier(world)
         ms_local = ev0.elapsed_time(ev1) / K
+        if fgraph is not None:          # the flushes alone, timed the same way
+            ev0.record(stream)
+            fgraph.replay()
+            ev1.record(stream)
+            torch.cuda.synchronize(device)
+            flush_ms = ev0.elapsed_time(ev1) / K
+            ms_local -= flush_ms
+        barrier(world)
     else:
         barrier(world)
         torch.cuda.synchronize(device)
@@ -559,7 +589,8 @@ def measure(args, cfg, device, rank, world, splits_override=None):
             "work_per_step_per_gpu": work, "work_unit": "FLOP" if prefill else "byte",
             "logical_kv_bytes_per_step_per_gpu": logical_bytes,
             "logical_kv_gbs": round(logical_bytes * world / (ms * 1e-3) / 1e9, 2),
-            "l2": ("flushed between steps (2x L2 write, outside the timed events)" if flush is not None
+            "l2": ("flushed before every step (2x L2 write in the step graph; the flushes' own time, "
+                   "flush_ms_per_step, is subtracted)" if flush is not None
                    else f"inputs larger than L2 ({kv_bytes / 2**20:.0f} MiB KV per step vs 129 MiB L2)"),
             "parallelism": f"replicas x{world}",
         },
@@ -572,6 +603,7 @@ def measure(args, cfg, device, rank, world, splits_override=None):
                                                                        "both": round(eager_ms, 5)}},
         "step_timing": graph_note,
         "single_step_graph_ms": round(single_ms, 5),
+        "flush_ms_per_step": None if flush_ms is None else round(flush_ms, 5),
         "roofline": {"kernel": (("prefill_tc_kernel (tcgen05: causal attention of the prompt, 128 tokens x 2 query heads per "
                                  "CTA, S and O in Tensor Memory)" if cfg.head_dim == 128 else
                                  "prefill_kernel (mma.sync: causal attention of the prompt, 64 query rows per CTA)") if prefill else

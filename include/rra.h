@@ -363,6 +363,15 @@ RRA_API const char* rra_status_str(int status);
 /* Text of the last CUDA error an entry point saw on this thread ("" if none). */
 RRA_API const char* rra_last_cuda_error(void);
 
+/* Test hook for the bounded-wait timeout path (no counterpart on the pages). While `hold` is
+ * nonzero, the fused bf16 steps (rra_decode_step_*, rra_verify_step up to gamma 8) launched
+ * from any thread write the new tokens but never release the barrier their TMA producer waits
+ * on before loading the tile that holds them: that wait, and the consumers' wait for the tile,
+ * run out after about a second each, the kernel sets RRA_ERR_TIMEOUT and finishes (its outputs
+ * are invalid), and the context stays usable. Nothing faults, traps or hangs. 0 restores normal
+ * operation. Always returns RRA_OK. */
+RRA_API int rra_test_hold_append(int hold);
+
 /* The library links its own copy of the CUDA runtime, whose current device is separate
  * from the caller's: every entry point launches on the device selected here for the
  * calling thread (device 0 until set), and `stream` must belong to that device. */

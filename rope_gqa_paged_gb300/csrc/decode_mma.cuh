@@ -58,6 +58,23 @@ struct MmaCfg {
   static constexpr int kKSteps = D / 16;
 };
 
+// The decode kernel with NT 8-head n-tiles per CTA (up to 8 * NT query heads of one KV head's
+// group): NT = 2 serves 16 heads from every K/V tile (groups of 16 or more heads stream the KV half
+// as often as with 8 heads per CTA); its larger register state runs at two CTAs per SM, with a
+// 3-stage ring so that an SM still keeps 192 KB of K/V in flight.
+template <int D, int NT>
+struct MmaCfgN : MmaCfg<D> {
+  using B = MmaCfg<D>;
+  static constexpr int kStages = NT == 1 ? B::kStages : 3;
+  static constexpr int kCtasPerSm = NT == 1 ? RRA_MMA_CTAS_PER_SM : 2;
+  static constexpr int kRingBytes = kStages * B::kStageBytes;
+  static constexpr int kOffBar = kRingBytes;
+  static constexpr int kOffTable = kOffBar + (2 * kStages + 1) * 8;
+  static constexpr int kOffCs = kOffTable + kMmaTableEntries * 4;
+  static constexpr int kSmemBytes = 1024 + kOffCs + 4 * (D / 2) * 4;
+  static constexpr int kMaxHeads = 8 * NT;
+};
+
 // Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled buffer.
 __device__ __forceinline__ uint32_t swz(int r, int c) { return (r << 7) + (((c ^ r) & 7) << 4); }
 
@@ -201,6 +218,104 @@ __device__ __forceinline__ void mma_step(MmaWarpState<D>& st, const uint32_t (&q
   }
 }
 
+// Online softmax of one 8-head n-tile's score fragment (as in mma_step); returns P as the B operand.
+template <int D, bool CHECK>
+__device__ __forceinline__ void softmax_tile(MmaWarpState<D>& st, const float (&s)[4], int t0, int valid, int lane,
+                                             float scale_log2, uint32_t& b0, uint32_t& b1) {
+  const int ta = t0 + (lane >> 2), tb = ta + 8;
+  float x[2][2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    x[j][0] = (!CHECK || ta < valid) ? s[j] * scale_log2 : -INFINITY;
+    x[j][1] = (!CHECK || tb < valid) ? s[2 + j] * scale_log2 : -INFINITY;
+  }
+  float mnew[2];
+  bool grow = false;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float mx = fmaxf(x[j][0], x[j][1]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    mnew[j] = fmaxf(st.m[j], mx);
+    grow |= mnew[j] > st.m[j];
+  }
+  if (__any_sync(0xffffffffu, grow)) {
+    float alpha[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      alpha[j] = mnew[j] > st.m[j] ? exp2f(st.m[j] - mnew[j]) : 1.f;
+      st.l[j] *= alpha[j];
+      st.m[j] = mnew[j];
+    }
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      st.o[i][0] *= alpha[0];
+      st.o[i][1] *= alpha[1];
+      st.o[i][2] *= alpha[0];
+      st.o[i][3] *= alpha[1];
+    }
+  }
+  float p[2][2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float mref = st.m[j] == -INFINITY ? 0.f : st.m[j];
+    p[j][0] = exp2f(x[j][0] - mref);
+    p[j][1] = exp2f(x[j][1] - mref);
+    st.l[j] += p[j][0] + p[j][1];
+  }
+  b0 = movmatrix_trans(pack_bf16x2(p[0][0], p[1][0]));
+  b1 = movmatrix_trans(pack_bf16x2(p[0][1], p[1][1]));
+}
+
+// mma_step for 16 query heads (two 8-head n-tiles, st[0] heads 0-7 and st[1] heads 8-15): each K
+// and V fragment read from shared memory feeds both n-tiles, whose score chains run side by side.
+template <int D, bool CHECK>
+__device__ __forceinline__ void mma_step2(MmaWarpState<D> (&st)[2], const uint32_t (&qb)[2][D / 16][2],
+                                          uint32_t k_base, uint32_t v_base, uint8_t* v_gen, int t0, int valid,
+                                          int lane, float scale_log2) {
+  using C = MmaCfg<D>;
+  constexpr int HALF = C::kHalfBytes;
+  if (CHECK) {  // zero V rows t0+i >= valid of this slice (each row: kHalves x 128 bytes)
+    const int first = max(valid - t0, 0);
+    if (first < 16) {
+      for (int idx = lane; idx < (16 - first) * C::kHalves * 8; idx += 32) {
+        const int r = t0 + first + idx / (C::kHalves * 8);
+        const int h = (idx / 8) % C::kHalves, c = idx % 8;
+        *reinterpret_cast<uint4*>(v_gen + h * HALF + swz(r, c)) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+    }
+  }
+  float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  {
+    const int mat = lane >> 3;
+    const int r = t0 + (lane & 7) + ((mat & 1) << 3);
+#pragma unroll
+    for (int kk = 0; kk < C::kKSteps; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(k_base + (kk >> 2) * HALF + swz(r, ((kk & 3) << 1) + (mat >> 1)), a);
+      mma_bf16(s[0], a, qb[0][kk][0], qb[0][kk][1]);
+      mma_bf16(s[1], a, qb[1][kk][0], qb[1][kk][1]);
+    }
+  }
+  uint32_t b0[2], b1[2];
+  softmax_tile<D, CHECK>(st[0], s[0], t0, valid, lane, scale_log2, b0[0], b1[0]);
+  softmax_tile<D, CHECK>(st[1], s[1], t0, valid, lane, scale_log2, b0[1], b1[1]);
+  {
+    const int mat = lane >> 3;
+    const int r = t0 + (lane & 7) + ((mat >> 1) << 3);
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      uint32_t a[4];
+      ldsm_x4_trans(v_base + (i >> 2) * HALF + swz(r, ((i & 3) << 1) + (mat & 1)), a);
+      mma_bf16(st[0].o[i], a, b0[0], b1[0]);
+      mma_bf16(st[1].o[i], a, b0[1], b1[1]);
+    }
+  }
+}
+
 // Fused step only: rotates the consumer lane's q fragment (raw bf16 pairs, same layout as
 // the B operand) in place, with cos/sin hi/lo per frequency in `cs`.
 template <int D>
@@ -296,14 +411,14 @@ __device__ __forceinline__ void append_token_bf16(const DecodeArgs& a, const flo
   }
   asm volatile("fence.proxy.async.global;" ::: "memory");  // visible to the TMA that reads the slot
   __syncwarp();
-  if (lane == 0) mbar_arrive(appended);
+  if (lane == 0 && !a.test_hold_append) mbar_arrive(appended);  // the hold: see DecodeArgs
 }
 
-template <int D, bool PAGED, bool FUSED>
-__global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
+template <int D, bool PAGED, bool FUSED, int NT = 1>
+__global__ void __launch_bounds__(MmaCfg<D>::kThreads, (NT == 1 ? RRA_MMA_CTAS_PER_SM : 2))
     decode_mma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                       const DecodeArgs a) {
-  using C = MmaCfg<D>;
+  using C = MmaCfgN<D, NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -474,16 +589,17 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
 
   // ------------------------------------------------------------------ consumers
   constexpr int kConsumerThreads = C::kConsumerWarps * 32;
-  // Q^T as the B operand: lane holds q[head lane/4][dims 16kk + 2(lane%4) + {0,1}] and (+8).
-  uint32_t qb[C::kKSteps][2];
+  // Q^T as the B operand: n-tile n, lane holds q[head 8n + lane/4][dims 16kk + 2(lane%4) + {0,1}] and (+8).
+  uint32_t qb[NT][C::kKSteps][2];
   const int hd = lane >> 2;
-  {
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
     const uint32_t* q = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.q) +
-                                                          (static_cast<size_t>(b) * a.Hq + h0 + hd) * D);
+                                                          (static_cast<size_t>(b) * a.Hq + h0 + 8 * n + hd) * D);
 #pragma unroll
     for (int kk = 0; kk < C::kKSteps; ++kk) {
-      qb[kk][0] = hd < hpc ? q[kk * 8 + (lane & 3)] : 0u;
-      qb[kk][1] = hd < hpc ? q[kk * 8 + 4 + (lane & 3)] : 0u;
+      qb[n][kk][0] = 8 * n + hd < hpc ? q[kk * 8 + (lane & 3)] : 0u;
+      qb[n][kk][1] = 8 * n + hd < hpc ? q[kk * 8 + 4 + (lane & 3)] : 0u;
     }
   }
   if constexpr (FUSED) {
@@ -517,23 +633,29 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
       cs[3 * (D / 2) + threadIdx.x] = static_cast<float>(sn - static_cast<double>(sh));
     }
     named_barrier_sync(1, kConsumerThreads);
-    rotate_q_fragment<D>(qb, cs, lane, a.rope_style);
-    if (warp == 0 && split == 0 && hd < hpc) {  // publish q_rot (rounded to bf16, as used here)
-      uint32_t* qo = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.q_out) +
-                                                 (static_cast<size_t>(b) * a.Hq + h0 + hd) * D);
 #pragma unroll
-      for (int kk = 0; kk < C::kKSteps; ++kk) {
-        qo[kk * 8 + (lane & 3)] = qb[kk][0];
-        qo[kk * 8 + 4 + (lane & 3)] = qb[kk][1];
+    for (int n = 0; n < NT; ++n) rotate_q_fragment<D>(qb[n], cs, lane, a.rope_style);
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+      if (warp == 0 && split == 0 && 8 * n + hd < hpc) {  // publish q_rot (rounded to bf16, as used here)
+        uint32_t* qo = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(a.q_out) +
+                                                   (static_cast<size_t>(b) * a.Hq + h0 + 8 * n + hd) * D);
+#pragma unroll
+        for (int kk = 0; kk < C::kKSteps; ++kk) {
+          qo[kk * 8 + (lane & 3)] = qb[n][kk][0];
+          qo[kk * 8 + 4 + (lane & 3)] = qb[n][kk][1];
+        }
       }
-    }
     if (app_warp) append_token_bf16<D, PAGED>(a, cs, kraw, vraw, phys, b, g, pos, lane, appended);
   }
-  MmaWarpState<D> st;
+  MmaWarpState<D> st[NT];
 #pragma unroll
-  for (int i = 0; i < D / 16; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
-  st.m[0] = st.m[1] = -INFINITY;
-  st.l[0] = st.l[1] = 0.f;
+  for (int n = 0; n < NT; ++n) {
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) st[n].o[i][0] = st[n].o[i][1] = st[n].o[i][2] = st[n].o[i][3] = 0.f;
+    st[n].m[0] = st[n].m[1] = -INFINITY;
+    st[n].l[0] = st[n].l[1] = 0.f;
+  }
 
   for (int it = 0; it < n_tiles; ++it) {
     const int s = it % C::kStages;
@@ -548,10 +670,17 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
 #pragma unroll
     for (int step = 0; step < C::kSteps; ++step) {
       const int t0 = warp * C::kWarpTokens + step * 16;
-      if (valid == C::kTile)
-        mma_step<D, false>(st, qb, k_base, v_base, vst, t0, valid, lane, a.scale_log2);
-      else if (t0 < valid)
-        mma_step<D, true>(st, qb, k_base, v_base, vst, t0, valid, lane, a.scale_log2);
+      if constexpr (NT == 1) {
+        if (valid == C::kTile)
+          mma_step<D, false>(st[0], qb[0], k_base, v_base, vst, t0, valid, lane, a.scale_log2);
+        else if (t0 < valid)
+          mma_step<D, true>(st[0], qb[0], k_base, v_base, vst, t0, valid, lane, a.scale_log2);
+      } else {
+        if (valid == C::kTile)
+          mma_step2<D, false>(st, qb, k_base, v_base, vst, t0, valid, lane, a.scale_log2);
+        else if (t0 < valid)
+          mma_step2<D, true>(st, qb, k_base, v_base, vst, t0, valid, lane, a.scale_log2);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
@@ -560,30 +689,33 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   // ------------------------------------------------------------------ merge the 4 warps
   constexpr int kConsumers = C::kConsumerWarps * 32;
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 4);
-    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 8);
-    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 16);
-  }
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      st[n].l[j] += __shfl_xor_sync(0xffffffffu, st[n].l[j], 4);
+      st[n].l[j] += __shfl_xor_sync(0xffffffffu, st[n].l[j], 8);
+      st[n].l[j] += __shfl_xor_sync(0xffffffffu, st[n].l[j], 16);
+    }
   named_barrier_sync(1, kConsumers);
-  float* red_o = reinterpret_cast<float*>(smem);                 // [warps][8 heads][D]
-  float* red_m = red_o + C::kConsumerWarps * C::kMaxHeads * D;   // [warps][8 heads]
+  float* red_o = reinterpret_cast<float*>(smem);                 // [warps][8 NT heads][D]
+  float* red_m = red_o + C::kConsumerWarps * C::kMaxHeads * D;   // [warps][8 NT heads]
   float* red_l = red_m + C::kConsumerWarps * C::kMaxHeads;
-  {
-    const int hd0 = 2 * (lane & 3), dl = lane >> 2;
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    const int hd0 = 8 * n + 2 * (lane & 3), dl = lane >> 2;
 #pragma unroll
     for (int i = 0; i < D / 16; ++i) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        red_o[(warp * C::kMaxHeads + hd0 + j) * D + 16 * i + dl] = st.o[i][j];
-        red_o[(warp * C::kMaxHeads + hd0 + j) * D + 16 * i + 8 + dl] = st.o[i][2 + j];
+        red_o[(warp * C::kMaxHeads + hd0 + j) * D + 16 * i + dl] = st[n].o[i][j];
+        red_o[(warp * C::kMaxHeads + hd0 + j) * D + 16 * i + 8 + dl] = st[n].o[i][2 + j];
       }
     }
     if (dl == 0) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        red_m[warp * C::kMaxHeads + hd0 + j] = st.m[j];
-        red_l[warp * C::kMaxHeads + hd0 + j] = st.l[j];
+        red_m[warp * C::kMaxHeads + hd0 + j] = st[n].m[j];
+        red_l[warp * C::kMaxHeads + hd0 + j] = st[n].l[j];
       }
     }
   }
@@ -621,16 +753,24 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   }
 }
 
-template <int D, bool PAGED, bool FUSED>
-cudaError_t launch_decode_mma_t(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm, int hpc,
-                                cudaStream_t st) {
-  using C = MmaCfg<D>;
+template <int D, bool PAGED, bool FUSED, int NT>
+cudaError_t launch_decode_mma_nt(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm, int hpc,
+                                 cudaStream_t st) {
+  using C = MmaCfgN<D, NT>;
   static int done[64] = {0};
-  auto kern = decode_mma_kernel<D, PAGED, FUSED>;
+  auto kern = decode_mma_kernel<D, PAGED, FUSED, NT>;
   cudaError_t e = ensure_smem(kern, C::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   const dim3 grid(a.num_splits * ((a.Hq / a.Hkv) / hpc), a.Hkv, a.B);
   return launch_pdl(kern, grid, dim3(C::kThreads), C::kSmemBytes, st, km, vm, a);
+}
+
+// 16 heads per CTA (two n-tiles) when hpc > 8.
+template <int D, bool PAGED, bool FUSED>
+cudaError_t launch_decode_mma_t(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm, int hpc,
+                                cudaStream_t st) {
+  if (hpc > 8) return launch_decode_mma_nt<D, PAGED, FUSED, 2>(a, km, vm, hpc, st);
+  return launch_decode_mma_nt<D, PAGED, FUSED, 1>(a, km, vm, hpc, st);
 }
 
 template <bool PAGED, bool FUSED = false>

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "rra_internal.h"
@@ -13,6 +14,9 @@
 namespace {
 
 thread_local char g_cuda_error[256] = "";
+// rra_test_hold_append: while set, fused bf16 steps launched from any thread hold their append
+// barrier (a test of the bounded waits' timeout path).
+std::atomic<int> g_test_hold_append{0};
 
 int cuda_fail(cudaError_t e, const char* where) {
   std::snprintf(g_cuda_error, sizeof(g_cuda_error), "%s: %s (%s)", where, cudaGetErrorName(e),
@@ -82,6 +86,10 @@ int heads_per_cta(int n_rep, bool mma) {
   return n_rep % 4 == 0 ? 4 : (n_rep % 2 == 0 ? 2 : 1);
 }
 
+// The bf16 decode kernel: 16 query heads per CTA (two 8-head n-tiles, two CTAs per SM) for query
+// groups of a multiple of 16 heads, so each K/V tile serves 16 of them; otherwise up to 8.
+int decode_mma_hpc(int n_rep) { return n_rep % 16 == 0 ? 16 : heads_per_cta(n_rep, true); }
+
 int check_shapes(int B, int Hq, int Hkv, int D, rra_dtype dt) {
   if (dt != RRA_F32 && dt != RRA_BF16) return RRA_EUNSUPPORTED;
   if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0) return RRA_EINVAL;
@@ -143,7 +151,8 @@ int make_plan(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
   if (max_tokens > (int64_t(1) << 30)) return RRA_ERANGE;
   const int n_rep = Hq / Hkv;
   p->mma = use_mma_kernel(dt, D, max_tokens, block_size);
-  p->hpc = heads_per_cta(n_rep, p->mma);
+  p->hpc = p->mma ? decode_mma_hpc(n_rep) : heads_per_cta(n_rep, false);
+  if (p->hpc > 8) p->ctas_per_sm = 2;
   if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
   p->tile = p->mma ? rra::decode_mma_tile_tokens(D) : rra::decode_tile_tokens(D, elem_bytes(dt));
   return plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
@@ -363,6 +372,7 @@ rra::DecodeArgs decode_args(const Plan& p, const void* q, const void* k, const v
   a.scale_log2 = s * 1.4426950408889634f;
   a.err = err;
   a.num_groups = (p.splits + rra::kMergeFanIn - 1) / rra::kMergeFanIn;
+  a.test_hold_append = g_test_hold_append.load(std::memory_order_relaxed);
   if (p.splits > 1) {
     const WsLayout l = ws_layout(B, Hq, D, p.splits);
     uint8_t* base = static_cast<uint8_t*>(ws);
@@ -705,6 +715,11 @@ const char* rra_status_str(int status) {
 }
 
 const char* rra_last_cuda_error(void) { return g_cuda_error; }
+
+int rra_test_hold_append(int hold) {
+  g_test_hold_append.store(hold != 0 ? 1 : 0, std::memory_order_relaxed);
+  return RRA_OK;
+}
 
 int rra_use_device(int device) {
   const cudaError_t e = cudaSetDevice(device);

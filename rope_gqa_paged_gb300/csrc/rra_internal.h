@@ -68,6 +68,10 @@ struct DecodeArgs {
   // positions[b] + 1 and seq_lens is unused; the fused kernel also reads unrotated q,
   // rotates it, writes q_out, and appends rotated k_new / raw v_new at the position.
   const int32_t* positions;
+  // Test of the timeout path (rra_test_hold_append): the append warp of a fused bf16 step writes
+  // the new token but never arrives on the append barrier, so the producer's bounded wait for it
+  // runs out and RRA_ERR_TIMEOUT is set. 0 in every ordinary call.
+  int test_hold_append;
   const void* k_new;            // [B, Hkv, D]
   const void* v_new;            // [B, Hkv, D]
   void* q_out;                  // [B, Hq, D], must not overlap q

@@ -37,6 +37,7 @@ _SIGNATURES = {
     "rra_status_str": (ctypes.c_char_p, [_c_int]),
     "rra_last_cuda_error": (ctypes.c_char_p, []),
     "rra_use_device": (_c_int, [_c_int]),
+    "rra_test_hold_append": (_c_int, [_c_int]),
     "rra_decode_step_contig": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int,
                                         _c_int, _c_f64, _c_int, _c_f32, _c_int, _vp, _c_size, _c_int, _vp, _vp]),
     "rra_decode_step_paged": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _c_int,
@@ -152,6 +153,12 @@ def rra_decode_num_splits(B: int, Hq: int, Hkv: int, D: int, max_tokens: int, bl
 
 def rra_decode_workspace_bytes(B: int, Hq: int, D: int, splits: int) -> int:
     return int(lib().rra_decode_workspace_bytes(B, Hq, D, splits))
+
+
+def rra_test_hold_append(hold: bool) -> None:
+    """Test hook of the bounded-wait timeout path: while held, fused bf16 steps never release
+    their append barrier, so their waits run out (~1 s) and set RRA_ERR_TIMEOUT."""
+    _check("rra_test_hold_append", lib().rra_test_hold_append(1 if hold else 0))
 
 
 def rra_status_str(status: int) -> str:
