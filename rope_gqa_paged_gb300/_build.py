@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB_DIR = os.path.join(HERE, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "librra_gb300.so")
-SOURCES = ["rra_abi.cu", "rope_append.cu", "decode_contig.cu", "decode_paged.cu", "decode_q8.cu", "verify.cu", "prefill.cu", "rra_noalloc.cu"]
+SOURCES = ["rra_abi.cu", "rope_append.cu", "decode_contig.cu", "decode_paged.cu", "decode_q8.cu", "verify.cu", "prefill.cu", "rra_noalloc.cu", "decode_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

@@ -592,6 +592,8 @@ __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_MMA_CTAS_PER_SM)
 
   // ------------------------------------------------------------------ producer
   if (warp == C::kConsumerWarps) {
+    // Lane 0 waits for the stage and sets its byte count; a stage of whole paged blocks (8 or 16
+    // copies) is then issued by all lanes at once, other stages by lane 0.
     if (lane == 0) {
       if (n_q8 > 0) {
         prefetch_tensormap(&k_map);
@@ -601,23 +603,47 @@ __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_MMA_CTAS_PER_SM)
         prefetch_tensormap(&kw_map);
         prefetch_tensormap(&vw_map);
       }
-      int issued = 0;
-      for (int it = 0; it < n_tiles; ++it) {
-        const int s = it % C::kStages;
+    }
+    int issued = 0;
+    for (int it = 0; it < n_tiles; ++it) {
+      const int s = it % C::kStages;
+      uint8_t* kst = smem + s * C::kStageBytes;
+      const bool ring = it >= n_q8;
+      const int t0 = ring ? (it - n_q8) * wrows : start + it * C::kTile;
+      int nblk = 0;  // > 0: whole paged blocks of this stage, issued by the warp
+      uint32_t bytes = ring ? 2 * M::kHalves * wrows * 128 : 2 * C::kTileBytes;
+      if constexpr (PAGED) {
+        const int bs = 1 << a.log2_bs;
+        if (!ring && bs <= C::kTile) {
+          nblk = (min(C::kTile, end - t0) + bs - 1) >> a.log2_bs;
+          bytes = 2 * nblk * bs * C::kRowBytes;
+        }
+      }
+      int ok = 1;
+      if (lane == 0) {
         if (it >= C::kStages && !mbar_wait(&empty[s], ((it / C::kStages) - 1) & 1)) {
           flag_error(a.err, RRA_ERR_TIMEOUT);
-          break;
-        }
-        // the new token: in the ring (before its first tile) or in the appender's last INT8 tile
-        if (appender && it == (has_win ? n_q8 : n_q8 - 1) && !mbar_wait(appended, 0)) {
+          ok = 0;
+        } else if (appender && it == (has_win ? n_q8 : n_q8 - 1) && !mbar_wait(appended, 0)) {
+          // the new token: in the ring (before its first tile) or in the appender's last INT8 tile
           flag_error(a.err, RRA_ERR_TIMEOUT);
-          break;
+          ok = 0;
+        } else {
+          mbar_arrive_expect_tx(&full[s], bytes);
         }
-        uint8_t* kst = smem + s * C::kStageBytes;
-        if (it >= n_q8) {  // bf16 ring rows [t0, t0 + wrows) of (b, g) in 64-dim halves
-          const int t0 = (it - n_q8) * wrows;
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (nblk > 0) {  // whole blocks, one box of bs rows per block
+        const int bs = 1 << a.log2_bs;
+        const int j0 = (t0 >> a.log2_bs) - first_blk;
+        for (int c = lane; c < 2 * nblk; c += 32) {
+          const int jb = c >> 1;
+          uint8_t* dst = (c & 1 ? kst + C::kTileBytes : kst) + jb * bs * C::kRowBytes;
+          tma_g2s_4d(dst, c & 1 ? &v_map : &k_map, 0, g, 0, tbl[j0 + jb], &full[s]);
+        }
+      } else if (lane == 0) {
+        if (ring) {  // bf16 ring rows [t0, t0 + wrows) of (b, g) in 64-dim halves
           uint8_t* vst = kst + M::kHalves * C::kWinHalf;
-          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * M::kHalves * wrows * 128));
           const int bg = b * a.Hkv + g;
 #pragma unroll
           for (int h = 0; h < M::kHalves; ++h) {
@@ -625,39 +651,26 @@ __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_MMA_CTAS_PER_SM)
             tma_g2s_3d(vst + h * C::kWinHalf, &vw_map, 64 * h, t0, bg, &full[s]);
           }
         } else {
-          const int t0 = start + it * C::kTile;
           uint8_t* vst = kst + C::kTileBytes;
-          if constexpr (PAGED) {
+          if constexpr (PAGED) {  // a kTile-row window of one block
             const int bs = 1 << a.log2_bs;
-            if (bs <= C::kTile) {  // whole blocks, one box of bs rows per block
-              const int n = min(C::kTile, end - t0);
-              const int nblk = (n + bs - 1) >> a.log2_bs;
-              mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * nblk * bs * C::kRowBytes));
-              const int j0 = (t0 >> a.log2_bs) - first_blk;
-              for (int jb = 0; jb < nblk; ++jb) {
-                const int phys = tbl[j0 + jb];
-                tma_g2s_4d(kst + jb * bs * C::kRowBytes, &k_map, 0, g, 0, phys, &full[s]);
-                tma_g2s_4d(vst + jb * bs * C::kRowBytes, &v_map, 0, g, 0, phys, &full[s]);
-              }
-            } else {  // a kTile-row window of one block
-              const int phys = tbl[(t0 >> a.log2_bs) - first_blk];
-              const int off = t0 & (bs - 1);
-              mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * C::kTileBytes));
-              tma_g2s_4d(kst, &k_map, 0, g, off, phys, &full[s]);
-              tma_g2s_4d(vst, &v_map, 0, g, off, phys, &full[s]);
-            }
+            const int phys = tbl[(t0 >> a.log2_bs) - first_blk];
+            const int off = t0 & (bs - 1);
+            tma_g2s_4d(kst, &k_map, 0, g, off, phys, &full[s]);
+            tma_g2s_4d(vst, &v_map, 0, g, off, phys, &full[s]);
           } else {  // contiguous: rows [t0, t0 + kTile) of (b, g); rows past max_len read as 0
-            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * C::kTileBytes));
             const int bg = b * a.Hkv + g;
             tma_g2s_3d(kst, &k_map, 0, t0, bg, &full[s]);
             tma_g2s_3d(vst, &v_map, 0, t0, bg, &full[s]);
           }
         }
-        issued = it + 1;
       }
+      __syncwarp();
+      issued = it + 1;
+    }
+    if (lane == 0)
       for (int it = issued > C::kStages ? issued - C::kStages : 0; it < issued; ++it)
         mbar_wait(&full[it % C::kStages], (it / C::kStages) & 1);
-    }
     return;
   }
 

@@ -62,6 +62,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 struct Plan {
   int ctas_per_sm = 0;  // resident CTAs per SM of the kernel (0: 3 for the tensor-core kernels, else 2)
   bool mma = false;  // bf16 tensor-core kernel
+  bool tc = false;   // bf16 tcgen05 kernel for query groups of 16..128 heads (head_dim 128)
   int hpc = 1;
   int tile = 0;
   int chunk = 0;
@@ -142,6 +143,12 @@ int plan_splits(int B, int Hkv, int n_rep, int64_t max_tokens, int block_size, i
   return RRA_OK;
 }
 
+// Smallest query group (heads per KV head) the bf16 decode at head_dim 128 runs on the tcgen05
+// kernel (one CTA per group) instead of the mma.sync kernel (8 or 16 heads per CTA).
+#ifndef RRA_TC_MIN_NREP
+#define RRA_TC_MIN_NREP 16
+#endif
+
 // max_tokens: per-sequence capacity; block_size: 0 for a contiguous cache.
 int make_plan(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size, int requested, rra_dtype dt,
               Plan* p) {
@@ -151,6 +158,15 @@ int make_plan(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
   if (max_tokens > (int64_t(1) << 30)) return RRA_ERANGE;
   const int n_rep = Hq / Hkv;
   p->mma = use_mma_kernel(dt, D, max_tokens, block_size);
+  if (p->mma && D == 128 && n_rep >= RRA_TC_MIN_NREP && n_rep <= 128 &&
+      (block_size > 0 || max_tokens >= rra::kDecodeTcTile)) {
+    // one CTA per (split, KV head, sequence) serving the whole query group on the tcgen05 cores
+    p->tc = true;
+    p->hpc = n_rep;
+    p->ctas_per_sm = 1;
+    p->tile = rra::kDecodeTcTile;
+    return plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
+  }
   p->hpc = p->mma ? decode_mma_hpc(n_rep) : heads_per_cta(n_rep, false);
   if (p->hpc > 8) p->ctas_per_sm = 2;
   if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
@@ -828,6 +844,7 @@ int rra_decode_attn_contig(const void* q_rot, const void* k_cache, const void* v
   a.max_len = max_len;
   a.capacity = max_len;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.tc) return finish_decode(rra::launch_decode_tc(a, km, vm, false, false, s));
   return finish_decode(rra::launch_decode_contig(a, km, vm, dt, p.mma, s));
 }
 
@@ -883,6 +900,7 @@ int decode_attn_paged_ext(const void* q_rot, const void* k_pool, const void* v_p
   a.max_len = 0;
   a.capacity = static_cast<int>(capacity);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (p.tc) return finish_decode(rra::launch_decode_tc(a, km, vm, true, false, s));
   return finish_decode(rra::launch_decode_paged(a, km, vm, dt, p.mma, s));
 }
 
@@ -926,6 +944,7 @@ int rra_decode_step_contig(const void* q, const void* k_new, const void* v_new, 
   a.q_out = q_out;
   a.rope_style = rope_style;
   fill_theta_pi(a.theta_pi, D, rope_base);
+  if (p.tc) return finish_decode(rra::launch_decode_tc(a, km, vm, false, true, s));
   return finish_decode(rra::launch_decode_step_contig(a, km, vm, s));
 }
 
@@ -973,6 +992,7 @@ int rra_decode_step_paged(const void* q, const void* k_new, const void* v_new, c
   a.q_out = q_out;
   a.rope_style = rope_style;
   fill_theta_pi(a.theta_pi, D, rope_base);
+  if (p.tc) return finish_decode(rra::launch_decode_tc(a, km, vm, true, true, s));
   return finish_decode(rra::launch_decode_step_paged(a, km, vm, s));
 }
 

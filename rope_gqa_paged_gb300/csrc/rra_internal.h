@@ -144,6 +144,13 @@ cudaError_t launch_decode_step_contig(const DecodeArgs& a, const CUtensorMap& k_
                                       cudaStream_t stream);
 cudaError_t launch_decode_step_paged(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map,
                                      cudaStream_t stream);
+// The tcgen05 decode kernel (bf16, head_dim 128, query groups of 16 to 128 heads: one CTA per
+// (split, KV head, sequence) serving the whole group, key tiles of 128 tokens); the whole step
+// when `fused` (a.positions, a.k_new, a.v_new, a.q_out set).
+cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map, bool paged,
+                             bool fused, cudaStream_t stream);
+constexpr int kDecodeTcTile = 128;
+
 // Pipeline of the INT8 decode kernel: RRA_Q8_STAGES stages of RRA_Q8_STAGE_BYTES (K + V codes).
 #ifndef RRA_Q8_STAGES
 #define RRA_Q8_STAGES 4

@@ -295,62 +295,59 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
 
   // ------------------------------------------------------------------ producer
   if (warp == C::kConsumerWarps) {
+    // Lane 0 waits for the stage and sets its byte count; the stage's copies then go out from
+    // all lanes at once (as in decode_mma_kernel).
     if (lane == 0) {
       prefetch_tensormap(&k_map);
       prefetch_tensormap(&v_map);
-      int issued = 0;
-      for (int it = 0; it < n_tiles; ++it) {
-        const int s = it % C::kStages;
+    }
+    int issued = 0;
+    for (int it = 0; it < n_tiles; ++it) {
+      const int s = it % C::kStages;
+      const int t0 = start + it * C::kTile;
+      uint8_t* kst = smem + s * C::kStageBytes;
+      uint8_t* vst = kst + C::kHalves * C::kHalfBytes;
+      int nblk = 1, bytes = 2 * C::kHalves * C::kTile * 128;
+      if constexpr (PAGED) {
+        const int bs = 1 << a.log2_bs;
+        if (bs <= C::kTile) {
+          nblk = (min(C::kTile, end - t0) + bs - 1) >> a.log2_bs;
+          bytes = 2 * C::kHalves * nblk * bs * 128;
+        }
+      }
+      int ok = 1;
+      if (lane == 0) {
         if (it >= C::kStages && !mbar_wait(&empty[s], ((it / C::kStages) - 1) & 1)) {
           flag_error(a.err, RRA_ERR_TIMEOUT);
-          break;
-        }
-        if (it == first_new_tile && !mbar_wait(appended, 0)) {  // the new tokens start in this tile
+          ok = 0;
+        } else if (it == first_new_tile && !mbar_wait(appended, 0)) {  // the new tokens start in this tile
           flag_error(a.err, RRA_ERR_TIMEOUT);
-          break;
+          ok = 0;
+        } else {
+          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(bytes));
         }
-        const int t0 = start + it * C::kTile;
-        uint8_t* kst = smem + s * C::kStageBytes;
-        uint8_t* vst = kst + C::kHalves * C::kHalfBytes;
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      for (int c = lane; c < 2 * C::kHalves * nblk; c += 32) {
+        const int kv = c & 1, h = (c >> 1) % C::kHalves, jb = (c >> 1) / C::kHalves;
+        uint8_t* dst = (kv ? vst : kst) + h * C::kHalfBytes;
+        const CUtensorMap* map = kv ? &v_map : &k_map;
         if constexpr (PAGED) {
           const int bs = 1 << a.log2_bs;
-          if (bs <= C::kTile) {
-            const int n = min(C::kTile, end - t0);
-            const int nblk = (n + bs - 1) >> a.log2_bs;
-            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * C::kHalves * nblk * bs * 128));
-            const int j0 = (t0 >> a.log2_bs) - first_blk;
-            for (int jb = 0; jb < nblk; ++jb) {
-              const int phys = tbl[j0 + jb];
-#pragma unroll
-              for (int h = 0; h < C::kHalves; ++h) {
-                tma_g2s_4d(kst + h * C::kHalfBytes + jb * bs * 128, &k_map, 64 * h, g, 0, phys, &full[s]);
-                tma_g2s_4d(vst + h * C::kHalfBytes + jb * bs * 128, &v_map, 64 * h, g, 0, phys, &full[s]);
-              }
-            }
-          } else {
-            const int phys = tbl[(t0 >> a.log2_bs) - first_blk];
-            const int off = t0 & (bs - 1);
-            mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * C::kHalves * C::kTile * 128));
-#pragma unroll
-            for (int h = 0; h < C::kHalves; ++h) {
-              tma_g2s_4d(kst + h * C::kHalfBytes, &k_map, 64 * h, g, off, phys, &full[s]);
-              tma_g2s_4d(vst + h * C::kHalfBytes, &v_map, 64 * h, g, off, phys, &full[s]);
-            }
-          }
+          if (bs <= C::kTile)
+            tma_g2s_4d(dst + jb * bs * 128, map, 64 * h, g, 0, tbl[(t0 >> a.log2_bs) - first_blk + jb], &full[s]);
+          else
+            tma_g2s_4d(dst, map, 64 * h, g, t0 & (bs - 1), tbl[(t0 >> a.log2_bs) - first_blk], &full[s]);
         } else {
-          mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * C::kHalves * C::kTile * 128));
-          const int bg = b * a.Hkv + g;
-#pragma unroll
-          for (int h = 0; h < C::kHalves; ++h) {
-            tma_g2s_3d(kst + h * C::kHalfBytes, &k_map, 64 * h, t0, bg, &full[s]);
-            tma_g2s_3d(vst + h * C::kHalfBytes, &v_map, 64 * h, t0, bg, &full[s]);
-          }
+          tma_g2s_3d(dst, map, 64 * h, t0, b * a.Hkv + g, &full[s]);
         }
-        issued = it + 1;
       }
+      __syncwarp();
+      issued = it + 1;
+    }
+    if (lane == 0)
       for (int it = issued > C::kStages ? issued - C::kStages : 0; it < issued; ++it)
         mbar_wait(&full[it % C::kStages], (it / C::kStages) & 1);
-    }
     return;
   }
 

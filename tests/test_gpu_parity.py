@@ -98,18 +98,20 @@ def test_tiny_fp32_matches_tightly():
 
 # ------------------------------------------------------------------ edge lengths
 @pytest.mark.parametrize("layout,bs", [("contiguous", 0), ("paged", 16), ("paged", 32), ("paged", 64), ("paged", 8)])
-def test_edge_lengths(layout, bs):
-    """L = 1 (the new token alone), around tile and block edges, and a full cache."""
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (32, 1)], ids=["gqa4", "mqa32"])
+def test_edge_lengths(layout, bs, hq, hkv):
+    """L = 1 (the new token alone), around tile and block edges (64-token tiles of the mma.sync
+    kernel, 128-token tiles of the tcgen05 kernel that serves the 32-head group), and a full cache."""
     import dataclasses
     base = CONFIGS["llama3_8b_layer"] if layout == "contiguous" else CONFIGS["batched_paged"]
     cap = 256
     lens = [1, 2, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 129, 200, 255, 256]
-    kw = dict(batch=len(lens), seq_len=None, len_range=(1, cap), num_splits=0)
+    kw = dict(batch=len(lens), seq_len=None, len_range=(1, cap), num_splits=0, n_q_heads=hq, n_kv_heads=hkv)
     if layout == "contiguous":
         kw["max_len"] = cap
     else:
         kw.update(block_size=bs, max_blocks_per_seq=cap // bs, num_blocks=len(lens) * (cap // bs) + 3)
-    cfg = dataclasses.replace(base, name=f"edge_{layout}_{bs}", **kw)
+    cfg = dataclasses.replace(base, name=f"edge_{layout}_{bs}_{hq}_{hkv}", **kw)
     from workloads import gen
     inp = gen.make_inputs(cfg, poison=False)
     inp.lengths[:] = lens
@@ -280,9 +282,11 @@ def test_fused_step_position_errors_are_flagged():
                          ids=["mha", "mqa", "nrep3", "nrep16", "nrep16b", "nrep64"])
 @pytest.mark.parametrize("head_dim", [64, 128])
 @pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused_step"])
-def test_heads_and_head_dim(hq, hkv, head_dim, fused):
-    """GQA groups of 1 to 64 query heads (up to 32 served by one CTA from one KV stream), both
-    head dims, paged blocks of 16, lengths across tiles; split counts 0 and 3."""
+@pytest.mark.parametrize("style", [0, 1], ids=["half_split", "interleaved"])
+def test_heads_and_head_dim(hq, hkv, head_dim, fused, style):
+    """GQA groups of 1 to 64 query heads (at head dim 128 groups of 16 or more run on the tcgen05
+    kernel, one CTA per group), both head dims and RoPE pairings, paged blocks of 16, lengths
+    across tiles; split counts 0 and 3."""
     import dataclasses
     lens = [5, 200, 611]
     cfg = dataclasses.replace(CONFIGS["batched_paged"], name=f"heads_{hq}_{hkv}_{head_dim}", batch=len(lens),
@@ -296,7 +300,6 @@ def test_heads_and_head_dim(hq, hkv, head_dim, fused):
     for b, L in enumerate(lens):
         inp.block_table[b, -(-L // 16):] = -1
     gen.poison_unread(inp)
-    style = 1 if head_dim == 64 else 0
     for splits in (0, 3):
         gpu = H.run_gpu(inp, num_splits=splits, fused=fused, rope_style=style)
         q_ref, k_ref, _, out_ref = H.run_oracle(inp, rope_style=style)
