@@ -68,17 +68,30 @@ struct MmaCfg {
 // group): NT = 2 serves 16 heads from every K/V tile (groups of 16 or more heads stream the KV half
 // as often as with 8 heads per CTA); its larger register state runs at two CTAs per SM, with a
 // 3-stage ring so that an SM still keeps 192 KB of K/V in flight.
-template <int D, int NT>
+//
+// NARROW (head_dim 128, NT 1): two consumer warps, 32-token stages (16 KB) in a 3-stage ring and
+// four CTAs per SM (608 on 152 SMs instead of 456), for grids of few sequences cut into more
+// splits than one wave holds (a 128-split 128K step: 1024 CTAs in 1.7 waves instead of 2.25, the
+// second wave of 416 CTAs still keeping 20 MB of K/V in flight).
+template <int D, int NT, bool NARROW = false>
 struct MmaCfgN : MmaCfg<D> {
   using B = MmaCfg<D>;
-  static constexpr int kStages = NT == 1 ? B::kStages : 3;
-  static constexpr int kCtasPerSm = NT == 1 ? RRA_MMA_CTAS_PER_SM : 2;
-  static constexpr int kRingBytes = kStages * B::kStageBytes;
+  static constexpr int kConsumerWarps = NARROW ? 2 : B::kConsumerWarps;
+  static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+  static constexpr int kTile = NARROW ? 32 : B::kTile;
+  static constexpr int kWarpTokens = kTile / kConsumerWarps;
+  static constexpr int kSteps = kWarpTokens / 16;
+  static constexpr int kHalfBytes = kTile * 128;
+  static constexpr int kStageBytes = 2 * B::kHalves * kHalfBytes;
+  static constexpr int kStages = NARROW || NT == 2 ? 3 : B::kStages;
+  static constexpr int kCtasPerSm = NARROW ? 4 : (NT == 1 ? RRA_MMA_CTAS_PER_SM : 2);
+  static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kOffBar = kRingBytes;
   static constexpr int kOffTable = kOffBar + (2 * kStages + 1) * 8;
   static constexpr int kOffCs = kOffTable + kMmaTableEntries * 4;
   static constexpr int kSmemBytes = 1024 + kOffCs + 4 * (D / 2) * 4;
   static constexpr int kMaxHeads = 8 * NT;
+  static_assert(!NARROW || (D == 128 && NT == 1), "narrow CTAs: head_dim 128, 8 heads");
 };
 
 // Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled buffer.
@@ -420,11 +433,11 @@ __device__ __forceinline__ void append_token_bf16(const DecodeArgs& a, const flo
   if (lane == 0 && !a.test_hold_append) mbar_arrive(appended);  // the hold: see DecodeArgs
 }
 
-template <int D, bool PAGED, bool FUSED, int NT = 1>
-__global__ void __launch_bounds__(MmaCfg<D>::kThreads, (NT == 1 ? RRA_MMA_CTAS_PER_SM : 2))
+template <int D, bool PAGED, bool FUSED, int NT = 1, bool NARROW = false>
+__global__ void __launch_bounds__(MmaCfgN<D, NT, NARROW>::kThreads, MmaCfgN<D, NT, NARROW>::kCtasPerSm)
     decode_mma_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                       const DecodeArgs a) {
-  using C = MmaCfgN<D, NT>;
+  using C = MmaCfgN<D, NT, NARROW>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -680,9 +693,9 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, (NT == 1 ? RRA_MMA_CTAS_P
       const int t0 = warp * C::kWarpTokens + step * 16;
       if constexpr (NT == 1) {
         if (valid == C::kTile)
-          mma_step<D, false>(st[0], qb[0], k_base, v_base, vst, t0, valid, lane, a.scale_log2);
+          mma_step<D, false, C::kHalfBytes>(st[0], qb[0], k_base, v_base, vst, t0, valid, lane, a.scale_log2);
         else if (t0 < valid)
-          mma_step<D, true>(st[0], qb[0], k_base, v_base, vst, t0, valid, lane, a.scale_log2);
+          mma_step<D, true, C::kHalfBytes>(st[0], qb[0], k_base, v_base, vst, t0, valid, lane, a.scale_log2);
       } else {
         if (valid == C::kTile)
           mma_step2<D, false>(st, qb, k_base, v_base, vst, t0, valid, lane, a.scale_log2);
@@ -761,23 +774,25 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, (NT == 1 ? RRA_MMA_CTAS_P
   }
 }
 
-template <int D, bool PAGED, bool FUSED, int NT>
+template <int D, bool PAGED, bool FUSED, int NT, bool NARROW = false>
 cudaError_t launch_decode_mma_nt(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm, int hpc,
                                  cudaStream_t st) {
-  using C = MmaCfgN<D, NT>;
+  using C = MmaCfgN<D, NT, NARROW>;
   static int done[64] = {0};
-  auto kern = decode_mma_kernel<D, PAGED, FUSED, NT>;
+  auto kern = decode_mma_kernel<D, PAGED, FUSED, NT, NARROW>;
   cudaError_t e = ensure_smem(kern, C::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   const dim3 grid(a.num_splits * ((a.Hq / a.Hkv) / hpc), a.Hkv, a.B);
   return launch_pdl(kern, grid, dim3(C::kThreads), C::kSmemBytes, st, km, vm, a);
 }
 
-// 16 heads per CTA (two n-tiles) when hpc > 8.
+// 16 heads per CTA (two n-tiles) when hpc > 8; narrow CTAs when the plan asks for them (a.narrow).
 template <int D, bool PAGED, bool FUSED>
 cudaError_t launch_decode_mma_t(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm, int hpc,
                                 cudaStream_t st) {
   if (hpc > 8) return launch_decode_mma_nt<D, PAGED, FUSED, 2>(a, km, vm, hpc, st);
+  if constexpr (D == 128)
+    if (a.narrow) return launch_decode_mma_nt<D, PAGED, FUSED, 1, true>(a, km, vm, hpc, st);
   return launch_decode_mma_nt<D, PAGED, FUSED, 1>(a, km, vm, hpc, st);
 }
 

@@ -63,6 +63,7 @@ struct Plan {
   int ctas_per_sm = 0;  // resident CTAs per SM of the kernel (0: 3 for the tensor-core kernels, else 2)
   bool mma = false;  // bf16 tensor-core kernel
   bool tc = false;   // bf16 tcgen05 kernel for query groups of 16..128 heads (head_dim 128)
+  bool narrow = false;  // bf16 mma.sync kernel with 2 consumer warps, 32-token stages, 4 CTAs per SM
   int hpc = 1;
   int tile = 0;
   int chunk = 0;
@@ -144,9 +145,11 @@ int plan_splits(int B, int Hkv, int n_rep, int64_t max_tokens, int block_size, i
 }
 
 // Smallest query group (heads per KV head) the bf16 decode at head_dim 128 runs on the tcgen05
-// kernel (one CTA per group) instead of the mma.sync kernel (8 or 16 heads per CTA).
+// kernel (one CTA per group) instead of the mma.sync kernel (16 heads per CTA, the group in
+// slices). Measured on one KV head, 16 sequences of 8192 tokens: 128 heads 76.0 us (tcgen05)
+// against 100.9 us; 64 heads 52.5 against 43.6 us; 32 heads 40.3 against 31.1 us.
 #ifndef RRA_TC_MIN_NREP
-#define RRA_TC_MIN_NREP 16
+#define RRA_TC_MIN_NREP 96
 #endif
 
 // max_tokens: per-sequence capacity; block_size: 0 for a contiguous cache.
@@ -171,7 +174,19 @@ int make_plan(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
   if (p->hpc > 8) p->ctas_per_sm = 2;
   if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
   p->tile = p->mma ? rra::decode_mma_tile_tokens(D) : rra::decode_tile_tokens(D, elem_bytes(dt));
-  return plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
+  st = plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
+  if (st != RRA_OK || !p->mma || D != 128 || p->hpc > 8 || requested == 0) return st;
+  // A requested split count that takes few (sequence, KV head) units past one wave of the
+  // 3-per-SM kernel: narrow CTAs, four per SM, so the grid needs fewer and fuller waves.
+  const int64_t resident = 3 * int64_t(std::max(1, sm_count()));
+  const int64_t units = int64_t(B) * Hkv * (n_rep / p->hpc);
+  if (2 * units > resident || units * p->splits <= resident) return st;
+  Plan q = *p;
+  q.narrow = true;
+  q.ctas_per_sm = 4;
+  q.tile = rra::kDecodeNarrowTile;
+  if (plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, &q) == RRA_OK) *p = q;
+  return st;
 }
 
 // INT8 caches: the INT8 tokens split like the bf16 tensor-core kernel's (tiles of
@@ -388,6 +403,7 @@ rra::DecodeArgs decode_args(const Plan& p, const void* q, const void* k, const v
   a.scale_log2 = s * 1.4426950408889634f;
   a.err = err;
   a.num_groups = (p.splits + rra::kMergeFanIn - 1) / rra::kMergeFanIn;
+  a.narrow = p.narrow ? 1 : 0;
   a.test_hold_append = g_test_hold_append.load(std::memory_order_relaxed);
   if (p.splits > 1) {
     const WsLayout l = ws_layout(B, Hq, D, p.splits);

@@ -62,6 +62,7 @@ struct DecodeArgs {
   int hpc;                      // query heads per CTA (divides Hq / Hkv)
   int num_splits;               // effective split count
   int chunk;                    // tokens per split (a multiple of the tile)
+  int narrow;                   // bf16 decode kernel: 2 consumer warps, 32-token stages, 4 CTAs per SM
   float scale_log2;             // softmax scale * log2(e)
   int32_t* err;
   // Fused step (RoPE + append inside the decode kernel). When `positions` is set, L_b =
@@ -150,6 +151,8 @@ cudaError_t launch_decode_step_paged(const DecodeArgs& a, const CUtensorMap& k_m
 cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map, bool paged,
                              bool fused, cudaStream_t stream);
 constexpr int kDecodeTcTile = 128;
+// Tokens per stage of the narrow bf16 decode CTAs (head_dim 128).
+constexpr int kDecodeNarrowTile = 32;
 
 // Pipeline of the INT8 decode kernel: RRA_Q8_STAGES stages of RRA_Q8_STAGE_BYTES (K + V codes).
 #ifndef RRA_Q8_STAGES

@@ -98,10 +98,10 @@ def test_tiny_fp32_matches_tightly():
 
 # ------------------------------------------------------------------ edge lengths
 @pytest.mark.parametrize("layout,bs", [("contiguous", 0), ("paged", 16), ("paged", 32), ("paged", 64), ("paged", 8)])
-@pytest.mark.parametrize("hq,hkv", [(32, 8), (32, 1)], ids=["gqa4", "mqa32"])
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (32, 1), (128, 1)], ids=["gqa4", "mqa32", "mqa128"])
 def test_edge_lengths(layout, bs, hq, hkv):
     """L = 1 (the new token alone), around tile and block edges (64-token tiles of the mma.sync
-    kernel, 128-token tiles of the tcgen05 kernel that serves the 32-head group), and a full cache."""
+    kernel, 128-token tiles of the tcgen05 kernel that serves the 128-head group), and a full cache."""
     import dataclasses
     base = CONFIGS["llama3_8b_layer"] if layout == "contiguous" else CONFIGS["batched_paged"]
     cap = 256
@@ -278,15 +278,15 @@ def test_fused_step_position_errors_are_flagged():
 
 
 # ------------------------------------------------------------------ heads per KV group
-@pytest.mark.parametrize("hq,hkv", [(8, 8), (32, 1), (12, 4), (32, 2), (64, 4), (64, 1)],
-                         ids=["mha", "mqa", "nrep3", "nrep16", "nrep16b", "nrep64"])
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (32, 1), (12, 4), (32, 2), (64, 4), (64, 1), (128, 1)],
+                         ids=["mha", "mqa", "nrep3", "nrep16", "nrep16b", "nrep64", "nrep128"])
 @pytest.mark.parametrize("head_dim", [64, 128])
 @pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused_step"])
 @pytest.mark.parametrize("style", [0, 1], ids=["half_split", "interleaved"])
 def test_heads_and_head_dim(hq, hkv, head_dim, fused, style):
-    """GQA groups of 1 to 64 query heads (at head dim 128 groups of 16 or more run on the tcgen05
-    kernel, one CTA per group), both head dims and RoPE pairings, paged blocks of 16, lengths
-    across tiles; split counts 0 and 3."""
+    """GQA groups of 1 to 128 query heads (16 heads per CTA from 16 on; at head dim 128 groups of
+    96 or more on the tcgen05 kernel, one CTA per group), both head dims and RoPE pairings, paged
+    blocks of 16, lengths across tiles; split counts 0 and 3."""
     import dataclasses
     lens = [5, 200, 611]
     cfg = dataclasses.replace(CONFIGS["batched_paged"], name=f"heads_{hq}_{hkv}_{head_dim}", batch=len(lens),
