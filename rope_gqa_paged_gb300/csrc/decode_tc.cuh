@@ -6,16 +6,25 @@
 // share one KV head; n_kv = 1 is MQA), "Transformer推理核心：KV Cache、GQA与RoPE原理与工程实践"
 // §2.1, §2.2, §4.2 (softmax(q K^T / sqrt(d)) V, blockwise with a running max and sum).
 //
-// The query heads of the group are the 128 rows of the M dimension (rows past the group are
-// zero); key tiles of 128 tokens stream through a ring of K and V tiles (TMA, 128-byte swizzle,
-// 64-dim halves; paged blocks gathered per block). For key tile j:
-//   S_(j%2) = Q K_j^T    8 MMAs (M 128, N 128, K 16) into TMEM columns [128 (j%2), + 128)
-//   softmax              warps 0-3, one row (query head) per thread: the S row from TMEM, running
-//                        max (moved only when it grows by more than 2^8), P in bf16 to shared
-//                        memory in the K-major 128-byte-swizzled layout
-//   O += P V_j           8 MMAs (V as an MN-major operand) into TMEM columns [256, 384)
+// The 128 rows of the M dimension hold 128 / R copies of the group's query heads (R = 32, 64 or
+// 128: the group size rounded up; rows past the group are zero). Copy c owns tokens
+// [c R, c R + R) of every key tile; key tiles of 128 tokens stream through a ring of K and V tiles
+// (TMA, 128-byte swizzle, 64-dim halves; paged blocks gathered per block). For key tile j:
+//   S_(j%2) = Q K_j^T    8 MMAs (M 128, N 128, K 16) into TMEM columns [128 (j%2), + 128), Q
+//                        (bf16 pairs) the A operand from TMEM columns [384, 448)
+//   softmax              warps 0-3, one row per thread: the R S columns of the row's copy from
+//                        TMEM, running max (moved only when it grows by more than 2^8), P as bf16
+//                        pairs over the first 64 columns of S_(j%2) (zeros in the columns of the
+//                        other copies)
+//   O += P V_j           8 MMAs, P the A operand from TMEM, V an MN-major operand in shared
+//                        memory, into TMEM columns [256, 384)
+// so the O rows of copy c accumulate that copy's share of every tile, and a group of 32 heads
+// spreads its softmax over the four warps (32 columns per thread) instead of running whole
+// 128-column rows in one. The copies' running max, sum and O rows merge in shared memory when
+// the split ends.
 // One lane of warp 5 issues the MMAs in the order S_0, S_1, PV_0, S_2, PV_1, ..., so the tensor
-// core computes the next tile's scores while the softmax of this one runs; warp 4 is the TMA
+// core computes the next tile's scores while the softmax of this one runs (S_(j+2) overwrites
+// P_j after PV_j, which reads it, in issue order); warp 4 is the TMA
 // producer. The split's partial (o unnormalised, running max and sum per head) goes to the
 // workspace and the splits merge as in the other decode kernels (finish_split); a sequence with
 // one split writes its rows directly.
@@ -33,6 +42,12 @@
 #include "decode_mma.cuh"
 #include "tcgen05.cuh"
 
+// K / V tile slots of 32 KB. Q and P live in Tensor Memory, so six slots (three key tiles, 192 KB
+// in flight per SM) fit next to the barriers and the block table.
+#ifndef RRA_TC_RING
+#define RRA_TC_RING 6
+#endif
+
 namespace rra {
 namespace dtc {
 
@@ -41,18 +56,17 @@ constexpr int kTile = 128;                    // tokens per key tile
 constexpr int kD = 128;                       // head dim
 constexpr int kHalfBytes = 128 * 128;         // one 64-element half of a 128-row bf16 tile
 constexpr int kTileBytes = 2 * kHalfBytes;    // a 128 x 128 bf16 tile
-constexpr int kRing = 4;                      // K / V tile slots (K_0, V_0, K_1, V_1, ...)
+constexpr int kRing = RRA_TC_RING;            // K / V tile slots (K_0, V_0, K_1, V_1, ...)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColO = 256;               // O: columns [256, 384)
+constexpr uint32_t kColQ = 384;               // Q as bf16 pairs: columns [384, 448)
 constexpr float kRescaleLog2 = 8.f;           // move the running max only when it grows by more
 
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(128, 128, false);   // Q (K-major) . K^T (K-major)
 constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, 128, true);   // P (K-major) . V (MN-major)
 
-constexpr int kOffQ = 0;
-constexpr int kOffRing = kOffQ + kTileBytes;
-constexpr int kOffP = kOffRing + kRing * kTileBytes;
-constexpr int kOffBar = kOffP + kTileBytes;
+constexpr int kOffRing = 0;
+constexpr int kOffBar = kOffRing + kRing * kTileBytes;
 // q_ready, ring_full[kRing], ring_empty[kRing], s_full[2], p_full, o_done, mma_done, appended
 constexpr int kNumBars = 1 + 2 * kRing + 2 + 3 + 1;
 constexpr int kOffTable = kOffBar + kNumBars * 8;
@@ -63,15 +77,10 @@ constexpr int kSoftmaxThreads = 128;
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
 constexpr int kThreads = kSoftmaxThreads + 64;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+static_assert((kRows * kD + 2 * kRows) * 4 <= kRing * kTileBytes, "the copy merge's scratch fits the ring");
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
-}
-
-// Byte offset of 16-byte chunk `c` (0..15: bf16 columns 8c .. 8c + 7) of row r of a 128 x 128
-// tile stored as two 64-column halves of 128-byte rows with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t chunk_offset(int r, int c) {
-  return (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
 __device__ __forceinline__ float ex2(float x) {  // 2^x on the special-function unit (2^-inf = 0)
@@ -80,26 +89,45 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x on the special-function 
   return y;
 }
 
-// This thread's S row (128 columns: four 32-column loads, one wait).
-__device__ __forceinline__ void ld_row(uint32_t taddr, float (&s)[kTile]) {
-  uint32_t v[kTile / 32][32];
+// N columns of this thread's S row from column address taddr (N / 32 loads, one wait).
+template <int N>
+__device__ __forceinline__ void ld_cols(uint32_t taddr, float (&s)[N]) {
+  uint32_t v[N / 32][32];
 #pragma unroll
-  for (int c = 0; c < kTile / 32; ++c) tc::tmem_ld32(taddr + 32 * c, v[c]);
+  for (int c = 0; c < N / 32; ++c) tc::tmem_ld32(taddr + 32 * c, v[c]);
   tc::tmem_wait_ld();
 #pragma unroll
-  for (int c = 0; c < kTile / 32; ++c)
+  for (int c = 0; c < N / 32; ++c)
 #pragma unroll
     for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(v[c][i]);
 }
 
-template <bool PAGED, bool FUSED>
+// N columns of this thread's row from registers (N = 16, 32 or 64).
+template <int N>
+__device__ __forceinline__ void st_cols(uint32_t taddr, const uint32_t (&v)[N]) {
+  if constexpr (N == 16) {
+    tc::tmem_st16(taddr, v);
+  } else {
+#pragma unroll
+    for (int h = 0; h < N / 32; ++h) {
+      uint32_t t[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) t[i] = v[32 * h + i];
+      tc::tmem_st32(taddr + 32 * h, t);
+    }
+  }
+}
+
+template <bool PAGED, bool FUSED, int R>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                      const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  const int n_rep = a.Hq / a.Hkv;   // rows of this CTA (<= 128)
+  static_assert(R == 32 || R == 64 || R == 128, "rows per copy of the query group");
+  constexpr int kCopies = kRows / R;
+  const int n_rep = a.Hq / a.Hkv;   // heads of the group (<= R)
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int h0 = g * n_rep;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -235,7 +263,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA issue (one lane)
     if (lane == 0) {
-      const uint32_t q_base = smem_addr(smem + kOffQ), p_base = smem_addr(smem + kOffP);
       const uint32_t ring_base = smem_addr(smem + kOffRing);
       bool ok = mbar_wait(q_ready, 0);
       tc::fence_after_sync();
@@ -247,8 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          tc::mma_bf16_ss(tmem + kTile * (j & 1), tc::sw128_desc(q_base + off, 1024, 1024),
-                          tc::sw128_desc(k_base + off, 1024, 1024), kIdescS, kk > 0 ? 1u : 0u);
+          tc::mma_bf16_ts(tmem + kTile * (j & 1), tmem + kColQ + 8 * kk, tc::sw128_desc(k_base + off, 1024, 1024),
+                          kIdescS, kk > 0 ? 1u : 0u);
         }
         tc::commit(&s_full[j & 1]);
         tc::commit(&ring_empty[slot_of(r)]);
@@ -265,11 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after_sync();
         const uint32_t v_base = ring_base + slot_of(rv) * kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t pd = tc::sw128_desc(p_base + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 1024, 1024);
-          tc::mma_bf16_ss(tmem + kColO, pd, tc::sw128_desc(v_base + kk * 2048, kHalfBytes, 1024), kIdescPV,
-                          (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kTile / 16; ++kk)  // P_j: bf16 pairs over S_(j%2)
+          tc::mma_bf16_ts(tmem + kColO, tmem + kTile * (j & 1) + 8 * kk,
+                          tc::sw128_desc(v_base + kk * 2048, kHalfBytes, 1024), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         tc::commit(o_done);
         tc::commit(&ring_empty[slot_of(rv)]);
         // the softmax of tile j has read S_(j%2): tile j + 2 may overwrite it
@@ -281,15 +306,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ softmax: thread = query head
-    const int r = threadIdx.x;                     // row = TMEM lane = head h0 + r
-    const bool real = r < n_rep;
+    const int r = threadIdx.x;                     // row = TMEM lane
+    const int copy = kCopies == 1 ? 0 : r / R;    // copy of the group
+    const int hr = r - copy * R;                   // head h0 + hr
+    const int col0 = copy * R;                     // first token (S column) of the copy
+    const bool real = hr < n_rep;
     const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
     const uint32_t o_col = tmem + lane_base + kColO;
     // the query row into the Q tile (K-major, swizzled): rotated here in the fused step
     {
       uint4 qv[kD / 8];
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
-                                                        (static_cast<size_t>(b) * a.Hq + h0 + (real ? r : 0)) * kD);
+                                                        (static_cast<size_t>(b) * a.Hq + h0 + (real ? hr : 0)) * kD);
 #pragma unroll
       for (int c = 0; c < kD / 8; ++c) qv[c] = real ? src[c] : make_uint4(0u, 0u, 0u, 0u);
       if constexpr (FUSED) {
@@ -355,21 +383,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (real && split == 0) {  // publish q_rot (rounded to bf16, as used here)
+        if (real && copy == 0 && split == 0) {  // publish q_rot (rounded to bf16, as used here)
           uint4* qo = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.q_out) +
-                                               (static_cast<size_t>(b) * a.Hq + h0 + r) * kD);
+                                               (static_cast<size_t>(b) * a.Hq + h0 + hr) * kD);
 #pragma unroll
           for (int c = 0; c < kD / 8; ++c) qo[c] = qv[c];
         }
         if (app_warp) append_token_bf16<kD, PAGED>(a, cs, kraw, vraw, phys, b, g, pos, lane, appended);
       }
+      {  // the row into Tensor Memory: dims (2c, 2c + 1) in column kColQ + c
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(qv);
 #pragma unroll
-      for (int c = 0; c < kD / 8; ++c)
-        *reinterpret_cast<uint4*>(smem + kOffQ + chunk_offset(r, c)) = qv[c];
-      tc::fence_smem_to_async();
+        for (int h = 0; h < 2; ++h) {
+          uint32_t t[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) t[i] = qw[32 * h + i];
+          tc::tmem_st32(tmem + lane_base + kColQ + 32 * h, t);
+        }
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+      }
       mbar_arrive(q_ready);
     }
-    uint8_t* p_smem = smem + kOffP;
     const float sl = a.scale_log2;
     float m_use = -INFINITY, l = 0.f;  // running max (log2 units) and sum
     bool ok = true;
@@ -380,17 +415,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_after_sync();
       const int nvalid = j == n_tiles - 1 ? last_valid : kTile;
-      float sv[kTile];
-      ld_row(tmem + lane_base + kTile * (j & 1), sv);
-      if (nvalid < kTile) {
+      float sv[R];
+      ld_cols<R>(tmem + lane_base + kTile * (j & 1) + col0, sv);
+      if (nvalid < col0 + R) {
 #pragma unroll
-        for (int i = 0; i < kTile; ++i) sv[i] = i < nvalid ? sv[i] : -INFINITY;
+        for (int i = 0; i < R; ++i) sv[i] = col0 + i < nvalid ? sv[i] : -INFINITY;
       }
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = sv[i];
 #pragma unroll
-      for (int i = 8; i < kTile; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
+      for (int i = 8; i < R; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
       const float rmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float m_new = fmaxf(m_use, rmax * sl);
       const bool rescale = m_new > m_use + kRescaleLog2;  // also the first finite max
@@ -426,17 +461,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pw[R / 2];  // P of the copy's tokens as bf16 pairs
 #pragma unroll
-      for (int q = 0; q < kTile / 8; ++q) {
-        uint32_t w[4];
+      for (int q = 0; q < R / 8; ++q) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int i = 8 * q + 2 * e;
           const float e0 = ex2(fmaf(sv[i], sl, -mref)), e1 = ex2(fmaf(sv[i + 1], sl, -mref));
           ls[e] += e0 + e1;
-          w[e] = pack_bf16x2(e0, e1);
+          pw[4 * q + e] = pack_bf16x2(e0, e1);
         }
-        *reinterpret_cast<uint4*>(p_smem + chunk_offset(r, q)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      {  // P_j over the first 64 columns of S_(j%2): this copy's pairs, zeros in the others'
+        const uint32_t pcol = tmem + lane_base + kTile * (j & 1);
+#pragma unroll
+        for (int c = 0; c < kCopies; ++c) {
+          uint32_t t[R / 2];
+#pragma unroll
+          for (int i = 0; i < R / 2; ++i) t[i] = c == copy ? pw[i] : 0u;
+          st_cols<R / 2>(pcol + c * (R / 2), t);
+        }
       }
       l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {  // O rows whose max moved (alpha = 1 elsewhere)
@@ -451,41 +495,105 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::tmem_wait_st();
       }
-      tc::fence_smem_to_async();
+      tc::tmem_wait_st();
+      tc::fence_smem_to_async();  // the zeroed V rows of a partial last tile, for the MMA's reads
       tc::fence_before_sync();
       mbar_arrive(p_full);
     }
     // ------------------------------------------------------------------ epilogue: this split's rows
-    if (ok && warp_wait(o_done, (n_tiles - 1) & 1)) {
-      tc::fence_after_sync();
-      const size_t bh = static_cast<size_t>(b) * a.Hq + h0 + r;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+    const bool done = ok && warp_wait(o_done, (n_tiles - 1) & 1);  // warp-uniform
+    if (!done) flag_error(a.err, RRA_ERR_TIMEOUT);
+    if constexpr (kCopies == 1) {
+      if (done) {
+        tc::fence_after_sync();
+        const size_t bh = static_cast<size_t>(b) * a.Hq + h0 + r;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t v[32];
+          tc::tmem_ld32(o_col + 32 * c, v);
+          tc::tmem_wait_ld();
+          if (!real) continue;
+          if (n_work == 1) {
+            uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + bh * kD) + 4 * c;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              out[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i]) * inv, __uint_as_float(v[8 * i + 1]) * inv),
+                                  pack_bf16x2(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv),
+                                  pack_bf16x2(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv),
+                                  pack_bf16x2(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv));
+          } else {
+            float4* po = reinterpret_cast<float4*>(a.ws_o + (bh * a.num_splits + split) * kD) + 8 * c;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              po[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                  __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+          }
+        }
+        if (real && n_work > 1)
+          *reinterpret_cast<float2*>(a.ws_ml + 2 * (bh * a.num_splits + split)) = make_float2(m_use, l);
+      }
+    } else {
+      // merge the copies of each head: O rows scaled to the common max go through shared memory
+      // (the ring: every copy has landed and every MMA has read it by now), float4 column group
+      // q of row x at slot (q + x) % 32 so that eight consecutive rows hit distinct banks
+      float* xo = reinterpret_cast<float*>(smem + kOffRing);  // [128 rows][kD]
+      float* xm = xo + kRows * kD;                             // [128] running max
+      float* xl = xm + kRows;                                  // [128] running sum
+      xm[r] = done ? m_use : -INFINITY;
+      xl[r] = done ? l : 0.f;
+      named_barrier_sync(1, kSoftmaxThreads);
+      float M = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kCopies; ++c) M = fmaxf(M, xm[c * R + hr]);
+      const float wself = (done && m_use != -INFINITY) ? ex2(m_use - M) : 0.f;
+      if (done) tc::fence_after_sync();
 #pragma unroll 1
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t v[32];
-        tc::tmem_ld32(o_col + 32 * c, v);
-        tc::tmem_wait_ld();
-        if (!real) continue;
-        if (n_work == 1) {
-          uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + bh * kD) + 4 * c;
+        if (done) {
+          tc::tmem_ld32(o_col + 32 * c, v);
+          tc::tmem_wait_ld();
+        }
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            out[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i]) * inv, __uint_as_float(v[8 * i + 1]) * inv),
-                                pack_bf16x2(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv),
-                                pack_bf16x2(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv),
-                                pack_bf16x2(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv));
-        } else {
-          float4* po = reinterpret_cast<float4*>(a.ws_o + (bh * a.num_splits + split) * kD) + 8 * c;
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            po[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
-                                __uint_as_float(v[4 * i + 3]));
+        for (int i = 0; i < 8; ++i) {
+          const float4 x = done ? make_float4(__uint_as_float(v[4 * i]) * wself, __uint_as_float(v[4 * i + 1]) * wself,
+                                              __uint_as_float(v[4 * i + 2]) * wself, __uint_as_float(v[4 * i + 3]) * wself)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+          *reinterpret_cast<float4*>(xo + r * kD + 4 * ((8 * c + i + r) & 31)) = x;
         }
       }
-      if (real && n_work > 1)
-        *reinterpret_cast<float2*>(a.ws_ml + 2 * (bh * a.num_splits + split)) = make_float2(m_use, l);
-    } else {
-      flag_error(a.err, RRA_ERR_TIMEOUT);
+      named_barrier_sync(1, kSoftmaxThreads);
+      if (copy == 0 && real) {  // one thread per head sums the copies
+        float L = 0.f;
+#pragma unroll
+        for (int c = 0; c < kCopies; ++c) {
+          const float mc = xm[c * R + hr];
+          if (mc != -INFINITY) L = fmaf(ex2(mc - M), xl[c * R + hr], L);
+        }
+        const size_t bh = static_cast<size_t>(b) * a.Hq + h0 + hr;
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll 1
+        for (int q = 0; q < kD / 4; ++q) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < kCopies; ++c) {
+            const int x = c * R + hr;
+            const float4 y = *reinterpret_cast<const float4*>(xo + x * kD + 4 * ((q + x) & 31));
+            acc.x += y.x;
+            acc.y += y.y;
+            acc.z += y.z;
+            acc.w += y.w;
+          }
+          if (n_work == 1) {
+            uint2* out = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.out) + bh * kD) + q;
+            *out = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+          } else {
+            reinterpret_cast<float4*>(a.ws_o + (bh * a.num_splits + split) * kD)[q] = acc;
+          }
+        }
+        if (n_work > 1) *reinterpret_cast<float2*>(a.ws_ml + 2 * (bh * a.num_splits + split)) = make_float2(M, L);
+      }
     }
     tc::fence_before_sync();
     if (n_work > 1) {  // the last split of this (sequence, KV head) merges the partials
@@ -502,14 +610,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool PAGED, bool FUSED>
-cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t st) {
+template <bool PAGED, bool FUSED, int R>
+cudaError_t launch_r(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t st) {
   static int done[64] = {0};
-  auto kern = decode_tc_kernel<PAGED, FUSED>;
+  auto kern = decode_tc_kernel<PAGED, FUSED, R>;
   cudaError_t e = ensure_smem(kern, kSmemBytes, done);
   if (e != cudaSuccess) return e;
   const dim3 grid(a.num_splits, a.Hkv, a.B);
   return launch_pdl(kern, grid, dim3(kThreads), kSmemBytes, st, km, vm, a);
+}
+
+// Rows per copy of the query group: the group size rounded up to 32, 64 or 128.
+template <bool PAGED, bool FUSED>
+cudaError_t launch_t(const DecodeArgs& a, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t st) {
+  const int n_rep = a.Hq / a.Hkv;
+  if (n_rep <= 32) return launch_r<PAGED, FUSED, 32>(a, km, vm, st);
+  if (n_rep <= 64) return launch_r<PAGED, FUSED, 64>(a, km, vm, st);
+  return launch_r<PAGED, FUSED, 128>(a, km, vm, st);
 }
 
 }  // namespace dtc

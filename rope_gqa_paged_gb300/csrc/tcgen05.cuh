@@ -1,6 +1,6 @@
 // Fifth-generation tensor core (tcgen05) primitives for sm_103a, as inline PTX: Tensor Memory
-// allocation, the single-thread MMA with operands in shared memory (by matrix descriptor) and
-// the accumulator in Tensor Memory, its completion through an mbarrier, and the warp loads and
+// allocation, the single-thread MMA with operands in shared memory (by matrix descriptor) or A
+// in Tensor Memory and the accumulator in Tensor Memory, its completion through an mbarrier, and the warp loads and
 // stores between Tensor Memory and registers.
 //
 // Tensor Memory (TMEM) is 128 lanes x 512 columns of 32-bit cells per SM; an address is
@@ -67,6 +67,20 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] . B[smem]: A is M rows (lane i = row i) of K 16-bit elements packed two
+// per 32-bit column (element 2c in the low half of column c); one MMA reads K = 16 of them,
+// 8 columns from `a_tmem`. The MMAs one thread issues run in issue order, so an MMA may
+// overwrite Tensor Memory that an earlier one reads as A.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued before has completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
@@ -92,6 +106,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
       "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
       RRA_W8(0), RRA_W8(8), RRA_W8(16), RRA_W8(24)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      RRA_W8(0), RRA_W8(8)
       : "memory");
 }
 #undef RRA_R8
