@@ -282,6 +282,117 @@ __device__ void merge_partials(const DecodeArgs& a, const float* src_o, const fl
   }
 }
 
+// merge_partials with the partial o rows brought into shared memory by bulk copies: the `count`
+// rows of one head are contiguous in the [rows][stride][D] array, so one copy per head moves
+// them, all copies of a chunk of heads in flight at once instead of one L2 round trip per output
+// item and batch. `scratch_bytes` of shared memory at `scratch` (16-byte aligned, free of pending
+// copies) hold a barrier, the weights and as many heads' rows as fit; returns false, having done
+// nothing, when not even one head fits.
+template <typename T, int D, typename OutRow = SameRow>
+__device__ bool merge_partials_bulk(const DecodeArgs& a, const float* src_o, const float* src_ml, int stride, int first,
+                                    int count, int hpc, size_t row0, float* dst_o, float* dst_ml, int dst_stride,
+                                    int dst_idx, float* scratch, int scratch_bytes, int tid, int nthreads,
+                                    OutRow out_row = OutRow()) {
+  constexpr int kQ = D / 4;
+  const int head_bytes = count * D * 4;
+  const int w_floats = ((2 * hpc * count + 2 * hpc) + 3) & ~3;  // weights, sums, merged (M, l)
+  const int o_off = 16 + w_floats * 4;                            // bytes: barrier, weights, rows
+  const int chunk = (scratch_bytes - o_off) / head_bytes;         // heads per chunk
+  if (chunk < 1) return false;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(scratch);
+  float* sm_w = scratch + 4;                 // [hpc][count]: m_i, then the weights
+  float* sm_l = sm_w + hpc * count;          // [hpc][count]
+  float* sm_ml = sm_l + hpc * count;         // [hpc][2]
+  float* obuf = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(scratch) + o_off);
+  const int warp = tid >> 5, lane = tid & 31;
+  // the first chunk's copies go out before the (m, l) loads so that the round trips overlap
+  auto issue = [&](int hA, int hB) {
+    if (warp != 0) return;
+    if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>((hB - hA) * head_bytes));
+    __syncwarp();
+    for (int h = hA + lane; h < hB; h += 32)
+      bulk_g2s(obuf + static_cast<size_t>(h - hA) * count * D, src_o + ((row0 + h) * stride + first) * D,
+               static_cast<uint32_t>(head_bytes), bar);
+  };
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    // the partials were written through the generic proxy and acquired by the arrival counter
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+  }
+  named_barrier_sync(1, nthreads);
+  issue(0, min(chunk, hpc));
+  for (int i = tid; i < hpc * count; i += nthreads) {
+    const int h = i / count, k = i - h * count;
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(src_ml) + (row0 + h) * stride + first + k);
+    sm_w[i] = ml.x;
+    sm_l[i] = ml.y;
+  }
+  named_barrier_sync(1, nthreads);
+  const bool final_row = dst_o == nullptr;
+  for (int h = warp; h < hpc; h += nthreads >> 5) {
+    float M = -INFINITY;
+    for (int k = lane; k < count; k += 32) M = fmaxf(M, sm_w[h * count + k]);
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+    float ls = 0.f;
+    if (M != -INFINITY)
+      for (int k = lane; k < count; k += 32) ls = fmaf(exp2f(sm_w[h * count + k] - M), sm_l[h * count + k], ls);
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, x);
+    const float scale = final_row ? (ls > 0.f ? 1.f / ls : 0.f) : 1.f;
+    __syncwarp();
+    for (int k = lane; k < count; k += 32)
+      sm_w[h * count + k] = M != -INFINITY ? exp2f(sm_w[h * count + k] - M) * scale : 0.f;
+    if (lane == 0) {
+      sm_ml[2 * h] = M;
+      sm_ml[2 * h + 1] = ls;
+    }
+  }
+  named_barrier_sync(1, nthreads);
+  bool ok = true;
+  uint32_t parity = 0;
+  for (int hA = 0; hA < hpc; hA += chunk, parity ^= 1u) {
+    const int hB = min(hpc, hA + chunk);
+    if (hA > 0) issue(hA, hB);
+    // every thread waits for the chunk; the vote keeps the threads on one path if a wait ran out
+    ok = named_barrier_and(1, nthreads, mbar_wait(bar, parity));
+    if (!ok) break;
+    {
+      for (int i = tid; i < (hB - hA) * kQ; i += nthreads) {
+        const int hl = i / kQ, q = i - hl * kQ, h = hA + hl;
+        const float4* o = reinterpret_cast<const float4*>(obuf + static_cast<size_t>(hl) * count * D) + q;
+        const float* wts = sm_w + h * count;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < count; ++k) {
+          const float4 v = o[k * kQ];
+          const float wv = wts[k];
+          acc.x = fmaf(wv, v.x, acc.x);
+          acc.y = fmaf(wv, v.y, acc.y);
+          acc.z = fmaf(wv, v.z, acc.z);
+          acc.w = fmaf(wv, v.w, acc.w);
+        }
+        const int d = 4 * q;
+        if (final_row) {
+          T* out = static_cast<T*>(a.out) + out_row(row0 + h) * D + d;
+          Elem<T>::store(out, acc.x);
+          Elem<T>::store(out + 1, acc.y);
+          Elem<T>::store(out + 2, acc.z);
+          Elem<T>::store(out + 3, acc.w);
+        } else {
+          const size_t pd = (row0 + h) * dst_stride + dst_idx;
+          *reinterpret_cast<float4*>(dst_o + pd * D + d) = acc;
+          if (d == 0) *reinterpret_cast<float2*>(dst_ml + 2 * pd) = make_float2(sm_ml[2 * h], sm_ml[2 * h + 1]);
+        }
+      }
+    }
+    named_barrier_sync(1, nthreads);  // the chunk's rows are read before the next copies land
+  }
+  if (!ok && tid == 0) flag_error(a.err, RRA_ERR_TIMEOUT);
+  if (tid == 0) asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+  return true;
+}
+
 // Run by all consumer threads of a CTA after each has written its share of this split's
 // partial (index `split` of the [rows][num_splits] partial arrays). With n <= kMergeFanIn
 // splits, the last split to arrive merges them all into the output. With more, splits form
@@ -291,29 +402,36 @@ __device__ void merge_partials(const DecodeArgs& a, const float* src_o, const fl
 template <typename T, int D, typename OutRow = SameRow, bool EARLY = true>
 __device__ __forceinline__ void finish_split_rows(const DecodeArgs& a, size_t row0, int hpc, int split, int n,
                                                   float* scratch, int* s_flag, int tid, int nthreads,
-                                                  OutRow out_row = OutRow()) {
+                                                  OutRow out_row = OutRow(), int scratch_bytes = 0) {
   const int S = a.num_splits, G = a.num_groups;
+  // scratch_bytes > 0: the partials come in by bulk copies when one head's rows fit
+  auto merge = [&](const float* so, const float* sml, int stride, int first, int count, float* dst_o, float* dst_ml,
+                   int dst_stride, int dst_idx, auto orow) {
+    if (scratch_bytes > 0 && merge_partials_bulk<T, D>(a, so, sml, stride, first, count, hpc, row0, dst_o, dst_ml,
+                                                       dst_stride, dst_idx, scratch, scratch_bytes, tid, nthreads, orow))
+      return;
+    merge_partials<T, D, decltype(orow), EARLY>(a, so, sml, stride, first, count, hpc, row0, dst_o, dst_ml, dst_stride,
+                                                dst_idx, scratch, tid, nthreads, orow);
+  };
   if (n <= kMergeFanIn) {
     if (arrive_last(a.counters + row0, n, s_flag, a.err, tid, nthreads))
-      merge_partials<T, D, OutRow, EARLY>(a, a.ws_o, a.ws_ml, S, 0, n, hpc, row0, nullptr, nullptr, 0, 0, scratch,
-                                          tid, nthreads, out_row);
+      merge(a.ws_o, a.ws_ml, S, 0, n, nullptr, nullptr, 0, 0, out_row);
     return;
   }
   const int grp = split / kMergeFanIn, first = grp * kMergeFanIn;
   const int gsize = min(kMergeFanIn, n - first);
   if (!arrive_last(a.group_counters + row0 * G + grp, gsize, s_flag, a.err, tid, nthreads)) return;
-  merge_partials<T, D, SameRow, EARLY>(a, a.ws_o, a.ws_ml, S, first, gsize, hpc, row0, a.ws2_o, a.ws2_ml, G, grp,
-                                       scratch, tid, nthreads);
+  merge(a.ws_o, a.ws_ml, S, first, gsize, a.ws2_o, a.ws2_ml, G, grp, SameRow());
   const int groups = (n + kMergeFanIn - 1) / kMergeFanIn;
   if (arrive_last(a.counters + row0, groups, s_flag, a.err, tid, nthreads))
-    merge_partials<T, D, OutRow, EARLY>(a, a.ws2_o, a.ws2_ml, G, 0, groups, hpc, row0, nullptr, nullptr, 0, 0,
-                                        scratch, tid, nthreads, out_row);
+    merge(a.ws2_o, a.ws2_ml, G, 0, groups, nullptr, nullptr, 0, 0, out_row);
 }
 
 template <typename T, int D>
 __device__ __forceinline__ void finish_split(const DecodeArgs& a, int b, int h0, int hpc, int split, int n,
-                                             float* scratch, int* s_flag, int tid, int nthreads) {
-  finish_split_rows<T, D>(a, static_cast<size_t>(b) * a.Hq + h0, hpc, split, n, scratch, s_flag, tid, nthreads);
+                                             float* scratch, int* s_flag, int tid, int nthreads, int scratch_bytes = 0) {
+  finish_split_rows<T, D>(a, static_cast<size_t>(b) * a.Hq + h0, hpc, split, n, scratch, s_flag, tid, nthreads,
+                          SameRow(), scratch_bytes);
 }
 
 template <typename T, int D, int HPC, bool PAGED>

@@ -910,7 +910,7 @@ __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_MMA_CTAS_PER_SM)
   if (n_work > 1) {
     __shared__ int s_last;
     finish_split<__nv_bfloat16, D>(a, b, h0, hpc, split, n_work, reinterpret_cast<float*>(smem), &s_last,
-                                   threadIdx.x, kConsumers);
+                                   threadIdx.x, kConsumers, C::kRingBytes);
   }
 }
 

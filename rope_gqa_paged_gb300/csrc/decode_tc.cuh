@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __shared__ int s_last;
       // scratch: the ring (every copy has landed and every MMA has read it by now)
       finish_split<__nv_bfloat16, kD>(a, b, h0, n_rep, split, n_work, reinterpret_cast<float*>(smem + kOffRing),
-                                      &s_last, threadIdx.x, kSoftmaxThreads);
+                                      &s_last, threadIdx.x, kSoftmaxThreads, kRing * kTileBytes);
     }
   }
   __syncthreads();

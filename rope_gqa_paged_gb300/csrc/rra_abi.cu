@@ -146,8 +146,9 @@ int plan_splits(int B, int Hkv, int n_rep, int64_t max_tokens, int block_size, i
 
 // Smallest query group (heads per KV head) the bf16 decode at head_dim 128 runs on the tcgen05
 // kernel (one CTA per group) instead of the mma.sync kernel (16 heads per CTA, the group in
-// slices). Measured on one KV head, 16 sequences of 8192 tokens: 128 heads 76.0 us (tcgen05)
-// against 100.9 us; 64 heads 52.5 against 43.6 us; 32 heads 40.3 against 31.1 us.
+// slices). Measured on one KV head, 16 sequences of 8192 tokens: 128 heads 64.6 us (tcgen05)
+// against 101.6 us; 64 heads 46.1 against 44.8 us; 32 heads 37.2 against 32.6 us; 16 heads 33.7
+// against 31.4 us.
 #ifndef RRA_TC_MIN_NREP
 #define RRA_TC_MIN_NREP 96
 #endif

@@ -114,6 +114,20 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Named barrier that also returns whether `v` held in every participating thread.
+__device__ __forceinline__ bool named_barrier_and(int id, int threads, bool v) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 q, %3, 0;\n\t"
+      "bar.red.and.pred p, %1, %2, q;\n\t"
+      "selp.s32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(threads), "r"(v ? 1 : 0)
+      : "memory");
+  return r != 0;
+}
+
 // Launches kern<<<grid, block, smem, stream>>>(args...) with programmatic stream serialisation
 // (the kernel may start before the previous kernel in the stream ends; it calls pdl_wait()
 // before reading anything that kernel may write).

@@ -527,7 +527,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     __shared__ int s_last;
     finish_split_rows<__nv_bfloat16, D, VerifyRows, false>(a, vbase, rows, split, n_work,
                                                            reinterpret_cast<float*>(smem), &s_last, threadIdx.x,
-                                                           kConsumers, out_row);
+                                                           kConsumers, out_row, C::kRingBytes);
   }
 }
 
