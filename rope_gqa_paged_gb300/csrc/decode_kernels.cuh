@@ -286,8 +286,10 @@ __device__ void merge_partials(const DecodeArgs& a, const float* src_o, const fl
 // rows of one head are contiguous in the [rows][stride][D] array, so one copy per head moves
 // them, all copies of a chunk of heads in flight at once instead of one L2 round trip per output
 // item and batch. `scratch_bytes` of shared memory at `scratch` (16-byte aligned, free of pending
-// copies) hold a barrier, the weights and as many heads' rows as fit; returns false, having done
-// nothing, when not even one head fits.
+// copies) hold a barrier, the weights and as many heads' rows as fit, chunk after chunk of
+// heads; returns false, having done nothing, when not even one head fits. (One CTA's bulk copies
+// move a few tens of GB/s, so the gain is largest where the register path is weakest: many heads,
+// many partials or few threads, as in the two-consumer-warp CTAs of a 128-split step.)
 template <typename T, int D, typename OutRow = SameRow>
 __device__ bool merge_partials_bulk(const DecodeArgs& a, const float* src_o, const float* src_ml, int stride, int first,
                                     int count, int hpc, size_t row0, float* dst_o, float* dst_ml, int dst_stride,
@@ -404,7 +406,7 @@ __device__ __forceinline__ void finish_split_rows(const DecodeArgs& a, size_t ro
                                                   float* scratch, int* s_flag, int tid, int nthreads,
                                                   OutRow out_row = OutRow(), int scratch_bytes = 0) {
   const int S = a.num_splits, G = a.num_groups;
-  // scratch_bytes > 0: the partials come in by bulk copies when one head's rows fit
+  // scratch_bytes > 0: the partials come in by bulk copies when they fit (see merge_partials_bulk)
   auto merge = [&](const float* so, const float* sml, int stride, int first, int count, float* dst_o, float* dst_ml,
                    int dst_stride, int dst_idx, auto orow) {
     if (scratch_bytes > 0 && merge_partials_bulk<T, D>(a, so, sml, stride, first, count, hpc, row0, dst_o, dst_ml,

@@ -472,7 +472,7 @@ __device__ __forceinline__ void append_token_q8(const DecodeArgs& a, const float
 }
 
 template <int D, int BITS, bool PAGED, bool FUSED>
-__global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_MMA_CTAS_PER_SM)
+__global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_Q8_CTAS_PER_SM)
     decode_q8_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                      const __grid_constant__ CUtensorMap kw_map, const __grid_constant__ CUtensorMap vw_map,
                      const DecodeArgs a) {

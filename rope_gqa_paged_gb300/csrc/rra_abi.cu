@@ -207,6 +207,7 @@ int make_plan_q8(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_si
   p->hpc = heads_per_cta(n_rep, true);
   if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
   p->tile = rra::decode_q8_tile_tokens(D, bits);
+  p->ctas_per_sm = RRA_Q8_CTAS_PER_SM;
   if (block_size > 0 ? block_size < 8 : max_tokens < p->tile) return RRA_EUNSUPPORTED;
   return plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
 }

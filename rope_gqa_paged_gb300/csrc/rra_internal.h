@@ -161,6 +161,10 @@ constexpr int kDecodeNarrowTile = 32;
 #ifndef RRA_Q8_STAGE_BYTES
 #define RRA_Q8_STAGE_BYTES 16384
 #endif
+// Resident CTAs per SM of the INT8 / INT4 decode kernel (its launch bounds and the split plan).
+#ifndef RRA_Q8_CTAS_PER_SM
+#define RRA_Q8_CTAS_PER_SM 3
+#endif
 // Speculative verify: attention of gamma new tokens per sequence (a.gamma, a.positions set).
 // fused: the whole step (a.q unrotated; a.k_new, a.v_new, a.q_out, a.rope_style, a.theta_pi set;
 // gamma <= 8).
