@@ -152,6 +152,38 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
   return old;
 }
 
+// The block ids of a split's chunk, loaded before the sequence length is known so that the two
+// global loads overlap: entries first_blk .. of sequence b's table row that the chunk can reach
+// whatever the length (clamped to the row), N per thread. Only the first n_blk, those the length
+// reaches, are checked and kept (store): the others may be unused (-1) entries.
+template <int N>
+struct ChunkBlockIds {
+  int id[N];
+  __device__ __forceinline__ void load(const DecodeArgs& a, int b, int first_blk, int tid, int nthreads) {
+    const int32_t* row = a.block_table + static_cast<size_t>(b) * a.max_blocks_per_seq + first_blk;
+    const int reach = min(((a.chunk + (1 << a.log2_bs) - 1) >> a.log2_bs) + 1, a.max_blocks_per_seq - first_blk);
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const int i = tid + k * nthreads;
+      id[k] = i < reach ? row[i] : 0;
+    }
+  }
+  __device__ __forceinline__ void store(const DecodeArgs& a, int32_t* tbl, int n_blk, int tid, int nthreads) const {
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      const int i = tid + k * nthreads;
+      if (i < n_blk) {
+        int v = id[k];
+        if (v < 0 || v >= a.num_blocks) {
+          flag_error(a.err, RRA_ERR_BLOCK_ID);
+          v = 0;
+        }
+        tbl[i] = v;
+      }
+    }
+  }
+};
+
 // Counts this CTA's arrival at `cnt` (all `nthreads` consumer threads call it after their
 // last write). True in the CTA whose arrival brings the count to `target`; that CTA also puts
 // the counter back to zero, ready for the next call. No CTA ever waits for another.

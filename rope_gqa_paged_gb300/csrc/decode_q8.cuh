@@ -518,6 +518,9 @@ __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_Q8_CTAS_PER_SM)
     }
   }
   pdl_wait();
+  // the chunk's block ids load alongside the sequence length
+  ChunkBlockIds<(kMmaTableEntries + C::kThreads - 1) / C::kThreads> pre_ids;
+  if constexpr (PAGED) pre_ids.load(a, b, (split * a.chunk) >> a.log2_bs, threadIdx.x, C::kThreads);
 
   int L;
   if constexpr (FUSED) {
@@ -578,15 +581,7 @@ __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_Q8_CTAS_PER_SM)
   if (PAGED && n_q8 > 0) {
     first_blk = start >> a.log2_bs;
     const int n_blk = ((end - 1) >> a.log2_bs) - first_blk + 1;
-    const int32_t* row = a.block_table + static_cast<size_t>(b) * a.max_blocks_per_seq + first_blk;
-    for (int i = threadIdx.x; i < n_blk; i += blockDim.x) {
-      int id = row[i];
-      if (id < 0 || id >= a.num_blocks) {
-        flag_error(a.err, RRA_ERR_BLOCK_ID);
-        id = 0;
-      }
-      tbl[i] = id;
-    }
+    pre_ids.store(a, tbl, n_blk, threadIdx.x, C::kThreads);
   }
   __syncthreads();
 

@@ -245,6 +245,9 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
 
   pdl_launch_dependents();
   pdl_wait();  // the kernel before this one (the append, or the previous step) has finished
+  // the chunk's block ids load alongside the position
+  ChunkBlockIds<(kMmaTableEntries + C::kThreads - 1) / C::kThreads> pre_ids;
+  if constexpr (PAGED) pre_ids.load(a, b, (split * a.chunk) >> a.log2_bs, threadIdx.x, C::kThreads);
 
   const int p0 = a.positions[b];
   int L = p0 + gamma;
@@ -281,15 +284,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   if constexpr (PAGED) {
     first_blk = start >> a.log2_bs;
     const int n_blk = ((end - 1) >> a.log2_bs) - first_blk + 1;
-    const int32_t* row = a.block_table + static_cast<size_t>(b) * a.max_blocks_per_seq + first_blk;
-    for (int i = threadIdx.x; i < n_blk; i += blockDim.x) {
-      int id = row[i];
-      if (id < 0 || id >= a.num_blocks) {
-        flag_error(a.err, RRA_ERR_BLOCK_ID);
-        id = 0;
-      }
-      tbl[i] = id;
-    }
+    pre_ids.store(a, tbl, n_blk, threadIdx.x, C::kThreads);
   }
   __syncthreads();
 
