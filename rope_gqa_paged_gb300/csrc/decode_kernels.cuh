@@ -428,16 +428,16 @@ __device__ bool merge_partials_bulk(const DecodeArgs& a, const float* src_o, con
 }
 
 // Run by all consumer threads of a CTA after each has written its share of this split's
-// partial (index `split` of the [rows][num_splits] partial arrays). With n <= kMergeFanIn
-// splits, the last split to arrive merges them all into the output. With more, splits form
-// groups of kMergeFanIn: the last arrival of each group merges the group into a level-2
+// partial (index `split` of the [rows][num_splits] partial arrays). With n <= F splits
+// (F = merge_fanin(num_splits)), the last split to arrive merges them all into the output. With
+// more, splits form groups of F: the last arrival of each group merges the group into a level-2
 // partial, and the last group to finish merges the level-2 partials into the output, so no
 // single CTA has to read every split at the end of the kernel.
 template <typename T, int D, typename OutRow = SameRow, bool EARLY = true>
 __device__ __forceinline__ void finish_split_rows(const DecodeArgs& a, size_t row0, int hpc, int split, int n,
                                                   float* scratch, int* s_flag, int tid, int nthreads,
                                                   OutRow out_row = OutRow(), int scratch_bytes = 0) {
-  const int S = a.num_splits, G = a.num_groups;
+  const int S = a.num_splits, G = a.num_groups, F = merge_fanin(S);
   // scratch_bytes > 0: the partials come in by bulk copies when they fit (see merge_partials_bulk)
   auto merge = [&](const float* so, const float* sml, int stride, int first, int count, float* dst_o, float* dst_ml,
                    int dst_stride, int dst_idx, auto orow) {
@@ -447,16 +447,16 @@ __device__ __forceinline__ void finish_split_rows(const DecodeArgs& a, size_t ro
     merge_partials<T, D, decltype(orow), EARLY>(a, so, sml, stride, first, count, hpc, row0, dst_o, dst_ml, dst_stride,
                                                 dst_idx, scratch, tid, nthreads, orow);
   };
-  if (n <= kMergeFanIn) {
+  if (n <= F) {
     if (arrive_last(a.counters + row0, n, s_flag, a.err, tid, nthreads))
       merge(a.ws_o, a.ws_ml, S, 0, n, nullptr, nullptr, 0, 0, out_row);
     return;
   }
-  const int grp = split / kMergeFanIn, first = grp * kMergeFanIn;
-  const int gsize = min(kMergeFanIn, n - first);
+  const int grp = split / F, first = grp * F;
+  const int gsize = min(F, n - first);
   if (!arrive_last(a.group_counters + row0 * G + grp, gsize, s_flag, a.err, tid, nthreads)) return;
   merge(a.ws_o, a.ws_ml, S, first, gsize, a.ws2_o, a.ws2_ml, G, grp, SameRow());
-  const int groups = (n + kMergeFanIn - 1) / kMergeFanIn;
+  const int groups = (n + F - 1) / F;
   if (arrive_last(a.counters + row0, groups, s_flag, a.err, tid, nthreads))
     merge(a.ws2_o, a.ws2_ml, G, 0, groups, nullptr, nullptr, 0, 0, out_row);
 }

@@ -269,7 +269,7 @@ int64_t verify_rows(int B, int gamma, int Hq, int Hkv) {
   return int64_t(B) * Hkv * ((Hq / Hkv) / verify_hpc(Hq / Hkv, gamma)) * 16;
 }
 
-// Workspace layout, each part 256-byte aligned (R = B*Hq, G = ceil(splits / kMergeFanIn)):
+// Workspace layout, each part 256-byte aligned (R = B*Hq, G = merge_groups(splits)):
 // partials o [R, splits, D] and (max, sum) [R, splits, 2] floats, level-2 partials o [R, G, D]
 // and (max, sum) [R, G, 2] floats, counters [R] and group counters [R, G] int32.
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -279,7 +279,7 @@ struct WsLayout {
 };
 
 WsLayout ws_layout(int B, int Hq, int D, int splits) {
-  const size_t R = size_t(B) * Hq, G = (size_t(splits) + rra::kMergeFanIn - 1) / rra::kMergeFanIn;
+  const size_t R = size_t(B) * Hq, G = size_t(rra::merge_groups(splits));
   WsLayout l{};
   l.o = 0;
   l.ml = l.o + align256(R * splits * D * sizeof(float));
@@ -304,7 +304,7 @@ size_t partial_bytes(int B, int Hq, int D, int splits) {
 
 size_t counter_ints(int B, int Hq, int splits) {
   if (splits <= 1 || B <= 0) return 0;
-  const size_t R = size_t(B) * Hq, G = (size_t(splits) + rra::kMergeFanIn - 1) / rra::kMergeFanIn;
+  const size_t R = size_t(B) * Hq, G = size_t(rra::merge_groups(splits));
   return R + R * G;
 }
 
@@ -404,7 +404,7 @@ rra::DecodeArgs decode_args(const Plan& p, const void* q, const void* k, const v
   const float s = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(D));
   a.scale_log2 = s * 1.4426950408889634f;
   a.err = err;
-  a.num_groups = (p.splits + rra::kMergeFanIn - 1) / rra::kMergeFanIn;
+  a.num_groups = rra::merge_groups(p.splits);
   a.narrow = p.narrow ? 1 : 0;
   a.test_hold_append = g_test_hold_append.load(std::memory_order_relaxed);
   if (p.splits > 1) {

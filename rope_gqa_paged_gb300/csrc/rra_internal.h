@@ -106,8 +106,21 @@ constexpr int kMaxTableEntries = 2048;
 // Most splits per sequence (the CTA that merges them stages 2 x 8 heads x splits floats in
 // shared memory).
 constexpr int kMaxSplits = 1024;
-// Splits merged by one CTA; more splits are merged in two levels.
+// Splits merged by one CTA in one level; more splits are merged in two levels: groups of
+// merge_fanin(splits) splits (about the square root of the split count, at least 8), then the
+// groups, so that the merge of a group and the merge of the groups read about as many partials
+// each (one group of 32 then 2 groups read 34 rows per head at 57 splits; 8 then 8 read 16).
 constexpr int kMergeFanIn = 32;
+__host__ __device__ inline int merge_fanin(int splits) {
+  if (splits <= kMergeFanIn) return kMergeFanIn;
+  int f = 8;
+  while (f < kMergeFanIn && f * f < splits) ++f;
+  return f;
+}
+__host__ __device__ inline int merge_groups(int splits) {
+  const int f = merge_fanin(splits);
+  return (splits + f - 1) / f;
+}
 
 // rra_decode_attn_paged with the split arrival counters at `counters` (decode_counter_ints
 // int32s, all zero when the kernel starts) and only the partial arrays (decode_partial_bytes)
