@@ -736,20 +736,33 @@ __global__ void __launch_bounds__(MmaCfgN<D, NT, NARROW>::kThreads, MmaCfgN<D, N
     }
   }
   named_barrier_sync(1, kConsumers);
-  for (int idx = threadIdx.x; idx < hpc * D; idx += kConsumers) {
-    const int h = idx / D, d = idx - h * D;
+  // the warps' weights and the merged (max, sum) once per head, then the rows: a loop of
+  // independent items (exp2f and the max per item would chain their latency through every item)
+  float* red_w = red_l + C::kConsumerWarps * C::kMaxHeads;  // [warps][heads] weights
+  float* red_ml = red_w + C::kConsumerWarps * C::kMaxHeads;  // [heads][2] merged max, sum
+  for (int h = threadIdx.x; h < hpc; h += kConsumers) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < C::kConsumerWarps; ++w) M = fmaxf(M, red_m[w * C::kMaxHeads + h]);
-    float lsum = 0.f, osum = 0.f;
-    if (M != -INFINITY) {
+    float lsum = 0.f;
 #pragma unroll
-      for (int w = 0; w < C::kConsumerWarps; ++w) {
-        const float wt = exp2f(red_m[w * C::kMaxHeads + h] - M);
-        lsum = fmaf(wt, red_l[w * C::kMaxHeads + h], lsum);
-        osum = fmaf(wt, red_o[(w * C::kMaxHeads + h) * D + d], osum);
-      }
+    for (int w = 0; w < C::kConsumerWarps; ++w) {
+      const float wt = M != -INFINITY ? exp2f(red_m[w * C::kMaxHeads + h] - M) : 0.f;
+      lsum = fmaf(wt, red_l[w * C::kMaxHeads + h], lsum);
+      red_w[w * C::kMaxHeads + h] = wt;
     }
+    red_ml[2 * h] = M;
+    red_ml[2 * h + 1] = lsum;
+  }
+  named_barrier_sync(1, kConsumers);
+#pragma unroll 4
+  for (int idx = threadIdx.x; idx < hpc * D; idx += kConsumers) {
+    const int h = idx / D, d = idx - h * D;
+    const float M = red_ml[2 * h], lsum = red_ml[2 * h + 1];
+    float osum = 0.f;
+#pragma unroll
+    for (int w = 0; w < C::kConsumerWarps; ++w)
+      osum = fmaf(red_w[w * C::kMaxHeads + h], red_o[(w * C::kMaxHeads + h) * D + d], osum);
     const size_t bh = static_cast<size_t>(b) * a.Hq + h0 + h;
     if (n_work == 1) {
       static_cast<__nv_bfloat16*>(a.out)[bh * D + d] = __float2bfloat16_rn(lsum > 0.f ? osum / lsum : 0.f);

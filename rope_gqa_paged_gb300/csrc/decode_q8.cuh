@@ -876,20 +876,32 @@ __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_Q8_CTAS_PER_SM)
     }
   }
   named_barrier_sync(1, kConsumers);
-  for (int idx = threadIdx.x; idx < hpc * D; idx += kConsumers) {
-    const int h = idx / D, d = idx - h * D;
+  // the warps' weights and the merged (max, sum) once per head, then independent row items
+  float* red_w = red_l + C::kConsumerWarps * M::kMaxHeads;  // [warps][heads] weights
+  float* red_ml = red_w + C::kConsumerWarps * M::kMaxHeads;  // [heads][2] merged max, sum
+  for (int h = threadIdx.x; h < hpc; h += kConsumers) {
     float Mx = -INFINITY;
 #pragma unroll
     for (int w = 0; w < C::kConsumerWarps; ++w) Mx = fmaxf(Mx, red_m[w * M::kMaxHeads + h]);
-    float lsum = 0.f, osum = 0.f;
-    if (Mx != -INFINITY) {
+    float lsum = 0.f;
 #pragma unroll
-      for (int w = 0; w < C::kConsumerWarps; ++w) {
-        const float wt = exp2f(red_m[w * M::kMaxHeads + h] - Mx);
-        lsum = fmaf(wt, red_l[w * M::kMaxHeads + h], lsum);
-        osum = fmaf(wt, red_o[(w * M::kMaxHeads + h) * D + d], osum);
-      }
+    for (int w = 0; w < C::kConsumerWarps; ++w) {
+      const float wt = Mx != -INFINITY ? exp2f(red_m[w * M::kMaxHeads + h] - Mx) : 0.f;
+      lsum = fmaf(wt, red_l[w * M::kMaxHeads + h], lsum);
+      red_w[w * M::kMaxHeads + h] = wt;
     }
+    red_ml[2 * h] = Mx;
+    red_ml[2 * h + 1] = lsum;
+  }
+  named_barrier_sync(1, kConsumers);
+#pragma unroll 4
+  for (int idx = threadIdx.x; idx < hpc * D; idx += kConsumers) {
+    const int h = idx / D, d = idx - h * D;
+    const float Mx = red_ml[2 * h], lsum = red_ml[2 * h + 1];
+    float osum = 0.f;
+#pragma unroll
+    for (int w = 0; w < C::kConsumerWarps; ++w)
+      osum = fmaf(red_w[w * M::kMaxHeads + h], red_o[(w * M::kMaxHeads + h) * D + d], osum);
     const size_t bh = static_cast<size_t>(b) * a.Hq + h0 + h;
     if (n_work == 1) {
       static_cast<__nv_bfloat16*>(a.out)[bh * D + d] = __float2bfloat16_rn(lsum > 0.f ? osum / lsum : 0.f);

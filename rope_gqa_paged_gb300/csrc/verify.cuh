@@ -493,20 +493,32 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     red_l[warp * kVerifyRows + rg + 8] = st.l[1];
   }
   named_barrier_sync(1, kConsumers);
-  for (int idx = threadIdx.x; idx < rows * D; idx += kConsumers) {
-    const int r = idx / D, d = idx - r * D;
+  // the warps' weights and the merged (max, sum) once per row, then independent row items
+  float* red_w = red_l + C::kConsumerWarps * kVerifyRows;   // [warps][16 rows] weights
+  float* red_ml = red_w + C::kConsumerWarps * kVerifyRows;  // [16 rows][2] merged max, sum
+  for (int r = threadIdx.x; r < rows; r += kConsumers) {
     float Mx = -INFINITY;
 #pragma unroll
     for (int w = 0; w < C::kConsumerWarps; ++w) Mx = fmaxf(Mx, red_m[w * kVerifyRows + r]);
-    float lsum = 0.f, osum = 0.f;
-    if (Mx != -INFINITY) {
+    float lsum = 0.f;
 #pragma unroll
-      for (int w = 0; w < C::kConsumerWarps; ++w) {
-        const float wt = exp2f(red_m[w * kVerifyRows + r] - Mx);
-        lsum = fmaf(wt, red_l[w * kVerifyRows + r], lsum);
-        osum = fmaf(wt, red_o[(w * kVerifyRows + r) * D + d], osum);
-      }
+    for (int w = 0; w < C::kConsumerWarps; ++w) {
+      const float wt = Mx != -INFINITY ? exp2f(red_m[w * kVerifyRows + r] - Mx) : 0.f;
+      lsum = fmaf(wt, red_l[w * kVerifyRows + r], lsum);
+      red_w[w * kVerifyRows + r] = wt;
     }
+    red_ml[2 * r] = Mx;
+    red_ml[2 * r + 1] = lsum;
+  }
+  named_barrier_sync(1, kConsumers);
+#pragma unroll 2
+  for (int idx = threadIdx.x; idx < rows * D; idx += kConsumers) {
+    const int r = idx / D, d = idx - r * D;
+    const float Mx = red_ml[2 * r], lsum = red_ml[2 * r + 1];
+    float osum = 0.f;
+#pragma unroll
+    for (int w = 0; w < C::kConsumerWarps; ++w)
+      osum = fmaf(red_w[w * kVerifyRows + r], red_o[(w * kVerifyRows + r) * D + d], osum);
     if (n_work == 1) {
       static_cast<__nv_bfloat16*>(a.out)[out_row(vbase + r) * D + d] = __float2bfloat16_rn(lsum > 0.f ? osum / lsum : 0.f);
     } else {
