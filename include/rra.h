@@ -377,6 +377,30 @@ RRA_API int rra_test_hold_append(int hold);
  * calling thread (device 0 until set), and `stream` must belong to that device. */
 RRA_API int rra_use_device(int device);
 
+/* --- RoPE angle tables (no counterpart on the pages: how every kernel here forms the sine and
+ *     cosine of m * theta_i, [KVC-GQA-RoPE] §3, exposed so that tests can check it) ---
+ * The kernels carry theta_i / 2pi (theta_i = rope_base^(-2i/head_dim), i < head_dim/2, formed in
+ * float64) as a 96-bit binary fraction phi_i, take m * phi_i mod 1 in integer arithmetic and
+ * evaluate cos and sin of that many turns in float32 as hi + lo pairs (absolute error below
+ * about 2^-44). */
+
+/* phi_i for i < head_dim/2 into phi[3 * i + w], w = 0 the least significant 32-bit word. Host
+ * only. RRA_EINVAL for a null phi, an odd head_dim or one outside [2, 512], or a rope_base that is
+ * not positive and finite. */
+RRA_API int rra_rope_phi(int head_dim, double rope_base, uint32_t* phi);
+
+/* cos and sin of 2pi * (position * phi mod 1) for one phi (3 words as above) on the host, by the
+ * same float32 operations as the kernels: out[0] + out[1] = cos, out[2] + out[3] = sin. RRA_EINVAL
+ * for a null pointer or a negative position. */
+RRA_API int rra_rope_cos_sin_host(int position, const uint32_t* phi, float* out);
+
+/* The same on the device for positions[p] (device int32, p < n) and every i < head_dim/2: out
+ * (device float32 [n, 4, head_dim/2]) holds the rows cos hi, cos lo, sin hi, sin lo; NaN for a
+ * negative position. Asynchronous on `stream`. RRA_EINVAL or RRA_ERANGE on bad arguments,
+ * RRA_ECUDA if the launch fails. */
+RRA_API int rra_rope_cos_sin(const int32_t* positions, int n, int head_dim, double rope_base, float* out,
+                             void* stream);
+
 /* --- Decode without a caller workspace (the pages have no counterpart: this exists for
  *     callers that must not allocate device memory when they run a step) ---
  *

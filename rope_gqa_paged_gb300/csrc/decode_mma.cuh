@@ -620,8 +620,7 @@ __global__ void __launch_bounds__(MmaCfgN<D, NT, NARROW>::kThreads, MmaCfgN<D, N
   }
   if constexpr (FUSED) {
     // RoPE ("Transformer推理核心：KV Cache、GQA与RoPE原理与工程实践" §3): sine and cosine of
-    // pos * theta_i in float64 (sincospi of pos * theta_i / pi: exact argument reduction),
-    // split into float32 hi + lo for the error-free rotation.
+    // pos * theta_i as float32 hi + lo pairs (rope_cos_sin) for the error-free rotation.
     const int pos = L - 1;
     // the appender warp fetches the new token's k and v (D / 32 dims per lane) and its block id
     // now, so that the loads overlap the sine / cosine below
@@ -640,13 +639,8 @@ __global__ void __launch_bounds__(MmaCfgN<D, NT, NARROW>::kThreads, MmaCfgN<D, N
       if constexpr (PAGED) phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (pos >> a.log2_bs)];
     }
     if (threadIdx.x < D / 2) {
-      double sn, cn;
-      sincospi(static_cast<double>(pos) * a.theta_pi[threadIdx.x], &sn, &cn);
-      const float ch = static_cast<float>(cn), sh = static_cast<float>(sn);
-      cs[threadIdx.x] = ch;
-      cs[D / 2 + threadIdx.x] = static_cast<float>(cn - static_cast<double>(ch));
-      cs[D + threadIdx.x] = sh;
-      cs[3 * (D / 2) + threadIdx.x] = static_cast<float>(sn - static_cast<double>(sh));
+      rope_cos_sin(pos, a.rope_phi[threadIdx.x], cs[threadIdx.x], cs[D / 2 + threadIdx.x], cs[D + threadIdx.x],
+                   cs[3 * (D / 2) + threadIdx.x]);
     }
     named_barrier_sync(1, kConsumerThreads);
 #pragma unroll

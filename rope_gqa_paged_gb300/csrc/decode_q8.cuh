@@ -705,13 +705,8 @@ __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_Q8_CTAS_PER_SM)
       if constexpr (PAGED) phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (pos >> a.log2_bs)];
     }
     if (threadIdx.x < D / 2) {
-      double sn, cn;
-      sincospi(static_cast<double>(pos) * a.theta_pi[threadIdx.x], &sn, &cn);
-      const float ch = static_cast<float>(cn), sh = static_cast<float>(sn);
-      cs[threadIdx.x] = ch;
-      cs[D / 2 + threadIdx.x] = static_cast<float>(cn - static_cast<double>(ch));
-      cs[D + threadIdx.x] = sh;
-      cs[3 * (D / 2) + threadIdx.x] = static_cast<float>(sn - static_cast<double>(sh));
+      rope_cos_sin(pos, a.rope_phi[threadIdx.x], cs[threadIdx.x], cs[D / 2 + threadIdx.x], cs[D + threadIdx.x],
+                   cs[3 * (D / 2) + threadIdx.x]);
     }
     named_barrier_sync(1, kConsumers);
     rotate_q_fragment<D>(qb, cs, lane, a.rope_style);

@@ -338,13 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (PAGED) phys = a.block_table[static_cast<size_t>(b) * a.max_blocks_per_seq + (pos >> a.log2_bs)];
         }
         if (r < kD / 2) {
-          double sn, cn;
-          sincospi(static_cast<double>(pos) * a.theta_pi[r], &sn, &cn);
-          const float ch = static_cast<float>(cn), sh = static_cast<float>(sn);
-          cs[r] = ch;
-          cs[kD / 2 + r] = static_cast<float>(cn - static_cast<double>(ch));
-          cs[kD + r] = sh;
-          cs[3 * (kD / 2) + r] = static_cast<float>(sn - static_cast<double>(sh));
+          rope_cos_sin(pos, a.rope_phi[r], cs[r], cs[kD / 2 + r], cs[kD + r], cs[3 * (kD / 2) + r]);
         }
         named_barrier_sync(1, kSoftmaxThreads);
         // rotate the row (16-byte chunks c of 8 dims; half-split pairs (i, i + D/2) are chunks c and c + 8)

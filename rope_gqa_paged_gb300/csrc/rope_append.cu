@@ -8,10 +8,10 @@
 // (contiguous) and PagedKVCache (block table -> physical block, slot in block).
 //
 // Grid: (sequence, group of kPairsPerCta frequencies). Each CTA takes the sine and cosine
-// of its frequencies once, in float64 (positions reach 131071, where a float32 angle is
-// already ~0.004 rad off) and in units of pi (sincospi: exact argument reduction, so no
-// slow path for large angles), splits them into float32 hi + lo parts, and rotates that slice
-// of every query and key head. The rotation a*c - b*s is computed from error-free
+// of its frequencies once as float32 hi + lo parts (rope_cos_sin: the angle in turns from an
+// exact 96-bit fraction theta_i / 2pi, so no precision is lost at large positions, where a
+// float32 angle is already ~0.004 rad off at 131071), and rotates that slice of every query
+// and key head. The rotation a*c - b*s is computed from error-free
 // float32 products (x*y = p + e exactly, with e = fma(x, y, -p): Dekker's product, using
 // the FMA) so that it keeps full relative accuracy when the two products cancel; the
 // result is then rounded once to the storage type.
@@ -20,6 +20,8 @@
 // recent tokens kept at high precision; rope_append_qx_kernel): the rotated k is rounded to
 // bf16 first, then quantised with its KV head's scale into the cache slot; with a window the
 // bf16 values also go to slot pos % window of the sequence's ring.
+#include <cmath>
+
 #include "rra_device.cuh"
 #include "rra_internal.h"
 
@@ -74,13 +76,8 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_kernel(const RopeArg
     return;
   }
   if (threadIdx.x < np) {
-    double sn, cn;  // angle / pi = pos * (theta_i / pi): sincospi reduces its argument exactly
-    sincospi(static_cast<double>(pos) * a.inv_freq[i0 + threadIdx.x], &sn, &cn);
-    const float ch = static_cast<float>(cn), sh = static_cast<float>(sn);
-    cs[0][threadIdx.x] = ch;
-    cs[1][threadIdx.x] = static_cast<float>(cn - static_cast<double>(ch));
-    cs[2][threadIdx.x] = sh;
-    cs[3][threadIdx.x] = static_cast<float>(sn - static_cast<double>(sh));
+    rope_cos_sin(pos, a.rope_phi[i0 + threadIdx.x], cs[0][threadIdx.x], cs[1][threadIdx.x], cs[2][threadIdx.x],
+                 cs[3][threadIdx.x]);
   }
   if (threadIdx.x == 32) {  // another warp resolves where the new token's K and V go
     int ok = 1;
@@ -162,13 +159,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_append_rows_kernel(const Ro
     return;
   }
   for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    double sn, cn;  // angle / pi = pos * (theta_i / pi): sincospi reduces its argument exactly
-    sincospi(static_cast<double>(pos) * a.inv_freq[i], &sn, &cn);
-    const float ch = static_cast<float>(cn), sh = static_cast<float>(sn);
-    cs[0][i] = ch;
-    cs[1][i] = static_cast<float>(cn - static_cast<double>(ch));
-    cs[2][i] = sh;
-    cs[3][i] = static_cast<float>(sn - static_cast<double>(sh));
+    rope_cos_sin(pos, a.rope_phi[i], cs[0][i], cs[1][i], cs[2][i], cs[3][i]);
   }
   if (threadIdx.x == kRopeThreads - 1) {  // where the token's K and V go
     int ok = 1;
@@ -305,13 +296,8 @@ __global__ void __launch_bounds__(kQ4Warps * 32) rope_append_qx_kernel(const Rop
     return;
   }
   if (threadIdx.x < HALF) {
-    double sn, cn;  // angle / pi = pos * (theta_i / pi): sincospi reduces its argument exactly
-    sincospi(static_cast<double>(pos) * a.inv_freq[threadIdx.x], &sn, &cn);
-    const float ch = static_cast<float>(cn), sh = static_cast<float>(sn);
-    cs[0][threadIdx.x] = ch;
-    cs[1][threadIdx.x] = static_cast<float>(cn - static_cast<double>(ch));
-    cs[2][threadIdx.x] = sh;
-    cs[3][threadIdx.x] = static_cast<float>(sn - static_cast<double>(sh));
+    rope_cos_sin(pos, a.rope_phi[threadIdx.x], cs[0][threadIdx.x], cs[1][threadIdx.x], cs[2][threadIdx.x],
+                 cs[3][threadIdx.x]);
   }
   if (threadIdx.x == kQ4Warps * 32 - 1) {  // where the token's codes go
     int ok = 1;
@@ -454,4 +440,95 @@ cudaError_t launch_rope_append_q8(const RopeArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// theta_i / 2pi for i < D/2, theta_i = base^(-2i/D) in float64, as a 96-bit binary fraction
+// (least significant 32-bit word first), exact up to truncation (< 2^-96): theta = m 2^(e-53) with
+// an integer m < 2^53, times floor(2^127 / pi) (2^128 / 2pi, a 128-bit integer), shifted down.
+void fill_rope_phi(uint32_t (*phi)[3], int D, double base) {
+  // floor(2^127 / pi), computed at 400-bit precision
+  constexpr uint64_t kHi = 0x28be60db9391054aULL, kLo = 0x7f09d5f47d4d3770ULL;
+  using u128 = unsigned __int128;
+  for (int i = 0; i < D / 2; ++i) {
+    const double th = std::pow(base, -2.0 * i / D);
+    int e = 0;
+    const uint64_t m = static_cast<uint64_t>(std::ldexp(std::frexp(th, &e), 53));  // th = m 2^(e-53)
+    // m * K as 192 bits p2:p1:p0
+    const u128 lo = u128(m) * kLo, hi = u128(m) * kHi;
+    const uint64_t p0 = uint64_t(lo);
+    const u128 mid = (lo >> 64) + u128(uint64_t(hi));
+    const uint64_t p1 = uint64_t(mid);
+    const uint64_t p2 = uint64_t(hi >> 64) + uint64_t(mid >> 64);
+    // theta / 2pi * 2^96 = m K 2^(e - 53 - 128 + 96) = (m K) >> (85 - e)
+    const int sh = 85 - e;
+    uint64_t w[3] = {p0, p1, p2}, out[2] = {0, 0};
+    for (int j = 0; j < 2; ++j) {  // bits [sh + 64 j, sh + 64 j + 64) of m K
+      const int bit = sh + 64 * j, word = bit >> 6, off = bit & 63;
+      uint64_t v = 0;
+      if (bit >= 0 && word < 3) v = w[word] >> off;
+      if (bit >= 0 && off != 0 && word + 1 < 3) v |= w[word + 1] << (64 - off);
+      out[j] = v;
+    }
+    phi[i][0] = static_cast<uint32_t>(out[0]);
+    phi[i][1] = static_cast<uint32_t>(out[0] >> 32);
+    phi[i][2] = static_cast<uint32_t>(out[1]);
+  }
+}
+
+namespace {
+struct RopePhiTable {
+  uint32_t phi[kMaxHeadDim / 2][3];
+};
+// out[n][4][half]: cos hi, cos lo, sin hi, sin lo of positions[n] * theta_i (NaN for a negative position).
+__global__ void rope_cos_sin_kernel(const int32_t* positions, int n, int half, const RopePhiTable t, float* out) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= n * half) return;
+  const int p = idx / half, i = idx - p * half;
+  const int pos = positions[p];
+  float* o = out + static_cast<size_t>(p) * 4 * half;
+  if (pos < 0) {
+    o[i] = o[half + i] = o[2 * half + i] = o[3 * half + i] = __int_as_float(0x7fc00000);
+    return;
+  }
+  rope_cos_sin(pos, t.phi[i], o[i], o[half + i], o[2 * half + i], o[3 * half + i]);
+}
+}  // namespace
+
 }  // namespace rra
+
+extern "C" {
+
+RRA_API int rra_rope_phi(int head_dim, double rope_base, uint32_t* phi) {
+  if (phi == nullptr || head_dim < 2 || head_dim % 2 != 0 || head_dim > rra::kMaxHeadDim ||
+      !(rope_base > 0.0) || !std::isfinite(rope_base))
+    return RRA_EINVAL;
+  rra::fill_rope_phi(reinterpret_cast<uint32_t(*)[3]>(phi), head_dim, rope_base);
+  return RRA_OK;
+}
+
+RRA_API int rra_rope_cos_sin_host(int position, const uint32_t* phi, float* out) {
+  if (phi == nullptr || out == nullptr || position < 0) return RRA_EINVAL;
+  rra::rope_cos_sin(position, phi, out[0], out[1], out[2], out[3]);
+  return RRA_OK;
+}
+
+RRA_API int rra_rope_cos_sin(const int32_t* positions, int n, int head_dim, double rope_base, float* out,
+                             void* stream) {
+  if (n < 0 || (n > 0 && (positions == nullptr || out == nullptr)) || head_dim < 2 || head_dim % 2 != 0 ||
+      head_dim > rra::kMaxHeadDim || !(rope_base > 0.0) || !std::isfinite(rope_base))
+    return RRA_EINVAL;
+  const int half = head_dim / 2;
+  if (int64_t(n) * half > int64_t(INT32_MAX)) return RRA_ERANGE;
+  if (n == 0) return RRA_OK;
+  rra::RopePhiTable t{};
+  rra::fill_rope_phi(t.phi, head_dim, rope_base);
+  const int items = n * half, threads = 128;
+  rra::rope_cos_sin_kernel<<<(items + threads - 1) / threads, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      positions, n, half, t, out);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    rra::record_cuda_error(e, "rope_cos_sin kernel launch");
+    return RRA_ECUDA;
+  }
+  return RRA_OK;
+}
+
+}  // extern "C"

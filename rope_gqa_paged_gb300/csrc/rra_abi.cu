@@ -426,21 +426,6 @@ rra::DecodeArgs decode_args(const Plan& p, const void* q, const void* k, const v
 
 int finish_decode(cudaError_t e) { return e == cudaSuccess ? RRA_OK : cuda_fail(e, "decode kernel launch"); }
 
-// theta_i / pi for i < D/2, theta_i = base^(-2i/D), in float64.
-void fill_theta_pi(double* t, int D, double base) {
-  constexpr double kPi = 3.14159265358979323846;
-  for (int i = 0; i < D / 2; ++i) t[i] = std::pow(base, -2.0 * i / D) / kPi;
-}
-
-// cos theta_i and sin theta_i in float64.
-void fill_cos_sin_theta(double* c, double* s, int D, double base) {
-  for (int i = 0; i < D / 2; ++i) {
-    const double th = std::pow(base, -2.0 * i / D);
-    c[i] = std::cos(th);
-    s[i] = std::sin(th);
-  }
-}
-
 bool overlap(const void* a, const void* b, size_t bytes) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + bytes && y < x + bytes;
@@ -586,7 +571,7 @@ static int rope_append_qk(int bits, const void* q, const void* k_new, const void
   a.k_win = k_win;
   a.v_win = v_win;
   a.window = window;
-  fill_theta_pi(a.inv_freq, D, rope_base);
+  rra::fill_rope_phi(a.rope_phi, D, rope_base);
   const cudaError_t e = bits == 4 ? rra::launch_rope_append_q4(a, static_cast<cudaStream_t>(stream))
                                   : rra::launch_rope_append_q8(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? RRA_OK : cuda_fail(e, "rope_append (quantised) launch");
@@ -654,7 +639,7 @@ static int decode_step_qk(int bits, const void* q, const void* k_new, const void
   a.v_new = v_new;
   a.q_out = q_out;
   a.rope_style = rope_style;
-  fill_theta_pi(a.theta_pi, D, rope_base);
+  rra::fill_rope_phi(a.rope_phi, D, rope_base);
   return finish_decode(rra::launch_decode_q8(a, km, vm, kwm, vwm, block_table != nullptr, true,
                                              static_cast<cudaStream_t>(stream)));
 }
@@ -725,8 +710,7 @@ int verify_launch(const void* q_rot, const void* k_cache, const void* v_cache, c
     a.v_new = fused->v_new;
     a.q_out = fused->q_out;
     a.rope_style = fused->rope_style;
-    fill_theta_pi(a.theta_pi, D, fused->rope_base);
-    fill_cos_sin_theta(a.cos_theta, a.sin_theta, D, fused->rope_base);
+    rra::fill_rope_phi(a.rope_phi, D, fused->rope_base);
   }
   return finish_decode(
       rra::launch_decode_verify(a, km, vm, block_table != nullptr, fused != nullptr, static_cast<cudaStream_t>(stream)));
@@ -831,7 +815,7 @@ int rra_rope_append_verify(const void* q, const void* k_new, const void* v_new, 
   a.Hkv = Hkv;
   a.D = D;
   a.gamma = gamma;
-  fill_theta_pi(a.inv_freq, D, rope_base);
+  rra::fill_rope_phi(a.rope_phi, D, rope_base);
   a.rope_style = rope_style;
   a.err = err_flag;
   const cudaError_t e = rra::launch_rope_append(a, dt, static_cast<cudaStream_t>(stream));
@@ -961,7 +945,7 @@ int rra_decode_step_contig(const void* q, const void* k_new, const void* v_new, 
   a.v_new = v_new;
   a.q_out = q_out;
   a.rope_style = rope_style;
-  fill_theta_pi(a.theta_pi, D, rope_base);
+  rra::fill_rope_phi(a.rope_phi, D, rope_base);
   if (p.tc) return finish_decode(rra::launch_decode_tc(a, km, vm, false, true, s));
   return finish_decode(rra::launch_decode_step_contig(a, km, vm, s));
 }
@@ -1009,7 +993,7 @@ int rra_decode_step_paged(const void* q, const void* k_new, const void* v_new, c
   a.v_new = v_new;
   a.q_out = q_out;
   a.rope_style = rope_style;
-  fill_theta_pi(a.theta_pi, D, rope_base);
+  rra::fill_rope_phi(a.rope_phi, D, rope_base);
   if (p.tc) return finish_decode(rra::launch_decode_tc(a, km, vm, true, true, s));
   return finish_decode(rra::launch_decode_step_paged(a, km, vm, s));
 }

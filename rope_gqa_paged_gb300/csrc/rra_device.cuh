@@ -229,4 +229,101 @@ __device__ __forceinline__ uint8_t pack_nibbles(int lo, int hi) {
   return static_cast<uint8_t>((lo & 0xf) | ((hi & 0xf) << 4));
 }
 
+// ---- RoPE angles in float32 arithmetic ------------------------------------------------------
+// ("Transformer推理核心：KV Cache、GQA与RoPE原理与工程实践" §3: token m rotates pair i by m·θ_i.)
+// The angle is carried in turns: φ_i = θ_i / 2π as a 96-bit binary fraction, made on the host
+// from the float64 θ_i by exact integer arithmetic, so m·φ_i mod 1 takes three 32-bit integer
+// multiplications. The fraction is centred on its nearest quarter turn k/4; the remainder r
+// (|r| <= 1/8 turn) becomes u = 2π·r as a float-float pair (hi + lo), and sin u, cos u are their
+// Taylor series at 0, the leading terms in float-float arithmetic (error-free products by fma,
+// Dekker; error-free sums, Knuth), the small tail in float32. sin and cos of the angle follow
+// from k by a swap and signs. Each comes out as float32 hi + lo, |hi + lo - exact| below ~2^-44:
+// the whole evaluation is float32 / integer work (the float64 pipe of the part is narrow).
+
+struct FF {  // hi + lo, |lo| <= ulp(hi) / 2
+  float hi, lo;
+};
+__host__ __device__ __forceinline__ FF ff_fast_two_sum(float a, float b) {  // requires |a| >= |b|
+  const float s = a + b;
+  return {s, b - (s - a)};
+}
+__host__ __device__ __forceinline__ FF ff_two_sum(float a, float b) {
+  const float s = a + b;
+  const float bb = s - a;
+  return {s, (a - (s - bb)) + (b - bb)};
+}
+__host__ __device__ __forceinline__ FF ff_mul(FF x, FF y) {
+  const float p = x.hi * y.hi;
+  float e = fmaf(x.hi, y.hi, -p);  // the rounding error of p, exactly
+  e = fmaf(x.hi, y.lo, e);
+  e = fmaf(x.lo, y.hi, e);
+  return ff_fast_two_sum(p, e);
+}
+__host__ __device__ __forceinline__ FF ff_mul_f(FF x, float y) {
+  const float p = x.hi * y;
+  float e = fmaf(x.hi, y, -p);
+  e = fmaf(x.lo, y, e);
+  return ff_fast_two_sum(p, e);
+}
+__host__ __device__ __forceinline__ FF ff_add(FF x, FF y) {
+  const FF s = ff_two_sum(x.hi, y.hi);
+  return ff_fast_two_sum(s.hi, s.lo + (x.lo + y.lo));
+}
+__host__ __device__ constexpr float ff_hi_of(double x) { return static_cast<float>(x); }
+__host__ __device__ constexpr float ff_lo_of(double x) {
+  return static_cast<float>(x - static_cast<double>(static_cast<float>(x)));
+}
+// float-float constants, split from float64 values at compile time
+constexpr double kRopeTwoPi = 6.283185307179586476925286766559;
+constexpr double kInvFact2 = 1.0 / 2.0, kInvFact3 = 1.0 / 6.0, kInvFact4 = 1.0 / 24.0, kInvFact5 = 1.0 / 120.0,
+                 kInvFact6 = 1.0 / 720.0, kInvFact7 = 1.0 / 5040.0, kInvFact8 = 1.0 / 40320.0;
+
+// cos and sin of 2π·(pos·φ mod 1), φ = (phi[2]·2^64 + phi[1]·2^32 + phi[0]) / 2^96, pos >= 0:
+// cos = ch + cl, sin = sh + sl. Host-callable too (the same float32 operations, for tests).
+__host__ __device__ __forceinline__ void rope_cos_sin(int pos, const uint32_t* phi, float& ch, float& cl, float& sh,
+                                             float& sl) {
+  const uint32_t m = static_cast<uint32_t>(pos);
+  const uint64_t t0 = static_cast<uint64_t>(m) * phi[0];
+  const uint64_t t1 = static_cast<uint64_t>(m) * phi[1] + (t0 >> 32);
+  const uint32_t w2 = m * phi[2] + static_cast<uint32_t>(t1 >> 32);
+  const uint64_t f = (static_cast<uint64_t>(w2) << 32) | static_cast<uint32_t>(t1);  // turns, units of 2^-64
+  const uint32_t k = static_cast<uint32_t>((f + (1ull << 61)) >> 62);              // nearest quarter (4 -> 0)
+  const int64_t r = static_cast<int64_t>(f - (static_cast<uint64_t>(k) << 62));     // |r| <= 2^61
+  // r as hi + lo: 2^40 a + 2^16 b + c with a (signed, < 2^21), b (24 bits) and c (16 bits) exact floats
+  const float ra = static_cast<float>(static_cast<int32_t>(r >> 40));
+  const float rb = static_cast<float>(static_cast<uint32_t>(r >> 16) & 0xffffffu);
+  const float rc = static_cast<float>(static_cast<uint32_t>(r) & 0xffffu);
+  FF x = ff_two_sum(ra * 0x1p40f, rb * 0x1p16f);
+  x = ff_two_sum(x.hi, x.lo + rc);
+  x.hi *= 0x1p-64f;
+  x.lo *= 0x1p-64f;
+  const FF u = ff_mul(x, FF{ff_hi_of(kRopeTwoPi), ff_lo_of(kRopeTwoPi)});  // radians, |u| <= π/4
+  const FF v = ff_mul(u, u);
+  // sin u = u + u·v·(-1/3! + v/5! - v²/7! + v³·t), t = 1/9! - v/11! + v²/13! - v³/15! in float32
+  float t = fmaf(v.hi, -1.f / 1307674368000.f, 1.f / 6227020800.f);
+  t = fmaf(v.hi, t, -1.f / 39916800.f);
+  t = fmaf(v.hi, t, 1.f / 362880.f);
+  FF s = ff_add(FF{-ff_hi_of(kInvFact7), -ff_lo_of(kInvFact7)}, ff_mul_f(v, t));
+  s = ff_add(FF{ff_hi_of(kInvFact5), ff_lo_of(kInvFact5)}, ff_mul(v, s));
+  s = ff_add(FF{-ff_hi_of(kInvFact3), -ff_lo_of(kInvFact3)}, ff_mul(v, s));
+  const FF sn = ff_add(u, ff_mul(ff_mul(u, v), s));
+  // cos u = 1 + v·(-1/2! + v/4! - v²/6! + v³/8! + v⁴·t), t = -1/10! + v/12! - v²/14! + v³/16! in float32
+  t = fmaf(v.hi, 1.f / 20922789888000.f, -1.f / 87178291200.f);
+  t = fmaf(v.hi, t, 1.f / 479001600.f);
+  t = fmaf(v.hi, t, -1.f / 3628800.f);
+  FF c = ff_add(FF{ff_hi_of(kInvFact8), ff_lo_of(kInvFact8)}, ff_mul_f(v, t));
+  c = ff_add(FF{-ff_hi_of(kInvFact6), -ff_lo_of(kInvFact6)}, ff_mul(v, c));
+  c = ff_add(FF{ff_hi_of(kInvFact4), ff_lo_of(kInvFact4)}, ff_mul(v, c));
+  c = ff_add(FF{-ff_hi_of(kInvFact2), 0.f}, ff_mul(v, c));
+  const FF cn = ff_add(FF{1.f, 0.f}, ff_mul(v, c));
+  // angle = k·π/2 + u
+  const bool odd = k & 1u;
+  const FF co = odd ? sn : cn, so = odd ? cn : sn;
+  const bool neg_c = k == 1u || k == 2u, neg_s = k >= 2u;
+  ch = neg_c ? -co.hi : co.hi;
+  cl = neg_c ? -co.lo : co.lo;
+  sh = neg_s ? -so.hi : so.hi;
+  sl = neg_s ? -so.lo : so.lo;
+}
+
 }  // namespace rra

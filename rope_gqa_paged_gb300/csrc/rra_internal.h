@@ -36,7 +36,7 @@ struct RopeArgs {
   void* k_win;                  // bf16 [B, Hkv, window, D]
   void* v_win;
   int window;
-  double inv_freq[kMaxHeadDim / 2];  // theta_i / pi, theta_i = base^(-2i/D), formed on the host in float64
+  uint32_t rope_phi[kMaxHeadDim / 2][3];  // theta_i / 2pi as 96-bit fractions (fill_rope_phi)
 };
 
 struct DecodeArgs {
@@ -92,11 +92,7 @@ struct DecodeArgs {
   // Prefill: CTAs run band by band, a band being kv_band KV groups (0: all of them) whose keys
   // and values fit in L2 together, longest query blocks first within a band.
   int kv_band;
-  double theta_pi[kMaxDecodeHeadDim / 2];  // theta_i / pi, theta_i = base^(-2i/D)
-  // cos theta_i and sin theta_i (float64, host): the verify step reaches the angles of positions
-  // p + 1, p + 2, ... from that of p by complex multiplication
-  double cos_theta[kMaxDecodeHeadDim / 2];
-  double sin_theta[kMaxDecodeHeadDim / 2];
+  uint32_t rope_phi[kMaxDecodeHeadDim / 2][3];  // theta_i / 2pi as 96-bit fractions (fill_rope_phi)
 };
 
 // Tokens per pipeline stage for a head_dim and element size: K + V tiles of 16 KB.
@@ -133,6 +129,10 @@ int decode_attn_paged_ext(const void* q_rot, const void* k_pool, const void* v_p
 // count (both 0 when splits <= 1).
 size_t decode_partial_bytes(int B, int Hq, int D, int splits);
 size_t decode_counter_ints(int B, int Hq, int splits);
+
+// theta_i / 2pi (theta_i = base^(-2i/D), i < D/2, float64) as 96-bit binary fractions, least
+// significant 32-bit word first: the angle tables of rope_cos_sin.
+void fill_rope_phi(uint32_t (*phi)[3], int D, double base);
 
 // Stores the text rra_last_cuda_error() returns on this thread.
 void record_cuda_error(cudaError_t e, const char* where);
@@ -179,7 +179,7 @@ constexpr int kDecodeNarrowTile = 32;
 #define RRA_Q8_CTAS_PER_SM 3
 #endif
 // Speculative verify: attention of gamma new tokens per sequence (a.gamma, a.positions set).
-// fused: the whole step (a.q unrotated; a.k_new, a.v_new, a.q_out, a.rope_style, a.theta_pi set;
+// fused: the whole step (a.q unrotated; a.k_new, a.v_new, a.q_out, a.rope_style, a.rope_phi set;
 // gamma <= 8).
 cudaError_t launch_decode_verify(const DecodeArgs& a, const CUtensorMap& k_map, const CUtensorMap& v_map, bool paged,
                                  bool fused, cudaStream_t stream);

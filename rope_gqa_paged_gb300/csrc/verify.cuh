@@ -217,7 +217,7 @@ struct VerifyRows {
 
 // FUSED: the whole verify step in this launch. a.q holds the unrotated q of the gamma new tokens
 // (gamma <= kVerifyFusedMaxGamma); the consumer warps take sin/cos of the gamma positions once per
-// CTA (float64 sincospi, as the decode step), rotate their query rows in registers, and split-0
+// CTA (rope_cos_sin, as the decode step), rotate their query rows in registers, and split-0
 // CTAs publish q_rot. A CTA whose chunk holds new tokens rotates their k_new and writes them and
 // v_new into the cache, one warp per token, and its producer waits for those writes (an mbarrier
 // with one arrival per token) before the TMA of the first tile that holds a new token. Head-slice
@@ -367,27 +367,13 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
   }
   if constexpr (FUSED) {
     // RoPE ("Transformer推理核心：KV Cache、GQA与RoPE原理与工程实践" §3) at positions p0 .. p0 + gamma - 1:
-    // sin / cos of p0 * theta_i in float64 (sincospi: exact argument reduction), then of
-    // (p0 + j) * theta_i by j float64 complex multiplications by e^(i theta_i) (relative error
-    // ~j * 2^-53, far below what the float32 hi + lo split keeps), split into float32 hi + lo
-    // for the error-free rotation; [gamma][4][D/2] floats. One float64 sincospi per frequency and
-    // CTA: the FP64 pipe is narrow, and every CTA of the sequence needs the same table.
+    // sine and cosine of (p0 + j) * theta_i as float32 hi + lo pairs (rope_cos_sin) for the
+    // error-free rotation, spread over the consumer threads; [gamma][4][D/2] floats.
     float* cs = reinterpret_cast<float*>(smem + C::kOffCs);
-    for (int i = threadIdx.x; i < D / 2; i += kConsumers) {
-      double sn, cn;
-      sincospi(static_cast<double>(p0) * a.theta_pi[i], &sn, &cn);
-      const double c1 = a.cos_theta[i], s1 = a.sin_theta[i];
-      for (int j = 0; j < gamma; ++j) {
-        float* c = cs + j * 2 * D;
-        const float ch = static_cast<float>(cn), sh = static_cast<float>(sn);
-        c[i] = ch;
-        c[D / 2 + i] = static_cast<float>(cn - static_cast<double>(ch));
-        c[D + i] = sh;
-        c[3 * (D / 2) + i] = static_cast<float>(sn - static_cast<double>(sh));
-        const double cn2 = fma(cn, c1, -sn * s1), sn2 = fma(sn, c1, cn * s1);
-        cn = cn2;
-        sn = sn2;
-      }
+    for (int e = threadIdx.x; e < gamma * (D / 2); e += kConsumers) {
+      const int j = e / (D / 2), i = e - j * (D / 2);
+      float* c = cs + j * 2 * D;
+      rope_cos_sin(p0 + j, a.rope_phi[i], c[i], c[D / 2 + i], c[D + i], c[3 * (D / 2) + i]);
     }
     named_barrier_sync(1, kConsumers);
     rotate_q_rows<D>(qa, cs, rows, gamma, lane, a.rope_style);

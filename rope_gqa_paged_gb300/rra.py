@@ -38,6 +38,9 @@ _SIGNATURES = {
     "rra_last_cuda_error": (ctypes.c_char_p, []),
     "rra_use_device": (_c_int, [_c_int]),
     "rra_test_hold_append": (_c_int, [_c_int]),
+    "rra_rope_phi": (_c_int, [_c_int, _c_f64, _vp]),
+    "rra_rope_cos_sin_host": (_c_int, [_c_int, _vp, _vp]),
+    "rra_rope_cos_sin": (_c_int, [_vp, _c_int, _c_int, _c_f64, _vp, _vp]),
     "rra_decode_step_contig": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _vp, _c_int, _c_int, _c_int,
                                         _c_int, _c_f64, _c_int, _c_f32, _c_int, _vp, _c_size, _c_int, _vp, _vp]),
     "rra_decode_step_paged": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _c_int,
@@ -161,11 +164,40 @@ def rra_test_hold_append(hold: bool) -> None:
     _check("rra_test_hold_append", lib().rra_test_hold_append(1 if hold else 0))
 
 
+def rra_rope_phi(head_dim: int, rope_base: float = 10000.0) -> list:
+    """theta_i / 2pi (i < head_dim/2) as 96-bit fractions: [[w0, w1, w2], ...], w0 least significant."""
+    buf = (ctypes.c_uint32 * (3 * (head_dim // 2) if head_dim > 0 else 1))()
+    _check("rra_rope_phi", lib().rra_rope_phi(head_dim, rope_base, ctypes.cast(buf, _vp)))
+    return [[int(buf[3 * i + w]) for w in range(3)] for i in range(head_dim // 2)]
+
+
+def rra_rope_cos_sin_host(position: int, phi) -> tuple:
+    """(cos hi, cos lo, sin hi, sin lo) of 2pi * (position * phi mod 1), by the kernels' float32 steps."""
+    ph = (ctypes.c_uint32 * 3)(*[int(w) & 0xffffffff for w in phi])
+    out = (ctypes.c_float * 4)()
+    _check("rra_rope_cos_sin_host",
+           lib().rra_rope_cos_sin_host(int(position), ctypes.cast(ph, _vp), ctypes.cast(out, _vp)))
+    return tuple(float(x) for x in out)
+
+
 def rra_status_str(status: int) -> str:
     return lib().rra_status_str(status).decode()
 
 
 # --------------------------------------------------------------------------- device entry points
+def rra_rope_cos_sin(positions: torch.Tensor, head_dim: int, rope_base: float = 10000.0, out=None,
+                     stream=None) -> torch.Tensor:
+    """cos hi, cos lo, sin hi, sin lo of positions[p] * theta_i on the device: float32 [n, 4, head_dim/2]."""
+    if positions.dtype != torch.int32 or not positions.is_cuda or not positions.is_contiguous():
+        raise ValueError("positions: a contiguous int32 CUDA tensor")
+    n = positions.numel()
+    if out is None:
+        out = torch.empty(n, 4, head_dim // 2, dtype=torch.float32, device=positions.device)
+    _check("rra_rope_cos_sin", lib().rra_rope_cos_sin(positions.data_ptr(), n, head_dim, rope_base, out.data_ptr(),
+                                                      _stream(stream, positions)))
+    return out
+
+
 def rra_rope_append(q, k_new, v_new, positions, q_out, k_cache, v_cache, block_table=None,
                     rope_base: float = 10000.0, rope_style: int = 0, err_flag=None, stream=None) -> None:
     """RoPE on q / k_new at ``positions`` and append of rotated k and raw v into the cache.
