@@ -707,8 +707,13 @@ __global__ void __launch_bounds__(MmaCfgN<D, NT, NARROW>::kThreads, MmaCfgN<D, N
       st[n].l[j] += __shfl_xor_sync(0xffffffffu, st[n].l[j], 16);
     }
   named_barrier_sync(1, kConsumers);
-  float* red_o = reinterpret_cast<float*>(smem);                 // [warps][8 NT heads][D]
-  float* red_m = red_o + C::kConsumerWarps * C::kMaxHeads * D;   // [warps][8 NT heads]
+  // [warps][8 NT heads][D + 4]: the padded row stride puts the four heads a store instruction
+  // covers in distinct banks
+  constexpr int kRS = D + 4;
+  static_assert(C::kConsumerWarps * C::kMaxHeads * (kRS + 4) * 4 + 2 * C::kMaxHeads * 4 <= C::kRingBytes,
+                "the warp merge fits in the ring");
+  float* red_o = reinterpret_cast<float*>(smem);
+  float* red_m = red_o + C::kConsumerWarps * C::kMaxHeads * kRS;  // [warps][8 NT heads]
   float* red_l = red_m + C::kConsumerWarps * C::kMaxHeads;
 #pragma unroll
   for (int n = 0; n < NT; ++n) {
@@ -717,8 +722,8 @@ __global__ void __launch_bounds__(MmaCfgN<D, NT, NARROW>::kThreads, MmaCfgN<D, N
     for (int i = 0; i < D / 16; ++i) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        red_o[(warp * C::kMaxHeads + hd0 + j) * D + 16 * i + dl] = st[n].o[i][j];
-        red_o[(warp * C::kMaxHeads + hd0 + j) * D + 16 * i + 8 + dl] = st[n].o[i][2 + j];
+        red_o[(warp * C::kMaxHeads + hd0 + j) * kRS + 16 * i + dl] = st[n].o[i][j];
+        red_o[(warp * C::kMaxHeads + hd0 + j) * kRS + 16 * i + 8 + dl] = st[n].o[i][2 + j];
       }
     }
     if (dl == 0) {
@@ -756,7 +761,7 @@ __global__ void __launch_bounds__(MmaCfgN<D, NT, NARROW>::kThreads, MmaCfgN<D, N
     float osum = 0.f;
 #pragma unroll
     for (int w = 0; w < C::kConsumerWarps; ++w)
-      osum = fmaf(red_w[w * C::kMaxHeads + h], red_o[(w * C::kMaxHeads + h) * D + d], osum);
+      osum = fmaf(red_w[w * C::kMaxHeads + h], red_o[(w * C::kMaxHeads + h) * kRS + d], osum);
     const size_t bh = static_cast<size_t>(b) * a.Hq + h0 + h;
     if (n_work == 1) {
       static_cast<__nv_bfloat16*>(a.out)[bh * D + d] = __float2bfloat16_rn(lsum > 0.f ? osum / lsum : 0.f);

@@ -850,8 +850,13 @@ __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_Q8_CTAS_PER_SM)
     st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 16);
   }
   named_barrier_sync(1, kConsumers);
-  float* red_o = reinterpret_cast<float*>(smem);                 // [warps][8 heads][D]
-  float* red_m = red_o + C::kConsumerWarps * M::kMaxHeads * D;   // [warps][8 heads]
+  // [warps][8 heads][D + 4]: the padded row stride puts the four heads a store instruction covers
+  // in distinct banks
+  constexpr int kRS = D + 4;
+  static_assert(C::kConsumerWarps * M::kMaxHeads * (kRS + 4) * 4 + 2 * M::kMaxHeads * 4 <= C::kRingBytes,
+                "the warp merge fits in the ring");
+  float* red_o = reinterpret_cast<float*>(smem);
+  float* red_m = red_o + C::kConsumerWarps * M::kMaxHeads * kRS;  // [warps][8 heads]
   float* red_l = red_m + C::kConsumerWarps * M::kMaxHeads;
   {
     const int hd0 = 2 * (lane & 3), dl = lane >> 2;
@@ -859,8 +864,8 @@ __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_Q8_CTAS_PER_SM)
     for (int i = 0; i < D / 16; ++i)
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        red_o[(warp * M::kMaxHeads + hd0 + j) * D + 16 * i + dl] = st.o[i][j];
-        red_o[(warp * M::kMaxHeads + hd0 + j) * D + 16 * i + 8 + dl] = st.o[i][2 + j];
+        red_o[(warp * M::kMaxHeads + hd0 + j) * kRS + 16 * i + dl] = st.o[i][j];
+        red_o[(warp * M::kMaxHeads + hd0 + j) * kRS + 16 * i + 8 + dl] = st.o[i][2 + j];
       }
     if (dl == 0) {
 #pragma unroll
@@ -896,7 +901,7 @@ __global__ void __launch_bounds__(Q8Cfg<D, BITS>::kThreads, RRA_Q8_CTAS_PER_SM)
     float osum = 0.f;
 #pragma unroll
     for (int w = 0; w < C::kConsumerWarps; ++w)
-      osum = fmaf(red_w[w * M::kMaxHeads + h], red_o[(w * M::kMaxHeads + h) * D + d], osum);
+      osum = fmaf(red_w[w * M::kMaxHeads + h], red_o[(w * M::kMaxHeads + h) * kRS + d], osum);
     const size_t bh = static_cast<size_t>(b) * a.Hq + h0 + h;
     if (n_work == 1) {
       static_cast<__nv_bfloat16*>(a.out)[bh * D + d] = __float2bfloat16_rn(lsum > 0.f ? osum / lsum : 0.f);

@@ -462,14 +462,19 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     st.l[i] += __shfl_xor_sync(0xffffffffu, st.l[i], 2);
   }
   named_barrier_sync(1, kConsumers);
-  float* red_o = reinterpret_cast<float*>(smem);                   // [warps][16 rows][D]
-  float* red_m = red_o + C::kConsumerWarps * kVerifyRows * D;      // [warps][16 rows]
+  // [warps][16 rows][D + 8]: the padded row stride keeps the float2 stores of a fragment's eight
+  // rows in distinct banks
+  constexpr int kRS = D + 8;
+  static_assert(C::kConsumerWarps * kVerifyRows * (kRS + 4) * 4 + 2 * kVerifyRows * 4 <= C::kRingBytes,
+                "the warp merge fits in the ring");
+  float* red_o = reinterpret_cast<float*>(smem);
+  float* red_m = red_o + C::kConsumerWarps * kVerifyRows * kRS;    // [warps][16 rows]
   float* red_l = red_m + C::kConsumerWarps * kVerifyRows;
 #pragma unroll
   for (int nt = 0; nt < D / 8; ++nt) {
-    *reinterpret_cast<float2*>(&red_o[(warp * kVerifyRows + rg) * D + 8 * nt + 2 * t]) =
+    *reinterpret_cast<float2*>(&red_o[(warp * kVerifyRows + rg) * kRS + 8 * nt + 2 * t]) =
         make_float2(st.o[nt][0], st.o[nt][1]);
-    *reinterpret_cast<float2*>(&red_o[(warp * kVerifyRows + rg + 8) * D + 8 * nt + 2 * t]) =
+    *reinterpret_cast<float2*>(&red_o[(warp * kVerifyRows + rg + 8) * kRS + 8 * nt + 2 * t]) =
         make_float2(st.o[nt][2], st.o[nt][3]);
   }
   if (t == 0) {
@@ -504,7 +509,7 @@ __global__ void __launch_bounds__(MmaCfg<D>::kThreads, RRA_MMA_CTAS_PER_SM)
     float osum = 0.f;
 #pragma unroll
     for (int w = 0; w < C::kConsumerWarps; ++w)
-      osum = fmaf(red_w[w * kVerifyRows + r], red_o[(w * kVerifyRows + r) * D + d], osum);
+      osum = fmaf(red_w[w * kVerifyRows + r], red_o[(w * kVerifyRows + r) * kRS + d], osum);
     if (n_work == 1) {
       static_cast<__nv_bfloat16*>(a.out)[out_row(vbase + r) * D + d] = __float2bfloat16_rn(lsum > 0.f ? osum / lsum : 0.f);
     } else {
