@@ -103,8 +103,10 @@ int check_shapes(int B, int Hq, int Hkv, int D, rra_dtype dt) {
 // Chunk and split count for a per-sequence capacity of max_tokens, once p->mma, p->hpc and
 // p->tile are set.
 // extra_units: CTAs per (sequence, head slice) beyond the splits (the INT8 kernel's ring unit).
+// short_splits: with few sequences x heads, chunks may go below 256 tokens (down to one tile) so
+// that a short capacity still gets this many splits.
 int plan_splits(int B, int Hkv, int n_rep, int64_t max_tokens, int block_size, int requested, Plan* p,
-                int extra_units = 0) {
+                int extra_units = 0, int short_splits = 0) {
   const int64_t tiles = std::max<int64_t>(1, (max_tokens + p->tile - 1) / p->tile);
   // A paged split copies its block ids to shared memory: at most kMaxTableEntries of them.
   int64_t max_chunk_tiles = tiles;
@@ -124,7 +126,9 @@ int plan_splits(int B, int Hkv, int n_rep, int64_t max_tokens, int block_size, i
       // started costs a whole CTA time), each at least 256 tokens long.
       const int64_t splits_one_wave = std::max<int64_t>(1, resident / units - extra_units);
       chunk_tiles = (tiles + splits_one_wave - 1) / splits_one_wave;
-      chunk_tiles = std::max<int64_t>(chunk_tiles, std::max(1, 256 / p->tile));
+      int64_t min_tiles = std::max(1, 256 / p->tile);
+      if (short_splits > 0) min_tiles = std::min<int64_t>(min_tiles, (tiles + short_splits - 1) / short_splits);
+      chunk_tiles = std::max<int64_t>(chunk_tiles, std::max<int64_t>(1, min_tiles));
     } else {
       // Many sequences x heads: about two waves, each CTA streaming 128..2048 tokens; fewer,
       // longer CTAs pay start-up and epilogue less often, two waves keep ragged tails short.
@@ -175,7 +179,10 @@ int make_plan(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_size,
   if (p->hpc > 8) p->ctas_per_sm = 2;
   if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
   p->tile = p->mma ? rra::decode_mma_tile_tokens(D) : rra::decode_tile_tokens(D, elem_bytes(dt));
-  st = plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
+  // bf16 tensor-core decode: at least 8 splits for short capacities (one sequence, 32q/8kv, 1K
+  // tokens: 11.4 us at 8 splits of 128 tokens against 12.8 us at 4 of 256; at 4K the 256-token
+  // floor stays, 13.8 us at 16 splits against 14.7 us at 32)
+  st = plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p, 0, p->mma ? 8 : 0);
   if (st != RRA_OK || !p->mma || D != 128 || p->hpc > 8 || requested == 0) return st;
   // A requested split count that takes few (sequence, KV head) units past one wave of the
   // 3-per-SM kernel: narrow CTAs, four per SM, so the grid needs fewer and fuller waves.
