@@ -88,8 +88,10 @@ enum {
  *     must have allocated that block. block_size must be a power of two.
  *   rope_base  RoPE base (10000 for the pages' models; > 1)
  *   rope_style 0 = half-split pairs (i, i + D/2) ("rotate_half"), 1 = interleaved (2i, 2i+1)
- * The angle pos * theta_i, its sine and cosine and the rotation are computed in float64
- * and rounded once to dt (nearest even). Hq + Hkv must not exceed 524280.
+ * theta_i is formed in float64; the angle pos * theta_i is taken exactly (theta_i / 2pi as a
+ * 96-bit fraction, see rra_rope_phi), its sine and cosine to about 2^-44 as float32 hi + lo
+ * pairs, the rotation with error-free float32 products, and the result is rounded once to dt
+ * (nearest even). Hq + Hkv must not exceed 524280.
  */
 RRA_API int rra_rope_append(const void* q, const void* k_new, const void* v_new,
                     const int32_t* positions, void* q_out,
@@ -290,7 +292,7 @@ RRA_API int rra_verify_attn(const void* q_rot, const void* k_cache, const void* 
 /* The whole verify step: RoPE of the gamma new tokens' q and k at positions p_b .. p_b + gamma - 1,
  * their append, and the attention of rra_verify_attn, with q_rot also written to q_out. Up to
  * gamma 8 this is ONE kernel: each CTA rotates its query rows in registers (sines and cosines
- * of the gamma positions in float64, once per CTA), and the CTAs whose chunk holds new tokens
+ * of the gamma positions as in rra_rope_append, once per CTA), and the CTAs whose chunk holds new tokens
  * write them into the cache before their own TMA reads the tile that holds them. Above gamma 8
  * it runs rra_rope_append_verify then rra_verify_attn on q_out (two kernels). Same results
  * either way. bf16. q_out must not overlap q. ("Transformer架构优化实战2026：注意力机制、KV
