@@ -68,6 +68,7 @@ struct Plan {
   int tile = 0;
   int chunk = 0;
   int splits = 1;
+  int max_chunk_tokens = 2048;  // longest chunk the many-sequence plan gives one CTA
 };
 
 // The tensor-core kernel takes bf16 with TMA destinations on 1024-byte swizzle atoms:
@@ -134,7 +135,7 @@ int plan_splits(int B, int Hkv, int n_rep, int64_t max_tokens, int block_size, i
       // longer CTAs pay start-up and epilogue less often, two waves keep ragged tails short.
       const int64_t target = 2 * resident;
       chunk_tiles = (tiles * units + target - 1) / target;
-      const int64_t lo = std::max(1, 128 / p->tile), hi = std::max(1, 2048 / p->tile);
+      const int64_t lo = std::max(1, 128 / p->tile), hi = std::max(1, p->max_chunk_tokens / p->tile);
       chunk_tiles = std::min(std::max(chunk_tiles, lo), hi);
     }
   }
@@ -215,6 +216,12 @@ int make_plan_q8(int B, int Hq, int Hkv, int D, int64_t max_tokens, int block_si
   if (static_cast<int64_t>(Hkv) * (n_rep / p->hpc) > 65535) return RRA_ERANGE;
   p->tile = rra::decode_q8_tile_tokens(D, bits);
   p->ctas_per_sm = RRA_Q8_CTAS_PER_SM;
+  // INT4 CTAs stream half an INT8 CTA's bytes per token for the same start-up and merge costs
+  // (per-CTA traces: ~7 us before the first tile and ~4 us merging around ~19 us of streaming), so
+  // the many-sequence plan gives them chunks of up to 3072 tokens: the batch-64 INT4 step 108.5 /
+  // 109.0 us at 3 splits against 112.4 / 112.6 us at 4; INT8 keeps 2048 (127.4 us at 4 splits
+  // against 130.4 us at 3).
+  if (bits == 4) p->max_chunk_tokens = 3072;
   if (block_size > 0 ? block_size < 8 : max_tokens < p->tile) return RRA_EUNSUPPORTED;
   return plan_splits(B, Hkv, n_rep, max_tokens, block_size, requested, p);
 }
