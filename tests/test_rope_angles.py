@@ -17,6 +17,7 @@ RRA_OK, RRA_EINVAL = 0, -1
 # float32 tails of the two series, ~2^-23 of terms below 5e-7) stay near 2^-45.
 BOUND = 2.0 ** -44
 CASES = [(128, 10000.0), (64, 500000.0), (128, 1.0e6), (512, 10000.0), (2, 10000.0)]
+EXTREME = [(512, 1.0e9), (64, 1.0001)]  # theta_i down to ~1e-9 (tiny fractions); every theta_i near 1
 
 
 @pytest.fixture(scope="module")
@@ -36,7 +37,7 @@ def _positions(seed):
     return edge + [rnd.randrange(0, 2 ** 31) for _ in range(30)] + [rnd.randrange(0, 1 << 17) for _ in range(30)]
 
 
-@pytest.mark.parametrize("D,base", CASES)
+@pytest.mark.parametrize("D,base", CASES + EXTREME)
 def test_phi_is_theta_over_two_pi(rra, D, base):
     mpmath.mp.prec = 200
     phi = rra.rra_rope_phi(D, base)
@@ -47,7 +48,7 @@ def test_phi_is_theta_over_two_pi(rra, D, base):
         assert 0 <= exact - got < mpmath.mpf(2) ** -95, (D, base, i)  # truncated, not rounded
 
 
-@pytest.mark.parametrize("D,base", CASES)
+@pytest.mark.parametrize("D,base", CASES + EXTREME)
 def test_cos_sin_within_bound(rra, D, base):
     mpmath.mp.prec = 200
     phi = rra.rra_rope_phi(D, base)
